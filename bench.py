@@ -1,0 +1,499 @@
+#!/usr/bin/env python
+"""Benchmark of MLA chunked-context prefill on one or more GB300s.
+
+One step = one call of mla_chunked_prefill (plan, metadata upload, empty-row
+fill, per chunk gather + W_kv_b up-projection + attention + accumulate,
+new-token up-projection + causal attention, final merge_attn_states) over the
+heterogeneous batch: 32 requests, one context of 131072 rows, 24 log-uniform
+on [1, 2048], 7 empty; queries uniform on [1, 256]; DeepSeek-V3 MLA shapes
+(128 heads, latent 512 + rope 64, nope 128, v 128, bf16, block 64);
+workspace 32768 rows, split alignment 64.  All inputs are seeded synthetic.
+
+Printed JSON line (rank 0):
+  value      tokens/s of the whole job, inputs resident in HBM
+  e2e        tokens/s with host buffers: pinned host->device copies of the
+             step's inputs and a device->host read of the output inside the
+             timed region
+  merge      merge_attn_states alone on 8192 tokens x 128 heads x 128 (bf16,
+             15% empty prefix rows, prefix_num_tokens 6144): GB/s of the bytes
+             that must move and the fraction of the measured HBM copy peak
+  roofline   the dominant kernel (the tcgen05 up-projection GEMM): algorithmic
+             FLOPs per launch / its CUDA-event duration vs. measured bf16 peak
+  cpu_baseline  the float64 oracle on the host cores, on a bounded sample
+             (every token, a few heads; throughput scaled to all heads)
+
+--impl reference times the oracle alone (the slow reference arm).
+Multi-GPU (torchrun): every rank runs its own replica of the batch (the path
+has no exchange step); value = all ranks' tokens / max over ranks of time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "chunked-context MLA prefill tok/s; merge_attn_states GB/s (% HBM peak)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.idx)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for ts, l in self.lines if self.t0 is None or (self.t0 - 0.15 <= ts <= self.t1 + 0.15)]
+        if not rows:
+            rows = [l for _, l in self.lines]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads --
+def flops_of(w, plans):
+    """Algorithmic FLOPs of one prefill (each multiply-add = 2)."""
+    H, L, Dn, Dv, P = w.num_heads, w.kv_lora_rank, w.qk_nope_dim, w.v_dim, w.qk_rope_dim
+    ctx_rows = sum(sum(p.seq_lens) for p in plans)
+    T = w.num_tokens
+    up = 2.0 * L * H * (Dn + Dv) * (ctx_rows + T)
+    attn_ctx = 2.0 * H * (Dn + P + Dv) * sum(q * c for q, c in zip(w.query_lens, w.context_lens))
+    attn_suf = 2.0 * H * (Dn + P + Dv) * sum(q * (q + 1) / 2 for q in w.query_lens)
+    return dict(up_proj_ctx=2.0 * L * H * (Dn + Dv) * ctx_rows,
+                up_proj_new=2.0 * L * H * (Dn + Dv) * T, attn_ctx=attn_ctx, attn_new=attn_suf,
+                total=up + attn_ctx + attn_suf)
+
+
+def merge_bytes(x, T, H, D, es=2):
+    """Bytes the merge must move: both LSEs of every row below the threshold,
+    each finite side's O, the output O and LSE; above it the suffix only."""
+    pnt = x["prefix_num_tokens"]
+    pl = x["prefix_lse"][:, :pnt]
+    sl = x["suffix_lse"][:, :pnt]
+    pf = torch.isfinite(pl).sum().item()
+    sf = torch.isfinite(sl).sum().item()
+    below = H * pnt
+    above = H * (T - pnt)
+    b = below * 8 + (pf + sf) * D * es + below * (D * es + 4)
+    b += above * (4 + D * es + D * es + 4)
+    full = T * H * (3 * D * es + 12)
+    return b, full
+
+
+# ------------------------------------------------------------ our arm -----
+def run_ours(args, rank, world, dev):
+    import mla_chunked_context_gb300 as M
+    from mla_chunked_context_gb300 import workloads as W
+
+    w = W.workload(args.workload)
+    peaks = load_peaks()
+    x = W.make_inputs(w)
+    g = {k: v.to(dev) for k, v in x.items()}
+    plans = M.mla_plan_context_chunks(w.context_lens, w.row_budget, w.max_context_chunk,
+                                      w.split_alignment)
+    dims = M.Dims.of(w)
+    pf = M.ChunkedPrefill(dims, w.context_lens, w.query_lens, w.row_budget,
+                          w.max_context_chunk, w.split_alignment, device=dev)
+    T, H = w.num_tokens, w.num_heads
+    out = torch.empty(T, H, w.v_dim, dtype=w.torch_dtype, device=dev)
+    out_lse = torch.empty(H, T, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pf(g["q"], g["new_latent"], g["kv_cache"], g["block_table"], g["w_kv_b"], out, out_lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("t0")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)                   # L2 flush outside the timed events
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    max_ms = t.item()
+    value = world * args.steps * T / (max_ms / 1e3)
+
+    # ---- e2e: host buffers, copies inside the timed region
+    host = {k: v.pin_memory() for k, v in x.items()}
+    host_out = torch.empty(T, H, w.v_dim, dtype=w.torch_dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        for k in g:
+            g[k].copy_(host[k], non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = world * args.steps * T / (t.item() / 1e3)
+
+    result = None
+    if rank == 0:
+        kernels = time_kernels(M, W, w, g, plans, dims, dev, args, flush)
+        fl = flops_of(w, plans)
+        merge = bench_merge(M, W, dev, peaks, flush)
+        up = kernels["up_proj_ctx"]
+        roofline = {
+            "kernel": "kv_up_proj (tcgen05 GEMM)" if M.mla_has_tcgen05() else "kv_up_proj (CUDA cores)",
+            "bound": "tensor", "unit": "TFLOP/s",
+            "achieved": fl["up_proj_ctx"] / up["launches"] / (up["ms"] / up["launches"] / 1e3) / 1e12,
+            "peak": peaks["bf16_tflops"], "peak_source": peaks["source"] + " bf16 burst",
+            "launches_per_step": up["launches"],
+            "traffic": committed_traffic("kv_up_proj"),
+        }
+        roofline["frac"] = roofline["achieved"] / roofline["peak"]
+        step_ms_mean = max_ms / args.steps
+        launches = kernels["launches_per_step"]
+        result = {
+            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_mean,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded host draws; random-init W_kv_b)",
+            "config": {"workload": f"{w.name}: {w.num_requests} requests, context rows "
+                                   f"{sum(w.context_lens)} (max {max(w.context_lens)}), "
+                                   f"{T} new tokens, {len(plans)} chunks",
+                       "heads": H, "kv_lora_rank": w.kv_lora_rank, "rope": w.qk_rope_dim,
+                       "nope": w.qk_nope_dim, "v": w.v_dim, "block_size": w.block_size,
+                       "row_budget": w.row_budget, "split_alignment": w.split_alignment,
+                       "chunks": len(plans), "parallelism": f"replicas x{world}",
+                       "l2": "flushed between timed steps (256 MB write outside the events); "
+                             "each step also streams >2 GB"},
+            "tflops": fl["total"] / (step_ms_mean / 1e3) / 1e12,
+            "tensor_frac_step": fl["total"] / (step_ms_mean / 1e3) / 1e12 / peaks["bf16_tflops_sustained"]
+            if peaks.get("bf16_tflops_sustained") else None,
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "roofline": roofline,
+            "merge": merge,
+            "kernels": kernels,
+            "flops_per_step": fl,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(w, x, heads=args.cpu_heads)
+    return result
+
+
+def committed_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources have not changed since it was taken (else null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(kernel)
+    if not e or e.get("csrc_sha1") != csrc_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def csrc_hash():
+    h = hashlib.sha1()
+    c = os.path.join(ROOT, "mla_chunked_context_gb300", "csrc")
+    for f in sorted(os.listdir(c)):
+        h.update(open(os.path.join(c, f), "rb").read())
+    return h.hexdigest()
+
+
+def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
+    """Replays one step through the per-step entry points with CUDA events
+    around each launch (same shapes, same stream), to split the step time."""
+    stream = torch.cuda.current_stream()
+    T, H = w.num_tokens, w.num_heads
+    qsl = [0]
+    for q in w.query_lens:
+        qsl.append(qsl[-1] + q)
+    max_rows = max([sum(p.seq_lens) for p in plans] + [1])
+    lat_ws = torch.empty(max_rows, w.latent_dim, dtype=w.torch_dtype, device=dev)
+    kv_ws = torch.empty(max_rows, H * (w.qk_nope_dim + w.v_dim), dtype=w.torch_dtype, device=dev)
+    kv_new = torch.empty(T, H * (w.qk_nope_dim + w.v_dim), dtype=w.torch_dtype, device=dev)
+    o_p = torch.zeros(T, H, w.v_dim, device=dev)
+    l_p = torch.zeros(H, T, device=dev)
+    o_s = torch.empty(T, H, w.v_dim, device=dev)
+    l_s = torch.empty(H, T, device=dev)
+    out = torch.empty(T, H, w.v_dim, dtype=w.torch_dtype, device=dev)
+    res = {k: {"ms": 0.0, "launches": 0} for k in
+           ("gather", "up_proj_ctx", "attn_ctx", "up_proj_new", "attn_new", "merge")}
+    meta = []
+    for p in plans:
+        n = p.request_end - p.request_start
+        cu = [0]
+        for l in p.seq_lens:
+            cu.append(cu[-1] + l)
+        meta.append(dict(
+            req=torch.arange(p.request_start, p.request_end, dtype=torch.int32, device=dev),
+            st=torch.tensor(p.starts, dtype=torch.int32, device=dev),
+            cu=torch.tensor(cu, dtype=torch.int32, device=dev), cu_h=cu,
+            ql=qsl[p.request_start:p.request_end + 1], rows=cu[-1],
+            acc=[1 if s > 0 else 0 for s in p.starts]))
+
+    def timed(name, fn):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        res[name]["ms"] += a.elapsed_time(b)
+        res[name]["launches"] += 1
+
+    reps = 2
+    for _ in range(reps):
+        for m in meta:
+            timed("gather", lambda: M.mla_gather_context_rows(
+                dims, g["kv_cache"], g["block_table"], m["req"], m["st"], m["cu"], m["rows"],
+                lat_ws))
+            timed("up_proj_ctx", lambda: M.mla_kv_up_proj(dims, lat_ws, m["rows"], g["w_kv_b"],
+                                                          kv_ws))
+            timed("attn_ctx", lambda: M.mla_varlen_attn(dims, False, m["ql"], m["cu_h"], g["q"],
+                                                        kv_ws, lat_ws, o_p, l_p,
+                                                        accumulate=m["acc"]))
+        timed("up_proj_new", lambda: M.mla_kv_up_proj(dims, g["new_latent"], T, g["w_kv_b"],
+                                                      kv_new))
+        timed("attn_new", lambda: M.mla_varlen_attn(dims, True, qsl, qsl, g["q"], kv_new,
+                                                    g["new_latent"], o_s, l_s))
+        pnt = 0
+        for r, c in enumerate(w.context_lens):
+            if c > 0:
+                pnt = qsl[r + 1]
+        timed("merge", lambda: M.merge_attn_states(out, None, o_p, l_p, o_s, l_s, pnt))
+    for k in res:
+        res[k]["ms"] /= reps
+        res[k]["launches"] //= reps
+    empty = any(c == 0 and qsl[r] < pnt for r, c in enumerate(w.context_lens))
+    res["launches_per_step"] = 3 * len(plans) + 3 + (1 if empty else 0)
+    return res
+
+
+def bench_merge(M, W, dev, peaks, flush, reps=20):
+    m = W.MergeWorkload()
+    x = W.make_merge_inputs(m, poison=True)
+    g = {k: v.to(dev) for k, v in x.items() if torch.is_tensor(v)}
+    T, H, D = m.num_tokens, m.num_heads, m.head_dim
+    out = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty(H, T, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def go():
+        M.merge_attn_states(out, out_lse, g["prefix_o"], g["prefix_lse"], g["suffix_o"],
+                            g["suffix_lse"], m.prefix_num_tokens)
+    for _ in range(3):
+        go()
+    ms = []
+    for _ in range(reps):
+        flush.fill_(2)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        go()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    med = statistics.median(ms)
+    need, full = merge_bytes(x, T, H, D)
+    gbs = need / (med / 1e3) / 1e9
+    return {"workload": "8192 tokens x 128 heads x 128, bf16, 15% empty prefix, "
+                        "prefix_num_tokens 6144", "us": med * 1e3, "bytes": need,
+            "gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "peak_gbs": peaks["hbm_gbs"],
+            "peak_source": peaks["source"] + " copy", "frac_of_8000": gbs / 8000.0,
+            "gbs_if_every_byte_read": full / (med / 1e3) / 1e9}
+
+
+# --------------------------------------------------------- oracle (CPU) ----
+def cpu_baseline(w, x, heads=2, start_head=0):
+    """The float64 oracle as it stands on a bounded sample: every token of
+    the batch for `heads` heads (the oracle run with those heads' W_kv_b rows
+    and query columns); tokens/s scaled to all heads."""
+    from oracle import mla as O
+    H = w.num_heads
+    Dn, Dv = w.qk_nope_dim, w.v_dim
+    q = x["q"].float().numpy()
+    lat = x["new_latent"].float().numpy()
+    cache = x["kv_cache"].float().numpy()
+    bt = x["block_table"].numpy()
+    wk = x["w_kv_b"].float().numpy()
+    t0 = time.perf_counter()
+    for h in range(start_head, start_head + heads):
+        hh = h % H
+        d = O.MlaDims(1, w.kv_lora_rank, w.qk_rope_dim, Dn, Dv, w.block_size, w.softmax_scale)
+        O.chunked_prefill(q[:, hh:hh + 1], lat, cache, bt, wk[hh * (Dn + Dv):(hh + 1) * (Dn + Dv)],
+                          w.context_lens, w.query_lens, d, w.row_budget, w.max_context_chunk,
+                          w.split_alignment)
+    dt = time.perf_counter() - t0
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((i.get("num_threads", 0) for i in threadpool_info()), default=None)
+    except Exception:
+        threads = None
+    return {"value": w.num_tokens * heads / H / dt, "unit": "tok/s",
+            "cores": threads or os.cpu_count(), "host_cpus": os.cpu_count(), "kind": "oracle",
+            "sample": f"all {w.num_tokens} tokens x {heads} of {H} heads of the {w.name} batch "
+                      f"(oracle.mla.chunked_prefill, float64, {dt:.1f} s); tok/s scaled by "
+                      f"{heads}/{H}"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from mla_chunked_context_gb300 import workloads as W
+    w = W.workload(args.workload)
+    x = W.make_inputs(w)
+    cpu_baseline(W.scaled(w, context_lens=[64], query_lens=[4]), W.make_inputs(
+        W.scaled(w, context_lens=[64], query_lens=[4])), heads=1)   # warm-up: imports, BLAS
+    vals = []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        cb = cpu_baseline(w, x, heads=1, start_head=i)
+        vals.append(cb)
+    dt = time.perf_counter() - t0
+    value = w.num_tokens * args.steps / w.num_heads / dt
+    cb = dict(vals[-1])
+    cb["value"] = value
+    cb["sample"] = (f"per step: all {w.num_tokens} tokens x 1 of {w.num_heads} heads "
+                    f"(float64 oracle); tok/s scaled by 1/{w.num_heads}")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "parallelism": "host oracle, rank 0 only"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="hetero", choices=["hetero", "uniform", "long"])
+    ap.add_argument("--cpu-heads", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    res = run_ours(args, rank, world, dev)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

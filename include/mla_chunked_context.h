@@ -1,0 +1,299 @@
+/*
+ * mla_chunked_context.h -- C ABI of the GB300 (sm_103a) MLA chunked-context
+ * prefill library, libmla_gb300.so.
+ *
+ * The method (three vLLM pull-request reports):
+ *   - PR #50613 ("MLA prefill schedules chunks per request"): a host planner
+ *     packs each request's cached context into workspace-sized chunks, cutting
+ *     an overflowing request at an aligned length; per chunk the context rows
+ *     are gathered once into a workspace, attended, and merged into a context
+ *     partial (O, LSE) that starts as O=0, LSE=-inf for requests without
+ *     context.
+ *   - PR #36540 ("Remove trtllm ragged mla prefills"): merge_attn_states takes
+ *     prefix_num_tokens; tokens at or past it copy the suffix output.
+ *   - PR #49294 ("Ignore empty MLA context chunks during merge"): rows with an
+ *     empty context carry LSE=-inf and O=0 and must merge without NaN.
+ * The MLA arithmetic (latent cache -> W_kv_b up-projection into K_nope and V,
+ * attention over concat(K_nope, k_pe)) is the standard MLA prefill.
+ *
+ * Conventions for every call
+ *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Arguments are
+ *     validated on the host before anything is enqueued; on an error nothing
+ *     has been enqueued.
+ *   - The caller owns all memory.  The library allocates no device memory;
+ *     calls that need scratch take a caller-provided device workspace whose
+ *     size a *_workspace_bytes query returns.
+ *   - "device" pointers are CUDA device pointers of the current device;
+ *     work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and nothing synchronises unless stated.  "host" pointers are
+ *     read before the call returns.
+ *   - Layouts (row-major, contiguous):
+ *       q            [T, H, Dn+P]            (nope first, then rope)
+ *       kv_cache     [num_blocks, block_size, L+P]  (c_kv first, then k_pe)
+ *       block_table  [R, block_table_stride] int32 physical block ids
+ *       new_latent   [T, L+P]                latent rows of the new tokens
+ *       w_kv_b       [H*(Dn+Dv), L]          rows h*(Dn+Dv)+[0,Dn) -> K_nope,
+ *                                            the next Dv rows -> V
+ *       O            [T, H, Dv];  LSE [H, T] float32, natural log
+ *     T = number of new tokens, H = heads, L = kv_lora_rank, P = rope dim,
+ *     Dn = qk_nope_dim, Dv = v_dim, R = requests.  Tokens of request r are
+ *     rows [qsl[r], qsl[r+1]) where qsl is the prefix sum of query lengths.
+ *   - dtype (mla_dims_t.dtype) is the storage type of q, kv_cache,
+ *     new_latent, w_kv_b and of the final output O.  Arithmetic is float32
+ *     (tensor-core products of bf16 operands accumulate in float32).
+ *   - dev_status (nullable, device int32): set to a nonzero MLA_STATUS_* bit
+ *     when a kernel meets a block id outside [0, num_blocks); that row is
+ *     then read as zeros.  The caller checks it when it chooses to.
+ */
+#ifndef MLA_CHUNKED_CONTEXT_H
+#define MLA_CHUNKED_CONTEXT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+typedef void *mla_stream_t; /* cudaStream_t */
+
+enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID = -1,        /* bad argument (null pointer, bad size)        */
+  MLA_ERR_TOO_SMALL = -2,      /* output array or workspace too small          */
+  MLA_ERR_PLANNER_STUCK = -3,  /* no aligned split fits an empty chunk         */
+  MLA_ERR_CUDA = -4,           /* a CUDA launch or runtime call failed         */
+  MLA_ERR_UNSUPPORTED = -5     /* dims / dtype combination not supported       */
+};
+
+enum { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1 };
+
+enum { MLA_STATUS_BAD_BLOCK = 1 };
+
+typedef struct {
+  int32_t num_heads;     /* H  */
+  int32_t kv_lora_rank;  /* L  */
+  int32_t qk_rope_dim;   /* P  */
+  int32_t qk_nope_dim;   /* Dn */
+  int32_t v_dim;         /* Dv */
+  int32_t block_size;    /* rows per paged-cache block */
+  float softmax_scale;   /* score = scale * (q_nope.k_nope + q_pe.k_pe) */
+  int32_t dtype;         /* MLA_DTYPE_* storage type, see above */
+} mla_dims_t;
+
+/* One chunk of the plan (PR #50613 report, key source snippet
+ * _ContextChunkPlan): requests [request_start, request_end); their entries
+ * are starts[entry_offset + i] / seq_lens[entry_offset + i]. */
+typedef struct {
+  int32_t request_start;
+  int32_t request_end;
+  int32_t entry_offset;
+  int32_t rows;            /* padded workspace rows the chunk uses */
+  int32_t is_continuation; /* 1 when starts[entry_offset] > 0 */
+} mla_chunk_t;
+
+/* ---------------------------------------------------------------------------
+ * mla_plan_context_chunks  (host only; PR #50613 report, "implementation
+ * breakdown" item 2 and key source snippet plan_mla_context_chunks /
+ * aligned_split_len)
+ *
+ * Packs the context rows of requests 0..num_requests-1, in order, into chunks
+ * of at most row_budget padded rows.  Requests with context_lens[r] == 0 are
+ * in no chunk.  A request that overflows the chunk is cut at the largest
+ * multiple of split_alignment that is <= max_context_chunk, < its remaining
+ * rows, and fits; the chunk then closes (also when no such length exists, in
+ * which case the request opens the next chunk).
+ *   context_lens   host [num_requests], >= 0
+ *   padded_rows    optional callback mapping a context offset to padded
+ *                  workspace rows (non-decreasing); NULL = identity
+ *   chunks, starts, seq_lens: host outputs.  Call with all three NULL (and
+ *                  caps 0) to get *num_chunks / *num_entries only.
+ * Errors: MLA_ERR_INVALID (negative length, budget/alignment < 1),
+ *         MLA_ERR_PLANNER_STUCK (a request cannot be placed even in an empty
+ *         chunk: row_budget smaller than one aligned split),
+ *         MLA_ERR_TOO_SMALL (caps below the counts; the counts are still set).
+ */
+int mla_plan_context_chunks(const int32_t *context_lens, int32_t num_requests,
+                            int32_t row_budget, int32_t max_context_chunk,
+                            int32_t split_alignment,
+                            int64_t (*padded_rows)(int64_t, void *),
+                            void *padded_rows_ctx, mla_chunk_t *chunks,
+                            int32_t chunks_cap, int32_t *starts,
+                            int32_t *seq_lens, int32_t entries_cap,
+                            int32_t *num_chunks, int32_t *num_entries);
+
+/* ---------------------------------------------------------------------------
+ * merge_attn_states  (PR #36540 report, "implementation breakdown", CUDA
+ * kernel layer; PR #49294 report, test_merge_attn_states_both_empty)
+ *
+ * Per token t < num_tokens and head h:
+ *   t >= prefix_num_tokens       -> out = suffix (prefix never read)
+ *   both LSE = -inf              -> out O = 0, LSE = -inf
+ *   one LSE = -inf               -> the other side (the empty side's O is
+ *                                   never read)
+ *   otherwise                    -> LSE-weighted average, new LSE =
+ *                                   m + ln(e^(pL-m) + e^(sL-m))
+ *   out, prefix_o, suffix_o  device [T, H, D]; in_dtype for the two inputs,
+ *                            out_dtype for out (bf16 output is rounded to
+ *                            nearest even)
+ *   prefix_lse, suffix_lse   device float32 [H, T];  out_lse nullable
+ *   head_dim must be a multiple of 8.  out may alias suffix_o (in place).
+ */
+int merge_attn_states(void *out, float *out_lse, const void *prefix_o,
+                      const float *prefix_lse, const void *suffix_o,
+                      const float *suffix_lse, int32_t num_tokens,
+                      int32_t num_heads, int32_t head_dim,
+                      int32_t prefix_num_tokens, int32_t in_dtype,
+                      int32_t out_dtype, mla_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Per-step calls of the chunk pipeline.  They exist so that every step can be
+ * tested and timed on its own; mla_context_chunk_attn and mla_chunked_prefill
+ * run them in order.
+ *
+ * mla_gather_context_rows  (PR #50613 report, item 2: every context row of a
+ * chunk is gathered exactly once)
+ *   For seq i < num_seqs (request seq_request[i], rows [seq_start[i],
+ *   seq_start[i] + cu_rows[i+1] - cu_rows[i]) of its context) copies cache row
+ *   j = kv_cache[block_table[r][j / bs]][j % bs][0 : L+P] to latent_ws row
+ *   cu_rows[i] + (j - seq_start[i]).
+ *   seq_request, seq_start device [num_seqs]; cu_rows device [num_seqs+1];
+ *   latent_ws device [total_rows, L+P] in dtype.  (L+P)*elem must be a
+ *   multiple of 16 bytes.
+ */
+int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache,
+                            int32_t num_blocks, const int32_t *block_table,
+                            int32_t block_table_stride, int32_t num_seqs,
+                            const int32_t *seq_request,
+                            const int32_t *seq_start, const int32_t *cu_rows,
+                            int32_t total_rows, void *latent_ws,
+                            int32_t *dev_status, mla_stream_t stream);
+
+/* mla_kv_up_proj: kv[rows, H*(Dn+Dv)] = latent[:, 0:L] . w_kv_b^T
+ *   latent device [rows, latent_ld] in dtype (latent_ld >= L); kv device,
+ *   row-major [rows, H*(Dn+Dv)] in dtype.  For bf16 with L % 64 == 0 and
+ *   H*(Dn+Dv) % 256 == 0 this runs on the tcgen05 tensor-core GEMM. */
+int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
+                   int32_t rows, const void *w_kv_b, void *kv,
+                   mla_stream_t stream);
+
+/* mla_varlen_attn: softmax attention per sequence, returning (O, LSE).
+ *   Sequence i owns query tokens [q_loc[i], q_loc[i+1]) (rows of q, o, lse)
+ *   and key rows [k_loc[i], k_loc[i+1]) of kv (up-projected, [rows,
+ *   H*(Dn+Dv)]) and of latent (k_pe = latent[row][L:L+P]).
+ *   causal = 0: every query sees all of its sequence's keys (context chunk).
+ *   causal = 1: keys are the sequence's own new tokens and query i sees keys
+ *               0..i (requires equal query and key counts).
+ *   accumulate (device [num_seqs], nullable): where nonzero, the result is
+ *   LSE-merged into the (o, lse) already stored for those tokens instead of
+ *   overwriting them (PR #50613 report, item 3, accumulate_mla_context_chunk).
+ *   q_loc, k_loc device [num_seqs+1]; max_q / max_k: upper bounds of the
+ *   per-sequence counts.  o device float32 [T, H, Dv]; lse float32 [H, T];
+ *   num_tokens = T (the row count of q, o and lse).
+ *   A row that sees no key gets O = 0, LSE = -inf. */
+int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
+                    const int32_t *q_loc, const int32_t *k_loc,
+                    const int32_t *q_loc_host, const int32_t *k_loc_host,
+                    int32_t num_tokens, const void *q, const void *kv,
+                    const void *latent, int64_t latent_ld,
+                    const int32_t *accumulate, float *o, float *lse,
+                    mla_stream_t stream);
+
+/* mla_fill_empty_rows  (PR #50613 report, item 3, init_mla_context_partial):
+ *   o[t, :, :] = 0 and lse[:, t] = -inf for t in each [slices[2k],
+ *   slices[2k+1]).  slices device int32 [2*num_slices]; o float32 [T, H, Dv];
+ *   lse float32 [H, T]. */
+int mla_fill_empty_rows(float *o, float *lse, int32_t num_tokens,
+                        int32_t num_heads, int32_t v_dim, int32_t num_slices,
+                        const int32_t *slices, mla_stream_t stream);
+
+/* mla_mask_empty_context  (PR #49294 report, mask_empty_context): the old
+ *   scheme's fix-up.  For every request r whose context length in the chunk,
+ *   context_start_loc[r+1] - context_start_loc[r], is 0, rows
+ *   [query_start_loc[r], query_start_loc[r+1]) get lse = -inf and o = 0 (o in
+ *   dtype, [T, H, D]); all other rows are left untouched.  Both loc arrays
+ *   device int32 [num_requests+1]. */
+int mla_mask_empty_context(float *lse, void *o, int32_t dtype,
+                           int32_t num_tokens, int32_t num_heads,
+                           int32_t head_dim, int32_t num_requests,
+                           const int32_t *query_start_loc,
+                           const int32_t *context_start_loc,
+                           mla_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Chunk-level and whole-prefill calls.
+ *
+ * mla_chunk_workspace_bytes: device bytes mla_context_chunk_attn needs for a
+ *   chunk of up to max_rows context rows and max_entries requests.
+ */
+int mla_chunk_workspace_bytes(const mla_dims_t *d, int32_t max_rows,
+                              int32_t max_entries, size_t *bytes);
+
+/* mla_context_chunk_attn  (PR #50613 report, items 2-4: one ContextChunk)
+ *   Gathers the chunk's rows, up-projects them, attends each of its
+ *   requests' new tokens to its rows, and accumulates into the context
+ *   partial: requests whose entry starts at 0 overwrite their rows, the
+ *   continued request (start > 0) is LSE-merged into what earlier chunks
+ *   stored.
+ *   chunk, starts, seq_lens: the planner's host outputs (starts/seq_lens
+ *     indexed from chunk->entry_offset); query_start_loc host [R+1].
+ *   o_partial device float32 [T, H, Dv]; lse_partial device float32 [H, T].
+ *   workspace: device, at least mla_chunk_workspace_bytes bytes.
+ *   The metadata is uploaded from host memory with cudaMemcpyAsync. */
+int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *chunk,
+                           const int32_t *starts, const int32_t *seq_lens,
+                           const int32_t *query_start_loc, int32_t num_tokens,
+                           const void *q, const void *kv_cache,
+                           int32_t num_blocks, const int32_t *block_table,
+                           int32_t block_table_stride, const void *w_kv_b,
+                           void *workspace, size_t workspace_bytes,
+                           float *o_partial, float *lse_partial,
+                           int32_t *dev_status, mla_stream_t stream);
+
+/* mla_prefill_workspace_bytes: device bytes mla_chunked_prefill needs for
+ *   these lengths and planner settings (it runs the planner). */
+int mla_prefill_workspace_bytes(const mla_dims_t *d,
+                                const int32_t *context_lens,
+                                const int32_t *query_lens,
+                                int32_t num_requests, int32_t row_budget,
+                                int32_t max_context_chunk,
+                                int32_t split_alignment, size_t *bytes);
+
+/* mla_chunked_prefill  (the whole path: plan, init partial, per chunk
+ *   gather + up-projection + attention + accumulate, new-token up-projection
+ *   and causal attention, final merge_attn_states with prefix_num_tokens)
+ *   context_lens, query_lens: host [num_requests].
+ *   prefix_num_tokens = end of the last request with context (tokens of a
+ *   context-free tail copy the suffix result).
+ *   out device [T, H, Dv] in dtype; out_lse device float32 [H, T], nullable.
+ *   workspace: device, >= mla_prefill_workspace_bytes.
+ *   All metadata goes to the device in one cudaMemcpyAsync from host memory.
+ */
+int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
+                        const int32_t *query_lens, int32_t num_requests,
+                        int32_t row_budget, int32_t max_context_chunk,
+                        int32_t split_alignment, const void *q,
+                        const void *new_latent, const void *kv_cache,
+                        int32_t num_blocks, const int32_t *block_table,
+                        int32_t block_table_stride, const void *w_kv_b,
+                        void *workspace, size_t workspace_bytes, void *out,
+                        float *out_lse, int32_t *dev_status,
+                        mla_stream_t stream);
+
+/* Library build information: 1 when the tcgen05 kernels were compiled for
+ * sm_103a in this binary. */
+int mla_has_tcgen05(void);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_CHUNKED_CONTEXT_H */

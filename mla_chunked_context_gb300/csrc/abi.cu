@@ -1,0 +1,477 @@
+// C-ABI entry points: argument checks, workspace carving, metadata upload and
+// the order of the steps (PR #50613 report, items 2-4; PR #36540 report).
+//
+// Step order of mla_chunked_prefill, all on the caller's stream:
+//   plan (host) -> one metadata upload -> fill context-free rows of the
+//   partial -> per chunk { gather, up-projection, attention + accumulate } ->
+//   new-token up-projection -> causal new-token attention -> final merge.
+#include <cstring>
+#include <vector>
+
+#include "common.cuh"
+#include "planner.h"
+
+namespace mla {
+
+// kernels (merge.cu, gather.cu, generic.cu, sm103_gemm.cu, sm103_attn.cu)
+int launch_merge(void *out, float *out_lse, const void *prefix_o, const float *prefix_lse,
+                 const void *suffix_o, const float *suffix_lse, int T, int H, int D,
+                 int pnt, int in_dtype, int out_dtype, cudaStream_t s);
+int launch_fill_empty_rows(float *o, float *lse, int T, int H, int Dv, int num_slices,
+                           const int32_t *slices, cudaStream_t s);
+int launch_mask_empty_context(float *lse, void *o, int dtype, int T, int H, int D, int R,
+                              const int32_t *qsl, const int32_t *csl, cudaStream_t s);
+int launch_gather(const void *cache, int num_blocks, int block_size, int row_bytes,
+                  const int32_t *block_table, int bt_stride, int num_seqs,
+                  const int32_t *seq_request, const int32_t *seq_start,
+                  const int32_t *cu_rows, int total_rows, void *ws, int32_t *status,
+                  cudaStream_t s);
+bool generic_dims_ok(const mla_dims_t &d);
+int launch_up_proj_simt(int dtype, const void *latent, int64_t lda, int rows, const void *w,
+                        void *kv, int N, int K, cudaStream_t s);
+int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
+                     const int32_t *k_loc, int num_q_rows, int T, const void *q,
+                     const void *kv, const void *latent, int64_t latent_ld,
+                     const int32_t *accumulate, float *o, float *lse, cudaStream_t s);
+bool tc_gemm_ok(const mla_dims_t &d, int64_t lda, const void *latent, const void *w,
+                const void *kv);
+int launch_up_proj_tc(const mla_dims_t &d, const void *latent, int64_t lda, int rows,
+                      const void *w, void *kv, cudaStream_t s);
+bool tc_attn_ok(const mla_dims_t &d, int64_t latent_ld);
+int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
+                   const int32_t *k_loc, const int32_t *q_loc_host,
+                   const int32_t *k_loc_host, int T, const void *q, const void *kv,
+                   const void *latent, int64_t latent_ld, const int32_t *accumulate,
+                   float *o, float *lse, cudaStream_t s);
+bool tc_available();
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+struct Carve {
+  char *base;
+  size_t off = 0;
+  explicit Carve(void *b) : base(static_cast<char *>(b)) {}
+  void *take(size_t bytes) {
+    off = (off + kAlign - 1) / kAlign * kAlign;
+    void *p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+int check_dims(const mla_dims_t *d) {
+  if (!d) return MLA_ERR_INVALID;
+  if (d->num_heads < 1 || d->kv_lora_rank < 1 || d->qk_rope_dim < 0 || d->qk_nope_dim < 1 ||
+      d->v_dim < 1 || d->block_size < 1 || !valid_dtype(d->dtype))
+    return MLA_ERR_INVALID;
+  if (!(d->softmax_scale > 0.f)) return MLA_ERR_INVALID;
+  const int es = elem_bytes(d->dtype);
+  if (((d->kv_lora_rank + d->qk_rope_dim) * es) % 16 != 0) return MLA_ERR_UNSUPPORTED;
+  if (d->v_dim % 8 != 0) return MLA_ERR_UNSUPPORTED;
+  if (!generic_dims_ok(*d)) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+inline int kv_width(const mla_dims_t &d) { return d.num_heads * (d.qk_nope_dim + d.v_dim); }
+
+int up_proj(const mla_dims_t &d, const void *latent, int64_t lda, int rows, const void *w,
+            void *kv, cudaStream_t s) {
+  if (rows == 0) return MLA_OK;
+  if (tc_available() && tc_gemm_ok(d, lda, latent, w, kv))
+    return launch_up_proj_tc(d, latent, lda, rows, w, kv, s);
+  return launch_up_proj_simt(d.dtype, latent, lda, rows, w, kv, kv_width(d), d.kv_lora_rank, s);
+}
+
+int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
+              const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
+              int T, const void *q, const void *kv, const void *latent, int64_t latent_ld,
+              const int32_t *acc, float *o, float *lse, cudaStream_t s) {
+  const int nq = q_loc_host[n] - q_loc_host[0];
+  if (n == 0 || nq == 0) return MLA_OK;
+  if (tc_available() && tc_attn_ok(d, latent_ld))
+    return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, q, kv,
+                          latent, latent_ld, acc, o, lse, s);
+  return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, q, kv, latent, latent_ld, acc, o,
+                          lse, s);
+}
+
+// Device metadata of one chunk, in this order (n = number of requests):
+//   seq_request[n] seq_start[n] cu_rows[n+1] q_loc[n+1] accumulate[n]
+struct ChunkMetaHost {
+  int n = 0, rows = 0;
+  std::vector<int32_t> ints;
+  std::vector<int32_t> q_loc, cu_rows;  // host copies for launch sizing
+};
+
+size_t chunk_meta_ints(int n) { return size_t(5) * n + 2; }
+
+void build_chunk_meta(const mla_chunk_t &c, const int32_t *starts, const int32_t *lens,
+                      const int32_t *qsl, ChunkMetaHost &m) {
+  const int n = c.request_end - c.request_start;
+  m.n = n;
+  m.ints.assign(chunk_meta_ints(n), 0);
+  m.q_loc.assign(n + 1, 0);
+  m.cu_rows.assign(n + 1, 0);
+  int32_t *req = m.ints.data(), *st = req + n, *cu = st + n, *ql = cu + n + 1,
+          *acc = ql + n + 1;
+  for (int i = 0; i < n; ++i) {
+    const int e = c.entry_offset + i;
+    req[i] = c.request_start + i;
+    st[i] = starts[e];
+    cu[i + 1] = cu[i] + lens[e];
+    acc[i] = starts[e] > 0 ? 1 : 0;
+  }
+  for (int i = 0; i <= n; ++i) ql[i] = qsl[c.request_start + i];
+  m.rows = cu[n];
+  std::memcpy(m.q_loc.data(), ql, sizeof(int32_t) * (n + 1));
+  std::memcpy(m.cu_rows.data(), cu, sizeof(int32_t) * (n + 1));
+}
+
+struct ChunkBuffers {
+  void *latent_ws;
+  void *kv_ws;
+};
+
+int run_chunk(const mla_dims_t &d, const ChunkMetaHost &m, const int32_t *meta_dev, int T,
+              const void *q, const void *kv_cache, int num_blocks, const int32_t *block_table,
+              int bt_stride, const void *w, const ChunkBuffers &b, float *o, float *lse,
+              int32_t *status, cudaStream_t s) {
+  const int n = m.n;
+  const int32_t *req = meta_dev, *st = req + n, *cu = st + n, *ql = cu + n + 1,
+                *acc = ql + n + 1;
+  const int LP = d.kv_lora_rank + d.qk_rope_dim;
+  const int es = elem_bytes(d.dtype);
+  int rc = launch_gather(kv_cache, num_blocks, d.block_size, LP * es, block_table, bt_stride,
+                         n, req, st, cu, m.rows, b.latent_ws, status, s);
+  if (rc) return rc;
+  rc = up_proj(d, b.latent_ws, LP, m.rows, w, b.kv_ws, s);
+  if (rc) return rc;
+  return attention(d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.kv_ws,
+                   b.latent_ws, LP, acc, o, lse, s);
+}
+
+void carve_chunk_buffers(Carve &cv, const mla_dims_t &d, int64_t rows, ChunkBuffers &b) {
+  const int es = elem_bytes(d.dtype);
+  const int LP = d.kv_lora_rank + d.qk_rope_dim;
+  b.latent_ws = cv.take(size_t(rows) * LP * es);
+  b.kv_ws = cv.take(size_t(rows) * kv_width(d) * es);
+}
+
+int upload(void *dst, const std::vector<int32_t> &src, cudaStream_t s) {
+  if (src.empty()) return MLA_OK;
+  return cudaMemcpyAsync(dst, src.data(), src.size() * sizeof(int32_t),
+                         cudaMemcpyHostToDevice, s) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int merge_attn_states(void *out, float *out_lse, const void *prefix_o,
+                                 const float *prefix_lse, const void *suffix_o,
+                                 const float *suffix_lse, int32_t num_tokens,
+                                 int32_t num_heads, int32_t head_dim,
+                                 int32_t prefix_num_tokens, int32_t in_dtype,
+                                 int32_t out_dtype, mla_stream_t stream) {
+  if (num_tokens < 0 || num_heads < 1 || head_dim < 8 || head_dim % 8 != 0 ||
+      !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return MLA_ERR_INVALID;
+  if (num_tokens == 0) return MLA_OK;
+  if (!out || !suffix_o || !suffix_lse) return MLA_ERR_INVALID;
+  if (prefix_num_tokens > 0 && (!prefix_o || !prefix_lse)) return MLA_ERR_INVALID;
+  return launch_merge(out, out_lse, prefix_o, prefix_lse, suffix_o, suffix_lse, num_tokens,
+                      num_heads, head_dim, prefix_num_tokens < 0 ? 0 : prefix_num_tokens,
+                      in_dtype, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache,
+                                       int32_t num_blocks, const int32_t *block_table,
+                                       int32_t block_table_stride, int32_t num_seqs,
+                                       const int32_t *seq_request, const int32_t *seq_start,
+                                       const int32_t *cu_rows, int32_t total_rows,
+                                       void *latent_ws, int32_t *dev_status,
+                                       mla_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (num_seqs < 0 || total_rows < 0 || num_blocks < 0 || block_table_stride < 1)
+    return MLA_ERR_INVALID;
+  if (total_rows == 0) return MLA_OK;
+  if (!kv_cache || !block_table || !seq_request || !seq_start || !cu_rows || !latent_ws ||
+      num_seqs == 0)
+    return MLA_ERR_INVALID;
+  return launch_gather(kv_cache, num_blocks, d->block_size,
+                       (d->kv_lora_rank + d->qk_rope_dim) * elem_bytes(d->dtype), block_table,
+                       block_table_stride, num_seqs, seq_request, seq_start, cu_rows,
+                       total_rows, latent_ws, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
+                              int32_t rows, const void *w_kv_b, void *kv,
+                              mla_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (rows < 0 || latent_ld < d->kv_lora_rank) return MLA_ERR_INVALID;
+  if (rows == 0) return MLA_OK;
+  if (!latent || !w_kv_b || !kv) return MLA_ERR_INVALID;
+  return up_proj(*d, latent, latent_ld, rows, w_kv_b, kv, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
+                               const int32_t *q_loc, const int32_t *k_loc,
+                               const int32_t *q_loc_host, const int32_t *k_loc_host,
+                               int32_t num_tokens, const void *q, const void *kv,
+                               const void *latent, int64_t latent_ld,
+                               const int32_t *accumulate, float *o, float *lse,
+                               mla_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (num_seqs < 0 || num_tokens < 0) return MLA_ERR_INVALID;
+  if (num_seqs == 0) return MLA_OK;
+  if (!q_loc || !k_loc || !q_loc_host || !k_loc_host || !q || !kv || !latent || !o || !lse)
+    return MLA_ERR_INVALID;
+  if (latent_ld < d->kv_lora_rank + d->qk_rope_dim) return MLA_ERR_INVALID;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int nq = q_loc_host[i + 1] - q_loc_host[i], nk = k_loc_host[i + 1] - k_loc_host[i];
+    if (nq < 0 || nk < 0) return MLA_ERR_INVALID;
+    if (causal && nq != nk) return MLA_ERR_INVALID;
+  }
+  if (q_loc_host[0] < 0 || q_loc_host[num_seqs] > num_tokens) return MLA_ERR_INVALID;
+  return attention(*d, causal ? 1 : 0, num_seqs, q_loc, k_loc, q_loc_host, k_loc_host,
+                   num_tokens, q, kv, latent, latent_ld, accumulate, o, lse,
+                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_fill_empty_rows(float *o, float *lse, int32_t num_tokens, int32_t num_heads,
+                                   int32_t v_dim, int32_t num_slices, const int32_t *slices,
+                                   mla_stream_t stream) {
+  if (num_tokens < 0 || num_heads < 1 || v_dim < 1 || num_slices < 0) return MLA_ERR_INVALID;
+  if (num_slices == 0) return MLA_OK;
+  if (!o || !lse || !slices) return MLA_ERR_INVALID;
+  return launch_fill_empty_rows(o, lse, num_tokens, num_heads, v_dim, num_slices, slices,
+                                static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_mask_empty_context(float *lse, void *o, int32_t dtype, int32_t num_tokens,
+                                      int32_t num_heads, int32_t head_dim,
+                                      int32_t num_requests, const int32_t *query_start_loc,
+                                      const int32_t *context_start_loc, mla_stream_t stream) {
+  if (num_tokens < 0 || num_heads < 1 || head_dim < 1 || num_requests < 0 ||
+      !valid_dtype(dtype))
+    return MLA_ERR_INVALID;
+  if (num_tokens == 0 || num_requests == 0) return MLA_OK;
+  if (!lse || !o || !query_start_loc || !context_start_loc) return MLA_ERR_INVALID;
+  return launch_mask_empty_context(lse, o, dtype, num_tokens, num_heads, head_dim,
+                                   num_requests, query_start_loc, context_start_loc,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_chunk_workspace_bytes(const mla_dims_t *d, int32_t max_rows,
+                                         int32_t max_entries, size_t *bytes) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (max_rows < 0 || max_entries < 0 || !bytes) return MLA_ERR_INVALID;
+  Carve cv(nullptr);
+  cv.take(chunk_meta_ints(max_entries) * sizeof(int32_t));
+  ChunkBuffers b;
+  carve_chunk_buffers(cv, *d, max_rows, b);
+  *bytes = cv.off;
+  return MLA_OK;
+}
+
+extern "C" int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *chunk,
+                                      const int32_t *starts, const int32_t *seq_lens,
+                                      const int32_t *query_start_loc, int32_t num_tokens,
+                                      const void *q, const void *kv_cache, int32_t num_blocks,
+                                      const int32_t *block_table, int32_t block_table_stride,
+                                      const void *w_kv_b, void *workspace,
+                                      size_t workspace_bytes, float *o_partial,
+                                      float *lse_partial, int32_t *dev_status,
+                                      mla_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!chunk || !starts || !seq_lens || !query_start_loc || !q || !kv_cache || !block_table ||
+      !w_kv_b || !workspace || !o_partial || !lse_partial)
+    return MLA_ERR_INVALID;
+  const int n = chunk->request_end - chunk->request_start;
+  if (n < 1 || chunk->request_start < 0 || chunk->entry_offset < 0 || block_table_stride < 1)
+    return MLA_ERR_INVALID;
+  for (int i = 0; i < n; ++i) {
+    const int e = chunk->entry_offset + i;
+    if (starts[e] < 0 || seq_lens[e] < 1 ||
+        int64_t(starts[e]) + seq_lens[e] > int64_t(block_table_stride) * d->block_size)
+      return MLA_ERR_INVALID;
+  }
+  if (query_start_loc[chunk->request_end] > num_tokens) return MLA_ERR_INVALID;
+  ChunkMetaHost m;
+  build_chunk_meta(*chunk, starts, seq_lens, query_start_loc, m);
+  size_t need = 0;
+  mla_chunk_workspace_bytes(d, m.rows, n, &need);
+  if (workspace_bytes < need) return MLA_ERR_TOO_SMALL;
+  Carve cv(workspace);
+  int32_t *meta = static_cast<int32_t *>(cv.take(m.ints.size() * sizeof(int32_t)));
+  ChunkBuffers b;
+  carve_chunk_buffers(cv, *d, m.rows, b);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = upload(meta, m.ints, s);
+  if (rc) return rc;
+  return run_chunk(*d, m, meta, num_tokens, q, kv_cache, num_blocks, block_table,
+                   block_table_stride, w_kv_b, b, o_partial, lse_partial, dev_status, s);
+}
+
+namespace {
+
+struct PrefillLayout {
+  std::vector<mla_chunk_t> chunks;
+  std::vector<int32_t> starts, lens, qsl;
+  std::vector<ChunkMetaHost> metas;
+  std::vector<size_t> meta_off;            // int offset of each chunk's metadata
+  std::vector<std::pair<int, int>> empty;  // token slices of context-free requests
+  size_t slices_off = 0, suffix_off = 0, meta_total = 0;
+  int T = 0, pnt = 0, max_rows = 0;
+};
+
+int build_prefill(const mla_dims_t &d, const int32_t *ctx, const int32_t *ql, int R,
+                  int budget, int max_chunk, int align, PrefillLayout &p) {
+  for (int r = 0; r < R; ++r)
+    if (ql[r] < 0 || ctx[r] < 0) return MLA_ERR_INVALID;
+  int rc = plan_chunks(ctx, R, budget, max_chunk, align, nullptr, nullptr, p.chunks, p.starts,
+                       p.lens);
+  if (rc) return rc;
+  p.qsl.assign(R + 1, 0);
+  for (int r = 0; r < R; ++r) p.qsl[r + 1] = p.qsl[r] + ql[r];
+  p.T = p.qsl[R];
+  int last = -1;
+  for (int r = 0; r < R; ++r)
+    if (ctx[r] > 0) last = r;
+  p.pnt = last >= 0 ? p.qsl[last + 1] : 0;
+  for (int r = 0; r < R; ++r) {
+    const int lo = p.qsl[r], hi = std::min(p.qsl[r + 1], p.pnt);
+    if (ctx[r] == 0 && lo < hi) p.empty.emplace_back(lo, hi);
+  }
+  size_t off = 0;
+  p.metas.resize(p.chunks.size());
+  for (size_t c = 0; c < p.chunks.size(); ++c) {
+    build_chunk_meta(p.chunks[c], p.starts.data(), p.lens.data(), p.qsl.data(), p.metas[c]);
+    p.meta_off.push_back(off);
+    off += p.metas[c].ints.size();
+    p.max_rows = std::max(p.max_rows, p.metas[c].rows);
+  }
+  p.slices_off = off;
+  off += 2 * p.empty.size();
+  p.suffix_off = off;
+  off += R + 1;
+  p.meta_total = off;
+  return MLA_OK;
+}
+
+struct PrefillBuffers {
+  int32_t *meta;
+  ChunkBuffers chunk;
+  void *kv_suffix;
+  float *o_part, *lse_part, *o_suf, *lse_suf;
+};
+
+size_t carve_prefill(void *base, const mla_dims_t &d, const PrefillLayout &p,
+                     PrefillBuffers &b) {
+  Carve cv(base);
+  const int es = elem_bytes(d.dtype);
+  b.meta = static_cast<int32_t *>(cv.take(p.meta_total * sizeof(int32_t)));
+  carve_chunk_buffers(cv, d, p.max_rows, b.chunk);
+  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * es);
+  const size_t o_bytes = size_t(p.T) * d.num_heads * d.v_dim * sizeof(float);
+  const size_t l_bytes = size_t(p.T) * d.num_heads * sizeof(float);
+  b.o_part = static_cast<float *>(cv.take(o_bytes));
+  b.lse_part = static_cast<float *>(cv.take(l_bytes));
+  b.o_suf = static_cast<float *>(cv.take(o_bytes));
+  b.lse_suf = static_cast<float *>(cv.take(l_bytes));
+  return cv.off;
+}
+
+}  // namespace
+
+extern "C" int mla_prefill_workspace_bytes(const mla_dims_t *d, const int32_t *context_lens,
+                                           const int32_t *query_lens, int32_t num_requests,
+                                           int32_t row_budget, int32_t max_context_chunk,
+                                           int32_t split_alignment, size_t *bytes) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!bytes || num_requests < 0 || (num_requests > 0 && (!context_lens || !query_lens)))
+    return MLA_ERR_INVALID;
+  PrefillLayout p;
+  rc = build_prefill(*d, context_lens, query_lens, num_requests, row_budget, max_context_chunk,
+                     split_alignment, p);
+  if (rc) return rc;
+  PrefillBuffers b;
+  *bytes = carve_prefill(nullptr, *d, p, b);
+  return MLA_OK;
+}
+
+extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
+                                   const int32_t *query_lens, int32_t num_requests,
+                                   int32_t row_budget, int32_t max_context_chunk,
+                                   int32_t split_alignment, const void *q,
+                                   const void *new_latent, const void *kv_cache,
+                                   int32_t num_blocks, const int32_t *block_table,
+                                   int32_t block_table_stride, const void *w_kv_b,
+                                   void *workspace, size_t workspace_bytes, void *out,
+                                   float *out_lse, int32_t *dev_status, mla_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (num_requests < 0 || (num_requests > 0 && (!context_lens || !query_lens)))
+    return MLA_ERR_INVALID;
+  PrefillLayout p;
+  rc = build_prefill(*d, context_lens, query_lens, num_requests, row_budget, max_context_chunk,
+                     split_alignment, p);
+  if (rc) return rc;
+  if (p.T == 0) return MLA_OK;
+  if (!q || !new_latent || !w_kv_b || !workspace || !out) return MLA_ERR_INVALID;
+  if (!p.chunks.empty() && (!kv_cache || !block_table || block_table_stride < 1))
+    return MLA_ERR_INVALID;
+  for (int r = 0; r < num_requests; ++r)
+    if (int64_t(context_lens[r]) > int64_t(block_table_stride) * d->block_size)
+      return MLA_ERR_INVALID;
+  PrefillBuffers b;
+  const size_t need = carve_prefill(nullptr, *d, p, b);
+  if (workspace_bytes < need) return MLA_ERR_TOO_SMALL;
+  carve_prefill(workspace, *d, p, b);
+
+  std::vector<int32_t> meta(p.meta_total, 0);
+  for (size_t c = 0; c < p.metas.size(); ++c)
+    std::memcpy(meta.data() + p.meta_off[c], p.metas[c].ints.data(),
+                p.metas[c].ints.size() * sizeof(int32_t));
+  for (size_t k = 0; k < p.empty.size(); ++k) {
+    meta[p.slices_off + 2 * k] = p.empty[k].first;
+    meta[p.slices_off + 2 * k + 1] = p.empty[k].second;
+  }
+  std::memcpy(meta.data() + p.suffix_off, p.qsl.data(), p.qsl.size() * sizeof(int32_t));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = upload(b.meta, meta, s);
+  if (rc) return rc;
+
+  const int H = d->num_heads, Dv = d->v_dim, T = p.T;
+  const int LP = d->kv_lora_rank + d->qk_rope_dim;
+  rc = launch_fill_empty_rows(b.o_part, b.lse_part, T, H, Dv, int(p.empty.size()),
+                              b.meta + p.slices_off, s);
+  if (rc) return rc;
+  for (size_t c = 0; c < p.chunks.size(); ++c) {
+    rc = run_chunk(*d, p.metas[c], b.meta + p.meta_off[c], T, q, kv_cache, num_blocks,
+                   block_table, block_table_stride, w_kv_b, b.chunk, b.o_part, b.lse_part,
+                   dev_status, s);
+    if (rc) return rc;
+  }
+  rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, s);
+  if (rc) return rc;
+  const int32_t *sq = b.meta + p.suffix_off;
+  rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
+                 new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+  if (rc) return rc;
+  return launch_merge(out, out_lse, b.o_part, b.lse_part, b.o_suf, b.lse_suf, T, H, Dv, p.pnt,
+                      MLA_DTYPE_F32, d->dtype, s);
+}
+
+extern "C" int mla_has_tcgen05(void) { return tc_available() ? 1 : 0; }

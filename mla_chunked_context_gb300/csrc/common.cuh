@@ -1,0 +1,66 @@
+// Small device helpers shared by the CUDA kernels of this library.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mla_chunked_context.h"
+
+namespace mla {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ bool is_neg_inf(float x) {
+  return x == -__int_as_float(0x7f800000);
+}
+
+__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
+
+// Index of the sequence that owns position `x`: the largest i in [0, n) with
+// loc[i] <= x, for a non-decreasing loc[0..n].
+__device__ __forceinline__ int find_seq(const int32_t *loc, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(loc + mid) <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+inline int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+inline int elem_bytes(int32_t dtype) { return dtype == MLA_DTYPE_BF16 ? 2 : 4; }
+
+inline bool valid_dtype(int32_t dtype) {
+  return dtype == MLA_DTYPE_BF16 || dtype == MLA_DTYPE_F32;
+}
+
+inline int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace mla

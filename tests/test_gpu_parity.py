@@ -1,0 +1,460 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Tolerances (written here, applied elementwise):
+  * merge, float32 in/out:   |gpu - oracle| <= 1e-5 (O and LSE)
+  * merge, bf16 in/out:      within one bf16 rounding of the float64 result
+                             (|d| <= 2^-8 |ref| + 1e-6)
+  * attention / prefill:     O: |d| <= 2e-2 + 2e-2 |ref|;  LSE: |d| <= 1e-3
+  * gather, planner:         bit-exact
+  * up-projection (bf16 out): |d| <= 2e-3 + 8e-3 |ref|
+Inputs come from mla_chunked_context_gb300.workloads (seeded, host-drawn);
+expected values come only from oracle/.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_chunked_context_gb300 as M
+from mla_chunked_context_gb300 import workloads as W
+from oracle import mla as O
+from oracle import planner as P
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    M.lib()
+    torch.cuda.set_device(0)
+
+
+def f64(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+def assert_close(got, ref, atol, rtol=0.0, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    both_ninf = np.isneginf(got) & np.isneginf(ref)
+    d = np.where(both_ninf, 0.0, np.abs(got - ref))
+    lim = atol + rtol * np.abs(np.where(np.isfinite(ref), ref, 0.0))
+    bad = ~(d <= lim)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; "
+                             f"first {idx.tolist()} got {got[tuple(idx.T)]} ref {ref[tuple(idx.T)]}")
+
+
+def dims_of(w):
+    return M.Dims.of(w)
+
+
+def to_dev(x):
+    return {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in x.items()}
+
+
+def np_inputs(x):
+    return {k: (f64(v) if v.is_floating_point() else v.numpy()) for k, v in x.items()
+            if torch.is_tensor(v)}
+
+
+def odims(w):
+    return O.MlaDims(w.num_heads, w.kv_lora_rank, w.qk_rope_dim, w.qk_nope_dim, w.v_dim,
+                     w.block_size, w.softmax_scale)
+
+
+# ------------------------------------------------------------------ merge --
+def _merge_case(T, H, D, pnt, dtype, seed):
+    m = W.MergeWorkload(num_tokens=T, num_heads=H, head_dim=D, prefix_num_tokens=pnt,
+                        dtype=dtype, seed=seed, both_empty=4)
+    return m, W.make_merge_inputs(m, poison=True)
+
+
+def _run_merge(x, out_dtype, with_lse=True):
+    g = {k: v.to(DEV) for k, v in x.items() if torch.is_tensor(v)}
+    T, H, D = g["suffix_o"].shape
+    out = torch.full((T, H, D), float("nan"), dtype=out_dtype, device=DEV)
+    out_lse = torch.full((H, T), float("nan"), device=DEV) if with_lse else None
+    M.merge_attn_states(out, out_lse, g["prefix_o"], g["prefix_lse"], g["suffix_o"],
+                        g["suffix_lse"], x["prefix_num_tokens"])
+    torch.cuda.synchronize()
+    return out, out_lse
+
+
+def test_merge_fp32_tight():
+    m, x = _merge_case(300, 4, 16, 200, "f32", 31)
+    out, lse = _run_merge(x, torch.float32)
+    ro, rl = O.merge_attn_states(f64(x["prefix_o"]), f64(x["prefix_lse"]), f64(x["suffix_o"]),
+                                 f64(x["suffix_lse"]), m.prefix_num_tokens)
+    assert not torch.isnan(out).any()
+    assert_close(f64(out), ro, 1e-5, what="O")
+    assert_close(f64(lse), rl, 1e-5, what="LSE")
+    for t, h in x["both_empty"]:
+        assert (out[t, h] == 0).all() and math.isinf(lse[h, t].item())
+
+
+def test_merge_bf16_one_rounding():
+    m, x = _merge_case(1024, 16, 128, 768, "bf16", 32)
+    out, lse = _run_merge(x, torch.bfloat16)
+    ro, rl = O.merge_attn_states(f64(x["prefix_o"]), f64(x["prefix_lse"]), f64(x["suffix_o"]),
+                                 f64(x["suffix_lse"]), m.prefix_num_tokens)
+    assert_close(f64(out), ro, 1e-6, 2.0 ** -8, what="O")
+    assert_close(f64(lse), rl, 1e-5, what="LSE")
+    # tokens at or past prefix_num_tokens: the suffix, bit for bit
+    assert torch.equal(out[768:].cpu(), x["suffix_o"][768:])
+
+
+def test_merge_full_size_sampled_and_properties():
+    m = W.MergeWorkload()
+    x = W.make_merge_inputs(m, poison=True)
+    out, lse = _run_merge(x, torch.bfloat16)
+    T, H, D = out.shape
+    assert not torch.isnan(out).any().item()
+    pnt = m.prefix_num_tokens
+    assert torch.equal(out[pnt:].cpu(), x["suffix_o"][pnt:])
+    assert torch.equal(lse[:, pnt:].cpu(), x["suffix_lse"][:, pnt:])
+    for t, h in x["both_empty"]:
+        assert (out[t, h] == 0).all() and math.isinf(lse[h, t].item()) and lse[h, t] < 0
+    rng = np.random.default_rng(5)
+    ts = rng.integers(0, pnt, size=4096)
+    hs = rng.integers(0, H, size=4096)
+    po = f64(x["prefix_o"][ts, hs])[:, None, :]
+    so = f64(x["suffix_o"][ts, hs])[:, None, :]
+    pl = f64(x["prefix_lse"][hs, ts])[None, :]
+    sl = f64(x["suffix_lse"][hs, ts])[None, :]
+    ro, rl = O.merge_attn_states(po.transpose(1, 0, 2).reshape(len(ts), 1, D), pl,
+                                 so.transpose(1, 0, 2).reshape(len(ts), 1, D), sl, len(ts))
+    got = f64(out[ts, hs])
+    assert_close(got, ro[:, 0, :], 1e-6, 2.0 ** -8, what="O sampled")
+    assert_close(f64(lse[hs, ts]), rl[0], 1e-5, what="LSE sampled")
+
+
+def test_merge_in_place_on_suffix():
+    m, x = _merge_case(257, 8, 64, 100, "f32", 33)
+    g = {k: v.to(DEV) for k, v in x.items() if torch.is_tensor(v)}
+    ro, _ = O.merge_attn_states(f64(x["prefix_o"]), f64(x["prefix_lse"]), f64(x["suffix_o"]),
+                                f64(x["suffix_lse"]), 100)
+    M.merge_attn_states(g["suffix_o"], None, g["prefix_o"], g["prefix_lse"], g["suffix_o"],
+                        g["suffix_lse"], 100)
+    torch.cuda.synchronize()
+    assert_close(f64(g["suffix_o"]), ro, 1e-5, what="in-place O")
+
+
+def test_merge_empty_batch_and_zero_prefix():
+    z = torch.empty(0, 2, 8, device=DEV)
+    zl = torch.empty(2, 0, device=DEV)
+    M.merge_attn_states(z, zl, z, zl, z, zl, 0)
+    m, x = _merge_case(64, 2, 8, 0, "f32", 34)
+    out, lse = _run_merge(x, torch.float32)
+    assert torch.equal(out.cpu(), x["suffix_o"]) and torch.equal(lse.cpu(), x["suffix_lse"])
+
+
+# ---------------------------------------------------- empty-context rows --
+def test_mask_empty_context_page_shape():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "mask_empty_context.json")))
+    H, T, D = g["num_heads"], g["num_tokens"], g["head_dim"]
+    lo, hi = g["masked_rows"]
+    gen = torch.Generator().manual_seed(3)
+    lse = torch.randn(H, T, generator=gen)
+    out = torch.randn(T, H, D, generator=gen)
+    out[lo:hi] = float("nan")
+    qsl = torch.tensor(P.query_start_loc(g["query_lens"]), dtype=torch.int32)
+    csl = torch.tensor(P.query_start_loc(g["context_lens"]), dtype=torch.int32)
+    rl, ro = O.mask_empty_context(lse.double().numpy(), out.double().numpy(), qsl.numpy(),
+                                  csl.numpy())
+    dl, do = lse.to(DEV), out.to(DEV)
+    M.mla_mask_empty_context(dl, do, qsl.to(DEV), csl.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(f64(dl), rl) and np.array_equal(f64(do), ro)
+    # the partial initialisation of the chunked scheme gives the same rows
+    o2 = torch.full((T, H, D), float("nan"), device=DEV)
+    l2 = torch.full((H, T), float("nan"), device=DEV)
+    M.mla_fill_empty_rows(o2, l2, P.empty_token_slices(g["context_lens"], g["query_lens"]))
+    torch.cuda.synchronize()
+    assert (o2[lo:hi] == 0).all() and torch.isneginf(l2[:, lo:hi]).all()
+    assert torch.isnan(o2[:lo]).all() and torch.isnan(l2[:, hi:]).all()
+
+
+# ---------------------------------------------------------------- gather --
+def _gather_case(w, plan):
+    x = W.make_inputs(w)
+    g = to_dev(x)
+    n = plan.request_end - plan.request_start
+    req = torch.arange(plan.request_start, plan.request_end, dtype=torch.int32, device=DEV)
+    st = torch.tensor(plan.starts, dtype=torch.int32, device=DEV)
+    cu = torch.tensor([0] + list(np.cumsum(plan.seq_lens)), dtype=torch.int32, device=DEV)
+    rows = int(sum(plan.seq_lens))
+    ws = torch.full((rows, w.latent_dim), float("nan"), dtype=w.torch_dtype, device=DEV)
+    return x, g, req, st, cu, rows, ws, n
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek"])
+def test_gather_bit_exact(name):
+    if name == "tiny":
+        w = W.workload("tiny")
+    else:
+        w = W.scaled(W.workload("uniform"), context_lens=[0, 300, 1000, 5, 700],
+                     query_lens=[1, 1, 1, 1, 1], num_heads=2, seed=40)
+    plans = P.plan_mla_context_chunks(w.context_lens, 512, 512, 16)
+    for plan in plans:
+        x, g, req, st, cu, rows, ws, n = _gather_case(w, plan)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        M.mla_gather_context_rows(M.Dims.of(w), g["kv_cache"], g["block_table"], req, st, cu,
+                                  rows, ws, status)
+        torch.cuda.synchronize()
+        ref = O.gather_chunk(f64(x["kv_cache"]), x["block_table"].numpy(), plan, w.block_size)
+        assert np.array_equal(f64(ws), ref)
+        assert status.item() == 0
+
+
+def test_gather_bad_block_sets_status():
+    w = W.workload("tiny")
+    plan = P.plan_mla_context_chunks(w.context_lens, 128, 128, 16)[0]
+    x, g, req, st, cu, rows, ws, n = _gather_case(w, plan)
+    bt = g["block_table"].clone()
+    bt[1, 2] = 10 ** 6                      # request 1, rows 32..47
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    M.mla_gather_context_rows(M.Dims.of(w), g["kv_cache"], bt, req, st, cu, rows, ws, status)
+    torch.cuda.synchronize()
+    assert status.item() == M.MLA_STATUS_BAD_BLOCK
+    assert (ws[32:48] == 0).all()
+    ref = O.gather_chunk(f64(x["kv_cache"]), x["block_table"].numpy(), plan, w.block_size)
+    assert np.array_equal(f64(ws[:32]), ref[:32]) and np.array_equal(f64(ws[48:]), ref[48:])
+
+
+# ----------------------------------------------------------- up-projection --
+@pytest.mark.parametrize("rows,heads", [(300, 8), (128, 2), (1, 2), (4099, 16)])
+def test_up_proj_deepseek(rows, heads):
+    w = W.scaled(W.workload("uniform"), num_heads=heads, seed=41)
+    gen = torch.Generator().manual_seed(rows)
+    lat = torch.randn(rows, w.latent_dim, generator=gen).to(torch.bfloat16)
+    wkv = (torch.randn(heads * 256, 512, generator=gen) * 0.02).to(torch.bfloat16)
+    kv = torch.full((rows, heads * 256), float("nan"), dtype=torch.bfloat16, device=DEV)
+    M.mla_kv_up_proj(M.Dims.of(w), lat.to(DEV), rows, wkv.to(DEV), kv)
+    torch.cuda.synchronize()
+    kn, v = O.up_project(f64(lat), f64(wkv), odims(w))
+    ref = np.concatenate([kn, v], axis=2).reshape(rows, heads * 256)
+    assert_close(f64(kv), ref, 2e-3, 8e-3, what="kv")
+
+
+def test_up_proj_fp32_tiny():
+    w = W.workload("tiny")
+    x = W.make_inputs(w)
+    lat = x["new_latent"]
+    kv = torch.empty(lat.shape[0], w.num_heads * 64, device=DEV)
+    M.mla_kv_up_proj(M.Dims.of(w), lat.to(DEV), lat.shape[0], x["w_kv_b"].to(DEV), kv)
+    torch.cuda.synchronize()
+    kn, v = O.up_project(f64(lat), f64(x["w_kv_b"]), odims(w))
+    ref = np.concatenate([kn, v], axis=2).reshape(lat.shape[0], -1)
+    assert_close(f64(kv), ref, 1e-5, 1e-5, what="kv fp32")
+
+
+# -------------------------------------------------------------- attention --
+def _attn_inputs(w, n_rows, T, seed):
+    gen = torch.Generator().manual_seed(seed)
+    H = w.num_heads
+    q = torch.randn(T, H, w.qk_dim, generator=gen).to(w.torch_dtype)
+    kv = (0.45 * torch.randn(n_rows, H * (w.qk_nope_dim + w.v_dim), generator=gen)).to(
+        w.torch_dtype)
+    lat = torch.randn(n_rows, w.latent_dim, generator=gen).to(w.torch_dtype)
+    return q, kv, lat
+
+
+def _oracle_attn(w, q, kv, lat, q_loc, k_loc, causal):
+    H, Dn, Dv, L = w.num_heads, w.qk_nope_dim, w.v_dim, w.kv_lora_rank
+    T = q.shape[0]
+    kvr = f64(kv).reshape(kv.shape[0], H, Dn + Dv)
+    o = np.full((T, H, Dv), np.nan)
+    lse = np.full((H, T), np.nan)
+    for i in range(len(q_loc) - 1):
+        a, b, c, e = q_loc[i], q_loc[i + 1], k_loc[i], k_loc[i + 1]
+        if a == b:
+            continue
+        vis = np.tril(np.ones((b - a, e - c), dtype=bool)) if causal else None
+        o[a:b], lse[:, a:b] = O.attention_with_lse(
+            f64(q[a:b]), kvr[c:e, :, :Dn], f64(lat[c:e, L:]), kvr[c:e, :, Dn:],
+            w.softmax_scale, visible=vis)
+    return o, lse
+
+
+@pytest.mark.parametrize("kind", ["deepseek", "tiny"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_attention(kind, causal):
+    if kind == "deepseek":
+        w = W.scaled(W.workload("uniform"), num_heads=4, seed=42)
+        if causal:
+            ql = [1, 130, 77, 256, 129]
+            kl = ql
+        else:
+            ql = [1, 130, 77, 3, 200]
+            kl = [5, 300, 129, 1000, 64]
+    else:
+        w = W.workload("tiny")
+        ql = [3, 16, 5]
+        kl = ql if causal else [64, 128, 37]
+    q_loc = [0] + list(np.cumsum(ql))
+    k_loc = [0] + list(np.cumsum(kl))
+    q, kv, lat = _attn_inputs(w, k_loc[-1], q_loc[-1], 7)
+    o = torch.full((q_loc[-1], w.num_heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((w.num_heads, q_loc[-1]), float("nan"), device=DEV)
+    M.mla_varlen_attn(M.Dims.of(w), causal, q_loc, k_loc, q.to(DEV), kv.to(DEV), lat.to(DEV),
+                      o, lse)
+    torch.cuda.synchronize()
+    ro, rl = _oracle_attn(w, q, kv, lat, q_loc, k_loc, causal)
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
+def test_varlen_attention_accumulate():
+    """Chunk 2 continues the requests of chunk 1 and merges into its partial;
+    the result equals attention over both key ranges at once."""
+    w = W.scaled(W.workload("uniform"), num_heads=2, seed=43)
+    ql = [7, 140]
+    k1, k2 = [100, 260], [60, 131]
+    q_loc = [0] + list(np.cumsum(ql))
+    q, kv, lat = _attn_inputs(w, sum(k1) + sum(k2), q_loc[-1], 8)
+    # key rows: chunk-1 rows of both requests, then chunk-2 rows of both
+    loc1 = [0, k1[0], k1[0] + k1[1]]
+    loc2 = [loc1[-1], loc1[-1] + k2[0], loc1[-1] + k2[0] + k2[1]]
+    o = torch.full((q_loc[-1], 2, 128), float("nan"), device=DEV)
+    lse = torch.full((2, q_loc[-1]), float("nan"), device=DEV)
+    d = M.Dims.of(w)
+    gq, gkv, glat = q.to(DEV), kv.to(DEV), lat.to(DEV)
+    M.mla_varlen_attn(d, False, q_loc, loc1, gq, gkv, glat, o, lse)
+    M.mla_varlen_attn(d, False, q_loc, loc2, gq, gkv, glat, o, lse, accumulate=[1, 1])
+    torch.cuda.synchronize()
+    idx = [np.r_[0:100, 360:420], np.r_[100:360, 420:551]]
+    kvr = f64(kv).reshape(kv.shape[0], 2, 256)
+    for i in range(2):
+        a, b = q_loc[i], q_loc[i + 1]
+        ro, rl = O.attention_with_lse(f64(q[a:b]), kvr[idx[i], :, :128], f64(lat[idx[i], 512:]),
+                                      kvr[idx[i], :, 128:], w.softmax_scale)
+        assert_close(f64(o[a:b]), ro, 2e-2, 2e-2, what="O")
+        assert_close(f64(lse[:, a:b]), rl, 1e-3, what="LSE")
+
+
+# ---------------------------------------------------------- whole prefill --
+def _run_prefill(w, x):
+    g = to_dev(x)
+    T = w.num_tokens
+    out = torch.full((T, w.num_heads, w.v_dim), float("nan"), dtype=w.torch_dtype, device=DEV)
+    out_lse = torch.full((w.num_heads, T), float("nan"), device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pf = M.ChunkedPrefill(M.Dims.of(w), w.context_lens, w.query_lens, w.row_budget,
+                          w.max_context_chunk, w.split_alignment, device=DEV)
+    pf(g["q"], g["new_latent"], g["kv_cache"], g["block_table"], g["w_kv_b"], out, out_lse,
+       status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    return out, out_lse
+
+
+def _oracle_prefill(w, x):
+    n = np_inputs(x)
+    return O.chunked_prefill(n["q"], n["new_latent"], n["kv_cache"], n["block_table"],
+                             n["w_kv_b"], w.context_lens, w.query_lens, odims(w), w.row_budget,
+                             w.max_context_chunk, w.split_alignment)
+
+
+def test_prefill_tiny_workload():
+    w = W.workload("tiny")
+    x = W.make_inputs(w)
+    out, lse = _run_prefill(w, x)
+    ro, rl, _ = _oracle_prefill(w, x)
+    assert not torch.isnan(out).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+    # float32 storage: far inside the contract
+    assert_close(f64(out), ro, 1e-4, 1e-4, what="O fp32")
+
+
+@pytest.mark.parametrize("budget", [512, 2048])
+def test_prefill_deepseek_shapes_multichunk(budget):
+    w = W.scaled(W.workload("uniform"), context_lens=[0, 300, 1000, 5, 0, 700, 64],
+                 query_lens=[3, 130, 1, 40, 7, 200, 0], num_heads=8, row_budget=budget,
+                 max_context_chunk=budget, split_alignment=64, seed=44)
+    x = W.make_inputs(w)
+    out, lse = _run_prefill(w, x)
+    ro, rl, plans = _oracle_prefill(w, x)
+    assert len(plans) >= 2
+    assert not torch.isnan(out).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
+def test_chunk_entry_composes_to_prefill():
+    """mla_context_chunk_attn per chunk + fill + new-token attention + merge
+    gives exactly what mla_chunked_prefill gives."""
+    w = W.scaled(W.workload("uniform"), context_lens=[200, 0, 900, 50],
+                 query_lens=[20, 5, 130, 9], num_heads=4, row_budget=512,
+                 max_context_chunk=512, split_alignment=64, seed=45)
+    x = W.make_inputs(w)
+    g = to_dev(x)
+    out_ref, lse_ref = _run_prefill(w, x)
+    d = M.Dims.of(w)
+    T, H = w.num_tokens, w.num_heads
+    qsl = P.query_start_loc(w.query_lens)
+    chunks = M.mla_plan_context_chunks(w.context_lens, 512, 512, 64)
+    op = torch.full((T, H, 128), float("nan"), device=DEV)
+    lp = torch.full((H, T), float("nan"), device=DEV)
+    M.mla_fill_empty_rows(op, lp, P.empty_token_slices(w.context_lens, w.query_lens))
+    ws = torch.empty(M.mla_chunk_workspace_bytes(d, max(c.rows for c in chunks), 8),
+                     dtype=torch.uint8, device=DEV)
+    for c in chunks:
+        M.mla_context_chunk_attn(d, c, qsl, g["q"], g["kv_cache"], g["block_table"],
+                                 g["w_kv_b"], ws, op, lp)
+    kvs = torch.empty(T, H * 256, dtype=torch.bfloat16, device=DEV)
+    M.mla_kv_up_proj(d, g["new_latent"], T, g["w_kv_b"], kvs)
+    os_ = torch.empty(T, H, 128, device=DEV)
+    ls = torch.empty(H, T, device=DEV)
+    M.mla_varlen_attn(d, True, qsl, qsl, g["q"], kvs, g["new_latent"], os_, ls)
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(H, T, device=DEV)
+    M.merge_attn_states(out, lse, op, lp, os_, ls,
+                        P.prefix_num_tokens(w.context_lens, w.query_lens))
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
+
+
+# -------------------------------------------- full sizes, sampled outputs --
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["uniform", "hetero", "long"])
+def test_prefill_full_size_sampled(name):
+    w = W.workload(name)
+    x = W.make_inputs(w)
+    out, lse = _run_prefill(w, x)
+    T, H = w.num_tokens, w.num_heads
+    assert not torch.isnan(out).any().item() and not torch.isnan(lse).any().item()
+    rng = np.random.default_rng(77)
+    qsl = P.query_start_loc(w.query_lens)
+    # samples: a few tokens of a few requests (always including the longest
+    # context and a context-free one when present), random heads
+    reqs = sorted(set([int(np.argmax(w.context_lens))] +
+                      [r for r, c in enumerate(w.context_lens) if c == 0][:1] +
+                      list(rng.choice(len(w.context_lens), size=3, replace=False))))
+    toks, heads = [], []
+    for r in reqs:
+        a, b = qsl[r], qsl[r + 1]
+        for t in sorted(set([a, b - 1, int(rng.integers(a, b))])):
+            for h in rng.choice(H, size=2, replace=False):
+                toks.append(t)
+                heads.append(int(h))
+    # float32 views of the bf16 inputs are exact; the oracle computes in float64
+    ro, rl = O.unchunked_rows(x["q"].float().numpy(), x["new_latent"].float().numpy(),
+                              x["kv_cache"].float().numpy(), x["block_table"].numpy(),
+                              x["w_kv_b"].float().numpy(), w.context_lens, w.query_lens,
+                              odims(w), toks, heads)
+    assert_close(f64(out[toks, heads]), ro, 2e-2, 2e-2, what="O sampled")
+    assert_close(f64(lse[heads, toks]), rl, 1e-3, what="LSE sampled")
