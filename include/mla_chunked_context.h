@@ -70,9 +70,15 @@ enum {
   MLA_ERR_UNSUPPORTED = -5     /* dims / dtype combination not supported       */
 };
 
-enum { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1 };
+/* Element types.  mla_dims_t.dtype (the inputs and the final output) is F32
+ * or BF16; F16 is used for the up-projected K/V workspace (see
+ * mla_kv_up_proj). */
+enum { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1, MLA_DTYPE_F16 = 2 };
 
 enum { MLA_STATUS_BAD_BLOCK = 1 };
+
+/* Bits of mla_device_error_flags(). */
+enum { MLA_DEVICE_ERR_WAIT_TIMEOUT = 1 };
 
 typedef struct {
   int32_t num_heads;     /* H  */
@@ -174,11 +180,16 @@ int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache,
                             int32_t *dev_status, mla_stream_t stream);
 
 /* mla_kv_up_proj: kv[rows, H*(Dn+Dv)] = latent[:, 0:L] . w_kv_b^T
- *   latent device [rows, latent_ld] in dtype (latent_ld >= L); kv device,
- *   row-major [rows, H*(Dn+Dv)] in dtype.  For bf16 with L % 64 == 0 and
- *   H*(Dn+Dv) % 256 == 0 this runs on the tcgen05 tensor-core GEMM. */
+ *   latent device [rows, latent_ld] in dtype (latent_ld >= L); w_kv_b in
+ *   dtype; kv device, row-major [rows, H*(Dn+Dv)] in kv_dtype (F32, BF16 or
+ *   F16; accumulation is float32, the result is rounded once to kv_dtype).
+ *   For bf16 inputs with L % 64 == 0, H*(Dn+Dv) % 256 == 0 and a 16-bit
+ *   kv_dtype this runs on the tcgen05 tensor-core GEMM.  The chunked path
+ *   stores K/V as F16 on the tensor-core path: bf16 keeps 8 significant bits
+ *   and its rounding of K_nope alone moves a one-key LSE by ~5e-4 (1 sigma),
+ *   fp16 keeps 11. */
 int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
-                   int32_t rows, const void *w_kv_b, void *kv,
+                   int32_t rows, const void *w_kv_b, void *kv, int32_t kv_dtype,
                    mla_stream_t stream);
 
 /* mla_varlen_attn: softmax attention per sequence, returning (O, LSE).
@@ -193,13 +204,17 @@ int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
  *   overwriting them (PR #50613 report, item 3, accumulate_mla_context_chunk).
  *   q_loc, k_loc device [num_seqs+1]; max_q / max_k: upper bounds of the
  *   per-sequence counts.  o device float32 [T, H, Dv]; lse float32 [H, T];
- *   num_tokens = T (the row count of q, o and lse).
+ *   num_tokens = T (the row count of q, o and lse).  kv is in kv_dtype
+ *   (F32, BF16 or F16); q and latent in d->dtype.  The tcgen05 kernel runs
+ *   for the DeepSeek-V3 head shape (L 512, P 64, Dn 128, Dv 128), bf16 q and
+ *   latent and F16 kv; it converts q_nope to fp16 on chip (exact for bf16
+ *   values of magnitude 2^-14 .. 65504).
  *   A row that sees no key gets O = 0, LSE = -inf. */
 int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
                     const int32_t *q_loc, const int32_t *k_loc,
                     const int32_t *q_loc_host, const int32_t *k_loc_host,
                     int32_t num_tokens, const void *q, const void *kv,
-                    const void *latent, int64_t latent_ld,
+                    int32_t kv_dtype, const void *latent, int64_t latent_ld,
                     const int32_t *accumulate, float *o, float *lse,
                     mla_stream_t stream);
 
@@ -223,6 +238,12 @@ int mla_mask_empty_context(float *lse, void *o, int32_t dtype,
                            const int32_t *query_start_loc,
                            const int32_t *context_start_loc,
                            mla_stream_t stream);
+
+/* mla_chunk_kv_dtype: the K/V workspace element type (MLA_DTYPE_*) that
+ *   mla_context_chunk_attn and mla_chunked_prefill use on the current device
+ *   for these dims: F16 where the tcgen05 kernels run, F32 otherwise.  For
+ *   callers that compose the per-step calls themselves. */
+int mla_chunk_kv_dtype(const mla_dims_t *d, int32_t *kv_dtype);
 
 /* ---------------------------------------------------------------------------
  * Chunk-level and whole-prefill calls.
@@ -272,6 +293,8 @@ int mla_prefill_workspace_bytes(const mla_dims_t *d,
  *   out device [T, H, Dv] in dtype; out_lse device float32 [H, T], nullable.
  *   workspace: device, >= mla_prefill_workspace_bytes.
  *   All metadata goes to the device in one cudaMemcpyAsync from host memory.
+ *   On the tensor-core path the workspace keeps K/V in fp16 (see
+ *   mla_kv_up_proj); on the CUDA-core path in float32.
  */
 int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
                         const int32_t *query_lens, int32_t num_requests,
@@ -284,9 +307,14 @@ int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
                         float *out_lse, int32_t *dev_status,
                         mla_stream_t stream);
 
-/* Library build information: 1 when the tcgen05 kernels were compiled for
- * sm_103a in this binary. */
+/* 1 when the current device runs the tcgen05 (sm_103a) kernels of this
+ * library. */
 int mla_has_tcgen05(void);
+
+/* Reads and clears the device-side error bits of the tensor-core kernels
+ * (MLA_DEVICE_ERR_*; nonzero means a kernel gave up waiting on one of its
+ * own barriers and its output is not valid).  Synchronises the device. */
+int mla_device_error_flags(int32_t *flags);
 
 #if defined(__GNUC__)
 #pragma GCC visibility pop

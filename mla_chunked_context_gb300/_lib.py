@@ -22,7 +22,7 @@ HEADER = os.path.join(HERE, "..", "include", "mla_chunked_context.h")
 
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_TOO_SMALL, MLA_ERR_PLANNER_STUCK, MLA_ERR_CUDA, \
     MLA_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
-MLA_DTYPE_F32, MLA_DTYPE_BF16 = 0, 1
+MLA_DTYPE_F32, MLA_DTYPE_BF16, MLA_DTYPE_F16 = 0, 1, 2
 MLA_STATUS_BAD_BLOCK = 1
 
 _ERRORS = {MLA_ERR_INVALID: "invalid argument", MLA_ERR_TOO_SMALL: "buffer too small",
@@ -32,7 +32,8 @@ _ERRORS = {MLA_ERR_INVALID: "invalid argument", MLA_ERR_TOO_SMALL: "buffer too s
 EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_rows",
             "mla_kv_up_proj", "mla_varlen_attn", "mla_fill_empty_rows", "mla_mask_empty_context",
             "mla_chunk_workspace_bytes", "mla_context_chunk_attn", "mla_prefill_workspace_bytes",
-            "mla_chunked_prefill", "mla_has_tcgen05")
+            "mla_chunked_prefill", "mla_has_tcgen05", "mla_device_error_flags",
+            "mla_chunk_kv_dtype")
 
 
 class MlaError(RuntimeError):
@@ -72,8 +73,8 @@ def lib() -> C.CDLL:
                                         I32, P, P],
             "merge_attn_states": [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P],
             "mla_gather_context_rows": [P, P, I32, P, I32, I32, P, P, P, I32, P, P, P],
-            "mla_kv_up_proj": [P, P, I64, I32, P, P, P],
-            "mla_varlen_attn": [P, I32, I32, P, P, P, P, I32, P, P, P, I64, P, P, P, P],
+            "mla_kv_up_proj": [P, P, I64, I32, P, P, I32, P],
+            "mla_varlen_attn": [P, I32, I32, P, P, P, P, I32, P, P, I32, P, I64, P, P, P, P],
             "mla_fill_empty_rows": [P, P, I32, I32, I32, I32, P, P],
             "mla_mask_empty_context": [P, P, I32, I32, I32, I32, I32, P, P, P],
             "mla_chunk_workspace_bytes": [P, I32, I32, P],
@@ -83,6 +84,8 @@ def lib() -> C.CDLL:
             "mla_chunked_prefill": [P, P, P, I32, I32, I32, I32, P, P, P, I32, P, I32, P, P, SZ,
                                     P, P, P, P],
             "mla_has_tcgen05": [],
+            "mla_device_error_flags": [P],
+            "mla_chunk_kv_dtype": [P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -119,7 +122,13 @@ def dtype_code(t: torch.dtype) -> int:
         return MLA_DTYPE_BF16
     if t == torch.float32:
         return MLA_DTYPE_F32
+    if t == torch.float16:
+        return MLA_DTYPE_F16
     raise ValueError(f"unsupported dtype {t}")
+
+
+_TORCH_OF = {MLA_DTYPE_F32: torch.float32, MLA_DTYPE_BF16: torch.bfloat16,
+             MLA_DTYPE_F16: torch.float16}
 
 
 @dataclass
@@ -215,9 +224,11 @@ def mla_gather_context_rows(dims: Dims, kv_cache, block_table, seq_request, seq_
 
 
 def mla_kv_up_proj(dims: Dims, latent, rows: int, w_kv_b, kv, stream=None) -> None:
+    """kv's torch dtype (float32 / bfloat16 / float16) selects the output type."""
     d = dims.c()
     _check(lib().mla_kv_up_proj(C.byref(d), _ptr(latent), latent.stride(0), rows, _ptr(w_kv_b),
-                                _ptr(kv), _stream(stream)), "mla_kv_up_proj")
+                                _ptr(kv), dtype_code(kv.dtype), _stream(stream)),
+           "mla_kv_up_proj")
 
 
 def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Sequence[int], q,
@@ -232,8 +243,9 @@ def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Seque
     d = dims.c()
     _check(lib().mla_varlen_attn(C.byref(d), int(causal), n, _ptr(ql), _ptr(kl),
                                  _i32_host(q_loc), _i32_host(k_loc), q.shape[0], _ptr(q),
-                                 _ptr(kv), _ptr(latent), latent.stride(0), _ptr(acc), _ptr(o),
-                                 _ptr(lse), _stream(stream)), "mla_varlen_attn")
+                                 _ptr(kv), dtype_code(kv.dtype), _ptr(latent), latent.stride(0),
+                                 _ptr(acc), _ptr(o), _ptr(lse), _stream(stream)),
+           "mla_varlen_attn")
 
 
 def mla_fill_empty_rows(o, lse, slices: Sequence, stream=None) -> None:
@@ -302,3 +314,16 @@ def mla_chunked_prefill(dims: Dims, context_lens, query_lens, row_budget: int,
 
 def mla_has_tcgen05() -> bool:
     return bool(lib().mla_has_tcgen05())
+
+
+def mla_device_error_flags() -> int:
+    f = C.c_int32(0)
+    _check(lib().mla_device_error_flags(C.byref(f)), "mla_device_error_flags")
+    return f.value
+
+
+def mla_chunk_kv_dtype(dims: Dims) -> torch.dtype:
+    d = dims.c()
+    k = C.c_int32(0)
+    _check(lib().mla_chunk_kv_dtype(C.byref(d), C.byref(k)), "mla_chunk_kv_dtype")
+    return _TORCH_OF[k.value]

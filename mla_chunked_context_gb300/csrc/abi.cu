@@ -27,17 +27,19 @@ int launch_gather(const void *cache, int num_blocks, int block_size, int row_byt
                   const int32_t *cu_rows, int total_rows, void *ws, int32_t *status,
                   cudaStream_t s);
 bool generic_dims_ok(const mla_dims_t &d);
-int launch_up_proj_simt(int dtype, const void *latent, int64_t lda, int rows, const void *w,
-                        void *kv, int N, int K, cudaStream_t s);
+int launch_up_proj_simt(int dtype, int kv_dtype, const void *latent, int64_t lda, int rows,
+                        const void *w, void *kv, int N, int K, cudaStream_t s);
 int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                      const int32_t *k_loc, int num_q_rows, int T, const void *q,
-                     const void *kv, const void *latent, int64_t latent_ld,
+                     const void *kv, int kv_dtype, const void *latent, int64_t latent_ld,
                      const int32_t *accumulate, float *o, float *lse, cudaStream_t s);
-bool tc_gemm_ok(const mla_dims_t &d, int64_t lda, const void *latent, const void *w,
-                const void *kv);
-int launch_up_proj_tc(const mla_dims_t &d, const void *latent, int64_t lda, int rows,
-                      const void *w, void *kv, cudaStream_t s);
-bool tc_attn_ok(const mla_dims_t &d, int64_t latent_ld);
+bool tc_gemm_ok(const mla_dims_t &d, int kv_dtype, int64_t lda, const void *latent,
+                const void *w, const void *kv);
+int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int64_t lda,
+                      int rows, const void *w, void *kv, cudaStream_t s);
+bool tc_attn_ok(const mla_dims_t &d, int kv_dtype, int64_t latent_ld);
+int gemm_take_errors();
+int attn_take_errors();
 int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                    const int32_t *k_loc, const int32_t *q_loc_host,
                    const int32_t *k_loc_host, int T, const void *q, const void *kv,
@@ -76,25 +78,37 @@ int check_dims(const mla_dims_t *d) {
 
 inline int kv_width(const mla_dims_t &d) { return d.num_heads * (d.qk_nope_dim + d.v_dim); }
 
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// K/V workspace type of the chunked path: fp16 where the tensor-core
+// attention runs (bf16 inputs of the DeepSeek-V3 head shape), float32 for the
+// CUDA-core kernels.
+int path_kv_dtype(const mla_dims_t &d) {
+  const int LP = d.kv_lora_rank + d.qk_rope_dim;
+  return (tc_available() && tc_attn_ok(d, MLA_DTYPE_F16, LP)) ? MLA_DTYPE_F16 : MLA_DTYPE_F32;
+}
+
 int up_proj(const mla_dims_t &d, const void *latent, int64_t lda, int rows, const void *w,
-            void *kv, cudaStream_t s) {
+            void *kv, int kv_dtype, cudaStream_t s) {
   if (rows == 0) return MLA_OK;
-  if (tc_available() && tc_gemm_ok(d, lda, latent, w, kv))
-    return launch_up_proj_tc(d, latent, lda, rows, w, kv, s);
-  return launch_up_proj_simt(d.dtype, latent, lda, rows, w, kv, kv_width(d), d.kv_lora_rank, s);
+  if (tc_available() && tc_gemm_ok(d, kv_dtype, lda, latent, w, kv))
+    return launch_up_proj_tc(d, kv_dtype, latent, lda, rows, w, kv, s);
+  return launch_up_proj_simt(d.dtype, kv_dtype, latent, lda, rows, w, kv, kv_width(d),
+                             d.kv_lora_rank, s);
 }
 
 int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
               const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
-              int T, const void *q, const void *kv, const void *latent, int64_t latent_ld,
-              const int32_t *acc, float *o, float *lse, cudaStream_t s) {
+              int T, const void *q, const void *kv, int kv_dtype, const void *latent,
+              int64_t latent_ld, const int32_t *acc, float *o, float *lse, cudaStream_t s) {
   const int nq = q_loc_host[n] - q_loc_host[0];
   if (n == 0 || nq == 0) return MLA_OK;
-  if (tc_available() && tc_attn_ok(d, latent_ld))
+  if (tc_available() && tc_attn_ok(d, kv_dtype, latent_ld) && aligned16(q) && aligned16(kv) &&
+      aligned16(latent))
     return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, q, kv,
                           latent, latent_ld, acc, o, lse, s);
-  return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, q, kv, latent, latent_ld, acc, o,
-                          lse, s);
+  return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, q, kv, kv_dtype, latent, latent_ld,
+                          acc, o, lse, s);
 }
 
 // Device metadata of one chunk, in this order (n = number of requests):
@@ -132,6 +146,7 @@ void build_chunk_meta(const mla_chunk_t &c, const int32_t *starts, const int32_t
 struct ChunkBuffers {
   void *latent_ws;
   void *kv_ws;
+  int kv_dtype;
 };
 
 int run_chunk(const mla_dims_t &d, const ChunkMetaHost &m, const int32_t *meta_dev, int T,
@@ -146,17 +161,18 @@ int run_chunk(const mla_dims_t &d, const ChunkMetaHost &m, const int32_t *meta_d
   int rc = launch_gather(kv_cache, num_blocks, d.block_size, LP * es, block_table, bt_stride,
                          n, req, st, cu, m.rows, b.latent_ws, status, s);
   if (rc) return rc;
-  rc = up_proj(d, b.latent_ws, LP, m.rows, w, b.kv_ws, s);
+  rc = up_proj(d, b.latent_ws, LP, m.rows, w, b.kv_ws, b.kv_dtype, s);
   if (rc) return rc;
-  return attention(d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.kv_ws,
+  return attention(d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.kv_ws, b.kv_dtype,
                    b.latent_ws, LP, acc, o, lse, s);
 }
 
 void carve_chunk_buffers(Carve &cv, const mla_dims_t &d, int64_t rows, ChunkBuffers &b) {
   const int es = elem_bytes(d.dtype);
   const int LP = d.kv_lora_rank + d.qk_rope_dim;
+  b.kv_dtype = path_kv_dtype(d);
   b.latent_ws = cv.take(size_t(rows) * LP * es);
-  b.kv_ws = cv.take(size_t(rows) * kv_width(d) * es);
+  b.kv_ws = cv.take(size_t(rows) * kv_width(d) * elem_bytes(b.kv_dtype));
 }
 
 int upload(void *dst, const std::vector<int32_t> &src, cudaStream_t s) {
@@ -211,26 +227,28 @@ extern "C" int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache
 }
 
 extern "C" int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
-                              int32_t rows, const void *w_kv_b, void *kv,
+                              int32_t rows, const void *w_kv_b, void *kv, int32_t kv_dtype,
                               mla_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
-  if (rows < 0 || latent_ld < d->kv_lora_rank) return MLA_ERR_INVALID;
+  if (rows < 0 || latent_ld < d->kv_lora_rank || !valid_kv_dtype(kv_dtype))
+    return MLA_ERR_INVALID;
   if (rows == 0) return MLA_OK;
   if (!latent || !w_kv_b || !kv) return MLA_ERR_INVALID;
-  return up_proj(*d, latent, latent_ld, rows, w_kv_b, kv, static_cast<cudaStream_t>(stream));
+  return up_proj(*d, latent, latent_ld, rows, w_kv_b, kv, kv_dtype,
+                 static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
                                const int32_t *q_loc, const int32_t *k_loc,
                                const int32_t *q_loc_host, const int32_t *k_loc_host,
                                int32_t num_tokens, const void *q, const void *kv,
-                               const void *latent, int64_t latent_ld,
+                               int32_t kv_dtype, const void *latent, int64_t latent_ld,
                                const int32_t *accumulate, float *o, float *lse,
                                mla_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
-  if (num_seqs < 0 || num_tokens < 0) return MLA_ERR_INVALID;
+  if (num_seqs < 0 || num_tokens < 0 || !valid_kv_dtype(kv_dtype)) return MLA_ERR_INVALID;
   if (num_seqs == 0) return MLA_OK;
   if (!q_loc || !k_loc || !q_loc_host || !k_loc_host || !q || !kv || !latent || !o || !lse)
     return MLA_ERR_INVALID;
@@ -242,7 +260,7 @@ extern "C" int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_
   }
   if (q_loc_host[0] < 0 || q_loc_host[num_seqs] > num_tokens) return MLA_ERR_INVALID;
   return attention(*d, causal ? 1 : 0, num_seqs, q_loc, k_loc, q_loc_host, k_loc_host,
-                   num_tokens, q, kv, latent, latent_ld, accumulate, o, lse,
+                   num_tokens, q, kv, kv_dtype, latent, latent_ld, accumulate, o, lse,
                    static_cast<cudaStream_t>(stream));
 }
 
@@ -268,6 +286,14 @@ extern "C" int mla_mask_empty_context(float *lse, void *o, int32_t dtype, int32_
   return launch_mask_empty_context(lse, o, dtype, num_tokens, num_heads, head_dim,
                                    num_requests, query_start_loc, context_start_loc,
                                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_chunk_kv_dtype(const mla_dims_t *d, int32_t *kv_dtype) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!kv_dtype) return MLA_ERR_INVALID;
+  *kv_dtype = path_kv_dtype(*d);
+  return MLA_OK;
 }
 
 extern "C" int mla_chunk_workspace_bytes(const mla_dims_t *d, int32_t max_rows,
@@ -382,7 +408,7 @@ size_t carve_prefill(void *base, const mla_dims_t &d, const PrefillLayout &p,
   const int es = elem_bytes(d.dtype);
   b.meta = static_cast<int32_t *>(cv.take(p.meta_total * sizeof(int32_t)));
   carve_chunk_buffers(cv, d, p.max_rows, b.chunk);
-  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * es);
+  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk.kv_dtype));
   const size_t o_bytes = size_t(p.T) * d.num_heads * d.v_dim * sizeof(float);
   const size_t l_bytes = size_t(p.T) * d.num_heads * sizeof(float);
   b.o_part = static_cast<float *>(cv.take(o_bytes));
@@ -464,14 +490,23 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                    dev_status, s);
     if (rc) return rc;
   }
-  rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, s);
+  rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, b.chunk.kv_dtype, s);
   if (rc) return rc;
   const int32_t *sq = b.meta + p.suffix_off;
   rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+                 b.chunk.kv_dtype, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
   if (rc) return rc;
   return launch_merge(out, out_lse, b.o_part, b.lse_part, b.o_suf, b.lse_suf, T, H, Dv, p.pnt,
                       MLA_DTYPE_F32, d->dtype, s);
 }
 
 extern "C" int mla_has_tcgen05(void) { return tc_available() ? 1 : 0; }
+
+extern "C" int mla_device_error_flags(int32_t *flags) {
+  if (!flags) return MLA_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+  const int a = gemm_take_errors(), b = attn_take_errors();
+  if (a < 0 || b < 0) return MLA_ERR_CUDA;
+  *flags = a | b;
+  return MLA_OK;
+}

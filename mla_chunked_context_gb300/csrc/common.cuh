@@ -1,6 +1,7 @@
 // Small device helpers shared by the CUDA kernels of this library.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -13,6 +14,7 @@ __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) {
   return __bfloat162float(x);
 }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 
 template <typename T>
 __device__ __forceinline__ T from_f32(float x);
@@ -23,6 +25,10 @@ __device__ __forceinline__ float from_f32<float>(float x) {
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) {
+  return __float2half_rn(x);
 }
 
 __device__ __forceinline__ bool is_neg_inf(float x) {
@@ -50,10 +56,15 @@ inline int launch_status() {
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-inline int elem_bytes(int32_t dtype) { return dtype == MLA_DTYPE_BF16 ? 2 : 4; }
+inline int elem_bytes(int32_t dtype) { return dtype == MLA_DTYPE_F32 ? 4 : 2; }
 
+// storage types of the inputs and of the final output
 inline bool valid_dtype(int32_t dtype) {
   return dtype == MLA_DTYPE_BF16 || dtype == MLA_DTYPE_F32;
+}
+// storage types of the up-projected K/V workspace
+inline bool valid_kv_dtype(int32_t dtype) {
+  return dtype == MLA_DTYPE_BF16 || dtype == MLA_DTYPE_F32 || dtype == MLA_DTYPE_F16;
 }
 
 inline int num_sms() {

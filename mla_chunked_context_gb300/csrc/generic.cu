@@ -72,7 +72,7 @@ struct AttnArgs {
   float scale_log2;  // softmax_scale * log2(e)
 };
 
-template <typename T>
+template <typename T, typename TK>
 __global__ void __launch_bounds__(128) attn_simt(AttnArgs a) {
   const int lane = threadIdx.x & 31;
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(128) attn_simt(AttnArgs a) {
   if (a.causal) nk = min(nk, t - a.q_loc[i] + 1);
   const int QK = a.Dn + a.P, W = a.H * (a.Dn + a.Dv);
   const T *q = static_cast<const T *>(a.q) + (int64_t(t) * a.H + h) * QK;
-  const T *kv = static_cast<const T *>(a.kv);
+  const TK *kv = static_cast<const TK *>(a.kv);
   const T *lat = static_cast<const T *>(a.latent);
   float qr[QK_PER_LANE], acc[V_PER_LANE];
 #pragma unroll
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(128) attn_simt(AttnArgs a) {
   float m = neg_inf(), l = 0.f;
   for (int j = 0; j < nk; ++j) {
     const int64_t row = kbeg + j;
-    const T *kn = kv + row * W + int64_t(h) * (a.Dn + a.Dv);
+    const TK *kn = kv + row * W + int64_t(h) * (a.Dn + a.Dv);
     const T *kp = lat + row * a.latent_ld + a.L;
     float s = 0.f;
 #pragma unroll
@@ -156,24 +156,45 @@ bool generic_dims_ok(const mla_dims_t &d) {
   return d.qk_nope_dim + d.qk_rope_dim <= 32 * QK_PER_LANE && d.v_dim <= 32 * V_PER_LANE;
 }
 
-int launch_up_proj_simt(int dtype, const void *latent, int64_t lda, int rows, const void *w,
-                        void *kv, int N, int K, cudaStream_t s) {
+template <typename T>
+int up_proj_simt_out(int kv_dtype, const T *latent, int64_t lda, int rows, const T *w, void *kv,
+                     int N, int K, dim3 grid, cudaStream_t s) {
+  if (kv_dtype == MLA_DTYPE_F32)
+    kv_up_proj_simt<T, float><<<grid, 256, 0, s>>>(latent, lda, w, static_cast<float *>(kv), rows,
+                                                   N, K);
+  else if (kv_dtype == MLA_DTYPE_F16)
+    kv_up_proj_simt<T, __half><<<grid, 256, 0, s>>>(latent, lda, w, static_cast<__half *>(kv),
+                                                    rows, N, K);
+  else
+    kv_up_proj_simt<T, __nv_bfloat16><<<grid, 256, 0, s>>>(
+        latent, lda, w, static_cast<__nv_bfloat16 *>(kv), rows, N, K);
+  return launch_status();
+}
+
+int launch_up_proj_simt(int dtype, int kv_dtype, const void *latent, int64_t lda, int rows,
+                        const void *w, void *kv, int N, int K, cudaStream_t s) {
   if (rows == 0) return MLA_OK;
   dim3 grid((N + GT - 1) / GT, (rows + GT - 1) / GT);
   if (dtype == MLA_DTYPE_BF16)
-    kv_up_proj_simt<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16 *>(latent), lda, static_cast<const __nv_bfloat16 *>(w),
-        static_cast<__nv_bfloat16 *>(kv), rows, N, K);
+    return up_proj_simt_out(kv_dtype, static_cast<const __nv_bfloat16 *>(latent), lda, rows,
+                            static_cast<const __nv_bfloat16 *>(w), kv, N, K, grid, s);
+  return up_proj_simt_out(kv_dtype, static_cast<const float *>(latent), lda, rows,
+                          static_cast<const float *>(w), kv, N, K, grid, s);
+}
+
+template <typename T>
+void attn_simt_kv(int kv_dtype, int blocks, const AttnArgs &a, cudaStream_t s) {
+  if (kv_dtype == MLA_DTYPE_F32)
+    attn_simt<T, float><<<blocks, 128, 0, s>>>(a);
+  else if (kv_dtype == MLA_DTYPE_F16)
+    attn_simt<T, __half><<<blocks, 128, 0, s>>>(a);
   else
-    kv_up_proj_simt<float, float><<<grid, 256, 0, s>>>(
-        static_cast<const float *>(latent), lda, static_cast<const float *>(w),
-        static_cast<float *>(kv), rows, N, K);
-  return launch_status();
+    attn_simt<T, __nv_bfloat16><<<blocks, 128, 0, s>>>(a);
 }
 
 int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                      const int32_t *k_loc, int num_q_rows, int T, const void *q,
-                     const void *kv, const void *latent, int64_t latent_ld,
+                     const void *kv, int kv_dtype, const void *latent, int64_t latent_ld,
                      const int32_t *accumulate, float *o, float *lse, cudaStream_t s) {
   if (num_q_rows == 0 || num_seqs == 0) return MLA_OK;
   AttnArgs a{q, kv, latent, latent_ld, o, lse, q_loc, k_loc, accumulate, num_seqs, T,
@@ -182,9 +203,9 @@ int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_
   const int64_t warps = int64_t(num_q_rows) * d.num_heads;
   const int blocks = int((warps * 32 + 127) / 128);
   if (d.dtype == MLA_DTYPE_BF16)
-    attn_simt<__nv_bfloat16><<<blocks, 128, 0, s>>>(a);
+    attn_simt_kv<__nv_bfloat16>(kv_dtype, blocks, a, s);
   else
-    attn_simt<float><<<blocks, 128, 0, s>>>(a);
+    attn_simt_kv<float>(kv_dtype, blocks, a, s);
   return launch_status();
 }
 

@@ -1,0 +1,450 @@
+// Varlen MLA attention on the 5th-generation tensor cores (sm_103a), for the
+// DeepSeek-V3 head shape: q/k = [nope 128 | rope 64] (192), v = 128.  q and
+// the latent (k_pe) are bf16; the up-projected K_nope and V are fp16.
+//
+// What it computes (PR #50613 report, item 4: a backend's
+// run_prefill_context_chunk over a ContextChunk returns (O, LSE) per query row
+// and head; item 3: the chunk result is accumulated into the context
+// partial): for each sequence i, query token t in [q_loc[i], q_loc[i+1]) and
+// head h, with keys j in [k_loc[i], k_loc[i+1]):
+//   s_j = scale * (q_nope . K_nope[j, h] + q_pe . k_pe[j])
+//   O   = sum_j softmax(s)_j V[j, h];   LSE = ln sum_j exp(s_j)
+// Context chunks see every key of their sequence; the causal (new-token)
+// mode lets query p see keys 0..p.  K_nope and V come from the up-projected
+// workspace kv [rows, H*256] (head h at columns h*256 + [0,128) / [128,256));
+// k_pe is the latent row's tail, latent[row][512:576], shared by all heads.
+//
+// One CTA = one (sequence, 128-query tile, head).  Warp-specialised:
+//   warp 0     TMA producer: the 128x192 Q tile once, then per 128-key tile
+//              K = [K_nope (2 boxes) | k_pe (1 box)] and V (2 boxes), into
+//              double-buffered slots, 128-byte swizzle.
+//   warp 1     TMEM owner + MMA issuer: S = Q K^T (M=128, N=128, K=192: 8
+//              fp16 tcgen05.mma for the nope part, 4 bf16 for the rope part,
+//              into a double-buffered S accumulator), and O += P V (M=128,
+//              N=128, K=128: 8 fp16 tcgen05.mma, P read from TMEM, V an
+//              MN-major shared-memory operand).
+//   warps 2-5  softmax, one thread per query row: tcgen05.ld the S row, mask,
+//              online softmax in base 2 with a lazily rescaled running max
+//              (O is rescaled in TMEM only when the max grows by more than
+//              2^8), P as fp16 written back to TMEM with tcgen05.st; at the
+//              end O/l and LSE go to global memory, or are LSE-merged into the
+//              stored partial (accumulate).
+// TMEM: S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512).
+#include <algorithm>
+#include <vector>
+
+#include "sm103.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm103;
+
+constexpr int BQ = 128, BKV = 128;
+constexpr int DN = 128, DR = 64, DV = 128, DQK = DN + DR, HD = DN + DV;
+constexpr int BOX_BYTES = 128 * 64 * 2;      // 16 KB: 128 rows x 64 bf16
+constexpr int Q_BYTES = 3 * BOX_BYTES;       // 48 KB
+constexpr int K_BYTES = 3 * BOX_BYTES;       // 48 KB
+constexpr int V_BYTES = 2 * BOX_BYTES;       // 32 KB
+constexpr int SMEM_BYTES = 1024 + Q_BYTES + 2 * K_BYTES + 2 * V_BYTES + 256;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
+constexpr int MAX_ITEMS = 2048;
+constexpr float kRescaleThreshold = 8.0f;    // log2 of the tolerated growth
+
+struct AttnParams {
+  int n_items, H, T, causal;
+  float scale_log2;
+  const int32_t *q_loc, *k_loc, *acc;
+  float *o, *lse;
+  int2 items[MAX_ITEMS];  // (sequence, query tile), longest first
+};
+
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_kv,
+                   const __grid_constant__ CUtensorMap tm_lat,
+                   const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sQ = smem;
+  uint8_t *sK = sQ + Q_BYTES;
+  uint8_t *sV = sK + 2 * K_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sV + 2 * V_BYTES);
+  const uint32_t b_q = smem_u32(bars + 0);
+  const uint32_t b_kfull = smem_u32(bars + 1), b_kempty = smem_u32(bars + 3);
+  const uint32_t b_vfull = smem_u32(bars + 5), b_vempty = smem_u32(bars + 7);
+  const uint32_t b_sfull = smem_u32(bars + 9), b_sfree = smem_u32(bars + 11);
+  const uint32_t b_pfull = smem_u32(bars + 13), b_odone = smem_u32(bars + 14);
+  const uint32_t b_done = smem_u32(bars + 15), b_qready = smem_u32(bars + 16);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x / p.n_items;
+  const int2 it = p.items[blockIdx.x - h * p.n_items];
+  const int seq = it.x, qt = it.y;
+  const int q_beg = __ldg(p.q_loc + seq), nq = __ldg(p.q_loc + seq + 1) - q_beg;
+  const int k_beg = __ldg(p.k_loc + seq), nk = __ldg(p.k_loc + seq + 1) - k_beg;
+  const int q0 = qt * BQ;  // first query of the tile, within the sequence
+  int n_tiles = (nk + BKV - 1) / BKV;
+  if (p.causal) n_tiles = min(n_tiles, qt + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(b_kfull + 8 * s, 1);
+      mbar_init(b_kempty + 8 * s, 1);
+      mbar_init(b_vfull + 8 * s, 1);
+      mbar_init(b_vempty + 8 * s, 1);
+      mbar_init(b_sfull + 8 * s, 1);
+      mbar_init(b_sfree + 8 * s, 4);
+    }
+    mbar_init(b_pfull, 4);
+    mbar_init(b_odone, 1);
+    mbar_init(b_done, 1);
+    mbar_init(b_qready, 4);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0 && n_tiles > 0) {
+      // ---------------- TMA producer
+      prefetch_map(&tm_q);
+      prefetch_map(&tm_kv);
+      prefetch_map(&tm_lat);
+      const int qrow = q_beg + q0;
+      mbar_expect_tx(b_q, Q_BYTES);
+      tma_load_2d(smem_u32(sQ), &tm_q, b_q, h * DQK, qrow);
+      tma_load_2d(smem_u32(sQ + BOX_BYTES), &tm_q, b_q, h * DQK + 64, qrow);
+      tma_load_2d(smem_u32(sQ + 2 * BOX_BYTES), &tm_q, b_q, h * DQK + 128, qrow);
+      int k_issued[2] = {-1, -1}, v_issued[2] = {-1, -1};
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j & 1;
+        const uint32_t par = uint32_t(((j >> 1) - 1) & 1);  // phase of tile j-2
+        const int krow = k_beg + j * BKV;
+        if (j >= 2 && !mbar_wait(b_kempty + 8 * s, par)) break;
+        uint8_t *k = sK + s * K_BYTES;
+        mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
+        tma_load_2d(smem_u32(k), &tm_kv, b_kfull + 8 * s, h * HD, krow);
+        tma_load_2d(smem_u32(k + BOX_BYTES), &tm_kv, b_kfull + 8 * s, h * HD + 64, krow);
+        tma_load_2d(smem_u32(k + 2 * BOX_BYTES), &tm_lat, b_kfull + 8 * s, 512, krow);
+        k_issued[s] = (j >> 1) & 1;
+        if (j >= 2 && !mbar_wait(b_vempty + 8 * s, par)) break;
+        uint8_t *v = sV + s * V_BYTES;
+        mbar_expect_tx(b_vfull + 8 * s, V_BYTES);
+        tma_load_2d(smem_u32(v), &tm_kv, b_vfull + 8 * s, h * HD + DN, krow);
+        tma_load_2d(smem_u32(v + BOX_BYTES), &tm_kv, b_vfull + 8 * s, h * HD + DN + 64, krow);
+        v_issued[s] = (j >> 1) & 1;
+      }
+      // every issued load has landed before the CTA may exit
+      mbar_wait(b_q, 0);
+      for (int s = 0; s < 2; ++s) {
+        if (k_issued[s] >= 0) mbar_wait(b_kfull + 8 * s, uint32_t(k_issued[s]));
+        if (v_issued[s] >= 0) mbar_wait(b_vfull + 8 * s, uint32_t(v_issued[s]));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_tiles > 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc_nope = idesc_f16kind(BQ, BKV, false, false, false);  // fp16
+      constexpr uint32_t idesc_rope = idesc_f16kind(BQ, BKV, false, false, true);   // bf16
+      constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
+      const uint32_t q_addr = smem_u32(sQ);
+      bool ok = mbar_wait(b_qready, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!mbar_wait(b_kfull + 8 * s, uint32_t((j >> 1) & 1))) return false;
+        if (j >= 2 && !mbar_wait(b_sfree + 8 * s, uint32_t(((j >> 1) - 1) & 1))) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + s * K_BYTES);
+        const uint32_t d = tmem + COL_S + uint32_t(s * BKV);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint32_t off = uint32_t((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
+          mma_bf16(d, desc_kmajor_sw128(q_addr + off), desc_kmajor_sw128(k_addr + off),
+                   kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
+        }
+        mma_commit(b_sfull + 8 * s);
+        mma_commit(b_kempty + 8 * s);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_tiles > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(b_pfull, uint32_t(j & 1)) ||
+            !mbar_wait(b_vfull + 8 * s, uint32_t((j >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + s * V_BYTES);
+        const uint32_t pa = tmem + COL_P + uint32_t(s * 64);
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          mma_bf16_ts(tmem + COL_O, pa + uint32_t(kk * 8),
+                      desc_mnmajor_sw128(v_addr + uint32_t(kk * 2048), BOX_BYTES), idesc_o,
+                      (j | kk) != 0);
+        mma_commit(b_odone);
+        mma_commit(b_vempty + 8 * s);
+        if (j + 2 < n_tiles) ok = issue_s(j + 2);
+      }
+      mma_commit(b_done);
+      mbar_wait(b_done, 0);
+    }
+  } else {
+    // ---------------- softmax: one thread per query row
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const int qpos = q0 + row;            // position within the sequence
+    float m_used = neg_inf(), l = 0.f;
+    bool ok = true;
+    if (n_tiles > 0) {
+      // q_nope (boxes 0 and 1 of the Q tile) to fp16 in place, to meet the
+      // fp16 K_nope in the S MMA; exact for bf16 values within fp16 range
+      if (!mbar_wait(b_q, 0)) {
+        ok = false;
+      } else {
+        const int tid = threadIdx.x - 64;
+        uint4 *qv = reinterpret_cast<uint4 *>(sQ);
+#pragma unroll 4
+        for (int v = 0; v < 2 * BOX_BYTES / 16 / 128; ++v) {
+          uint4 x = qv[v * 128 + tid];
+          uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_f16(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+          qv[v * 128 + tid] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qready);
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait(b_sfull + 8 * s, uint32_t((j >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[BKV];
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + COL_S + uint32_t(s * BKV + c * 32), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(r[e]) * p.scale_log2;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_sfree + 8 * s);
+      // mask keys past the sequence (and, causal, past the query)
+      int valid = nk - j * BKV;
+      if (p.causal) valid = min(valid, qpos - j * BKV + 1);
+      if (valid < BKV) {
+#pragma unroll
+        for (int e = 0; e < BKV; ++e)
+          if (e >= valid) sv[e] = neg_inf();
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int e = 1; e < BKV; ++e) mx = fmaxf(mx, sv[e]);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mx > m_used + kRescaleThreshold || j == 0) {
+        const float m_new = fmaxf(mx, m_used);
+        if (j > 0 && m_new != neg_inf()) {
+          alpha = exp2f(m_used - m_new);
+          rescale = true;
+        }
+        m_used = m_new;
+      }
+      const float base = (m_used == neg_inf()) ? 0.f : m_used;
+      l *= alpha;
+      uint32_t pk[BKV / 2];
+#pragma unroll
+      for (int e = 0; e < BKV / 2; ++e) {
+        const float a = exp2f(sv[2 * e] - base), b = exp2f(sv[2 * e + 1] - base);
+        l += a + b;
+        pk[e] = pack_f16(a, b);
+      }
+      // O and this P buffer are free once the previous P.V has finished
+      if (j > 0 && !mbar_wait(b_odone, uint32_t((j - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t pcol = tmem + lane_off + COL_P + uint32_t(s * 64);
+      tmem_st32(pcol, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st32(pcol + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t r[32];
+          const uint32_t oc = tmem + lane_off + COL_O + uint32_t(c * 32);
+          tmem_ld32(oc, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(oc, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_pfull);
+    }
+    // ---------------- epilogue
+    const bool store = ok && qpos < nq;
+    if (ok && n_tiles > 0 && !mbar_wait(b_odone, uint32_t((n_tiles - 1) & 1))) ok = false;
+    tc_fence_after();
+    const int t = q_beg + qpos;
+    const bool accumulate = p.acc != nullptr && __ldg(p.acc + seq) != 0;
+    float lse = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : neg_inf();
+    float w_new = (l > 0.f) ? 1.f / l : 0.f, w_old = 0.f;
+    const int64_t li = int64_t(h) * p.T + t;
+    float *orow = p.o + (int64_t(t) * p.H + h) * DV;
+    bool write = store;
+    if (store && accumulate) {
+      const float old = p.lse[li];
+      if (l == 0.f) {
+        write = false;  // nothing new: keep the stored partial
+      } else if (!is_neg_inf(old)) {
+        const float mx = fmaxf(old, lse);
+        const float eo = expf(old - mx), en = expf(lse - mx);
+        w_old = eo / (eo + en);
+        w_new *= en / (eo + en);
+        lse = mx + logf(eo + en);
+      }
+    }
+    if (ok && n_tiles > 0) {
+#pragma unroll 1
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + COL_O + uint32_t(c * 32), r);
+        tmem_wait_ld();
+        if (write) {
+          float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 v = make_float4(__uint_as_float(r[4 * e]) * w_new,
+                                   __uint_as_float(r[4 * e + 1]) * w_new,
+                                   __uint_as_float(r[4 * e + 2]) * w_new,
+                                   __uint_as_float(r[4 * e + 3]) * w_new);
+            if (w_old != 0.f) {
+              const float4 o = dst[e];
+              v.x += w_old * o.x;
+              v.y += w_old * o.y;
+              v.z += w_old * o.z;
+              v.w += w_old * o.w;
+            }
+            dst[e] = v;
+          }
+        }
+      }
+    } else if (write && n_tiles == 0 && !accumulate) {
+      for (int c = 0; c < DV; c += 4)
+        *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (write && (ok || n_tiles == 0)) p.lse[li] = lse;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+bool tc_attn_ok(const mla_dims_t &d, int kv_dtype, int64_t latent_ld) {
+  return d.dtype == MLA_DTYPE_BF16 && kv_dtype == MLA_DTYPE_F16 && d.qk_nope_dim == DN &&
+         d.qk_rope_dim == DR &&
+         d.v_dim == DV && d.kv_lora_rank == 512 && (latent_ld * 2) % 16 == 0 &&
+         latent_ld >= 576;
+}
+
+int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
+                   const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                   int T, const void *q, const void *kv, const void *latent, int64_t latent_ld,
+                   const int32_t *accumulate, float *o, float *lse, cudaStream_t s) {
+  auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+  if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
+  const int H = d.num_heads;
+  const int rows = k_loc_host[num_seqs];
+  CUtensorMap tq, tkv, tlat;
+  if (!make_tmap_2d_16(&tq, false, q, uint64_t(H) * DQK, uint64_t(T), uint64_t(H) * DQK * 2, 64,
+                       128, true) ||
+      !make_tmap_2d_16(&tkv, true, kv, uint64_t(H) * HD, uint64_t(rows > 0 ? rows : 1),
+                       uint64_t(H) * HD * 2, 64, 128, true) ||
+      !make_tmap_2d_16(&tlat, false, latent, 576, uint64_t(rows > 0 ? rows : 1),
+                       uint64_t(latent_ld) * 2, 64, 128, true))
+    return MLA_ERR_CUDA;
+  // work items: (sequence, query tile), the ones with the most key tiles first
+  struct Item {
+    int seq, qt, cost;
+  };
+  std::vector<Item> items;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int nq = q_loc_host[i + 1] - q_loc_host[i];
+    const int nk = k_loc_host[i + 1] - k_loc_host[i];
+    for (int qt = 0; qt * BQ < nq; ++qt) {
+      int tiles = (nk + BKV - 1) / BKV;
+      if (causal) tiles = std::min(tiles, qt + 1);
+      items.push_back({i, qt, tiles});
+    }
+  }
+  std::stable_sort(items.begin(), items.end(),
+                   [](const Item &a, const Item &b) { return a.cost > b.cost; });
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    attr_set = true;
+  }
+  static AttnParams prm;  // large; filled per launch batch
+  for (size_t b = 0; b < items.size(); b += MAX_ITEMS) {
+    const int n = int(std::min<size_t>(MAX_ITEMS, items.size() - b));
+    prm.n_items = n;
+    prm.H = H;
+    prm.T = T;
+    prm.causal = causal;
+    prm.scale_log2 = d.softmax_scale * 1.4426950408889634f;
+    prm.q_loc = q_loc;
+    prm.k_loc = k_loc;
+    prm.acc = accumulate;
+    prm.o = o;
+    prm.lse = lse;
+    for (int k = 0; k < n; ++k) prm.items[k] = make_int2(items[b + k].seq, items[b + k].qt);
+    attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES, s>>>(tq, tkv, tlat, prm);
+    const int rc = launch_status();
+    if (rc) return rc;
+  }
+  return MLA_OK;
+}
+
+int attn_take_errors() { return sm103::take_error_flags_here(); }
+
+}  // namespace mla

@@ -1,11 +1,308 @@
-// placeholder, replaced by the tcgen05 GEMM
-#include "common.cuh"
+// W_kv_b up-projection on the 5th-generation tensor cores (sm_103a):
+//   kv[M, N] = latent[M, 0:K] . w_kv_b[N, K]^T      (bf16 in, f32 accumulate,
+//                                                    fp16/bf16 out)
+// M = context rows of a chunk (or new tokens), K = kv_lora_rank, N = H*(Dn+Dv).
+// The MLA up-projection is not on the pages; it is the standard MLA prefill
+// step that turns the gathered latent rows into per-head K_nope and V.
+//
+// Design: persistent, warp-specialised, one CTA per SM.
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage
+//               (128-byte swizzle), 4-stage mbarrier ring.
+//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
+//               (M=128, N=256, K=16; 4 per stage) into one of two 256-column
+//               f32 accumulators and commits stage / accumulator barriers.
+//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns, round to fp16 (or
+//               bf16),
+//               write a 32x64 tile into a swizzled staging buffer, TMA store.
+// The two accumulators let the epilogue of tile i overlap the MMAs of tile
+// i+1.  Tiles are visited m-major with n fastest, so a 128-row slice of the
+// latent and the whole weight stay in L2 while 152 CTAs sweep them.
+#include <cstdio>
+
+#include "sm103.cuh"
+
 namespace mla {
-bool tc_available() { return false; }
-bool tc_gemm_ok(const mla_dims_t &, int64_t, const void *, const void *, const void *) { return false; }
-int launch_up_proj_tc(const mla_dims_t &, const void *, int64_t, int, const void *, void *, cudaStream_t) { return MLA_ERR_UNSUPPORTED; }
-bool tc_attn_ok(const mla_dims_t &, int64_t) { return false; }
-int launch_attn_tc(const mla_dims_t &, int, int, const int32_t *, const int32_t *, const int32_t *,
-                   const int32_t *, int, const void *, const void *, const void *, int64_t,
-                   const int32_t *, float *, float *, cudaStream_t) { return MLA_ERR_UNSUPPORTED; }
+namespace sm103 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 4;
+constexpr int STG_BYTES = 32 * 64 * 2;        // one warp's 32x64 bf16 staging tile
+constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES +
+                           EPI_WARPS * 2 * STG_BYTES + 256 /*barriers*/;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct GemmArgs {
+  int M, N, K;
+  int num_m, num_n;
+};
+
+template <bool kF16Out>
+__global__ void __launch_bounds__(THREADS, 1)
+    up_proj_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
+                      const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_c, GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_BYTES;
+  uint8_t *sStage = smem + STAGES * STAGE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + EPI_WARPS * 2 * STG_BYTES);
+  // bars: full[S], empty[S], acc_full[2], acc_empty[2], mma_done; then the
+  // TMEM base address slot
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = g.num_m * g.num_n;
+  const int kblocks = g.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf0 + 8 * a, 1);
+      mbar_init(acce0 + 8 * a, EPI_WARPS);
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init();
+    prefetch_map(&tm_a);
+    prefetch_map(&tm_b);
+    prefetch_map(&tm_c);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued_parity[STAGES];
+    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const int m0 = (t / g.num_n) * BM, n0 = (t % g.num_n) * BN;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + 8 * stage;
+        mbar_expect_tx(fb, STAGE_BYTES);
+        tma_load_2d(smem_u32(sA + stage * A_BYTES), &tm_a, fb, kb * BK, m0);
+        tma_load_2d(smem_u32(sB + stage * B_BYTES), &tm_b, fb, kb * BK, n0);
+        issued_parity[stage] = int(phase);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // every load this thread issued has landed before the CTA may exit
+    for (int s = 0; s < STAGES; ++s)
+      if (issued_parity[s] >= 0) mbar_wait(full0 + 8 * s, uint32_t(issued_parity[s]));
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = idesc_f16kind(BM, BN, false, false, true);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(full0 + 8 * stage, phase)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
+                   desc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+        mma_commit(empty0 + 8 * stage);  // stage free once these MMAs finish
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      mma_commit(accf0 + 8 * acc);  // accumulator complete
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    // every MMA this thread issued has completed before TMEM is released
+    mma_commit(done_bar);
+    mbar_wait(done_bar, 0);
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> bf16 -> smem -> TMA store
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    uint8_t *stg = sStage + (warp - 2) * 2 * STG_BYTES;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int buf = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const int m0 = (t / g.num_n) * BM, n0 = (t % g.num_n) * BN;
+      if (!mbar_wait(accf0 + 8 * acc, acc_phase)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int j = 0; j < BN / 64; ++j) {
+        uint32_t lo[32], hi[32];
+        tmem_ld32(t_row + j * 64, lo);
+        tmem_ld32(t_row + j * 64 + 32, hi);
+        tmem_wait_ld();
+        // the staging buffer is reused every other chunk: its previous TMA
+        // store must have finished reading it
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t *row = stg + buf * STG_BYTES + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t *src = (c < 4) ? lo + 8 * c : hi + 8 * (c - 4);
+          uint4 v;
+          if (kF16Out) {
+            v.x = pack_f16(__uint_as_float(src[0]), __uint_as_float(src[1]));
+            v.y = pack_f16(__uint_as_float(src[2]), __uint_as_float(src[3]));
+            v.z = pack_f16(__uint_as_float(src[4]), __uint_as_float(src[5]));
+            v.w = pack_f16(__uint_as_float(src[6]), __uint_as_float(src[7]));
+          } else {
+            v.x = pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1]));
+            v.y = pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3]));
+            v.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
+            v.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
+          }
+          *reinterpret_cast<uint4 *>(row + ((c ^ (lane & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_c, smem_u32(stg + buf * STG_BYTES), n0 + j * 64, m0 + quarter * 32);
+          bulk_commit();
+        }
+        buf ^= 1;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
 }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+}  // namespace sm103
+
+bool make_tmap_2d_16(CUtensorMap *map, bool fp16, const void *base, uint64_t dim0, uint64_t dim1,
+                     uint64_t row_stride_bytes, uint32_t box0, uint32_t box1, bool swizzle128) {
+  auto fn = sm103::encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool tc_available() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return major == 10 && minor == 3 && sm103::encode_fn() != nullptr;
+}
+
+bool tc_gemm_ok(const mla_dims_t &d, int kv_dtype, int64_t lda, const void *latent,
+                const void *w, const void *kv) {
+  const int N = d.num_heads * (d.qk_nope_dim + d.v_dim);
+  auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  return d.dtype == MLA_DTYPE_BF16 && (kv_dtype == MLA_DTYPE_F16 || kv_dtype == MLA_DTYPE_BF16) &&
+         d.kv_lora_rank % sm103::BK == 0 && N % sm103::BN == 0 && (lda * 2) % 16 == 0 &&
+         al16(latent) && al16(w) && al16(kv);
+}
+
+int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int64_t lda,
+                      int rows, const void *w, void *kv, cudaStream_t s) {
+  using namespace sm103;
+  const int K = d.kv_lora_rank;
+  const int N = d.num_heads * (d.qk_nope_dim + d.v_dim);
+  CUtensorMap ta, tb, tc;
+  const bool f16 = kv_dtype == MLA_DTYPE_F16;
+  if (!make_tmap_2d_16(&ta, false, latent, K, rows, uint64_t(lda) * 2, BK, BM, true) ||
+      !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN, true) ||
+      !make_tmap_2d_16(&tc, f16, kv, N, rows, uint64_t(N) * 2, 64, 32, true))
+    return MLA_ERR_CUDA;
+  GemmArgs g{rows, N, K, (rows + BM - 1) / BM, N / BN};
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(up_proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(up_proj_tc_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    attr_set = true;
+  }
+  const int tiles = g.num_m * g.num_n;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  if (f16)
+    up_proj_tc_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, tc, g);
+  else
+    up_proj_tc_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, tc, g);
+  return launch_status();
+}
+
+}  // namespace mla
+
+namespace mla {
+int gemm_take_errors() { return sm103::take_error_flags_here(); }
+}  // namespace mla

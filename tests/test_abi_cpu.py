@@ -118,7 +118,8 @@ def test_workspace_queries():
                                       w.max_context_chunk, w.split_alignment)
     T, H = w.num_tokens, w.num_heads
     rows = 65536
-    lower = rows * 576 * 2 + rows * H * 256 * 2 + T * H * 256 * 2 + 2 * T * H * 128 * 4
+    kv_es = M.mla_chunk_kv_dtype(dims).itemsize
+    lower = rows * 576 * 2 + rows * H * 256 * kv_es + T * H * 256 * kv_es + 2 * T * H * 128 * 4
     assert lower <= b <= lower + 64 * 1024 * 1024
     cb = M.mla_chunk_workspace_bytes(dims, 1000, 10)
     assert cb >= 1000 * 576 * 2 + 1000 * H * 256 * 2
@@ -133,10 +134,13 @@ def test_argument_errors_before_any_launch():
         _lib.MLA_ERR_INVALID
     assert L.merge_attn_states(None, None, None, None, None, None, 4, 2, 12, 0, 1, 1, None) == \
         _lib.MLA_ERR_INVALID          # head_dim not a multiple of 8
-    assert L.mla_kv_up_proj(C.byref(d), None, 80, 5, None, None, None) == _lib.MLA_ERR_INVALID
+    assert L.mla_kv_up_proj(C.byref(d), None, 80, 5, None, None, 0, None) == \
+        _lib.MLA_ERR_INVALID
+    assert L.mla_kv_up_proj(C.byref(d), None, 80, 5, None, None, 7, None) == \
+        _lib.MLA_ERR_INVALID          # unknown K/V dtype
     bad = _lib.Dims.of(w)
     bad.v_dim = 12
-    assert L.mla_kv_up_proj(C.byref(bad.c()), None, 80, 5, None, None, None) == \
+    assert L.mla_kv_up_proj(C.byref(bad.c()), None, 80, 5, None, None, 0, None) == \
         _lib.MLA_ERR_UNSUPPORTED
     ctx, ql = _lib._i32_host(w.context_lens), _lib._i32_host(w.query_lens)
     rc = L.mla_chunked_prefill(C.byref(d), ctx, ql, 4, w.row_budget, w.max_context_chunk,

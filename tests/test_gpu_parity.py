@@ -36,6 +36,12 @@ def _cuda():
     torch.cuda.set_device(0)
 
 
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    yield
+    assert M.mla_device_error_flags() == 0, "a tensor-core kernel gave up waiting"
+
+
 def f64(t):
     return t.detach().to("cpu").double().numpy()
 
@@ -235,18 +241,24 @@ def test_gather_bad_block_sets_status():
 
 
 # ----------------------------------------------------------- up-projection --
+# one rounding of the f32 accumulation to the output type, plus f32 ordering
+UP_TOL = {torch.bfloat16: (2e-3, 8e-3), torch.float16: (1e-4, 1.5e-3),
+          torch.float32: (1e-4, 1e-4)}
+
+
+@pytest.mark.parametrize("kv_dtype", [torch.float16, torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("rows,heads", [(300, 8), (128, 2), (1, 2), (4099, 16)])
-def test_up_proj_deepseek(rows, heads):
+def test_up_proj_deepseek(rows, heads, kv_dtype):
     w = W.scaled(W.workload("uniform"), num_heads=heads, seed=41)
     gen = torch.Generator().manual_seed(rows)
     lat = torch.randn(rows, w.latent_dim, generator=gen).to(torch.bfloat16)
     wkv = (torch.randn(heads * 256, 512, generator=gen) * 0.02).to(torch.bfloat16)
-    kv = torch.full((rows, heads * 256), float("nan"), dtype=torch.bfloat16, device=DEV)
+    kv = torch.full((rows, heads * 256), float("nan"), dtype=kv_dtype, device=DEV)
     M.mla_kv_up_proj(M.Dims.of(w), lat.to(DEV), rows, wkv.to(DEV), kv)
     torch.cuda.synchronize()
     kn, v = O.up_project(f64(lat), f64(wkv), odims(w))
     ref = np.concatenate([kn, v], axis=2).reshape(rows, heads * 256)
-    assert_close(f64(kv), ref, 2e-3, 8e-3, what="kv")
+    assert_close(f64(kv), ref, *UP_TOL[kv_dtype], what="kv")
 
 
 def test_up_proj_fp32_tiny():
@@ -262,12 +274,12 @@ def test_up_proj_fp32_tiny():
 
 
 # -------------------------------------------------------------- attention --
-def _attn_inputs(w, n_rows, T, seed):
+def _attn_inputs(w, n_rows, T, seed, kv_dtype=None):
     gen = torch.Generator().manual_seed(seed)
     H = w.num_heads
     q = torch.randn(T, H, w.qk_dim, generator=gen).to(w.torch_dtype)
     kv = (0.45 * torch.randn(n_rows, H * (w.qk_nope_dim + w.v_dim), generator=gen)).to(
-        w.torch_dtype)
+        kv_dtype or w.torch_dtype)
     lat = torch.randn(n_rows, w.latent_dim, generator=gen).to(w.torch_dtype)
     return q, kv, lat
 
@@ -289,10 +301,13 @@ def _oracle_attn(w, q, kv, lat, q_loc, k_loc, causal):
     return o, lse
 
 
-@pytest.mark.parametrize("kind", ["deepseek", "tiny"])
+@pytest.mark.parametrize("kind", ["deepseek", "deepseek_bf16kv", "tiny"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_varlen_attention(kind, causal):
-    if kind == "deepseek":
+    """deepseek: fp16 K/V (the tcgen05 kernel on GB300); deepseek_bf16kv: the
+    CUDA-core kernel on the same shapes; tiny: float32 storage."""
+    kv_dtype = {"deepseek": torch.float16, "deepseek_bf16kv": torch.bfloat16}.get(kind)
+    if kind != "tiny":
         w = W.scaled(W.workload("uniform"), num_heads=4, seed=42)
         if causal:
             ql = [1, 130, 77, 256, 129]
@@ -306,7 +321,7 @@ def test_varlen_attention(kind, causal):
         kl = ql if causal else [64, 128, 37]
     q_loc = [0] + list(np.cumsum(ql))
     k_loc = [0] + list(np.cumsum(kl))
-    q, kv, lat = _attn_inputs(w, k_loc[-1], q_loc[-1], 7)
+    q, kv, lat = _attn_inputs(w, k_loc[-1], q_loc[-1], 7, kv_dtype)
     o = torch.full((q_loc[-1], w.num_heads, w.v_dim), float("nan"), device=DEV)
     lse = torch.full((w.num_heads, q_loc[-1]), float("nan"), device=DEV)
     M.mla_varlen_attn(M.Dims.of(w), causal, q_loc, k_loc, q.to(DEV), kv.to(DEV), lat.to(DEV),
@@ -324,7 +339,7 @@ def test_varlen_attention_accumulate():
     ql = [7, 140]
     k1, k2 = [100, 260], [60, 131]
     q_loc = [0] + list(np.cumsum(ql))
-    q, kv, lat = _attn_inputs(w, sum(k1) + sum(k2), q_loc[-1], 8)
+    q, kv, lat = _attn_inputs(w, sum(k1) + sum(k2), q_loc[-1], 8, torch.float16)
     # key rows: chunk-1 rows of both requests, then chunk-2 rows of both
     loc1 = [0, k1[0], k1[0] + k1[1]]
     loc2 = [loc1[-1], loc1[-1] + k2[0], loc1[-1] + k2[0] + k2[1]]
@@ -415,7 +430,7 @@ def test_chunk_entry_composes_to_prefill():
     for c in chunks:
         M.mla_context_chunk_attn(d, c, qsl, g["q"], g["kv_cache"], g["block_table"],
                                  g["w_kv_b"], ws, op, lp)
-    kvs = torch.empty(T, H * 256, dtype=torch.bfloat16, device=DEV)
+    kvs = torch.empty(T, H * 256, dtype=M.mla_chunk_kv_dtype(d), device=DEV)
     M.mla_kv_up_proj(d, g["new_latent"], T, g["w_kv_b"], kvs)
     os_ = torch.empty(T, H, 128, device=DEV)
     ls = torch.empty(H, T, device=DEV)
