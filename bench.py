@@ -306,9 +306,10 @@ def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
     for q in w.query_lens:
         qsl.append(qsl[-1] + q)
     max_rows = max([sum(p.seq_lens) for p in plans] + [1])
+    kv_dtype = M.mla_chunk_kv_dtype(dims)          # what mla_chunked_prefill uses
     lat_ws = torch.empty(max_rows, w.latent_dim, dtype=w.torch_dtype, device=dev)
-    kv_ws = torch.empty(max_rows, H * (w.qk_nope_dim + w.v_dim), dtype=w.torch_dtype, device=dev)
-    kv_new = torch.empty(T, H * (w.qk_nope_dim + w.v_dim), dtype=w.torch_dtype, device=dev)
+    kv_ws = torch.empty(max_rows, H * (w.qk_nope_dim + w.v_dim), dtype=kv_dtype, device=dev)
+    kv_new = torch.empty(T, H * (w.qk_nope_dim + w.v_dim), dtype=kv_dtype, device=dev)
     o_p = torch.zeros(T, H, w.v_dim, device=dev)
     l_p = torch.zeros(H, T, device=dev)
     o_s = torch.empty(T, H, w.v_dim, device=dev)
@@ -463,6 +464,86 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_kernel_case(args, dev):
+    """One kernel alone on a small DeepSeek-shaped case (for ncu captures and
+    quick timing): up_proj, attn (context or causal), merge or gather."""
+    import mla_chunked_context_gb300 as M
+    from mla_chunked_context_gb300 import workloads as W
+    peaks = load_peaks()
+    w = W.scaled(W.workload("uniform"), num_heads=args.heads)
+    dims = M.Dims.of(w)
+    H = args.heads
+    kvd = M.mla_chunk_kv_dtype(dims)
+    torch.manual_seed(5)
+    bf = torch.bfloat16
+    info = {}
+    if args.kernel == "up_proj":
+        rows = args.rows
+        lat = torch.randn(rows, 576, device=dev).to(bf)
+        wkv = (torch.randn(H * 256, 512, device=dev) * 0.02).to(bf)
+        kv = torch.empty(rows, H * 256, dtype=kvd, device=dev)
+        fn = lambda: M.mla_kv_up_proj(dims, lat, rows, wkv, kv)  # noqa: E731
+        work, unit, peak = 2.0 * rows * 512 * H * 256, "TFLOP/s", peaks["bf16_tflops"]
+        info = {"rows": rows, "N": H * 256, "K": 512,
+                "bytes": rows * 576 * 2 + H * 256 * 512 * 2 + rows * H * 256 * kv.element_size()}
+    elif args.kernel == "attn":
+        n, ql, kl = args.seqs, args.qlen, (args.qlen if args.causal else args.klen)
+        q = torch.randn(n * ql, H, 192, device=dev).to(bf)
+        kv = (0.45 * torch.randn(n * kl, H * 256, device=dev)).to(kvd)
+        lat = torch.randn(n * kl, 576, device=dev).to(bf)
+        o = torch.empty(n * ql, H, 128, device=dev)
+        lse = torch.empty(H, n * ql, device=dev)
+        q_loc = [i * ql for i in range(n + 1)]
+        k_loc = [i * kl for i in range(n + 1)]
+        fn = lambda: M.mla_varlen_attn(dims, args.causal, q_loc, k_loc, q, kv, lat, o, lse)  # noqa
+        pairs = n * (ql * (ql + 1) / 2 if args.causal else ql * kl)
+        work, unit, peak = 2.0 * H * (192 + 128) * pairs, "TFLOP/s", peaks["bf16_tflops"]
+        info = {"seqs": n, "q": ql, "k": kl, "causal": bool(args.causal)}
+    elif args.kernel == "merge":
+        m = W.MergeWorkload()
+        x = W.make_merge_inputs(m, poison=True)
+        g = {k: v.to(dev) for k, v in x.items() if torch.is_tensor(v)}
+        out = torch.empty_like(g["suffix_o"])
+        out_lse = torch.empty_like(g["suffix_lse"])
+        fn = lambda: M.merge_attn_states(out, out_lse, g["prefix_o"], g["prefix_lse"],  # noqa
+                                         g["suffix_o"], g["suffix_lse"], m.prefix_num_tokens)
+        need, _ = merge_bytes(x, m.num_tokens, m.num_heads, m.head_dim)
+        work, unit, peak = float(need), "GB/s", peaks["hbm_gbs"]
+    elif args.kernel == "gather":
+        wl = W.workload("hetero")
+        x = W.make_inputs(wl)
+        cache, bt = x["kv_cache"].to(dev), x["block_table"].to(dev)
+        rows = 32768
+        req = torch.tensor([int(np.argmax(wl.context_lens))], dtype=torch.int32, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        cu = torch.tensor([0, rows], dtype=torch.int32, device=dev)
+        ws = torch.empty(rows, 576, dtype=bf, device=dev)
+        fn = lambda: M.mla_gather_context_rows(M.Dims.of(wl), cache, bt, req, st, cu, rows, ws)  # noqa
+        work, unit, peak = 2.0 * rows * 576 * 2, "GB/s", peaks["hbm_gbs"]
+    else:
+        raise SystemExit(f"unknown kernel {args.kernel}")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.launches):
+        flush.fill_(3)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    med = statistics.median(ms)
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    ach = work / (med / 1e3) / scale
+    print(json.dumps({"kernel": args.kernel, "us": med * 1e3, "achieved": ach, "unit": unit,
+                      "peak": peak, "frac": ach / peak, "heads": H, **info,
+                      "errors": M.mla_device_error_flags()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,7 +553,21 @@ def main():
     ap.add_argument("--workload", default="hetero", choices=["hetero", "uniform", "long"])
     ap.add_argument("--cpu-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default=None,
+                    choices=["up_proj", "attn", "merge", "gather"],
+                    help="time one kernel alone on a small case instead of the full step")
+    ap.add_argument("--heads", type=int, default=128)
+    ap.add_argument("--rows", type=int, default=8192)
+    ap.add_argument("--seqs", type=int, default=4)
+    ap.add_argument("--qlen", type=int, default=256)
+    ap.add_argument("--klen", type=int, default=4096)
+    ap.add_argument("--causal", type=int, default=0)
+    ap.add_argument("--launches", type=int, default=10)
     args = ap.parse_args()
+    if args.kernel:
+        torch.cuda.set_device(0)
+        run_kernel_case(args, torch.device("cuda", 0))
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
