@@ -275,6 +275,35 @@ int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *chunk,
                            float *o_partial, float *lse_partial,
                            int32_t *dev_status, mla_stream_t stream);
 
+/* mla_context_chunk_attn_noalloc: mla_context_chunk_attn without a caller
+ *   workspace.  (No counterpart in the paper; it serves callers that cannot
+ *   allocate device memory themselves, e.g. a plugin whose host framework
+ *   owns every device allocation and hands it no workspace, or a path where a
+ *   cudaMalloc, which can synchronise the device, is not allowed.)
+ *   The scratch is a library-owned device array of MLA_NOALLOC_SCRATCH_BYTES
+ *   (64 MiB) that every GPU which loads the library holds until the process
+ *   exits.  The call allocates nothing.  A chunk whose workspace
+ *   (mla_chunk_workspace_bytes for its rows and requests) exceeds that size
+ *   is rejected with MLA_ERR_TOO_SMALL before anything is enqueued.
+ *   The first call on a device, with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.  All calls share the one array and it keeps
+ *   the last call's contents; nothing in it needs to start at zero (each call
+ *   writes all it reads), but calls that overlap on the GPU race on it and
+ *   must be serialised by the caller.  Other arguments and results as for
+ *   mla_context_chunk_attn. */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int mla_context_chunk_attn_noalloc(const mla_dims_t *d, const mla_chunk_t *chunk,
+                                   const int32_t *starts, const int32_t *seq_lens,
+                                   const int32_t *query_start_loc,
+                                   int32_t num_tokens, const void *q,
+                                   const void *kv_cache, int32_t num_blocks,
+                                   const int32_t *block_table,
+                                   int32_t block_table_stride,
+                                   const void *w_kv_b, float *o_partial,
+                                   float *lse_partial, int32_t *dev_status,
+                                   mla_stream_t stream);
+
 /* mla_prefill_workspace_bytes: device bytes mla_chunked_prefill needs for
  *   these lengths and planner settings (it runs the planner). */
 int mla_prefill_workspace_bytes(const mla_dims_t *d,

@@ -8,14 +8,16 @@ marshal arguments; PyTorch provides device memory and streams.
 
 from ._lib import (Chunk, Dims, MlaError, lib, merge_attn_states, mla_chunk_kv_dtype,
                    mla_chunk_workspace_bytes, mla_device_error_flags,
-                   mla_chunked_prefill, mla_context_chunk_attn, mla_fill_empty_rows,
+                   mla_chunked_prefill, mla_context_chunk_attn, mla_context_chunk_attn_noalloc,
+                   mla_fill_empty_rows,
                    mla_gather_context_rows, mla_has_tcgen05, mla_kv_up_proj,
                    mla_mask_empty_context, mla_plan_context_chunks, mla_prefill_workspace_bytes,
                    mla_varlen_attn, MLA_STATUS_BAD_BLOCK)
 
 __all__ = ["Chunk", "Dims", "MlaError", "lib", "merge_attn_states", "mla_chunk_kv_dtype",
            "mla_chunk_workspace_bytes", "mla_device_error_flags",
-           "mla_chunked_prefill", "mla_context_chunk_attn", "mla_fill_empty_rows",
+           "mla_chunked_prefill", "mla_context_chunk_attn", "mla_context_chunk_attn_noalloc",
+           "mla_fill_empty_rows",
            "mla_gather_context_rows", "mla_has_tcgen05", "mla_kv_up_proj",
            "mla_mask_empty_context", "mla_plan_context_chunks", "mla_prefill_workspace_bytes",
            "mla_varlen_attn", "MLA_STATUS_BAD_BLOCK", "ChunkedPrefill"]

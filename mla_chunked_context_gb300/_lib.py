@@ -33,7 +33,8 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_kv_up_proj", "mla_varlen_attn", "mla_fill_empty_rows", "mla_mask_empty_context",
             "mla_chunk_workspace_bytes", "mla_context_chunk_attn", "mla_prefill_workspace_bytes",
             "mla_chunked_prefill", "mla_has_tcgen05", "mla_device_error_flags",
-            "mla_chunk_kv_dtype")
+            "mla_chunk_kv_dtype", "mla_context_chunk_attn_noalloc")
+MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class MlaError(RuntimeError):
@@ -86,6 +87,8 @@ def lib() -> C.CDLL:
             "mla_has_tcgen05": [],
             "mla_device_error_flags": [P],
             "mla_chunk_kv_dtype": [P, P],
+            "mla_context_chunk_attn_noalloc": [P, P, P, P, P, I32, P, P, I32, P, I32, P, P, P,
+                                               P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -286,6 +289,21 @@ def mla_context_chunk_attn(dims: Dims, chunk: Chunk, query_start_loc: Sequence[i
         workspace.numel() * workspace.element_size(), _ptr(o_partial), _ptr(lse_partial),
         _ptr(dev_status), _stream(stream)), "mla_context_chunk_attn")
     assert n >= 1
+
+
+def mla_context_chunk_attn_noalloc(dims: Dims, chunk: Chunk, query_start_loc: Sequence[int], q,
+                                   kv_cache, block_table, w_kv_b, o_partial, lse_partial,
+                                   dev_status=None, stream=None) -> None:
+    """mla_context_chunk_attn with the library's own device scratch array
+    (for callers that cannot allocate device memory; see the C header)."""
+    d = dims.c()
+    c = mla_chunk_t(chunk.request_start, chunk.request_end, 0, chunk.rows,
+                    int(chunk.is_continuation))
+    _check(lib().mla_context_chunk_attn_noalloc(
+        C.byref(d), C.byref(c), _i32_host(chunk.starts), _i32_host(chunk.seq_lens),
+        _i32_host(query_start_loc), q.shape[0], _ptr(q), _ptr(kv_cache), kv_cache.shape[0],
+        _ptr(block_table), block_table.shape[1], _ptr(w_kv_b), _ptr(o_partial),
+        _ptr(lse_partial), _ptr(dev_status), _stream(stream)), "mla_context_chunk_attn_noalloc")
 
 
 def mla_prefill_workspace_bytes(dims: Dims, context_lens, query_lens, row_budget: int,
