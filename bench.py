@@ -328,7 +328,11 @@ def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
             st=torch.tensor(p.starts, dtype=torch.int32, device=dev),
             cu=torch.tensor(cu, dtype=torch.int32, device=dev), cu_h=cu,
             ql=qsl[p.request_start:p.request_end + 1], rows=cu[-1],
-            acc=[1 if s > 0 else 0 for s in p.starts]))
+            ql_d=torch.tensor(qsl[p.request_start:p.request_end + 1], dtype=torch.int32,
+                              device=dev),
+            acc_d=torch.tensor([1 if s > 0 else 0 for s in p.starts], dtype=torch.int32,
+                               device=dev)))
+    qsl_d = torch.tensor(qsl, dtype=torch.int32, device=dev)
 
     def timed(name, fn):
         flush.fill_(1)
@@ -350,11 +354,13 @@ def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
                                                           kv_ws))
             timed("attn_ctx", lambda: M.mla_varlen_attn(dims, False, m["ql"], m["cu_h"], g["q"],
                                                         kv_ws, lat_ws, o_p, l_p,
-                                                        accumulate=m["acc"]))
+                                                        q_loc_dev=m["ql_d"], k_loc_dev=m["cu"],
+                                                        accumulate_dev=m["acc_d"]))
         timed("up_proj_new", lambda: M.mla_kv_up_proj(dims, g["new_latent"], T, g["w_kv_b"],
                                                       kv_new))
         timed("attn_new", lambda: M.mla_varlen_attn(dims, True, qsl, qsl, g["q"], kv_new,
-                                                    g["new_latent"], o_s, l_s))
+                                                    g["new_latent"], o_s, l_s,
+                                                    q_loc_dev=qsl_d, k_loc_dev=qsl_d))
         pnt = 0
         for r, c in enumerate(w.context_lens):
             if c > 0:
@@ -495,7 +501,10 @@ def run_kernel_case(args, dev):
         lse = torch.empty(H, n * ql, device=dev)
         q_loc = [i * ql for i in range(n + 1)]
         k_loc = [i * kl for i in range(n + 1)]
-        fn = lambda: M.mla_varlen_attn(dims, args.causal, q_loc, k_loc, q, kv, lat, o, lse)  # noqa
+        qd = torch.tensor(q_loc, dtype=torch.int32, device=dev)
+        kd = torch.tensor(k_loc, dtype=torch.int32, device=dev)
+        fn = lambda: M.mla_varlen_attn(dims, args.causal, q_loc, k_loc, q, kv, lat, o, lse,  # noqa
+                                       q_loc_dev=qd, k_loc_dev=kd)
         pairs = n * (ql * (ql + 1) / 2 if args.causal else ql * kl)
         work, unit, peak = 2.0 * H * (192 + 128) * pairs, "TFLOP/s", peaks["bf16_tflops"]
         info = {"seqs": n, "q": ql, "k": kl, "causal": bool(args.causal)}

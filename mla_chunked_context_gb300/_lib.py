@@ -236,13 +236,18 @@ def mla_kv_up_proj(dims: Dims, latent, rows: int, w_kv_b, kv, stream=None) -> No
 
 def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Sequence[int], q,
                     kv, latent, o, lse, accumulate: Optional[Sequence[int]] = None,
-                    stream=None) -> None:
-    """q_loc / k_loc are host sequences; they are copied to the device here."""
+                    stream=None, q_loc_dev=None, k_loc_dev=None, accumulate_dev=None) -> None:
+    """q_loc / k_loc (and accumulate) are host sequences; they are copied to
+    the device here unless device copies are passed as *_dev tensors."""
     n = len(q_loc) - 1
     dev = q.device
-    ql = torch.tensor(list(q_loc), dtype=torch.int32, device=dev)
-    kl = torch.tensor(list(k_loc), dtype=torch.int32, device=dev)
-    acc = torch.tensor(list(accumulate), dtype=torch.int32, device=dev) if accumulate else None
+    ql = q_loc_dev if q_loc_dev is not None else torch.tensor(list(q_loc), dtype=torch.int32,
+                                                              device=dev)
+    kl = k_loc_dev if k_loc_dev is not None else torch.tensor(list(k_loc), dtype=torch.int32,
+                                                              device=dev)
+    acc = accumulate_dev
+    if acc is None and accumulate:
+        acc = torch.tensor(list(accumulate), dtype=torch.int32, device=dev)
     d = dims.c()
     _check(lib().mla_varlen_attn(C.byref(d), int(causal), n, _ptr(ql), _ptr(kl),
                                  _i32_host(q_loc), _i32_host(k_loc), q.shape[0], _ptr(q),

@@ -5,18 +5,26 @@
 // The MLA up-projection is not on the pages; it is the standard MLA prefill
 // step that turns the gathered latent rows into per-head K_nope and V.
 //
-// Design: persistent, warp-specialised, one CTA per SM.
-//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage
-//               (128-byte swizzle), 4-stage mbarrier ring.
-//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
-//               (M=128, N=256, K=16; 4 per stage) into one of two 256-column
-//               f32 accumulators and commits stage / accumulator barriers.
-//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns, round to fp16 (or
-//               bf16),
-//               write a 32x64 tile into a swizzled staging buffer, TMA store.
-// The two accumulators let the epilogue of tile i overlap the MMAs of tile
-// i+1.  Tiles are visited m-major with n fastest, so a 128-row slice of the
-// latent and the whole weight stay in L2 while 152 CTAs sweep them.
+// Design: persistent, warp-specialised, 2-SM MMA.  CTAs run in pairs (a
+// cluster of two, one CTA per SM); a pair computes 256x256 output tiles with
+// tcgen05.mma.cta_group::2 (M=256: 128 rows in each SM's tensor memory).
+// Each SM holds only its own 128 A rows and its half (128 rows) of the B
+// tile, so per SM a 64-deep K step moves 32 KB through shared memory for
+// 2x128x256x64 FLOP -- half the shared-memory traffic per FLOP of a 1-SM
+// M=128 tile, which is what bounds a 1-SM kernel.
+//   warp 0      (both CTAs) TMA producer: own A 128x64 and B-half 128x64 per
+//               stage, 6-stage ring; the loads of both CTAs complete on the
+//               even CTA's "full" barrier.
+//   warp 1      (both CTAs) allocates 512 TMEM columns in the pair; in the
+//               even CTA lane 0 issues the MMAs (M=256, N=256, K=16; 4 per
+//               stage) into one of two 256-column f32 accumulators, and
+//               commits stage and accumulator barriers to both CTAs.
+//   warps 2-5   (both CTAs) epilogue of the CTA's own 128 rows: tcgen05.ld
+//               32 lanes x 32 columns, round to fp16 (or bf16), swizzled 32x64
+//               staging tile, TMA store; then release the accumulator on the
+//               even CTA's barrier.
+// Pair tiles are visited m-major with n fastest, so a 256-row slice of the
+// latent and the whole weight stay in L2 while the pairs sweep them.
 #include <cstdio>
 
 #include "sm103.cuh"
@@ -26,12 +34,13 @@ namespace sm103 {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6;
+constexpr int PAIR_M = 2 * BM;                // rows of a pair tile
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB: this CTA's A rows
+constexpr int B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 4;
-constexpr int STG_BYTES = 32 * 64 * 2;        // one warp's 32x64 bf16 staging tile
+constexpr int STG_BYTES = 32 * 64 * 2;        // one warp's 32x64 16-bit staging tile
 constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES +
                            EPI_WARPS * 2 * STG_BYTES + 256 /*barriers*/;
 constexpr int THREADS = 192;
@@ -39,7 +48,7 @@ constexpr uint32_t TMEM_COLS = 512;
 
 struct GemmArgs {
   int M, N, K;
-  int num_m, num_n;
+  int num_pm, num_n;  // pair tiles along M, tiles along N
 };
 
 template <bool kF16Out>
@@ -55,15 +64,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *sStage = smem + STAGES * STAGE_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + EPI_WARPS * 2 * STG_BYTES);
   // bars: full[S], empty[S], acc_full[2], acc_empty[2], mma_done; then the
-  // TMEM base address slot
+  // TMEM base address slot.  full and acc_empty are used in the even CTA only.
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = g.num_m * g.num_n;
+  const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the MMAs
+  const int num_tiles = g.num_pm * g.num_n;
+  const int first = blockIdx.x >> 1, step = gridDim.x >> 1;
   const int kblocks = g.K / BK;
+  // the even CTA's barriers, as seen from this CTA
+  const uint32_t full0_lead = mapa_shared(full0, 0);
+  const uint32_t acce0_lead = mapa_shared(acce0, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -72,7 +86,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf0 + 8 * a, 1);
-      mbar_init(acce0 + 8 * a, EPI_WARPS);
+      mbar_init(acce0 + 8 * a, 2 * EPI_WARPS);  // epilogue warps of both CTAs
     }
     mbar_init(done_bar, 1);
     fence_mbar_init();
@@ -80,30 +94,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_map(&tm_b);
     prefetch_map(&tm_c);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any load or arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer (both CTAs)
     int stage = 0;
     uint32_t phase = 0;
     int issued_parity[STAGES];
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const int m0 = (t / g.num_n) * BM, n0 = (t % g.num_n) * BN;
+    for (int t = first; t < num_tiles && ok; t += step) {
+      const int m0 = (t / g.num_n) * PAIR_M + int(rank) * BM;
+      const int nb = (t % g.num_n) * BN + int(rank) * (BN / 2);
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) {
           ok = false;
           break;
         }
-        const uint32_t fb = full0 + 8 * stage;
-        mbar_expect_tx(fb, STAGE_BYTES);
-        tma_load_2d(smem_u32(sA + stage * A_BYTES), &tm_a, fb, kb * BK, m0);
-        tma_load_2d(smem_u32(sB + stage * B_BYTES), &tm_b, fb, kb * BK, n0);
+        const uint32_t fb = full0_lead + 8 * stage;
+        if (rank == 0) mbar_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);  // both CTAs' bytes
+        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &tm_a, fb, kb * BK, m0);
+        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &tm_b, fb, kb * BK, nb);
         issued_parity[stage] = int(phase);
         if (++stage == STAGES) {
           stage = 0;
@@ -111,18 +127,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-    // every load this thread issued has landed before the CTA may exit
-    for (int s = 0; s < STAGES; ++s)
-      if (issued_parity[s] >= 0) mbar_wait(full0 + 8 * s, uint32_t(issued_parity[s]));
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_f16kind(BM, BN, false, false, true);
+    // every load this CTA issued has landed before the pair may exit: the
+    // even CTA's full barrier counts both CTAs' bytes; the odd CTA knows its
+    // loads landed once the MMAs that read them released the stage
+    for (int s = 0; s < STAGES; ++s) {
+      if (issued_parity[s] < 0) continue;
+      if (rank == 0)
+        mbar_wait(full0 + 8 * s, uint32_t(issued_parity[s]));
+      else
+        mbar_wait(empty0 + 8 * s, uint32_t(issued_parity[s]));
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (even CTA)
+    constexpr uint32_t idesc = idesc_f16kind(PAIR_M, BN, false, false, true);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int t = first; t < num_tiles && ok; t += step) {
       if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
@@ -136,33 +159,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
-                   desc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
-        mma_commit(empty0 + 8 * stage);  // stage free once these MMAs finish
+          mma_bf16_pair(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
+                        desc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+        // the stage is free in both CTAs once these MMAs finish
+        mma_commit_pair_mc(empty0 + 8 * stage, uint16_t(0x3));
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (!ok) break;
-      mma_commit(accf0 + 8 * acc);  // accumulator complete
+      mma_commit_pair_mc(accf0 + 8 * acc, uint16_t(0x3));  // accumulator complete
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
       }
     }
     // every MMA this thread issued has completed before TMEM is released
-    mma_commit(done_bar);
+    mma_commit_pair_mc(done_bar, uint16_t(0x1));
     mbar_wait(done_bar, 0);
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM -> bf16 -> smem -> TMA store
+    // ---------------- epilogue: TMEM -> 16-bit -> smem -> TMA store
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     uint8_t *stg = sStage + (warp - 2) * 2 * STG_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
     int buf = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const int m0 = (t / g.num_n) * BM, n0 = (t % g.num_n) * BN;
+    for (int t = first; t < num_tiles; t += step) {
+      const int m0 = (t / g.num_n) * PAIR_M + int(rank) * BM, n0 = (t % g.num_n) * BN;
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * BN);
@@ -204,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+      if (lane == 0) mbar_arrive_cluster(acce0_lead + 8 * acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
@@ -214,10 +238,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs or loads may touch it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -278,10 +303,10 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
   CUtensorMap ta, tb, tc;
   const bool f16 = kv_dtype == MLA_DTYPE_F16;
   if (!make_tmap_2d_16(&ta, false, latent, K, rows, uint64_t(lda) * 2, BK, BM, true) ||
-      !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN, true) ||
+      !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN / 2, true) ||
       !make_tmap_2d_16(&tc, f16, kv, N, rows, uint64_t(N) * 2, 64, 32, true))
     return MLA_ERR_CUDA;
-  GemmArgs g{rows, N, K, (rows + BM - 1) / BM, N / BN};
+  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN};
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(up_proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -292,12 +317,32 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
       return MLA_ERR_CUDA;
     attr_set = true;
   }
-  const int tiles = g.num_m * g.num_n;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  if (f16)
-    up_proj_tc_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, tc, g);
-  else
-    up_proj_tc_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, tc, g);
+  const int pair_tiles = g.num_pm * g.num_n;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, up_proj_tc_kernel<true>, &cfg) != cudaSuccess ||
+        n < 1)
+      n = num_sms() / 2;
+    max_clusters = n;
+  }
+  const int clusters = pair_tiles < max_clusters ? pair_tiles : max_clusters;
+  cfg.gridDim = dim3(2 * clusters);
+  const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<true>, ta, tb, tc, g)
+                            : cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<false>, ta, tb, tc, g);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
   return launch_status();
 }
 
