@@ -205,21 +205,57 @@ def run_ours(args, rank, world, dev):
     max_ms = t.item()
     value = world * args.steps * T / (max_ms / 1e3)
 
-    # ---- e2e: host buffers, copies inside the timed region
+    # ---- e2e: host buffers, copies inside the timed region.  Inputs are
+    # double-buffered on the device: step i+1's host->device copy (on a copy
+    # stream) overlaps step i's compute; each step's output is read back to
+    # pinned host memory.  The region runs from the first copy to the last
+    # read-back.
     host = {k: v.pin_memory() for k, v in x.items()}
-    host_out = torch.empty(T, H, w.v_dim, dtype=w.torch_dtype).pin_memory()
+    sets = [g, {k: torch.empty_like(v) for k, v in g.items()}]
+    outs = [out, torch.empty_like(out)]
+    host_out = [torch.empty(T, H, w.v_dim, dtype=w.torch_dtype).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    copy_stream = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    copy_stream.wait_event(e0)
+    in_ready, done, read_back = [None, None], [None, None], [None, None]
+
+    def h2d_into(k):
+        with torch.cuda.stream(copy_stream):
+            if done[k] is not None:
+                copy_stream.wait_event(done[k])      # the step that used this set is done
+            for name in sets[k]:
+                sets[k][name].copy_(host[name], non_blocking=True)
+            in_ready[k] = ev()
+            in_ready[k].record(copy_stream)
+
+    h2d_into(0)
     for i in range(args.steps):
-        for k in g:
-            g[k].copy_(host[k], non_blocking=True)
-        step()
-        host_out.copy_(out, non_blocking=True)
+        k = i & 1
+        if i + 1 < args.steps:
+            h2d_into(1 - k)
+        stream.wait_event(in_ready[k])
+        if read_back[k] is not None:
+            stream.wait_event(read_back[k])          # output buffer k was read back
+        sk = sets[k]
+        pf(sk["q"], sk["new_latent"], sk["kv_cache"], sk["block_table"], sk["w_kv_b"], outs[k],
+           None)
+        done[k] = ev()
+        done[k].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(done[k])
+            host_out[k].copy_(outs[k], non_blocking=True)
+            read_back[k] = ev()
+            read_back[k].record(copy_stream)
+    for k in range(2):
+        if read_back[k] is not None:
+            stream.wait_event(read_back[k])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -227,12 +263,14 @@ def run_ours(args, rank, world, dev):
     if world > 1:
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     e2e_value = world * args.steps * T / (t.item() / 1e3)
+    del sets[1], outs[1]
 
     result = None
     if rank == 0:
         kernels = time_kernels(M, W, w, g, plans, dims, dev, args, flush)
         fl = flops_of(w, plans)
         merge = bench_merge(M, W, dev, peaks, flush)
+        comparator = bench_equal_window(M, w, g, dims, dev, flush, max_ms / args.steps)
         up = kernels["up_proj_ctx"]
         roofline = {
             "kernel": "kv_up_proj (tcgen05 GEMM)" if M.mla_has_tcgen05() else "kv_up_proj (CUDA cores)",
@@ -268,6 +306,7 @@ def run_ours(args, rank, world, dev):
             "gpu_launches": launches * args.steps,
             "roofline": roofline,
             "merge": merge,
+            "comparator": comparator,
             "kernels": kernels,
             "flops_per_step": fl,
         }
@@ -372,6 +411,41 @@ def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
     empty = any(c == 0 and qsl[r] < pnt for r, c in enumerate(w.context_lens))
     res["launches_per_step"] = 3 * len(plans) + 3 + (1 if empty else 0)
     return res
+
+
+def bench_equal_window(M, w, g, dims, dev, flush, new_ms, steps=3):
+    """The old equal-window scheme on the same batch (comparator for the
+    pages' claim that per-request packing cuts chunks and latency)."""
+    window, n_chunks = M.mla_plan_equal_window_chunks(w.context_lens, w.row_budget,
+                                                      w.split_alignment)
+    ws = torch.empty(M.mla_prefill_equal_window_workspace_bytes(
+        dims, w.context_lens, w.query_lens, w.row_budget, w.split_alignment),
+        dtype=torch.uint8, device=dev)
+    out = torch.empty(w.num_tokens, w.num_heads, w.v_dim, dtype=w.torch_dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def go():
+        M.mla_chunked_prefill_equal_window(dims, w.context_lens, w.query_lens, w.row_budget,
+                                           w.split_alignment, g["q"], g["new_latent"],
+                                           g["kv_cache"], g["block_table"], g["w_kv_b"], ws, out)
+    go()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        flush.fill_(4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        go()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    med = statistics.median(ms)
+    plans = M.mla_plan_context_chunks(w.context_lens, w.row_budget, w.max_context_chunk,
+                                      w.split_alignment)
+    return {"scheme": "equal context windows (the scheme per-request packing replaced)",
+            "window_rows": window, "chunks": n_chunks, "ms_per_step": med,
+            "packed_chunks": len(plans), "packed_ms_per_step": new_ms,
+            "latency_ratio": med / new_ms}
 
 
 def bench_merge(M, W, dev, peaks, flush, reps=20):

@@ -147,7 +147,9 @@ int mla_plan_context_chunks(const int32_t *context_lens, int32_t num_requests,
  *                            out_dtype for out (bf16 output is rounded to
  *                            nearest even)
  *   prefix_lse, suffix_lse   device float32 [H, T];  out_lse nullable
- *   head_dim must be a multiple of 8.  out may alias suffix_o (in place).
+ *   head_dim must be a multiple of 8.  out may alias either input O (each
+ *   element is read before it is written, by the same thread); out_lse must
+ *   not alias an input LSE (one LSE is read by all threads of its row).
  */
 int merge_attn_states(void *out, float *out_lse, const void *prefix_o,
                       const float *prefix_lse, const void *suffix_o,
@@ -335,6 +337,41 @@ int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
                         void *workspace, size_t workspace_bytes, void *out,
                         float *out_lse, int32_t *dev_status,
                         mla_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The old scheme, kept as a comparator (PR #50613 report, motivation: the
+ * workspace was divided evenly among the requests with context and every
+ * iteration processed the same context window of every request; PR #49294
+ * report: per chunk, rows of requests whose window is empty are fixed up with
+ * mask_empty_context before the merge).
+ *
+ * mla_plan_equal_window_chunks (host only): window = row_budget / (requests
+ *   with context), rounded down to split_alignment; chunk c covers rows
+ *   [c*window, (c+1)*window) of every request, clipped to its length;
+ *   *num_chunks = ceil(max context / window).  MLA_ERR_PLANNER_STUCK when the
+ *   window rounds to 0.
+ * mla_chunked_prefill_equal_window: the whole prefill under that plan: per
+ *   chunk gather + up-projection + attention over every request, the
+ *   empty-window fix-up, and a merge over the whole batch into the running
+ *   partial; then the new-token attention and the final merge.  Same
+ *   arguments, layouts and result as mla_chunked_prefill (no
+ *   max_context_chunk); workspace from
+ *   mla_prefill_equal_window_workspace_bytes. */
+int mla_plan_equal_window_chunks(const int32_t *context_lens,
+                                 int32_t num_requests, int32_t row_budget,
+                                 int32_t split_alignment, int32_t *window,
+                                 int32_t *num_chunks);
+int mla_prefill_equal_window_workspace_bytes(
+    const mla_dims_t *d, const int32_t *context_lens, const int32_t *query_lens,
+    int32_t num_requests, int32_t row_budget, int32_t split_alignment,
+    size_t *bytes);
+int mla_chunked_prefill_equal_window(
+    const mla_dims_t *d, const int32_t *context_lens, const int32_t *query_lens,
+    int32_t num_requests, int32_t row_budget, int32_t split_alignment,
+    const void *q, const void *new_latent, const void *kv_cache,
+    int32_t num_blocks, const int32_t *block_table, int32_t block_table_stride,
+    const void *w_kv_b, void *workspace, size_t workspace_bytes, void *out,
+    float *out_lse, int32_t *dev_status, mla_stream_t stream);
 
 /* 1 when the current device runs the tcgen05 (sm_103a) kernels of this
  * library. */

@@ -33,7 +33,9 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_kv_up_proj", "mla_varlen_attn", "mla_fill_empty_rows", "mla_mask_empty_context",
             "mla_chunk_workspace_bytes", "mla_context_chunk_attn", "mla_prefill_workspace_bytes",
             "mla_chunked_prefill", "mla_has_tcgen05", "mla_device_error_flags",
-            "mla_chunk_kv_dtype", "mla_context_chunk_attn_noalloc")
+            "mla_chunk_kv_dtype", "mla_context_chunk_attn_noalloc",
+            "mla_plan_equal_window_chunks", "mla_prefill_equal_window_workspace_bytes",
+            "mla_chunked_prefill_equal_window")
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -89,6 +91,10 @@ def lib() -> C.CDLL:
             "mla_chunk_kv_dtype": [P, P],
             "mla_context_chunk_attn_noalloc": [P, P, P, P, P, I32, P, P, I32, P, I32, P, P, P,
                                                P, P],
+            "mla_plan_equal_window_chunks": [P, I32, I32, I32, P, P],
+            "mla_prefill_equal_window_workspace_bytes": [P, P, P, I32, I32, I32, P],
+            "mla_chunked_prefill_equal_window": [P, P, P, I32, I32, I32, P, P, P, I32, P, I32, P,
+                                                 P, SZ, P, P, P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -350,3 +356,36 @@ def mla_chunk_kv_dtype(dims: Dims) -> torch.dtype:
     k = C.c_int32(0)
     _check(lib().mla_chunk_kv_dtype(C.byref(d), C.byref(k)), "mla_chunk_kv_dtype")
     return _TORCH_OF[k.value]
+
+
+def mla_plan_equal_window_chunks(context_lens: Sequence[int], row_budget: int,
+                                 split_alignment: int):
+    """(window, number of chunks) of the old equal-window scheme."""
+    w, n = C.c_int32(0), C.c_int32(0)
+    _check(lib().mla_plan_equal_window_chunks(_i32_host(context_lens), len(context_lens),
+                                              row_budget, split_alignment, C.byref(w),
+                                              C.byref(n)), "mla_plan_equal_window_chunks")
+    return w.value, n.value
+
+
+def mla_prefill_equal_window_workspace_bytes(dims: Dims, context_lens, query_lens,
+                                             row_budget: int, split_alignment: int) -> int:
+    d = dims.c()
+    b = C.c_size_t(0)
+    _check(lib().mla_prefill_equal_window_workspace_bytes(
+        C.byref(d), _i32_host(context_lens), _i32_host(query_lens), len(context_lens),
+        row_budget, split_alignment, C.byref(b)), "mla_prefill_equal_window_workspace_bytes")
+    return b.value
+
+
+def mla_chunked_prefill_equal_window(dims: Dims, context_lens, query_lens, row_budget: int,
+                                     split_alignment: int, q, new_latent, kv_cache, block_table,
+                                     w_kv_b, workspace, out, out_lse=None, dev_status=None,
+                                     stream=None) -> None:
+    d = dims.c()
+    _check(lib().mla_chunked_prefill_equal_window(
+        C.byref(d), _i32_host(context_lens), _i32_host(query_lens), len(context_lens),
+        row_budget, split_alignment, _ptr(q), _ptr(new_latent), _ptr(kv_cache),
+        kv_cache.shape[0], _ptr(block_table), block_table.shape[1], _ptr(w_kv_b),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(out_lse),
+        _ptr(dev_status), _stream(stream)), "mla_chunked_prefill_equal_window")

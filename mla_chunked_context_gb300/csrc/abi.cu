@@ -510,3 +510,217 @@ extern "C" int mla_device_error_flags(int32_t *flags) {
   *flags = a | b;
   return MLA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// The old scheme, kept as a comparator: equal context windows for every
+// request with context (PR #50613 report, motivation; PR #49294 report,
+// build_mla_chunked_context_metadata and mask_empty_context).  Each chunk
+// runs the gather, up-projection and attention over the whole batch, fixes
+// the rows of requests whose window is empty, and merges into the running
+// partial.
+namespace mla {
+namespace {
+
+int plan_equal_window(const int32_t *ctx, int R, int budget, int align, int &window,
+                      int &n_chunks) {
+  if (R < 0 || budget < 1 || align < 1 || (R > 0 && !ctx)) return MLA_ERR_INVALID;
+  int with_ctx = 0, mx = 0;
+  for (int r = 0; r < R; ++r) {
+    if (ctx[r] < 0) return MLA_ERR_INVALID;
+    if (ctx[r] > 0) ++with_ctx;
+    mx = std::max(mx, int(ctx[r]));
+  }
+  window = n_chunks = 0;
+  if (with_ctx == 0) return MLA_OK;
+  window = budget / with_ctx / align * align;
+  if (window <= 0) return MLA_ERR_PLANNER_STUCK;
+  n_chunks = (mx + window - 1) / window;
+  return MLA_OK;
+}
+
+struct EqualWindowLayout {
+  int window = 0, n_chunks = 0, T = 0, pnt = 0, max_rows = 0, R = 0;
+  std::vector<int32_t> qsl;
+  std::vector<ChunkMetaHost> metas;  // every chunk lists every request
+  std::vector<size_t> meta_off;
+  std::vector<char> has_empty;
+  size_t slice_off = 0, suffix_off = 0, meta_total = 0;
+};
+
+int build_equal_window(const int32_t *ctx, const int32_t *ql, int R, int budget, int align,
+                       EqualWindowLayout &p) {
+  for (int r = 0; r < R; ++r)
+    if (ql[r] < 0) return MLA_ERR_INVALID;
+  int rc = plan_equal_window(ctx, R, budget, align, p.window, p.n_chunks);
+  if (rc) return rc;
+  p.R = R;
+  p.qsl.assign(R + 1, 0);
+  for (int r = 0; r < R; ++r) p.qsl[r + 1] = p.qsl[r] + ql[r];
+  p.T = p.qsl[R];
+  int last = -1;
+  for (int r = 0; r < R; ++r)
+    if (ctx[r] > 0) last = r;
+  p.pnt = last >= 0 ? p.qsl[last + 1] : 0;
+  std::vector<int32_t> st(R), ln(R);
+  size_t off = 0;
+  p.metas.resize(p.n_chunks);
+  for (int c = 0; c < p.n_chunks; ++c) {
+    bool empty = false;
+    int rows = 0;
+    for (int r = 0; r < R; ++r) {
+      const int64_t lo = std::min<int64_t>(int64_t(c) * p.window, ctx[r]);
+      const int64_t hi = std::min<int64_t>(int64_t(c + 1) * p.window, ctx[r]);
+      st[r] = int32_t(lo);
+      ln[r] = int32_t(hi - lo);
+      rows += ln[r];
+      empty = empty || ln[r] == 0;
+    }
+    const mla_chunk_t chunk{0, R, 0, rows, 0};
+    build_chunk_meta(chunk, st.data(), ln.data(), p.qsl.data(), p.metas[c]);
+    // the old scheme writes every chunk's result in full: no accumulate flags
+    std::fill(p.metas[c].ints.begin() + 4 * R + 2, p.metas[c].ints.end(), 0);
+    p.meta_off.push_back(off);
+    off += p.metas[c].ints.size();
+    p.has_empty.push_back(empty ? 1 : 0);
+    p.max_rows = std::max(p.max_rows, rows);
+  }
+  p.slice_off = off;
+  off += 2;
+  p.suffix_off = off;
+  off += R + 1;
+  p.meta_total = off;
+  return MLA_OK;
+}
+
+struct EqualWindowBuffers {
+  int32_t *meta;
+  ChunkBuffers chunk;
+  void *kv_suffix;
+  float *o_run[2], *lse_run[2];  // running partial, ping-ponged per chunk
+  float *o_chunk, *lse_chunk, *o_suf, *lse_suf;
+};
+
+size_t carve_equal_window(void *base, const mla_dims_t &d, const EqualWindowLayout &p,
+                          EqualWindowBuffers &b) {
+  Carve cv(base);
+  b.meta = static_cast<int32_t *>(cv.take(p.meta_total * sizeof(int32_t)));
+  carve_chunk_buffers(cv, d, p.max_rows, b.chunk);
+  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk.kv_dtype));
+  const size_t o_bytes = size_t(p.T) * d.num_heads * d.v_dim * sizeof(float);
+  const size_t l_bytes = size_t(p.T) * d.num_heads * sizeof(float);
+  for (int k = 0; k < 2; ++k) {
+    b.o_run[k] = static_cast<float *>(cv.take(o_bytes));
+    b.lse_run[k] = static_cast<float *>(cv.take(l_bytes));
+  }
+  b.o_chunk = static_cast<float *>(cv.take(o_bytes));
+  b.lse_chunk = static_cast<float *>(cv.take(l_bytes));
+  b.o_suf = static_cast<float *>(cv.take(o_bytes));
+  b.lse_suf = static_cast<float *>(cv.take(l_bytes));
+  return cv.off;
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" int mla_plan_equal_window_chunks(const int32_t *context_lens, int32_t num_requests,
+                                            int32_t row_budget, int32_t split_alignment,
+                                            int32_t *window, int32_t *num_chunks) {
+  if (!window || !num_chunks) return MLA_ERR_INVALID;
+  int w = 0, n = 0;
+  const int rc = plan_equal_window(context_lens, num_requests, row_budget, split_alignment, w, n);
+  if (rc) return rc;
+  *window = w;
+  *num_chunks = n;
+  return MLA_OK;
+}
+
+extern "C" int mla_prefill_equal_window_workspace_bytes(const mla_dims_t *d,
+                                                        const int32_t *context_lens,
+                                                        const int32_t *query_lens,
+                                                        int32_t num_requests, int32_t row_budget,
+                                                        int32_t split_alignment, size_t *bytes) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!bytes || num_requests < 0 || (num_requests > 0 && (!context_lens || !query_lens)))
+    return MLA_ERR_INVALID;
+  EqualWindowLayout p;
+  rc = build_equal_window(context_lens, query_lens, num_requests, row_budget, split_alignment, p);
+  if (rc) return rc;
+  EqualWindowBuffers b;
+  *bytes = carve_equal_window(nullptr, *d, p, b);
+  return MLA_OK;
+}
+
+extern "C" int mla_chunked_prefill_equal_window(
+    const mla_dims_t *d, const int32_t *context_lens, const int32_t *query_lens,
+    int32_t num_requests, int32_t row_budget, int32_t split_alignment, const void *q,
+    const void *new_latent, const void *kv_cache, int32_t num_blocks, const int32_t *block_table,
+    int32_t block_table_stride, const void *w_kv_b, void *workspace, size_t workspace_bytes,
+    void *out, float *out_lse, int32_t *dev_status, mla_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (num_requests < 0 || (num_requests > 0 && (!context_lens || !query_lens)))
+    return MLA_ERR_INVALID;
+  EqualWindowLayout p;
+  rc = build_equal_window(context_lens, query_lens, num_requests, row_budget, split_alignment, p);
+  if (rc) return rc;
+  if (p.T == 0) return MLA_OK;
+  if (!q || !new_latent || !w_kv_b || !workspace || !out) return MLA_ERR_INVALID;
+  if (p.n_chunks > 0 && (!kv_cache || !block_table || block_table_stride < 1))
+    return MLA_ERR_INVALID;
+  for (int r = 0; r < num_requests; ++r)
+    if (int64_t(context_lens[r]) > int64_t(block_table_stride) * d->block_size)
+      return MLA_ERR_INVALID;
+  EqualWindowBuffers b;
+  if (workspace_bytes < carve_equal_window(nullptr, *d, p, b)) return MLA_ERR_TOO_SMALL;
+  carve_equal_window(workspace, *d, p, b);
+  std::vector<int32_t> meta(p.meta_total, 0);
+  for (int c = 0; c < p.n_chunks; ++c)
+    std::memcpy(meta.data() + p.meta_off[c], p.metas[c].ints.data(),
+                p.metas[c].ints.size() * sizeof(int32_t));
+  meta[p.slice_off] = 0;
+  meta[p.slice_off + 1] = p.T;
+  std::memcpy(meta.data() + p.suffix_off, p.qsl.data(), p.qsl.size() * sizeof(int32_t));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = upload(b.meta, meta, s);
+  if (rc) return rc;
+  const int H = d->num_heads, Dv = d->v_dim, T = p.T, R = p.R;
+  const int LP = d->kv_lora_rank + d->qk_rope_dim;
+  const int es = elem_bytes(d->dtype);
+  // the running partial starts empty: O = 0, LSE = -inf
+  rc = launch_fill_empty_rows(b.o_run[0], b.lse_run[0], T, H, Dv, 1, b.meta + p.slice_off, s);
+  if (rc) return rc;
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const ChunkMetaHost &m = p.metas[c];
+    const int32_t *req = b.meta + p.meta_off[c], *st = req + R, *cu = st + R, *ql = cu + R + 1;
+    if (m.rows > 0) {
+      rc = launch_gather(kv_cache, num_blocks, d->block_size, LP * es, block_table,
+                         block_table_stride, R, req, st, cu, m.rows, b.chunk.latent_ws,
+                         dev_status, s);
+      if (rc) return rc;
+      rc = up_proj(*d, b.chunk.latent_ws, LP, m.rows, w_kv_b, b.chunk.kv_ws, b.chunk.kv_dtype, s);
+      if (rc) return rc;
+    }
+    rc = attention(*d, 0, R, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.chunk.kv_ws,
+                   b.chunk.kv_dtype, b.chunk.latent_ws, LP, nullptr, b.o_chunk, b.lse_chunk, s);
+    if (rc) return rc;
+    if (p.has_empty[c]) {
+      rc = launch_mask_empty_context(b.lse_chunk, b.o_chunk, MLA_DTYPE_F32, T, H, Dv, R, ql, cu,
+                                     s);
+      if (rc) return rc;
+    }
+    rc = launch_merge(b.o_run[(c + 1) & 1], b.lse_run[(c + 1) & 1], b.o_run[c & 1],
+                      b.lse_run[c & 1], b.o_chunk, b.lse_chunk, T, H, Dv, T, MLA_DTYPE_F32,
+                      MLA_DTYPE_F32, s);
+    if (rc) return rc;
+  }
+  rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, b.chunk.kv_dtype, s);
+  if (rc) return rc;
+  const int32_t *sq = b.meta + p.suffix_off;
+  rc = attention(*d, 1, R, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
+                 b.chunk.kv_dtype, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+  if (rc) return rc;
+  const int fin = p.n_chunks & 1;  // the buffer the last chunk merged into
+  return launch_merge(out, out_lse, b.o_run[fin], b.lse_run[fin], b.o_suf, b.lse_suf, T, H, Dv,
+                      p.pnt, MLA_DTYPE_F32, d->dtype, s);
+}

@@ -14,22 +14,31 @@
 // workspace kv [rows, H*256] (head h at columns h*256 + [0,128) / [128,256));
 // k_pe is the latent row's tail, latent[row][512:576], shared by all heads.
 //
-// One CTA = one (sequence, 128-query tile, head).  Warp-specialised:
-//   warp 0     TMA producer: the 128x192 Q tile once, then per 128-key tile
-//              K = [K_nope (2 boxes) | k_pe (1 box)] and V (2 boxes), into
-//              double-buffered slots, 128-byte swizzle.
+// One CTA = one (sequence, 128-query tile, head); keys in 128-key tiles.
+// Two softmax warpgroups share every S tile: A takes its keys 0-63, B keys
+// 64-127, each with its own running max and sum and its own O accumulator
+// (a split of the key set, merged by LSE in the epilogue).  Each thread thus
+// exponentiates half a row per tile and two warps share each SM sub-partition,
+// so the softmax keeps up with the tensor cores.
+//   warp 0     TMA producer: the 128x192 Q tile once, then per key tile
+//              K = [K_nope (2 boxes) | k_pe (1 box)] and V (2 boxes),
+//              double-buffered, 128-byte swizzle.
 //   warp 1     TMEM owner + MMA issuer: S = Q K^T (M=128, N=128, K=192: 8
-//              fp16 tcgen05.mma for the nope part, 4 bf16 for the rope part,
-//              into a double-buffered S accumulator), and O += P V (M=128,
-//              N=128, K=128: 8 fp16 tcgen05.mma, P read from TMEM, V an
-//              MN-major shared-memory operand).
-//   warps 2-5  softmax, one thread per query row: tcgen05.ld the S row, mask,
-//              online softmax in base 2 with a lazily rescaled running max
-//              (O is rescaled in TMEM only when the max grows by more than
-//              2^8), P as fp16 written back to TMEM with tcgen05.st; at the
-//              end O/l and LSE go to global memory, or are LSE-merged into the
-//              stored partial (accumulate).
-// TMEM: S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512).
+//              fp16 tcgen05.mma for the nope part, 4 bf16 for the rope part)
+//              into a double-buffered S; O_A += P_A V[0:64] and O_B += P_B
+//              V[64:128] (M=128, N=128, K=64: 4 fp16 tcgen05.mma each, P read
+//              from TMEM, V an MN-major shared-memory operand).
+//   warps 2-5  softmax warpgroup A, warps 6-9 warpgroup B: one thread per
+//              query row and half row; tcgen05.ld the half row of S, mask,
+//              online softmax in base 2 with a lazily raised running max (O
+//              is rescaled in TMEM only when the max grows by more than 2^8;
+//              exact, since O/l and LSE use the same max), P as fp16 written
+//              over the warpgroup's own S columns with tcgen05.st.
+//              Epilogue: A writes columns 0-63 of O, B columns 64-127, after
+//              merging the two partials; the result is written or LSE-merged
+//              into the stored partial (accumulate).
+// TMEM: S0 [0,128) S1 [128,256) (P_A over S cols [0,32), P_B over [64,96)),
+//       O_A [256,384) O_B [384,512).
 #include <algorithm>
 #include <vector>
 
@@ -40,16 +49,18 @@ namespace {
 
 using namespace sm103;
 
-constexpr int BQ = 128, BKV = 128;
+constexpr int BQ = 128, BKV = 128, RING = 2, HALF = BKV / 2;
 constexpr int DN = 128, DR = 64, DV = 128, DQK = DN + DR, HD = DN + DV;
-constexpr int BOX_BYTES = 128 * 64 * 2;      // 16 KB: 128 rows x 64 bf16
-constexpr int Q_BYTES = 3 * BOX_BYTES;       // 48 KB
-constexpr int K_BYTES = 3 * BOX_BYTES;       // 48 KB
-constexpr int V_BYTES = 2 * BOX_BYTES;       // 32 KB
-constexpr int SMEM_BYTES = 1024 + Q_BYTES + 2 * K_BYTES + 2 * V_BYTES + 256;
-constexpr int THREADS = 192;
+constexpr int QBOX = 128 * 64 * 2;           // 16 KB: 128 rows x 64 16-bit
+constexpr int KBOX = BKV * 64 * 2;           // 16 KB: 128 rows x 64 16-bit
+constexpr int Q_BYTES = 3 * QBOX;            // 48 KB
+constexpr int K_BYTES = 3 * KBOX;            // 48 KB: K_nope (2 boxes) + k_pe
+constexpr int V_BYTES = 2 * KBOX;            // 32 KB
+constexpr int XCHG_BYTES = 4 * 128 * 4;       // per-row (m, l) of both warpgroups
+constexpr int SMEM_BYTES = 1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + XCHG_BYTES + 256;
+constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
+constexpr uint32_t COL_S = 0, COL_O = 256;
 constexpr int MAX_ITEMS = 2048;
 constexpr float kRescaleThreshold = 8.0f;    // log2 of the tolerated growth
 
@@ -61,13 +72,24 @@ struct AttnParams {
   int2 items[MAX_ITEMS];  // (sequence, query tile), longest first
 };
 
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -80,15 +102,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + Q_BYTES;
-  uint8_t *sV = sK + 2 * K_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sV + 2 * V_BYTES);
-  const uint32_t b_q = smem_u32(bars + 0);
-  const uint32_t b_kfull = smem_u32(bars + 1), b_kempty = smem_u32(bars + 3);
-  const uint32_t b_vfull = smem_u32(bars + 5), b_vempty = smem_u32(bars + 7);
-  const uint32_t b_sfull = smem_u32(bars + 9), b_sfree = smem_u32(bars + 11);
-  const uint32_t b_pfull = smem_u32(bars + 13), b_odone = smem_u32(bars + 14);
-  const uint32_t b_done = smem_u32(bars + 15), b_qready = smem_u32(bars + 16);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+  uint8_t *sV = sK + RING * K_BYTES;
+  float *xchg = reinterpret_cast<float *>(sV + RING * V_BYTES);  // [4][128]: m, l of B then A
+  uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + XCHG_BYTES);
+  // barriers
+  const uint32_t b_q = smem_u32(bars + 0), b_qready = smem_u32(bars + 1);
+  const uint32_t b_kfull = smem_u32(bars + 2), b_kempty = smem_u32(bars + 2 + RING);
+  const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
+  const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);  // [2]: per S buffer
+  const uint32_t b_pfull = b_sfull + 16;                    // [2]: per warpgroup
+  const uint32_t b_odone = b_sfull + 32, b_done = b_sfull + 40;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x / p.n_items;
@@ -102,18 +126,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(b_qready, 4);
+    for (int s = 0; s < RING; ++s) {
       mbar_init(b_kfull + 8 * s, 1);
       mbar_init(b_kempty + 8 * s, 1);
       mbar_init(b_vfull + 8 * s, 1);
       mbar_init(b_vempty + 8 * s, 1);
-      mbar_init(b_sfull + 8 * s, 1);
-      mbar_init(b_sfree + 8 * s, 4);
     }
-    mbar_init(b_pfull, 4);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(b_sfull + 8 * w, 1);
+      mbar_init(b_pfull + 8 * w, 4);
+    }
     mbar_init(b_odone, 1);
     mbar_init(b_done, 1);
-    mbar_init(b_qready, 4);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -131,30 +156,31 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int qrow = q_beg + q0;
       mbar_expect_tx(b_q, Q_BYTES);
       tma_load_2d(smem_u32(sQ), &tm_q, b_q, h * DQK, qrow);
-      tma_load_2d(smem_u32(sQ + BOX_BYTES), &tm_q, b_q, h * DQK + 64, qrow);
-      tma_load_2d(smem_u32(sQ + 2 * BOX_BYTES), &tm_q, b_q, h * DQK + 128, qrow);
-      int k_issued[2] = {-1, -1}, v_issued[2] = {-1, -1};
+      tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, h * DQK + 64, qrow);
+      tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, h * DQK + 128, qrow);
+      int k_issued[RING], v_issued[RING];
+      for (int s = 0; s < RING; ++s) k_issued[s] = v_issued[s] = -1;
       for (int j = 0; j < n_tiles; ++j) {
-        const int s = j & 1;
-        const uint32_t par = uint32_t(((j >> 1) - 1) & 1);  // phase of tile j-2
+        const int s = j % RING;
+        const uint32_t use = uint32_t(j / RING);          // use count of slot s
         const int krow = k_beg + j * BKV;
-        if (j >= 2 && !mbar_wait(b_kempty + 8 * s, par)) break;
+        if (j >= RING && !mbar_wait(b_kempty + 8 * s, (use - 1) & 1)) break;
         uint8_t *k = sK + s * K_BYTES;
         mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
         tma_load_2d(smem_u32(k), &tm_kv, b_kfull + 8 * s, h * HD, krow);
-        tma_load_2d(smem_u32(k + BOX_BYTES), &tm_kv, b_kfull + 8 * s, h * HD + 64, krow);
-        tma_load_2d(smem_u32(k + 2 * BOX_BYTES), &tm_lat, b_kfull + 8 * s, 512, krow);
-        k_issued[s] = (j >> 1) & 1;
-        if (j >= 2 && !mbar_wait(b_vempty + 8 * s, par)) break;
+        tma_load_2d(smem_u32(k + KBOX), &tm_kv, b_kfull + 8 * s, h * HD + 64, krow);
+        tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, b_kfull + 8 * s, 512, krow);
+        k_issued[s] = int(use & 1);
+        if (j >= RING && !mbar_wait(b_vempty + 8 * s, (use - 1) & 1)) break;
         uint8_t *v = sV + s * V_BYTES;
         mbar_expect_tx(b_vfull + 8 * s, V_BYTES);
         tma_load_2d(smem_u32(v), &tm_kv, b_vfull + 8 * s, h * HD + DN, krow);
-        tma_load_2d(smem_u32(v + BOX_BYTES), &tm_kv, b_vfull + 8 * s, h * HD + DN + 64, krow);
-        v_issued[s] = (j >> 1) & 1;
+        tma_load_2d(smem_u32(v + KBOX), &tm_kv, b_vfull + 8 * s, h * HD + DN + 64, krow);
+        v_issued[s] = int(use & 1);
       }
       // every issued load has landed before the CTA may exit
       mbar_wait(b_q, 0);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < RING; ++s) {
         if (k_issued[s] >= 0) mbar_wait(b_kfull + 8 * s, uint32_t(k_issued[s]));
         if (v_issued[s] >= 0) mbar_wait(b_vfull + 8 * s, uint32_t(v_issued[s]));
       }
@@ -167,16 +193,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
       const uint32_t q_addr = smem_u32(sQ);
       bool ok = mbar_wait(b_qready, 0);
+      // S for key tile j into S buffer j & 1.  The buffer held P of tile
+      // j-2, whose P.V MMAs were issued before: the tensor pipe runs them in
+      // order, so they read P before this S overwrites it.
       auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!mbar_wait(b_kfull + 8 * s, uint32_t((j >> 1) & 1))) return false;
-        if (j >= 2 && !mbar_wait(b_sfree + 8 * s, uint32_t(((j >> 1) - 1) & 1))) return false;
+        const int s = j % RING;
+        if (!mbar_wait(b_kfull + 8 * s, uint32_t((j / RING) & 1))) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + s * K_BYTES);
         const uint32_t d = tmem + COL_S + uint32_t(s * BKV);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = uint32_t((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
+          const uint32_t off = uint32_t((kk >> 2) * QBOX + (kk & 3) * 32);
           mma_bf16(d, desc_kmajor_sw128(q_addr + off), desc_kmajor_sw128(k_addr + off),
                    kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
         }
@@ -187,20 +215,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok) ok = issue_s(0);
       if (ok && n_tiles > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(b_pfull, uint32_t(j & 1)) ||
-            !mbar_wait(b_vfull + 8 * s, uint32_t((j >> 1) & 1))) {
+        const int s = j % RING;
+        if (!mbar_wait(b_vfull + 8 * s, uint32_t((j / RING) & 1))) {
           ok = false;
           break;
         }
-        tc_fence_after();
         const uint32_t v_addr = smem_u32(sV + s * V_BYTES);
-        const uint32_t pa = tmem + COL_P + uint32_t(s * 64);
+        for (int w = 0; w < 2 && ok; ++w) {
+          if (!mbar_wait(b_pfull + 8 * w, uint32_t(j & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // warpgroup w's keys are rows [w*64, w*64+64) of the V tile
+          const uint32_t pa = tmem + COL_S + uint32_t(s * BKV + w * HALF);
+          const uint32_t vb = v_addr + uint32_t(w * HALF * 128);
+          const uint32_t od = tmem + COL_O + uint32_t(w * DV);
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_bf16_ts(tmem + COL_O, pa + uint32_t(kk * 8),
-                      desc_mnmajor_sw128(v_addr + uint32_t(kk * 2048), BOX_BYTES), idesc_o,
-                      (j | kk) != 0);
+          for (int kk = 0; kk < HALF / 16; ++kk)
+            mma_f16_ts(od, pa + uint32_t(kk * 8),
+                       desc_mnmajor_sw128(vb + uint32_t(kk * 2048), KBOX), idesc_o,
+                       (j | kk) != 0);
+        }
+        if (!ok) break;
         mma_commit(b_odone);
         mma_commit(b_vempty + 8 * s);
         if (j + 2 < n_tiles) ok = issue_s(j + 2);
@@ -209,70 +246,71 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(b_done, 0);
     }
   } else {
-    // ---------------- softmax: one thread per query row
+    // ---------------- softmax warpgroups
+    const int wg = (warp - 2) >> 2;        // 0: A (even key tiles), 1: B (odd)
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    const int row = quarter * 32 + lane;   // query row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const int qpos = q0 + row;            // position within the sequence
+    const int qpos = q0 + row;             // position within the sequence
     float m_used = neg_inf(), l = 0.f;
     bool ok = true;
-    if (n_tiles > 0) {
-      // q_nope (boxes 0 and 1 of the Q tile) to fp16 in place, to meet the
-      // fp16 K_nope in the S MMA; exact for bf16 values within fp16 range
+    if (n_tiles > 0 && wg == 0) {
+      // q_nope (Q boxes 0 and 1) to fp16 in place, to meet the fp16 K_nope in
+      // the S MMA; exact for bf16 values within fp16 range
       if (!mbar_wait(b_q, 0)) {
         ok = false;
       } else {
         const int tid = threadIdx.x - 64;
         uint4 *qv = reinterpret_cast<uint4 *>(sQ);
 #pragma unroll 4
-        for (int v = 0; v < 2 * BOX_BYTES / 16 / 128; ++v) {
+        for (int v = 0; v < 2 * QBOX / 16 / 128; ++v) {
           uint4 x = qv[v * 128 + tid];
-          uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            w[e] = pack_f16(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
-          qv[v * 128 + tid] = make_uint4(w[0], w[1], w[2], w[3]);
+            w4[e] = pack_f16(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
+          qv[v * 128 + tid] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         fence_async_smem();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
     }
+    const uint32_t o_col = tmem + lane_off + COL_O + uint32_t(wg * DV);
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait(b_sfull + 8 * s, uint32_t((j >> 1) & 1))) {
+      const int s = j % RING;
+      const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(s * BKV + wg * HALF);
+      if (!mbar_wait(b_sfull + 8 * s, uint32_t((j / RING) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float sv[BKV];
+      float sv[HALF];
 #pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
+      for (int c = 0; c < HALF / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + COL_S + uint32_t(s * BKV + c * 32), r);
+        tmem_ld32(s_col + uint32_t(c * 32), r);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(r[e]) * p.scale_log2;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_sfree + 8 * s);
       // mask keys past the sequence (and, causal, past the query)
-      int valid = nk - j * BKV;
-      if (p.causal) valid = min(valid, qpos - j * BKV + 1);
-      if (valid < BKV) {
+      const int k0 = j * BKV + wg * HALF;   // first key of this half tile
+      int valid = nk - k0;
+      if (p.causal) valid = min(valid, qpos - k0 + 1);
+      if (valid < HALF) {
 #pragma unroll
-        for (int e = 0; e < BKV; ++e)
+        for (int e = 0; e < HALF; ++e)
           if (e >= valid) sv[e] = neg_inf();
       }
       float mx = sv[0];
 #pragma unroll
-      for (int e = 1; e < BKV; ++e) mx = fmaxf(mx, sv[e]);
+      for (int e = 1; e < HALF; ++e) mx = fmaxf(mx, sv[e]);
       float alpha = 1.f;
       bool rescale = false;
-      if (mx > m_used + kRescaleThreshold || j == 0) {
+      if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
         const float m_new = fmaxf(mx, m_used);
-        if (j > 0 && m_new != neg_inf()) {
+        if (m_used != neg_inf() && m_new != neg_inf()) {
           alpha = exp2f(m_used - m_new);
           rescale = true;
         }
@@ -280,27 +318,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float base = (m_used == neg_inf()) ? 0.f : m_used;
       l *= alpha;
-      uint32_t pk[BKV / 2];
+      uint32_t pk[HALF / 2];
 #pragma unroll
-      for (int e = 0; e < BKV / 2; ++e) {
+      for (int e = 0; e < HALF / 2; ++e) {
         const float a = exp2f(sv[2 * e] - base), b = exp2f(sv[2 * e + 1] - base);
         l += a + b;
         pk[e] = pack_f16(a, b);
       }
-      // O and this P buffer are free once the previous P.V has finished
+      // P over this warpgroup's own S columns (already read).  The previous
+      // tile's P.V must have finished before O is rescaled; waiting for it on
+      // every tile costs nothing (this tile's P.V runs after it anyway) and
+      // keeps the waits on the done barrier one phase apart.
+      tmem_st32(s_col, pk);
       if (j > 0 && !mbar_wait(b_odone, uint32_t((j - 1) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t pcol = tmem + lane_off + COL_P + uint32_t(s * 64);
-      tmem_st32(pcol, *reinterpret_cast<uint32_t(*)[32]>(pk));
-      tmem_st32(pcol + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int c = 0; c < DV / 32; ++c) {
           uint32_t r[32];
-          const uint32_t oc = tmem + lane_off + COL_O + uint32_t(c * 32);
+          const uint32_t oc = o_col + uint32_t(c * 32);
           tmem_ld32(oc, r);
           tmem_wait_ld();
 #pragma unroll
@@ -311,62 +350,90 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_pfull);
+      if (lane == 0) mbar_arrive(b_pfull + 8 * wg);
     }
-    // ---------------- epilogue
-    const bool store = ok && qpos < nq;
+    // ---------------- epilogue: merge the two warpgroups' partials
     if (ok && n_tiles > 0 && !mbar_wait(b_odone, uint32_t((n_tiles - 1) & 1))) ok = false;
-    tc_fence_after();
+    float *xm = xchg, *xl = xchg + 128;        // warpgroup B's (m, l) per row
+    float *ym = xchg + 256, *yl = xchg + 384;  // warpgroup A's (m, l) per row
+    if (wg == 1) {
+      xm[row] = m_used;
+      xl[row] = l;
+    } else {
+      ym[row] = m_used;
+      yl[row] = l;
+    }
     const int t = q_beg + qpos;
-    const bool accumulate = p.acc != nullptr && __ldg(p.acc + seq) != 0;
-    float lse = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : neg_inf();
-    float w_new = (l > 0.f) ? 1.f / l : 0.f, w_old = 0.f;
     const int64_t li = int64_t(h) * p.T + t;
-    float *orow = p.o + (int64_t(t) * p.H + h) * DV;
+    const bool accumulate = p.acc != nullptr && __ldg(p.acc + seq) != 0;
+    // the stored LSE is read by both warpgroups before either writes it
+    const float old = (accumulate && qpos < nq) ? p.lse[li] : neg_inf();
+    tc_fence_before();
+    // both warpgroups' O are complete after this barrier (each waited for
+    // its own last P.V); all threads take part, the MMA warps too
+    const int okv = __syncthreads_and(ok ? 1 : 0);
+    tc_fence_after();
+    const float mA = ym[row], lA = yl[row], mB = xm[row], lB = xl[row];
+    const float mx = fmaxf(mA, mB);
+    const float fA = (lA > 0.f) ? exp2f(mA - mx) : 0.f;  // scale of each partial
+    const float fB = (lB > 0.f) ? exp2f(mB - mx) : 0.f;
+    const float lsum = lA * fA + lB * fB;
+    const bool store = okv && qpos < nq;
+    float lse = (lsum > 0.f) ? (mx + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
+    float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
+    float *orow = p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);  // this warpgroup's half
     bool write = store;
     if (store && accumulate) {
-      const float old = p.lse[li];
-      if (l == 0.f) {
+      if (lsum == 0.f) {
         write = false;  // nothing new: keep the stored partial
       } else if (!is_neg_inf(old)) {
-        const float mx = fmaxf(old, lse);
-        const float eo = expf(old - mx), en = expf(lse - mx);
+        const float m2 = fmaxf(old, lse);
+        const float eo = expf(old - m2), en = expf(lse - m2);
         w_old = eo / (eo + en);
         w_new *= en / (eo + en);
-        lse = mx + logf(eo + en);
+        lse = m2 + logf(eo + en);
       }
     }
-    if (ok && n_tiles > 0) {
+    if (okv && n_tiles > 0) {
+      // O = (fA O_A + fB O_B) / lsum over this warpgroup's 64 columns
+      const uint32_t oa = tmem + lane_off + COL_O + uint32_t(wg * (DV / 2));
+      const uint32_t ob = oa + uint32_t(DV);
 #pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + COL_O + uint32_t(c * 32), r);
+      for (int c = 0; c < DV / 2 / 16; ++c) {
+        uint32_t ra[16], rb[16];
+        tmem_ld16(oa + uint32_t(c * 16), ra);
+        tmem_ld16(ob + uint32_t(c * 16), rb);
         tmem_wait_ld();
         if (write) {
-          float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+          float4 *dst = reinterpret_cast<float4 *>(orow + c * 16);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float4 v = make_float4(__uint_as_float(r[4 * e]) * w_new,
-                                   __uint_as_float(r[4 * e + 1]) * w_new,
-                                   __uint_as_float(r[4 * e + 2]) * w_new,
-                                   __uint_as_float(r[4 * e + 3]) * w_new);
-            if (w_old != 0.f) {
-              const float4 o = dst[e];
-              v.x += w_old * o.x;
-              v.y += w_old * o.y;
-              v.z += w_old * o.z;
-              v.w += w_old * o.w;
+          for (int e = 0; e < 4; ++e) {
+            float v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a = (fA != 0.f) ? __uint_as_float(ra[4 * e + k]) * fA : 0.f;
+              const float b = (fB != 0.f) ? __uint_as_float(rb[4 * e + k]) * fB : 0.f;
+              v[k] = (a + b) * w_new;
             }
-            dst[e] = v;
+            float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
+            if (w_old != 0.f) {
+              const float4 old = dst[e];
+              o4.x += w_old * old.x;
+              o4.y += w_old * old.y;
+              o4.z += w_old * old.z;
+              o4.w += w_old * old.w;
+            }
+            dst[e] = o4;
           }
         }
       }
     } else if (write && n_tiles == 0 && !accumulate) {
-      for (int c = 0; c < DV; c += 4)
+      for (int c = 0; c < DV / 2; c += 4)
         *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (write && (ok || n_tiles == 0)) p.lse[li] = lse;
+    if (write && wg == 0) p.lse[li] = lse;
   }
+  if (warp < 2) __syncthreads_and(1);  // matches the softmax warps' vote
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -397,9 +464,9 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
   if (!make_tmap_2d_16(&tq, false, q, uint64_t(H) * DQK, uint64_t(T), uint64_t(H) * DQK * 2, 64,
                        128, true) ||
       !make_tmap_2d_16(&tkv, true, kv, uint64_t(H) * HD, uint64_t(rows > 0 ? rows : 1),
-                       uint64_t(H) * HD * 2, 64, 128, true) ||
+                       uint64_t(H) * HD * 2, 64, BKV, true) ||
       !make_tmap_2d_16(&tlat, false, latent, 576, uint64_t(rows > 0 ? rows : 1),
-                       uint64_t(latent_ld) * 2, 64, 128, true))
+                       uint64_t(latent_ld) * 2, 64, BKV, true))
     return MLA_ERR_CUDA;
   // work items: (sequence, query tile), the ones with the most key tiles first
   struct Item {
@@ -424,7 +491,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
       return MLA_ERR_CUDA;
     attr_set = true;
   }
-  static AttnParams prm;  // large; filled per launch batch
+  thread_local AttnParams prm;  // large (16 KB); filled per launch batch
   for (size_t b = 0; b < items.size(); b += MAX_ITEMS) {
     const int n = int(std::min<size_t>(MAX_ITEMS, items.size() - b));
     prm.n_items = n;

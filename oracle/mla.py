@@ -338,3 +338,45 @@ def unchunked_prefill(q, new_latent, cache, block_table, w_kv_b,
     o, l = unchunked_rows(q, new_latent, cache, block_table, w_kv_b,
                           context_lens, query_lens, dims, toks, hs)
     return o.reshape(T, H, dims.v_dim), l.reshape(T, H).T.copy()
+
+
+def equal_window_prefill(q, new_latent, cache, block_table, w_kv_b,
+                         context_lens: Sequence[int], query_lens: Sequence[int],
+                         dims: MlaDims, row_budget: int, split_alignment: int):
+    """The old scheme end to end (PR #49294 report: per chunk, attention over
+    the whole prefill batch's windows, then mask_empty_context on requests
+    whose window is empty, then a merge into the running result; PR #36540
+    report: the final merge with the new-token attention).  Same result as
+    chunked_prefill up to rounding.  Returns (O, LSE, number of chunks)."""
+    L = dims.kv_lora_rank
+    window, starts, seq_lens, _ = _planner.plan_equal_window_chunks(
+        context_lens, row_budget, split_alignment)
+    qsl = _planner.query_start_loc(query_lens)
+    T = qsl[-1]
+    R = len(context_lens)
+    q = np.asarray(q, dtype=np.float64)
+    pO = np.zeros((T, dims.num_heads, dims.v_dim))
+    pL = np.full((dims.num_heads, T), NEG_INF)
+    for c in range(len(starts)):
+        cO = np.full((T, dims.num_heads, dims.v_dim), np.nan)   # rows a backend leaves
+        cL = np.full((dims.num_heads, T), np.nan)
+        for r in range(R):
+            a, b = qsl[r], qsl[r + 1]
+            n = seq_lens[c][r]
+            if a == b or n == 0:
+                continue
+            rows = np.array([context_row(cache, block_table, r, j, dims.block_size)
+                             for j in range(starts[c][r], starts[c][r] + n)],
+                            dtype=np.float64).reshape(n, -1)
+            k_nope, v = up_project(rows, w_kv_b, dims)
+            cO[a:b], cL[:, a:b] = attention_with_lse(q[a:b], k_nope, rows[:, L:], v,
+                                                     dims.softmax_scale)
+        csl = [0]
+        for r in range(R):
+            csl.append(csl[-1] + seq_lens[c][r])
+        cL, cO = mask_empty_context(cL, cO, qsl, csl)
+        pO, pL = merge_attn_states(pO, pL, cO, cL, T)
+    sO, sL = suffix_attention(q, new_latent, w_kv_b, query_lens, dims)
+    pnt = _planner.prefix_num_tokens(context_lens, query_lens)
+    out, out_lse = merge_attn_states(pO, pL, sO, sL, pnt)
+    return out, out_lse, len(starts)

@@ -197,3 +197,39 @@ def empty_token_slices(context_lens: Sequence[int],
         if c == 0 and lo < hi:
             out.append((lo, hi))
     return out
+
+
+# --------------------------------------------------------------------------
+# the old scheme: equal context windows
+# --------------------------------------------------------------------------
+def plan_equal_window_chunks(context_lens: Sequence[int], row_budget: int,
+                             split_alignment: int):
+    """The scheme the per-request packing replaced (PR #50613 report,
+    "motivation": the workspace was divided evenly among the requests with
+    context and every iteration processed the same context window of every
+    request; PR #49294 report, snippet of build_mla_chunked_context_metadata:
+    per chunk a row of starts/ends over the requests, seq_lens =
+    clamp(ends - starts, 0), has_empty_context = any(seq_lens == 0)).
+
+    Reading: window = budget // (requests with context), rounded down to the
+    split alignment; chunk c covers context rows [c*window, (c+1)*window) of
+    every request, clipped to its length.  Returns (window, starts, seq_lens,
+    has_empty_context) with starts / seq_lens as lists of per-request lists.
+    """
+    lens = [int(x) for x in context_lens]
+    with_ctx = sum(1 for c in lens if c > 0)
+    if with_ctx == 0:
+        return 0, [], [], []
+    window = (row_budget // with_ctx) // split_alignment * split_alignment
+    if window <= 0:
+        raise PlannerStuck("budget below one aligned window per request")
+    n_chunks = -(-max(lens) // window)
+    starts, seq_lens, empty = [], [], []
+    for c in range(n_chunks):
+        st = [min(c * window, x) for x in lens]
+        en = [min((c + 1) * window, x) for x in lens]
+        sl = [max(e - s, 0) for s, e in zip(st, en)]
+        starts.append(st)
+        seq_lens.append(sl)
+        empty.append(any(x == 0 for x in sl))
+    return window, starts, seq_lens, empty

@@ -162,3 +162,23 @@ def test_argument_errors_before_any_launch():
                                w.split_alignment, fake, fake, fake, 100, fake, 2, fake, fake,
                                1 << 40, fake, None, None, None)
     assert rc == _lib.MLA_ERR_INVALID
+
+
+def test_c_equal_window_planner_matches_oracle():
+    rng = np.random.default_rng(23)
+    for _ in range(2000):
+        n = int(rng.integers(1, 12))
+        ctx = [int(x) if rng.random() > 0.3 else 0 for x in rng.integers(1, 5000, size=n)]
+        if not any(ctx):
+            assert M.mla_plan_equal_window_chunks(ctx, 4096, 16) == (0, 0)
+            continue
+        align = int(rng.choice([1, 16, 64]))
+        budget = int(rng.integers(align * n, 9000))
+        win, starts, _, _ = P.plan_equal_window_chunks(ctx, budget, align)
+        assert M.mla_plan_equal_window_chunks(ctx, budget, align) == (win, len(starts))
+    w = W.workload("hetero")
+    assert M.mla_plan_equal_window_chunks(w.context_lens, w.row_budget, w.split_alignment) == \
+        (1280, 103)
+    with pytest.raises(M.MlaError) as e:
+        M.mla_plan_equal_window_chunks([5, 5, 5], 2, 1)
+    assert e.value.code == _lib.MLA_ERR_PLANNER_STUCK

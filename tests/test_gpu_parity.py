@@ -443,6 +443,45 @@ def test_chunk_entry_composes_to_prefill():
     assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
 
 
+def _run_equal_window(w, x):
+    g = to_dev(x)
+    T = w.num_tokens
+    out = torch.full((T, w.num_heads, w.v_dim), float("nan"), dtype=w.torch_dtype, device=DEV)
+    out_lse = torch.full((w.num_heads, T), float("nan"), device=DEV)
+    d = M.Dims.of(w)
+    ws = torch.empty(M.mla_prefill_equal_window_workspace_bytes(
+        d, w.context_lens, w.query_lens, w.row_budget, w.split_alignment),
+        dtype=torch.uint8, device=DEV)
+    M.mla_chunked_prefill_equal_window(d, w.context_lens, w.query_lens, w.row_budget,
+                                       w.split_alignment, g["q"], g["new_latent"], g["kv_cache"],
+                                       g["block_table"], g["w_kv_b"], ws, out, out_lse)
+    torch.cuda.synchronize()
+    return out, out_lse
+
+
+@pytest.mark.parametrize("kind", ["tiny", "deepseek"])
+def test_equal_window_comparator_matches_oracle(kind):
+    """The old equal-window scheme (kept as a comparator) gives the oracle's
+    result for that scheme, which equals the per-request packing's."""
+    if kind == "tiny":
+        w = W.scaled(W.workload("tiny"), row_budget=64, max_context_chunk=64)
+    else:
+        w = W.scaled(W.workload("uniform"), context_lens=[0, 300, 1000, 5, 0, 700, 64],
+                     query_lens=[3, 130, 1, 40, 7, 200, 0], num_heads=8, row_budget=1024,
+                     max_context_chunk=1024, split_alignment=64, seed=47)
+    x = W.make_inputs(w)
+    out, lse = _run_equal_window(w, x)
+    n = np_inputs(x)
+    ro, rl, chunks = O.equal_window_prefill(n["q"], n["new_latent"], n["kv_cache"],
+                                            n["block_table"], n["w_kv_b"], w.context_lens,
+                                            w.query_lens, odims(w), w.row_budget,
+                                            w.split_alignment)
+    assert chunks > 1
+    assert not torch.isnan(out).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 # -------------------------------------------- full sizes, sampled outputs --
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["uniform", "hetero", "long"])

@@ -486,3 +486,50 @@ def test_pins_catch_planted_mistakes():
         return plans
     with pytest.raises(AssertionError):
         check_plan_invariants([1020, 10], literal_reading([1020, 10], 1024, 1024, 16), 1024)
+
+
+# ------------------------------------------- the old equal-window scheme --
+def test_equal_window_plan_invariants():
+    rng = np.random.default_rng(16)
+    for _ in range(500):
+        n = int(rng.integers(1, 10))
+        ctx = [int(x) if rng.random() > 0.3 else 0 for x in rng.integers(1, 3000, size=n)]
+        if not any(ctx):
+            continue
+        align = int(rng.choice([1, 16, 64]))
+        budget = int(rng.integers(align * n, 8000))
+        win, starts, lens, empty = P.plan_equal_window_chunks(ctx, budget, align)
+        with_ctx = sum(1 for c in ctx if c > 0)
+        assert win % align == 0 and win * with_ctx <= budget and win > 0
+        assert len(starts) == -(-max(ctx) // win)
+        for c in range(len(starts)):
+            assert sum(lens[c]) <= budget
+            assert empty[c] == any(x == 0 for x in lens[c])
+        for r in range(n):          # every row exactly once, in window order
+            covered = [(starts[c][r], lens[c][r]) for c in range(len(starts)) if lens[c][r]]
+            pos = 0
+            for s, l in covered:
+                assert s == pos
+                pos += l
+            assert pos == ctx[r]
+    w = W.workload("hetero")
+    win, starts, _, _ = P.plan_equal_window_chunks(w.context_lens, w.row_budget,
+                                                   w.split_alignment)
+    assert win == 1280 and len(starts) == 103     # vs 11 chunks of per-request packing
+
+
+def test_equal_window_prefill_equals_chunked():
+    for budget in (128, 64):
+        w = W.scaled(W.workload("tiny"), row_budget=budget, max_context_chunk=budget)
+        x = _np_inputs(w)
+        d = _dims(w)
+        o1, l1, n1 = O.equal_window_prefill(x["q"], x["new_latent"], x["kv_cache"],
+                                            x["block_table"], x["w_kv_b"], w.context_lens,
+                                            w.query_lens, d, w.row_budget, w.split_alignment)
+        o2, l2, _ = O.chunked_prefill(x["q"], x["new_latent"], x["kv_cache"], x["block_table"],
+                                      x["w_kv_b"], w.context_lens, w.query_lens, d, w.row_budget,
+                                      w.max_context_chunk, w.split_alignment)
+        assert n1 > 1
+        np.testing.assert_allclose(o1, o2, atol=1e-11)
+        np.testing.assert_allclose(l1, l2, atol=1e-11)
+        np.testing.assert_allclose(o1, sdpa_full_prefill(x, w), atol=1e-11)
