@@ -181,23 +181,26 @@ int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache,
                             int32_t total_rows, void *latent_ws,
                             int32_t *dev_status, mla_stream_t stream);
 
-/* mla_kv_up_proj: kv[rows, H*(Dn+Dv)] = latent[:, 0:L] . w_kv_b^T
+/* mla_kv_up_proj: kv[h, row, c] = latent[row, 0:L] . w_kv_b[h*(Dn+Dv) + c, :]
  *   latent device [rows, latent_ld] in dtype (latent_ld >= L); w_kv_b in
- *   dtype; kv device, row-major [rows, H*(Dn+Dv)] in kv_dtype (F32, BF16 or
- *   F16; accumulation is float32, the result is rounded once to kv_dtype).
- *   For bf16 inputs with L % 64 == 0, H*(Dn+Dv) % 256 == 0 and a 16-bit
- *   kv_dtype this runs on the tcgen05 tensor-core GEMM.  The chunked path
- *   stores K/V as F16 on the tensor-core path: bf16 keeps 8 significant bits
- *   and its rounding of K_nope alone moves a one-key LSE by ~5e-4 (1 sigma),
- *   fp16 keeps 11. */
+ *   dtype; kv device, HEAD-MAJOR [H, rows, Dn+Dv] in kv_dtype (F32, BF16 or
+ *   F16; accumulation is float32, the result is rounded once to kv_dtype):
+ *   columns [0, Dn) of head h are K_nope, [Dn, Dn+Dv) are V.  Head-major
+ *   keeps every output tile of the GEMM and every key tile of the attention
+ *   one contiguous block of HBM.  For bf16 inputs with L % 64 == 0,
+ *   H*(Dn+Dv) % 256 == 0, (Dn+Dv) % 64 == 0 and a 16-bit kv_dtype this runs
+ *   on the 2-SM tcgen05 GEMM.  The chunked path stores K/V as F16 on the
+ *   tensor-core path: bf16 keeps 8 significant bits and its rounding of
+ *   K_nope alone moves a one-key LSE by ~5e-4 (1 sigma), fp16 keeps 11. */
 int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
                    int32_t rows, const void *w_kv_b, void *kv, int32_t kv_dtype,
                    mla_stream_t stream);
 
 /* mla_varlen_attn: softmax attention per sequence, returning (O, LSE).
  *   Sequence i owns query tokens [q_loc[i], q_loc[i+1]) (rows of q, o, lse)
- *   and key rows [k_loc[i], k_loc[i+1]) of kv (up-projected, [rows,
- *   H*(Dn+Dv)]) and of latent (k_pe = latent[row][L:L+P]).
+ *   and key rows [k_loc[i], k_loc[i+1]) of kv (the head-major up-projection
+ *   output [H, kv_rows, Dn+Dv] of mla_kv_up_proj, kv_rows >= k_loc[num_seqs])
+ *   and of latent (k_pe = latent[row][L:L+P]).
  *   causal = 0: every query sees all of its sequence's keys (context chunk).
  *   causal = 1: keys are the sequence's own new tokens and query i sees keys
  *               0..i (requires equal query and key counts).
@@ -216,7 +219,8 @@ int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
                     const int32_t *q_loc, const int32_t *k_loc,
                     const int32_t *q_loc_host, const int32_t *k_loc_host,
                     int32_t num_tokens, const void *q, const void *kv,
-                    int32_t kv_dtype, const void *latent, int64_t latent_ld,
+                    int32_t kv_dtype, int32_t kv_rows, const void *latent,
+                    int64_t latent_ld,
                     const int32_t *accumulate, float *o, float *lse,
                     mla_stream_t stream);
 

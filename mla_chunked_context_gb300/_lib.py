@@ -77,7 +77,7 @@ def lib() -> C.CDLL:
             "merge_attn_states": [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P],
             "mla_gather_context_rows": [P, P, I32, P, I32, I32, P, P, P, I32, P, P, P],
             "mla_kv_up_proj": [P, P, I64, I32, P, P, I32, P],
-            "mla_varlen_attn": [P, I32, I32, P, P, P, P, I32, P, P, I32, P, I64, P, P, P, P],
+            "mla_varlen_attn": [P, I32, I32, P, P, P, P, I32, P, P, I32, I32, P, I64, P, P, P, P],
             "mla_fill_empty_rows": [P, P, I32, I32, I32, I32, P, P],
             "mla_mask_empty_context": [P, P, I32, I32, I32, I32, I32, P, P, P],
             "mla_chunk_workspace_bytes": [P, I32, I32, P],
@@ -242,9 +242,11 @@ def mla_kv_up_proj(dims: Dims, latent, rows: int, w_kv_b, kv, stream=None) -> No
 
 def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Sequence[int], q,
                     kv, latent, o, lse, accumulate: Optional[Sequence[int]] = None,
-                    stream=None, q_loc_dev=None, k_loc_dev=None, accumulate_dev=None) -> None:
+                    stream=None, q_loc_dev=None, k_loc_dev=None, accumulate_dev=None,
+                    kv_rows: Optional[int] = None) -> None:
     """q_loc / k_loc (and accumulate) are host sequences; they are copied to
-    the device here unless device copies are passed as *_dev tensors."""
+    the device here unless device copies are passed as *_dev tensors.  kv is
+    head-major [H, kv_rows, Dn+Dv]; kv_rows defaults to k_loc[-1]."""
     n = len(q_loc) - 1
     dev = q.device
     ql = q_loc_dev if q_loc_dev is not None else torch.tensor(list(q_loc), dtype=torch.int32,
@@ -255,11 +257,12 @@ def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Seque
     if acc is None and accumulate:
         acc = torch.tensor(list(accumulate), dtype=torch.int32, device=dev)
     d = dims.c()
+    rows = int(k_loc[-1]) if kv_rows is None else int(kv_rows)
     _check(lib().mla_varlen_attn(C.byref(d), int(causal), n, _ptr(ql), _ptr(kl),
                                  _i32_host(q_loc), _i32_host(k_loc), q.shape[0], _ptr(q),
-                                 _ptr(kv), dtype_code(kv.dtype), _ptr(latent), latent.stride(0),
-                                 _ptr(acc), _ptr(o), _ptr(lse), _stream(stream)),
-           "mla_varlen_attn")
+                                 _ptr(kv), dtype_code(kv.dtype), rows, _ptr(latent),
+                                 latent.stride(0), _ptr(acc), _ptr(o), _ptr(lse),
+                                 _stream(stream)), "mla_varlen_attn")
 
 
 def mla_fill_empty_rows(o, lse, slices: Sequence, stream=None) -> None:

@@ -28,9 +28,9 @@ int launch_gather(const void *cache, int num_blocks, int block_size, int row_byt
                   cudaStream_t s);
 bool generic_dims_ok(const mla_dims_t &d);
 int launch_up_proj_simt(int dtype, int kv_dtype, const void *latent, int64_t lda, int rows,
-                        const void *w, void *kv, int N, int K, cudaStream_t s);
+                        const void *w, void *kv, int N, int K, int hd, cudaStream_t s);
 int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
-                     const int32_t *k_loc, int num_q_rows, int T, const void *q,
+                     const int32_t *k_loc, int num_q_rows, int T, int kv_rows, const void *q,
                      const void *kv, int kv_dtype, const void *latent, int64_t latent_ld,
                      const int32_t *accumulate, float *o, float *lse, cudaStream_t s);
 bool tc_gemm_ok(const mla_dims_t &d, int kv_dtype, int64_t lda, const void *latent,
@@ -42,7 +42,7 @@ int gemm_take_errors();
 int attn_take_errors();
 int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                    const int32_t *k_loc, const int32_t *q_loc_host,
-                   const int32_t *k_loc_host, int T, const void *q, const void *kv,
+                   const int32_t *k_loc_host, int T, int kv_rows, const void *q, const void *kv,
                    const void *latent, int64_t latent_ld, const int32_t *accumulate,
                    float *o, float *lse, cudaStream_t s);
 bool tc_available();
@@ -94,21 +94,22 @@ int up_proj(const mla_dims_t &d, const void *latent, int64_t lda, int rows, cons
   if (tc_available() && tc_gemm_ok(d, kv_dtype, lda, latent, w, kv))
     return launch_up_proj_tc(d, kv_dtype, latent, lda, rows, w, kv, s);
   return launch_up_proj_simt(d.dtype, kv_dtype, latent, lda, rows, w, kv, kv_width(d),
-                             d.kv_lora_rank, s);
+                             d.kv_lora_rank, d.qk_nope_dim + d.v_dim, s);
 }
 
 int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
               const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
-              int T, const void *q, const void *kv, int kv_dtype, const void *latent,
-              int64_t latent_ld, const int32_t *acc, float *o, float *lse, cudaStream_t s) {
+              int T, const void *q, const void *kv, int kv_dtype, int kv_rows,
+              const void *latent, int64_t latent_ld, const int32_t *acc, float *o, float *lse,
+              cudaStream_t s) {
   const int nq = q_loc_host[n] - q_loc_host[0];
   if (n == 0 || nq == 0) return MLA_OK;
   if (tc_available() && tc_attn_ok(d, kv_dtype, latent_ld) && aligned16(q) && aligned16(kv) &&
       aligned16(latent))
-    return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, q, kv,
+    return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, kv_rows, q, kv,
                           latent, latent_ld, acc, o, lse, s);
-  return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, q, kv, kv_dtype, latent, latent_ld,
-                          acc, o, lse, s);
+  return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, kv_rows, q, kv, kv_dtype, latent,
+                          latent_ld, acc, o, lse, s);
 }
 
 // Device metadata of one chunk, in this order (n = number of requests):
@@ -164,7 +165,7 @@ int run_chunk(const mla_dims_t &d, const ChunkMetaHost &m, const int32_t *meta_d
   rc = up_proj(d, b.latent_ws, LP, m.rows, w, b.kv_ws, b.kv_dtype, s);
   if (rc) return rc;
   return attention(d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.kv_ws, b.kv_dtype,
-                   b.latent_ws, LP, acc, o, lse, s);
+                   m.rows, b.latent_ws, LP, acc, o, lse, s);
 }
 
 void carve_chunk_buffers(Carve &cv, const mla_dims_t &d, int64_t rows, ChunkBuffers &b) {
@@ -243,9 +244,9 @@ extern "C" int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_
                                const int32_t *q_loc, const int32_t *k_loc,
                                const int32_t *q_loc_host, const int32_t *k_loc_host,
                                int32_t num_tokens, const void *q, const void *kv,
-                               int32_t kv_dtype, const void *latent, int64_t latent_ld,
-                               const int32_t *accumulate, float *o, float *lse,
-                               mla_stream_t stream) {
+                               int32_t kv_dtype, int32_t kv_rows, const void *latent,
+                               int64_t latent_ld, const int32_t *accumulate, float *o,
+                               float *lse, mla_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (num_seqs < 0 || num_tokens < 0 || !valid_kv_dtype(kv_dtype)) return MLA_ERR_INVALID;
@@ -259,8 +260,9 @@ extern "C" int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_
     if (causal && nq != nk) return MLA_ERR_INVALID;
   }
   if (q_loc_host[0] < 0 || q_loc_host[num_seqs] > num_tokens) return MLA_ERR_INVALID;
+  if (k_loc_host[0] < 0 || kv_rows < k_loc_host[num_seqs]) return MLA_ERR_INVALID;
   return attention(*d, causal ? 1 : 0, num_seqs, q_loc, k_loc, q_loc_host, k_loc_host,
-                   num_tokens, q, kv, kv_dtype, latent, latent_ld, accumulate, o, lse,
+                   num_tokens, q, kv, kv_dtype, kv_rows, latent, latent_ld, accumulate, o, lse,
                    static_cast<cudaStream_t>(stream));
 }
 
@@ -494,7 +496,7 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   if (rc) return rc;
   const int32_t *sq = b.meta + p.suffix_off;
   rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 b.chunk.kv_dtype, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+                 b.chunk.kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
   if (rc) return rc;
   return launch_merge(out, out_lse, b.o_part, b.lse_part, b.o_suf, b.lse_suf, T, H, Dv, p.pnt,
                       MLA_DTYPE_F32, d->dtype, s);
@@ -702,7 +704,8 @@ extern "C" int mla_chunked_prefill_equal_window(
       if (rc) return rc;
     }
     rc = attention(*d, 0, R, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.chunk.kv_ws,
-                   b.chunk.kv_dtype, b.chunk.latent_ws, LP, nullptr, b.o_chunk, b.lse_chunk, s);
+                   b.chunk.kv_dtype, m.rows, b.chunk.latent_ws, LP, nullptr, b.o_chunk,
+                   b.lse_chunk, s);
     if (rc) return rc;
     if (p.has_empty[c]) {
       rc = launch_mask_empty_context(b.lse_chunk, b.o_chunk, MLA_DTYPE_F32, T, H, Dv, R, ql, cu,
@@ -718,7 +721,7 @@ extern "C" int mla_chunked_prefill_equal_window(
   if (rc) return rc;
   const int32_t *sq = b.meta + p.suffix_off;
   rc = attention(*d, 1, R, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 b.chunk.kv_dtype, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+                 b.chunk.kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
   if (rc) return rc;
   const int fin = p.n_chunks & 1;  // the buffer the last chunk merged into
   return launch_merge(out, out_lse, b.o_run[fin], b.lse_run[fin], b.o_suf, b.lse_suf, T, H, Dv,

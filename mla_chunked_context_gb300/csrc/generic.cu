@@ -2,8 +2,9 @@
 // (any head dims, float32 or bf16 storage; e.g. a 64-rank latent with 32-wide
 // heads).  Arithmetic is float32 throughout.
 //
-//  * kv_up_proj_simt: kv[rows, N] = latent[rows, 0:L] . w_kv_b[N, L]^T, a
-//    64x64-tile shared-memory GEMM (each thread 4x4 outputs).
+//  * kv_up_proj_simt: kv[h, row, c] = latent[row, 0:L] . w_kv_b[h*hd + c, :],
+//    head-major [H, rows, hd]; a 64x64-tile shared-memory GEMM (each thread
+//    4x4 outputs).
 //  * attn_simt: one warp per (query token, head); online softmax over the
 //    sequence's keys in the base-2 domain, O accumulated in registers spread
 //    over the lanes; result (O, LSE) written or LSE-merged into the partial.
@@ -17,7 +18,7 @@ constexpr int GT = 64, GK = 16;
 template <typename T, typename TO>
 __global__ void __launch_bounds__(256) kv_up_proj_simt(const T *__restrict__ A, int64_t lda,
                                                        const T *__restrict__ B, TO *__restrict__ C,
-                                                       int M, int N, int K) {
+                                                       int M, int N, int K, int hd) {
   __shared__ float As[GK][GT + 1];
   __shared__ float Bs[GK][GT + 1];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -51,7 +52,9 @@ __global__ void __launch_bounds__(256) kv_up_proj_simt(const T *__restrict__ A, 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int gm = m0 + ty + 16 * i, gn = n0 + tx + 16 * j;
-      if (gm < M && gn < N) C[int64_t(gm) * N + gn] = from_f32<TO>(acc[i][j]);
+      // head-major output [N / hd, M, hd]
+      if (gm < M && gn < N)
+        C[(int64_t(gn / hd) * M + gm) * hd + gn % hd] = from_f32<TO>(acc[i][j]);
     }
 }
 
@@ -69,6 +72,7 @@ struct AttnArgs {
   const int32_t *k_loc;
   const int32_t *accumulate;
   int num_seqs, T, H, L, P, Dn, Dv, causal;
+  int kv_rows;       // rows of the head-major kv [H, kv_rows, Dn+Dv]
   float scale_log2;  // softmax_scale * log2(e)
 };
 
@@ -84,7 +88,7 @@ __global__ void __launch_bounds__(128) attn_simt(AttnArgs a) {
   const int kbeg = a.k_loc[i];
   int nk = a.k_loc[i + 1] - kbeg;
   if (a.causal) nk = min(nk, t - a.q_loc[i] + 1);
-  const int QK = a.Dn + a.P, W = a.H * (a.Dn + a.Dv);
+  const int QK = a.Dn + a.P, HDIM = a.Dn + a.Dv;
   const T *q = static_cast<const T *>(a.q) + (int64_t(t) * a.H + h) * QK;
   const TK *kv = static_cast<const TK *>(a.kv);
   const T *lat = static_cast<const T *>(a.latent);
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(128) attn_simt(AttnArgs a) {
   float m = neg_inf(), l = 0.f;
   for (int j = 0; j < nk; ++j) {
     const int64_t row = kbeg + j;
-    const TK *kn = kv + row * W + int64_t(h) * (a.Dn + a.Dv);
+    const TK *kn = kv + (int64_t(h) * a.kv_rows + row) * HDIM;
     const T *kp = lat + row * a.latent_ld + a.L;
     float s = 0.f;
 #pragma unroll
@@ -158,28 +162,28 @@ bool generic_dims_ok(const mla_dims_t &d) {
 
 template <typename T>
 int up_proj_simt_out(int kv_dtype, const T *latent, int64_t lda, int rows, const T *w, void *kv,
-                     int N, int K, dim3 grid, cudaStream_t s) {
+                     int N, int K, int hd, dim3 grid, cudaStream_t s) {
   if (kv_dtype == MLA_DTYPE_F32)
     kv_up_proj_simt<T, float><<<grid, 256, 0, s>>>(latent, lda, w, static_cast<float *>(kv), rows,
-                                                   N, K);
+                                                   N, K, hd);
   else if (kv_dtype == MLA_DTYPE_F16)
     kv_up_proj_simt<T, __half><<<grid, 256, 0, s>>>(latent, lda, w, static_cast<__half *>(kv),
-                                                    rows, N, K);
+                                                    rows, N, K, hd);
   else
     kv_up_proj_simt<T, __nv_bfloat16><<<grid, 256, 0, s>>>(
-        latent, lda, w, static_cast<__nv_bfloat16 *>(kv), rows, N, K);
+        latent, lda, w, static_cast<__nv_bfloat16 *>(kv), rows, N, K, hd);
   return launch_status();
 }
 
 int launch_up_proj_simt(int dtype, int kv_dtype, const void *latent, int64_t lda, int rows,
-                        const void *w, void *kv, int N, int K, cudaStream_t s) {
+                        const void *w, void *kv, int N, int K, int hd, cudaStream_t s) {
   if (rows == 0) return MLA_OK;
   dim3 grid((N + GT - 1) / GT, (rows + GT - 1) / GT);
   if (dtype == MLA_DTYPE_BF16)
     return up_proj_simt_out(kv_dtype, static_cast<const __nv_bfloat16 *>(latent), lda, rows,
-                            static_cast<const __nv_bfloat16 *>(w), kv, N, K, grid, s);
+                            static_cast<const __nv_bfloat16 *>(w), kv, N, K, hd, grid, s);
   return up_proj_simt_out(kv_dtype, static_cast<const float *>(latent), lda, rows,
-                          static_cast<const float *>(w), kv, N, K, grid, s);
+                          static_cast<const float *>(w), kv, N, K, hd, grid, s);
 }
 
 template <typename T>
@@ -193,13 +197,13 @@ void attn_simt_kv(int kv_dtype, int blocks, const AttnArgs &a, cudaStream_t s) {
 }
 
 int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
-                     const int32_t *k_loc, int num_q_rows, int T, const void *q,
+                     const int32_t *k_loc, int num_q_rows, int T, int kv_rows, const void *q,
                      const void *kv, int kv_dtype, const void *latent, int64_t latent_ld,
                      const int32_t *accumulate, float *o, float *lse, cudaStream_t s) {
   if (num_q_rows == 0 || num_seqs == 0) return MLA_OK;
   AttnArgs a{q, kv, latent, latent_ld, o, lse, q_loc, k_loc, accumulate, num_seqs, T,
              d.num_heads, d.kv_lora_rank, d.qk_rope_dim, d.qk_nope_dim, d.v_dim, causal,
-             d.softmax_scale * 1.4426950408889634f};
+             kv_rows, d.softmax_scale * 1.4426950408889634f};
   const int64_t warps = int64_t(num_q_rows) * d.num_heads;
   const int blocks = int((warps * 32 + 127) / 128);
   if (d.dtype == MLA_DTYPE_BF16)

@@ -11,7 +11,7 @@
 //   O   = sum_j softmax(s)_j V[j, h];   LSE = ln sum_j exp(s_j)
 // Context chunks see every key of their sequence; the causal (new-token)
 // mode lets query p see keys 0..p.  K_nope and V come from the up-projected
-// workspace kv [rows, H*256] (head h at columns h*256 + [0,128) / [128,256));
+// head-major workspace kv [H, rows, 256] (columns [0,128) / [128,256));
 // k_pe is the latent row's tail, latent[row][512:576], shared by all heads.
 //
 // One CTA = one (sequence, 128-query tile, head); keys in 128-key tiles.
@@ -167,15 +167,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (j >= RING && !mbar_wait(b_kempty + 8 * s, (use - 1) & 1)) break;
         uint8_t *k = sK + s * K_BYTES;
         mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
-        tma_load_2d(smem_u32(k), &tm_kv, b_kfull + 8 * s, h * HD, krow);
-        tma_load_2d(smem_u32(k + KBOX), &tm_kv, b_kfull + 8 * s, h * HD + 64, krow);
+        tma_load_3d(smem_u32(k), &tm_kv, b_kfull + 8 * s, 0, krow, h);
+        tma_load_3d(smem_u32(k + KBOX), &tm_kv, b_kfull + 8 * s, 64, krow, h);
         tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, b_kfull + 8 * s, 512, krow);
         k_issued[s] = int(use & 1);
         if (j >= RING && !mbar_wait(b_vempty + 8 * s, (use - 1) & 1)) break;
         uint8_t *v = sV + s * V_BYTES;
         mbar_expect_tx(b_vfull + 8 * s, V_BYTES);
-        tma_load_2d(smem_u32(v), &tm_kv, b_vfull + 8 * s, h * HD + DN, krow);
-        tma_load_2d(smem_u32(v + KBOX), &tm_kv, b_vfull + 8 * s, h * HD + DN + 64, krow);
+        tma_load_3d(smem_u32(v), &tm_kv, b_vfull + 8 * s, DN, krow, h);
+        tma_load_3d(smem_u32(v + KBOX), &tm_kv, b_vfull + 8 * s, DN + 64, krow, h);
         v_issued[s] = int(use & 1);
       }
       // every issued load has landed before the CTA may exit
@@ -454,7 +454,8 @@ bool tc_attn_ok(const mla_dims_t &d, int kv_dtype, int64_t latent_ld) {
 
 int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                    const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
-                   int T, const void *q, const void *kv, const void *latent, int64_t latent_ld,
+                   int T, int kv_rows, const void *q, const void *kv, const void *latent,
+                   int64_t latent_ld,
                    const int32_t *accumulate, float *o, float *lse, cudaStream_t s) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
@@ -463,8 +464,9 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
   CUtensorMap tq, tkv, tlat;
   if (!make_tmap_2d_16(&tq, false, q, uint64_t(H) * DQK, uint64_t(T), uint64_t(H) * DQK * 2, 64,
                        128, true) ||
-      !make_tmap_2d_16(&tkv, true, kv, uint64_t(H) * HD, uint64_t(rows > 0 ? rows : 1),
-                       uint64_t(H) * HD * 2, 64, BKV, true) ||
+      !make_tmap_3d_16(&tkv, true, kv, HD, uint64_t(kv_rows > 0 ? kv_rows : 1), uint64_t(H),
+                       uint64_t(HD) * 2, uint64_t(kv_rows > 0 ? kv_rows : 1) * HD * 2, 64, BKV,
+                       true) ||
       !make_tmap_2d_16(&tlat, false, latent, 576, uint64_t(rows > 0 ? rows : 1),
                        uint64_t(latent_ld) * 2, 64, BKV, true))
     return MLA_ERR_CUDA;

@@ -1,7 +1,11 @@
 // W_kv_b up-projection on the 5th-generation tensor cores (sm_103a):
-//   kv[M, N] = latent[M, 0:K] . w_kv_b[N, K]^T      (bf16 in, f32 accumulate,
-//                                                    fp16/bf16 out)
+//   kv[h, m, c] = sum_k latent[m, k] w_kv_b[h*(Dn+Dv) + c, k]
+//   (bf16 in, f32 accumulate, fp16/bf16 out; head-major output [H, M, Dn+Dv])
 // M = context rows of a chunk (or new tokens), K = kv_lora_rank, N = H*(Dn+Dv).
+// Head-major output makes each 128x256 output tile one contiguous 64 KB block
+// (row-major [M, N] put its 128 rows 64 KB apart, and the TMA stores of that
+// pattern ran at 2.7 TB/s and held the kernel to 70% of the tensor peak it
+// reaches without them).
 // The MLA up-projection is not on the pages; it is the standard MLA prefill
 // step that turns the gathered latent rows into per-head K_nope and V.
 //
@@ -49,6 +53,7 @@ constexpr uint32_t TMEM_COLS = 512;
 struct GemmArgs {
   int M, N, K;
   int num_pm, num_n;  // pair tiles along M, tiles along N
+  int hd;             // output columns per head (Dn + Dv): the output is [N/hd, M, hd]
 };
 
 template <bool kF16Out>
@@ -221,7 +226,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tm_c, smem_u32(stg + buf * STG_BYTES), n0 + j * 64, m0 + quarter * 32);
+          const int n = n0 + j * 64;  // head-major output: (column in head, row, head)
+          tma_store_3d(&tm_c, smem_u32(stg + buf * STG_BYTES), n % g.hd, m0 + quarter * 32,
+                       n / g.hd);
           bulk_commit();
         }
         buf ^= 1;
@@ -262,6 +269,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 }  // namespace sm103
 
+bool make_tmap_3d_16(CUtensorMap *map, bool fp16, const void *base, uint64_t dim0, uint64_t dim1,
+                     uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                     uint32_t box1, bool swizzle128) {
+  auto fn = sm103::encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_2d_16(CUtensorMap *map, bool fp16, const void *base, uint64_t dim0, uint64_t dim1,
                      uint64_t row_stride_bytes, uint32_t box0, uint32_t box1, bool swizzle128) {
   auto fn = sm103::encode_fn();
@@ -288,25 +312,28 @@ bool tc_available() {
 
 bool tc_gemm_ok(const mla_dims_t &d, int kv_dtype, int64_t lda, const void *latent,
                 const void *w, const void *kv) {
-  const int N = d.num_heads * (d.qk_nope_dim + d.v_dim);
+  const int hd = d.qk_nope_dim + d.v_dim;
+  const int N = d.num_heads * hd;
   auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   return d.dtype == MLA_DTYPE_BF16 && (kv_dtype == MLA_DTYPE_F16 || kv_dtype == MLA_DTYPE_BF16) &&
-         d.kv_lora_rank % sm103::BK == 0 && N % sm103::BN == 0 && (lda * 2) % 16 == 0 &&
-         al16(latent) && al16(w) && al16(kv);
+         d.kv_lora_rank % sm103::BK == 0 && N % sm103::BN == 0 && hd % 64 == 0 &&
+         (lda * 2) % 16 == 0 && al16(latent) && al16(w) && al16(kv);
 }
 
 int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int64_t lda,
                       int rows, const void *w, void *kv, cudaStream_t s) {
   using namespace sm103;
   const int K = d.kv_lora_rank;
-  const int N = d.num_heads * (d.qk_nope_dim + d.v_dim);
+  const int hd = d.qk_nope_dim + d.v_dim;
+  const int N = d.num_heads * hd;
   CUtensorMap ta, tb, tc;
   const bool f16 = kv_dtype == MLA_DTYPE_F16;
   if (!make_tmap_2d_16(&ta, false, latent, K, rows, uint64_t(lda) * 2, BK, BM, true) ||
       !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN / 2, true) ||
-      !make_tmap_2d_16(&tc, f16, kv, N, rows, uint64_t(N) * 2, 64, 32, true))
+      !make_tmap_3d_16(&tc, f16, kv, hd, rows, d.num_heads, uint64_t(hd) * 2,
+                       uint64_t(rows) * hd * 2, 64, 32, true))
     return MLA_ERR_CUDA;
-  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN};
+  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, hd};
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(up_proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

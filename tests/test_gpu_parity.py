@@ -257,8 +257,8 @@ def test_up_proj_deepseek(rows, heads, kv_dtype):
     M.mla_kv_up_proj(M.Dims.of(w), lat.to(DEV), rows, wkv.to(DEV), kv)
     torch.cuda.synchronize()
     kn, v = O.up_project(f64(lat), f64(wkv), odims(w))
-    ref = np.concatenate([kn, v], axis=2).reshape(rows, heads * 256)
-    assert_close(f64(kv), ref, *UP_TOL[kv_dtype], what="kv")
+    ref = np.concatenate([kn, v], axis=2).transpose(1, 0, 2)   # head-major [H, rows, 256]
+    assert_close(f64(kv).reshape(heads, rows, 256), ref, *UP_TOL[kv_dtype], what="kv")
 
 
 def test_up_proj_fp32_tiny():
@@ -269,8 +269,9 @@ def test_up_proj_fp32_tiny():
     M.mla_kv_up_proj(M.Dims.of(w), lat.to(DEV), lat.shape[0], x["w_kv_b"].to(DEV), kv)
     torch.cuda.synchronize()
     kn, v = O.up_project(f64(lat), f64(x["w_kv_b"]), odims(w))
-    ref = np.concatenate([kn, v], axis=2).reshape(lat.shape[0], -1)
-    assert_close(f64(kv), ref, 1e-5, 1e-5, what="kv fp32")
+    ref = np.concatenate([kn, v], axis=2).transpose(1, 0, 2)
+    assert_close(f64(kv).reshape(w.num_heads, lat.shape[0], 64), ref, 1e-5, 1e-5,
+                 what="kv fp32")
 
 
 # -------------------------------------------------------------- attention --
@@ -278,7 +279,8 @@ def _attn_inputs(w, n_rows, T, seed, kv_dtype=None):
     gen = torch.Generator().manual_seed(seed)
     H = w.num_heads
     q = torch.randn(T, H, w.qk_dim, generator=gen).to(w.torch_dtype)
-    kv = (0.45 * torch.randn(n_rows, H * (w.qk_nope_dim + w.v_dim), generator=gen)).to(
+    # head-major [H, rows, Dn+Dv], as mla_kv_up_proj writes it
+    kv = (0.45 * torch.randn(H, n_rows, w.qk_nope_dim + w.v_dim, generator=gen)).to(
         kv_dtype or w.torch_dtype)
     lat = torch.randn(n_rows, w.latent_dim, generator=gen).to(w.torch_dtype)
     return q, kv, lat
@@ -287,7 +289,7 @@ def _attn_inputs(w, n_rows, T, seed, kv_dtype=None):
 def _oracle_attn(w, q, kv, lat, q_loc, k_loc, causal):
     H, Dn, Dv, L = w.num_heads, w.qk_nope_dim, w.v_dim, w.kv_lora_rank
     T = q.shape[0]
-    kvr = f64(kv).reshape(kv.shape[0], H, Dn + Dv)
+    kvr = f64(kv).transpose(1, 0, 2)            # [rows, H, Dn+Dv]
     o = np.full((T, H, Dv), np.nan)
     lse = np.full((H, T), np.nan)
     for i in range(len(q_loc) - 1):
@@ -347,11 +349,12 @@ def test_varlen_attention_accumulate():
     lse = torch.full((2, q_loc[-1]), float("nan"), device=DEV)
     d = M.Dims.of(w)
     gq, gkv, glat = q.to(DEV), kv.to(DEV), lat.to(DEV)
-    M.mla_varlen_attn(d, False, q_loc, loc1, gq, gkv, glat, o, lse)
-    M.mla_varlen_attn(d, False, q_loc, loc2, gq, gkv, glat, o, lse, accumulate=[1, 1])
+    M.mla_varlen_attn(d, False, q_loc, loc1, gq, gkv, glat, o, lse, kv_rows=551)
+    M.mla_varlen_attn(d, False, q_loc, loc2, gq, gkv, glat, o, lse, accumulate=[1, 1],
+                      kv_rows=551)
     torch.cuda.synchronize()
     idx = [np.r_[0:100, 360:420], np.r_[100:360, 420:551]]
-    kvr = f64(kv).reshape(kv.shape[0], 2, 256)
+    kvr = f64(kv).transpose(1, 0, 2)
     for i in range(2):
         a, b = q_loc[i], q_loc[i + 1]
         ro, rl = O.attention_with_lse(f64(q[a:b]), kvr[idx[i], :, :128], f64(lat[idx[i], 512:]),
