@@ -25,8 +25,8 @@
 //               commits stage and accumulator barriers to both CTAs.
 //   warps 2-5   (both CTAs) epilogue of the CTA's own 128 rows: tcgen05.ld
 //               32 lanes x 32 columns, round to fp16 (or bf16), swizzled 32x64
-//               staging tile, TMA store; then release the accumulator on the
-//               even CTA's barrier.
+//               staging tile, coalesced 16-byte stores; then release the
+//               accumulator on the even CTA's barrier.
 // Pair tiles are visited m-major with n fastest, so a 256-row slice of the
 // latent and the whole weight stay in L2 while the pairs sweep them.
 #include <cstdio>
@@ -54,13 +54,13 @@ struct GemmArgs {
   int M, N, K;
   int num_pm, num_n;  // pair tiles along M, tiles along N
   int hd;             // output columns per head (Dn + Dv): the output is [N/hd, M, hd]
+  uint16_t *out;      // fp16 / bf16 bits
 };
 
 template <bool kF16Out>
 __global__ void __launch_bounds__(THREADS, 1)
     up_proj_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
-                      const __grid_constant__ CUtensorMap tm_b,
-                      const __grid_constant__ CUtensorMap tm_c, GemmArgs g) {
+                      const __grid_constant__ CUtensorMap tm_b, GemmArgs g) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -97,7 +97,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_mbar_init();
     prefetch_map(&tm_a);
     prefetch_map(&tm_b);
-    prefetch_map(&tm_c);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
@@ -184,12 +183,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     mma_commit_pair_mc(done_bar, uint16_t(0x1));
     mbar_wait(done_bar, 0);
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM -> 16-bit -> smem -> TMA store
+    // ---------------- epilogue: TMEM -> 16-bit -> swizzled smem -> coalesced stores
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     uint8_t *stg = sStage + (warp - 2) * 2 * STG_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
-    int buf = 0;
     for (int t = first; t < num_tiles; t += step) {
       const int m0 = (t / g.num_n) * PAIR_M + int(rank) * BM, n0 = (t % g.num_n) * BN;
       if (!mbar_wait(accf0 + 8 * acc, acc_phase)) break;
@@ -201,11 +199,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(t_row + j * 64, lo);
         tmem_ld32(t_row + j * 64 + 32, hi);
         tmem_wait_ld();
-        // the staging buffer is reused every other chunk: its previous TMA
-        // store must have finished reading it
-        if (lane == 0) bulk_wait_read<1>();
-        __syncwarp();
-        uint8_t *row = stg + buf * STG_BYTES + lane * 128;
+        // lane = row: its 64 values as 8 16-byte pieces, XOR-swizzled so the
+        // writes and the reads below are free of bank conflicts
+        uint8_t *row = stg + lane * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t *src = (c < 4) ? lo + 8 * c : hi + 8 * (c - 4);
@@ -223,15 +219,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           *reinterpret_cast<uint4 *>(row + ((c ^ (lane & 7)) << 4)) = v;
         }
-        fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          const int n = n0 + j * 64;  // head-major output: (column in head, row, head)
-          tma_store_3d(&tm_c, smem_u32(stg + buf * STG_BYTES), n % g.hd, m0 + quarter * 32,
-                       n / g.hd);
-          bulk_commit();
+        // write back 4 rows x 128 B per instruction: in the head-major output
+        // the warp's 32 rows are consecutive 2*hd-byte rows, so every store
+        // instruction covers four full 128-byte lines.  The stores go through
+        // the LSU; the TMA unit stays free for the operand loads (TMA stores
+        // here held the kernel to 70% of the tensor peak it reaches without
+        // them).
+        const int n = n0 + j * 64, head = n / g.hd, col = n % g.hd;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3), ch = lane & 7;
+          const int grow = m0 + quarter * 32 + r;
+          const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 128 + ((ch ^ (r & 7)) << 4));
+          if (grow < g.M)
+            __stcs(reinterpret_cast<uint4 *>(g.out + (int64_t(head) * g.M + grow) * g.hd + col +
+                                             ch * 8),
+                   v);
         }
-        buf ^= 1;
+        __syncwarp();  // the staging tile is rewritten by the next chunk
       }
       tc_fence_before();
       __syncwarp();
@@ -241,7 +247,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         acc_phase ^= 1;
       }
     }
-    if (lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -326,14 +331,12 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
   const int K = d.kv_lora_rank;
   const int hd = d.qk_nope_dim + d.v_dim;
   const int N = d.num_heads * hd;
-  CUtensorMap ta, tb, tc;
+  CUtensorMap ta, tb;
   const bool f16 = kv_dtype == MLA_DTYPE_F16;
   if (!make_tmap_2d_16(&ta, false, latent, K, rows, uint64_t(lda) * 2, BK, BM, true) ||
-      !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN / 2, true) ||
-      !make_tmap_3d_16(&tc, f16, kv, hd, rows, d.num_heads, uint64_t(hd) * 2,
-                       uint64_t(rows) * hd * 2, 64, 32, true))
+      !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN / 2, true))
     return MLA_ERR_CUDA;
-  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, hd};
+  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, hd, static_cast<uint16_t *>(kv)};
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(up_proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -367,8 +370,8 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
   }
   const int clusters = pair_tiles < max_clusters ? pair_tiles : max_clusters;
   cfg.gridDim = dim3(2 * clusters);
-  const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<true>, ta, tb, tc, g)
-                            : cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<false>, ta, tb, tc, g);
+  const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<true>, ta, tb, g)
+                            : cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<false>, ta, tb, g);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return launch_status();
 }
