@@ -409,7 +409,13 @@ def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
         res[k]["ms"] /= reps
         res[k]["launches"] //= reps
     empty = any(c == 0 and qsl[r] < pnt for r, c in enumerate(w.context_lens))
-    res["launches_per_step"] = 3 * len(plans) + 3 + (1 if empty else 0)
+    # mla_chunked_prefill: fill of context-free rows, 3 per chunk, new-token
+    # up-projection and attention, and a separate merge unless the tensor-core
+    # attention merges in its epilogue
+    fused = M.mla_has_tcgen05() and w.dtype == "bf16" and (w.kv_lora_rank, w.qk_rope_dim,
+                                                           w.qk_nope_dim, w.v_dim) == (512, 64,
+                                                                                       128, 128)
+    res["launches_per_step"] = (1 if empty else 0) + 3 * len(plans) + 2 + (0 if fused else 1)
     return res
 
 

@@ -381,6 +381,16 @@ int mla_chunked_prefill_equal_window(
  * library. */
 int mla_has_tcgen05(void);
 
+/* Failure-detection self test: launches one thread that waits on an
+ * mbarrier nothing arrives on, with the same bounded wait the tensor-core
+ * kernels use but a limit of limit_us microseconds (1 .. 10^6).  The wait
+ * gives up, sets MLA_DEVICE_ERR_WAIT_TIMEOUT (read with
+ * mla_device_error_flags) and writes 1 to gave_up (device int32); the kernel
+ * returns normally and the context stays usable.  MLA_ERR_UNSUPPORTED off
+ * sm_103a. */
+int mla_selftest_bounded_wait(int32_t limit_us, int32_t *gave_up,
+                              mla_stream_t stream);
+
 /* Reads and clears the device-side error bits of the tensor-core kernels
  * (MLA_DEVICE_ERR_*; nonzero means a kernel gave up waiting on one of its
  * own barriers and its output is not valid).  Synchronises the device. */

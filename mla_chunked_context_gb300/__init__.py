@@ -13,7 +13,8 @@ from ._lib import (Chunk, Dims, MlaError, lib, merge_attn_states, mla_chunk_kv_d
                    mla_gather_context_rows, mla_has_tcgen05, mla_kv_up_proj,
                    mla_mask_empty_context, mla_plan_context_chunks, mla_prefill_workspace_bytes,
                    mla_varlen_attn, MLA_STATUS_BAD_BLOCK, mla_plan_equal_window_chunks,
-                   mla_prefill_equal_window_workspace_bytes, mla_chunked_prefill_equal_window)
+                   mla_prefill_equal_window_workspace_bytes, mla_chunked_prefill_equal_window,
+                   mla_selftest_bounded_wait)
 
 __all__ = ["Chunk", "Dims", "MlaError", "lib", "merge_attn_states", "mla_chunk_kv_dtype",
            "mla_chunk_workspace_bytes", "mla_device_error_flags",
@@ -23,7 +24,7 @@ __all__ = ["Chunk", "Dims", "MlaError", "lib", "merge_attn_states", "mla_chunk_k
            "mla_mask_empty_context", "mla_plan_context_chunks", "mla_prefill_workspace_bytes",
            "mla_varlen_attn", "MLA_STATUS_BAD_BLOCK", "mla_plan_equal_window_chunks",
            "mla_prefill_equal_window_workspace_bytes", "mla_chunked_prefill_equal_window",
-           "ChunkedPrefill"]
+           "mla_selftest_bounded_wait", "ChunkedPrefill"]
 
 
 class ChunkedPrefill:

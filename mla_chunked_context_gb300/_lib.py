@@ -35,7 +35,7 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_chunked_prefill", "mla_has_tcgen05", "mla_device_error_flags",
             "mla_chunk_kv_dtype", "mla_context_chunk_attn_noalloc",
             "mla_plan_equal_window_chunks", "mla_prefill_equal_window_workspace_bytes",
-            "mla_chunked_prefill_equal_window")
+            "mla_chunked_prefill_equal_window", "mla_selftest_bounded_wait")
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -92,6 +92,7 @@ def lib() -> C.CDLL:
             "mla_context_chunk_attn_noalloc": [P, P, P, P, P, I32, P, P, I32, P, I32, P, P, P,
                                                P, P],
             "mla_plan_equal_window_chunks": [P, I32, I32, I32, P, P],
+            "mla_selftest_bounded_wait": [I32, P, P],
             "mla_prefill_equal_window_workspace_bytes": [P, P, P, I32, I32, I32, P],
             "mla_chunked_prefill_equal_window": [P, P, P, I32, I32, I32, P, P, P, I32, P, I32, P,
                                                  P, SZ, P, P, P, P],
@@ -392,3 +393,9 @@ def mla_chunked_prefill_equal_window(dims: Dims, context_lens, query_lens, row_b
         kv_cache.shape[0], _ptr(block_table), block_table.shape[1], _ptr(w_kv_b),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(out_lse),
         _ptr(dev_status), _stream(stream)), "mla_chunked_prefill_equal_window")
+
+
+def mla_selftest_bounded_wait(limit_us: int, gave_up, stream=None) -> None:
+    """Run the bounded-wait self test (gave_up: device int32 tensor)."""
+    _check(lib().mla_selftest_bounded_wait(int(limit_us), _ptr(gave_up), _stream(stream)),
+           "mla_selftest_bounded_wait")

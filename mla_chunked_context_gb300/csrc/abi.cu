@@ -40,11 +40,13 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
 bool tc_attn_ok(const mla_dims_t &d, int kv_dtype, int64_t latent_ld);
 int gemm_take_errors();
 int attn_take_errors();
+int launch_bounded_wait_selftest(long long limit_cycles, int32_t *gave_up, cudaStream_t s);
 int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                    const int32_t *k_loc, const int32_t *q_loc_host,
                    const int32_t *k_loc_host, int T, int kv_rows, const void *q, const void *kv,
                    const void *latent, int64_t latent_ld, const int32_t *accumulate,
-                   float *o, float *lse, cudaStream_t s);
+                   float *o, float *lse, void *final_out, float *final_lse, int final_dtype,
+                   int pnt, cudaStream_t s);
 bool tc_available();
 
 namespace {
@@ -107,7 +109,7 @@ int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
   if (tc_available() && tc_attn_ok(d, kv_dtype, latent_ld) && aligned16(q) && aligned16(kv) &&
       aligned16(latent))
     return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, kv_rows, q, kv,
-                          latent, latent_ld, acc, o, lse, s);
+                          latent, latent_ld, acc, o, lse, nullptr, nullptr, 0, 0, s);
   return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, kv_rows, q, kv, kv_dtype, latent,
                           latent_ld, acc, o, lse, s);
 }
@@ -495,6 +497,14 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, b.chunk.kv_dtype, s);
   if (rc) return rc;
   const int32_t *sq = b.meta + p.suffix_off;
+  if (tc_available() && tc_attn_ok(*d, b.chunk.kv_dtype, LP) && aligned16(q) &&
+      aligned16(b.kv_suffix) && aligned16(new_latent)) {
+    // new-token attention with the final merge in its epilogue (row f3): the
+    // context partial is read where needed, the output written once
+    return launch_attn_tc(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, T, q,
+                          b.kv_suffix, new_latent, LP, nullptr, b.o_part, b.lse_part, out,
+                          out_lse, d->dtype, p.pnt, s);
+  }
   rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
                  b.chunk.kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
   if (rc) return rc;
@@ -503,6 +513,18 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
 }
 
 extern "C" int mla_has_tcgen05(void) { return tc_available() ? 1 : 0; }
+
+extern "C" int mla_selftest_bounded_wait(int32_t limit_us, int32_t *gave_up,
+                                         mla_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000 || !gave_up) return MLA_ERR_INVALID;
+  if (!tc_available()) return MLA_ERR_UNSUPPORTED;
+  int dev = 0, khz = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+  if (khz <= 0) khz = 2000000;
+  return launch_bounded_wait_selftest(static_cast<long long>(limit_us) * khz / 1000, gave_up,
+                                      static_cast<cudaStream_t>(stream));
+}
 
 extern "C" int mla_device_error_flags(int32_t *flags) {
   if (!flags) return MLA_ERR_INVALID;

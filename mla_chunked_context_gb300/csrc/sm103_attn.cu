@@ -69,6 +69,12 @@ struct AttnParams {
   float scale_log2;
   const int32_t *q_loc, *k_loc, *acc;
   float *o, *lse;
+  // final-merge mode (fout != nullptr): (o, lse) hold the context partial,
+  // read only; tokens below pnt are LSE-merged with it, the result goes to
+  // fout (bf16 if fout_bf16, else f32) and flse (nullable)
+  void *fout;
+  float *flse;
+  int pnt, fout_bf16;
   int2 items[MAX_ITEMS];  // (sequence, query tile), longest first
 };
 
@@ -365,9 +371,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     const int t = q_beg + qpos;
     const int64_t li = int64_t(h) * p.T + t;
-    const bool accumulate = p.acc != nullptr && __ldg(p.acc + seq) != 0;
+    const bool fin = p.fout != nullptr;
+    const bool accumulate = !fin && p.acc != nullptr && __ldg(p.acc + seq) != 0;
+    const bool merge_old = accumulate || (fin && t < p.pnt);
     // the stored LSE is read by both warpgroups before either writes it
-    const float old = (accumulate && qpos < nq) ? p.lse[li] : neg_inf();
+    const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
     tc_fence_before();
     // both warpgroups' O are complete after this barrier (each waited for
     // its own last P.V); all threads take part, the MMA warps too
@@ -383,9 +391,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
     float *orow = p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);  // this warpgroup's half
     bool write = store;
-    if (store && accumulate) {
+    if (store && merge_old) {
       if (lsum == 0.f) {
-        write = false;  // nothing new: keep the stored partial
+        if (!fin) {
+          write = false;  // nothing new: keep the stored partial
+        } else if (!is_neg_inf(old)) {
+          w_old = 1.f;  // the result is the context partial alone
+          lse = old;
+        }
       } else if (!is_neg_inf(old)) {
         const float m2 = fmaxf(old, lse);
         const float eo = expf(old - m2), en = expf(lse - m2);
@@ -405,7 +418,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld16(ob + uint32_t(c * 16), rb);
         tmem_wait_ld();
         if (write) {
-          float4 *dst = reinterpret_cast<float4 *>(orow + c * 16);
+          const float4 *src = reinterpret_cast<const float4 *>(orow + c * 16);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float v[4];
@@ -416,14 +429,24 @@ __global__ void __launch_bounds__(THREADS, 1)
               v[k] = (a + b) * w_new;
             }
             float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
-            if (w_old != 0.f) {
-              const float4 old = dst[e];
+            if (w_old != 0.f) {  // an unused side is never read
+              const float4 old = src[e];
               o4.x += w_old * old.x;
               o4.y += w_old * old.y;
               o4.z += w_old * old.z;
               o4.w += w_old * old.w;
             }
-            dst[e] = o4;
+            const int64_t col = (int64_t(t) * p.H + h) * DV + wg * (DV / 2) + c * 16 + e * 4;
+            if (!fin) {
+              reinterpret_cast<float4 *>(orow + c * 16)[e] = o4;
+            } else if (p.fout_bf16) {
+              uint2 b2;
+              b2.x = pack_bf16(o4.x, o4.y);
+              b2.y = pack_bf16(o4.z, o4.w);
+              *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + col) = b2;
+            } else {
+              *reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + col) = o4;
+            }
           }
         }
       }
@@ -431,7 +454,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int c = 0; c < DV / 2; c += 4)
         *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (write && wg == 0) p.lse[li] = lse;
+    if (write && wg == 0) {
+      if (!fin)
+        p.lse[li] = lse;
+      else if (p.flse)
+        p.flse[li] = lse;
+    }
   }
   if (warp < 2) __syncthreads_and(1);  // matches the softmax warps' vote
   tc_fence_before();
@@ -455,8 +483,8 @@ bool tc_attn_ok(const mla_dims_t &d, int kv_dtype, int64_t latent_ld) {
 int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                    const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
                    int T, int kv_rows, const void *q, const void *kv, const void *latent,
-                   int64_t latent_ld,
-                   const int32_t *accumulate, float *o, float *lse, cudaStream_t s) {
+                   int64_t latent_ld, const int32_t *accumulate, float *o, float *lse,
+                   void *final_out, float *final_lse, int final_dtype, int pnt, cudaStream_t s) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
   const int H = d.num_heads;
@@ -506,6 +534,10 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     prm.acc = accumulate;
     prm.o = o;
     prm.lse = lse;
+    prm.fout = final_out;
+    prm.flse = final_lse;
+    prm.pnt = pnt;
+    prm.fout_bf16 = final_dtype == MLA_DTYPE_BF16 ? 1 : 0;
     for (int k = 0; k < n; ++k) prm.items[k] = make_int2(items[b + k].seq, items[b + k].qt);
     attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES, s>>>(tq, tkv, tlat, prm);
     const int rc = launch_status();

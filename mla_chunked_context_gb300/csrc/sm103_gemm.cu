@@ -379,5 +379,22 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
 }  // namespace mla
 
 namespace mla {
+namespace {
+// Waits on an mbarrier that nothing arrives on, with a short limit: the wait
+// gives up, records the timeout bit and the kernel returns normally.
+__global__ void bounded_wait_selftest_kernel(long long limit, int32_t *gave_up) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = sm103::smem_u32(&bar);
+  sm103::mbar_init(b, 1);
+  sm103::fence_mbar_init();
+  *gave_up = sm103::mbar_wait_limit(b, 0, limit) ? 0 : 1;
+}
+}  // namespace
+
 int gemm_take_errors() { return sm103::take_error_flags_here(); }
+
+int launch_bounded_wait_selftest(long long limit_cycles, int32_t *gave_up, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 1, 0, s>>>(limit_cycles, gave_up);
+  return launch_status();
+}
 }  // namespace mla
