@@ -87,6 +87,15 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// 2^x with the SFU's approximate exponent (relative error below 2^-21; P is
+// then rounded to fp16, 2^-11).  Arguments here are at most 8 (the lazily
+// raised running max), results below 2^-126 flush to zero.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 16 consecutive 32-bit TMEM columns of the warp's 32 lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -291,14 +300,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      float sv[HALF];
-#pragma unroll
-      for (int c = 0; c < HALF / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(s_col + uint32_t(c * 32), r);
+      float sv[HALF];  // raw scores (scale applied below)
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(s_col, r0);  // both halves in flight before the wait
+        tmem_ld32(s_col + 32u, r1);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(r[e]) * p.scale_log2;
+        for (int e = 0; e < 32; ++e) {
+          sv[e] = __uint_as_float(r0[e]);
+          sv[32 + e] = __uint_as_float(r1[e]);
+        }
       }
       // mask keys past the sequence (and, causal, past the query)
       const int k0 = j * BKV + wg * HALF;   // first key of this half tile
@@ -309,9 +321,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int e = 0; e < HALF; ++e)
           if (e >= valid) sv[e] = neg_inf();
       }
-      float mx = sv[0];
+      // row max as a tree (no serial dependency chain); scale > 0, so the
+      // max of the scaled scores is the scaled max
+      float tm[HALF / 2];
 #pragma unroll
-      for (int e = 1; e < HALF; ++e) mx = fmaxf(mx, sv[e]);
+      for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
+#pragma unroll
+      for (int w = HALF / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
+      const float mx = tm[0] * p.scale_log2;
       float alpha = 1.f;
       bool rescale = false;
       if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
@@ -322,15 +341,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         m_used = m_new;
       }
-      const float base = (m_used == neg_inf()) ? 0.f : m_used;
+      const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
       l *= alpha;
       uint32_t pk[HALF / 2];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
       for (int e = 0; e < HALF / 2; ++e) {
-        const float a = exp2f(sv[2 * e] - base), b = exp2f(sv[2 * e + 1] - base);
-        l += a + b;
+        const float a = ex2_approx(fmaf(sv[2 * e], p.scale_log2, nbase));
+        const float b = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, nbase));
+        ls[e & 3] += a + b;
         pk[e] = pack_f16(a, b);
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // P over this warpgroup's own S columns (already read).  The previous
       // tile's P.V must have finished before O is rescaled; waiting for it on
       // every tile costs nothing (this tile's P.V runs after it anyway) and
