@@ -152,6 +152,21 @@ def merge_bytes(x, T, H, D, es=2):
     return b, full
 
 
+# ------------------------------------------------------- multi-rank glue ---
+def job_time_ms(local_ms: float, world: int, device) -> float:
+    """The job's time: the maximum over ranks of each rank's timed region
+    (every rank runs its own replica of the batch; no data-path exchange)."""
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, steps: int, job_ms: float) -> float:
+    """Units all ranks processed per second of job time (weak scaling)."""
+    return world * steps * units_per_rank_step / (job_ms / 1e3)
+
+
 # ------------------------------------------------------------ our arm -----
 def run_ours(args, rank, world, dev):
     import mla_chunked_context_gb300 as M
@@ -198,12 +213,8 @@ def run_ours(args, rank, world, dev):
         torch.distributed.barrier()
     clocks = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    max_ms = t.item()
-    value = world * args.steps * T / (max_ms / 1e3)
+    max_ms = job_time_ms(sum(step_ms), world, dev)
+    value = whole_job_rate(T, world, args.steps, max_ms)
 
     # ---- e2e: host buffers, copies inside the timed region.  Inputs are
     # double-buffered on the device: step i+1's host->device copy (on a copy
@@ -258,11 +269,7 @@ def run_ours(args, rank, world, dev):
             stream.wait_event(read_back[k])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = world * args.steps * T / (t.item() / 1e3)
+    e2e_value = whole_job_rate(T, world, args.steps, job_time_ms(e0.elapsed_time(e1), world, dev))
     del sets[1], outs[1]
 
     result = None
