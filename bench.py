@@ -202,11 +202,13 @@ def run_ours(args, rank, world, dev):
     sampler.mark("t0")
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    launched0 = M.mla_kernel_launches()
     for i in range(args.steps):
         flush.fill_(i & 0xff)                   # L2 flush outside the timed events
         evs[i][0].record(stream)
         step()
         evs[i][1].record(stream)
+    launched = M.mla_kernel_launches() - launched0  # this library's kernels only
     torch.cuda.synchronize()
     sampler.mark("t1")
     if world > 1:
@@ -289,7 +291,7 @@ def run_ours(args, rank, world, dev):
         }
         roofline["frac"] = roofline["achieved"] / roofline["peak"]
         step_ms_mean = max_ms / args.steps
-        launches = kernels["launches_per_step"]
+
         result = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_mean,
@@ -310,7 +312,7 @@ def run_ours(args, rank, world, dev):
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches * args.steps,
+            "gpu_launches": launched,
             "roofline": roofline,
             "merge": merge,
             "comparator": comparator,
@@ -415,14 +417,6 @@ def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
     for k in res:
         res[k]["ms"] /= reps
         res[k]["launches"] //= reps
-    empty = any(c == 0 and qsl[r] < pnt for r, c in enumerate(w.context_lens))
-    # mla_chunked_prefill: fill of context-free rows, 3 per chunk, new-token
-    # up-projection and attention, and a separate merge unless the tensor-core
-    # attention merges in its epilogue
-    fused = M.mla_has_tcgen05() and w.dtype == "bf16" and (w.kv_lora_rank, w.qk_rope_dim,
-                                                           w.qk_nope_dim, w.v_dim) == (512, 64,
-                                                                                       128, 128)
-    res["launches_per_step"] = (1 if empty else 0) + 3 * len(plans) + 2 + (0 if fused else 1)
     return res
 
 

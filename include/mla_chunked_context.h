@@ -282,7 +282,7 @@ int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *chunk,
                            int32_t *dev_status, mla_stream_t stream);
 
 /* mla_context_chunk_attn_noalloc: mla_context_chunk_attn without a caller
- *   workspace.  (No counterpart in the paper; it serves callers that cannot
+ *   workspace.  (Not a step of the method; it serves callers that cannot
  *   allocate device memory themselves, e.g. a plugin whose host framework
  *   owns every device allocation and hands it no workspace, or a path where a
  *   cudaMalloc, which can synchronise the device, is not allowed.)
@@ -330,6 +330,16 @@ int mla_prefill_workspace_bytes(const mla_dims_t *d,
  *   All metadata goes to the device in one cudaMemcpyAsync from host memory.
  *   On the tensor-core path the workspace keeps K/V in fp16 (see
  *   mla_kv_up_proj); on the CUDA-core path in float32.
+ *   Streams: the chunks run as a two-buffer pipeline.  Gathers and
+ *   up-projections go to two library-owned side streams of the highest
+ *   priority (one pair per device, made on first use); attention, merges
+ *   and every write of out/out_lse stay on `stream`.  All of it is ordered
+ *   after the work already on `stream` (an event recorded there), and
+ *   `stream` waits for all of it before the call's last kernel, so to the
+ *   caller the call behaves like work enqueued on `stream` alone (also under
+ *   stream capture).  Calls from several host threads are serialised while
+ *   they enqueue.  The workspace holds two chunk buffer sets and the
+ *   key-split scratch of the context attention.
  */
 int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
                         const int32_t *query_lens, int32_t num_requests,
@@ -380,6 +390,13 @@ int mla_chunked_prefill_equal_window(
 /* 1 when the current device runs the tcgen05 (sm_103a) kernels of this
  * library. */
 int mla_has_tcgen05(void);
+
+/* Number of kernels this library has enqueued since it was loaded, over all
+ * threads and devices (each launcher counts its launch as it enqueues it).
+ * Host-only, no synchronisation: a caller brackets a region with two reads
+ * to count the kernels that region launched.  Errors: MLA_ERR_INVALID for a
+ * NULL count. */
+int mla_kernel_launches(uint64_t *count);
 
 /* Failure-detection self test: launches one thread that waits on an
  * mbarrier nothing arrives on, with the same bounded wait the tensor-core

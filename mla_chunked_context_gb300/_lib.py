@@ -35,7 +35,8 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_chunked_prefill", "mla_has_tcgen05", "mla_device_error_flags",
             "mla_chunk_kv_dtype", "mla_context_chunk_attn_noalloc",
             "mla_plan_equal_window_chunks", "mla_prefill_equal_window_workspace_bytes",
-            "mla_chunked_prefill_equal_window", "mla_selftest_bounded_wait")
+            "mla_chunked_prefill_equal_window", "mla_selftest_bounded_wait",
+            "mla_kernel_launches")
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -87,6 +88,7 @@ def lib() -> C.CDLL:
             "mla_chunked_prefill": [P, P, P, I32, I32, I32, I32, P, P, P, I32, P, I32, P, P, SZ,
                                     P, P, P, P],
             "mla_has_tcgen05": [],
+            "mla_kernel_launches": [P],
             "mla_device_error_flags": [P],
             "mla_chunk_kv_dtype": [P, P],
             "mla_context_chunk_attn_noalloc": [P, P, P, P, P, I32, P, P, I32, P, I32, P, P, P,
@@ -347,6 +349,13 @@ def mla_chunked_prefill(dims: Dims, context_lens, query_lens, row_budget: int,
 
 def mla_has_tcgen05() -> bool:
     return bool(lib().mla_has_tcgen05())
+
+
+def mla_kernel_launches() -> int:
+    """Kernels the library has enqueued since it was loaded (all threads)."""
+    n = C.c_uint64(0)
+    _check(lib().mla_kernel_launches(C.byref(n)), "mla_kernel_launches")
+    return n.value
 
 
 def mla_device_error_flags() -> int:

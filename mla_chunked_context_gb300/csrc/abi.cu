@@ -5,7 +5,9 @@
 //   plan (host) -> one metadata upload -> fill context-free rows of the
 //   partial -> per chunk { gather, up-projection, attention + accumulate } ->
 //   new-token up-projection -> causal new-token attention -> final merge.
+#include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -46,7 +48,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    const int32_t *k_loc_host, int T, int kv_rows, const void *q, const void *kv,
                    const void *latent, int64_t latent_ld, const int32_t *accumulate,
                    float *o, float *lse, void *final_out, float *final_lse, int final_dtype,
-                   int pnt, cudaStream_t s);
+                   int pnt, const SplitScratch *split, cudaStream_t s);
 bool tc_available();
 
 namespace {
@@ -103,13 +105,13 @@ int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
               const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
               int T, const void *q, const void *kv, int kv_dtype, int kv_rows,
               const void *latent, int64_t latent_ld, const int32_t *acc, float *o, float *lse,
-              cudaStream_t s) {
+              cudaStream_t s, const SplitScratch *split = nullptr) {
   const int nq = q_loc_host[n] - q_loc_host[0];
   if (n == 0 || nq == 0) return MLA_OK;
   if (tc_available() && tc_attn_ok(d, kv_dtype, latent_ld) && aligned16(q) && aligned16(kv) &&
       aligned16(latent))
     return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, kv_rows, q, kv,
-                          latent, latent_ld, acc, o, lse, nullptr, nullptr, 0, 0, s);
+                          latent, latent_ld, acc, o, lse, nullptr, nullptr, 0, 0, split, s);
   return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, kv_rows, q, kv, kv_dtype, latent,
                           latent_ld, acc, o, lse, s);
 }
@@ -355,6 +357,41 @@ extern "C" int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *ch
 
 namespace {
 
+// Side streams and events of the chunk pipeline, one set per device, made on
+// first use and kept for the life of the process.  A prefill enqueues its
+// whole pipeline under g_pipeline_mu, so concurrent callers never interleave
+// their records and waits on these streams.
+struct Pipeline {
+  cudaStream_t gather = nullptr, gemm = nullptr;
+  std::vector<cudaEvent_t> ev;
+};
+std::mutex g_pipeline_mu;
+
+int pipeline_for_current_device(size_t events, Pipeline **out) {
+  static std::vector<Pipeline> per_device;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (per_device.size() <= size_t(dev)) per_device.resize(dev + 1);
+  Pipeline &pl = per_device[dev];
+  if (!pl.gemm) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&pl.gather, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&pl.gemm, cudaStreamNonBlocking, greatest) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  while (pl.ev.size() < events) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return MLA_ERR_CUDA;
+    pl.ev.push_back(e);
+  }
+  *out = &pl;
+  return MLA_OK;
+}
+
+bool record(cudaEvent_t e, cudaStream_t s) { return cudaEventRecord(e, s) == cudaSuccess; }
+bool wait_on(cudaStream_t s, cudaEvent_t e) { return cudaStreamWaitEvent(s, e, 0) == cudaSuccess; }
+
 struct PrefillLayout {
   std::vector<mla_chunk_t> chunks;
   std::vector<int32_t> starts, lens, qsl;
@@ -399,20 +436,36 @@ int build_prefill(const mla_dims_t &d, const int32_t *ctx, const int32_t *ql, in
   return MLA_OK;
 }
 
+// Key-split scratch slots of the context attention (a few (sequence, query
+// tile) units of a chunk, split over their keys when the chunk has too few
+// units to fill the GPU).
+constexpr int kSplitSlots = 16;
+
 struct PrefillBuffers {
   int32_t *meta;
-  ChunkBuffers chunk;
+  ChunkBuffers chunk[2];  // chunk c uses set c % 2
   void *kv_suffix;
   float *o_part, *lse_part, *o_suf, *lse_suf;
+  SplitScratch split;
 };
 
 size_t carve_prefill(void *base, const mla_dims_t &d, const PrefillLayout &p,
                      PrefillBuffers &b) {
   Carve cv(base);
-  const int es = elem_bytes(d.dtype);
   b.meta = static_cast<int32_t *>(cv.take(p.meta_total * sizeof(int32_t)));
-  carve_chunk_buffers(cv, d, p.max_rows, b.chunk);
-  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk.kv_dtype));
+  const int sets = p.chunks.size() > 1 ? 2 : 1;
+  for (int k = 0; k < 2; ++k) {
+    if (k < sets)
+      carve_chunk_buffers(cv, d, p.max_rows, b.chunk[k]);
+    else
+      b.chunk[k] = b.chunk[0];
+  }
+  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk[0].kv_dtype));
+  const size_t rows_split = size_t(kSplitSlots) * d.num_heads * 128;
+  b.split.o = static_cast<float *>(cv.take(rows_split * d.v_dim * sizeof(float)));
+  b.split.lse = static_cast<float *>(cv.take(rows_split * sizeof(float)));
+  b.split.slots = kSplitSlots;
+  b.split.target_ctas = 4 * num_sms();
   const size_t o_bytes = size_t(p.T) * d.num_heads * d.v_dim * sizeof(float);
   const size_t l_bytes = size_t(p.T) * d.num_heads * sizeof(float);
   b.o_part = static_cast<float *>(cv.take(o_bytes));
@@ -485,34 +538,86 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
 
   const int H = d->num_heads, Dv = d->v_dim, T = p.T;
   const int LP = d->kv_lora_rank + d->qk_rope_dim;
+  const int es = elem_bytes(d->dtype);
+  const int kv_dtype = b.chunk[0].kv_dtype;
   rc = launch_fill_empty_rows(b.o_part, b.lse_part, T, H, Dv, int(p.empty.size()),
                               b.meta + p.slices_off, s);
   if (rc) return rc;
-  for (size_t c = 0; c < p.chunks.size(); ++c) {
-    rc = run_chunk(*d, p.metas[c], b.meta + p.meta_off[c], T, q, kv_cache, num_blocks,
-                   block_table, block_table_stride, w_kv_b, b.chunk, b.o_part, b.lse_part,
-                   dev_status, s);
-    if (rc) return rc;
-  }
-  rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, b.chunk.kv_dtype, s);
+
+  // The chunk pipeline.  Streams: `s` (the caller's) runs every attention and
+  // everything that writes the partial or the output, `sg` the gathers, `sm`
+  // the up-projections.  Chunk c uses buffer set c % 2: its gather waits until
+  // the attention of chunk c-2 has read that set, its up-projection follows
+  // its gather, its attention its up-projection.  So gathers never sit
+  // between two GEMMs, and the up-projection of chunk c+1 fills the SMs that
+  // the attention of chunk c leaves idle (its tail, or a long request's few
+  // CTAs, which is also why that attention is split over its keys).  The
+  // side streams have the higher priority, so a GEMM takes SMs as soon as
+  // attention CTAs retire.  (Capping the GEMM at a share of the SMs, to run
+  // the two side by side, was slower: its per-SM rate does not grow when
+  // fewer SMs share HBM.)
+  std::lock_guard<std::mutex> lock(g_pipeline_mu);
+  Pipeline *pl = nullptr;
+  const size_t nc = p.chunks.size();
+  rc = pipeline_for_current_device(3 * nc + 4, &pl);
   if (rc) return rc;
+  cudaEvent_t *ev = pl->ev.data();
+  const cudaStream_t sg = pl->gather, sm = pl->gemm;
+  auto ev_lat = [&](size_t c) { return ev[1 + 3 * c]; };
+  auto ev_kv = [&](size_t c) { return ev[2 + 3 * c]; };
+  auto ev_attn = [&](size_t c) { return ev[3 + 3 * c]; };
+  cudaEvent_t ev_new = ev[1 + 3 * nc], ev_join = ev[2 + 3 * nc];
+  if (!record(ev[0], s) || !wait_on(sg, ev[0]) || !wait_on(sm, ev[0])) return MLA_ERR_CUDA;
+  for (size_t c = 0; c < nc && rc == MLA_OK; ++c) {
+    const ChunkMetaHost &m = p.metas[c];
+    const ChunkBuffers &cb = b.chunk[c & 1];
+    const int n = m.n;
+    const int32_t *req = b.meta + p.meta_off[c], *st = req + n, *cu = st + n, *ql = cu + n + 1,
+                  *acc = ql + n + 1;
+    if (c >= 2 && !wait_on(sg, ev_attn(c - 2))) rc = MLA_ERR_CUDA;
+    if (!rc)
+      rc = launch_gather(kv_cache, num_blocks, d->block_size, LP * es, block_table,
+                         block_table_stride, n, req, st, cu, m.rows, cb.latent_ws, dev_status, sg);
+    if (!rc && (!record(ev_lat(c), sg) || !wait_on(sm, ev_lat(c)))) rc = MLA_ERR_CUDA;
+    if (!rc) rc = up_proj(*d, cb.latent_ws, LP, m.rows, w_kv_b, cb.kv_ws, kv_dtype, sm);
+    if (!rc && (!record(ev_kv(c), sm) || !wait_on(s, ev_kv(c)))) rc = MLA_ERR_CUDA;
+    if (!rc)
+      rc = attention(*d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, cb.kv_ws,
+                     kv_dtype, m.rows, cb.latent_ws, LP, acc, b.o_part, b.lse_part, s, &b.split);
+    if (!rc && !record(ev_attn(c), s)) rc = MLA_ERR_CUDA;
+  }
+  // new-token up-projection, beside the last chunk's attention
+  if (!rc) rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, sm);
+  // join the side streams back into the caller's stream, also after an error
+  // (the caller may free the workspace once its stream has passed this point)
+  const bool joined = record(ev_new, sm) && record(ev_join, sg) && wait_on(s, ev_new) &&
+                      wait_on(s, ev_join);
+  if (rc) return rc;
+  if (!joined) return MLA_ERR_CUDA;
+
   const int32_t *sq = b.meta + p.suffix_off;
-  if (tc_available() && tc_attn_ok(*d, b.chunk.kv_dtype, LP) && aligned16(q) &&
+  if (tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
       aligned16(b.kv_suffix) && aligned16(new_latent)) {
     // new-token attention with the final merge in its epilogue (row f3): the
     // context partial is read where needed, the output written once
     return launch_attn_tc(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, T, q,
                           b.kv_suffix, new_latent, LP, nullptr, b.o_part, b.lse_part, out,
-                          out_lse, d->dtype, p.pnt, s);
+                          out_lse, d->dtype, p.pnt, nullptr, s);
   }
   rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 b.chunk.kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
   if (rc) return rc;
   return launch_merge(out, out_lse, b.o_part, b.lse_part, b.o_suf, b.lse_suf, T, H, Dv, p.pnt,
                       MLA_DTYPE_F32, d->dtype, s);
 }
 
 extern "C" int mla_has_tcgen05(void) { return tc_available() ? 1 : 0; }
+
+extern "C" int mla_kernel_launches(uint64_t *count) {
+  if (!count) return MLA_ERR_INVALID;
+  *count = g_kernel_launches.load(std::memory_order_relaxed);
+  return MLA_OK;
+}
 
 extern "C" int mla_selftest_bounded_wait(int32_t limit_us, int32_t *gave_up,
                                          mla_stream_t stream) {

@@ -4,6 +4,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/mla_chunked_context.h"
@@ -51,7 +52,12 @@ __device__ __forceinline__ int find_seq(const int32_t *loc, int n, int x) {
   return lo;
 }
 
+// Kernels this library has enqueued since it was loaded (every launcher
+// calls launch_status() once, right after its launch).
+inline std::atomic<unsigned long long> g_kernel_launches{0};
+
 inline int launch_status() {
+  g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -66,6 +72,14 @@ inline bool valid_dtype(int32_t dtype) {
 inline bool valid_kv_dtype(int32_t dtype) {
   return dtype == MLA_DTYPE_BF16 || dtype == MLA_DTYPE_F32 || dtype == MLA_DTYPE_F16;
 }
+
+// Scratch of the key-split attention: `slots` partials of [H][128][Dv] f32
+// (O) and [H][128] f32 (LSE); a launch splits its longest (sequence, query
+// tile) units over their keys until it has about `target_ctas` CTAs.
+struct SplitScratch {
+  float *o = nullptr, *lse = nullptr;
+  int slots = 0, target_ctas = 0;
+};
 
 inline int num_sms() {
   int dev = 0, n = 0;

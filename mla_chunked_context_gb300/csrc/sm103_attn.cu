@@ -14,7 +14,11 @@
 // head-major workspace kv [H, rows, 256] (columns [0,128) / [128,256));
 // k_pe is the latent row's tail, latent[row][512:576], shared by all heads.
 //
-// One CTA = one (sequence, 128-query tile, head); keys in 128-key tiles.
+// One CTA = one (sequence, 128-query tile, head) and a range of its 128-key
+// tiles: all of them, or -- when a launch has too few (sequence, tile, head)
+// units to fill the GPU -- one of several key splits, whose partial (O, LSE)
+// go to a scratch slot and are LSE-merged by split_combine_kernel (the same
+// merge as the chunk accumulation, over a split of the key set).
 // Two softmax warpgroups share every S tile: A takes its keys 0-63, B keys
 // 64-127, each with its own running max and sum and its own O accumulator
 // (a split of the key set, merged by LSE in the epilogue).  Each thread thus
@@ -61,7 +65,8 @@ constexpr int SMEM_BYTES = 1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + XCHG_BY
 constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256;
-constexpr int MAX_ITEMS = 2048;
+constexpr int MAX_ITEMS = 1536;
+constexpr int MAX_SPLIT_GROUPS = 16;   // split (sequence, tile)s per launch
 constexpr float kRescaleThreshold = 8.0f;    // log2 of the tolerated growth
 
 struct AttnParams {
@@ -75,7 +80,12 @@ struct AttnParams {
   void *fout;
   float *flse;
   int pnt, fout_bf16;
-  int2 items[MAX_ITEMS];  // (sequence, query tile), longest first
+  // key-split scratch: slot k holds O [H][BQ][DV] (normalised) and LSE
+  // [H][BQ] of one split
+  float *split_o, *split_lse;
+  // (sequence, query tile | (split slot + 1) << 16, first key tile, end key
+  // tile), the most key tiles first
+  int4 items[MAX_ITEMS];
 };
 
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -131,13 +141,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x / p.n_items;
-  const int2 it = p.items[blockIdx.x - h * p.n_items];
-  const int seq = it.x, qt = it.y;
+  const int4 it = p.items[blockIdx.x - h * p.n_items];
+  const int seq = it.x, qt = it.y & 0xffff, slot = (it.y >> 16) - 1;
   const int q_beg = __ldg(p.q_loc + seq), nq = __ldg(p.q_loc + seq + 1) - q_beg;
   const int k_beg = __ldg(p.k_loc + seq), nk = __ldg(p.k_loc + seq + 1) - k_beg;
   const int q0 = qt * BQ;  // first query of the tile, within the sequence
-  int n_tiles = (nk + BKV - 1) / BKV;
-  if (p.causal) n_tiles = min(n_tiles, qt + 1);
+  // key tiles [kt0, kt0 + n_tiles) of the sequence (the host applied the
+  // causal limit)
+  const int kt0 = it.z, n_tiles = it.w - it.z;
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % RING;
         const uint32_t use = uint32_t(j / RING);          // use count of slot s
-        const int krow = k_beg + j * BKV;
+        const int krow = k_beg + (kt0 + j) * BKV;
         if (j >= RING && !mbar_wait(b_kempty + 8 * s, (use - 1) & 1)) break;
         uint8_t *k = sK + s * K_BYTES;
         mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       // mask keys past the sequence (and, causal, past the query)
-      const int k0 = j * BKV + wg * HALF;   // first key of this half tile
+      const int k0 = (kt0 + j) * BKV + wg * HALF;   // first key of this half tile
       int valid = nk - k0;
       if (p.causal) valid = min(valid, qpos - k0 + 1);
       if (valid < HALF) {
@@ -394,7 +405,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int t = q_beg + qpos;
     const int64_t li = int64_t(h) * p.T + t;
     const bool fin = p.fout != nullptr;
-    const bool accumulate = !fin && p.acc != nullptr && __ldg(p.acc + seq) != 0;
+    const bool split = slot >= 0;  // a key split: its own partial goes to the scratch slot
+    const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
     const bool merge_old = accumulate || (fin && t < p.pnt);
     // the stored LSE is read by both warpgroups before either writes it
     const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
@@ -411,7 +423,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool store = okv && qpos < nq;
     float lse = (lsum > 0.f) ? (mx + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
     float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
-    float *orow = p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);  // this warpgroup's half
+    // this warpgroup's half of the output row, and the row's LSE
+    float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + row) * DV + wg * (DV / 2)
+                        : p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
+    float *lse_dst = split ? p.split_lse + (int64_t(slot) * p.H + h) * BQ + row : p.lse + li;
     bool write = store;
     if (store && merge_old) {
       if (lsum == 0.f) {
@@ -478,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (write && wg == 0) {
       if (!fin)
-        p.lse[li] = lse;
+        *lse_dst = lse;
       else if (p.flse)
         p.flse[li] = lse;
     }
@@ -491,6 +506,126 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// LSE merge of the key splits of one (sequence, query tile, head) -- the
+// merge the epilogue applies between its two warpgroups, over n partials --
+// then written, or merged into the stored partial of a continued request,
+// exactly as an unsplit CTA's epilogue does.  One warp per query row, a
+// lane per 4 of the 128 output columns.
+struct SplitGroups {
+  int n, H, T;
+  const int32_t *q_loc, *acc;
+  const float *split_o, *split_lse;
+  float *o, *lse;
+  int4 g[MAX_SPLIT_GROUPS];  // (sequence, query tile, first slot, number of slots)
+};
+
+__global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ SplitGroups a) {
+  const int gw = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  const int row = gw % BQ, gh = gw / BQ;
+  if (gh >= a.n * a.H) return;
+  const int h = gh % a.H;
+  const int4 g = a.g[gh / a.H];
+  const int q_beg = __ldg(a.q_loc + g.x), nq = __ldg(a.q_loc + g.x + 1) - q_beg;
+  const int qpos = g.y * BQ + row;
+  if (qpos >= nq) return;
+  const int t = q_beg + qpos;
+  float m = neg_inf();
+  for (int k = 0; k < g.w; ++k)
+    m = fmaxf(m, __ldg(a.split_lse + (int64_t(g.z + k) * a.H + h) * BQ + row));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  if (!is_neg_inf(m)) {
+    for (int k = 0; k < g.w; ++k) {
+      const int64_t r = (int64_t(g.z + k) * a.H + h) * BQ + row;
+      const float ls = __ldg(a.split_lse + r);
+      if (is_neg_inf(ls)) continue;  // an empty split is never read
+      const float w = expf(ls - m);
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(a.split_o + r * DV) + lane);
+      l += w;
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+  }
+  float lse = (l > 0.f) ? m + logf(l) : neg_inf();
+  float w_new = (l > 0.f) ? 1.f / l : 0.f, w_old = 0.f;
+  const int64_t li = int64_t(h) * a.T + t;
+  float *orow = a.o + (int64_t(t) * a.H + h) * DV;
+  const bool accumulate = a.acc != nullptr && __ldg(a.acc + g.x) != 0;
+  if (accumulate) {
+    const float old = a.lse[li];
+    if (l == 0.f) return;  // nothing new: keep the stored partial
+    if (!is_neg_inf(old)) {
+      const float m2 = fmaxf(old, lse);
+      const float eo = expf(old - m2), en = expf(lse - m2);
+      w_old = eo / (eo + en);
+      w_new *= en / (eo + en);
+      lse = m2 + logf(eo + en);
+    }
+  }
+  float4 o4 = make_float4(acc.x * w_new, acc.y * w_new, acc.z * w_new, acc.w * w_new);
+  if (w_old != 0.f) {
+    const float4 old = reinterpret_cast<const float4 *>(orow)[lane];
+    o4.x += w_old * old.x;
+    o4.y += w_old * old.y;
+    o4.z += w_old * old.z;
+    o4.w += w_old * old.w;
+  }
+  __syncwarp();  // every lane has read the stored LSE before lane 0 rewrites it
+  reinterpret_cast<float4 *>(orow)[lane] = o4;
+  if (lane == 0) a.lse[li] = lse;
+}
+
+// Work items of one launch: (sequence, query tile, key tiles [kt0, kt1),
+// split slot or -1), the most key tiles first.  When the units (items x
+// heads) are too few to fill the GPU (a long request with few queries), the
+// longest items are split over their keys, at least kMinSplitTiles key
+// tiles a split, into scratch slots that split_combine_kernel merges.
+struct Item {
+  int seq, qt, kt0, kt1, slot;
+};
+constexpr int kMinSplitTiles = 16;
+
+int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
+               int H, const SplitScratch *split, std::vector<Item> &items, SplitGroups &sg) {
+  auto by_cost = [](const Item &a, const Item &b) { return a.kt1 - a.kt0 > b.kt1 - b.kt0; };
+  items.clear();
+  sg.n = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int nq = q_loc_host[i + 1] - q_loc_host[i];
+    const int nk = k_loc_host[i + 1] - k_loc_host[i];
+    if ((nq + BQ - 1) / BQ > 0xffff) return MLA_ERR_UNSUPPORTED;  // 16-bit tile index
+    for (int qt = 0; qt * BQ < nq; ++qt) {
+      int tiles = (nk + BKV - 1) / BKV;
+      if (causal) tiles = std::min(tiles, qt + 1);
+      items.push_back({i, qt, 0, tiles, -1});
+    }
+  }
+  std::stable_sort(items.begin(), items.end(), by_cost);
+  const int64_t units = int64_t(items.size()) * H;
+  if (split && split->o && !causal && units > 0 && units < split->target_ctas) {
+    const int want = int((split->target_ctas + units - 1) / units);
+    std::vector<Item> out;
+    int used = 0;
+    for (const Item &it : items) {
+      const int nt = it.kt1 - it.kt0;
+      const int f = std::min(want, nt / kMinSplitTiles);
+      if (f < 2 || used + f > split->slots || sg.n == MAX_SPLIT_GROUPS) {
+        out.push_back(it);
+        continue;
+      }
+      sg.g[sg.n++] = make_int4(it.seq, it.qt, used, f);
+      for (int k = 0; k < f; ++k)
+        out.push_back({it.seq, it.qt, it.kt0 + nt * k / f, it.kt0 + nt * (k + 1) / f, used + k});
+      used += f;
+    }
+    items.swap(out);
+    std::stable_sort(items.begin(), items.end(), by_cost);
+  }
+  return MLA_OK;
 }
 
 }  // namespace
@@ -506,7 +641,8 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
                    int T, int kv_rows, const void *q, const void *kv, const void *latent,
                    int64_t latent_ld, const int32_t *accumulate, float *o, float *lse,
-                   void *final_out, float *final_lse, int final_dtype, int pnt, cudaStream_t s) {
+                   void *final_out, float *final_lse, int final_dtype, int pnt,
+                   const SplitScratch *split, cudaStream_t s) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
   const int H = d.num_heads;
@@ -520,22 +656,11 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
       !make_tmap_2d_16(&tlat, false, latent, 576, uint64_t(rows > 0 ? rows : 1),
                        uint64_t(latent_ld) * 2, 64, BKV, true))
     return MLA_ERR_CUDA;
-  // work items: (sequence, query tile), the ones with the most key tiles first
-  struct Item {
-    int seq, qt, cost;
-  };
   std::vector<Item> items;
-  for (int i = 0; i < num_seqs; ++i) {
-    const int nq = q_loc_host[i + 1] - q_loc_host[i];
-    const int nk = k_loc_host[i + 1] - k_loc_host[i];
-    for (int qt = 0; qt * BQ < nq; ++qt) {
-      int tiles = (nk + BKV - 1) / BKV;
-      if (causal) tiles = std::min(tiles, qt + 1);
-      items.push_back({i, qt, tiles});
-    }
-  }
-  std::stable_sort(items.begin(), items.end(),
-                   [](const Item &a, const Item &b) { return a.cost > b.cost; });
+  SplitGroups sg{};
+  const int rc = plan_items(causal, num_seqs, q_loc_host, k_loc_host, H,
+                            final_out == nullptr ? split : nullptr, items, sg);
+  if (rc) return rc;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -543,7 +668,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
       return MLA_ERR_CUDA;
     attr_set = true;
   }
-  thread_local AttnParams prm;  // large (16 KB); filled per launch batch
+  thread_local AttnParams prm;  // large (24 KB); filled per launch batch
   for (size_t b = 0; b < items.size(); b += MAX_ITEMS) {
     const int n = int(std::min<size_t>(MAX_ITEMS, items.size() - b));
     prm.n_items = n;
@@ -560,10 +685,28 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     prm.flse = final_lse;
     prm.pnt = pnt;
     prm.fout_bf16 = final_dtype == MLA_DTYPE_BF16 ? 1 : 0;
-    for (int k = 0; k < n; ++k) prm.items[k] = make_int2(items[b + k].seq, items[b + k].qt);
+    prm.split_o = split ? split->o : nullptr;
+    prm.split_lse = split ? split->lse : nullptr;
+    for (int k = 0; k < n; ++k) {
+      const Item &it = items[b + k];
+      prm.items[k] = make_int4(it.seq, it.qt | ((it.slot + 1) << 16), it.kt0, it.kt1);
+    }
     attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES, s>>>(tq, tkv, tlat, prm);
     const int rc = launch_status();
     if (rc) return rc;
+  }
+  if (sg.n > 0) {
+    sg.H = H;
+    sg.T = T;
+    sg.q_loc = q_loc;
+    sg.acc = accumulate;
+    sg.split_o = split->o;
+    sg.split_lse = split->lse;
+    sg.o = o;
+    sg.lse = lse;
+    const int64_t warps = int64_t(sg.n) * H * BQ;
+    split_combine_kernel<<<int((warps * 32 + 255) / 256), 256, 0, s>>>(sg);
+    return launch_status();
   }
   return MLA_OK;
 }

@@ -9,26 +9,33 @@
 // The MLA up-projection is not on the pages; it is the standard MLA prefill
 // step that turns the gathered latent rows into per-head K_nope and V.
 //
-// Design: persistent, warp-specialised, 2-SM MMA.  CTAs run in pairs (a
-// cluster of two, one CTA per SM); a pair computes 256x256 output tiles with
-// tcgen05.mma.cta_group::2 (M=256: 128 rows in each SM's tensor memory).
-// Each SM holds only its own 128 A rows and its half (128 rows) of the B
-// tile, so per SM a 64-deep K step moves 32 KB through shared memory for
-// 2x128x256x64 FLOP -- half the shared-memory traffic per FLOP of a 1-SM
-// M=128 tile, which is what bounds a 1-SM kernel.
-//   warp 0      (both CTAs) TMA producer: own A 128x64 and B-half 128x64 per
-//               stage, 6-stage ring; the loads of both CTAs complete on the
-//               even CTA's "full" barrier.
+// Design: persistent, warp-specialised, 2-SM MMA, A-stationary.  CTAs run
+// in pairs (a cluster of two, one CTA per SM); a pair computes 256x256 output
+// tiles with tcgen05.mma.cta_group::2 (M=256: 128 rows in each SM's tensor
+// memory).  Each SM holds only its own 128 A rows and its half (128 rows) of
+// the B tile.  A work unit is (256-row block of the latent, segment of the
+// N tiles): the pair loads the block's A rows once (all of K, 128 KB per SM,
+// resident for the unit) and streams only B through a 5-stage ring.  Per
+// tile an SM then reads 128 KB of operands instead of 256 KB; with the
+// output written at the same time, the SM's memory interface is what bounds
+// this kernel (halving the operand loads alone took it from 1393 to 1724
+// TFLOP/s on 32768 rows).
+//   warp 0      (both CTAs) TMA producer: the unit's A rows, then its own B
+//               half 128x64 per stage; the loads of both CTAs complete on the
+//               even CTA's barriers.
 //   warp 1      (both CTAs) allocates 512 TMEM columns in the pair; in the
 //               even CTA lane 0 issues the MMAs (M=256, N=256, K=16; 4 per
 //               stage) into one of two 256-column f32 accumulators, and
-//               commits stage and accumulator barriers to both CTAs.
+//               commits stage, accumulator and A barriers to both CTAs.
 //   warps 2-5   (both CTAs) epilogue of the CTA's own 128 rows: tcgen05.ld
 //               32 lanes x 32 columns, round to fp16 (or bf16), swizzled 32x64
 //               staging tile, coalesced 16-byte stores; then release the
 //               accumulator on the even CTA's barrier.
-// Pair tiles are visited m-major with n fastest, so a 256-row slice of the
-// latent and the whole weight stay in L2 while the pairs sweep them.
+// Units are numbered segment-major, row block fastest, and dealt to the
+// pairs round-robin: the pairs that run at the same time sweep the same
+// weight tiles in step (read once from L2 for all of them, and kept there
+// with an evict-last hint while the output streams past); this ordering ran
+// 8% faster than giving concurrent pairs different segments.
 #include <cstdio>
 
 #include "sm103.cuh"
@@ -38,24 +45,34 @@ namespace sm103 {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 5;
+constexpr int MAX_K = 512;                    // A rows are resident: K <= 512
 constexpr int PAIR_M = 2 * BM;                // rows of a pair tile
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB: this CTA's A rows
-constexpr int B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's half of B
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BLOCK = BM * BK * 2;          // 16 KB: this CTA's A rows, one K block
+constexpr int A_BYTES = (MAX_K / BK) * A_BLOCK;  // 128 KB: all of K
+constexpr int B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's half of B, one K block
 constexpr int EPI_WARPS = 4;
 constexpr int STG_BYTES = 32 * 64 * 2;        // one warp's 32x64 16-bit staging tile
-constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES +
-                           EPI_WARPS * 2 * STG_BYTES + 256 /*barriers*/;
+constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_BYTES + STAGES * B_BYTES +
+                           EPI_WARPS * STG_BYTES + 256 /*barriers*/;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 
 struct GemmArgs {
   int M, N, K;
   int num_pm, num_n;  // pair tiles along M, tiles along N
+  int nseg;           // N segments per 256-row block: a unit is (block, segment)
   int hd;             // output columns per head (Dn + Dv): the output is [N/hd, M, hd]
   uint16_t *out;      // fp16 / bf16 bits
 };
+
+// Unit u: N tiles [t0, t1) of segment u / num_pm, row block u % num_pm.
+__device__ __forceinline__ void unit_range(const GemmArgs &g, int u, int &pm, int &t0, int &t1) {
+  const int sgm = u / g.num_pm;
+  pm = u - sgm * g.num_pm;
+  t0 = sgm * g.num_n / g.nseg;
+  t1 = (sgm + 1) * g.num_n / g.nseg;
+}
 
 template <bool kF16Out>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -65,24 +82,28 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = smem + STAGES * A_BYTES;
-  uint8_t *sStage = smem + STAGES * STAGE_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + EPI_WARPS * 2 * STG_BYTES);
-  // bars: full[S], empty[S], acc_full[2], acc_empty[2], mma_done; then the
-  // TMEM base address slot.  full and acc_empty are used in the even CTA only.
+  uint8_t *sB = smem + A_BYTES;
+  uint8_t *sStage = sB + STAGES * B_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + EPI_WARPS * STG_BYTES);
+  // bars: full[S], empty[S], acc_full[2], acc_empty[2], a_full, a_empty,
+  // mma_done; then the TMEM base address slot.  full, acc_empty and a_full
+  // are used in the even CTA only.
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
-  const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  const uint32_t a_full = smem_u32(bars + 2 * STAGES + 4);
+  const uint32_t a_empty = smem_u32(bars + 2 * STAGES + 5);
+  const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 6);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 7);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the MMAs
-  const int num_tiles = g.num_pm * g.num_n;
+  const int num_units = g.num_pm * g.nseg;
   const int first = blockIdx.x >> 1, step = gridDim.x >> 1;
   const int kblocks = g.K / BK;
   // the even CTA's barriers, as seen from this CTA
   const uint32_t full0_lead = mapa_shared(full0, 0);
   const uint32_t acce0_lead = mapa_shared(acce0, 0);
+  const uint32_t a_full_lead = mapa_shared(a_full, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -93,6 +114,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(accf0 + 8 * a, 1);
       mbar_init(acce0 + 8 * a, 2 * EPI_WARPS);  // epilogue warps of both CTAs
     }
+    mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
     mbar_init(done_bar, 1);
     fence_mbar_init();
     prefetch_map(&tm_a);
@@ -111,35 +134,53 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     int issued_parity[STAGES];
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+    int a_issued = -1;  // parity of the last A load, -1: none
+    const uint64_t pol_w = policy_evict_last();
     bool ok = true;
-    for (int t = first; t < num_tiles && ok; t += step) {
-      const int m0 = (t / g.num_n) * PAIR_M + int(rank) * BM;
-      const int nb = (t % g.num_n) * BN + int(rank) * (BN / 2);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = full0_lead + 8 * stage;
-        if (rank == 0) mbar_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);  // both CTAs' bytes
-        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &tm_a, fb, kb * BK, m0);
-        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &tm_b, fb, kb * BK, nb);
-        issued_parity[stage] = int(phase);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+    int k = 0;          // units of this pair so far
+    for (int u = first; u < num_units && ok; u += step, ++k) {
+      int pm, t0, t1;
+      unit_range(g, u, pm, t0, t1);
+      const int m0 = pm * PAIR_M + int(rank) * BM;
+      // the previous unit's MMAs are done with the resident A rows
+      if (!mbar_wait(a_empty, uint32_t((k & 1) ^ 1))) break;
+      if (rank == 0) mbar_expect_tx(a_full, uint32_t(2 * kblocks * A_BLOCK));  // both CTAs
+      for (int kb = 0; kb < kblocks; ++kb)
+        tma_load_2d_pair(smem_u32(sA + kb * A_BLOCK), &tm_a, a_full_lead, kb * BK, m0);
+      a_issued = k & 1;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const int nb = t * BN + int(rank) * (BN / 2);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_expect_tx(full0 + 8 * stage, 2 * B_BYTES);  // both CTAs' bytes
+          tma_load_2d_pair_hint(smem_u32(sB + stage * B_BYTES), &tm_b, full0_lead + 8 * stage,
+                                kb * BK, nb, pol_w);
+          issued_parity[stage] = int(phase);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
     }
     // every load this CTA issued has landed before the pair may exit: the
-    // even CTA's full barrier counts both CTAs' bytes; the odd CTA knows its
-    // loads landed once the MMAs that read them released the stage
+    // even CTA's barriers count both CTAs' bytes; the odd CTA knows its loads
+    // landed once the MMAs that read them released the buffer
     for (int s = 0; s < STAGES; ++s) {
       if (issued_parity[s] < 0) continue;
       if (rank == 0)
         mbar_wait(full0 + 8 * s, uint32_t(issued_parity[s]));
       else
         mbar_wait(empty0 + 8 * s, uint32_t(issued_parity[s]));
+    }
+    if (a_issued >= 0) {
+      if (rank == 0)
+        mbar_wait(a_full, uint32_t(a_issued));
+      else
+        mbar_wait(a_empty, uint32_t(a_issued));
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer (even CTA)
@@ -149,35 +190,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = first; t < num_tiles && ok; t += step) {
-      if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1)) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(full0 + 8 * stage, phase)) {
+    int k = 0;
+    for (int u = first; u < num_units && ok; u += step, ++k) {
+      int pm, t0, t1;
+      unit_range(g, u, pm, t0, t1);
+      if (!mbar_wait(a_full, uint32_t(k & 1))) break;
+      for (int t = t0; t < t1 && ok; ++t) {
+        if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + kb * A_BLOCK);
+          const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16_pair(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
-                        desc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
-        // the stage is free in both CTAs once these MMAs finish
-        mma_commit_pair_mc(empty0 + 8 * stage, uint16_t(0x3));
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16_pair(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
+                          desc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+          // the B stage is free in both CTAs once these MMAs finish
+          mma_commit_pair_mc(empty0 + 8 * stage, uint16_t(0x3));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(accf0 + 8 * acc, uint16_t(0x3));  // accumulator complete
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
         }
       }
-      if (!ok) break;
-      mma_commit_pair_mc(accf0 + 8 * acc, uint16_t(0x3));  // accumulator complete
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
-      }
+      // the resident A rows are free in both CTAs once this unit's MMAs finish
+      mma_commit_pair_mc(a_empty, uint16_t(0x3));
     }
     // every MMA this thread issued has completed before TMEM is released
     mma_commit_pair_mc(done_bar, uint16_t(0x1));
@@ -185,66 +237,73 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> 16-bit -> swizzled smem -> coalesced stores
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    uint8_t *stg = sStage + (warp - 2) * 2 * STG_BYTES;
+    uint8_t *stg = sStage + (warp - 2) * STG_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = first; t < num_tiles; t += step) {
-      const int m0 = (t / g.num_n) * PAIR_M + int(rank) * BM, n0 = (t % g.num_n) * BN;
-      if (!mbar_wait(accf0 + 8 * acc, acc_phase)) break;
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * BN);
+    bool ok = true;
+    for (int u = first; u < num_units && ok; u += step) {
+      int pm, t0, t1;
+      unit_range(g, u, pm, t0, t1);
+      const int m0 = pm * PAIR_M + int(rank) * BM;
+      for (int t = t0; t < t1; ++t) {
+        const int n0 = t * BN;
+        if (!mbar_wait(accf0 + 8 * acc, acc_phase)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
-      for (int j = 0; j < BN / 64; ++j) {
-        uint32_t lo[32], hi[32];
-        tmem_ld32(t_row + j * 64, lo);
-        tmem_ld32(t_row + j * 64 + 32, hi);
-        tmem_wait_ld();
-        // lane = row: its 64 values as 8 16-byte pieces, XOR-swizzled so the
-        // writes and the reads below are free of bank conflicts
-        uint8_t *row = stg + lane * 128;
+        for (int j = 0; j < BN / 64; ++j) {
+          uint32_t lo[32], hi[32];
+          tmem_ld32(t_row + j * 64, lo);
+          tmem_ld32(t_row + j * 64 + 32, hi);
+          tmem_wait_ld();
+          // lane = row: its 64 values as 8 16-byte pieces, XOR-swizzled so the
+          // writes and the reads below are free of bank conflicts
+          uint8_t *row = stg + lane * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t *src = (c < 4) ? lo + 8 * c : hi + 8 * (c - 4);
-          uint4 v;
-          if (kF16Out) {
-            v.x = pack_f16(__uint_as_float(src[0]), __uint_as_float(src[1]));
-            v.y = pack_f16(__uint_as_float(src[2]), __uint_as_float(src[3]));
-            v.z = pack_f16(__uint_as_float(src[4]), __uint_as_float(src[5]));
-            v.w = pack_f16(__uint_as_float(src[6]), __uint_as_float(src[7]));
-          } else {
-            v.x = pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1]));
-            v.y = pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3]));
-            v.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
-            v.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t *src = (c < 4) ? lo + 8 * c : hi + 8 * (c - 4);
+            uint4 v;
+            if (kF16Out) {
+              v.x = pack_f16(__uint_as_float(src[0]), __uint_as_float(src[1]));
+              v.y = pack_f16(__uint_as_float(src[2]), __uint_as_float(src[3]));
+              v.z = pack_f16(__uint_as_float(src[4]), __uint_as_float(src[5]));
+              v.w = pack_f16(__uint_as_float(src[6]), __uint_as_float(src[7]));
+            } else {
+              v.x = pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1]));
+              v.y = pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3]));
+              v.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
+              v.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
+            }
+            *reinterpret_cast<uint4 *>(row + ((c ^ (lane & 7)) << 4)) = v;
           }
-          *reinterpret_cast<uint4 *>(row + ((c ^ (lane & 7)) << 4)) = v;
-        }
-        __syncwarp();
-        // write back 4 rows x 128 B per instruction: in the head-major output
-        // the warp's 32 rows are consecutive 2*hd-byte rows, so every store
-        // instruction covers four full 128-byte lines.  The stores go through
-        // the LSU; the TMA unit stays free for the operand loads (TMA stores
-        // here held the kernel to 70% of the tensor peak it reaches without
-        // them).
-        const int n = n0 + j * 64, head = n / g.hd, col = n % g.hd;
+          __syncwarp();
+          // write back 4 rows x 128 B per instruction: in the head-major output
+          // the warp's 32 rows are consecutive 2*hd-byte rows, so every store
+          // instruction covers four full 128-byte lines.  The stores go through
+          // the LSU; the TMA unit stays free for the operand loads.
+          const int n = n0 + j * 64, head = n / g.hd, col = n % g.hd;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = 4 * i + (lane >> 3), ch = lane & 7;
-          const int grow = m0 + quarter * 32 + r;
-          const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 128 + ((ch ^ (r & 7)) << 4));
-          if (grow < g.M)
-            __stcs(reinterpret_cast<uint4 *>(g.out + (int64_t(head) * g.M + grow) * g.hd + col +
-                                             ch * 8),
-                   v);
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3), ch = lane & 7;
+            const int grow = m0 + quarter * 32 + r;
+            const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 128 + ((ch ^ (r & 7)) << 4));
+            if (grow < g.M)
+              __stcs(reinterpret_cast<uint4 *>(g.out + (int64_t(head) * g.M + grow) * g.hd + col +
+                                               ch * 8),
+                     v);
+          }
+          __syncwarp();  // the staging tile is rewritten by the next chunk
         }
-        __syncwarp();  // the staging tile is rewritten by the next chunk
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acce0_lead + 8 * acc);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce0_lead + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
     }
   }
@@ -321,7 +380,8 @@ bool tc_gemm_ok(const mla_dims_t &d, int kv_dtype, int64_t lda, const void *late
   const int N = d.num_heads * hd;
   auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   return d.dtype == MLA_DTYPE_BF16 && (kv_dtype == MLA_DTYPE_F16 || kv_dtype == MLA_DTYPE_BF16) &&
-         d.kv_lora_rank % sm103::BK == 0 && N % sm103::BN == 0 && hd % 64 == 0 &&
+         d.kv_lora_rank % sm103::BK == 0 && d.kv_lora_rank <= sm103::MAX_K &&
+         N % sm103::BN == 0 && hd % 64 == 0 &&
          (lda * 2) % 16 == 0 && al16(latent) && al16(w) && al16(kv);
 }
 
@@ -336,7 +396,8 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
   if (!make_tmap_2d_16(&ta, false, latent, K, rows, uint64_t(lda) * 2, BK, BM, true) ||
       !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN / 2, true))
     return MLA_ERR_CUDA;
-  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, hd, static_cast<uint16_t *>(kv)};
+  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, 1, hd,
+             static_cast<uint16_t *>(kv)};
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(up_proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -347,7 +408,6 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
       return MLA_ERR_CUDA;
     attr_set = true;
   }
-  const int pair_tiles = g.num_pm * g.num_n;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -368,7 +428,20 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
       n = num_sms() / 2;
     max_clusters = n;
   }
-  const int clusters = pair_tiles < max_clusters ? pair_tiles : max_clusters;
+  const int pairs = max_clusters;
+  // N segments per row block: the fewest tile-times for the busiest pair,
+  // counting a unit's A load as about one tile of B traffic
+  long best = -1;
+  for (int ns = 1; ns <= g.num_n; ++ns) {
+    const long rounds = (long(g.num_pm) * ns + pairs - 1) / pairs;
+    const long cost = rounds * ((g.num_n + ns - 1) / ns + 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      g.nseg = ns;
+    }
+  }
+  const int units = g.num_pm * g.nseg;
+  const int clusters = units < pairs ? units : pairs;
   cfg.gridDim = dim3(2 * clusters);
   const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<true>, ta, tb, g)
                             : cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<false>, ta, tb, g);

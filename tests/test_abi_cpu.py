@@ -119,8 +119,19 @@ def test_workspace_queries():
     T, H = w.num_tokens, w.num_heads
     rows = 65536
     kv_es = M.mla_chunk_kv_dtype(dims).itemsize
-    lower = rows * 576 * 2 + rows * H * 256 * kv_es + T * H * 256 * kv_es + 2 * T * H * 128 * 4
-    assert lower <= b <= lower + 64 * 1024 * 1024
+    split = 16 * H * 128 * (128 + 1) * 4        # key-split scratch of the context attention
+
+    def lower(sets, rows, T):
+        return (sets * (rows * 576 * 2 + rows * H * 256 * kv_es) + T * H * 256 * kv_es +
+                2 * T * H * 128 * 4 + split)
+    # one chunk: one buffer set
+    assert lower(1, rows, T) <= b <= lower(1, rows, T) + 64 * 1024 * 1024
+    # several chunks: two buffer sets for the pipeline
+    h = W.workload("hetero")
+    bh = M.mla_prefill_workspace_bytes(dims, h.context_lens, h.query_lens, h.row_budget,
+                                       h.max_context_chunk, h.split_alignment)
+    lo = lower(2, h.row_budget, h.num_tokens)
+    assert lo <= bh <= lo + 64 * 1024 * 1024
     cb = M.mla_chunk_workspace_bytes(dims, 1000, 10)
     assert cb >= 1000 * 576 * 2 + 1000 * H * 256 * 2
 

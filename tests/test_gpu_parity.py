@@ -430,6 +430,25 @@ def test_prefill_deepseek_shapes_multichunk(budget):
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+def test_prefill_key_split_and_pipeline():
+    # few (request, query tile, head) units and long contexts: the context
+    # attention splits them over their keys (2 splits of 16+ key tiles) and
+    # merges the splits, also into a continued request's stored partial
+    # (second chunk of request 0; request 3 has two query tiles); the chunks
+    # run through the two-buffer pipeline (gathers and up-projections on
+    # their own streams)
+    w = W.scaled(W.workload("uniform"), context_lens=[8192, 3, 0, 5000],
+                 query_lens=[100, 20, 5, 130], num_heads=16, row_budget=4096,
+                 max_context_chunk=4096, split_alignment=64, seed=51)
+    x = W.make_inputs(w)
+    out, lse = _run_prefill(w, x)
+    ro, rl, plans = _oracle_prefill(w, x)
+    assert len(plans) == 5 and plans[1].is_continuation and plans[4].is_continuation
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 EDGE_CASES = {
     # no request has context: the output is the new-token attention alone
     "no_context": dict(context_lens=[0, 0, 0], query_lens=[5, 1, 130]),
