@@ -325,22 +325,23 @@ def run_ours(args, rank, world, dev):
 
 
 def committed_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    sources have not changed since it was taken (else null)."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source files have not changed since it was taken (else null)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     e = d.get(kernel)
-    if not e or e.get("csrc_sha1") != csrc_hash():
+    if not e or e.get("sources_sha1") != sources_hash(e.get("sources", [])):
         return None
     return e.get("bytes_per_launch")
 
 
-def csrc_hash():
+def sources_hash(files):
+    """sha1 over the named files under the package's csrc/, in order."""
     h = hashlib.sha1()
     c = os.path.join(ROOT, "mla_chunked_context_gb300", "csrc")
-    for f in sorted(os.listdir(c)):
+    for f in files:
         h.update(open(os.path.join(c, f), "rb").read())
     return h.hexdigest()
 
