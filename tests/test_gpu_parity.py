@@ -352,6 +352,27 @@ def test_varlen_attention(kind, causal):
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_attention_multi_tile(causal):
+    """Sequences of 3, 5 and 2 query tiles, several tiles of a sequence and
+    head side by side (sharing K/V through L2); causal tiles see a growing
+    number of key tiles."""
+    w = W.scaled(W.workload("uniform"), num_heads=2, seed=45)
+    ql = [300, 520, 129]
+    kl = ql if causal else [700, 1030, 64]
+    q_loc = [0] + list(np.cumsum(ql))
+    k_loc = [0] + list(np.cumsum(kl))
+    q, kv, lat = _attn_inputs(w, k_loc[-1], q_loc[-1], 9, torch.float16)
+    o = torch.full((q_loc[-1], w.num_heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((w.num_heads, q_loc[-1]), float("nan"), device=DEV)
+    M.mla_varlen_attn(M.Dims.of(w), causal, q_loc, k_loc, q.to(DEV), kv.to(DEV), lat.to(DEV),
+                      o, lse)
+    torch.cuda.synchronize()
+    ro, rl = _oracle_attn(w, q, kv, lat, q_loc, k_loc, causal)
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_varlen_attention_accumulate():
     """Chunk 2 continues the requests of chunk 1 and merges into its partial;
     the result equals attention over both key ranges at once."""
