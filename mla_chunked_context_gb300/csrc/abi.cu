@@ -48,7 +48,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    const int32_t *k_loc_host, int T, int kv_rows, const void *q, const void *kv,
                    const void *latent, int64_t latent_ld, const int32_t *accumulate,
                    float *o, float *lse, void *final_out, float *final_lse, int final_dtype,
-                   int pnt, const SplitScratch *split, cudaStream_t s);
+                   int pnt, const SplitScratch *split, bool skip_keyless, cudaStream_t s);
 bool tc_available();
 
 namespace {
@@ -105,13 +105,15 @@ int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
               const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
               int T, const void *q, const void *kv, int kv_dtype, int kv_rows,
               const void *latent, int64_t latent_ld, const int32_t *acc, float *o, float *lse,
-              cudaStream_t s, const SplitScratch *split = nullptr) {
+              cudaStream_t s, const SplitScratch *split = nullptr,
+              bool skip_keyless = false) {
   const int nq = q_loc_host[n] - q_loc_host[0];
   if (n == 0 || nq == 0) return MLA_OK;
   if (tc_available() && tc_attn_ok(d, kv_dtype, latent_ld) && aligned16(q) && aligned16(kv) &&
       aligned16(latent))
     return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, kv_rows, q, kv,
-                          latent, latent_ld, acc, o, lse, nullptr, nullptr, 0, 0, split, s);
+                          latent, latent_ld, acc, o, lse, nullptr, nullptr, 0, 0, split,
+                          skip_keyless, s);
   return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, kv_rows, q, kv, kv_dtype, latent,
                           latent_ld, acc, o, lse, s);
 }
@@ -143,6 +145,41 @@ void build_chunk_meta(const mla_chunk_t &c, const int32_t *starts, const int32_t
     acc[i] = starts[e] > 0 ? 1 : 0;
   }
   for (int i = 0; i <= n; ++i) ql[i] = qsl[c.request_start + i];
+  m.rows = cu[n];
+  std::memcpy(m.q_loc.data(), ql, sizeof(int32_t) * (n + 1));
+  std::memcpy(m.cu_rows.data(), cu, sizeof(int32_t) * (n + 1));
+}
+
+// Execution group: consecutive chunks [c0, c1) whose requests are all new
+// (no chunk after the first continues a request) and whose rows fit the
+// budget together.  The zero-context requests between them become sequences
+// without rows, so the group's sequences are the contiguous request range
+// and q_loc stays a prefix sum of query counts; the attention skips them
+// (their partial rows are initialised to O=0, LSE=-inf).
+void build_group_meta(const std::vector<mla_chunk_t> &chunks, size_t c0, size_t c1,
+                      const int32_t *starts, const int32_t *lens, const int32_t *qsl,
+                      ChunkMetaHost &m) {
+  const int r0 = chunks[c0].request_start, r1 = chunks[c1 - 1].request_end;
+  const int n = r1 - r0;
+  m.n = n;
+  m.ints.assign(chunk_meta_ints(n), 0);
+  m.q_loc.assign(n + 1, 0);
+  m.cu_rows.assign(n + 1, 0);
+  int32_t *req = m.ints.data(), *st = req + n, *cu = st + n, *ql = cu + n + 1,
+          *acc = ql + n + 1;
+  std::vector<int32_t> rows(n, 0);
+  for (size_t c = c0; c < c1; ++c)
+    for (int i = 0; i < chunks[c].request_end - chunks[c].request_start; ++i) {
+      const int e = chunks[c].entry_offset + i, k = chunks[c].request_start + i - r0;
+      st[k] = starts[e];
+      rows[k] = lens[e];
+      acc[k] = starts[e] > 0 ? 1 : 0;
+    }
+  for (int k = 0; k < n; ++k) {
+    req[k] = r0 + k;
+    cu[k + 1] = cu[k] + rows[k];
+  }
+  for (int k = 0; k <= n; ++k) ql[k] = qsl[r0 + k];
   m.rows = cu[n];
   std::memcpy(m.q_loc.data(), ql, sizeof(int32_t) * (n + 1));
   std::memcpy(m.cu_rows.data(), cu, sizeof(int32_t) * (n + 1));
@@ -395,8 +432,8 @@ bool wait_on(cudaStream_t s, cudaEvent_t e) { return cudaStreamWaitEvent(s, e, 0
 struct PrefillLayout {
   std::vector<mla_chunk_t> chunks;
   std::vector<int32_t> starts, lens, qsl;
-  std::vector<ChunkMetaHost> metas;
-  std::vector<size_t> meta_off;            // int offset of each chunk's metadata
+  std::vector<ChunkMetaHost> metas;        // one per execution group
+  std::vector<size_t> meta_off;            // int offset of each group's metadata
   std::vector<std::pair<int, int>> empty;  // token slices of context-free requests
   size_t slices_off = 0, suffix_off = 0, meta_total = 0;
   int T = 0, pnt = 0, max_rows = 0;
@@ -421,12 +458,21 @@ int build_prefill(const mla_dims_t &d, const int32_t *ctx, const int32_t *ql, in
     if (ctx[r] == 0 && lo < hi) p.empty.emplace_back(lo, hi);
   }
   size_t off = 0;
-  p.metas.resize(p.chunks.size());
-  for (size_t c = 0; c < p.chunks.size(); ++c) {
-    build_chunk_meta(p.chunks[c], p.starts.data(), p.lens.data(), p.qsl.data(), p.metas[c]);
+  for (size_t c0 = 0; c0 < p.chunks.size();) {
+    // a group ends before a continuation (its first request must see the
+    // previous chunk's result) and before the budget would overflow
+    size_t c1 = c0 + 1;
+    int64_t rows = p.chunks[c0].rows;
+    while (c1 < p.chunks.size() && !p.chunks[c1].is_continuation &&
+           rows + p.chunks[c1].rows <= budget)
+      rows += p.chunks[c1++].rows;
+    p.metas.emplace_back();
+    build_group_meta(p.chunks, c0, c1, p.starts.data(), p.lens.data(), p.qsl.data(),
+                     p.metas.back());
     p.meta_off.push_back(off);
-    off += p.metas[c].ints.size();
-    p.max_rows = std::max(p.max_rows, p.metas[c].rows);
+    off += p.metas.back().ints.size();
+    p.max_rows = std::max(p.max_rows, p.metas.back().rows);
+    c0 = c1;
   }
   p.slices_off = off;
   off += 2 * p.empty.size();
@@ -453,7 +499,7 @@ size_t carve_prefill(void *base, const mla_dims_t &d, const PrefillLayout &p,
                      PrefillBuffers &b) {
   Carve cv(base);
   b.meta = static_cast<int32_t *>(cv.take(p.meta_total * sizeof(int32_t)));
-  const int sets = p.chunks.size() > 1 ? 2 : 1;
+  const int sets = p.metas.size() > 1 ? 2 : 1;
   for (int k = 0; k < 2; ++k) {
     if (k < sets)
       carve_chunk_buffers(cv, d, p.max_rows, b.chunk[k]);
@@ -544,11 +590,15 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                               b.meta + p.slices_off, s);
   if (rc) return rc;
 
-  // The chunk pipeline.  Streams: `s` (the caller's) runs every attention and
-  // everything that writes the partial or the output, `sg` the gathers, `sm`
-  // the up-projections.  Chunk c uses buffer set c % 2: its gather waits until
-  // the attention of chunk c-2 has read that set, its up-projection follows
-  // its gather, its attention its up-projection.  So gathers never sit
+  // The chunk pipeline, over execution groups (consecutive chunks with no
+  // continuation between them and rows within the budget together, run as
+  // one gather, one up-projection and one attention: the seven small chunks
+  // of the hetero batch cost 0.67 ms as separate launches).  Streams: `s`
+  // (the caller's) runs every attention and everything that writes the
+  // partial or the output, `sg` the gathers, `sm` the up-projections.  Group c
+  // uses buffer set c % 2: its gather waits until the attention of group c-2
+  // has read that set, its up-projection follows its gather, its attention
+  // its up-projection.  So gathers never sit
   // between two GEMMs, and the up-projection of chunk c+1 fills the SMs that
   // the attention of chunk c leaves idle (its tail, or a long request's few
   // CTAs, which is also why that attention is split over its keys).  The
@@ -558,7 +608,7 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   // fewer SMs share HBM.)
   std::lock_guard<std::mutex> lock(g_pipeline_mu);
   Pipeline *pl = nullptr;
-  const size_t nc = p.chunks.size();
+  const size_t nc = p.metas.size();  // execution groups of chunks
   rc = pipeline_for_current_device(3 * nc + 4, &pl);
   if (rc) return rc;
   cudaEvent_t *ev = pl->ev.data();
@@ -583,7 +633,8 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
     if (!rc && (!record(ev_kv(c), sm) || !wait_on(s, ev_kv(c)))) rc = MLA_ERR_CUDA;
     if (!rc)
       rc = attention(*d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, cb.kv_ws,
-                     kv_dtype, m.rows, cb.latent_ws, LP, acc, b.o_part, b.lse_part, s, &b.split);
+                     kv_dtype, m.rows, cb.latent_ws, LP, acc, b.o_part, b.lse_part, s, &b.split,
+                     true);
     if (!rc && !record(ev_attn(c), s)) rc = MLA_ERR_CUDA;
   }
   // new-token up-projection, beside the last chunk's attention
@@ -602,7 +653,7 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
     // context partial is read where needed, the output written once
     return launch_attn_tc(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, T, q,
                           b.kv_suffix, new_latent, LP, nullptr, b.o_part, b.lse_part, out,
-                          out_lse, d->dtype, p.pnt, nullptr, s);
+                          out_lse, d->dtype, p.pnt, nullptr, false, s);
   }
   rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
                  kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);

@@ -590,7 +590,8 @@ struct Item {
 constexpr int kMinSplitTiles = 16;
 
 int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
-               int H, const SplitScratch *split, std::vector<Item> &items, SplitGroups &sg) {
+               int H, const SplitScratch *split, bool skip_keyless, std::vector<Item> &items,
+               SplitGroups &sg) {
   auto by_cost = [](const Item &a, const Item &b) { return a.kt1 - a.kt0 > b.kt1 - b.kt0; };
   items.clear();
   sg.n = 0;
@@ -598,6 +599,7 @@ int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_
     const int nq = q_loc_host[i + 1] - q_loc_host[i];
     const int nk = k_loc_host[i + 1] - k_loc_host[i];
     if ((nq + BQ - 1) / BQ > 0xffff) return MLA_ERR_UNSUPPORTED;  // 16-bit tile index
+    if (skip_keyless && nk == 0) continue;  // its rows already hold O=0, LSE=-inf
     for (int qt = 0; qt * BQ < nq; ++qt) {
       int tiles = (nk + BKV - 1) / BKV;
       if (causal) tiles = std::min(tiles, qt + 1);
@@ -642,7 +644,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    int T, int kv_rows, const void *q, const void *kv, const void *latent,
                    int64_t latent_ld, const int32_t *accumulate, float *o, float *lse,
                    void *final_out, float *final_lse, int final_dtype, int pnt,
-                   const SplitScratch *split, cudaStream_t s) {
+                   const SplitScratch *split, bool skip_keyless, cudaStream_t s) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
   const int H = d.num_heads;
@@ -659,7 +661,8 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
   std::vector<Item> items;
   SplitGroups sg{};
   const int rc = plan_items(causal, num_seqs, q_loc_host, k_loc_host, H,
-                            final_out == nullptr ? split : nullptr, items, sg);
+                            final_out == nullptr ? split : nullptr,
+                            skip_keyless && !causal && final_out == nullptr, items, sg);
   if (rc) return rc;
   static bool attr_set = false;
   if (!attr_set) {

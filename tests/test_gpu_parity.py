@@ -470,6 +470,28 @@ def test_prefill_key_split_and_pipeline():
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+def test_prefill_groups_small_chunks_into_one_launch_set():
+    # three chunks, separated only by context-free requests and together
+    # within the budget, run as one execution group: one gather, one
+    # up-projection and one attention launch for all of them
+    w = W.scaled(W.workload("uniform"), context_lens=[100, 0, 50, 0, 30],
+                 query_lens=[5, 7, 130, 3, 9], num_heads=4, row_budget=4096,
+                 max_context_chunk=4096, split_alignment=64, seed=52)
+    x = W.make_inputs(w)
+    n0 = M.mla_kernel_launches()
+    out, lse = _run_prefill(w, x)
+    launched = M.mla_kernel_launches() - n0
+    ro, rl, plans = _oracle_prefill(w, x)
+    assert len(plans) == 3
+    # fill of context-free rows + gather + up-projection + attention of the
+    # group + new-token up-projection + new-token attention (the tensor-core
+    # attention merges in its epilogue; otherwise one merge more)
+    assert launched == (6 if M.mla_has_tcgen05() else 7)
+    assert not torch.isnan(out).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 EDGE_CASES = {
     # no request has context: the output is the new-token attention alone
     "no_context": dict(context_lens=[0, 0, 0], query_lens=[5, 1, 130]),
