@@ -373,6 +373,37 @@ def test_varlen_attention_multi_tile(causal):
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_attention_many_short_units(causal):
+    """Many more (query tile, head) units than SMs, each of one or two key
+    tiles; context sequences without keys between them write O=0,
+    LSE=-inf; a second pass over the same keys accumulates (LSE + ln 2)."""
+    w = W.scaled(W.workload("uniform"), num_heads=64, seed=46)
+    ql = [130, 1, 200, 77, 256, 3, 129, 40]
+    kl = ql if causal else [100, 0, 250, 129, 0, 5, 256, 1]
+    q_loc = [0] + list(np.cumsum(ql))
+    k_loc = [0] + list(np.cumsum(kl))
+    q, kv, lat = _attn_inputs(w, k_loc[-1], q_loc[-1], 10, torch.float16)
+    o = torch.full((q_loc[-1], w.num_heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((w.num_heads, q_loc[-1]), float("nan"), device=DEV)
+    d = M.Dims.of(w)
+    gq, gkv, glat = q.to(DEV), kv.to(DEV), lat.to(DEV)
+    M.mla_varlen_attn(d, causal, q_loc, k_loc, gq, gkv, glat, o, lse)
+    torch.cuda.synchronize()
+    ro, rl = _oracle_attn(w, q, kv, lat, q_loc, k_loc, causal)  # keyless: O=0, LSE=-inf
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+    if not causal:
+        # the same keys again, accumulated: the result is attention over the
+        # keys twice (LSE + ln 2, same O), keyless rows unchanged
+        acc = [1] * len(ql)
+        M.mla_varlen_attn(d, False, q_loc, k_loc, gq, gkv, glat, o, lse, accumulate=acc)
+        torch.cuda.synchronize()
+        rl2 = np.where(np.isfinite(rl), rl + np.log(2.0), rl)
+        assert_close(f64(o), ro, 2e-2, 2e-2, what="O accumulated")
+        assert_close(f64(lse), rl2, 1e-3, what="LSE accumulated")
+
+
 def test_varlen_attention_accumulate():
     """Chunk 2 continues the requests of chunk 1 and merges into its partial;
     the result equals attention over both key ranges at once."""
