@@ -117,6 +117,263 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ int softmax_bar_and(int pred) {
+  // named barrier 1 over the 256 softmax threads (warps 2-9), AND of pred
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred)
+      : "memory");
+  return int(r);
+}
+
+// q_nope (Q boxes 0 and 1) to fp16 in place, to meet the fp16 K_nope in the
+// S MMA; exact for bf16 values within fp16 range.  Thread tid of nthr.
+__device__ __forceinline__ void convert_q_nope(uint8_t *sQ, int tid, int nthr) {
+  uint4 *qv = reinterpret_cast<uint4 *>(sQ);
+#pragma unroll 4
+  for (int v = tid; v < 2 * QBOX / 16; v += nthr) {
+    uint4 x = qv[v];
+    uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w4[e] = pack_f16(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
+    qv[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+  fence_async_smem();
+}
+
+// One 128-key tile of the online softmax, for one warpgroup's half (64
+// keys, the first being key k0 of the sequence) of query row qpos: S from
+// TMEM (s_col), masked past the sequence (and, causal, past the query),
+// running max in base 2 raised lazily, P as fp16 over the S columns, O
+// (o_col) rescaled when the max grew -- after the previous tile's P.V (tile
+// J-1 of the CTA) is done -- then an arrival on pfull_bar.  Returns false
+// when a wait gave up.
+__device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col, uint32_t o_col,
+                                             uint32_t sfull_bar, uint32_t sfull_parity,
+                                             uint32_t b_odone, uint32_t pfull_bar, int J,
+                                             int k0, int nk, int qpos, float &m_used, float &l,
+                                             int lane) {
+  if (!mbar_wait(sfull_bar, sfull_parity)) return false;
+  tc_fence_after();
+  float sv[HALF];  // raw scores (scale applied below)
+  {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(s_col, r0);  // both halves in flight before the wait
+    tmem_ld32(s_col + 32u, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      sv[e] = __uint_as_float(r0[e]);
+      sv[32 + e] = __uint_as_float(r1[e]);
+    }
+  }
+  // mask keys past the sequence (and, causal, past the query)
+  int valid = nk - k0;
+  if (p.causal) valid = min(valid, qpos - k0 + 1);
+  if (valid < HALF) {
+#pragma unroll
+    for (int e = 0; e < HALF; ++e)
+      if (e >= valid) sv[e] = neg_inf();
+  }
+  // row max as a tree (no serial dependency chain); scale > 0, so the
+  // max of the scaled scores is the scaled max
+  float tm[HALF / 2];
+#pragma unroll
+  for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
+#pragma unroll
+  for (int w = HALF / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
+  const float mx = tm[0] * p.scale_log2;
+  float alpha = 1.f;
+  bool rescale = false;
+  if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
+    const float m_new = fmaxf(mx, m_used);
+    if (m_used != neg_inf() && m_new != neg_inf()) {
+      alpha = exp2f(m_used - m_new);
+      rescale = true;
+    }
+    m_used = m_new;
+  }
+  const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
+  l *= alpha;
+  uint32_t pk[HALF / 2];
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+#pragma unroll
+  for (int e = 0; e < HALF / 2; ++e) {
+    const float a = ex2_approx(fmaf(sv[2 * e], p.scale_log2, nbase));
+    const float b = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, nbase));
+    ls[e & 3] += a + b;
+    pk[e] = pack_f16(a, b);
+  }
+  l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  // P over this warpgroup's own S columns (already read).  The previous
+  // tile's P.V must have finished before O is rescaled; waiting for it on
+  // every tile costs nothing (this tile's P.V runs after it anyway) and
+  // keeps the waits on the done barrier one phase apart.
+  tmem_st32(s_col, pk);
+  if (J > 0 && !mbar_wait(b_odone, uint32_t((J - 1) & 1))) return false;
+  tc_fence_after();
+  if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+    for (int c = 0; c < DV / 32; ++c) {
+      uint32_t r[32];
+      const uint32_t oc = o_col + uint32_t(c * 32);
+      tmem_ld32(oc, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+      tmem_st32(oc, r);
+    }
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(pfull_bar);
+  return true;
+}
+
+// Epilogue of one (query tile, head) unit, run by both softmax warpgroups:
+// after the unit's last P.V (odone at odone_parity), exchange the two
+// warpgroups' (max, sum) per row through xchg, merge O_A and O_B and write
+// the row -- or LSE-merge it into the stored partial (a continued request),
+// into the key-split scratch slot, or with the context partial into the
+// final output -- as the launch asks.  The softmax threads meet at one
+// barrier (named barrier 1 when kNamedBar, else all threads of the CTA).
+// b_ofree (nonzero): arrived on once the warp has read O from TMEM.
+// Returns the AND over the threads of `ok`.
+template <bool kNamedBar>
+__device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem,
+                                              uint32_t lane_off, float *xchg, uint32_t b_odone,
+                                              uint32_t odone_parity, uint32_t b_ofree, int wg,
+                                              int row, int lane, int h, int seq, int slot,
+                                              int q_beg, int nq, int qpos, int n_tiles,
+                                              float m_used, float l, bool ok) {
+  if (ok && n_tiles > 0 && !mbar_wait(b_odone, odone_parity)) ok = false;
+  float *xm = xchg, *xl = xchg + 128;        // warpgroup B's (m, l) per row
+  float *ym = xchg + 256, *yl = xchg + 384;  // warpgroup A's (m, l) per row
+  if (wg == 1) {
+    xm[row] = m_used;
+    xl[row] = l;
+  } else {
+    ym[row] = m_used;
+    yl[row] = l;
+  }
+  const int t = q_beg + qpos;
+  const int64_t li = int64_t(h) * p.T + t;
+  const bool fin = p.fout != nullptr;
+  const bool split = slot >= 0;  // a key split: its own partial goes to the scratch slot
+  const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
+  const bool merge_old = accumulate || (fin && t < p.pnt);
+  // the stored LSE is read by both warpgroups before either writes it
+  const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
+  tc_fence_before();
+  // both warpgroups' O are complete after this barrier (each waited for
+  // its own last P.V); all threads take part, the MMA warps too
+  const int okv = kNamedBar ? softmax_bar_and(ok ? 1 : 0) : __syncthreads_and(ok ? 1 : 0);
+  tc_fence_after();
+  const float mA = ym[row], lA = yl[row], mB = xm[row], lB = xl[row];
+  const float mx = fmaxf(mA, mB);
+  const float fA = (lA > 0.f) ? exp2f(mA - mx) : 0.f;  // scale of each partial
+  const float fB = (lB > 0.f) ? exp2f(mB - mx) : 0.f;
+  const float lsum = lA * fA + lB * fB;
+  const bool store = okv && qpos < nq;
+  float lse = (lsum > 0.f) ? (mx + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
+  float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
+  // this warpgroup's half of the output row, and the row's LSE
+  float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + row) * DV + wg * (DV / 2)
+                      : p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
+  float *lse_dst = split ? p.split_lse + (int64_t(slot) * p.H + h) * BQ + row : p.lse + li;
+  bool write = store;
+  if (store && merge_old) {
+    if (lsum == 0.f) {
+      if (!fin) {
+        write = false;  // nothing new: keep the stored partial
+      } else if (!is_neg_inf(old)) {
+        w_old = 1.f;  // the result is the context partial alone
+        lse = old;
+      }
+    } else if (!is_neg_inf(old)) {
+      const float m2 = fmaxf(old, lse);
+      const float eo = expf(old - m2), en = expf(lse - m2);
+      w_old = eo / (eo + en);
+      w_new *= en / (eo + en);
+      lse = m2 + logf(eo + en);
+    }
+  }
+  if (okv && n_tiles > 0) {
+    // O = (fA O_A + fB O_B) / lsum over this warpgroup's 64 columns
+    const uint32_t oa = tmem + lane_off + COL_O + uint32_t(wg * (DV / 2));
+    const uint32_t ob = oa + uint32_t(DV);
+#pragma unroll 1
+    for (int c = 0; c < DV / 2 / 16; ++c) {
+      uint32_t ra[16], rb[16];
+      tmem_ld16(oa + uint32_t(c * 16), ra);
+      tmem_ld16(ob + uint32_t(c * 16), rb);
+      tmem_wait_ld();
+      if (b_ofree != 0 && c == DV / 2 / 16 - 1) {
+        // O_A and O_B are read: the next unit's P.V may overwrite them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_ofree);
+      }
+      if (write) {
+        const float4 *src = reinterpret_cast<const float4 *>(orow + c * 16);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float a = (fA != 0.f) ? __uint_as_float(ra[4 * e + k]) * fA : 0.f;
+            const float b = (fB != 0.f) ? __uint_as_float(rb[4 * e + k]) * fB : 0.f;
+            v[k] = (a + b) * w_new;
+          }
+          float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
+          if (w_old != 0.f) {  // an unused side is never read
+            const float4 old = src[e];
+            o4.x += w_old * old.x;
+            o4.y += w_old * old.y;
+            o4.z += w_old * old.z;
+            o4.w += w_old * old.w;
+          }
+          const int64_t col = (int64_t(t) * p.H + h) * DV + wg * (DV / 2) + c * 16 + e * 4;
+          if (!fin) {
+            reinterpret_cast<float4 *>(orow + c * 16)[e] = o4;
+          } else if (p.fout_bf16) {
+            uint2 b2;
+            b2.x = pack_bf16(o4.x, o4.y);
+            b2.y = pack_bf16(o4.z, o4.w);
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + col) = b2;
+          } else {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + col) = o4;
+          }
+        }
+      }
+    }
+  } else {
+    if (b_ofree != 0 && n_tiles > 0) {  // O unread (a wait gave up): release it all the same
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_ofree);
+    }
+    if (write && n_tiles == 0 && !accumulate) {
+      for (int c = 0; c < DV / 2; c += 4)
+        *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  if (write && wg == 0) {
+    if (!fin)
+      *lse_dst = lse;
+    else if (p.flse)
+      p.flse[li] = lse;
+  }
+  return okv != 0;
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_kv,
@@ -273,7 +530,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- softmax warpgroups
-    const int wg = (warp - 2) >> 2;        // 0: A (even key tiles), 1: B (odd)
+    const int wg = (warp - 2) >> 2;        // 0: A (keys 0-63 of a tile), 1: B (64-127)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;   // query row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
@@ -281,24 +538,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m_used = neg_inf(), l = 0.f;
     bool ok = true;
     if (n_tiles > 0 && wg == 0) {
-      // q_nope (Q boxes 0 and 1) to fp16 in place, to meet the fp16 K_nope in
-      // the S MMA; exact for bf16 values within fp16 range
-      if (!mbar_wait(b_q, 0)) {
+      if (!mbar_wait(b_q, 0))
         ok = false;
-      } else {
-        const int tid = threadIdx.x - 64;
-        uint4 *qv = reinterpret_cast<uint4 *>(sQ);
-#pragma unroll 4
-        for (int v = 0; v < 2 * QBOX / 16 / 128; ++v) {
-          uint4 x = qv[v * 128 + tid];
-          uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w4[e] = pack_f16(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
-          qv[v * 128 + tid] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        fence_async_smem();
-      }
+      else
+        convert_q_nope(sQ, threadIdx.x - 64, 128);
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
     }
@@ -306,199 +549,268 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % RING;
       const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(s * BKV + wg * HALF);
-      if (!mbar_wait(b_sfull + 8 * s, uint32_t((j / RING) & 1))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sv[HALF];  // raw scores (scale applied below)
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(s_col, r0);  // both halves in flight before the wait
-        tmem_ld32(s_col + 32u, r1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[e] = __uint_as_float(r0[e]);
-          sv[32 + e] = __uint_as_float(r1[e]);
-        }
-      }
-      // mask keys past the sequence (and, causal, past the query)
-      const int k0 = (kt0 + j) * BKV + wg * HALF;   // first key of this half tile
-      int valid = nk - k0;
-      if (p.causal) valid = min(valid, qpos - k0 + 1);
-      if (valid < HALF) {
-#pragma unroll
-        for (int e = 0; e < HALF; ++e)
-          if (e >= valid) sv[e] = neg_inf();
-      }
-      // row max as a tree (no serial dependency chain); scale > 0, so the
-      // max of the scaled scores is the scaled max
-      float tm[HALF / 2];
-#pragma unroll
-      for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
-#pragma unroll
-      for (int w = HALF / 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
-      const float mx = tm[0] * p.scale_log2;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
-        const float m_new = fmaxf(mx, m_used);
-        if (m_used != neg_inf() && m_new != neg_inf()) {
-          alpha = exp2f(m_used - m_new);
-          rescale = true;
-        }
-        m_used = m_new;
-      }
-      const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
-      l *= alpha;
-      uint32_t pk[HALF / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
-#pragma unroll
-      for (int e = 0; e < HALF / 2; ++e) {
-        const float a = ex2_approx(fmaf(sv[2 * e], p.scale_log2, nbase));
-        const float b = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, nbase));
-        ls[e & 3] += a + b;
-        pk[e] = pack_f16(a, b);
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // P over this warpgroup's own S columns (already read).  The previous
-      // tile's P.V must have finished before O is rescaled; waiting for it on
-      // every tile costs nothing (this tile's P.V runs after it anyway) and
-      // keeps the waits on the done barrier one phase apart.
-      tmem_st32(s_col, pk);
-      if (j > 0 && !mbar_wait(b_odone, uint32_t((j - 1) & 1))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t r[32];
-          const uint32_t oc = o_col + uint32_t(c * 32);
-          tmem_ld32(oc, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tmem_st32(oc, r);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_pfull + 8 * wg);
+      ok = softmax_tile(p, s_col, o_col, b_sfull + 8 * s, uint32_t((j / RING) & 1), b_odone,
+                        b_pfull + 8 * wg, j, (kt0 + j) * BKV + wg * HALF, nk, qpos, m_used, l,
+                        lane);
     }
-    // ---------------- epilogue: merge the two warpgroups' partials
-    if (ok && n_tiles > 0 && !mbar_wait(b_odone, uint32_t((n_tiles - 1) & 1))) ok = false;
-    float *xm = xchg, *xl = xchg + 128;        // warpgroup B's (m, l) per row
-    float *ym = xchg + 256, *yl = xchg + 384;  // warpgroup A's (m, l) per row
-    if (wg == 1) {
-      xm[row] = m_used;
-      xl[row] = l;
-    } else {
-      ym[row] = m_used;
-      yl[row] = l;
-    }
-    const int t = q_beg + qpos;
-    const int64_t li = int64_t(h) * p.T + t;
-    const bool fin = p.fout != nullptr;
-    const bool split = slot >= 0;  // a key split: its own partial goes to the scratch slot
-    const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
-    const bool merge_old = accumulate || (fin && t < p.pnt);
-    // the stored LSE is read by both warpgroups before either writes it
-    const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
-    tc_fence_before();
-    // both warpgroups' O are complete after this barrier (each waited for
-    // its own last P.V); all threads take part, the MMA warps too
-    const int okv = __syncthreads_and(ok ? 1 : 0);
-    tc_fence_after();
-    const float mA = ym[row], lA = yl[row], mB = xm[row], lB = xl[row];
-    const float mx = fmaxf(mA, mB);
-    const float fA = (lA > 0.f) ? exp2f(mA - mx) : 0.f;  // scale of each partial
-    const float fB = (lB > 0.f) ? exp2f(mB - mx) : 0.f;
-    const float lsum = lA * fA + lB * fB;
-    const bool store = okv && qpos < nq;
-    float lse = (lsum > 0.f) ? (mx + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
-    float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
-    // this warpgroup's half of the output row, and the row's LSE
-    float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + row) * DV + wg * (DV / 2)
-                        : p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
-    float *lse_dst = split ? p.split_lse + (int64_t(slot) * p.H + h) * BQ + row : p.lse + li;
-    bool write = store;
-    if (store && merge_old) {
-      if (lsum == 0.f) {
-        if (!fin) {
-          write = false;  // nothing new: keep the stored partial
-        } else if (!is_neg_inf(old)) {
-          w_old = 1.f;  // the result is the context partial alone
-          lse = old;
-        }
-      } else if (!is_neg_inf(old)) {
-        const float m2 = fmaxf(old, lse);
-        const float eo = expf(old - m2), en = expf(lse - m2);
-        w_old = eo / (eo + en);
-        w_new *= en / (eo + en);
-        lse = m2 + logf(eo + en);
-      }
-    }
-    if (okv && n_tiles > 0) {
-      // O = (fA O_A + fB O_B) / lsum over this warpgroup's 64 columns
-      const uint32_t oa = tmem + lane_off + COL_O + uint32_t(wg * (DV / 2));
-      const uint32_t ob = oa + uint32_t(DV);
-#pragma unroll 1
-      for (int c = 0; c < DV / 2 / 16; ++c) {
-        uint32_t ra[16], rb[16];
-        tmem_ld16(oa + uint32_t(c * 16), ra);
-        tmem_ld16(ob + uint32_t(c * 16), rb);
-        tmem_wait_ld();
-        if (write) {
-          const float4 *src = reinterpret_cast<const float4 *>(orow + c * 16);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float a = (fA != 0.f) ? __uint_as_float(ra[4 * e + k]) * fA : 0.f;
-              const float b = (fB != 0.f) ? __uint_as_float(rb[4 * e + k]) * fB : 0.f;
-              v[k] = (a + b) * w_new;
-            }
-            float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
-            if (w_old != 0.f) {  // an unused side is never read
-              const float4 old = src[e];
-              o4.x += w_old * old.x;
-              o4.y += w_old * old.y;
-              o4.z += w_old * old.z;
-              o4.w += w_old * old.w;
-            }
-            const int64_t col = (int64_t(t) * p.H + h) * DV + wg * (DV / 2) + c * 16 + e * 4;
-            if (!fin) {
-              reinterpret_cast<float4 *>(orow + c * 16)[e] = o4;
-            } else if (p.fout_bf16) {
-              uint2 b2;
-              b2.x = pack_bf16(o4.x, o4.y);
-              b2.y = pack_bf16(o4.z, o4.w);
-              *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + col) = b2;
-            } else {
-              *reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + col) = o4;
-            }
-          }
-        }
-      }
-    } else if (write && n_tiles == 0 && !accumulate) {
-      for (int c = 0; c < DV / 2; c += 4)
-        *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (write && wg == 0) {
-      if (!fin)
-        *lse_dst = lse;
-      else if (p.flse)
-        p.flse[li] = lse;
-    }
+    unit_epilogue<false>(p, tmem, lane_off, xchg, b_odone, uint32_t((n_tiles - 1) & 1), 0u, wg,
+                         row, lane, h, seq, slot, q_beg, nq, qpos, n_tiles, m_used, l, ok);
   }
   if (warp < 2) __syncthreads_and(1);  // matches the softmax warps' vote
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// The same attention for launches of many short units (a few key tiles per
+// (query tile, head)): a CTA per SM walks its units u = blockIdx.x,
+// + gridDim.x, ... in turn, keeping its barriers and TMEM.  The barriers
+// count on across units (key tile J is the CTA's J-th over all its units, a
+// unit with key tiles its kq-th such unit), and a converter warp (warp 10)
+// turns each unit's q_nope to fp16 as soon as it lands, so the next unit's
+// Q and K/V loads and its S MMAs overlap this unit's softmax and epilogue.
+// Barriers beyond the per-unit kernel: qfree (the unit's last S MMA is done
+// with Q) and ofree (the epilogue warps have read O_A, O_B).
+constexpr int THREADS_LOOP = THREADS + 32;
+constexpr int SMEM_BYTES_LOOP = SMEM_BYTES + XCHG_BYTES;  // xchg per unit parity
+
+__global__ void __launch_bounds__(THREADS_LOOP, 1)
+    attn_tc_loop_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_kv,
+                        const __grid_constant__ CUtensorMap tm_lat,
+                        const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sQ = smem;
+  uint8_t *sK = sQ + Q_BYTES;
+  uint8_t *sV = sK + RING * K_BYTES;
+  float *xchg0 = reinterpret_cast<float *>(sV + RING * V_BYTES);  // [2 unit parities][4][128]
+  uint64_t *bars =
+      reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg0) + 2 * XCHG_BYTES);
+  const uint32_t b_q = smem_u32(bars + 0), b_qready = smem_u32(bars + 1);
+  const uint32_t b_kfull = smem_u32(bars + 2), b_kempty = smem_u32(bars + 2 + RING);
+  const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
+  const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);  // [2]: per S buffer
+  const uint32_t b_pfull = b_sfull + 16;                    // [2]: per warpgroup
+  const uint32_t b_odone = b_sfull + 32, b_done = b_sfull + 40;
+  const uint32_t b_qfree = b_sfull + 48, b_ofree = b_sfull + 56;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_units = p.n_items * p.H;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    mbar_init(b_qready, 1);
+    for (int s = 0; s < RING; ++s) {
+      mbar_init(b_kfull + 8 * s, 1);
+      mbar_init(b_kempty + 8 * s, 1);
+      mbar_init(b_vfull + 8 * s, 1);
+      mbar_init(b_vempty + 8 * s, 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(b_sfull + 8 * w, 1);
+      mbar_init(b_pfull + 8 * w, 4);
+    }
+    mbar_init(b_odone, 1);
+    mbar_init(b_done, 1);
+    mbar_init(b_qfree, 1);
+    mbar_init(b_ofree, 8);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  struct Unit {
+    int h, seq, qt, slot, kt0, n_tiles;
+  };
+  auto unit_of = [&](int u) {
+    Unit x;
+    x.h = u / p.n_items;
+    const int4 it = p.items[u - x.h * p.n_items];
+    x.seq = it.x;
+    x.qt = it.y & 0xffff;
+    x.slot = (it.y >> 16) - 1;
+    x.kt0 = it.z;
+    x.n_tiles = it.w - it.z;
+    return x;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      prefetch_map(&tm_q);
+      prefetch_map(&tm_kv);
+      prefetch_map(&tm_lat);
+      int k_issued[RING], v_issued[RING], q_issued = -1;
+      for (int s = 0; s < RING; ++s) k_issued[s] = v_issued[s] = -1;
+      int J = 0, kq = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit x = unit_of(u);
+        if (x.n_tiles <= 0) continue;
+        const int q_beg = __ldg(p.q_loc + x.seq), k_beg = __ldg(p.k_loc + x.seq);
+        // the previous unit's S MMAs are done with the Q tile
+        if (kq > 0 && !mbar_wait(b_qfree, uint32_t((kq - 1) & 1))) break;
+        const int qrow = q_beg + x.qt * BQ;
+        mbar_expect_tx(b_q, Q_BYTES);
+        tma_load_2d(smem_u32(sQ), &tm_q, b_q, x.h * DQK, qrow);
+        tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, x.h * DQK + 64, qrow);
+        tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, x.h * DQK + 128, qrow);
+        q_issued = kq & 1;
+        ++kq;
+        for (int j = 0; j < x.n_tiles; ++j, ++J) {
+          const int s = J % RING;
+          const uint32_t use = uint32_t(J / RING);        // use count of slot s
+          const int krow = k_beg + (x.kt0 + j) * BKV;
+          if (J >= RING && !mbar_wait(b_kempty + 8 * s, (use - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t *k = sK + s * K_BYTES;
+          mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
+          tma_load_3d(smem_u32(k), &tm_kv, b_kfull + 8 * s, 0, krow, x.h);
+          tma_load_3d(smem_u32(k + KBOX), &tm_kv, b_kfull + 8 * s, 64, krow, x.h);
+          tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, b_kfull + 8 * s, 512, krow);
+          k_issued[s] = int(use & 1);
+          if (J >= RING && !mbar_wait(b_vempty + 8 * s, (use - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t *v = sV + s * V_BYTES;
+          mbar_expect_tx(b_vfull + 8 * s, V_BYTES);
+          tma_load_3d(smem_u32(v), &tm_kv, b_vfull + 8 * s, DN, krow, x.h);
+          tma_load_3d(smem_u32(v + KBOX), &tm_kv, b_vfull + 8 * s, DN + 64, krow, x.h);
+          v_issued[s] = int(use & 1);
+        }
+      }
+      // every issued load has landed before the CTA may exit
+      if (q_issued >= 0) mbar_wait(b_q, uint32_t(q_issued));
+      for (int s = 0; s < RING; ++s) {
+        if (k_issued[s] >= 0) mbar_wait(b_kfull + 8 * s, uint32_t(k_issued[s]));
+        if (v_issued[s] >= 0) mbar_wait(b_vfull + 8 * s, uint32_t(v_issued[s]));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc_nope = idesc_f16kind(BQ, BKV, false, false, false);  // fp16
+      constexpr uint32_t idesc_rope = idesc_f16kind(BQ, BKV, false, false, true);   // bf16
+      constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
+      const uint32_t q_addr = smem_u32(sQ);
+      int J0 = 0, kq = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit x = unit_of(u);
+        const int n_tiles = x.n_tiles;
+        if (n_tiles <= 0) continue;
+        if (!mbar_wait(b_qready, uint32_t(kq & 1))) break;
+        // S for key tile J into S buffer J & 1 (which held P of tile J-2,
+        // whose P.V MMAs were issued before); after the unit's last S the
+        // Q tile is released
+        auto issue_s = [&](int j) -> bool {
+          const int J = J0 + j, s = J % RING;
+          if (!mbar_wait(b_kfull + 8 * s, uint32_t((J / RING) & 1))) return false;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sK + s * K_BYTES);
+          const uint32_t d = tmem + COL_S + uint32_t(s * BKV);
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t off = uint32_t((kk >> 2) * QBOX + (kk & 3) * 32);
+            mma_bf16(d, desc_kmajor_sw128(q_addr + off), desc_kmajor_sw128(k_addr + off),
+                     kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
+          }
+          mma_commit(b_sfull + 8 * s);
+          mma_commit(b_kempty + 8 * s);
+          if (j == n_tiles - 1) mma_commit(b_qfree);
+          return true;
+        };
+        ok = issue_s(0);
+        if (ok && n_tiles > 1) ok = issue_s(1);
+        // the previous unit's epilogue has read O_A and O_B
+        if (ok && kq > 0 && !mbar_wait(b_ofree, uint32_t((kq - 1) & 1))) ok = false;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int J = J0 + j, s = J % RING;
+          if (!mbar_wait(b_vfull + 8 * s, uint32_t((J / RING) & 1))) {
+            ok = false;
+            break;
+          }
+          const uint32_t v_addr = smem_u32(sV + s * V_BYTES);
+          for (int w = 0; w < 2 && ok; ++w) {
+            if (!mbar_wait(b_pfull + 8 * w, uint32_t(J & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t pa = tmem + COL_S + uint32_t(s * BKV + w * HALF);
+            const uint32_t vb = v_addr + uint32_t(w * HALF * 128);
+            const uint32_t od = tmem + COL_O + uint32_t(w * DV);
+#pragma unroll
+            for (int kk = 0; kk < HALF / 16; ++kk)
+              mma_f16_ts(od, pa + uint32_t(kk * 8),
+                         desc_mnmajor_sw128(vb + uint32_t(kk * 2048), KBOX), idesc_o,
+                         (j | kk) != 0);
+          }
+          if (!ok) break;
+          mma_commit(b_odone);
+          mma_commit(b_vempty + 8 * s);
+          if (j + 2 < n_tiles) ok = issue_s(j + 2);
+        }
+        J0 += n_tiles;
+        ++kq;
+      }
+      mma_commit(b_done);
+      mbar_wait(b_done, 0);
+    }
+  } else if (warp == THREADS / 32) {
+    // ---------------- Q converter (warp 10)
+    int kq = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const Unit x = unit_of(u);
+      if (x.n_tiles <= 0) continue;
+      const bool ok = mbar_wait(b_q, uint32_t(kq & 1));
+      if (ok) convert_q_nope(sQ, lane, 32);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qready);
+      ++kq;
+      if (!ok) break;
+    }
+  } else {
+    // ---------------- softmax warpgroups
+    const int wg = (warp - 2) >> 2;        // 0: A (keys 0-63 of a tile), 1: B (64-127)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;   // query row of the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const uint32_t o_col = tmem + lane_off + COL_O + uint32_t(wg * DV);
+    int J0 = 0, ku = 0;                    // key tiles and units so far
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++ku) {
+      const Unit x = unit_of(u);
+      const int q_beg = __ldg(p.q_loc + x.seq), nq = __ldg(p.q_loc + x.seq + 1) - q_beg;
+      const int nk = __ldg(p.k_loc + x.seq + 1) - __ldg(p.k_loc + x.seq);
+      const int qpos = x.qt * BQ + row;    // position within the sequence
+      float m_used = neg_inf(), l = 0.f;
+      for (int j = 0; ok && j < x.n_tiles; ++j) {
+        const int J = J0 + j, s = J % RING;
+        const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(s * BKV + wg * HALF);
+        ok = softmax_tile(p, s_col, o_col, b_sfull + 8 * s, uint32_t((J / RING) & 1), b_odone,
+                          b_pfull + 8 * wg, J, (x.kt0 + j) * BKV + wg * HALF, nk, qpos, m_used,
+                          l, lane);
+      }
+      ok = unit_epilogue<true>(p, tmem, lane_off, xchg0 + (ku & 1) * (XCHG_BYTES / 4), b_odone,
+                               uint32_t((J0 + x.n_tiles - 1) & 1), b_ofree, wg, row, lane, x.h,
+                               x.seq, x.slot, q_beg, nq, qpos, x.n_tiles, m_used, l, ok);
+      if (x.n_tiles > 0) J0 += x.n_tiles;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -588,6 +900,9 @@ struct Item {
   int seq, qt, kt0, kt1, slot;
 };
 constexpr int kMinSplitTiles = 16;
+// launches whose items average at most this many key tiles run on the
+// looping kernel (one CTA per SM walking its units)
+constexpr int kLoopTiles = 4;
 
 int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
                int H, const SplitScratch *split, bool skip_keyless, std::vector<Item> &items,
@@ -667,7 +982,9 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+                             SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_tc_loop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES_LOOP) != cudaSuccess)
       return MLA_ERR_CUDA;
     attr_set = true;
   }
@@ -694,7 +1011,16 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
       const Item &it = items[b + k];
       prm.items[k] = make_int4(it.seq, it.qt | ((it.slot + 1) << 16), it.kt0, it.kt1);
     }
-    attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES, s>>>(tq, tkv, tlat, prm);
+    // many short units: one CTA per SM walks them (the next unit's loads and
+    // S MMAs overlapping this one's softmax and epilogue); otherwise a CTA
+    // per unit, so that a kernel running beside this one gets SMs as they
+    // retire
+    int64_t tiles = 0;
+    for (int k = 0; k < n; ++k) tiles += items[b + k].kt1 - items[b + k].kt0;
+    if (int64_t(n) * H > num_sms() && tiles <= int64_t(kLoopTiles) * n)
+      attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, prm);
+    else
+      attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES, s>>>(tq, tkv, tlat, prm);
     const int rc = launch_status();
     if (rc) return rc;
   }
