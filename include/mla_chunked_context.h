@@ -336,9 +336,10 @@ int mla_prefill_workspace_bytes(const mla_dims_t *d,
  *   and every write of out/out_lse stay on `stream`.  All of it is ordered
  *   after the work already on `stream` (an event recorded there), and
  *   `stream` waits for all of it before the call's last kernel, so to the
- *   caller the call behaves like work enqueued on `stream` alone (also under
- *   stream capture).  Calls from several host threads are serialised while
- *   they enqueue.  The workspace holds two chunk buffer sets and the
+ *   caller the call behaves like work enqueued on `stream` alone.  (Not for
+ *   stream capture: the metadata upload is a copy from pageable host
+ *   memory.)  Calls from several host threads are serialised while they
+ *   enqueue.  The workspace holds two chunk buffer sets and the
  *   key-split scratch of the context attention.
  */
 int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
