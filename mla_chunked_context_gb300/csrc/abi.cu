@@ -429,6 +429,45 @@ int pipeline_for_current_device(size_t events, Pipeline **out) {
 bool record(cudaEvent_t e, cudaStream_t s) { return cudaEventRecord(e, s) == cudaSuccess; }
 bool wait_on(cudaStream_t s, cudaEvent_t e) { return cudaStreamWaitEvent(s, e, 0) == cudaSuccess; }
 
+// The two-buffer pipeline of the chunked paths.  For units c = 0..n-1:
+// gather(c, stream) on the gather side stream once consume(c-2) has released
+// buffer set c % 2, up(c, stream) on the GEMM side stream after it, and
+// consume(c, stream) on the caller's stream `s` after that; then tail(stream)
+// on the GEMM side stream (the new tokens' up-projection, beside the last
+// consume).  Both side streams start after the work already on `s` and are
+// joined back into `s` before returning, also after an error (the caller may
+// free the workspace once `s` has passed this point).  The side streams run
+// at the highest priority, so a GEMM takes SMs as soon as attention CTAs
+// retire.  Holds g_pipeline_mu while it enqueues.
+template <class Gather, class Up, class Consume, class Tail>
+int run_pipeline(cudaStream_t s, size_t n, Gather gather, Up up, Consume consume, Tail tail) {
+  std::lock_guard<std::mutex> lock(g_pipeline_mu);
+  Pipeline *pl = nullptr;
+  int rc = pipeline_for_current_device(3 * n + 3, &pl);
+  if (rc) return rc;
+  cudaEvent_t *ev = pl->ev.data();
+  const cudaStream_t sg = pl->gather, sm = pl->gemm;
+  auto ev_lat = [&](size_t c) { return ev[1 + 3 * c]; };
+  auto ev_kv = [&](size_t c) { return ev[2 + 3 * c]; };
+  auto ev_used = [&](size_t c) { return ev[3 + 3 * c]; };
+  cudaEvent_t ev_tail = ev[1 + 3 * n], ev_join = ev[2 + 3 * n];
+  if (!record(ev[0], s) || !wait_on(sg, ev[0]) || !wait_on(sm, ev[0])) return MLA_ERR_CUDA;
+  for (size_t c = 0; c < n && rc == MLA_OK; ++c) {
+    if (c >= 2 && !wait_on(sg, ev_used(c - 2))) rc = MLA_ERR_CUDA;
+    if (!rc) rc = gather(c, sg);
+    if (!rc && (!record(ev_lat(c), sg) || !wait_on(sm, ev_lat(c)))) rc = MLA_ERR_CUDA;
+    if (!rc) rc = up(c, sm);
+    if (!rc && (!record(ev_kv(c), sm) || !wait_on(s, ev_kv(c)))) rc = MLA_ERR_CUDA;
+    if (!rc) rc = consume(c, s);
+    if (!rc && !record(ev_used(c), s)) rc = MLA_ERR_CUDA;
+  }
+  if (!rc) rc = tail(sm);
+  const bool joined = record(ev_tail, sm) && record(ev_join, sg) && wait_on(s, ev_tail) &&
+                      wait_on(s, ev_join);
+  if (rc) return rc;
+  return joined ? MLA_OK : MLA_ERR_CUDA;
+}
+
 struct PrefillLayout {
   std::vector<mla_chunk_t> chunks;
   std::vector<int32_t> starts, lens, qsl;
@@ -590,61 +629,51 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                               b.meta + p.slices_off, s);
   if (rc) return rc;
 
-  // The chunk pipeline, over execution groups (consecutive chunks with no
-  // continuation between them and rows within the budget together, run as
-  // one gather, one up-projection and one attention: the seven small chunks
-  // of the hetero batch cost 0.67 ms as separate launches).  Streams: `s`
-  // (the caller's) runs every attention and everything that writes the
-  // partial or the output, `sg` the gathers, `sm` the up-projections.  Group c
-  // uses buffer set c % 2: its gather waits until the attention of group c-2
-  // has read that set, its up-projection follows its gather, its attention
-  // its up-projection.  So gathers never sit
-  // between two GEMMs, and the up-projection of chunk c+1 fills the SMs that
-  // the attention of chunk c leaves idle (its tail, or a long request's few
-  // CTAs, which is also why that attention is split over its keys).  The
-  // side streams have the higher priority, so a GEMM takes SMs as soon as
-  // attention CTAs retire.  (Capping the GEMM at a share of the SMs, to run
-  // the two side by side, was slower: its per-SM rate does not grow when
-  // fewer SMs share HBM.)
-  std::lock_guard<std::mutex> lock(g_pipeline_mu);
-  Pipeline *pl = nullptr;
-  const size_t nc = p.metas.size();  // execution groups of chunks
-  rc = pipeline_for_current_device(3 * nc + 4, &pl);
+  // The chunk pipeline (run_pipeline) over execution groups: consecutive
+  // chunks with no continuation between them and rows within the budget
+  // together run as one gather, one up-projection and one attention (the
+  // seven small chunks of the hetero batch cost 0.67 ms as separate
+  // launches).  Group c uses buffer set c % 2, so the up-projection of group
+  // c+1 fills the SMs that the attention of group c leaves idle (its tail, or
+  // a long request's few CTAs, which is also why that attention is split over
+  // its keys).  (Capping the GEMM at a share of the SMs, to run the two side
+  // by side, was slower: its per-SM rate does not grow when fewer SMs share
+  // HBM.)
+  auto meta_of = [&](size_t c, const int32_t *&req, const int32_t *&st, const int32_t *&cu,
+                     const int32_t *&ql, const int32_t *&acc) {
+    const int n = p.metas[c].n;
+    req = b.meta + p.meta_off[c];
+    st = req + n;
+    cu = st + n;
+    ql = cu + n + 1;
+    acc = ql + n + 1;
+  };
+  rc = run_pipeline(
+      s, p.metas.size(),
+      [&](size_t c, cudaStream_t st_) {
+        const int32_t *req, *st, *cu, *ql, *acc;
+        meta_of(c, req, st, cu, ql, acc);
+        return launch_gather(kv_cache, num_blocks, d->block_size, LP * es, block_table,
+                             block_table_stride, p.metas[c].n, req, st, cu, p.metas[c].rows,
+                             b.chunk[c & 1].latent_ws, dev_status, st_);
+      },
+      [&](size_t c, cudaStream_t st_) {
+        return up_proj(*d, b.chunk[c & 1].latent_ws, LP, p.metas[c].rows, w_kv_b,
+                       b.chunk[c & 1].kv_ws, kv_dtype, st_);
+      },
+      [&](size_t c, cudaStream_t st_) {
+        const ChunkMetaHost &m = p.metas[c];
+        const int32_t *req, *st, *cu, *ql, *acc;
+        meta_of(c, req, st, cu, ql, acc);
+        return attention(*d, 0, m.n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
+                         b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
+                         acc, b.o_part, b.lse_part, st_, &b.split, true);
+      },
+      // new-token up-projection, beside the last group's attention
+      [&](cudaStream_t st_) {
+        return up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, st_);
+      });
   if (rc) return rc;
-  cudaEvent_t *ev = pl->ev.data();
-  const cudaStream_t sg = pl->gather, sm = pl->gemm;
-  auto ev_lat = [&](size_t c) { return ev[1 + 3 * c]; };
-  auto ev_kv = [&](size_t c) { return ev[2 + 3 * c]; };
-  auto ev_attn = [&](size_t c) { return ev[3 + 3 * c]; };
-  cudaEvent_t ev_new = ev[1 + 3 * nc], ev_join = ev[2 + 3 * nc];
-  if (!record(ev[0], s) || !wait_on(sg, ev[0]) || !wait_on(sm, ev[0])) return MLA_ERR_CUDA;
-  for (size_t c = 0; c < nc && rc == MLA_OK; ++c) {
-    const ChunkMetaHost &m = p.metas[c];
-    const ChunkBuffers &cb = b.chunk[c & 1];
-    const int n = m.n;
-    const int32_t *req = b.meta + p.meta_off[c], *st = req + n, *cu = st + n, *ql = cu + n + 1,
-                  *acc = ql + n + 1;
-    if (c >= 2 && !wait_on(sg, ev_attn(c - 2))) rc = MLA_ERR_CUDA;
-    if (!rc)
-      rc = launch_gather(kv_cache, num_blocks, d->block_size, LP * es, block_table,
-                         block_table_stride, n, req, st, cu, m.rows, cb.latent_ws, dev_status, sg);
-    if (!rc && (!record(ev_lat(c), sg) || !wait_on(sm, ev_lat(c)))) rc = MLA_ERR_CUDA;
-    if (!rc) rc = up_proj(*d, cb.latent_ws, LP, m.rows, w_kv_b, cb.kv_ws, kv_dtype, sm);
-    if (!rc && (!record(ev_kv(c), sm) || !wait_on(s, ev_kv(c)))) rc = MLA_ERR_CUDA;
-    if (!rc)
-      rc = attention(*d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, cb.kv_ws,
-                     kv_dtype, m.rows, cb.latent_ws, LP, acc, b.o_part, b.lse_part, s, &b.split,
-                     true);
-    if (!rc && !record(ev_attn(c), s)) rc = MLA_ERR_CUDA;
-  }
-  // new-token up-projection, beside the last chunk's attention
-  if (!rc) rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, sm);
-  // join the side streams back into the caller's stream, also after an error
-  // (the caller may free the workspace once its stream has passed this point)
-  const bool joined = record(ev_new, sm) && record(ev_join, sg) && wait_on(s, ev_new) &&
-                      wait_on(s, ev_join);
-  if (rc) return rc;
-  if (!joined) return MLA_ERR_CUDA;
 
   const int32_t *sq = b.meta + p.suffix_off;
   if (tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
@@ -774,7 +803,7 @@ int build_equal_window(const int32_t *ctx, const int32_t *ql, int R, int budget,
 
 struct EqualWindowBuffers {
   int32_t *meta;
-  ChunkBuffers chunk;
+  ChunkBuffers chunk[2];  // chunk c uses set c % 2 (the same pipeline as the new path)
   void *kv_suffix;
   float *o_run[2], *lse_run[2];  // running partial, ping-ponged per chunk
   float *o_chunk, *lse_chunk, *o_suf, *lse_suf;
@@ -784,8 +813,14 @@ size_t carve_equal_window(void *base, const mla_dims_t &d, const EqualWindowLayo
                           EqualWindowBuffers &b) {
   Carve cv(base);
   b.meta = static_cast<int32_t *>(cv.take(p.meta_total * sizeof(int32_t)));
-  carve_chunk_buffers(cv, d, p.max_rows, b.chunk);
-  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk.kv_dtype));
+  const int sets = p.n_chunks > 1 ? 2 : 1;
+  for (int k = 0; k < 2; ++k) {
+    if (k < sets)
+      carve_chunk_buffers(cv, d, p.max_rows, b.chunk[k]);
+    else
+      b.chunk[k] = b.chunk[0];
+  }
+  b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk[0].kv_dtype));
   const size_t o_bytes = size_t(p.T) * d.num_heads * d.v_dim * sizeof(float);
   const size_t l_bytes = size_t(p.T) * d.num_heads * sizeof(float);
   for (int k = 0; k < 2; ++k) {
@@ -870,36 +905,46 @@ extern "C" int mla_chunked_prefill_equal_window(
   // the running partial starts empty: O = 0, LSE = -inf
   rc = launch_fill_empty_rows(b.o_run[0], b.lse_run[0], T, H, Dv, 1, b.meta + p.slice_off, s);
   if (rc) return rc;
-  for (int c = 0; c < p.n_chunks; ++c) {
-    const ChunkMetaHost &m = p.metas[c];
-    const int32_t *req = b.meta + p.meta_off[c], *st = req + R, *cu = st + R, *ql = cu + R + 1;
-    if (m.rows > 0) {
-      rc = launch_gather(kv_cache, num_blocks, d->block_size, LP * es, block_table,
-                         block_table_stride, R, req, st, cu, m.rows, b.chunk.latent_ws,
-                         dev_status, s);
-      if (rc) return rc;
-      rc = up_proj(*d, b.chunk.latent_ws, LP, m.rows, w_kv_b, b.chunk.kv_ws, b.chunk.kv_dtype, s);
-      if (rc) return rc;
-    }
-    rc = attention(*d, 0, R, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.chunk.kv_ws,
-                   b.chunk.kv_dtype, m.rows, b.chunk.latent_ws, LP, nullptr, b.o_chunk,
-                   b.lse_chunk, s);
-    if (rc) return rc;
-    if (p.has_empty[c]) {
-      rc = launch_mask_empty_context(b.lse_chunk, b.o_chunk, MLA_DTYPE_F32, T, H, Dv, R, ql, cu,
-                                     s);
-      if (rc) return rc;
-    }
-    rc = launch_merge(b.o_run[(c + 1) & 1], b.lse_run[(c + 1) & 1], b.o_run[c & 1],
-                      b.lse_run[c & 1], b.o_chunk, b.lse_chunk, T, H, Dv, T, MLA_DTYPE_F32,
-                      MLA_DTYPE_F32, s);
-    if (rc) return rc;
-  }
-  rc = up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, b.chunk.kv_dtype, s);
+  const int kv_dtype = b.chunk[0].kv_dtype;
+  // the chunks run through the same two-buffer pipeline as the new path, so
+  // the two schemes differ in their chunks, not in how a chunk is executed
+  rc = run_pipeline(
+      s, size_t(p.n_chunks),
+      [&](size_t c, cudaStream_t st_) {
+        const ChunkMetaHost &m = p.metas[c];
+        const int32_t *req = b.meta + p.meta_off[c], *st = req + R, *cu = st + R;
+        if (m.rows == 0) return int(MLA_OK);
+        return launch_gather(kv_cache, num_blocks, d->block_size, LP * es, block_table,
+                             block_table_stride, R, req, st, cu, m.rows,
+                             b.chunk[c & 1].latent_ws, dev_status, st_);
+      },
+      [&](size_t c, cudaStream_t st_) {
+        return up_proj(*d, b.chunk[c & 1].latent_ws, LP, p.metas[c].rows, w_kv_b,
+                       b.chunk[c & 1].kv_ws, kv_dtype, st_);
+      },
+      [&](size_t c, cudaStream_t st_) {
+        const ChunkMetaHost &m = p.metas[c];
+        const int32_t *req = b.meta + p.meta_off[c], *st = req + R, *cu = st + R,
+                      *ql = cu + R + 1;
+        int r = attention(*d, 0, R, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
+                          b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
+                          nullptr, b.o_chunk, b.lse_chunk, st_);
+        if (!r && p.has_empty[c])
+          r = launch_mask_empty_context(b.lse_chunk, b.o_chunk, MLA_DTYPE_F32, T, H, Dv, R, ql,
+                                        cu, st_);
+        if (!r)
+          r = launch_merge(b.o_run[(c + 1) & 1], b.lse_run[(c + 1) & 1], b.o_run[c & 1],
+                           b.lse_run[c & 1], b.o_chunk, b.lse_chunk, T, H, Dv, T, MLA_DTYPE_F32,
+                           MLA_DTYPE_F32, st_);
+        return r;
+      },
+      [&](cudaStream_t st_) {
+        return up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, st_);
+      });
   if (rc) return rc;
   const int32_t *sq = b.meta + p.suffix_off;
   rc = attention(*d, 1, R, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 b.chunk.kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
   if (rc) return rc;
   const int fin = p.n_chunks & 1;  // the buffer the last chunk merged into
   return launch_merge(out, out_lse, b.o_run[fin], b.lse_run[fin], b.o_suf, b.lse_suf, T, H, Dv,
