@@ -338,7 +338,7 @@ static inline int take_error_flags_here() {
 
 // Host: encode a 2-D tensor map of 16-bit elements (bf16 or fp16; dim0
 // contiguous), optionally with the 128-byte swizzle, zero fill out of
-// bounds.  Returns false when the driver rejects it.
+// bounds.  Returns false when cuTensorMapEncodeTiled rejects it.
 bool make_tmap_2d_16(CUtensorMap *map, bool fp16, const void *base, uint64_t dim0, uint64_t dim1,
                      uint64_t row_stride_bytes, uint32_t box0, uint32_t box1, bool swizzle128);
 // 3-D variant (dim0 contiguous; box depth 1 along dim2).

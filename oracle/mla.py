@@ -17,7 +17,7 @@ Sources
   past the threshold copy the suffix, the others merge prefix and suffix.
 * The MLA arithmetic itself (latent cache, W_kv_b up-projection into K_nope
   and V, attention over concat(K_nope, k_pe), causal new-token attention) is
-  not written on the pages; the plainest reading is used (the design doc lists it):
+  not written on the pages; the plainest reading is used:
   cache row = [c_kv (kv_lora_rank) | k_pe (qk_rope_dim)], W_kv_b is
   [H*(Dn+Dv), kv_lora_rank] with head h's rows [h*(Dn+Dv), h*(Dn+Dv)+Dn)
   giving K_nope and the next Dv rows giving V; q = [q_nope | q_pe]; natural

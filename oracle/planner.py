@@ -15,7 +15,7 @@ request that overflows is cut at the largest aligned length that still fits
 (the rest of it opens the next chunk, which is then a "continuation"), and the
 chunk is closed.
 
-Readings taken where the page is silent or garbled (all listed in the design doc):
+Readings taken where the page is silent or garbled:
 
 * An overflowing request whose aligned split is empty (no aligned length fits
   in the rows left) closes the chunk without being appended; it opens the next
