@@ -145,6 +145,22 @@ __device__ __forceinline__ void convert_q_nope(uint8_t *sQ, int tid, int nthr) {
   fence_async_smem();
 }
 
+// Brings the half row of the stored partial that the epilogue will merge
+// with (a continued request, or the context partial in final-merge mode)
+// into L2 while the unit computes, instead of leaving the epilogue to wait
+// on it from HBM.
+__device__ __forceinline__ void prefetch_partial(const AttnParams &p, int h, int seq, int slot,
+                                                 int q_beg, int nq, int qpos, int wg) {
+  if (qpos >= nq || slot >= 0) return;
+  const int t = q_beg + qpos;
+  const bool fin = p.fout != nullptr;
+  const bool acc = !fin && p.acc != nullptr && __ldg(p.acc + seq) != 0;
+  if (!acc && !(fin && t < p.pnt)) return;
+  const float *row = p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 32));
+}
+
 // One 128-key tile of the online softmax, for one warpgroup's half (64
 // keys, the first being key k0 of the sequence) of query row qpos: S from
 // TMEM (s_col), masked past the sequence (and, causal, past the query),
@@ -545,6 +561,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
     }
+    prefetch_partial(p, h, seq, slot, q_beg, nq, qpos, wg);
     const uint32_t o_col = tmem + lane_off + COL_O + uint32_t(wg * DV);
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % RING;
@@ -632,10 +649,16 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   struct Unit {
     int h, seq, qt, slot, kt0, n_tiles;
   };
+  // units item-major (the items come longest first), the CTA's k-th unit
+  // taken from the k-th block of gridDim.x units in zigzag order, so the
+  // long items spread over the CTAs
+  const int G = int(gridDim.x), b = int(blockIdx.x);
+  auto unit_at = [&](int k) { return k * G + ((k & 1) ? G - 1 - b : b); };
   auto unit_of = [&](int u) {
     Unit x;
-    x.h = u / p.n_items;
-    const int4 it = p.items[u - x.h * p.n_items];
+    const int item = u / p.H;
+    x.h = u - item * p.H;
+    const int4 it = p.items[item];
     x.seq = it.x;
     x.qt = it.y & 0xffff;
     x.slot = (it.y >> 16) - 1;
@@ -654,7 +677,9 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       for (int s = 0; s < RING; ++s) k_issued[s] = v_issued[s] = -1;
       int J = 0, kq = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= n_units) break;
         const Unit x = unit_of(u);
         if (x.n_tiles <= 0) continue;
         const int q_beg = __ldg(p.q_loc + x.seq), k_beg = __ldg(p.k_loc + x.seq);
@@ -708,7 +733,9 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       const uint32_t q_addr = smem_u32(sQ);
       int J0 = 0, kq = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= n_units) break;
         const Unit x = unit_of(u);
         const int n_tiles = x.n_tiles;
         if (n_tiles <= 0) continue;
@@ -773,7 +800,9 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   } else if (warp == THREADS / 32) {
     // ---------------- Q converter (warp 10)
     int kq = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (int k = 0;; ++k) {
+      const int u = unit_at(k);
+      if (u >= n_units) break;
       const Unit x = unit_of(u);
       if (x.n_tiles <= 0) continue;
       const bool ok = mbar_wait(b_q, uint32_t(kq & 1));
@@ -792,12 +821,15 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
     const uint32_t o_col = tmem + lane_off + COL_O + uint32_t(wg * DV);
     int J0 = 0, ku = 0;                    // key tiles and units so far
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++ku) {
+    for (int k = 0;; ++k, ++ku) {
+      const int u = unit_at(k);
+      if (u >= n_units) break;
       const Unit x = unit_of(u);
       const int q_beg = __ldg(p.q_loc + x.seq), nq = __ldg(p.q_loc + x.seq + 1) - q_beg;
       const int nk = __ldg(p.k_loc + x.seq + 1) - __ldg(p.k_loc + x.seq);
       const int qpos = x.qt * BQ + row;    // position within the sequence
       float m_used = neg_inf(), l = 0.f;
+      prefetch_partial(p, x.h, x.seq, x.slot, q_beg, nq, qpos, wg);
       for (int j = 0; ok && j < x.n_tiles; ++j) {
         const int J = J0 + j, s = J % RING;
         const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(s * BKV + wg * HALF);
