@@ -48,7 +48,9 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    const int32_t *k_loc_host, int T, int kv_rows, const void *q, const void *kv,
                    const void *latent, int64_t latent_ld, const int32_t *accumulate,
                    float *o, float *lse, void *final_out, float *final_lse, int final_dtype,
-                   int pnt, const SplitScratch *split, bool skip_keyless, cudaStream_t s);
+                   int pnt, const SplitScratch *split, bool skip_keyless, bool q_prepared,
+                   cudaStream_t s);
+int launch_prepare_q(const void *q, void *qh, int T, int H, cudaStream_t s);
 bool tc_available();
 
 namespace {
@@ -106,14 +108,16 @@ int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
               int T, const void *q, const void *kv, int kv_dtype, int kv_rows,
               const void *latent, int64_t latent_ld, const int32_t *acc, float *o, float *lse,
               cudaStream_t s, const SplitScratch *split = nullptr,
-              bool skip_keyless = false) {
+              bool skip_keyless = false, const void *q_prep = nullptr) {
   const int nq = q_loc_host[n] - q_loc_host[0];
   if (n == 0 || nq == 0) return MLA_OK;
+  // q_prep: the same queries head-major with q_nope in fp16 (prepare_q), for
+  // the tensor-core kernel
   if (tc_available() && tc_attn_ok(d, kv_dtype, latent_ld) && aligned16(q) && aligned16(kv) &&
       aligned16(latent))
-    return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, kv_rows, q, kv,
-                          latent, latent_ld, acc, o, lse, nullptr, nullptr, 0, 0, split,
-                          skip_keyless, s);
+    return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, kv_rows,
+                          q_prep ? q_prep : q, kv, latent, latent_ld, acc, o, lse, nullptr,
+                          nullptr, 0, 0, split, skip_keyless, q_prep != nullptr, s);
   return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, kv_rows, q, kv, kv_dtype, latent,
                           latent_ld, acc, o, lse, s);
 }
@@ -529,6 +533,7 @@ constexpr int kSplitSlots = 16;
 struct PrefillBuffers {
   int32_t *meta;
   ChunkBuffers chunk[2];  // chunk c uses set c % 2
+  void *q_prep;           // queries head-major, q_nope in fp16 (tensor-core path)
   void *kv_suffix;
   float *o_part, *lse_part, *o_suf, *lse_suf;
   SplitScratch split;
@@ -545,6 +550,7 @@ size_t carve_prefill(void *base, const mla_dims_t &d, const PrefillLayout &p,
     else
       b.chunk[k] = b.chunk[0];
   }
+  b.q_prep = cv.take(size_t(p.T) * d.num_heads * (d.qk_nope_dim + d.qk_rope_dim) * 2);
   b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk[0].kv_dtype));
   const size_t rows_split = size_t(kSplitSlots) * d.num_heads * 128;
   b.split.o = static_cast<float *>(cv.take(rows_split * d.v_dim * sizeof(float)));
@@ -628,6 +634,17 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   rc = launch_fill_empty_rows(b.o_part, b.lse_part, T, H, Dv, int(p.empty.size()),
                               b.meta + p.slices_off, s);
   if (rc) return rc;
+  // the tensor-core attention reads the queries head-major with q_nope
+  // already fp16: one pass here instead of a strided load and an fp16
+  // conversion in every attention CTA
+  const bool tc_attn = tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
+                       aligned16(new_latent);
+  const void *q_prep = nullptr;
+  if (tc_attn) {
+    rc = launch_prepare_q(q, b.q_prep, T, H, s);
+    if (rc) return rc;
+    q_prep = b.q_prep;
+  }
 
   // The chunk pipeline (run_pipeline) over execution groups: consecutive
   // chunks with no continuation between them and rows within the budget
@@ -667,7 +684,7 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
         meta_of(c, req, st, cu, ql, acc);
         return attention(*d, 0, m.n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
                          b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
-                         acc, b.o_part, b.lse_part, st_, &b.split, true);
+                         acc, b.o_part, b.lse_part, st_, &b.split, true, q_prep);
       },
       // new-token up-projection, beside the last group's attention
       [&](cudaStream_t st_) {
@@ -676,13 +693,12 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   if (rc) return rc;
 
   const int32_t *sq = b.meta + p.suffix_off;
-  if (tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
-      aligned16(b.kv_suffix) && aligned16(new_latent)) {
+  if (tc_attn && aligned16(b.kv_suffix)) {
     // new-token attention with the final merge in its epilogue (row f3): the
     // context partial is read where needed, the output written once
-    return launch_attn_tc(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, T, q,
+    return launch_attn_tc(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, T, q_prep,
                           b.kv_suffix, new_latent, LP, nullptr, b.o_part, b.lse_part, out,
-                          out_lse, d->dtype, p.pnt, nullptr, false, s);
+                          out_lse, d->dtype, p.pnt, nullptr, false, true, s);
   }
   rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
                  kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
@@ -804,6 +820,7 @@ int build_equal_window(const int32_t *ctx, const int32_t *ql, int R, int budget,
 struct EqualWindowBuffers {
   int32_t *meta;
   ChunkBuffers chunk[2];  // chunk c uses set c % 2 (the same pipeline as the new path)
+  void *q_prep;           // as in the new path
   void *kv_suffix;
   float *o_run[2], *lse_run[2];  // running partial, ping-ponged per chunk
   float *o_chunk, *lse_chunk, *o_suf, *lse_suf;
@@ -820,6 +837,7 @@ size_t carve_equal_window(void *base, const mla_dims_t &d, const EqualWindowLayo
     else
       b.chunk[k] = b.chunk[0];
   }
+  b.q_prep = cv.take(size_t(p.T) * d.num_heads * (d.qk_nope_dim + d.qk_rope_dim) * 2);
   b.kv_suffix = cv.take(size_t(p.T) * kv_width(d) * elem_bytes(b.chunk[0].kv_dtype));
   const size_t o_bytes = size_t(p.T) * d.num_heads * d.v_dim * sizeof(float);
   const size_t l_bytes = size_t(p.T) * d.num_heads * sizeof(float);
@@ -906,6 +924,12 @@ extern "C" int mla_chunked_prefill_equal_window(
   rc = launch_fill_empty_rows(b.o_run[0], b.lse_run[0], T, H, Dv, 1, b.meta + p.slice_off, s);
   if (rc) return rc;
   const int kv_dtype = b.chunk[0].kv_dtype;
+  const void *q_prep = nullptr;
+  if (tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q)) {
+    rc = launch_prepare_q(q, b.q_prep, T, H, s);
+    if (rc) return rc;
+    q_prep = b.q_prep;
+  }
   // the chunks run through the same two-buffer pipeline as the new path, so
   // the two schemes differ in their chunks, not in how a chunk is executed
   rc = run_pipeline(
@@ -928,7 +952,7 @@ extern "C" int mla_chunked_prefill_equal_window(
                       *ql = cu + R + 1;
         int r = attention(*d, 0, R, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
                           b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
-                          nullptr, b.o_chunk, b.lse_chunk, st_);
+                          nullptr, b.o_chunk, b.lse_chunk, st_, nullptr, false, q_prep);
         if (!r && p.has_empty[c])
           r = launch_mask_empty_context(b.lse_chunk, b.o_chunk, MLA_DTYPE_F32, T, H, Dv, R, ql,
                                         cu, st_);
@@ -944,7 +968,8 @@ extern "C" int mla_chunked_prefill_equal_window(
   if (rc) return rc;
   const int32_t *sq = b.meta + p.suffix_off;
   rc = attention(*d, 1, R, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s, nullptr, false,
+                 q_prep);
   if (rc) return rc;
   const int fin = p.n_chunks & 1;  // the buffer the last chunk merged into
   return launch_merge(out, out_lse, b.o_run[fin], b.lse_run[fin], b.o_suf, b.lse_suf, T, H, Dv,

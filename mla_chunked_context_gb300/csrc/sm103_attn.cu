@@ -80,6 +80,10 @@ struct AttnParams {
   void *fout;
   float *flse;
   int pnt, fout_bf16;
+  // q layout: 0 = the caller's [T, H, 192] bf16 (q_nope converted to fp16 in
+  // shared memory); 1 = prepared head-major [H, T, 192] with q_nope already
+  // fp16 (prepare_q_kernel), so a Q tile is one contiguous 48 KB block
+  int q_prepared;
   // key-split scratch: slot k holds O [H][BQ][DV] (normalised) and LSE
   // [H][BQ] of one split
   float *split_o, *split_lse;
@@ -287,6 +291,17 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
   const bool merge_old = accumulate || (fin && t < p.pnt);
   // the stored LSE is read by both warpgroups before either writes it
   const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
+  // this warpgroup's half of the output row, and the row's LSE
+  float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + row) * DV + wg * (DV / 2)
+                      : p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
+  // the stored half row, when it holds a result (finite LSE), read now with
+  // all 16 loads in flight, not one 64-byte piece at a time below
+  float4 ov[DV / 2 / 4];
+  const bool have_old = merge_old && qpos < nq && !is_neg_inf(old);
+  if (have_old) {
+#pragma unroll
+    for (int i = 0; i < DV / 2 / 4; ++i) ov[i] = reinterpret_cast<const float4 *>(orow)[i];
+  }
   tc_fence_before();
   // both warpgroups' O are complete after this barrier (each waited for
   // its own last P.V); all threads take part, the MMA warps too
@@ -300,9 +315,6 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
   const bool store = okv && qpos < nq;
   float lse = (lsum > 0.f) ? (mx + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
   float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
-  // this warpgroup's half of the output row, and the row's LSE
-  float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + row) * DV + wg * (DV / 2)
-                      : p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
   float *lse_dst = split ? p.split_lse + (int64_t(slot) * p.H + h) * BQ + row : p.lse + li;
   bool write = store;
   if (store && merge_old) {
@@ -325,7 +337,7 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
     // O = (fA O_A + fB O_B) / lsum over this warpgroup's 64 columns
     const uint32_t oa = tmem + lane_off + COL_O + uint32_t(wg * (DV / 2));
     const uint32_t ob = oa + uint32_t(DV);
-#pragma unroll 1
+#pragma unroll
     for (int c = 0; c < DV / 2 / 16; ++c) {
       uint32_t ra[16], rb[16];
       tmem_ld16(oa + uint32_t(c * 16), ra);
@@ -338,7 +350,6 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
         if (lane == 0) mbar_arrive(b_ofree);
       }
       if (write) {
-        const float4 *src = reinterpret_cast<const float4 *>(orow + c * 16);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float v[4];
@@ -349,12 +360,12 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
             v[k] = (a + b) * w_new;
           }
           float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
-          if (w_old != 0.f) {  // an unused side is never read
-            const float4 old = src[e];
-            o4.x += w_old * old.x;
-            o4.y += w_old * old.y;
-            o4.z += w_old * old.z;
-            o4.w += w_old * old.w;
+          if (w_old != 0.f) {  // only when the stored LSE is finite (have_old)
+            const float4 ovv = ov[c * 4 + e];
+            o4.x += w_old * ovv.x;
+            o4.y += w_old * ovv.y;
+            o4.z += w_old * ovv.z;
+            o4.w += w_old * ovv.w;
           }
           const int64_t col = (int64_t(t) * p.H + h) * DV + wg * (DV / 2) + c * 16 + e * 4;
           if (!fin) {
@@ -452,11 +463,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_map(&tm_q);
       prefetch_map(&tm_kv);
       prefetch_map(&tm_lat);
-      const int qrow = q_beg + q0;
+      const int qx = p.q_prepared ? 0 : h * DQK, qy = (p.q_prepared ? h * p.T : 0) + q_beg + q0;
       mbar_expect_tx(b_q, Q_BYTES);
-      tma_load_2d(smem_u32(sQ), &tm_q, b_q, h * DQK, qrow);
-      tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, h * DQK + 64, qrow);
-      tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, h * DQK + 128, qrow);
+      tma_load_2d(smem_u32(sQ), &tm_q, b_q, qx, qy);
+      tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, qx + 64, qy);
+      tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, qx + 128, qy);
       int k_issued[RING], v_issued[RING];
       for (int s = 0; s < RING; ++s) k_issued[s] = v_issued[s] = -1;
       for (int j = 0; j < n_tiles; ++j) {
@@ -557,7 +568,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(b_q, 0))
         ok = false;
       else
-        convert_q_nope(sQ, threadIdx.x - 64, 128);
+        if (!p.q_prepared) convert_q_nope(sQ, threadIdx.x - 64, 128);
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
     }
@@ -685,11 +696,12 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
         const int q_beg = __ldg(p.q_loc + x.seq), k_beg = __ldg(p.k_loc + x.seq);
         // the previous unit's S MMAs are done with the Q tile
         if (kq > 0 && !mbar_wait(b_qfree, uint32_t((kq - 1) & 1))) break;
-        const int qrow = q_beg + x.qt * BQ;
+        const int qx = p.q_prepared ? 0 : x.h * DQK;
+        const int qy = (p.q_prepared ? x.h * p.T : 0) + q_beg + x.qt * BQ;
         mbar_expect_tx(b_q, Q_BYTES);
-        tma_load_2d(smem_u32(sQ), &tm_q, b_q, x.h * DQK, qrow);
-        tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, x.h * DQK + 64, qrow);
-        tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, x.h * DQK + 128, qrow);
+        tma_load_2d(smem_u32(sQ), &tm_q, b_q, qx, qy);
+        tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, qx + 64, qy);
+        tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, qx + 128, qy);
         q_issued = kq & 1;
         ++kq;
         for (int j = 0; j < x.n_tiles; ++j, ++J) {
@@ -806,7 +818,7 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       const Unit x = unit_of(u);
       if (x.n_tiles <= 0) continue;
       const bool ok = mbar_wait(b_q, uint32_t(kq & 1));
-      if (ok) convert_q_nope(sQ, lane, 32);
+      if (ok && !p.q_prepared) convert_q_nope(sQ, lane, 32);
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
       ++kq;
@@ -849,6 +861,30 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// q [T, H, 192] bf16 -> head-major [H, T, 192] with q_nope (columns 0-127)
+// rounded to fp16 (exact for bf16 values within fp16's range) and q_pe
+// copied: one warp per (token, head) row, 24 lanes x 16 bytes, reads and
+// writes both 384 contiguous bytes.
+__global__ void __launch_bounds__(256) prepare_q_kernel(const uint4 *__restrict__ q,
+                                                        uint4 *__restrict__ qh, int T, int H) {
+  const int64_t rows = int64_t(T) * H;
+  const int lane = threadIdx.x & 31;
+  for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows;
+       r += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+    if (lane >= DQK / 8) continue;
+    const int64_t t = r / H, h = r - t * H;
+    uint4 x = __ldg(q + r * (DQK / 8) + lane);
+    if (lane < DN / 8) {
+      uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w4[e] = pack_f16(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
+      x = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    qh[(h * T + t) * (DQK / 8) + lane] = x;
   }
 }
 
@@ -991,14 +1027,19 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    int T, int kv_rows, const void *q, const void *kv, const void *latent,
                    int64_t latent_ld, const int32_t *accumulate, float *o, float *lse,
                    void *final_out, float *final_lse, int final_dtype, int pnt,
-                   const SplitScratch *split, bool skip_keyless, cudaStream_t s) {
+                   const SplitScratch *split, bool skip_keyless, bool q_prepared,
+                   cudaStream_t s) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
   const int H = d.num_heads;
   const int rows = k_loc_host[num_seqs];
   CUtensorMap tq, tkv, tlat;
-  if (!make_tmap_2d_16(&tq, false, q, uint64_t(H) * DQK, uint64_t(T), uint64_t(H) * DQK * 2, 64,
-                       128, true) ||
+  const bool tq_ok =
+      q_prepared
+          ? make_tmap_2d_16(&tq, false, q, DQK, uint64_t(H) * T, uint64_t(DQK) * 2, 64, 128, true)
+          : make_tmap_2d_16(&tq, false, q, uint64_t(H) * DQK, uint64_t(T), uint64_t(H) * DQK * 2,
+                            64, 128, true);
+  if (!tq_ok ||
       !make_tmap_3d_16(&tkv, true, kv, HD, uint64_t(kv_rows > 0 ? kv_rows : 1), uint64_t(H),
                        uint64_t(HD) * 2, uint64_t(kv_rows > 0 ? kv_rows : 1) * HD * 2, 64, BKV,
                        true) ||
@@ -1039,6 +1080,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     prm.fout_bf16 = final_dtype == MLA_DTYPE_BF16 ? 1 : 0;
     prm.split_o = split ? split->o : nullptr;
     prm.split_lse = split ? split->lse : nullptr;
+    prm.q_prepared = q_prepared ? 1 : 0;
     for (int k = 0; k < n; ++k) {
       const Item &it = items[b + k];
       prm.items[k] = make_int4(it.seq, it.qt | ((it.slot + 1) << 16), it.kt0, it.kt1);
@@ -1070,6 +1112,17 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     return launch_status();
   }
   return MLA_OK;
+}
+
+int launch_prepare_q(const void *q, void *qh, int T, int H, cudaStream_t s) {
+  if (T == 0) return MLA_OK;
+  const int64_t warps = int64_t(T) * H;
+  int64_t blocks = (warps * 32 + 255) / 256;
+  const int64_t cap = int64_t(num_sms()) * 16;
+  if (blocks > cap) blocks = cap;
+  prepare_q_kernel<<<int(blocks), 256, 0, s>>>(static_cast<const uint4 *>(q),
+                                               static_cast<uint4 *>(qh), T, H);
+  return launch_status();
 }
 
 int attn_take_errors() { return sm103::take_error_flags_here(); }

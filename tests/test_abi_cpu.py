@@ -122,8 +122,9 @@ def test_workspace_queries():
     split = 16 * H * 128 * (128 + 1) * 4        # key-split scratch of the context attention
 
     def lower(sets, rows, T):
-        return (sets * (rows * 576 * 2 + rows * H * 256 * kv_es) + T * H * 256 * kv_es +
-                2 * T * H * 128 * 4 + split)
+        # buffer sets, prepared queries, new-token K/V, partials, split scratch
+        return (sets * (rows * 576 * 2 + rows * H * 256 * kv_es) + T * H * 192 * 2 +
+                T * H * 256 * kv_es + 2 * T * H * 128 * 4 + split)
     # one chunk: one buffer set
     assert lower(1, rows, T) <= b <= lower(1, rows, T) + 64 * 1024 * 1024
     # several chunks: two buffer sets for the pipeline
