@@ -524,6 +524,30 @@ def test_prefill_groups_small_chunks_into_one_launch_set():
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+def test_prefill_many_short_requests_loop_path():
+    # 64 heads and many short requests: more (query tile, head) units than
+    # SMs with few key tiles each, so the group attention and the new-token
+    # attention (with the final merge) run on the looping kernel, with the
+    # prepared queries; a continuation (budget 256), context-free requests
+    # between and after the ones with context; compared in full
+    rng = np.random.default_rng(53)
+    ctx = [int(x) for x in rng.integers(0, 300, size=12)]
+    ctx[3] = 0
+    ctx[7] = 0
+    ctx[1] = 600                       # split over three chunks of 256
+    ctx += [0, 0]                      # context-free tail
+    ql = [int(x) for x in rng.integers(1, 200, size=len(ctx))]
+    w = W.scaled(W.workload("uniform"), context_lens=ctx, query_lens=ql, num_heads=64,
+                 row_budget=1024, max_context_chunk=256, split_alignment=64, seed=53)
+    x = W.make_inputs(w)
+    out, lse = _run_prefill(w, x)
+    ro, rl, plans = _oracle_prefill(w, x)
+    assert any(p.is_continuation for p in plans)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 EDGE_CASES = {
     # no request has context: the output is the new-token attention alone
     "no_context": dict(context_lens=[0, 0, 0], query_lens=[5, 1, 130]),
