@@ -433,18 +433,20 @@ int pipeline_for_current_device(size_t events, Pipeline **out) {
 bool record(cudaEvent_t e, cudaStream_t s) { return cudaEventRecord(e, s) == cudaSuccess; }
 bool wait_on(cudaStream_t s, cudaEvent_t e) { return cudaStreamWaitEvent(s, e, 0) == cudaSuccess; }
 
-// The two-buffer pipeline of the chunked paths.  For units c = 0..n-1:
-// gather(c, stream) on the gather side stream once consume(c-2) has released
-// buffer set c % 2, up(c, stream) on the GEMM side stream after it, and
-// consume(c, stream) on the caller's stream `s` after that; then tail(stream)
-// on the GEMM side stream (the new tokens' up-projection, beside the last
-// consume).  Both side streams start after the work already on `s` and are
+// The two-buffer pipeline of the chunked paths.  First pre(s) on the
+// caller's stream `s` (work only the consumers need, beside the first gather
+// and up-projection); then for units c = 0..n-1: gather(c, stream) on the
+// gather side stream once consume(c-2) has released buffer set c % 2,
+// up(c, stream) on the GEMM side stream after it, and consume(c, stream) on
+// `s` after that; then tail(stream) on the GEMM side stream (the new tokens'
+// up-projection, beside the last consume).  Both side streams start after the work already on `s` and are
 // joined back into `s` before returning, also after an error (the caller may
 // free the workspace once `s` has passed this point).  The side streams run
 // at the highest priority, so a GEMM takes SMs as soon as attention CTAs
 // retire.  Holds g_pipeline_mu while it enqueues.
-template <class Gather, class Up, class Consume, class Tail>
-int run_pipeline(cudaStream_t s, size_t n, Gather gather, Up up, Consume consume, Tail tail) {
+template <class Pre, class Gather, class Up, class Consume, class Tail>
+int run_pipeline(cudaStream_t s, size_t n, Pre pre, Gather gather, Up up, Consume consume,
+                 Tail tail) {
   std::lock_guard<std::mutex> lock(g_pipeline_mu);
   Pipeline *pl = nullptr;
   int rc = pipeline_for_current_device(3 * n + 3, &pl);
@@ -456,6 +458,7 @@ int run_pipeline(cudaStream_t s, size_t n, Gather gather, Up up, Consume consume
   auto ev_used = [&](size_t c) { return ev[3 + 3 * c]; };
   cudaEvent_t ev_tail = ev[1 + 3 * n], ev_join = ev[2 + 3 * n];
   if (!record(ev[0], s) || !wait_on(sg, ev[0]) || !wait_on(sm, ev[0])) return MLA_ERR_CUDA;
+  rc = pre(s);
   for (size_t c = 0; c < n && rc == MLA_OK; ++c) {
     if (c >= 2 && !wait_on(sg, ev_used(c - 2))) rc = MLA_ERR_CUDA;
     if (!rc) rc = gather(c, sg);
@@ -631,20 +634,12 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   const int LP = d->kv_lora_rank + d->qk_rope_dim;
   const int es = elem_bytes(d->dtype);
   const int kv_dtype = b.chunk[0].kv_dtype;
-  rc = launch_fill_empty_rows(b.o_part, b.lse_part, T, H, Dv, int(p.empty.size()),
-                              b.meta + p.slices_off, s);
-  if (rc) return rc;
   // the tensor-core attention reads the queries head-major with q_nope
-  // already fp16: one pass here instead of a strided load and an fp16
-  // conversion in every attention CTA
+  // already fp16: one pass (in the pipeline's pre step) instead of a strided
+  // load and an fp16 conversion in every attention CTA
   const bool tc_attn = tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
                        aligned16(new_latent);
-  const void *q_prep = nullptr;
-  if (tc_attn) {
-    rc = launch_prepare_q(q, b.q_prep, T, H, s);
-    if (rc) return rc;
-    q_prep = b.q_prep;
-  }
+  const void *q_prep = tc_attn ? b.q_prep : nullptr;
 
   // The chunk pipeline (run_pipeline) over execution groups: consecutive
   // chunks with no continuation between them and rows within the budget
@@ -667,6 +662,14 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   };
   rc = run_pipeline(
       s, p.metas.size(),
+      // the partial's context-free rows and the prepared queries, beside the
+      // first gather and up-projection
+      [&](cudaStream_t st_) {
+        int r = launch_fill_empty_rows(b.o_part, b.lse_part, T, H, Dv, int(p.empty.size()),
+                                       b.meta + p.slices_off, st_);
+        if (!r && q_prep) r = launch_prepare_q(q, b.q_prep, T, H, st_);
+        return r;
+      },
       [&](size_t c, cudaStream_t st_) {
         const int32_t *req, *st, *cu, *ql, *acc;
         meta_of(c, req, st, cu, ql, acc);
@@ -920,20 +923,21 @@ extern "C" int mla_chunked_prefill_equal_window(
   const int H = d->num_heads, Dv = d->v_dim, T = p.T, R = p.R;
   const int LP = d->kv_lora_rank + d->qk_rope_dim;
   const int es = elem_bytes(d->dtype);
-  // the running partial starts empty: O = 0, LSE = -inf
-  rc = launch_fill_empty_rows(b.o_run[0], b.lse_run[0], T, H, Dv, 1, b.meta + p.slice_off, s);
-  if (rc) return rc;
   const int kv_dtype = b.chunk[0].kv_dtype;
-  const void *q_prep = nullptr;
-  if (tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q)) {
-    rc = launch_prepare_q(q, b.q_prep, T, H, s);
-    if (rc) return rc;
-    q_prep = b.q_prep;
-  }
+  const void *q_prep =
+      (tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q)) ? b.q_prep : nullptr;
   // the chunks run through the same two-buffer pipeline as the new path, so
   // the two schemes differ in their chunks, not in how a chunk is executed
   rc = run_pipeline(
       s, size_t(p.n_chunks),
+      // the running partial starts empty (O = 0, LSE = -inf); the prepared
+      // queries
+      [&](cudaStream_t st_) {
+        int r = launch_fill_empty_rows(b.o_run[0], b.lse_run[0], T, H, Dv, 1,
+                                       b.meta + p.slice_off, st_);
+        if (!r && q_prep) r = launch_prepare_q(q, b.q_prep, T, H, st_);
+        return r;
+      },
       [&](size_t c, cudaStream_t st_) {
         const ChunkMetaHost &m = p.metas[c];
         const int32_t *req = b.meta + p.meta_off[c], *st = req + R, *cu = st + R;
