@@ -1,10 +1,14 @@
 // C-ABI entry points: argument checks, workspace carving, metadata upload and
 // the order of the steps (PR #50613 report, items 2-4; PR #36540 report).
 //
-// Step order of mla_chunked_prefill, all on the caller's stream:
-//   plan (host) -> one metadata upload -> fill context-free rows of the
-//   partial -> per chunk { gather, up-projection, attention + accumulate } ->
-//   new-token up-projection -> causal new-token attention -> final merge.
+// Step order of mla_chunked_prefill:
+//   plan (host), chunks grouped for execution -> one metadata upload -> fill
+//   of context-free rows of the partial, query preparation -> per execution
+//   group { gather, up-projection (side streams), attention + accumulate } as
+//   a two-buffer pipeline -> new-token up-projection -> causal new-token
+//   attention with the final merge (tensor-core path; else attention, merge).
+//   Everything that writes the partial or the output runs on the caller's
+//   stream, which waits for the side streams before the last kernel.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
