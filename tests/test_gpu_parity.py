@@ -548,6 +548,30 @@ def test_prefill_many_short_requests_loop_path():
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+@pytest.mark.parametrize("seed", [61, 62, 63])
+def test_prefill_random_batches(seed):
+    # seeded random batches over the execution paths at once: random context
+    # and query lengths (some zero), random budget and split cap, 32 heads
+    # (enough units for the looping attention, few enough for key splits when
+    # a request is long), compared in full with the oracle
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(4, 14))
+    ctx = [int(x) if rng.random() > 0.25 else 0 for x in rng.integers(1, 1500, size=R)]
+    ctx[int(rng.integers(0, R))] = int(rng.integers(3000, 6000))   # one long request
+    ql = [int(x) if rng.random() > 0.1 else 0 for x in rng.integers(1, 300, size=R)]
+    ql[0] = max(ql[0], 1)
+    budget = int(rng.choice([512, 1024, 2048, 4096, 8192]))
+    mcc = int(rng.choice([budget, max(64, budget // 4)]))
+    w = W.scaled(W.workload("uniform"), context_lens=ctx, query_lens=ql, num_heads=32,
+                 row_budget=budget, max_context_chunk=mcc, split_alignment=64, seed=seed)
+    x = W.make_inputs(w)
+    out, lse = _run_prefill(w, x)
+    ro, rl, _ = _oracle_prefill(w, x)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 EDGE_CASES = {
     # no request has context: the output is the new-token attention alone
     "no_context": dict(context_lens=[0, 0, 0], query_lens=[5, 1, 130]),
