@@ -53,20 +53,26 @@ __device__ __forceinline__ void store8(__nv_bfloat16 *p, const Vec8 &x) {
   __stcs(reinterpret_cast<uint4 *>(p), make_uint4(w[0], w[1], w[2], w[3]));
 }
 
-template <typename TI, typename TO>
+// Piece index math in 32 bits (Idx = uint32_t) when T*H*(D/8) fits, else 64
+// bits, and with shifts when D/8 and H are powers of two (kPow2): integer
+// division is a long instruction sequence, 64-bit division several times
+// longer, and this kernel issues it once per 16-byte piece (32-bit indices
+// took the 8192 x 128 x 128 case from 131.7 to 127.6 us).
+template <typename TI, typename TO, typename Idx, bool kPow2>
 __global__ void __launch_bounds__(256) merge_kernel(
     TO *out, float *__restrict__ out_lse, const TI *prefix_o,
     const float *__restrict__ prefix_lse, const TI *suffix_o,
-    const float *__restrict__ suffix_lse, int T, int H, int D, int pnt) {
-  const int vpr = D >> 3;  // 8-element pieces per (token, head) row
-  const int64_t total = int64_t(T) * H * vpr;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t row = i / vpr;
+    const float *__restrict__ suffix_lse, int T, int H, int D, int pnt, int vpr_log2,
+    int h_log2) {
+  const Idx vpr = Idx(D >> 3);  // 8-element pieces per (token, head) row
+  const Idx total = Idx(T) * Idx(H) * vpr;
+  const Idx stride = Idx(gridDim.x) * blockDim.x;
+  for (Idx i = Idx(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const Idx row = kPow2 ? (i >> vpr_log2) : i / vpr;
     const int piece = int(i - row * vpr);
-    const int t = int(row / H);
-    const int h = int(row - int64_t(t) * H);
-    const int64_t off = row * D + int64_t(piece) * 8;
+    const Idx tt = kPow2 ? (row >> h_log2) : row / Idx(H);
+    const int t = int(tt), h = int(row - tt * Idx(H));
+    const int64_t off = int64_t(row) * D + int64_t(piece) * 8;
     const int64_t li = int64_t(h) * T + t;
     Vec8 r;
     float lse;
@@ -149,10 +155,25 @@ int launch_merge(void *out, float *out_lse, const void *prefix_o, const float *p
                  int pnt, int in_dtype, int out_dtype, cudaStream_t s) {
   const int64_t work = int64_t(T) * H * (D / 8);
   const int grid = grid_for(work, 256);
-#define MLA_MERGE(TI, TO)                                                        \
-  merge_kernel<TI, TO><<<grid, 256, 0, s>>>(                                     \
-      static_cast<TO *>(out), out_lse, static_cast<const TI *>(prefix_o),        \
-      prefix_lse, static_cast<const TI *>(suffix_o), suffix_lse, T, H, D, pnt)
+  // 32-bit piece indices while they and the grid stride fit; shifts when
+  // D/8 and H are powers of two
+  const bool small = work + int64_t(grid) * 256 < (int64_t(1) << 32);
+  const int vpr = D / 8;
+  const bool pow2 = (vpr & (vpr - 1)) == 0 && (H & (H - 1)) == 0;
+  const int vl = __builtin_ctz(unsigned(vpr)), hl = __builtin_ctz(unsigned(H));
+#define MLA_MERGE_K(TI, TO, IDX, P2)                                                   \
+  merge_kernel<TI, TO, IDX, P2><<<grid, 256, 0, s>>>(                                  \
+      static_cast<TO *>(out), out_lse, static_cast<const TI *>(prefix_o), prefix_lse,  \
+      static_cast<const TI *>(suffix_o), suffix_lse, T, H, D, pnt, vl, hl)
+#define MLA_MERGE(TI, TO)                                                              \
+  do {                                                                                 \
+    if (small && pow2)                                                                 \
+      MLA_MERGE_K(TI, TO, uint32_t, true);                                             \
+    else if (small)                                                                    \
+      MLA_MERGE_K(TI, TO, uint32_t, false);                                            \
+    else                                                                               \
+      MLA_MERGE_K(TI, TO, uint64_t, false);                                            \
+  } while (0)
   if (in_dtype == MLA_DTYPE_BF16 && out_dtype == MLA_DTYPE_BF16)
     MLA_MERGE(__nv_bfloat16, __nv_bfloat16);
   else if (in_dtype == MLA_DTYPE_BF16)
@@ -162,6 +183,7 @@ int launch_merge(void *out, float *out_lse, const void *prefix_o, const float *p
   else
     MLA_MERGE(float, float);
 #undef MLA_MERGE
+#undef MLA_MERGE_K
   return launch_status();
 }
 
