@@ -554,7 +554,8 @@ def run_reference(args, rank, world):
 
 def run_kernel_case(args, dev):
     """One kernel alone on a small DeepSeek-shaped case (for ncu captures and
-    quick timing): up_proj, attn (context or causal), merge or gather."""
+    quick timing): up_proj, attn (context or causal), fused (context attention
+    with the up-projection fused in), merge or gather."""
     import mla_chunked_context_gb300 as M
     from mla_chunked_context_gb300 import workloads as W
     peaks = load_peaks()
@@ -590,6 +591,26 @@ def run_kernel_case(args, dev):
         pairs = n * (ql * (ql + 1) / 2 if args.causal else ql * kl)
         work, unit, peak = 2.0 * H * (192 + 128) * pairs, "TFLOP/s", peaks["bf16_tflops"]
         info = {"seqs": n, "q": ql, "k": kl, "causal": bool(args.causal)}
+    elif args.kernel == "fused":
+        # context attention with the up-projection fused in (one query tile
+        # per sequence); work = the up-projection plus the attention
+        n, ql, kl = args.seqs, args.qlen, args.klen
+        q = torch.randn(n * ql, H, 192, device=dev).to(bf)
+        lat = torch.randn(n * kl, 576, device=dev).to(bf)
+        wkv = (torch.randn(H * 256, 512, device=dev) * 0.02).to(bf)
+        o = torch.empty(n * ql, H, 128, device=dev)
+        lse = torch.empty(H, n * ql, device=dev)
+        q_loc = [i * ql for i in range(n + 1)]
+        k_loc = [i * kl for i in range(n + 1)]
+        qd = torch.tensor(q_loc, dtype=torch.int32, device=dev)
+        kd = torch.tensor(k_loc, dtype=torch.int32, device=dev)
+        ws = torch.empty(M.mla_fused_attn_workspace_bytes(dims, n * ql), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: M.mla_fused_context_attn(dims, q_loc, k_loc, q, lat, wkv, o, lse,  # noqa
+                                              workspace=ws, q_loc_dev=qd, k_loc_dev=kd)
+        work = 2.0 * n * kl * 512 * H * 256 + 2.0 * H * (192 + 128) * n * ql * kl
+        unit, peak = "TFLOP/s", peaks["bf16_tflops"]
+        info = {"seqs": n, "q": ql, "k": kl}
     elif args.kernel == "merge":
         m = W.MergeWorkload()
         x = W.make_merge_inputs(m, poison=True)
@@ -645,7 +666,7 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default=None,
-                    choices=["up_proj", "attn", "merge", "gather"],
+                    choices=["up_proj", "attn", "fused", "merge", "gather"],
                     help="time one kernel alone on a small case instead of the full step")
     ap.add_argument("--heads", type=int, default=128)
     ap.add_argument("--rows", type=int, default=8192)

@@ -224,6 +224,39 @@ int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
                     const int32_t *accumulate, float *o, float *lse,
                     mla_stream_t stream);
 
+/* mla_fused_context_attn: the context attention of mla_varlen_attn
+ *   (causal = 0, PR #50613 report, items 3-4) with the W_kv_b up-projection
+ *   fused in (the report's Triton/CUDA kernels are prior art; this is the
+ *   same arithmetic as mla_kv_up_proj followed by mla_varlen_attn, K_nope and
+ *   V rounded to F16 as that path stores them): the keys and values of each
+ *   128-key tile are computed on chip from latent[row][0:L] and w_kv_b and
+ *   never written to memory.
+ *   Sequence i owns query tokens [q_loc[i], q_loc[i+1]) and latent rows
+ *   [k_loc[i], k_loc[i+1]) of latent (device [latent_rows, latent_ld],
+ *   bf16; k_pe = latent[row][L:L+P]); w_kv_b device [H*(Dn+Dv), L] bf16; q
+ *   device [T, H, Dn+P] bf16 (T = num_tokens); o float32 [T, H, Dv]; lse
+ *   float32 [H, T]; accumulate as in mla_varlen_attn.  Every sequence with
+ *   both queries and keys may have at most 128 queries (one query tile: more
+ *   would repeat the up-projection per tile); rows of sequences without keys
+ *   are left untouched.
+ *   workspace: device, 16-byte aligned, mla_fused_attn_workspace_bytes()
+ *   bytes (the queries head-major with q_nope in F16, and key-split scratch);
+ *   owned by the caller, reusable once the stream has passed the call.
+ *   Runs for the DeepSeek-V3 head shape (L 512, P 64, Dn 128, Dv 128) on a
+ *   tcgen05 GPU; MLA_ERR_UNSUPPORTED otherwise or when a sequence has more
+ *   than 128 queries.  mla_chunked_prefill takes this path by itself for
+ *   execution groups whose sequences all have at most 128 queries. */
+int mla_fused_attn_workspace_bytes(const mla_dims_t *d, int32_t num_tokens,
+                                   size_t *bytes);
+int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
+                           const int32_t *q_loc, const int32_t *k_loc,
+                           const int32_t *q_loc_host, const int32_t *k_loc_host,
+                           int32_t num_tokens, const void *q, const void *latent,
+                           int64_t latent_ld, int32_t latent_rows,
+                           const void *w_kv_b, const int32_t *accumulate,
+                           float *o, float *lse, void *workspace,
+                           size_t workspace_bytes, mla_stream_t stream);
+
 /* mla_fill_empty_rows  (PR #50613 report, item 3, init_mla_context_partial):
  *   o[t, :, :] = 0 and lse[:, t] = -inf for t in each [slices[2k],
  *   slices[2k+1]).  slices device int32 [2*num_slices]; o float32 [T, H, Dv];

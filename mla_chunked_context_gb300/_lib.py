@@ -36,7 +36,8 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_chunk_kv_dtype", "mla_context_chunk_attn_noalloc",
             "mla_plan_equal_window_chunks", "mla_prefill_equal_window_workspace_bytes",
             "mla_chunked_prefill_equal_window", "mla_selftest_bounded_wait",
-            "mla_kernel_launches")
+            "mla_kernel_launches", "mla_fused_attn_workspace_bytes",
+            "mla_fused_context_attn")
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -89,6 +90,9 @@ def lib() -> C.CDLL:
                                     P, P, P, P],
             "mla_has_tcgen05": [],
             "mla_kernel_launches": [P],
+            "mla_fused_attn_workspace_bytes": [P, I32, P],
+            "mla_fused_context_attn": [P, I32, P, P, P, P, I32, P, P, I64, I32, P, P, P, P, P,
+                                       SZ, P],
             "mla_device_error_flags": [P],
             "mla_chunk_kv_dtype": [P, P],
             "mla_context_chunk_attn_noalloc": [P, P, P, P, P, I32, P, P, I32, P, I32, P, P, P,
@@ -266,6 +270,42 @@ def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Seque
                                  _ptr(kv), dtype_code(kv.dtype), rows, _ptr(latent),
                                  latent.stride(0), _ptr(acc), _ptr(o), _ptr(lse),
                                  _stream(stream)), "mla_varlen_attn")
+
+
+def mla_fused_attn_workspace_bytes(dims: Dims, num_tokens: int) -> int:
+    d = dims.c()
+    n = C.c_size_t(0)
+    _check(lib().mla_fused_attn_workspace_bytes(C.byref(d), int(num_tokens), C.byref(n)),
+           "mla_fused_attn_workspace_bytes")
+    return int(n.value)
+
+
+def mla_fused_context_attn(dims: Dims, q_loc: Sequence[int], k_loc: Sequence[int], q, latent,
+                           w_kv_b, o, lse, accumulate: Optional[Sequence[int]] = None,
+                           workspace=None, stream=None, q_loc_dev=None, k_loc_dev=None,
+                           accumulate_dev=None) -> None:
+    """Context attention with the up-projection fused in: latent rows
+    [k_loc[i], k_loc[i+1]) are sequence i's keys.  workspace: a uint8 device
+    tensor of mla_fused_attn_workspace_bytes bytes (allocated here if None)."""
+    n = len(q_loc) - 1
+    dev = q.device
+    ql = q_loc_dev if q_loc_dev is not None else torch.tensor(list(q_loc), dtype=torch.int32,
+                                                              device=dev)
+    kl = k_loc_dev if k_loc_dev is not None else torch.tensor(list(k_loc), dtype=torch.int32,
+                                                              device=dev)
+    acc = accumulate_dev
+    if acc is None and accumulate:
+        acc = torch.tensor(list(accumulate), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(mla_fused_attn_workspace_bytes(dims, q.shape[0]),
+                                dtype=torch.uint8, device=dev)
+    d = dims.c()
+    _check(lib().mla_fused_context_attn(C.byref(d), n, _ptr(ql), _ptr(kl), _i32_host(q_loc),
+                                        _i32_host(k_loc), q.shape[0], _ptr(q), _ptr(latent),
+                                        latent.stride(0), latent.shape[0], _ptr(w_kv_b),
+                                        _ptr(acc), _ptr(o), _ptr(lse), _ptr(workspace),
+                                        workspace.numel(), _stream(stream)),
+           "mla_fused_context_attn")
 
 
 def mla_fill_empty_rows(o, lse, slices: Sequence, stream=None) -> None:

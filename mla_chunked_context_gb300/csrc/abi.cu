@@ -55,6 +55,15 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    int pnt, const SplitScratch *split, bool skip_keyless, bool q_prepared,
                    cudaStream_t s);
 int launch_prepare_q(const void *q, void *qh, int T, int H, cudaStream_t s);
+bool fused_attn_ok(const mla_dims_t &d, int64_t latent_ld);
+bool fused_attn_fits(int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                     int min_tiles);
+int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
+                      const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                      int T, const void *q_prep, const void *latent, int64_t latent_ld, int rows,
+                      const void *w, const int32_t *acc, float *o, float *lse,
+                      const SplitScratch *split, cudaStream_t s);
+int fused_take_errors();
 bool tc_available();
 
 namespace {
@@ -536,6 +545,9 @@ int build_prefill(const mla_dims_t &d, const int32_t *ctx, const int32_t *ql, in
 // tile) units of a chunk, split over their keys when the chunk has too few
 // units to fill the GPU).
 constexpr int kSplitSlots = 16;
+// Groups of sequences averaging fewer key tiles than this stay on the
+// unfused path (each fused unit pays a queries load and a pipeline refill).
+constexpr int kFusedMinTiles = 8;
 
 struct PrefillBuffers {
   int32_t *meta;
@@ -644,6 +656,15 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   const bool tc_attn = tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
                        aligned16(new_latent);
   const void *q_prep = tc_attn ? b.q_prep : nullptr;
+  // groups whose sequences each have at most one query tile (and enough
+  // keys) run the attention with the up-projection fused in (row f2): no
+  // K/V in HBM, no separate GEMM
+  std::vector<char> fused(p.metas.size(), 0);
+  if (q_prep && fused_attn_ok(*d, LP) && aligned16(w_kv_b))
+    for (size_t c = 0; c < p.metas.size(); ++c)
+      fused[c] = fused_attn_fits(p.metas[c].n, p.metas[c].q_loc.data(),
+                                 p.metas[c].cu_rows.data(), kFusedMinTiles) &&
+                 aligned16(b.chunk[c & 1].latent_ws);
 
   // The chunk pipeline (run_pipeline) over execution groups: consecutive
   // chunks with no continuation between them and rows within the budget
@@ -682,6 +703,7 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                              b.chunk[c & 1].latent_ws, dev_status, st_);
       },
       [&](size_t c, cudaStream_t st_) {
+        if (fused[c]) return int(MLA_OK);
         return up_proj(*d, b.chunk[c & 1].latent_ws, LP, p.metas[c].rows, w_kv_b,
                        b.chunk[c & 1].kv_ws, kv_dtype, st_);
       },
@@ -689,6 +711,10 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
         const ChunkMetaHost &m = p.metas[c];
         const int32_t *req, *st, *cu, *ql, *acc;
         meta_of(c, req, st, cu, ql, acc);
+        if (fused[c])
+          return launch_attn_fused(*d, m.n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q_prep,
+                                   b.chunk[c & 1].latent_ws, LP, m.rows, w_kv_b, acc, b.o_part,
+                                   b.lse_part, &b.split, st_);
         return attention(*d, 0, m.n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
                          b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
                          acc, b.o_part, b.lse_part, st_, &b.split, true, q_prep);
@@ -714,6 +740,70 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                       MLA_DTYPE_F32, d->dtype, s);
 }
 
+namespace mla {
+namespace {
+size_t fused_workspace(const mla_dims_t &d, int T, void *base, PrefillBuffers *b) {
+  Carve cv(base);
+  void *qp = cv.take(size_t(T) * d.num_heads * (d.qk_nope_dim + d.qk_rope_dim) * 2);
+  const size_t rows_split = size_t(kSplitSlots) * d.num_heads * 128;
+  void *so = cv.take(rows_split * d.v_dim * sizeof(float));
+  void *sl = cv.take(rows_split * sizeof(float));
+  if (b) {
+    b->q_prep = qp;
+    b->split.o = static_cast<float *>(so);
+    b->split.lse = static_cast<float *>(sl);
+    b->split.slots = kSplitSlots;
+  }
+  return cv.off;
+}
+}  // namespace
+}  // namespace mla
+
+extern "C" int mla_fused_attn_workspace_bytes(const mla_dims_t *d, int32_t num_tokens,
+                                              size_t *bytes) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!bytes || num_tokens < 0) return MLA_ERR_INVALID;
+  *bytes = fused_workspace(*d, num_tokens, nullptr, nullptr);
+  return MLA_OK;
+}
+
+extern "C" int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
+                                      const int32_t *q_loc, const int32_t *k_loc,
+                                      const int32_t *q_loc_host, const int32_t *k_loc_host,
+                                      int32_t num_tokens, const void *q, const void *latent,
+                                      int64_t latent_ld, int32_t latent_rows,
+                                      const void *w_kv_b, const int32_t *accumulate, float *o,
+                                      float *lse, void *workspace, size_t workspace_bytes,
+                                      mla_stream_t stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (num_seqs < 0 || num_tokens < 0 || latent_rows < 0) return MLA_ERR_INVALID;
+  if (num_seqs == 0) return MLA_OK;
+  if (!q_loc || !k_loc || !q_loc_host || !k_loc_host || !q || !latent || !w_kv_b || !o ||
+      !lse || !workspace)
+    return MLA_ERR_INVALID;
+  if (latent_ld < d->kv_lora_rank + d->qk_rope_dim) return MLA_ERR_INVALID;
+  for (int i = 0; i < num_seqs; ++i)
+    if (q_loc_host[i + 1] < q_loc_host[i] || k_loc_host[i + 1] < k_loc_host[i])
+      return MLA_ERR_INVALID;
+  if (q_loc_host[0] < 0 || q_loc_host[num_seqs] > num_tokens) return MLA_ERR_INVALID;
+  if (k_loc_host[0] < 0 || latent_rows < k_loc_host[num_seqs]) return MLA_ERR_INVALID;
+  if (!tc_available() || !fused_attn_ok(*d, latent_ld) ||
+      !fused_attn_fits(num_seqs, q_loc_host, k_loc_host, 1))
+    return MLA_ERR_UNSUPPORTED;
+  PrefillBuffers b{};
+  if (workspace_bytes < fused_workspace(*d, num_tokens, nullptr, nullptr))
+    return MLA_ERR_TOO_SMALL;
+  fused_workspace(*d, num_tokens, workspace, &b);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_prepare_q(q, b.q_prep, num_tokens, d->num_heads, s);
+  if (rc) return rc;
+  return launch_attn_fused(*d, num_seqs, q_loc, k_loc, q_loc_host, k_loc_host, num_tokens,
+                           b.q_prep, latent, latent_ld, latent_rows, w_kv_b, accumulate, o, lse,
+                           &b.split, s);
+}
+
 extern "C" int mla_has_tcgen05(void) { return tc_available() ? 1 : 0; }
 
 extern "C" int mla_kernel_launches(uint64_t *count) {
@@ -737,9 +827,9 @@ extern "C" int mla_selftest_bounded_wait(int32_t limit_us, int32_t *gave_up,
 extern "C" int mla_device_error_flags(int32_t *flags) {
   if (!flags) return MLA_ERR_INVALID;
   if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
-  const int a = gemm_take_errors(), b = attn_take_errors();
-  if (a < 0 || b < 0) return MLA_ERR_CUDA;
-  *flags = a | b;
+  const int a = gemm_take_errors(), b = attn_take_errors(), c = fused_take_errors();
+  if (a < 0 || b < 0 || c < 0) return MLA_ERR_CUDA;
+  *flags = a | b | c;
   return MLA_OK;
 }
 

@@ -1125,6 +1125,30 @@ int launch_prepare_q(const void *q, void *qh, int T, int H, cudaStream_t s) {
   return launch_status();
 }
 
+// The key-split merge on its own, for launches that cut (sequence, query
+// tile, head) units elsewhere (the fused kernel): groups are (sequence, query
+// tile, first slot, number of slots).
+int launch_split_combine(int n_groups, const int4 *groups, int H, int T, const int32_t *q_loc,
+                         const int32_t *acc, const SplitScratch &split, float *o, float *lse,
+                         cudaStream_t s) {
+  if (n_groups <= 0) return MLA_OK;
+  if (n_groups > MAX_SPLIT_GROUPS) return MLA_ERR_UNSUPPORTED;
+  SplitGroups sg{};
+  sg.n = n_groups;
+  sg.H = H;
+  sg.T = T;
+  sg.q_loc = q_loc;
+  sg.acc = acc;
+  sg.split_o = split.o;
+  sg.split_lse = split.lse;
+  sg.o = o;
+  sg.lse = lse;
+  for (int k = 0; k < n_groups; ++k) sg.g[k] = groups[k];
+  const int64_t warps = int64_t(n_groups) * H * BQ;
+  split_combine_kernel<<<int((warps * 32 + 255) / 256), 256, 0, s>>>(sg);
+  return launch_status();
+}
+
 int attn_take_errors() { return sm103::take_error_flags_here(); }
 
 }  // namespace mla

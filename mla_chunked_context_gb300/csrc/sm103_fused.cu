@@ -1,0 +1,953 @@
+// Context-chunk attention with the W_kv_b up-projection fused in (sm_103a):
+// K_nope and V of every key tile are computed on chip from the gathered
+// latent rows and consumed there, never written to HBM.
+//
+// What it computes is the context attention of a chunk (PR #50613 report,
+// item 4: (O, LSE) per query row and head over the chunk's keys; item 3: a
+// continued request's result LSE-merged into its stored partial), with the
+// keys and values of the up-projection (DeepSeek-V3 MLA: W_kv_b [H*(Dn+Dv),
+// L], K_nope = c_kv W_k^T, V = c_kv W_v^T per head):
+//   s_j = scale * (q_nope . K_nope[j, h] + q_pe . k_pe[j]),
+//   O = sum_j softmax(s)_j V[j, h],  LSE = ln sum_j exp(s_j).
+// K_nope and V are rounded to fp16 once from the fp32 accumulator, as the
+// unfused path stores them, so both paths compute the same numbers.
+//
+// A cluster of two CTAs (one per SM) works on one head at a time, each CTA
+// holding half of the head's W_kv_b rows resident in tensor memory as the A
+// operand of its up-projection (128 rows x 512 bf16 = 256 TMEM columns):
+//   rank 0 (keys):   K^T tile = W_k (TMEM) x latent^T (the latent tile is the
+//                    B operand, multicast by TMA into both CTAs), converted to
+//                    fp16 in shared memory; S = Q K^T (M=128 queries, N=128
+//                    keys, K=192) and the online softmax; P is written as fp16
+//                    straight into rank 1's shared memory.
+//   rank 1 (values): V^T tile = W_v (TMEM) x latent^T, converted the same way;
+//                    O += P V (M=128, N=128, K=128) in TMEM; rescales O when
+//                    rank 0's running max grew; the epilogue.
+// Per 128-key tile each SM does 40-44 MMAs of 128x128x16 and moves about
+// 400 KB through shared memory, where the unfused path writes and re-reads
+// 64 KB of K/V per key and head through HBM.
+//
+// Units: a sequence of at most 128 queries (one query tile), a head, and a
+// range of its 128-key tiles.  The (head, sequence, key tile) space is cut
+// into one contiguous range per cluster; a (head, sequence) cut between
+// clusters writes each piece to a key-split scratch slot, merged afterwards
+// by the attention's split-combine kernel.
+//
+// Warps of each CTA (384 threads):
+//   0  rank 0: TMA producer (latent ring, k_pe, Q); rank 1: re-arms its ring
+//      barriers and tells rank 0 when a stage is free in both CTAs
+//   1  TMEM owner and MMA issuer
+//   2  rank 1: tells rank 0 when a P buffer is free again
+//   4-7  W rows into TMEM at each head change; accumulator -> fp16 staging
+//   8-11 rank 0: softmax (a thread per query row); rank 1: O rescale and the
+//        unit epilogue (a thread per query row)
+// TMEM, rank 0: W_k [0,256), up-projection / S buffers [256,384) [384,512)
+//       (a buffer holds a tile's K^T accumulator, then its S);
+//       rank 1: W_v [0,256), V^T accumulator [256,384), O [384,512).
+// Every wait is bounded (a timeout sets the error word and the roles wind
+// down); both CTAs meet at a cluster barrier before either leaves.
+#include <algorithm>
+#include <vector>
+
+#include "sm103.cuh"
+
+namespace mla {
+
+int launch_split_combine(int n_groups, const int4 *groups, int H, int T, const int32_t *q_loc,
+                         const int32_t *acc, const SplitScratch &split, float *o, float *lse,
+                         cudaStream_t s);
+
+namespace {
+
+using namespace sm103;
+
+constexpr int BQ = 128, BKV = 128;
+constexpr int LR = 512, DN = 128, DR = 64, DV = 128, DQK = DN + DR, HD = DN + DV;
+constexpr int KBLK = LR / 64;          // latent K-blocks of 64 per key tile
+constexpr int RING = 4;
+constexpr int STAGE = BKV * 64 * 2;     // 16 KB: 128 keys x 64 latent columns
+constexpr int QBOX = BQ * 64 * 2;       // 16 KB
+constexpr int HALF_OP = 128 * 64 * 2;   // one 64-wide block of a 128-row operand
+constexpr int OPND = 2 * HALF_OP;       // 32 KB: a 128 x 128 16-bit operand
+// shared memory, offsets from the 1024-aligned base, the same in both CTAs
+constexpr int OFF_RING = 0;                           // RING stages (both)
+constexpr int OFF_A = OFF_RING + RING * STAGE;
+constexpr int OFF_Q = OFF_A;                          // rank 0: Q, 3 boxes
+constexpr int OFF_KPE = OFF_A + 3 * QBOX;             // rank 0: k_pe [2]
+constexpr int OFF_P = OFF_A;                          // rank 1: P [2]
+constexpr int OFF_STG = OFF_A + 80 * 1024;            // K^T (rank 0) / V^T (rank 1) [2]
+constexpr int OFF_ALPHA = OFF_STG + 2 * OPND;         // rank 1: alpha [2][BQ]
+constexpr int OFF_STATS = OFF_ALPHA + 2 * BQ * 4;     // rank 1: [2 units][m, l][BQ]
+constexpr int OFF_BARS = OFF_STATS + 4 * BQ * 4;
+constexpr int NBARS = 48;
+constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
+constexpr int THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512, COL_W = 0, COL_ACC = 256, COL_O = 384;
+constexpr int MAX_PAIRS = 128;
+constexpr int MAX_ITEMS = 1024;
+constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth of the running max
+
+// mbarrier indices
+enum : int {
+  B_FULL = 0,     // [RING] stage landed (multicast; both CTAs)
+  B_EMPTY = 4,    // [RING] rank 0: stage used by both CTAs (own MMA commit + rank 1's relay)
+  B_RDONE = 8,    // [RING] rank 1: its MMAs are done with the stage
+  B_ACCF = 12,    // [2] up-projection accumulator complete (rank 1: [0])
+  B_STGR = 14,    // [2] fp16 staging written (K^T / V^T), 4 warps
+  B_STGF = 16,    // [2] staging read by the S MMA / P.V MMA
+  B_SFULL = 18,   // [2] rank 0: S complete
+  B_SREAD = 20,   // [2] rank 0: softmax has read S (4 warps); rank 1 [0]: accumulator read (4 warps)
+  B_KPEF = 22,    // [2] rank 0: k_pe landed
+  B_KPEE = 24,    // [2] rank 0: k_pe used
+  B_QF = 26,      // rank 0: Q landed
+  B_QE = 27,      // rank 0: Q used by the unit's last S
+  B_W = 28,       // W rows in TMEM (4 warps)
+  B_PFREE = 29,   // [2] rank 0: P buffer free in rank 1 (relay)
+  B_PFULL = 31,   // [2] rank 1: P and alpha written by rank 0 (4 warps)
+  B_OGO = 33,     // [2] rank 1: O ready for the tile's P.V (4 warps)
+  B_ODONE = 35,   // rank 1: a P.V completed
+  B_PDONE = 36,   // [2] rank 1: P.V done with a P buffer
+  B_STATS = 38,   // [2] rank 1: a unit's (m, l) written by rank 0 (4 warps)
+  B_OFREE = 40,   // rank 1: the epilogue has read O (4 warps)
+  B_DONE = 41,
+};
+
+struct FusedParams {
+  int n_items, H, T, npairs, tiles_per_head;
+  float scale_log2;
+  const int32_t *q_loc, *k_loc, *acc;
+  const uint16_t *w;                 // W_kv_b [H*(Dn+Dv)][L] bf16
+  float *o, *lse, *split_o, *split_lse;
+  int bounds[MAX_PAIRS + 1];         // cluster c: flattened key tiles [bounds[c], bounds[c+1])
+  // (sequence, key tiles, first tile in a head's order, (slot base + 1) | max pieces << 16)
+  int4 items[MAX_ITEMS];
+};
+
+// One unit of a cluster: head h, the sequence of item i, its key tiles
+// [kt0, kt1); slot >= 0: a piece of a split (h, sequence), whose last piece
+// also sets LSE = -inf in the slots [slot + 1, clear_to) no piece of this
+// head uses.
+struct Unit {
+  int h, seq, kt0, kt1, slot, clear_to;
+};
+
+__host__ __device__ inline int pair_of(const int *bounds, int npairs, int x) {
+  int lo = 0, hi = npairs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (bounds[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ bool next_unit(const FusedParams &p, int pair, int &f, Unit &u) {
+  const int f1 = p.bounds[pair + 1];
+  if (f >= f1) return false;
+  const int h = f / p.tiles_per_head, r = f - h * p.tiles_per_head;
+  int lo = 0, hi = p.n_items - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.items[mid].z <= r)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int4 it = p.items[lo];
+  u.h = h;
+  u.seq = it.x;
+  u.kt0 = r - it.z;
+  u.kt1 = min(it.y, u.kt0 + (f1 - f));
+  const int sb = (it.w & 0xffff) - 1, maxp = it.w >> 16;
+  if (sb < 0) {
+    u.slot = -1;
+    u.clear_to = 0;
+  } else {
+    u.slot = sb + pair - pair_of(p.bounds, p.npairs, h * p.tiles_per_head + it.z);
+    u.clear_to = u.kt1 == it.y ? sb + maxp : 0;
+  }
+  f += u.kt1 - u.kt0;
+  return true;
+}
+
+// D (+)= A (TMEM) x B (shared-memory descriptor)^T, kind::f16.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Wait with cluster-scope acquire: for phases completed by arrivals of the
+// other CTA, whose shared-memory writes this thread then reads.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  auto try_once = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once()) return true;
+  const long long t0 = clock64();
+  while (!try_once()) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(&g_error_flags, kErrWaitTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// This thread's generic-proxy writes to shared memory of the cluster become
+// visible to the async proxy (the tensor cores read P from there).
+__device__ __forceinline__ void fence_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Byte offset of 16-byte chunk c (0..15: columns 8c..8c+7) of row r in a
+// 128-row operand of two 64-column blocks, 128-byte swizzle.
+__device__ __forceinline__ uint32_t opnd_off(int r, int c) {
+  return uint32_t((c >> 3) * HALF_OP + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_lat,
+                      const __grid_constant__ FusedParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + OFF_BARS;
+  auto bar = [&](int k) { return bar0 + 8u * uint32_t(k); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BARS + NBARS * 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int f_begin = p.bounds[pair];
+
+  // ring uses and key tiles of this cluster (both CTAs walk the same units)
+  int total_tiles = 0;
+  {
+    int f = f_begin;
+    Unit u;
+    while (next_unit(p, pair, f, u)) total_tiles += u.kt1 - u.kt0;
+  }
+  const int total_uses = total_tiles * KBLK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RING; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), 2);
+      mbar_init(bar(B_RDONE + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_ACCF + b), 1);
+      mbar_init(bar(B_STGR + b), 4);
+      mbar_init(bar(B_STGF + b), 1);
+      mbar_init(bar(B_SFULL + b), 1);
+      mbar_init(bar(B_SREAD + b), 4);
+      mbar_init(bar(B_KPEF + b), 1);
+      mbar_init(bar(B_KPEE + b), 1);
+      mbar_init(bar(B_PFREE + b), 1);
+      mbar_init(bar(B_PFULL + b), 4);
+      mbar_init(bar(B_OGO + b), 4);
+      mbar_init(bar(B_PDONE + b), 1);
+      mbar_init(bar(B_STATS + b), 4);
+    }
+    mbar_init(bar(B_QF), 1);
+    mbar_init(bar(B_QE), 1);
+    mbar_init(bar(B_W), 4);
+    mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_OFREE), 4);
+    mbar_init(bar(B_DONE), 1);
+    fence_mbar_init();
+    if (rank == 0) {
+      prefetch_map(&tm_q);
+      prefetch_map(&tm_lat);
+    } else {
+      // rank 1's stages expect their first multicast before rank 0 issues it
+      for (int s = 0; s < RING && s < total_uses; ++s) mbar_expect_tx(bar(B_FULL + s), STAGE);
+    }
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any load or remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    if (rank == 0) {
+      // ---------------- TMA producer
+      int f = f_begin, J = 0, nu = 0;
+      Unit u;
+      bool ok = true;
+      int last_use[RING], kpe_par[2] = {-1, -1}, q_par = -1;
+      for (int s = 0; s < RING; ++s) last_use[s] = -1;
+      while (ok && next_unit(p, pair, f, u)) {
+        const int k_beg = __ldg(p.k_loc + u.seq), q_beg = __ldg(p.q_loc + u.seq);
+        for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
+          const int row = k_beg + j * BKV;
+          for (int kb = 0; kb < KBLK; ++kb) {
+            const int g = J * KBLK + kb, s = g % RING, n = g / RING;
+            if (n > 0 && !mbar_wait(bar(B_EMPTY + s), uint32_t((n - 1) & 1))) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(bar(B_FULL + s), STAGE);
+            tma_load_2d_mc(sbase + OFF_RING + s * STAGE, &tm_lat, bar(B_FULL + s), kb * 64, row,
+                           0x3);
+            last_use[s] = n;
+          }
+          if (!ok) break;
+          const int b = J & 1;
+          if (J >= 2 && !mbar_wait(bar(B_KPEE + b), uint32_t(((J - 2) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(B_KPEF + b), STAGE);
+          tma_load_2d(sbase + OFF_KPE + b * STAGE, &tm_lat, bar(B_KPEF + b), LR, row);
+          kpe_par[b] = (J >> 1) & 1;
+          if (j == u.kt0) {
+            // the unit's queries, once the previous unit's last S is done
+            // with the buffer (after this tile's loads: the up-projection
+            // needs no Q)
+            if (nu > 0 && !mbar_wait(bar(B_QE), uint32_t((nu - 1) & 1))) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(bar(B_QF), 3 * QBOX);
+            const int qy = u.h * p.T + q_beg;
+            for (int i = 0; i < 3; ++i)
+              tma_load_2d(sbase + OFF_Q + i * QBOX, &tm_q, bar(B_QF), i * 64, qy);
+            q_par = nu & 1;
+            ++nu;
+          }
+        }
+      }
+      // every load has landed (a stage: in both CTAs) before the CTA may leave
+      for (int s = 0; s < RING; ++s)
+        if (last_use[s] >= 0) {
+          mbar_wait(bar(B_FULL + s), uint32_t(last_use[s] & 1));
+          mbar_wait(bar(B_EMPTY + s), uint32_t(last_use[s] & 1));
+        }
+      for (int b = 0; b < 2; ++b)
+        if (kpe_par[b] >= 0) mbar_wait(bar(B_KPEF + b), uint32_t(kpe_par[b]));
+      if (q_par >= 0) mbar_wait(bar(B_QF), uint32_t(q_par));
+    } else {
+      // ---------------- rank 1: ring relay.  Once this CTA's MMAs are done
+      // with a stage, arm it for its next multicast, then tell the producer.
+      const uint32_t empty_rem = mapa_shared(bar(B_EMPTY), 0);
+      for (int g = 0; g < total_uses; ++g) {
+        const int s = g % RING, n = g / RING;
+        if (!mbar_wait(bar(B_RDONE + s), uint32_t(n & 1))) break;
+        if (g + RING < total_uses) mbar_expect_tx(bar(B_FULL + s), STAGE);
+        mbar_arrive_cluster(empty_rem + 8u * uint32_t(s));
+      }
+    }
+  } else if (warp == 2 && lane == 0 && rank == 1) {
+    // ---------------- rank 1: P-buffer relay to rank 0's softmax
+    const uint32_t pfree_rem = mapa_shared(bar(B_PFREE), 0);
+    for (int J = 0; J < total_tiles; ++J) {
+      const int b = J & 1;
+      if (!mbar_wait(bar(B_PDONE + b), uint32_t((J >> 1) & 1))) break;
+      mbar_arrive_cluster(pfree_rem + 8u * uint32_t(b));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t ID_G = idesc_f16kind(128, BKV, false, false, true);   // W x latent, bf16
+    constexpr uint32_t ID_SN = idesc_f16kind(BQ, BKV, false, true, false);   // q_nope x K^T, fp16
+    constexpr uint32_t ID_SR = idesc_f16kind(BQ, BKV, false, false, true);   // q_pe x k_pe, bf16
+    constexpr uint32_t ID_PV = idesc_f16kind(BQ, DV, false, false, false);   // P x V^T, fp16
+    const uint32_t q_addr = sbase + OFF_Q;
+    int f = f_begin, J = 0, nu = 0, prev_h = -1, wl = 0;
+    Unit u;
+    bool ok = true;
+    // the tile whose second MMA group (S on rank 0, P.V on rank 1) is still
+    // to be issued: it follows the next tile's up-projection
+    int pend = -1, pend_nu = 0;
+    bool pend_first = false, pend_last = false;
+    auto issue_second = [&](int Jx, bool first, bool last, int un) -> bool {
+      const int b = Jx & 1;
+      const uint32_t par = uint32_t((Jx >> 1) & 1);
+      if (rank == 0) {
+        if (!mbar_wait(bar(B_STGR + b), par) || !mbar_wait(bar(B_KPEF + b), par)) return false;
+        if (first && !mbar_wait(bar(B_QF), uint32_t(un & 1))) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + COL_ACC + uint32_t(b * 128);
+        const uint32_t kt = sbase + OFF_STG + uint32_t(b * OPND);
+        const uint32_t kp = sbase + OFF_KPE + uint32_t(b * STAGE);
+#pragma unroll
+        for (int kk = 0; kk < DN / 16; ++kk)
+          mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t((kk >> 2) * QBOX + (kk & 3) * 32)),
+                   desc_mnmajor_sw128(kt + uint32_t(kk * 2048), HALF_OP), ID_SN, kk != 0);
+#pragma unroll
+        for (int kk = 0; kk < DR / 16; ++kk)
+          mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t(2 * QBOX + kk * 32)),
+                   desc_kmajor_sw128(kp + uint32_t(kk * 32)), ID_SR, 1u);
+        mma_commit(bar(B_SFULL + b));
+        mma_commit(bar(B_STGF + b));
+        mma_commit(bar(B_KPEE + b));
+        if (last) mma_commit(bar(B_QE));
+      } else {
+        if (!mbar_wait(bar(B_STGR + b), par) || !mbar_wait(bar(B_OGO + b), par)) return false;
+        if (first && un > 0 && !mbar_wait(bar(B_OFREE), uint32_t((un - 1) & 1))) return false;
+        tc_fence_after();
+        const uint32_t pa = sbase + OFF_P + uint32_t(b * OPND);
+        const uint32_t vb = sbase + OFF_STG + uint32_t(b * OPND);
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk) {
+          const uint32_t off = uint32_t((kk >> 2) * HALF_OP + (kk & 3) * 32);
+          mma_bf16(tmem + COL_O, desc_kmajor_sw128(pa + off), desc_kmajor_sw128(vb + off), ID_PV,
+                   (first && kk == 0) ? 0u : 1u);
+        }
+        mma_commit(bar(B_PDONE + b));
+        mma_commit(bar(B_STGF + b));
+        mma_commit(bar(B_ODONE));
+      }
+      return true;
+    };
+    while (ok && next_unit(p, pair, f, u)) {
+      const int nt = u.kt1 - u.kt0;
+      // the previous unit's last tile first: it frees Q (rank 0) before this
+      // unit's queries are loaded, and needs no W
+      if (pend >= 0) {
+        ok = issue_second(pend, pend_first, pend_last, pend_nu);
+        pend = -1;
+        if (!ok) break;
+      }
+      if (u.h != prev_h) {
+        if (!mbar_wait(bar(B_W), uint32_t(wl & 1))) {
+          ok = false;
+          break;
+        }
+        ++wl;
+        prev_h = u.h;
+      }
+      for (int j = 0; ok && j < nt; ++j, ++J) {
+        const int b = J & 1;
+        // the accumulator: rank 0 alternates two buffers (each then holds
+        // the tile's S until the softmax has read it); rank 1 has one, free
+        // once the previous tile's V^T is read
+        const bool free_ok =
+            rank == 0 ? (J < 2 || mbar_wait(bar(B_SREAD + b), uint32_t(((J - 2) >> 1) & 1)))
+                      : (J < 1 || mbar_wait(bar(B_SREAD), uint32_t((J - 1) & 1)));
+        if (!free_ok) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + COL_ACC + uint32_t(rank == 0 ? b * 128 : 0);
+        for (int kb = 0; kb < KBLK; ++kb) {
+          const int g = J * KBLK + kb, s = g % RING, n = g / RING;
+          if (!mbar_wait(bar(B_FULL + s), uint32_t(n & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + OFF_RING + uint32_t(s * STAGE);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(d, tmem + COL_W + uint32_t(kb * 32 + k * 8),
+                   desc_kmajor_sw128(st + uint32_t(k * 32)), ID_G, (kb | k) != 0);
+          mma_commit(bar((rank == 0 ? B_EMPTY : B_RDONE) + s));
+        }
+        if (!ok) break;
+        mma_commit(bar(B_ACCF + (rank == 0 ? b : 0)));
+        if (pend >= 0) {
+          ok = issue_second(pend, pend_first, pend_last, pend_nu);
+          pend = -1;
+          if (!ok) break;
+        }
+        pend = J;
+        pend_first = j == 0;
+        pend_last = j == nt - 1;
+        pend_nu = nu;
+      }
+      ++nu;
+    }
+    if (ok && pend >= 0) issue_second(pend, pend_first, pend_last, pend_nu);
+    mma_commit(bar(B_DONE));
+    mbar_wait(bar(B_DONE), 0);
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- W rows into TMEM; accumulator -> fp16 operand staging
+    const int quarter = warp & 3, d = quarter * 32 + lane;  // W row / TMEM lane
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    int f = f_begin, J = 0, prev_h = -1;
+    Unit u;
+    bool ok = true;
+    while (ok && next_unit(p, pair, f, u)) {
+      if (u.h != prev_h) {
+        // the previous head's up-projections are complete: this warp has
+        // converted their last result
+        const uint4 *wr = reinterpret_cast<const uint4 *>(
+            p.w + (int64_t(u.h) * HD + int64_t(rank) * DN + d) * LR);
+#pragma unroll 1
+        for (int c = 0; c < LR / 64; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint4 v = __ldg(wr + c * 8 + e);
+            r[4 * e] = v.x;
+            r[4 * e + 1] = v.y;
+            r[4 * e + 2] = v.z;
+            r[4 * e + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_off + COL_W + uint32_t(c * 32), r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_W));
+        prev_h = u.h;
+      }
+      for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
+        const int b = J & 1;
+        const bool got = rank == 0 ? mbar_wait(bar(B_ACCF + b), uint32_t((J >> 1) & 1))
+                                   : mbar_wait(bar(B_ACCF), uint32_t(J & 1));
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t src = tmem + lane_off + COL_ACC + uint32_t(rank == 0 ? b * 128 : 0);
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(src + uint32_t(c * 32), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[c * 16 + e] = pack_f16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+        }
+        if (rank == 1) {  // the next tile's V^T may overwrite the accumulator
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_SREAD));
+        }
+        if (J >= 2 && !mbar_wait(bar(B_STGF + b), uint32_t(((J - 2) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        uint8_t *stg = smem + OFF_STG + b * OPND;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4 *>(stg + opnd_off(d, c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_async_smem();
+        tc_fence_before();  // rank 0: the tile's S overwrites the accumulator after this
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_STGR + b));
+      }
+    }
+  } else if (warp >= 8 && rank == 0) {
+    // ---------------- softmax, a thread per query row
+    const int quarter = warp & 3, row = quarter * 32 + lane;
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const uint32_t p_rem = mapa_shared(sbase + OFF_P, 1);
+    const uint32_t alpha_rem = mapa_shared(sbase + OFF_ALPHA, 1);
+    const uint32_t stats_rem = mapa_shared(sbase + OFF_STATS, 1);
+    const uint32_t pfull_rem = mapa_shared(bar(B_PFULL), 1);
+    const uint32_t statsb_rem = mapa_shared(bar(B_STATS), 1);
+    int f = f_begin, J = 0, ui = 0;
+    Unit u;
+    bool ok = true;
+    while (ok && next_unit(p, pair, f, u)) {
+      const int nk = __ldg(p.k_loc + u.seq + 1) - __ldg(p.k_loc + u.seq);
+      float m_used = neg_inf(), l = 0.f;
+      for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
+        const int b = J & 1;
+        if (!mbar_wait(bar(B_SFULL + b), uint32_t((J >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t s_col = tmem + lane_off + COL_ACC + uint32_t(b * 128);
+        const int valid = nk - j * BKV;  // keys of the sequence in this tile
+        float mx = neg_inf();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_col + uint32_t(c * 32), r);
+          tmem_wait_ld();
+          float t[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = (c * 32 + e < valid) ? __uint_as_float(r[e]) : neg_inf();
+            const float bb = (c * 32 + 16 + e < valid) ? __uint_as_float(r[16 + e]) : neg_inf();
+            t[e] = fmaxf(a, bb);
+          }
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+          mx = fmaxf(mx, t[0]);
+        }
+        mx *= p.scale_log2;
+        float alpha = 1.f;
+        if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
+          const float m_new = fmaxf(mx, m_used);
+          if (m_used != neg_inf() && m_new != neg_inf()) alpha = exp2f(m_used - m_new);
+          m_used = m_new;
+        }
+        const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
+        l *= alpha;
+        if (J >= 2 && !mbar_wait(bar(B_PFREE + b), uint32_t(((J - 2) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        const uint32_t pb = p_rem + uint32_t(b * OPND);
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_col + uint32_t(c * 32), r);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int k0 = c * 32 + 2 * e;
+            const float a =
+                k0 < valid ? ex2_approx(fmaf(__uint_as_float(r[2 * e]), p.scale_log2, nbase)) : 0.f;
+            const float bb = k0 + 1 < valid
+                                 ? ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), p.scale_log2, nbase))
+                                 : 0.f;
+            ls[e & 3] += a + bb;
+            pk[e] = pack_f16(a, bb);
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_cluster_v4(pb + opnd_off(row, c * 4 + q4), pk[4 * q4], pk[4 * q4 + 1],
+                          pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+        // S is read: the accumulator buffer may take the tile after next
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SREAD + b));
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        st_cluster_f32(alpha_rem + uint32_t((b * BQ + row) * 4), alpha);
+        fence_async_cluster();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(pfull_rem + 8u * uint32_t(b));
+      }
+      if (!ok) break;
+      st_cluster_f32(stats_rem + uint32_t(((ui & 1) * 2 * BQ + row) * 4), m_used);
+      st_cluster_f32(stats_rem + uint32_t(((ui & 1) * 2 * BQ + BQ + row) * 4), l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(statsb_rem + 8u * uint32_t(ui & 1));
+      ++ui;
+    }
+  } else if (warp >= 8) {
+    // ---------------- rank 1: O rescale and the unit epilogue, a thread per row
+    const int quarter = warp & 3, row = quarter * 32 + lane;
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const uint32_t o_col = tmem + lane_off + COL_O;
+    const float *alpha_s = reinterpret_cast<const float *>(smem + OFF_ALPHA);
+    const float *stats_s = reinterpret_cast<const float *>(smem + OFF_STATS);
+    int f = f_begin, J = 0, ui = 0;
+    Unit u;
+    bool ok = true;
+    while (ok && next_unit(p, pair, f, u)) {
+      for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
+        const int b = J & 1;
+        if (!mbar_wait_cluster(bar(B_PFULL + b), uint32_t((J >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        // the previous tile's P.V is done (waited on every tile, so the waits
+        // on the done barrier stay one phase apart; it costs nothing: this
+        // tile's P.V follows the next up-projection anyway)
+        if (J > 0 && !mbar_wait(bar(B_ODONE), uint32_t((J - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        const float alpha = alpha_s[b * BQ + row];
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // the running max grew: rescale O of this unit so far (alpha is 1
+          // on a unit's first tile)
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(o_col + uint32_t(c * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(o_col + uint32_t(c * 32), r);
+          }
+          tmem_wait_st();
+        }
+        fence_async_smem();  // P, written by rank 0, is read by this CTA's tensor cores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_OGO + b));
+      }
+      if (!ok) break;
+      // ---- epilogue of the unit
+      if (!mbar_wait(bar(B_ODONE), uint32_t((J - 1) & 1)) ||
+          !mbar_wait_cluster(bar(B_STATS + (ui & 1)), uint32_t((ui >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float m = stats_s[(ui & 1) * 2 * BQ + row];
+      const float lsum = stats_s[(ui & 1) * 2 * BQ + BQ + row];
+      const int q_beg = __ldg(p.q_loc + u.seq), nq = __ldg(p.q_loc + u.seq + 1) - q_beg;
+      const int t = q_beg + row;
+      float lse = (lsum > 0.f) ? (m + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
+      float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
+      bool write = row < nq;
+      float *orow, *lse_dst;
+      if (u.slot >= 0) {
+        const int64_t r = (int64_t(u.slot) * p.H + u.h) * BQ + row;
+        orow = p.split_o + r * DV;
+        lse_dst = p.split_lse + r;
+      } else {
+        orow = p.o + (int64_t(t) * p.H + u.h) * DV;
+        lse_dst = p.lse + int64_t(u.h) * p.T + t;
+        if (write && p.acc != nullptr && __ldg(p.acc + u.seq) != 0) {
+          const float old = *lse_dst;
+          if (lsum == 0.f) {
+            write = false;  // nothing new: keep the stored partial
+          } else if (!is_neg_inf(old)) {
+            const float m2 = fmaxf(old, lse);
+            const float eo = expf(old - m2), en = expf(lse - m2);
+            w_old = eo / (eo + en);
+            w_new *= en / (eo + en);
+            lse = m2 + logf(eo + en);
+          }
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(o_col + uint32_t(c * 32), r);
+        tmem_wait_ld();
+        if (c == DV / 32 - 1) {  // O is read: the next unit's first P.V may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_OFREE));
+        }
+        if (write) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 v = make_float4(__uint_as_float(r[4 * e]) * w_new,
+                                   __uint_as_float(r[4 * e + 1]) * w_new,
+                                   __uint_as_float(r[4 * e + 2]) * w_new,
+                                   __uint_as_float(r[4 * e + 3]) * w_new);
+            float4 *dst = reinterpret_cast<float4 *>(orow + c * 32) + e;
+            if (w_old != 0.f) {
+              const float4 ov = *dst;
+              v.x += w_old * ov.x;
+              v.y += w_old * ov.y;
+              v.z += w_old * ov.z;
+              v.w += w_old * ov.w;
+            }
+            *dst = v;
+          }
+        }
+      }
+      if (write) *lse_dst = lse;
+      if (row < nq)
+        for (int s2 = u.slot + 1; s2 < u.clear_to; ++s2)
+          p.split_lse[(int64_t(s2) * p.H + u.h) * BQ + row] = neg_inf();
+      ++ui;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still write to it
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+struct FusedItem {
+  int seq, tiles, tbase;
+};
+
+}  // namespace
+
+bool fused_attn_ok(const mla_dims_t &d, int64_t latent_ld) {
+  return d.dtype == MLA_DTYPE_BF16 && d.qk_nope_dim == DN && d.qk_rope_dim == DR &&
+         d.v_dim == DV && d.kv_lora_rank == LR && (latent_ld * 2) % 16 == 0 && latent_ld >= 576;
+}
+
+// Whether the fused kernel takes these sequences: at most 128 queries each
+// (one query tile: a second would repeat the up-projection), at most
+// MAX_ITEMS with keys, and on average at least `min_tiles` key tiles each
+// (each unit pays a queries load and a pipeline refill).
+bool fused_attn_fits(int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                     int min_tiles) {
+  int items = 0;
+  int64_t tiles = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int nq = q_loc_host[i + 1] - q_loc_host[i], nk = k_loc_host[i + 1] - k_loc_host[i];
+    if (nq <= 0 || nk <= 0) continue;
+    if (nq > BQ) return false;
+    ++items;
+    tiles += (nk + BKV - 1) / BKV;
+  }
+  return items > 0 && items <= MAX_ITEMS && tiles >= int64_t(min_tiles) * items;
+}
+
+int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
+                      const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                      int T, const void *q_prep, const void *latent, int64_t latent_ld, int rows,
+                      const void *w, const int32_t *acc, float *o, float *lse,
+                      const SplitScratch *split, cudaStream_t s) {
+  auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+  if (!fused_attn_ok(d, latent_ld) || !al16(q_prep) || !al16(latent) || !al16(w))
+    return MLA_ERR_UNSUPPORTED;
+  std::vector<FusedItem> items;
+  int tph = 0;  // key tiles per head
+  for (int i = 0; i < num_seqs; ++i) {
+    const int nq = q_loc_host[i + 1] - q_loc_host[i], nk = k_loc_host[i + 1] - k_loc_host[i];
+    if (nq <= 0 || nk <= 0) continue;  // no queries, or rows that keep O=0, LSE=-inf
+    if (nq > BQ) return MLA_ERR_UNSUPPORTED;
+    const int tiles = (nk + BKV - 1) / BKV;
+    items.push_back({i, tiles, tph});
+    tph += tiles;
+  }
+  if (items.empty()) return MLA_OK;
+  if (int(items.size()) > MAX_ITEMS) return MLA_ERR_UNSUPPORTED;
+  const int H = d.num_heads;
+  const int64_t N = int64_t(H) * tph;
+  if (N > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_fused_kernel, &cfg) != cudaSuccess || n < 1)
+      n = num_sms() / 2;
+    max_clusters = std::min(n, MAX_PAIRS);
+  }
+  const int P = int(std::min<int64_t>(max_clusters, N));
+
+  thread_local FusedParams prm;
+  prm.n_items = int(items.size());
+  prm.H = H;
+  prm.T = T;
+  prm.npairs = P;
+  prm.tiles_per_head = tph;
+  prm.scale_log2 = d.softmax_scale * 1.4426950408889634f;
+  prm.q_loc = q_loc;
+  prm.k_loc = k_loc;
+  prm.acc = acc;
+  prm.w = static_cast<const uint16_t *>(w);
+  prm.o = o;
+  prm.lse = lse;
+  prm.split_o = split ? split->o : nullptr;
+  prm.split_lse = split ? split->lse : nullptr;
+  // equal shares of the (head, sequence, key tile) space
+  for (int c = 0; c <= P; ++c) prm.bounds[c] = int(int64_t(c) * N / P);
+  // pieces of each (head, sequence) cut between clusters: the most over the
+  // heads sets the item's scratch slots
+  auto pieces = [&](std::vector<int> &maxp) {
+    maxp.assign(items.size(), 1);
+    for (int h = 0; h < H; ++h)
+      for (size_t i = 0; i < items.size(); ++i) {
+        const int x0 = h * tph + items[i].tbase, x1 = x0 + items[i].tiles - 1;
+        const int k = pair_of(prm.bounds, P, x1) - pair_of(prm.bounds, P, x0) + 1;
+        maxp[i] = std::max(maxp[i], k);
+      }
+  };
+  std::vector<int> maxp;
+  pieces(maxp);
+  int slots = 0, groups = 0;
+  for (int k : maxp)
+    if (k > 1) {
+      slots += k;
+      ++groups;
+    }
+  if (groups > 0 && (split == nullptr || split->o == nullptr || slots > split->slots ||
+                     groups > 16)) {
+    // too many cut units for the scratch: cut only between units instead,
+    // at the unit start nearest each equal share
+    for (int c = 1; c < P; ++c) {
+      const int x = prm.bounds[c], h = x / tph, r = x - h * tph;
+      size_t i = 0;
+      while (i + 1 < items.size() && items[i + 1].tbase <= r) ++i;
+      const int s0 = h * tph + items[i].tbase, s1 = s0 + items[i].tiles;
+      prm.bounds[c] = std::max(prm.bounds[c - 1], (x - s0 <= s1 - x) ? s0 : s1);
+    }
+    pieces(maxp);
+    slots = groups = 0;
+  }
+  std::vector<int4> sg;
+  int used = 0;
+  for (size_t i = 0; i < items.size(); ++i) {
+    int info = 0;
+    if (maxp[i] > 1) {
+      info = (used + 1) | (maxp[i] << 16);
+      sg.push_back(make_int4(items[i].seq, 0, used, maxp[i]));
+      used += maxp[i];
+    }
+    prm.items[i] = make_int4(items[i].seq, items[i].tiles, items[i].tbase, info);
+  }
+
+  CUtensorMap tq, tlat;
+  if (!make_tmap_2d_16(&tq, false, q_prep, DQK, uint64_t(H) * T, uint64_t(DQK) * 2, 64, BQ,
+                       true) ||
+      !make_tmap_2d_16(&tlat, false, latent, 576, uint64_t(rows > 0 ? rows : 1),
+                       uint64_t(latent_ld) * 2, 64, BKV, true))
+    return MLA_ERR_CUDA;
+  cfg.gridDim = dim3(2 * P);
+  if (cudaLaunchKernelEx(&cfg, attn_fused_kernel, tq, tlat, prm) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  int rc = launch_status();
+  if (rc) return rc;
+  if (!sg.empty())
+    rc = launch_split_combine(int(sg.size()), sg.data(), H, T, q_loc, acc, *split, o, lse, s);
+  return rc;
+}
+
+int fused_take_errors() { return sm103::take_error_flags_here(); }
+
+}  // namespace mla

@@ -433,6 +433,122 @@ def test_varlen_attention_accumulate():
         assert_close(f64(lse[:, a:b]), rl, 1e-3, what="LSE")
 
 
+# ------------------------------------------- fused up-projection (f2) --
+def _fused_inputs(w, n_rows, T, seed):
+    gen = torch.Generator().manual_seed(seed)
+    H = w.num_heads
+    q = torch.randn(T, H, w.qk_dim, generator=gen).to(w.torch_dtype)
+    lat = torch.randn(n_rows, w.latent_dim, generator=gen).to(w.torch_dtype)
+    wkv = (0.02 * torch.randn(H * (w.qk_nope_dim + w.v_dim), w.kv_lora_rank,
+                              generator=gen)).to(w.torch_dtype)
+    return q, lat, wkv
+
+
+def _oracle_fused(w, q, lat, wkv, q_loc, k_loc, key_rows=None):
+    """(O, LSE) of each sequence over its latent rows, up-projected by the
+    oracle; key_rows[i] overrides the rows of sequence i."""
+    L = w.kv_lora_rank
+    kn, v = O.up_project(f64(lat), f64(wkv), odims(w))
+    T, H = q.shape[0], w.num_heads
+    o = np.full((T, H, w.v_dim), np.nan)
+    lse = np.full((H, T), np.nan)
+    la = f64(lat)
+    for i in range(len(q_loc) - 1):
+        a, b = q_loc[i], q_loc[i + 1]
+        rows = key_rows[i] if key_rows is not None else np.arange(k_loc[i], k_loc[i + 1])
+        if a == b or len(rows) == 0:
+            continue
+        o[a:b], lse[:, a:b] = O.attention_with_lse(f64(q[a:b]), kn[rows], la[rows, L:], v[rows],
+                                                   w.softmax_scale)
+    return o, lse
+
+
+def _fused_case(heads, ql, kl, seed):
+    w = W.scaled(W.workload("uniform"), num_heads=heads, seed=seed)
+    q_loc = [0] + [int(x) for x in np.cumsum(ql)]
+    k_loc = [0] + [int(x) for x in np.cumsum(kl)]
+    q, lat, wkv = _fused_inputs(w, k_loc[-1], q_loc[-1], seed)
+    return w, q_loc, k_loc, q, lat, wkv
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_fused_context_attention(heads):
+    """Up-projection fused into the attention: ragged sequences of 1-128
+    queries and 1-8 key tiles (tails of 5, 44, 1 and 104 keys); a sequence
+    without queries and one without keys leave their rows untouched.  The
+    (head, sequence, key tile) space is cut into one range per cluster, so
+    some (head, sequence) units are split between clusters and merged."""
+    ql = [1, 128, 77, 5, 0, 100]
+    kl = [5, 300, 129, 1000, 64, 0]
+    w, q_loc, k_loc, q, lat, wkv = _fused_case(heads, ql, kl, 50)
+    T = q_loc[-1]
+    o = torch.full((T, heads, w.v_dim), 7.0, device=DEV)
+    lse = torch.full((heads, T), 3.0, device=DEV)
+    M.mla_fused_context_attn(M.Dims.of(w), q_loc, k_loc, q.to(DEV), lat.to(DEV), wkv.to(DEV),
+                             o, lse)
+    torch.cuda.synchronize()
+    ro, rl = _oracle_fused(w, q, lat, wkv, q_loc, k_loc)
+    keyless = slice(q_loc[5], q_loc[6])
+    ro[keyless], rl[:, keyless] = 7.0, 3.0   # untouched
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
+def test_fused_context_attention_split_and_accumulate():
+    """One long sequence over 16 heads, its 40 key tiles cut over many
+    clusters per head (up to 16 scratch slots), in two chunks: the second
+    accumulates into the first's partial; the result is attention over
+    both chunks' keys."""
+    heads, nq = 16, 99
+    k1, k2 = 2500, 2620
+    w, _, _, q, lat, wkv = _fused_case(heads, [nq], [k1 + k2], 51)
+    o = torch.full((nq, heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((heads, nq), float("nan"), device=DEV)
+    d = M.Dims.of(w)
+    gq, glat, gw = q.to(DEV), lat.to(DEV), wkv.to(DEV)
+    M.mla_fused_context_attn(d, [0, nq], [0, k1], gq, glat, gw, o, lse)
+    torch.cuda.synchronize()
+    ro1, rl1 = _oracle_fused(w, q, lat, wkv, [0, nq], [0, k1])
+    assert_close(f64(o), ro1, 2e-2, 2e-2, what="O chunk 1")
+    assert_close(f64(lse), rl1, 1e-3, what="LSE chunk 1")
+    M.mla_fused_context_attn(d, [0, nq], [k1, k1 + k2], gq, glat, gw, o, lse, accumulate=[1])
+    torch.cuda.synchronize()
+    ro, rl = _oracle_fused(w, q, lat, wkv, [0, nq], [0, k1 + k2])
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O accumulated")
+    assert_close(f64(lse), rl, 1e-3, what="LSE accumulated")
+
+
+@pytest.mark.parametrize("heads,seed", [(16, 52), (4, 53)])
+def test_fused_context_attention_many_sequences(heads, seed):
+    """40 sequences of 1-128 queries and 130-420 keys.  16 heads (seed 52):
+    six sequences are cut between clusters and merged from scratch slots;
+    4 heads (seed 53): more cut units than scratch slots, so the cluster
+    ranges end on unit boundaries instead."""
+    rng = np.random.default_rng(seed)
+    ql = [int(x) for x in rng.integers(1, 129, 40)]
+    kl = [int(x) for x in rng.integers(130, 421, 40)]
+    w, q_loc, k_loc, q, lat, wkv = _fused_case(heads, ql, kl, seed)
+    T = q_loc[-1]
+    o = torch.full((T, heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((heads, T), float("nan"), device=DEV)
+    M.mla_fused_context_attn(M.Dims.of(w), q_loc, k_loc, q.to(DEV), lat.to(DEV), wkv.to(DEV),
+                             o, lse)
+    torch.cuda.synchronize()
+    ro, rl = _oracle_fused(w, q, lat, wkv, q_loc, k_loc)
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
+def test_fused_context_attention_rejects_two_query_tiles():
+    w, q_loc, k_loc, q, lat, wkv = _fused_case(16, [129], [300], 53)
+    o = torch.zeros(129, 16, 128, device=DEV)
+    lse = torch.zeros(16, 129, device=DEV)
+    with pytest.raises(M.MlaError) as e:
+        M.mla_fused_context_attn(M.Dims.of(w), q_loc, k_loc, q.to(DEV), lat.to(DEV),
+                                 wkv.to(DEV), o, lse)
+    assert e.value.code == -5
+
+
 # ---------------------------------------------------------- whole prefill --
 def _run_prefill(w, x):
     g = to_dev(x)
