@@ -244,8 +244,8 @@ int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
  *   owned by the caller, reusable once the stream has passed the call.
  *   Runs for the DeepSeek-V3 head shape (L 512, P 64, Dn 128, Dv 128) on a
  *   tcgen05 GPU; MLA_ERR_UNSUPPORTED otherwise or when a sequence has more
- *   than 128 queries.  mla_chunked_prefill takes this path by itself for
- *   execution groups whose sequences all have at most 128 queries. */
+ *   than 128 queries.  Needs no K/V workspace; on GB300 it is slower than
+ *   the two-step path (mla_chunked_prefill does not use it). */
 int mla_fused_attn_workspace_bytes(const mla_dims_t *d, int32_t num_tokens,
                                    size_t *bytes);
 int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,

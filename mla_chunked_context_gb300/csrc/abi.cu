@@ -545,9 +545,6 @@ int build_prefill(const mla_dims_t &d, const int32_t *ctx, const int32_t *ql, in
 // tile) units of a chunk, split over their keys when the chunk has too few
 // units to fill the GPU).
 constexpr int kSplitSlots = 16;
-// Groups of sequences averaging fewer key tiles than this stay on the
-// unfused path (each fused unit pays a queries load and a pipeline refill).
-constexpr int kFusedMinTiles = 8;
 
 struct PrefillBuffers {
   int32_t *meta;
@@ -656,15 +653,6 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   const bool tc_attn = tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
                        aligned16(new_latent);
   const void *q_prep = tc_attn ? b.q_prep : nullptr;
-  // groups whose sequences each have at most one query tile (and enough
-  // keys) run the attention with the up-projection fused in (row f2): no
-  // K/V in HBM, no separate GEMM
-  std::vector<char> fused(p.metas.size(), 0);
-  if (q_prep && fused_attn_ok(*d, LP) && aligned16(w_kv_b))
-    for (size_t c = 0; c < p.metas.size(); ++c)
-      fused[c] = fused_attn_fits(p.metas[c].n, p.metas[c].q_loc.data(),
-                                 p.metas[c].cu_rows.data(), kFusedMinTiles) &&
-                 aligned16(b.chunk[c & 1].latent_ws);
 
   // The chunk pipeline (run_pipeline) over execution groups: consecutive
   // chunks with no continuation between them and rows within the budget
@@ -703,7 +691,6 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                              b.chunk[c & 1].latent_ws, dev_status, st_);
       },
       [&](size_t c, cudaStream_t st_) {
-        if (fused[c]) return int(MLA_OK);
         return up_proj(*d, b.chunk[c & 1].latent_ws, LP, p.metas[c].rows, w_kv_b,
                        b.chunk[c & 1].kv_ws, kv_dtype, st_);
       },
@@ -711,10 +698,6 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
         const ChunkMetaHost &m = p.metas[c];
         const int32_t *req, *st, *cu, *ql, *acc;
         meta_of(c, req, st, cu, ql, acc);
-        if (fused[c])
-          return launch_attn_fused(*d, m.n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q_prep,
-                                   b.chunk[c & 1].latent_ws, LP, m.rows, w_kv_b, acc, b.o_part,
-                                   b.lse_part, &b.split, st_);
         return attention(*d, 0, m.n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
                          b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
                          acc, b.o_part, b.lse_part, st_, &b.split, true, q_prep);

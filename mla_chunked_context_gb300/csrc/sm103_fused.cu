@@ -34,16 +34,16 @@
 // by the attention's split-combine kernel.
 //
 // Warps of each CTA (384 threads):
-//   0  rank 0: TMA producer (latent ring, k_pe, Q); rank 1: re-arms its ring
-//      barriers and tells rank 0 when a stage is free in both CTAs
-//   1  TMEM owner and MMA issuer
-//   2  rank 1: tells rank 0 when a P buffer is free again
+//   0  rank 0: TMA producer (latent ring, k_pe, Q)
+//   1  TMEM owner and MMA issuer; rank 1's MMA commits also arrive on rank
+//      0's barriers (a latent stage, a P buffer free again)
 //   4-7  W rows into TMEM at each head change; accumulator -> fp16 staging
 //   8-11 rank 0: softmax (a thread per query row); rank 1: O rescale and the
 //        unit epilogue (a thread per query row)
-// TMEM, rank 0: W_k [0,256), up-projection / S buffers [256,384) [384,512)
-//       (a buffer holds a tile's K^T accumulator, then its S);
+// TMEM, rank 0: W_k [0,256), K^T accumulator [256,384), S [384,512);
 //       rank 1: W_v [0,256), V^T accumulator [256,384), O [384,512).
+// The accumulator is free again once the convert warps have loaded it, so
+// the next tile's up-projection overlaps the conversion, S and the softmax.
 // Every wait is bounded (a timeout sets the error word and the roles wind
 // down); both CTAs meet at a cluster barrier before either leaves.
 #include <algorithm>
@@ -64,7 +64,8 @@ using namespace sm103;
 constexpr int BQ = 128, BKV = 128;
 constexpr int LR = 512, DN = 128, DR = 64, DV = 128, DQK = DN + DR, HD = DN + DV;
 constexpr int KBLK = LR / 64;          // latent K-blocks of 64 per key tile
-constexpr int RING = 4;
+constexpr int RING = 4;                 // latent stages in flight
+constexpr int NKPE = 2;                 // k_pe buffers
 constexpr int STAGE = BKV * 64 * 2;     // 16 KB: 128 keys x 64 latent columns
 constexpr int QBOX = BQ * 64 * 2;       // 16 KB
 constexpr int HALF_OP = 128 * 64 * 2;   // one 64-wide block of a 128-row operand
@@ -73,44 +74,48 @@ constexpr int OPND = 2 * HALF_OP;       // 32 KB: a 128 x 128 16-bit operand
 constexpr int OFF_RING = 0;                           // RING stages (both)
 constexpr int OFF_A = OFF_RING + RING * STAGE;
 constexpr int OFF_Q = OFF_A;                          // rank 0: Q, 3 boxes
-constexpr int OFF_KPE = OFF_A + 3 * QBOX;             // rank 0: k_pe [2]
+constexpr int OFF_KPE = OFF_A + 3 * QBOX;             // rank 0: k_pe [NKPE]
 constexpr int OFF_P = OFF_A;                          // rank 1: P [2]
-constexpr int OFF_STG = OFF_A + 80 * 1024;            // K^T (rank 0) / V^T (rank 1) [2]
+constexpr int OFF_STG = OFF_A + (3 * QBOX + NKPE * STAGE > 2 * OPND ? 3 * QBOX + NKPE * STAGE
+                                                                    : 2 * OPND);
+                                                      // K^T (rank 0) / V^T (rank 1) [2]
 constexpr int OFF_ALPHA = OFF_STG + 2 * OPND;         // rank 1: alpha [2][BQ]
 constexpr int OFF_STATS = OFF_ALPHA + 2 * BQ * 4;     // rank 1: [2 units][m, l][BQ]
 constexpr int OFF_BARS = OFF_STATS + 4 * BQ * 4;
-constexpr int NBARS = 48;
+constexpr int NBARS = 64;
 constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int THREADS = 384;
-constexpr uint32_t TMEM_COLS = 512, COL_W = 0, COL_ACC = 256, COL_O = 384;
+constexpr uint32_t TMEM_COLS = 512, COL_W = 0, COL_ACC = 256, COL_S = 384, COL_O = 384;
 constexpr int MAX_PAIRS = 128;
 constexpr int MAX_ITEMS = 1024;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth of the running max
 
 // mbarrier indices
 enum : int {
-  B_FULL = 0,     // [RING] stage landed (multicast; both CTAs)
-  B_EMPTY = 4,    // [RING] rank 0: stage used by both CTAs (own MMA commit + rank 1's relay)
-  B_RDONE = 8,    // [RING] rank 1: its MMAs are done with the stage
-  B_ACCF = 12,    // [2] up-projection accumulator complete (rank 1: [0])
-  B_STGR = 14,    // [2] fp16 staging written (K^T / V^T), 4 warps
-  B_STGF = 16,    // [2] staging read by the S MMA / P.V MMA
-  B_SFULL = 18,   // [2] rank 0: S complete
-  B_SREAD = 20,   // [2] rank 0: softmax has read S (4 warps); rank 1 [0]: accumulator read (4 warps)
-  B_KPEF = 22,    // [2] rank 0: k_pe landed
-  B_KPEE = 24,    // [2] rank 0: k_pe used
-  B_QF = 26,      // rank 0: Q landed
-  B_QE = 27,      // rank 0: Q used by the unit's last S
-  B_W = 28,       // W rows in TMEM (4 warps)
-  B_PFREE = 29,   // [2] rank 0: P buffer free in rank 1 (relay)
-  B_PFULL = 31,   // [2] rank 1: P and alpha written by rank 0 (4 warps)
-  B_OGO = 33,     // [2] rank 1: O ready for the tile's P.V (4 warps)
-  B_ODONE = 35,   // rank 1: a P.V completed
-  B_PDONE = 36,   // [2] rank 1: P.V done with a P buffer
-  B_STATS = 38,   // [2] rank 1: a unit's (m, l) written by rank 0 (4 warps)
-  B_OFREE = 40,   // rank 1: the epilogue has read O (4 warps)
-  B_DONE = 41,
+  B_FULL = 0,                // [RING] stage landed (multicast; both CTAs)
+  B_EMPTY = B_FULL + RING,   // [RING] rank 0: stage used by both CTAs' MMAs (a commit from each)
+  B_ACCF = B_EMPTY + RING,   // the up-projection accumulator is complete
+  B_ACCR,                    // the convert warps have loaded the accumulator (4 warps)
+  B_STGR,                    // [2] fp16 staging written (K^T / V^T), 4 warps
+  B_STGF = B_STGR + 2,       // [2] staging read by the S MMA / P.V MMA
+  B_SFULL = B_STGF + 2,      // rank 0: S complete
+  B_SREAD,                   // rank 0: the softmax has read S (4 warps)
+  B_KPEF,                    // [NKPE] rank 0: k_pe landed
+  B_KPEE = B_KPEF + NKPE,    // [NKPE] rank 0: k_pe used
+  B_QF = B_KPEE + NKPE,      // rank 0: Q landed
+  B_QE,                      // rank 0: Q used by the unit's last S
+  B_W,                       // W rows in TMEM (4 warps)
+  B_PFREE,                   // [2] rank 0: P buffer free in rank 1 (its P.V commit)
+  B_PFULL = B_PFREE + 2,     // [2] rank 1: P and alpha written by rank 0 (4 warps)
+  B_OGO = B_PFULL + 2,       // [2] rank 1: O ready for the tile's P.V (4 warps)
+  B_ODONE = B_OGO + 2,       // rank 1: a P.V completed
+  B_STATS,                   // [2] rank 1: a unit's (m, l) written by rank 0 (4 warps)
+  B_OFREE = B_STATS + 2,     // rank 1: the epilogue has read O (4 warps)
+  B_DONE,
+  B_COUNT
 };
+static_assert(B_COUNT <= NBARS, "barrier slots");
 
 struct FusedParams {
   int n_items, H, T, npairs, tiles_per_head;
@@ -262,22 +267,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < RING; ++s) {
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 2);
-      mbar_init(bar(B_RDONE + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_ACCF + b), 1);
       mbar_init(bar(B_STGR + b), 4);
       mbar_init(bar(B_STGF + b), 1);
-      mbar_init(bar(B_SFULL + b), 1);
-      mbar_init(bar(B_SREAD + b), 4);
-      mbar_init(bar(B_KPEF + b), 1);
-      mbar_init(bar(B_KPEE + b), 1);
       mbar_init(bar(B_PFREE + b), 1);
       mbar_init(bar(B_PFULL + b), 4);
       mbar_init(bar(B_OGO + b), 4);
-      mbar_init(bar(B_PDONE + b), 1);
       mbar_init(bar(B_STATS + b), 4);
     }
+    for (int b = 0; b < NKPE; ++b) {
+      mbar_init(bar(B_KPEF + b), 1);
+      mbar_init(bar(B_KPEE + b), 1);
+    }
+    mbar_init(bar(B_ACCF), 1);
+    mbar_init(bar(B_ACCR), 4);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SREAD), 4);
     mbar_init(bar(B_QF), 1);
     mbar_init(bar(B_QE), 1);
     mbar_init(bar(B_W), 4);
@@ -306,7 +312,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       int f = f_begin, J = 0, nu = 0;
       Unit u;
       bool ok = true;
-      int last_use[RING], kpe_par[2] = {-1, -1}, q_par = -1;
+      int last_use[RING], kpe_par[NKPE], q_par = -1;
+      for (int b = 0; b < NKPE; ++b) kpe_par[b] = -1;
       for (int s = 0; s < RING; ++s) last_use[s] = -1;
       while (ok && next_unit(p, pair, f, u)) {
         const int k_beg = __ldg(p.k_loc + u.seq), q_beg = __ldg(p.q_loc + u.seq);
@@ -324,14 +331,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             last_use[s] = n;
           }
           if (!ok) break;
-          const int b = J & 1;
-          if (J >= 2 && !mbar_wait(bar(B_KPEE + b), uint32_t(((J - 2) >> 1) & 1))) {
+          const int b = J % NKPE;
+          if (J >= NKPE && !mbar_wait(bar(B_KPEE + b), uint32_t((J / NKPE - 1) & 1))) {
             ok = false;
             break;
           }
           mbar_expect_tx(bar(B_KPEF + b), STAGE);
           tma_load_2d(sbase + OFF_KPE + b * STAGE, &tm_lat, bar(B_KPEF + b), LR, row);
-          kpe_par[b] = (J >> 1) & 1;
+          kpe_par[b] = (J / NKPE) & 1;
           if (j == u.kt0) {
             // the unit's queries, once the previous unit's last S is done
             // with the buffer (after this tile's loads: the up-projection
@@ -355,27 +362,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait(bar(B_FULL + s), uint32_t(last_use[s] & 1));
           mbar_wait(bar(B_EMPTY + s), uint32_t(last_use[s] & 1));
         }
-      for (int b = 0; b < 2; ++b)
+      for (int b = 0; b < NKPE; ++b)
         if (kpe_par[b] >= 0) mbar_wait(bar(B_KPEF + b), uint32_t(kpe_par[b]));
       if (q_par >= 0) mbar_wait(bar(B_QF), uint32_t(q_par));
-    } else {
-      // ---------------- rank 1: ring relay.  Once this CTA's MMAs are done
-      // with a stage, arm it for its next multicast, then tell the producer.
-      const uint32_t empty_rem = mapa_shared(bar(B_EMPTY), 0);
-      for (int g = 0; g < total_uses; ++g) {
-        const int s = g % RING, n = g / RING;
-        if (!mbar_wait(bar(B_RDONE + s), uint32_t(n & 1))) break;
-        if (g + RING < total_uses) mbar_expect_tx(bar(B_FULL + s), STAGE);
-        mbar_arrive_cluster(empty_rem + 8u * uint32_t(s));
-      }
-    }
-  } else if (warp == 2 && lane == 0 && rank == 1) {
-    // ---------------- rank 1: P-buffer relay to rank 0's softmax
-    const uint32_t pfree_rem = mapa_shared(bar(B_PFREE), 0);
-    for (int J = 0; J < total_tiles; ++J) {
-      const int b = J & 1;
-      if (!mbar_wait(bar(B_PDONE + b), uint32_t((J >> 1) & 1))) break;
-      mbar_arrive_cluster(pfree_rem + 8u * uint32_t(b));
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
@@ -395,12 +384,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int b = Jx & 1;
       const uint32_t par = uint32_t((Jx >> 1) & 1);
       if (rank == 0) {
-        if (!mbar_wait(bar(B_STGR + b), par) || !mbar_wait(bar(B_KPEF + b), par)) return false;
+        const int kb = Jx % NKPE;
+        if (!mbar_wait(bar(B_STGR + b), par) ||
+            !mbar_wait(bar(B_KPEF + kb), uint32_t((Jx / NKPE) & 1)))
+          return false;
         if (first && !mbar_wait(bar(B_QF), uint32_t(un & 1))) return false;
+        // the previous tile's S has been read by the softmax
+        if (Jx > 0 && !mbar_wait(bar(B_SREAD), uint32_t((Jx - 1) & 1))) return false;
         tc_fence_after();
-        const uint32_t d = tmem + COL_ACC + uint32_t(b * 128);
+        const uint32_t d = tmem + COL_S;
         const uint32_t kt = sbase + OFF_STG + uint32_t(b * OPND);
-        const uint32_t kp = sbase + OFF_KPE + uint32_t(b * STAGE);
+        const uint32_t kp = sbase + OFF_KPE + uint32_t(kb * STAGE);
 #pragma unroll
         for (int kk = 0; kk < DN / 16; ++kk)
           mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t((kk >> 2) * QBOX + (kk & 3) * 32)),
@@ -409,9 +403,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kk = 0; kk < DR / 16; ++kk)
           mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t(2 * QBOX + kk * 32)),
                    desc_kmajor_sw128(kp + uint32_t(kk * 32)), ID_SR, 1u);
-        mma_commit(bar(B_SFULL + b));
+        mma_commit(bar(B_SFULL));
         mma_commit(bar(B_STGF + b));
-        mma_commit(bar(B_KPEE + b));
+        mma_commit(bar(B_KPEE + kb));
         if (last) mma_commit(bar(B_QE));
       } else {
         if (!mbar_wait(bar(B_STGR + b), par) || !mbar_wait(bar(B_OGO + b), par)) return false;
@@ -425,7 +419,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mma_bf16(tmem + COL_O, desc_kmajor_sw128(pa + off), desc_kmajor_sw128(vb + off), ID_PV,
                    (first && kk == 0) ? 0u : 1u);
         }
-        mma_commit(bar(B_PDONE + b));
+        mma_commit_mc(bar(B_PFREE + b), 0x1);  // rank 0's softmax may write P again
         mma_commit(bar(B_STGF + b));
         mma_commit(bar(B_ODONE));
       }
@@ -449,35 +443,35 @@ __global__ void __launch_bounds__(THREADS, 1)
         prev_h = u.h;
       }
       for (int j = 0; ok && j < nt; ++j, ++J) {
-        const int b = J & 1;
-        // the accumulator: rank 0 alternates two buffers (each then holds
-        // the tile's S until the softmax has read it); rank 1 has one, free
-        // once the previous tile's V^T is read
-        const bool free_ok =
-            rank == 0 ? (J < 2 || mbar_wait(bar(B_SREAD + b), uint32_t(((J - 2) >> 1) & 1)))
-                      : (J < 1 || mbar_wait(bar(B_SREAD), uint32_t((J - 1) & 1)));
-        if (!free_ok) {
+        // the accumulator is free once the previous tile's result is loaded
+        if (J > 0 && !mbar_wait(bar(B_ACCR), uint32_t((J - 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + COL_ACC + uint32_t(rank == 0 ? b * 128 : 0);
+        const uint32_t d = tmem + COL_ACC;
         for (int kb = 0; kb < KBLK; ++kb) {
           const int g = J * KBLK + kb, s = g % RING, n = g / RING;
           if (!mbar_wait(bar(B_FULL + s), uint32_t(n & 1))) {
             ok = false;
             break;
           }
+          // rank 1 arms the stage's next phase itself: the producer issues
+          // that multicast only after this CTA's commit below
+          if (rank == 1 && g + RING < total_uses) mbar_expect_tx(bar(B_FULL + s), STAGE);
           tc_fence_after();
           const uint32_t st = sbase + OFF_RING + uint32_t(s * STAGE);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ts(d, tmem + COL_W + uint32_t(kb * 32 + k * 8),
                    desc_kmajor_sw128(st + uint32_t(k * 32)), ID_G, (kb | k) != 0);
-          mma_commit(bar((rank == 0 ? B_EMPTY : B_RDONE) + s));
+          if (rank == 0)
+            mma_commit(bar(B_EMPTY + s));
+          else
+            mma_commit_mc(bar(B_EMPTY + s), 0x1);  // rank 0's barrier
         }
         if (!ok) break;
-        mma_commit(bar(B_ACCF + (rank == 0 ? b : 0)));
+        mma_commit(bar(B_ACCF));
         if (pend >= 0) {
           ok = issue_second(pend, pend_first, pend_last, pend_nu);
           pend = -1;
@@ -527,14 +521,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
         const int b = J & 1;
-        const bool got = rank == 0 ? mbar_wait(bar(B_ACCF + b), uint32_t((J >> 1) & 1))
-                                   : mbar_wait(bar(B_ACCF), uint32_t(J & 1));
-        if (!got) {
+        if (!mbar_wait(bar(B_ACCF), uint32_t(J & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t src = tmem + lane_off + COL_ACC + uint32_t(rank == 0 ? b * 128 : 0);
+        const uint32_t src = tmem + lane_off + COL_ACC;
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -545,11 +537,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int e = 0; e < 16; ++e)
             pk[c * 16 + e] = pack_f16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
         }
-        if (rank == 1) {  // the next tile's V^T may overwrite the accumulator
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_SREAD));
-        }
+        // the next tile's up-projection may overwrite the accumulator
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_ACCR));
         if (J >= 2 && !mbar_wait(bar(B_STGF + b), uint32_t(((J - 2) >> 1) & 1))) {
           ok = false;
           break;
@@ -560,7 +551,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           *reinterpret_cast<uint4 *>(stg + opnd_off(d, c)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         fence_async_smem();
-        tc_fence_before();  // rank 0: the tile's S overwrites the accumulator after this
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_STGR + b));
       }
@@ -582,12 +572,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       float m_used = neg_inf(), l = 0.f;
       for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
         const int b = J & 1;
-        if (!mbar_wait(bar(B_SFULL + b), uint32_t((J >> 1) & 1))) {
+        if (!mbar_wait(bar(B_SFULL), uint32_t(J & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t s_col = tmem + lane_off + COL_ACC + uint32_t(b * 128);
+        const uint32_t s_col = tmem + lane_off + COL_S;
         const int valid = nk - j * BKV;  // keys of the sequence in this tile
         float mx = neg_inf();
 #pragma unroll
@@ -645,10 +635,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             st_cluster_v4(pb + opnd_off(row, c * 4 + q4), pk[4 * q4], pk[4 * q4 + 1],
                           pk[4 * q4 + 2], pk[4 * q4 + 3]);
         }
-        // S is read: the accumulator buffer may take the tile after next
+        // S is read: the next tile's S may overwrite it
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_SREAD + b));
+        if (lane == 0) mbar_arrive(bar(B_SREAD));
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         st_cluster_f32(alpha_rem + uint32_t((b * BQ + row) * 4), alpha);
         fence_async_cluster();
@@ -662,6 +652,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(statsb_rem + 8u * uint32_t(ui & 1));
       ++ui;
     }
+    // rank 1's last P.V commits arrive here: wait for them before leaving
+    for (int Jx = (J >= 2 ? J - 2 : 0); ok && Jx < J; ++Jx)
+      ok = mbar_wait(bar(B_PFREE + (Jx & 1)), uint32_t((Jx >> 1) & 1));
   } else if (warp >= 8) {
     // ---------------- rank 1: O rescale and the unit epilogue, a thread per row
     const int quarter = warp & 3, row = quarter * 32 + lane;
