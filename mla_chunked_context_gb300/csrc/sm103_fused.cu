@@ -21,8 +21,9 @@
 //                    keys, K=192) and the online softmax; P is written as fp16
 //                    straight into rank 1's shared memory.
 //   rank 1 (values): V^T tile = W_v (TMEM) x latent^T, converted the same way;
-//                    O += P V (M=128, N=128, K=128) in TMEM; rescales O when
-//                    rank 0's running max grew; the epilogue.
+//                    each tile's P V (M=128, N=128, K=128) into TMEM, summed
+//                    into O in registers with rank 0's rescale factor; the
+//                    epilogue.
 // Per 128-key tile each SM does 40-44 MMAs of 128x128x16 and moves about
 // 400 KB through shared memory, where the unfused path writes and re-reads
 // 64 KB of K/V per key and head through HBM.
@@ -33,17 +34,21 @@
 // clusters writes each piece to a key-split scratch slot, merged afterwards
 // by the attention's split-combine kernel.
 //
-// Warps of each CTA (384 threads):
+// Warps of each CTA (512 threads):
 //   0  rank 0: TMA producer (latent ring, k_pe, Q)
-//   1  TMEM owner and MMA issuer; rank 1's MMA commits also arrive on rank
-//      0's barriers (a latent stage, a P buffer free again)
+//   1  TMEM owner; issues each key tile's up-projection MMAs
+//   2  issues the tile's second MMA group (S on rank 0, P.V on rank 1)
+//      Rank 1's MMA commits also arrive on rank 0's barriers (a latent stage,
+//      a P buffer free again).
 //   4-7  W rows into TMEM at each head change; accumulator -> fp16 staging
-//   8-11 rank 0: softmax (a thread per query row); rank 1: O rescale and the
-//        unit epilogue (a thread per query row)
-// TMEM, rank 0: W_k [0,256), K^T accumulator [256,384), S [384,512);
-//       rank 1: W_v [0,256), V^T accumulator [256,384), O [384,512).
-// The accumulator is free again once the convert warps have loaded it, so
-// the next tile's up-projection overlaps the conversion, S and the softmax.
+//   8-15 rank 0: softmax (a thread per query row and half tile); rank 1: O
+//        in registers (a thread per query row and half of the columns),
+//        rescaled and summed over the tiles' P.V results, and the epilogue
+// TMEM: W half [0,256), buffers [256,384) [384,512).  Buffer b holds key
+// tile J's (J = b mod 2) up-projection accumulator until the convert warps
+// have loaded it, then the tile's second result (rank 0: S, rank 1: its P.V),
+// until the softmax / O warps have loaded that: the next tile's
+// up-projection never waits for the previous one's conversion.
 // Every wait is bounded (a timeout sets the error word and the roles wind
 // down); both CTAs meet at a cluster barrier before either leaves.
 #include <algorithm>
@@ -70,6 +75,7 @@ constexpr int STAGE = BKV * 64 * 2;     // 16 KB: 128 keys x 64 latent columns
 constexpr int QBOX = BQ * 64 * 2;       // 16 KB
 constexpr int HALF_OP = 128 * 64 * 2;   // one 64-wide block of a 128-row operand
 constexpr int OPND = 2 * HALF_OP;       // 32 KB: a 128 x 128 16-bit operand
+constexpr int P_BYTES = OPND + BQ * 4;  // a tile's P and alpha, sent by rank 0
 // shared memory, offsets from the 1024-aligned base, the same in both CTAs
 constexpr int OFF_RING = 0;                           // RING stages (both)
 constexpr int OFF_A = OFF_RING + RING * STAGE;
@@ -85,34 +91,32 @@ constexpr int OFF_BARS = OFF_STATS + 4 * BQ * 4;
 constexpr int NBARS = 64;
 constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-constexpr int THREADS = 384;
-constexpr uint32_t TMEM_COLS = 512, COL_W = 0, COL_ACC = 256, COL_S = 384, COL_O = 384;
+constexpr int THREADS = 512;
+constexpr uint32_t TMEM_COLS = 512, COL_W = 0, COL_BUF = 256;  // buffer b at COL_BUF + 128 b
 constexpr int MAX_PAIRS = 128;
 constexpr int MAX_ITEMS = 1024;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth of the running max
 
-// mbarrier indices
+// mbarrier indices.  TMEM buffer b (of 2) holds a key tile's up-projection
+// accumulator, then that tile's second result (rank 0: S, rank 1: its P.V).
 enum : int {
   B_FULL = 0,                // [RING] stage landed (multicast; both CTAs)
   B_EMPTY = B_FULL + RING,   // [RING] rank 0: stage used by both CTAs' MMAs (a commit from each)
-  B_ACCF = B_EMPTY + RING,   // the up-projection accumulator is complete
-  B_ACCR,                    // the convert warps have loaded the accumulator (4 warps)
-  B_STGR,                    // [2] fp16 staging written (K^T / V^T), 4 warps
-  B_STGF = B_STGR + 2,       // [2] staging read by the S MMA / P.V MMA
-  B_SFULL = B_STGF + 2,      // rank 0: S complete
-  B_SREAD,                   // rank 0: the softmax has read S (4 warps)
-  B_KPEF,                    // [NKPE] rank 0: k_pe landed
+  B_ACCF = B_EMPTY + RING,   // [2] the up-projection in buffer b is complete
+  B_STGR = B_ACCF + 2,       // [2] accumulator loaded and fp16 staging written (4 warps)
+  B_STGF = B_STGR + 2,       // [2] staging read by the tile's second MMA group
+  B_RESF = B_STGF + 2,       // [2] the tile's second result (S / P.V) is complete
+  B_RESR = B_RESF + 2,       // [2] ... and loaded (rank 0: softmax, rank 1: O warps; 8 warps)
+  B_KPEF = B_RESR + 2,       // [NKPE] rank 0: k_pe landed
   B_KPEE = B_KPEF + NKPE,    // [NKPE] rank 0: k_pe used
   B_QF = B_KPEE + NKPE,      // rank 0: Q landed
   B_QE,                      // rank 0: Q used by the unit's last S
   B_W,                       // W rows in TMEM (4 warps)
-  B_PFREE,                   // [2] rank 0: P buffer free in rank 1 (its P.V commit)
-  B_PFULL = B_PFREE + 2,     // [2] rank 1: P and alpha written by rank 0 (4 warps)
-  B_OGO = B_PFULL + 2,       // [2] rank 1: O ready for the tile's P.V (4 warps)
-  B_ODONE = B_OGO + 2,       // rank 1: a P.V completed
-  B_STATS,                   // [2] rank 1: a unit's (m, l) written by rank 0 (4 warps)
-  B_OFREE = B_STATS + 2,     // rank 1: the epilogue has read O (4 warps)
-  B_DONE,
+  B_PFREE,                   // [2] rank 0: P buffer free: rank 1's P.V commit + its 8 O warps
+  B_PFULL = B_PFREE + 2,     // [2] rank 1: P and alpha of a tile landed (rank 0's st.async bytes)
+  B_STATS = B_PFULL + 2,     // [2] rank 1: a unit's (m, l) written by rank 0 (4 warps)
+  B_DONE = B_STATS + 2,      // the up-projection issuer's MMAs are complete
+  B_DONE2,                   // the second issuer's MMAs are complete
   B_COUNT
 };
 static_assert(B_COUNT <= NBARS, "barrier slots");
@@ -211,19 +215,36 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
   return true;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
+// Asynchronous stores into a cluster peer's shared memory, each counting its
+// bytes on the peer's mbarrier at `rbar` (complete_tx): no fence and no
+// arrival by the writer.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(__float_as_uint(v)), "r"(rbar)
                : "memory");
 }
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-// This thread's generic-proxy writes to shared memory of the cluster become
-// visible to the async proxy (the tensor cores read P from there).
-__device__ __forceinline__ void fence_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+
+// Named barrier `id` over 8 warps (256 threads): AND of pred.
+__device__ __forceinline__ bool named_bar_and(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, %2, 256, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1 : 0), "r"(id)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -269,34 +290,33 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar(B_EMPTY + s), 2);
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_ACCF + b), 1);
       mbar_init(bar(B_STGR + b), 4);
       mbar_init(bar(B_STGF + b), 1);
-      mbar_init(bar(B_PFREE + b), 1);
-      mbar_init(bar(B_PFULL + b), 4);
-      mbar_init(bar(B_OGO + b), 4);
+      mbar_init(bar(B_RESF + b), 1);
+      mbar_init(bar(B_RESR + b), 8);
+      mbar_init(bar(B_PFREE + b), 9);
+      mbar_init(bar(B_PFULL + b), 1);
       mbar_init(bar(B_STATS + b), 4);
     }
     for (int b = 0; b < NKPE; ++b) {
       mbar_init(bar(B_KPEF + b), 1);
       mbar_init(bar(B_KPEE + b), 1);
     }
-    mbar_init(bar(B_ACCF), 1);
-    mbar_init(bar(B_ACCR), 4);
-    mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SREAD), 4);
     mbar_init(bar(B_QF), 1);
     mbar_init(bar(B_QE), 1);
     mbar_init(bar(B_W), 4);
-    mbar_init(bar(B_ODONE), 1);
-    mbar_init(bar(B_OFREE), 4);
     mbar_init(bar(B_DONE), 1);
+    mbar_init(bar(B_DONE2), 1);
     fence_mbar_init();
     if (rank == 0) {
       prefetch_map(&tm_q);
       prefetch_map(&tm_lat);
     } else {
-      // rank 1's stages expect their first multicast before rank 0 issues it
+      // rank 1's stages expect their first multicast before rank 0 issues it,
+      // its P buffers their first tile's P and alpha
       for (int s = 0; s < RING && s < total_uses; ++s) mbar_expect_tx(bar(B_FULL + s), STAGE);
+      for (int b = 0; b < 2 && b < total_tiles; ++b) mbar_expect_tx(bar(B_PFULL + b), P_BYTES);
     }
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -366,8 +386,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (kpe_par[b] >= 0) mbar_wait(bar(B_KPEF + b), uint32_t(kpe_par[b]));
       if (q_par >= 0) mbar_wait(bar(B_QF), uint32_t(q_par));
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+  } else if ((warp == 1 || warp == 2) && lane == 0) {
+    // ---------------- MMA issuers: warp 1 the up-projection of each key tile,
+    // warp 2 the tile's second group (S on rank 0, P.V on rank 1) as soon as
+    // its operands are staged, so that neither waits behind the other
     constexpr uint32_t ID_G = idesc_f16kind(128, BKV, false, false, true);   // W x latent, bf16
     constexpr uint32_t ID_SN = idesc_f16kind(BQ, BKV, false, true, false);   // q_nope x K^T, fp16
     constexpr uint32_t ID_SR = idesc_f16kind(BQ, BKV, false, false, true);   // q_pe x k_pe, bf16
@@ -376,117 +398,113 @@ __global__ void __launch_bounds__(THREADS, 1)
     int f = f_begin, J = 0, nu = 0, prev_h = -1, wl = 0;
     Unit u;
     bool ok = true;
-    // the tile whose second MMA group (S on rank 0, P.V on rank 1) is still
-    // to be issued: it follows the next tile's up-projection
-    int pend = -1, pend_nu = 0;
-    bool pend_first = false, pend_last = false;
-    auto issue_second = [&](int Jx, bool first, bool last, int un) -> bool {
-      const int b = Jx & 1;
-      const uint32_t par = uint32_t((Jx >> 1) & 1);
-      if (rank == 0) {
-        const int kb = Jx % NKPE;
-        if (!mbar_wait(bar(B_STGR + b), par) ||
-            !mbar_wait(bar(B_KPEF + kb), uint32_t((Jx / NKPE) & 1)))
-          return false;
-        if (first && !mbar_wait(bar(B_QF), uint32_t(un & 1))) return false;
-        // the previous tile's S has been read by the softmax
-        if (Jx > 0 && !mbar_wait(bar(B_SREAD), uint32_t((Jx - 1) & 1))) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + COL_S;
-        const uint32_t kt = sbase + OFF_STG + uint32_t(b * OPND);
-        const uint32_t kp = sbase + OFF_KPE + uint32_t(kb * STAGE);
-#pragma unroll
-        for (int kk = 0; kk < DN / 16; ++kk)
-          mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t((kk >> 2) * QBOX + (kk & 3) * 32)),
-                   desc_mnmajor_sw128(kt + uint32_t(kk * 2048), HALF_OP), ID_SN, kk != 0);
-#pragma unroll
-        for (int kk = 0; kk < DR / 16; ++kk)
-          mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t(2 * QBOX + kk * 32)),
-                   desc_kmajor_sw128(kp + uint32_t(kk * 32)), ID_SR, 1u);
-        mma_commit(bar(B_SFULL));
-        mma_commit(bar(B_STGF + b));
-        mma_commit(bar(B_KPEE + kb));
-        if (last) mma_commit(bar(B_QE));
-      } else {
-        if (!mbar_wait(bar(B_STGR + b), par) || !mbar_wait(bar(B_OGO + b), par)) return false;
-        if (first && un > 0 && !mbar_wait(bar(B_OFREE), uint32_t((un - 1) & 1))) return false;
-        tc_fence_after();
-        const uint32_t pa = sbase + OFF_P + uint32_t(b * OPND);
-        const uint32_t vb = sbase + OFF_STG + uint32_t(b * OPND);
-#pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint32_t off = uint32_t((kk >> 2) * HALF_OP + (kk & 3) * 32);
-          mma_bf16(tmem + COL_O, desc_kmajor_sw128(pa + off), desc_kmajor_sw128(vb + off), ID_PV,
-                   (first && kk == 0) ? 0u : 1u);
-        }
-        mma_commit_mc(bar(B_PFREE + b), 0x1);  // rank 0's softmax may write P again
-        mma_commit(bar(B_STGF + b));
-        mma_commit(bar(B_ODONE));
-      }
-      return true;
-    };
-    while (ok && next_unit(p, pair, f, u)) {
-      const int nt = u.kt1 - u.kt0;
-      // the previous unit's last tile first: it frees Q (rank 0) before this
-      // unit's queries are loaded, and needs no W
-      if (pend >= 0) {
-        ok = issue_second(pend, pend_first, pend_last, pend_nu);
-        pend = -1;
-        if (!ok) break;
-      }
-      if (u.h != prev_h) {
-        if (!mbar_wait(bar(B_W), uint32_t(wl & 1))) {
-          ok = false;
-          break;
-        }
-        ++wl;
-        prev_h = u.h;
-      }
-      for (int j = 0; ok && j < nt; ++j, ++J) {
-        // the accumulator is free once the previous tile's result is loaded
-        if (J > 0 && !mbar_wait(bar(B_ACCR), uint32_t((J - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem + COL_ACC;
-        for (int kb = 0; kb < KBLK; ++kb) {
-          const int g = J * KBLK + kb, s = g % RING, n = g / RING;
-          if (!mbar_wait(bar(B_FULL + s), uint32_t(n & 1))) {
+    if (warp == 1) {
+      while (ok && next_unit(p, pair, f, u)) {
+        if (u.h != prev_h) {
+          if (!mbar_wait(bar(B_W), uint32_t(wl & 1))) {
             ok = false;
             break;
           }
-          // rank 1 arms the stage's next phase itself: the producer issues
-          // that multicast only after this CTA's commit below
-          if (rank == 1 && g + RING < total_uses) mbar_expect_tx(bar(B_FULL + s), STAGE);
+          ++wl;
+          prev_h = u.h;
+        }
+        for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
+          const int b = J & 1;
+          // buffer b is free once tile J-2's second result has been loaded
+          if (J >= 2 && !mbar_wait(bar(B_RESR + b), uint32_t(((J - 2) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t st = sbase + OFF_RING + uint32_t(s * STAGE);
+          const uint32_t d = tmem + COL_BUF + uint32_t(b * 128);
+          for (int kb = 0; kb < KBLK; ++kb) {
+            const int g = J * KBLK + kb, s = g % RING, n = g / RING;
+            if (!mbar_wait(bar(B_FULL + s), uint32_t(n & 1))) {
+              ok = false;
+              break;
+            }
+            // rank 1 arms the stage's next phase itself: the producer issues
+            // that multicast only after this CTA's commit below
+            if (rank == 1 && g + RING < total_uses) mbar_expect_tx(bar(B_FULL + s), STAGE);
+            tc_fence_after();
+            const uint32_t st = sbase + OFF_RING + uint32_t(s * STAGE);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(d, tmem + COL_W + uint32_t(kb * 32 + k * 8),
-                   desc_kmajor_sw128(st + uint32_t(k * 32)), ID_G, (kb | k) != 0);
-          if (rank == 0)
-            mma_commit(bar(B_EMPTY + s));
-          else
-            mma_commit_mc(bar(B_EMPTY + s), 0x1);  // rank 0's barrier
-        }
-        if (!ok) break;
-        mma_commit(bar(B_ACCF));
-        if (pend >= 0) {
-          ok = issue_second(pend, pend_first, pend_last, pend_nu);
-          pend = -1;
+            for (int k = 0; k < 4; ++k)
+              mma_ts(d, tmem + COL_W + uint32_t(kb * 32 + k * 8),
+                     desc_kmajor_sw128(st + uint32_t(k * 32)), ID_G, (kb | k) != 0);
+            if (rank == 0)
+              mma_commit(bar(B_EMPTY + s));
+            else
+              mma_commit_mc(bar(B_EMPTY + s), 0x1);  // rank 0's barrier
+          }
           if (!ok) break;
+          mma_commit(bar(B_ACCF + b));
         }
-        pend = J;
-        pend_first = j == 0;
-        pend_last = j == nt - 1;
-        pend_nu = nu;
       }
-      ++nu;
+    } else {
+      while (ok && next_unit(p, pair, f, u)) {
+        const int nt = u.kt1 - u.kt0;
+        for (int j = 0; ok && j < nt; ++j, ++J) {
+          const int b = J & 1;
+          const uint32_t par = uint32_t((J >> 1) & 1);
+          const uint32_t d = tmem + COL_BUF + uint32_t(b * 128);
+          // the staging is written and the accumulator in buffer b loaded
+          if (!mbar_wait(bar(B_STGR + b), par)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) {
+            const int kb = J % NKPE;
+            if (!mbar_wait(bar(B_KPEF + kb), uint32_t((J / NKPE) & 1)) ||
+                (j == 0 && !mbar_wait(bar(B_QF), uint32_t(nu & 1)))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t kt = sbase + OFF_STG + uint32_t(b * OPND);
+            const uint32_t kp = sbase + OFF_KPE + uint32_t(kb * STAGE);
+#pragma unroll
+            for (int kk = 0; kk < DN / 16; ++kk)
+              mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t((kk >> 2) * QBOX + (kk & 3) * 32)),
+                       desc_mnmajor_sw128(kt + uint32_t(kk * 2048), HALF_OP), ID_SN, kk != 0);
+#pragma unroll
+            for (int kk = 0; kk < DR / 16; ++kk)
+              mma_bf16(d, desc_kmajor_sw128(q_addr + uint32_t(2 * QBOX + kk * 32)),
+                       desc_kmajor_sw128(kp + uint32_t(kk * 32)), ID_SR, 1u);
+            mma_commit(bar(B_RESF + b));
+            mma_commit(bar(B_STGF + b));
+            mma_commit(bar(B_KPEE + kb));
+            if (j == nt - 1) mma_commit(bar(B_QE));
+          } else {
+            // P and alpha of the tile, written by rank 0
+            if (!mbar_wait_cluster(bar(B_PFULL + b), par)) {
+              ok = false;
+              break;
+            }
+            // the buffer's next phase expects tile J+2's bytes (rank 0 sends
+            // them only after this tile's P.V and the O warps are done)
+            if (J + 2 < total_tiles) mbar_expect_tx(bar(B_PFULL + b), P_BYTES);
+            fence_async_smem();
+            tc_fence_after();
+            const uint32_t pa = sbase + OFF_P + uint32_t(b * OPND);
+            const uint32_t vb = sbase + OFF_STG + uint32_t(b * OPND);
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk) {
+              const uint32_t off = uint32_t((kk >> 2) * HALF_OP + (kk & 3) * 32);
+              mma_bf16(d, desc_kmajor_sw128(pa + off), desc_kmajor_sw128(vb + off), ID_PV,
+                       kk != 0);
+            }
+            mma_commit(bar(B_RESF + b));
+            mma_commit(bar(B_STGF + b));
+            mma_commit_mc(bar(B_PFREE + b), 0x1);  // rank 0's barrier
+          }
+        }
+        ++nu;
+      }
     }
-    if (ok && pend >= 0) issue_second(pend, pend_first, pend_last, pend_nu);
-    mma_commit(bar(B_DONE));
-    mbar_wait(bar(B_DONE), 0);
+    const uint32_t done = bar(warp == 1 ? B_DONE : B_DONE2);
+    mma_commit(done);
+    mbar_wait(done, 0);
   } else if (warp >= 4 && warp < 8) {
     // ---------------- W rows into TMEM; accumulator -> fp16 operand staging
     const int quarter = warp & 3, d = quarter * 32 + lane;  // W row / TMEM lane
@@ -521,12 +539,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
         const int b = J & 1;
-        if (!mbar_wait(bar(B_ACCF), uint32_t(J & 1))) {
+        if (!mbar_wait(bar(B_ACCF + b), uint32_t((J >> 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t src = tmem + lane_off + COL_ACC;
+        const uint32_t src = tmem + lane_off + COL_BUF + uint32_t(b * 128);
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -537,10 +555,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int e = 0; e < 16; ++e)
             pk[c * 16 + e] = pack_f16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
         }
-        // the next tile's up-projection may overwrite the accumulator
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_ACCR));
         if (J >= 2 && !mbar_wait(bar(B_STGF + b), uint32_t(((J - 2) >> 1) & 1))) {
           ok = false;
           break;
@@ -551,54 +565,69 @@ __global__ void __launch_bounds__(THREADS, 1)
           *reinterpret_cast<uint4 *>(stg + opnd_off(d, c)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         fence_async_smem();
+        tc_fence_before();  // the tile's second MMA group overwrites the accumulator after this
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_STGR + b));
       }
     }
   } else if (warp >= 8 && rank == 0) {
-    // ---------------- softmax, a thread per query row
-    const int quarter = warp & 3, row = quarter * 32 + lane;
+    // ---------------- softmax: two warps per TMEM sub-partition, a thread per
+    // query row and half tile (keys hw*64 .. hw*64+63).  The halves of a row
+    // agree on its running max through shared memory at a named barrier
+    // (an AND of the warps' status, so that all leave together after a wait
+    // gave up), then each writes its half of P and keeps its half of the sum.
+    const int quarter = warp & 3, row = quarter * 32 + lane, hw = (warp - 8) >> 2;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const uint32_t p_rem = mapa_shared(sbase + OFF_P, 1);
     const uint32_t alpha_rem = mapa_shared(sbase + OFF_ALPHA, 1);
     const uint32_t stats_rem = mapa_shared(sbase + OFF_STATS, 1);
     const uint32_t pfull_rem = mapa_shared(bar(B_PFULL), 1);
     const uint32_t statsb_rem = mapa_shared(bar(B_STATS), 1);
+    // exchange buffers (this CTA's copy of the alpha/stats area is unused):
+    // xmax [2 tiles][2 halves][BQ], xl [2 halves][BQ]
+    float *xmax = reinterpret_cast<float *>(smem + OFF_ALPHA);
+    float *xl = xmax + 4 * BQ;
     int f = f_begin, J = 0, ui = 0;
     Unit u;
     bool ok = true;
-    while (ok && next_unit(p, pair, f, u)) {
+    while (next_unit(p, pair, f, u)) {
       const int nk = __ldg(p.k_loc + u.seq + 1) - __ldg(p.k_loc + u.seq);
       float m_used = neg_inf(), l = 0.f;
-      for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
+      bool all = true;
+      for (int j = u.kt0; j < u.kt1; ++j, ++J) {
         const int b = J & 1;
-        if (!mbar_wait(bar(B_SFULL), uint32_t(J & 1))) {
-          ok = false;
-          break;
-        }
+        if (ok) ok = mbar_wait(bar(B_RESF + b), uint32_t((J >> 1) & 1));
         tc_fence_after();
-        const uint32_t s_col = tmem + lane_off + COL_S;
-        const int valid = nk - j * BKV;  // keys of the sequence in this tile
-        float mx = neg_inf();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_col + uint32_t(c * 32), r);
+        float sv[64];
+        if (ok) {
+          uint32_t r0[32], r1[32];
+          const uint32_t s_col = tmem + lane_off + COL_BUF + uint32_t(b * 128 + hw * 64);
+          tmem_ld32(s_col, r0);
+          tmem_ld32(s_col + 32u, r1);
           tmem_wait_ld();
-          float t[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float a = (c * 32 + e < valid) ? __uint_as_float(r[e]) : neg_inf();
-            const float bb = (c * 32 + 16 + e < valid) ? __uint_as_float(r[16 + e]) : neg_inf();
-            t[e] = fmaxf(a, bb);
+          for (int e = 0; e < 32; ++e) {
+            sv[e] = __uint_as_float(r0[e]);
+            sv[32 + e] = __uint_as_float(r1[e]);
           }
-#pragma unroll
-          for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-            for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
-          mx = fmaxf(mx, t[0]);
         }
-        mx *= p.scale_log2;
+        // S is loaded: the buffer may take the tile after next
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_RESR + b));
+        const int valid = nk - j * BKV - hw * 64;  // keys of the sequence in this half
+        float t[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          t[e] = fmaxf(e < valid ? sv[e] : neg_inf(), e + 32 < valid ? sv[e + 32] : neg_inf());
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+        xmax[(b * 2 + hw) * BQ + row] = t[0];
+        all = named_bar_and(1, ok);
+        if (!all) break;
+        const float mx = fmaxf(t[0], xmax[(b * 2 + (hw ^ 1)) * BQ + row]) * p.scale_log2;
         float alpha = 1.f;
         if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
           const float m_new = fmaxf(mx, m_used);
@@ -607,107 +636,90 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
         l *= alpha;
-        if (J >= 2 && !mbar_wait(bar(B_PFREE + b), uint32_t(((J - 2) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
+        if (J >= 2) ok = mbar_wait(bar(B_PFREE + b), uint32_t(((J - 2) >> 1) & 1));
+        if (!ok) continue;  // the next barrier takes every warp out
         const uint32_t pb = p_rem + uint32_t(b * OPND);
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_col + uint32_t(c * 32), r);
-          tmem_wait_ld();
-          uint32_t pk[16];
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int k0 = c * 32 + 2 * e;
-            const float a =
-                k0 < valid ? ex2_approx(fmaf(__uint_as_float(r[2 * e]), p.scale_log2, nbase)) : 0.f;
-            const float bb = k0 + 1 < valid
-                                 ? ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), p.scale_log2, nbase))
-                                 : 0.f;
-            ls[e & 3] += a + bb;
-            pk[e] = pack_f16(a, bb);
+          for (int e = 0; e < 4; ++e) {
+            const int k0 = c * 8 + 2 * e;
+            const float x0 = k0 < valid ? ex2_approx(fmaf(sv[k0], p.scale_log2, nbase)) : 0.f;
+            const float x1 =
+                k0 + 1 < valid ? ex2_approx(fmaf(sv[k0 + 1], p.scale_log2, nbase)) : 0.f;
+            ls[e] += x0 + x1;
+            pk[e] = pack_f16(x0, x1);
           }
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            st_cluster_v4(pb + opnd_off(row, c * 4 + q4), pk[4 * q4], pk[4 * q4 + 1],
-                          pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          st_async_v4(pb + opnd_off(row, hw * 8 + c), pk[0], pk[1], pk[2], pk[3],
+                      pfull_rem + 8u * uint32_t(b));
         }
-        // S is read: the next tile's S may overwrite it
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_SREAD));
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        st_cluster_f32(alpha_rem + uint32_t((b * BQ + row) * 4), alpha);
-        fence_async_cluster();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(pfull_rem + 8u * uint32_t(b));
+        if (hw == 0)
+          st_async_f32(alpha_rem + uint32_t((b * BQ + row) * 4), alpha, pfull_rem + 8u * uint32_t(b));
       }
-      if (!ok) break;
-      st_cluster_f32(stats_rem + uint32_t(((ui & 1) * 2 * BQ + row) * 4), m_used);
-      st_cluster_f32(stats_rem + uint32_t(((ui & 1) * 2 * BQ + BQ + row) * 4), l);
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(statsb_rem + 8u * uint32_t(ui & 1));
+      if (!all) break;
+      // the unit's (m, l) per row: the halves' sums share the running max
+      xl[hw * BQ + row] = l;
+      if (!named_bar_and(1, ok)) break;
+      if (hw == 0) {
+        st_cluster_f32(stats_rem + uint32_t(((ui & 1) * 2 * BQ + row) * 4), m_used);
+        st_cluster_f32(stats_rem + uint32_t(((ui & 1) * 2 * BQ + BQ + row) * 4),
+                       l + xl[BQ + row]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(statsb_rem + 8u * uint32_t(ui & 1));
+      }
       ++ui;
     }
-    // rank 1's last P.V commits arrive here: wait for them before leaving
+    // rank 1's last arrivals on the P buffers land here: wait for them
     for (int Jx = (J >= 2 ? J - 2 : 0); ok && Jx < J; ++Jx)
       ok = mbar_wait(bar(B_PFREE + (Jx & 1)), uint32_t((Jx >> 1) & 1));
   } else if (warp >= 8) {
-    // ---------------- rank 1: O rescale and the unit epilogue, a thread per row
-    const int quarter = warp & 3, row = quarter * 32 + lane;
+    // ---------------- rank 1: O accumulated in registers, a thread per query
+    // row and half of the 128 output columns: O = alpha O + (this tile's
+    // P.V), then the unit epilogue
+    const int quarter = warp & 3, row = quarter * 32 + lane, hw = (warp - 8) >> 2;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const uint32_t o_col = tmem + lane_off + COL_O;
+    const uint32_t pfree_rem = mapa_shared(bar(B_PFREE), 0);
     const float *alpha_s = reinterpret_cast<const float *>(smem + OFF_ALPHA);
     const float *stats_s = reinterpret_cast<const float *>(smem + OFF_STATS);
     int f = f_begin, J = 0, ui = 0;
     Unit u;
     bool ok = true;
-    while (ok && next_unit(p, pair, f, u)) {
-      for (int j = u.kt0; ok && j < u.kt1; ++j, ++J) {
+    // after a wait gave up, the remaining waits are skipped and the named
+    // barrier of the epilogue (an AND of the warps' status) takes all out
+    while (next_unit(p, pair, f, u)) {
+      float o[64];
+#pragma unroll
+      for (int e = 0; e < 64; ++e) o[e] = 0.f;
+      for (int j = u.kt0; j < u.kt1; ++j, ++J) {
         const int b = J & 1;
-        if (!mbar_wait_cluster(bar(B_PFULL + b), uint32_t((J >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-        // the previous tile's P.V is done (waited on every tile, so the waits
-        // on the done barrier stay one phase apart; it costs nothing: this
-        // tile's P.V follows the next up-projection anyway)
-        if (J > 0 && !mbar_wait(bar(B_ODONE), uint32_t((J - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        const float alpha = alpha_s[b * BQ + row];
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          // the running max grew: rescale O of this unit so far (alpha is 1
-          // on a unit's first tile)
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < DV / 32; ++c) {
+        const uint32_t par = uint32_t((J >> 1) & 1);
+        if (ok) ok = mbar_wait_cluster(bar(B_PFULL + b), par);
+        const float alpha = ok ? alpha_s[b * BQ + row] : 1.f;
+        __syncwarp();  // the warp's rows have read alpha: the P buffer may be rewritten
+        if (ok && lane == 0) mbar_arrive_cluster(pfree_rem + 8u * uint32_t(b));
+        if (ok) ok = mbar_wait(bar(B_RESF + b), par);
+        tc_fence_after();
+        if (ok) {
+          const uint32_t src = tmem + lane_off + COL_BUF + uint32_t(b * 128 + hw * 64);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
             uint32_t r[32];
-            tmem_ld32(o_col + uint32_t(c * 32), r);
+            tmem_ld32(src + uint32_t(c * 32), r);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(o_col + uint32_t(c * 32), r);
+            for (int e = 0; e < 32; ++e)
+              o[c * 32 + e] = fmaf(o[c * 32 + e], alpha, __uint_as_float(r[e]));
           }
-          tmem_wait_st();
         }
-        fence_async_smem();  // P, written by rank 0, is read by this CTA's tensor cores
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_OGO + b));
+        if (ok && lane == 0) mbar_arrive(bar(B_RESR + b));
       }
-      if (!ok) break;
       // ---- epilogue of the unit
-      if (!mbar_wait(bar(B_ODONE), uint32_t((J - 1) & 1)) ||
-          !mbar_wait_cluster(bar(B_STATS + (ui & 1)), uint32_t((ui >> 1) & 1))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      if (ok) ok = mbar_wait_cluster(bar(B_STATS + (ui & 1)), uint32_t((ui >> 1) & 1));
       const float m = stats_s[(ui & 1) * 2 * BQ + row];
       const float lsum = stats_s[(ui & 1) * 2 * BQ + BQ + row];
       const int q_beg = __ldg(p.q_loc + u.seq), nq = __ldg(p.q_loc + u.seq + 1) - q_beg;
@@ -736,37 +748,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-#pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(o_col + uint32_t(c * 32), r);
-        tmem_wait_ld();
-        if (c == DV / 32 - 1) {  // O is read: the next unit's first P.V may overwrite it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_OFREE));
-        }
-        if (write) {
+      // both halves have read the stored LSE before the first writes it
+      if (!named_bar_and(2, ok)) break;
+      if (write) {
+        float4 *dst = reinterpret_cast<float4 *>(orow + hw * 64);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float4 v = make_float4(__uint_as_float(r[4 * e]) * w_new,
-                                   __uint_as_float(r[4 * e + 1]) * w_new,
-                                   __uint_as_float(r[4 * e + 2]) * w_new,
-                                   __uint_as_float(r[4 * e + 3]) * w_new);
-            float4 *dst = reinterpret_cast<float4 *>(orow + c * 32) + e;
-            if (w_old != 0.f) {
-              const float4 ov = *dst;
-              v.x += w_old * ov.x;
-              v.y += w_old * ov.y;
-              v.z += w_old * ov.z;
-              v.w += w_old * ov.w;
-            }
-            *dst = v;
+        for (int e = 0; e < 16; ++e) {
+          float4 v = make_float4(o[4 * e] * w_new, o[4 * e + 1] * w_new, o[4 * e + 2] * w_new,
+                                 o[4 * e + 3] * w_new);
+          if (w_old != 0.f) {
+            const float4 ov = dst[e];
+            v.x += w_old * ov.x;
+            v.y += w_old * ov.y;
+            v.z += w_old * ov.z;
+            v.w += w_old * ov.w;
           }
+          dst[e] = v;
         }
+        if (hw == 0) *lse_dst = lse;
       }
-      if (write) *lse_dst = lse;
-      if (row < nq)
+      if (hw == 0 && row < nq)
         for (int s2 = u.slot + 1; s2 < u.clear_to; ++s2)
           p.split_lse[(int64_t(s2) * p.H + u.h) * BQ + row] = neg_inf();
       ++ui;
