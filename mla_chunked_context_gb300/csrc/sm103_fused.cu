@@ -16,8 +16,8 @@
 // holding half of the head's W_kv_b rows resident in tensor memory as the A
 // operand of its up-projection (128 rows x 512 bf16 = 256 TMEM columns):
 //   rank 0 (keys):   K^T tile = W_k (TMEM) x latent^T (the latent tile is the
-//                    B operand, multicast by TMA into both CTAs), converted to
-//                    fp16 in shared memory; S = Q K^T (M=128 queries, N=128
+//                    B operand, loaded by each CTA's own TMA producer),
+//                    converted to fp16 in shared memory; S = Q K^T (M=128 queries, N=128
 //                    keys, K=192) and the online softmax; P is written as fp16
 //                    straight into rank 1's shared memory.
 //   rank 1 (values): V^T tile = W_v (TMEM) x latent^T, converted the same way;
@@ -35,11 +35,15 @@
 // by the attention's split-combine kernel.
 //
 // Warps of each CTA (512 threads):
-//   0  rank 0: TMA producer (latent ring, k_pe, Q)
+//   0  TMA producer: the latent ring (both ranks), k_pe and Q (rank 0).
+//      Each CTA loads the latent itself: a stage multicast to both would
+//      wait for both SMs' MMAs before its refill and hold the two SMs in
+//      lock step (measured 1.59 ms against 1.25 ms on a 99 x 32768 chunk);
+//      the second read comes from L2, which is 12% busy.
 //   1  TMEM owner; issues each key tile's up-projection MMAs
-//   2  issues the tile's second MMA group (S on rank 0, P.V on rank 1)
-//      Rank 1's MMA commits also arrive on rank 0's barriers (a latent stage,
-//      a P buffer free again).
+//   2  issues the tile's second MMA group (S on rank 0, P.V on rank 1);
+//      rank 1's P.V commit also arrives on rank 0's barrier (a P buffer
+//      free again)
 //   4-7  W rows into TMEM at each head change; accumulator -> fp16 staging
 //   8-15 rank 0: softmax (a thread per query row and half tile); rank 1: O
 //        in registers (a thread per query row and half of the columns),
@@ -69,8 +73,8 @@ using namespace sm103;
 constexpr int BQ = 128, BKV = 128;
 constexpr int LR = 512, DN = 128, DR = 64, DV = 128, DQK = DN + DR, HD = DN + DV;
 constexpr int KBLK = LR / 64;          // latent K-blocks of 64 per key tile
-constexpr int RING = 4;                 // latent stages in flight
-constexpr int NKPE = 2;                 // k_pe buffers
+constexpr int RING = 5;                 // latent stages in flight
+constexpr int NKPE = 1;                 // k_pe buffers
 constexpr int STAGE = BKV * 64 * 2;     // 16 KB: 128 keys x 64 latent columns
 constexpr int QBOX = BQ * 64 * 2;       // 16 KB
 constexpr int HALF_OP = 128 * 64 * 2;   // one 64-wide block of a 128-row operand
@@ -100,8 +104,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth of th
 // mbarrier indices.  TMEM buffer b (of 2) holds a key tile's up-projection
 // accumulator, then that tile's second result (rank 0: S, rank 1: its P.V).
 enum : int {
-  B_FULL = 0,                // [RING] stage landed (multicast; both CTAs)
-  B_EMPTY = B_FULL + RING,   // [RING] rank 0: stage used by both CTAs' MMAs (a commit from each)
+  B_FULL = 0,                // [RING] latent stage landed
+  B_EMPTY = B_FULL + RING,   // [RING] latent stage used by this CTA's MMAs
   B_ACCF = B_EMPTY + RING,   // [2] the up-projection in buffer b is complete
   B_STGR = B_ACCF + 2,       // [2] accumulator loaded and fp16 staging written (4 warps)
   B_STGF = B_STGR + 2,       // [2] staging read by the tile's second MMA group
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RING; ++s) {
       mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_EMPTY + s), 2);
+      mbar_init(bar(B_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_ACCF + b), 1);
@@ -313,9 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_map(&tm_q);
       prefetch_map(&tm_lat);
     } else {
-      // rank 1's stages expect their first multicast before rank 0 issues it,
-      // its P buffers their first tile's P and alpha
-      for (int s = 0; s < RING && s < total_uses; ++s) mbar_expect_tx(bar(B_FULL + s), STAGE);
+      // rank 1's P buffers expect their first tile's P and alpha
       for (int b = 0; b < 2 && b < total_tiles; ++b) mbar_expect_tx(bar(B_PFULL + b), P_BYTES);
     }
   }
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    if (rank == 0) {
+    {
       // ---------------- TMA producer
       int f = f_begin, J = 0, nu = 0;
       Unit u;
@@ -346,11 +348,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             mbar_expect_tx(bar(B_FULL + s), STAGE);
-            tma_load_2d_mc(sbase + OFF_RING + s * STAGE, &tm_lat, bar(B_FULL + s), kb * 64, row,
-                           0x3);
+            tma_load_2d(sbase + OFF_RING + s * STAGE, &tm_lat, bar(B_FULL + s), kb * 64, row);
             last_use[s] = n;
           }
           if (!ok) break;
+          if (rank == 1) continue;
           const int b = J % NKPE;
           if (J >= NKPE && !mbar_wait(bar(B_KPEE + b), uint32_t((J / NKPE - 1) & 1))) {
             ok = false;
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // every load has landed (a stage: in both CTAs) before the CTA may leave
+      // every load has landed before the CTA may leave
       for (int s = 0; s < RING; ++s)
         if (last_use[s] >= 0) {
           mbar_wait(bar(B_FULL + s), uint32_t(last_use[s] & 1));
@@ -423,19 +425,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               ok = false;
               break;
             }
-            // rank 1 arms the stage's next phase itself: the producer issues
-            // that multicast only after this CTA's commit below
-            if (rank == 1 && g + RING < total_uses) mbar_expect_tx(bar(B_FULL + s), STAGE);
             tc_fence_after();
             const uint32_t st = sbase + OFF_RING + uint32_t(s * STAGE);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_ts(d, tmem + COL_W + uint32_t(kb * 32 + k * 8),
                      desc_kmajor_sw128(st + uint32_t(k * 32)), ID_G, (kb | k) != 0);
-            if (rank == 0)
-              mma_commit(bar(B_EMPTY + s));
-            else
-              mma_commit_mc(bar(B_EMPTY + s), 0x1);  // rank 0's barrier
+            mma_commit(bar(B_EMPTY + s));
           }
           if (!ok) break;
           mma_commit(bar(B_ACCF + b));
