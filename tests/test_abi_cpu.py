@@ -194,3 +194,31 @@ def test_c_equal_window_planner_matches_oracle():
     with pytest.raises(M.MlaError) as e:
         M.mla_plan_equal_window_chunks([5, 5, 5], 2, 1)
     assert e.value.code == _lib.MLA_ERR_PLANNER_STUCK
+
+
+def test_fused_entry_host_checks():
+    """mla_fused_context_attn: workspace size, argument errors, and the
+    shape limit (at most 128 queries per sequence), all returned before
+    anything is launched."""
+    L = _lib.lib()
+    w = W.workload("uniform")
+    dims = _lib.Dims.of(w)
+    d = dims.c()
+    T, H = 512, w.num_heads
+    need = T * H * 192 * 2 + 16 * H * 128 * (128 + 1) * 4
+    got = M.mla_fused_attn_workspace_bytes(dims, T)
+    assert need <= got <= need + 4096
+    fake = C.c_void_p(16)
+    ql, kl = _lib._i32_host([0, 100]), _lib._i32_host([0, 300])
+
+    def call(q_loc, k_loc, q=fake, latent_ld=576, rows=300, n=1):
+        return L.mla_fused_context_attn(C.byref(d), n, fake, fake, q_loc, k_loc, T, q, fake,
+                                        latent_ld, rows, fake, None, fake, fake, fake, 1 << 30,
+                                        None)
+    assert call(ql, kl, q=None) == _lib.MLA_ERR_INVALID
+    assert call(ql, kl, latent_ld=500) == _lib.MLA_ERR_INVALID
+    assert call(ql, kl, rows=299) == _lib.MLA_ERR_INVALID            # keys past the latent rows
+    assert call(_lib._i32_host([100, 0]), kl) == _lib.MLA_ERR_INVALID
+    assert call(ql, kl, n=0) == _lib.MLA_OK                            # nothing to do
+    # a sequence of two query tiles is refused whatever the GPU
+    assert call(_lib._i32_host([0, 129]), kl) == _lib.MLA_ERR_UNSUPPORTED

@@ -539,6 +539,25 @@ def test_fused_context_attention_many_sequences(heads, seed):
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+@pytest.mark.parametrize("heads,ql,kl", [(1, [1, 128], [1, 128]), (7, [57], [3000]),
+                                         (3, [57], [3000])])
+def test_fused_context_attention_edge_heads(heads, ql, kl):
+    """One head with a one-key and a one-full-tile sequence (two clusters,
+    one tile each); 7 heads of one 24-tile sequence cut into up to 12 pieces
+    each, cluster ranges crossing head boundaries; 3 heads of it: more
+    pieces than scratch slots, so one cluster per head and most idle."""
+    w, q_loc, k_loc, q, lat, wkv = _fused_case(heads, ql, kl, 54)
+    T = q_loc[-1]
+    o = torch.full((T, heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((heads, T), float("nan"), device=DEV)
+    M.mla_fused_context_attn(M.Dims.of(w), q_loc, k_loc, q.to(DEV), lat.to(DEV), wkv.to(DEV),
+                             o, lse)
+    torch.cuda.synchronize()
+    ro, rl = _oracle_fused(w, q, lat, wkv, q_loc, k_loc)
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_fused_context_attention_rejects_two_query_tiles():
     w, q_loc, k_loc, q, lat, wkv = _fused_case(16, [129], [300], 53)
     o = torch.zeros(129, 16, 128, device=DEV)
