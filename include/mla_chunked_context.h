@@ -257,6 +257,26 @@ int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
                            float *o, float *lse, void *workspace,
                            size_t workspace_bytes, mla_stream_t stream);
 
+/* mla_fused_attn_plan (host only, no GPU needed): how mla_fused_context_attn
+ *   splits its work over `clusters` 2-SM clusters.  items[4*i .. 4*i+3] =
+ *   (sequence, key tiles of 128, first tile in a head's order, slot info =
+ *   (first scratch slot + 1) | slots << 16, or 0 when the item is never cut),
+ *   one per sequence with queries and keys; cluster c takes the flattened
+ *   (head, item, key tile) positions [bounds[c], bounds[c+1]), head-major.
+ *   A (head, item) unit cut between clusters writes each piece to a key-split
+ *   scratch slot; when that would take more than split_slots slots or 16 cut
+ *   items, the ranges end on unit boundaries instead.  num_clusters (at most
+ *   min(clusters, 128)), num_items and num_groups (cut items) are returned;
+ *   pass bounds = items = NULL for those counts alone, else capacities of at
+ *   least num_clusters + 1 and num_items (MLA_ERR_TOO_SMALL otherwise).
+ *   MLA_ERR_UNSUPPORTED when a sequence has more than 128 queries. */
+int mla_fused_attn_plan(int32_t num_heads, int32_t num_seqs,
+                        const int32_t *q_loc_host, const int32_t *k_loc_host,
+                        int32_t clusters, int32_t split_slots, int32_t *bounds,
+                        int32_t bounds_cap, int32_t *items, int32_t items_cap,
+                        int32_t *num_clusters, int32_t *num_items,
+                        int32_t *num_groups);
+
 /* mla_fill_empty_rows  (PR #50613 report, item 3, init_mla_context_partial):
  *   o[t, :, :] = 0 and lse[:, t] = -inf for t in each [slices[2k],
  *   slices[2k+1]).  slices device int32 [2*num_slices]; o float32 [T, H, Dv];

@@ -15,7 +15,8 @@ from ._lib import (Chunk, Dims, MlaError, lib, merge_attn_states, mla_chunk_kv_d
                    mla_varlen_attn, MLA_STATUS_BAD_BLOCK, mla_plan_equal_window_chunks,
                    mla_prefill_equal_window_workspace_bytes, mla_chunked_prefill_equal_window,
                    mla_selftest_bounded_wait, mla_kernel_launches,
-                   mla_fused_attn_workspace_bytes, mla_fused_context_attn)
+                   mla_fused_attn_workspace_bytes, mla_fused_context_attn,
+                   mla_fused_attn_plan)
 
 __all__ = ["Chunk", "Dims", "MlaError", "lib", "merge_attn_states", "mla_chunk_kv_dtype",
            "mla_chunk_workspace_bytes", "mla_device_error_flags",
@@ -26,7 +27,7 @@ __all__ = ["Chunk", "Dims", "MlaError", "lib", "merge_attn_states", "mla_chunk_k
            "mla_varlen_attn", "MLA_STATUS_BAD_BLOCK", "mla_plan_equal_window_chunks",
            "mla_prefill_equal_window_workspace_bytes", "mla_chunked_prefill_equal_window",
            "mla_selftest_bounded_wait", "mla_kernel_launches", "mla_fused_attn_workspace_bytes",
-           "mla_fused_context_attn", "ChunkedPrefill"]
+           "mla_fused_context_attn", "mla_fused_attn_plan", "ChunkedPrefill"]
 
 
 class ChunkedPrefill:

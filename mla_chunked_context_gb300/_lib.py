@@ -37,7 +37,7 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_plan_equal_window_chunks", "mla_prefill_equal_window_workspace_bytes",
             "mla_chunked_prefill_equal_window", "mla_selftest_bounded_wait",
             "mla_kernel_launches", "mla_fused_attn_workspace_bytes",
-            "mla_fused_context_attn")
+            "mla_fused_context_attn", "mla_fused_attn_plan")
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -91,6 +91,7 @@ def lib() -> C.CDLL:
             "mla_has_tcgen05": [],
             "mla_kernel_launches": [P],
             "mla_fused_attn_workspace_bytes": [P, I32, P],
+            "mla_fused_attn_plan": [I32, I32, P, P, I32, I32, P, I32, P, I32, P, P, P],
             "mla_fused_context_attn": [P, I32, P, P, P, P, I32, P, P, I64, I32, P, P, P, P, P,
                                        SZ, P],
             "mla_device_error_flags": [P],
@@ -306,6 +307,25 @@ def mla_fused_context_attn(dims: Dims, q_loc: Sequence[int], k_loc: Sequence[int
                                         _ptr(acc), _ptr(o), _ptr(lse), _ptr(workspace),
                                         workspace.numel(), _stream(stream)),
            "mla_fused_context_attn")
+
+
+def mla_fused_attn_plan(num_heads: int, q_loc: Sequence[int], k_loc: Sequence[int],
+                        clusters: int, split_slots: int):
+    """The fused kernel's work split (host only): (bounds, items, groups)
+    with items as (sequence, key tiles, first tile, slot info) tuples."""
+    L = lib()
+    n = len(q_loc) - 1
+    ql, kl = _i32_host(q_loc), _i32_host(k_loc)
+    nc, ni, ng = C.c_int32(0), C.c_int32(0), C.c_int32(0)
+    _check(L.mla_fused_attn_plan(num_heads, n, ql, kl, clusters, split_slots, None, 0, None, 0,
+                                 C.byref(nc), C.byref(ni), C.byref(ng)), "mla_fused_attn_plan")
+    b = (C.c_int32 * (nc.value + 1))()
+    it = (C.c_int32 * max(1, 4 * ni.value))()
+    _check(L.mla_fused_attn_plan(num_heads, n, ql, kl, clusters, split_slots, b, nc.value + 1,
+                                 it, ni.value, C.byref(nc), C.byref(ni), C.byref(ng)),
+           "mla_fused_attn_plan")
+    items = [tuple(it[4 * i:4 * i + 4]) for i in range(ni.value)]
+    return list(b), items, ng.value
 
 
 def mla_fill_empty_rows(o, lse, slices: Sequence, stream=None) -> None:

@@ -62,6 +62,13 @@
 
 namespace mla {
 
+struct FusedPlan {
+  int tph = 0, P = 0;          // key tiles per head, clusters
+  std::vector<int4> items;     // (sequence, key tiles, first tile, (slot base + 1) | pieces << 16)
+  std::vector<int> bounds;     // P + 1 range ends
+  std::vector<int4> groups;    // split-combine groups (sequence, 0, first slot, slots)
+};
+
 int launch_split_combine(int n_groups, const int4 *groups, int H, int T, const int32_t *q_loc,
                          const int32_t *acc, const SplitScratch &split, float *o, float *lse,
                          cudaStream_t s);
@@ -143,6 +150,8 @@ struct FusedParams {
 struct Unit {
   int h, seq, kt0, kt1, slot, clear_to;
 };
+
+constexpr int MAX_SPLIT_GROUPS = 16;  // groups one split-combine launch takes
 
 __host__ __device__ inline int pair_of(const int *bounds, int npairs, int x) {
   int lo = 0, hi = npairs - 1;
@@ -279,14 +288,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int pair = blockIdx.x >> 1;
   const int f_begin = p.bounds[pair];
 
-  // ring uses and key tiles of this cluster (both CTAs walk the same units)
+  // key tiles of this cluster (both CTAs walk the same units)
   int total_tiles = 0;
   {
     int f = f_begin;
     Unit u;
     while (next_unit(p, pair, f, u)) total_tiles += u.kt1 - u.kt0;
   }
-  const int total_uses = total_tiles * KBLK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RING; ++s) {
@@ -779,10 +787,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-struct FusedItem {
-  int seq, tiles, tbase;
-};
-
 }  // namespace
 
 bool fused_attn_ok(const mla_dims_t &d, int64_t latent_ld) {
@@ -808,16 +812,21 @@ bool fused_attn_fits(int num_seqs, const int32_t *q_loc_host, const int32_t *k_l
   return items > 0 && items <= MAX_ITEMS && tiles >= int64_t(min_tiles) * items;
 }
 
-int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
-                      const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
-                      int T, const void *q_prep, const void *latent, int64_t latent_ld, int rows,
-                      const void *w, const int32_t *acc, float *o, float *lse,
-                      const SplitScratch *split, cudaStream_t s) {
-  auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
-  if (!fused_attn_ok(d, latent_ld) || !al16(q_prep) || !al16(latent) || !al16(w))
-    return MLA_ERR_UNSUPPORTED;
-  std::vector<FusedItem> items;
-  int tph = 0;  // key tiles per head
+// The fused kernel's work split (host only): the sequences with queries
+// and keys become items (sequence, key tiles, first tile in a head's order,
+// slot info); cluster c takes the flattened (head, item, key tile) range
+// [bounds[c], bounds[c+1]) of equal shares; a (head, item) unit cut between
+// clusters writes each piece to a key-split scratch slot (the item gets as
+// many slots as the most pieces of any head), merged by the split-combine
+// groups.  When the cut items need more than `split_slots` slots or 16
+// groups, the ranges end on unit boundaries instead (the unit start nearest
+// each equal share) and nothing is cut.
+int plan_fused(int H, int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
+               int clusters, int split_slots, FusedPlan &plan) {
+  plan = FusedPlan{};
+  struct It { int seq, tiles, tbase; };
+  std::vector<It> items;
+  int tph = 0;
   for (int i = 0; i < num_seqs; ++i) {
     const int nq = q_loc_host[i + 1] - q_loc_host[i], nk = k_loc_host[i + 1] - k_loc_host[i];
     if (nq <= 0 || nk <= 0) continue;  // no queries, or rows that keep O=0, LSE=-inf
@@ -827,11 +836,64 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
     tph += tiles;
   }
   if (items.empty()) return MLA_OK;
-  if (int(items.size()) > MAX_ITEMS) return MLA_ERR_UNSUPPORTED;
-  const int H = d.num_heads;
+  if (int(items.size()) > MAX_ITEMS || clusters < 1) return MLA_ERR_UNSUPPORTED;
   const int64_t N = int64_t(H) * tph;
   if (N > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  const int P = int(std::min<int64_t>(std::min(clusters, MAX_PAIRS), N));
+  plan.tph = tph;
+  plan.P = P;
+  plan.bounds.resize(P + 1);
+  for (int c = 0; c <= P; ++c) plan.bounds[c] = int(int64_t(c) * N / P);
+  auto pieces = [&](std::vector<int> &maxp) {
+    maxp.assign(items.size(), 1);
+    for (int h = 0; h < H; ++h)
+      for (size_t i = 0; i < items.size(); ++i) {
+        const int x0 = h * tph + items[i].tbase, x1 = x0 + items[i].tiles - 1;
+        const int k =
+            pair_of(plan.bounds.data(), P, x1) - pair_of(plan.bounds.data(), P, x0) + 1;
+        maxp[i] = std::max(maxp[i], k);
+      }
+  };
+  std::vector<int> maxp;
+  pieces(maxp);
+  int slots = 0, groups = 0;
+  for (int k : maxp)
+    if (k > 1) {
+      slots += k;
+      ++groups;
+    }
+  if (groups > 0 && (slots > split_slots || groups > MAX_SPLIT_GROUPS)) {
+    for (int c = 1; c < P; ++c) {
+      const int x = plan.bounds[c], h = x / tph, r = x - h * tph;
+      size_t i = 0;
+      while (i + 1 < items.size() && items[i + 1].tbase <= r) ++i;
+      const int s0 = h * tph + items[i].tbase, s1 = s0 + items[i].tiles;
+      plan.bounds[c] = std::max(plan.bounds[c - 1], (x - s0 <= s1 - x) ? s0 : s1);
+    }
+    pieces(maxp);
+  }
+  int used = 0;
+  for (size_t i = 0; i < items.size(); ++i) {
+    int info = 0;
+    if (maxp[i] > 1) {
+      info = (used + 1) | (maxp[i] << 16);
+      plan.groups.push_back(make_int4(items[i].seq, 0, used, maxp[i]));
+      used += maxp[i];
+    }
+    plan.items.push_back(make_int4(items[i].seq, items[i].tiles, items[i].tbase, info));
+  }
+  return MLA_OK;
+}
 
+int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
+                      const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                      int T, const void *q_prep, const void *latent, int64_t latent_ld, int rows,
+                      const void *w, const int32_t *acc, float *o, float *lse,
+                      const SplitScratch *split, cudaStream_t s) {
+  auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+  if (!fused_attn_ok(d, latent_ld) || !al16(q_prep) || !al16(latent) || !al16(w))
+    return MLA_ERR_UNSUPPORTED;
+  const int H = d.num_heads;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -858,14 +920,17 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
       n = num_sms() / 2;
     max_clusters = std::min(n, MAX_PAIRS);
   }
-  const int P = int(std::min<int64_t>(max_clusters, N));
-
+  FusedPlan plan;
+  int rc = plan_fused(H, num_seqs, q_loc_host, k_loc_host, max_clusters,
+                      (split && split->o) ? split->slots : 0, plan);
+  if (rc || plan.items.empty()) return rc;
+  const int P = plan.P;
   thread_local FusedParams prm;
-  prm.n_items = int(items.size());
+  prm.n_items = int(plan.items.size());
   prm.H = H;
   prm.T = T;
   prm.npairs = P;
-  prm.tiles_per_head = tph;
+  prm.tiles_per_head = plan.tph;
   prm.scale_log2 = d.softmax_scale * 1.4426950408889634f;
   prm.q_loc = q_loc;
   prm.k_loc = k_loc;
@@ -875,52 +940,8 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
   prm.lse = lse;
   prm.split_o = split ? split->o : nullptr;
   prm.split_lse = split ? split->lse : nullptr;
-  // equal shares of the (head, sequence, key tile) space
-  for (int c = 0; c <= P; ++c) prm.bounds[c] = int(int64_t(c) * N / P);
-  // pieces of each (head, sequence) cut between clusters: the most over the
-  // heads sets the item's scratch slots
-  auto pieces = [&](std::vector<int> &maxp) {
-    maxp.assign(items.size(), 1);
-    for (int h = 0; h < H; ++h)
-      for (size_t i = 0; i < items.size(); ++i) {
-        const int x0 = h * tph + items[i].tbase, x1 = x0 + items[i].tiles - 1;
-        const int k = pair_of(prm.bounds, P, x1) - pair_of(prm.bounds, P, x0) + 1;
-        maxp[i] = std::max(maxp[i], k);
-      }
-  };
-  std::vector<int> maxp;
-  pieces(maxp);
-  int slots = 0, groups = 0;
-  for (int k : maxp)
-    if (k > 1) {
-      slots += k;
-      ++groups;
-    }
-  if (groups > 0 && (split == nullptr || split->o == nullptr || slots > split->slots ||
-                     groups > 16)) {
-    // too many cut units for the scratch: cut only between units instead,
-    // at the unit start nearest each equal share
-    for (int c = 1; c < P; ++c) {
-      const int x = prm.bounds[c], h = x / tph, r = x - h * tph;
-      size_t i = 0;
-      while (i + 1 < items.size() && items[i + 1].tbase <= r) ++i;
-      const int s0 = h * tph + items[i].tbase, s1 = s0 + items[i].tiles;
-      prm.bounds[c] = std::max(prm.bounds[c - 1], (x - s0 <= s1 - x) ? s0 : s1);
-    }
-    pieces(maxp);
-    slots = groups = 0;
-  }
-  std::vector<int4> sg;
-  int used = 0;
-  for (size_t i = 0; i < items.size(); ++i) {
-    int info = 0;
-    if (maxp[i] > 1) {
-      info = (used + 1) | (maxp[i] << 16);
-      sg.push_back(make_int4(items[i].seq, 0, used, maxp[i]));
-      used += maxp[i];
-    }
-    prm.items[i] = make_int4(items[i].seq, items[i].tiles, items[i].tbase, info);
-  }
+  for (int c = 0; c <= P; ++c) prm.bounds[c] = plan.bounds[c];
+  for (size_t i = 0; i < plan.items.size(); ++i) prm.items[i] = plan.items[i];
 
   CUtensorMap tq, tlat;
   if (!make_tmap_2d_16(&tq, false, q_prep, DQK, uint64_t(H) * T, uint64_t(DQK) * 2, 64, BQ,
@@ -931,13 +952,47 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
   cfg.gridDim = dim3(2 * P);
   if (cudaLaunchKernelEx(&cfg, attn_fused_kernel, tq, tlat, prm) != cudaSuccess)
     return MLA_ERR_CUDA;
-  int rc = launch_status();
+  rc = launch_status();
   if (rc) return rc;
-  if (!sg.empty())
-    rc = launch_split_combine(int(sg.size()), sg.data(), H, T, q_loc, acc, *split, o, lse, s);
+  if (!plan.groups.empty())
+    rc = launch_split_combine(int(plan.groups.size()), plan.groups.data(), H, T, q_loc, acc,
+                              *split, o, lse, s);
   return rc;
 }
 
 int fused_take_errors() { return sm103::take_error_flags_here(); }
 
 }  // namespace mla
+
+// Host-only view of the fused kernel's work split (what launch_attn_fused
+// would hand each cluster), for checks without a GPU.
+extern "C" int mla_fused_attn_plan(int32_t num_heads, int32_t num_seqs, const int32_t *q_loc_host,
+                                   const int32_t *k_loc_host, int32_t clusters,
+                                   int32_t split_slots, int32_t *bounds, int32_t bounds_cap,
+                                   int32_t *items, int32_t items_cap, int32_t *num_clusters,
+                                   int32_t *num_items, int32_t *num_groups) {
+  if (num_heads < 1 || num_seqs < 0 || clusters < 1 || split_slots < 0 || !num_clusters ||
+      !num_items || !num_groups || (num_seqs > 0 && (!q_loc_host || !k_loc_host)))
+    return MLA_ERR_INVALID;
+  for (int i = 0; i < num_seqs; ++i)
+    if (q_loc_host[i + 1] < q_loc_host[i] || k_loc_host[i + 1] < k_loc_host[i])
+      return MLA_ERR_INVALID;
+  mla::FusedPlan plan;
+  const int rc = mla::plan_fused(num_heads, num_seqs, q_loc_host, k_loc_host, clusters,
+                                 split_slots, plan);
+  if (rc) return rc;
+  *num_clusters = plan.P;
+  *num_items = int32_t(plan.items.size());
+  *num_groups = int32_t(plan.groups.size());
+  if (bounds == nullptr && items == nullptr) return MLA_OK;  // sizes only
+  if (!bounds || !items || bounds_cap < plan.P + 1 || items_cap < int(plan.items.size()))
+    return MLA_ERR_TOO_SMALL;
+  for (int c = 0; c <= plan.P; ++c) bounds[c] = plan.bounds[c];
+  for (size_t i = 0; i < plan.items.size(); ++i) {
+    items[4 * i] = plan.items[i].x;
+    items[4 * i + 1] = plan.items[i].y;
+    items[4 * i + 2] = plan.items[i].z;
+    items[4 * i + 3] = plan.items[i].w;
+  }
+  return MLA_OK;
+}

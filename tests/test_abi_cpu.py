@@ -222,3 +222,93 @@ def test_fused_entry_host_checks():
     assert call(ql, kl, n=0) == _lib.MLA_OK                            # nothing to do
     # a sequence of two query tiles is refused whatever the GPU
     assert call(_lib._i32_host([0, 129]), kl) == _lib.MLA_ERR_UNSUPPORTED
+
+
+def _walk_fused_plan(H, bounds, items):
+    """Decode every cluster's range the way the fused kernel does; return
+    the coverage count per flattened position and the (slot, head) writes."""
+    tph = sum(t for _, t, _, _ in items)
+    N = H * tph
+    P = len(bounds) - 1
+    starts = [tb for _, _, tb, _ in items]
+
+    def pair_of(x):
+        lo, hi = 0, P - 1
+        while lo < hi:
+            mid = (lo + hi + 1) >> 1
+            if bounds[mid] <= x:
+                lo = mid
+            else:
+                hi = mid - 1
+        return lo
+    cover = np.zeros(N, dtype=np.int64)
+    writes = {}
+    for c in range(P):
+        f, f1 = bounds[c], bounds[c + 1]
+        while f < f1:
+            h, r = divmod(f, tph)
+            i = max(k for k in range(len(items)) if starts[k] <= r)
+            seq, tiles, tb, info = items[i]
+            kt0 = r - tb
+            kt1 = min(tiles, kt0 + (f1 - f))
+            assert 0 <= kt0 < kt1 <= tiles
+            cover[h * tph + tb + kt0:h * tph + tb + kt1] += 1
+            sb, maxp = (info & 0xffff) - 1, info >> 16
+            if sb >= 0:
+                slot = sb + c - pair_of(h * tph + tb)
+                assert sb <= slot < sb + maxp
+                writes[(slot, h)] = writes.get((slot, h), 0) + 1
+                if kt1 == tiles:       # the last piece clears the head's unused slots
+                    for s2 in range(slot + 1, sb + maxp):
+                        writes[(s2, h)] = writes.get((s2, h), 0) + 1
+            f += kt1 - kt0
+    return cover, writes
+
+
+def test_fused_plan_covers_every_tile_once():
+    """The fused kernel's work split (C++ host planner): every (head,
+    sequence, key tile) lands in exactly one cluster; each cut item's scratch
+    slots are written exactly once per head (a piece or a clear); the slot
+    and group limits hold; equal shares when nothing is snapped."""
+    rng = np.random.default_rng(7)
+    cases = [(128, [99], [32768], 76, 16), (16, [1, 128, 77, 5, 0, 100],
+                                            [5, 300, 129, 1000, 64, 0], 76, 16),
+             (4, [1] * 40, [300] * 40, 76, 16), (1, [1, 128], [1, 128], 76, 16),
+             (3, [57], [3000], 76, 16), (7, [57], [3000], 76, 0)]
+    for _ in range(60):
+        n = int(rng.integers(1, 30))
+        H = int(rng.choice([1, 2, 3, 16, 128]))
+        ql = [int(x) for x in rng.integers(0, 129, n)]
+        kl = [int(x) for x in rng.integers(0, 4000, n) * (rng.random(n) < 0.8)]
+        cases.append((H, ql, kl, int(rng.choice([1, 2, 7, 76, 300])),
+                      int(rng.choice([0, 4, 16]))))
+    for H, ql, kl, clusters, slots in cases:
+        q_loc = [0] + [int(x) for x in np.cumsum(ql)]
+        k_loc = [0] + [int(x) for x in np.cumsum(kl)]
+        bounds, items, groups = M.mla_fused_attn_plan(H, q_loc, k_loc, clusters, slots)
+        want = [i for i in range(len(ql)) if ql[i] > 0 and kl[i] > 0]
+        assert [it[0] for it in items] == want
+        if not want:
+            continue
+        tiles = [(kl[i] + 127) // 128 for i in want]
+        assert [it[1] for it in items] == tiles
+        assert [it[2] for it in items] == [int(x) for x in np.cumsum([0] + tiles[:-1])]
+        N = H * sum(tiles)
+        P = len(bounds) - 1
+        assert P == min(clusters, 128, N) and bounds[0] == 0 and bounds[-1] == N
+        assert all(a <= b for a, b in zip(bounds, bounds[1:]))
+        cover, writes = _walk_fused_plan(H, bounds, items)
+        assert (cover == 1).all()
+        cut = [it for it in items if it[3]]
+        assert len(cut) == groups <= 16
+        assert sum(it[3] >> 16 for it in cut) <= slots
+        for seq, _, _, info in cut:
+            sb, maxp = (info & 0xffff) - 1, info >> 16
+            for h in range(H):
+                for s in range(sb, sb + maxp):
+                    assert writes.get((s, h), 0) == 1, (H, ql, kl, seq, h, s)
+        if bounds == [c * N // P for c in range(P + 1)]:
+            assert max(b - a for a, b in zip(bounds, bounds[1:])) <= -(-N // P)
+    with pytest.raises(M.MlaError) as e:
+        M.mla_fused_attn_plan(16, [0, 129], [0, 300], 76, 16)
+    assert e.value.code == _lib.MLA_ERR_UNSUPPORTED
