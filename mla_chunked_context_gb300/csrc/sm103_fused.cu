@@ -17,9 +17,10 @@
 // operand of its up-projection (128 rows x 512 bf16 = 256 TMEM columns):
 //   rank 0 (keys):   K^T tile = W_k (TMEM) x latent^T (the latent tile is the
 //                    B operand, loaded by each CTA's own TMA producer),
-//                    converted to fp16 in shared memory; S = Q K^T (M=128 queries, N=128
-//                    keys, K=192) and the online softmax; P is written as fp16
-//                    straight into rank 1's shared memory.
+//                    converted to fp16 in shared memory; S = Q K^T (M=128
+//                    queries, N=128 keys, K=192) and the online softmax; P
+//                    (fp16) and the rescale factor go to rank 1's shared
+//                    memory with st.async.
 //   rank 1 (values): V^T tile = W_v (TMEM) x latent^T, converted the same way;
 //                    each tile's P V (M=128, N=128, K=128) into TMEM, summed
 //                    into O in registers with rank 0's rescale factor; the
@@ -39,7 +40,7 @@
 //      Each CTA loads the latent itself: a stage multicast to both would
 //      wait for both SMs' MMAs before its refill and hold the two SMs in
 //      lock step (measured 1.59 ms against 1.25 ms on a 99 x 32768 chunk);
-//      the second read comes from L2, which is 12% busy.
+//      the second read comes from L2 (27% busy with it).
 //   1  TMEM owner; issues each key tile's up-projection MMAs
 //   2  issues the tile's second MMA group (S on rank 0, P.V on rank 1);
 //      rank 1's P.V commit also arrives on rank 0's barrier (a P buffer
@@ -48,8 +49,8 @@
 //   8-15 rank 0: softmax (a thread per query row and half tile); rank 1: O
 //        in registers (a thread per query row and half of the columns),
 //        rescaled and summed over the tiles' P.V results, and the epilogue
-// TMEM: W half [0,256), buffers [256,384) [384,512).  Buffer b holds key
-// tile J's (J = b mod 2) up-projection accumulator until the convert warps
+// TMEM: W half [0,256), buffers [256,384) [384,512).  Buffer b = J mod 2
+// holds key tile J's up-projection accumulator until the convert warps
 // have loaded it, then the tile's second result (rank 0: S, rank 1: its P.V),
 // until the softmax / O warps have loaded that: the next tile's
 // up-projection never waits for the previous one's conversion.
