@@ -72,17 +72,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// Same load issued by one CTA, written at the same shared-memory offset of
-// every CTA in `mask` (a cluster of this GPU), each of whose mbarrier at
-// `bar`'s offset receives the bytes it got.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may sit in the peer CTA of a 2-SM pair (`bar` is a
 // shared::cluster address, e.g. from mapa_shared).

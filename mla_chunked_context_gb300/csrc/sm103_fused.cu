@@ -37,10 +37,10 @@
 //
 // Warps of each CTA (512 threads):
 //   0  TMA producer: the latent ring (both ranks), k_pe and Q (rank 0).
-//      Each CTA loads the latent itself: a stage multicast to both would
-//      wait for both SMs' MMAs before its refill and hold the two SMs in
-//      lock step (measured 1.59 ms against 1.25 ms on a 99 x 32768 chunk);
-//      the second read comes from L2 (27% busy with it).
+//      Each CTA loads the latent itself into its own ring; the second
+//      read of a tile comes from L2 (27% busy with it).  A ring shared by
+//      the two SMs would make each refill wait for both SMs' MMAs and hold
+//      them in lock step.
 //   1  TMEM owner; issues each key tile's up-projection MMAs
 //   2  issues the tile's second MMA group (S on rank 0, P.V on rank 1);
 //      rank 1's P.V commit also arrives on rank 0's barrier (a P buffer
