@@ -111,8 +111,10 @@ def attention_with_lse(q, k_nope, k_pe, v, scale: float, visible=None):
     n, Dn, Dv = k_nope.shape[0], k_nope.shape[2], v.shape[2]
     if n == 0:
         return np.zeros((m, H, Dv)), np.full((H, m), NEG_INF)
-    s = np.einsum("mhd,nhd->hmn", q[:, :, :Dn], k_nope)
-    s = s + np.einsum("mhp,np->hmn", q[:, :, Dn:], k_pe)
+    # (einsum with optimize=True contracts through BLAS: the same float64
+    # sums as numpy's own loops, in another order)
+    s = np.einsum("mhd,nhd->hmn", q[:, :, :Dn], k_nope, optimize=True)
+    s = s + np.einsum("mhp,np->hmn", q[:, :, Dn:], k_pe, optimize=True)
     s = s * scale
     if visible is not None:
         s = np.where(np.asarray(visible, dtype=bool)[None, :, :], s, NEG_INF)
@@ -123,7 +125,7 @@ def attention_with_lse(q, k_nope, k_pe, v, scale: float, visible=None):
     tot = e.sum(axis=2)
     lse = np.where(seen, safe_mx + np.log(np.where(seen, tot, 1.0)), NEG_INF)
     p = np.where(seen[:, :, None], e / np.where(seen, tot, 1.0)[:, :, None], 0.0)
-    o = np.einsum("hmn,nhd->mhd", p, v)
+    o = np.einsum("hmn,nhd->mhd", p, v, optimize=True)
     return o, lse
 
 
