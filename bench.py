@@ -14,11 +14,16 @@ Printed JSON line (rank 0):
   e2e        tokens/s with host buffers: pinned host->device copies of the
              step's inputs and a device->host read of the output inside the
              timed region
+  breakdown  every launch of the timed steps timed in place (the library's
+             per-launch CUDA events on the launching streams), summed per step
+             of the method; the spec bar = (up-projection + context
+             attention FLOPs) / (span of the gather .. context attention)
+  rooflines  per kernel: algorithmic work / its in-step CUDA-event time vs the
+             measured peak; roofline = the one with the largest share
+  configs    the other workloads (tiny, uniform, long) through the same call
   merge      merge_attn_states alone on 8192 tokens x 128 heads x 128 (bf16,
              15% empty prefix rows, prefix_num_tokens 6144): GB/s of the bytes
              that must move and the fraction of the measured HBM copy peak
-  roofline   the dominant kernel (the tcgen05 up-projection GEMM): algorithmic
-             FLOPs per launch / its CUDA-event duration vs. measured bf16 peak
   cpu_baseline  the float64 oracle on the host cores, on a bounded sample
              (every token, a few heads; throughput scaled to all heads)
 
@@ -124,7 +129,9 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workloads --
 def flops_of(w, plans):
-    """Algorithmic FLOPs of one prefill (each multiply-add = 2)."""
+    """Algorithmic FLOPs of one prefill (each multiply-add = 2): the
+    up-projection of every context row and new token, the context attention
+    over every (query, context row) pair and the causal new-token attention."""
     H, L, Dn, Dv, P = w.num_heads, w.kv_lora_rank, w.qk_nope_dim, w.v_dim, w.qk_rope_dim
     ctx_rows = sum(sum(p.seq_lens) for p in plans)
     T = w.num_tokens
@@ -133,7 +140,19 @@ def flops_of(w, plans):
     attn_suf = 2.0 * H * (Dn + P + Dv) * sum(q * (q + 1) / 2 for q in w.query_lens)
     return dict(up_proj_ctx=2.0 * L * H * (Dn + Dv) * ctx_rows,
                 up_proj_new=2.0 * L * H * (Dn + Dv) * T, attn_ctx=attn_ctx, attn_new=attn_suf,
-                total=up + attn_ctx + attn_suf)
+                total=up + attn_ctx + attn_suf, context_rows=ctx_rows)
+
+
+def config_of(w, plans, world):
+    """The workload description both arms print."""
+    return {"workload": f"{w.name}: {w.num_requests} requests, context rows "
+                        f"{sum(w.context_lens)} (max {max(w.context_lens)}), "
+                        f"{w.num_tokens} new tokens, {len(plans)} chunks",
+            "heads": w.num_heads, "kv_lora_rank": w.kv_lora_rank, "rope": w.qk_rope_dim,
+            "nope": w.qk_nope_dim, "v": w.v_dim, "block_size": w.block_size,
+            "row_budget": w.row_budget, "split_alignment": w.split_alignment,
+            "chunks": len(plans), "storage": w.dtype, "parallelism": f"replicas x{world}",
+            "l2": "flushed between timed steps (256 MB write outside the events)"}
 
 
 def merge_bytes(x, T, H, D, es=2):
@@ -167,6 +186,194 @@ def whole_job_rate(units_per_rank_step: float, world: int, steps: int, job_ms: f
     return world * steps * units_per_rank_step / (job_ms / 1e3)
 
 
+# ------------------------------------------------- in-step launch profile --
+ROLE_GATHER, ROLE_UP, ROLE_ATTN = "a4 gather", "a5 up-projection", "a6-a7 context attention"
+ROLE_UP_NEW, ROLE_ATTN_NEW = "a8 new-token up-projection", "a9-a10 new-token attention + merge"
+
+
+def split_steps(records, steps):
+    """The per-launch records of `steps` identical steps, one list per step
+    (every step enqueues the same launches in the same order)."""
+    n = len(records)
+    if steps < 1 or n % steps:
+        raise RuntimeError(f"{n} launch records do not split into {steps} steps")
+    k = n // steps
+    return [records[i * k:(i + 1) * k] for i in range(steps)]
+
+
+def breakdown_of(records, steps, w, plans, peaks):
+    """Per step of the method: launches and summed in-place CUDA-event time
+    per prefill step; per kernel: its rooflines; the spec bar:
+    (a5 + a6 FLOPs) / (span from the first gather's start to the end of the
+    last context-attention launch)."""
+    per_step = split_steps(records, steps)
+    fl = flops_of(w, plans)
+    roles, kernels = {}, {}
+    spans = []
+    for rs in per_step:
+        ctx = [r for r in rs if r[4] in (ROLE_GATHER, ROLE_UP, ROLE_ATTN)]
+        if ctx:
+            t0 = min(r[2] for r in ctx)
+            t1 = max(r[2] + r[3] for r in ctx if r[4] == ROLE_ATTN) if any(
+                r[4] == ROLE_ATTN for r in ctx) else max(r[2] + r[3] for r in ctx)
+            spans.append(t1 - t0)
+        for name, stream, start, ms, role in rs:
+            e = roles.setdefault(role or "(other)", {"launches": 0, "ms": 0.0, "kernels": set()})
+            e["launches"] += 1
+            e["ms"] += ms
+            e["kernels"].add(name)
+            k = kernels.setdefault(name, {"launches": 0, "ms": 0.0})
+            k["launches"] += 1
+            k["ms"] += ms
+    for e in roles.values():
+        e["launches"] /= steps
+        e["ms"] /= steps
+        e["kernels"] = sorted(e["kernels"])
+    for k in kernels.values():
+        k["launches"] /= steps
+        k["ms"] /= steps
+    span_ms = statistics.median(spans) if spans else None
+    es = 2 if w.dtype == "bf16" else 4
+    row_bytes = (w.kv_lora_rank + w.qk_rope_dim) * es
+
+    def rl(ms, work, launches, unit, peak, peak_src, bound):
+        if not ms or not launches:
+            return None
+        sc = 1e12 if unit == "TFLOP/s" else 1e9
+        ach = work / (ms / 1e3) / sc
+        return {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                "peak_source": peak_src, "launches_per_step": launches,
+                "ms_per_step": ms, "work_per_step": work}
+    g = roles.get(ROLE_UP, {"ms": 0, "launches": 0})
+    gn = roles.get(ROLE_UP_NEW, {"ms": 0, "launches": 0})
+    a = roles.get(ROLE_ATTN, {"ms": 0, "launches": 0})
+    an = roles.get(ROLE_ATTN_NEW, {"ms": 0, "launches": 0})
+    ga = roles.get(ROLE_GATHER, {"ms": 0, "launches": 0})
+    bf = peaks["bf16_tflops"]
+    src = peaks["source"]
+    rooflines = {
+        "up_proj": rl(g["ms"] + gn["ms"], fl["up_proj_ctx"] + fl["up_proj_new"],
+                      g["launches"] + gn["launches"], "TFLOP/s", bf, src + " bf16 burst",
+                      "tensor"),
+        "context_attention": rl(a["ms"], fl["attn_ctx"], a["launches"], "TFLOP/s", bf,
+                                src + " bf16 burst", "tensor"),
+        "new_token_attention_merge": rl(an["ms"], fl["attn_new"], an["launches"], "TFLOP/s", bf,
+                                        src + " bf16 burst", "tensor"),
+        "gather": rl(ga["ms"], 2.0 * fl["context_rows"] * row_bytes, ga["launches"], "GB/s",
+                     peaks["hbm_gbs"], src + " copy", "hbm"),
+    }
+    rooflines = {k: v for k, v in rooflines.items() if v is not None}
+    bar = None
+    if span_ms:
+        ach = (fl["up_proj_ctx"] + fl["attn_ctx"]) / (span_ms / 1e3) / 1e12
+        bar = {"what": "(a5 up-projection + a6 context attention FLOPs) / (a4..a7 span)",
+               "a4_a7_span_ms": span_ms, "tflops": ach, "frac_burst": ach / bf,
+               "frac_sustained": (ach / peaks["bf16_tflops_sustained"]
+                                  if peaks.get("bf16_tflops_sustained") else None)}
+    return {"roles": roles, "kernels": kernels, "north_star_bar": bar, "rooflines": rooflines}
+
+
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if the kernel's source files have not changed since it was
+    taken (else null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = (d.get(kernel) or {}).get(workload)
+    if not e or e.get("sources_sha1") != sources_hash(e.get("sources", [])):
+        return None
+    return e.get("bytes_per_launch")
+
+
+def sources_hash(files):
+    """sha1 over the named files under the package's csrc/, in order."""
+    h = hashlib.sha1()
+    c = os.path.join(ROOT, "mla_chunked_context_gb300", "csrc")
+    for f in files:
+        h.update(open(os.path.join(c, f), "rb").read())
+    return h.hexdigest()
+
+
+def timed_steps(M, step, steps, warmup, flush, stream, profile=True, world=1, sampler=None):
+    """W untimed steps, then K steps each bracketed by CUDA events on the
+    launching stream, an L2 flush (a 256 MB write) between them outside the
+    events; the library's per-launch profile covers the K timed steps.
+    Returns (per-step ms, launch records, launches counted)."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.mark("t0")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    launched0 = M.mla_kernel_launches()
+    if profile:
+        M.mla_profile_begin()
+    for i in range(steps):
+        flush.fill_(i & 0xff)                   # L2 flush outside the timed events
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    launched = M.mla_kernel_launches() - launched0  # this library's kernels only
+    torch.cuda.synchronize()
+    records = M.mla_profile_end() if profile else []
+    if sampler is not None:
+        sampler.mark("t1")
+    if world > 1:
+        torch.distributed.barrier()
+    return [a.elapsed_time(b) for a, b in evs], records, launched
+
+
+def prefill_runner(M, W, w, dev):
+    x = W.make_inputs(w)
+    g = {k: v.to(dev) for k, v in x.items()}
+    plans = M.mla_plan_context_chunks(w.context_lens, w.row_budget, w.max_context_chunk,
+                                      w.split_alignment)
+    pf = M.ChunkedPrefill(M.Dims.of(w), w.context_lens, w.query_lens, w.row_budget,
+                          w.max_context_chunk, w.split_alignment, device=dev)
+    out = torch.empty(w.num_tokens, w.num_heads, w.v_dim, dtype=w.torch_dtype, device=dev)
+    out_lse = torch.empty(w.num_heads, w.num_tokens, device=dev)
+
+    def step():
+        pf(g["q"], g["new_latent"], g["kv_cache"], g["block_table"], g["w_kv_b"], out, out_lse)
+    return x, g, plans, pf, out, step
+
+
+def bench_config(M, W, name, dev, peaks, flush, steps, warmup):
+    """One more workload through mla_chunked_prefill: step time, algorithmic
+    throughput and the in-step breakdown (same method as the main line)."""
+    w = W.workload(name)
+    x, g, plans, pf, out, step = prefill_runner(M, W, w, dev)
+    ms, records, launched = timed_steps(M, step, steps, warmup, flush,
+                                        torch.cuda.current_stream())
+    step_ms = statistics.median(ms)
+    fl = flops_of(w, plans)
+    br = breakdown_of(records, steps, w, plans, peaks)
+    tf = fl["total"] / (step_ms / 1e3) / 1e12
+    res = {"config": config_of(w, plans, 1), "steps": steps, "ms_per_step": step_ms,
+           "ms_per_step_all": ms, "tok_per_s": w.num_tokens / (step_ms / 1e3),
+           "tflops": tf, "flops_per_step": fl, "gpu_launches_per_step": launched / steps,
+           "frac_burst": tf / peaks["bf16_tflops"],
+           "frac_sustained": (tf / peaks["bf16_tflops_sustained"]
+                              if peaks.get("bf16_tflops_sustained") else None),
+           "north_star_bar": br["north_star_bar"], "rooflines": br["rooflines"],
+           "roles": br["roles"]}
+    if w.dtype != "bf16":
+        res["note"] = ("float32 storage: the CUDA-core kernels (the tensor-core kernels serve "
+                       "bf16); fractions are of the bf16 tensor peak for reference only")
+    del x, g, pf, out
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------ our arm -----
 def run_ours(args, rank, world, dev):
     import mla_chunked_context_gb300 as M
@@ -174,49 +381,18 @@ def run_ours(args, rank, world, dev):
 
     w = W.workload(args.workload)
     peaks = load_peaks()
-    x = W.make_inputs(w)
-    g = {k: v.to(dev) for k, v in x.items()}
-    plans = M.mla_plan_context_chunks(w.context_lens, w.row_budget, w.max_context_chunk,
-                                      w.split_alignment)
-    dims = M.Dims.of(w)
-    pf = M.ChunkedPrefill(dims, w.context_lens, w.query_lens, w.row_budget,
-                          w.max_context_chunk, w.split_alignment, device=dev)
+    x, g, plans, pf, out, step = prefill_runner(M, W, w, dev)
     T, H = w.num_tokens, w.num_heads
-    out = torch.empty(T, H, w.v_dim, dtype=w.torch_dtype, device=dev)
-    out_lse = torch.empty(H, T, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step():
-        pf(g["q"], g["new_latent"], g["kv_cache"], g["block_table"], g["w_kv_b"], out, out_lse)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
-    time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    sampler.mark("t0")
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    launched0 = M.mla_kernel_launches()
-    for i in range(args.steps):
-        flush.fill_(i & 0xff)                   # L2 flush outside the timed events
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
-    launched = M.mla_kernel_launches() - launched0  # this library's kernels only
-    torch.cuda.synchronize()
-    sampler.mark("t1")
-    if world > 1:
-        torch.distributed.barrier()
+    step_ms, records, launched = timed_steps(M, step, args.steps, args.warmup, flush, stream,
+                                             profile=True, world=world, sampler=sampler)
     clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
     max_ms = job_time_ms(sum(step_ms), world, dev)
     value = whole_job_rate(T, world, args.steps, max_ms)
+    # the same steps without the per-launch events, for the profile's cost
+    plain_ms, _, _ = timed_steps(M, step, args.steps, 1, flush, stream, profile=False)
 
     # ---- e2e: host buffers, copies inside the timed region.  Inputs are
     # double-buffered on the device: step i+1's host->device copy (on a copy
@@ -276,149 +452,59 @@ def run_ours(args, rank, world, dev):
 
     result = None
     if rank == 0:
-        kernels = time_kernels(M, W, w, g, plans, dims, dev, args, flush)
         fl = flops_of(w, plans)
-        merge = bench_merge(M, W, dev, peaks, flush)
-        comparator = bench_equal_window(M, w, g, dims, dev, flush, max_ms / args.steps)
-        up = kernels["up_proj_ctx"]
-        roofline = {
-            "kernel": "kv_up_proj (tcgen05 GEMM)" if M.mla_has_tcgen05() else "kv_up_proj (CUDA cores)",
-            "bound": "tensor", "unit": "TFLOP/s",
-            "achieved": fl["up_proj_ctx"] / up["launches"] / (up["ms"] / up["launches"] / 1e3) / 1e12,
-            "peak": peaks["bf16_tflops"], "peak_source": peaks["source"] + " bf16 burst",
-            "launches_per_step": up["launches"],
-            "traffic": committed_traffic("kv_up_proj"),
-        }
-        roofline["frac"] = roofline["achieved"] / roofline["peak"]
+        br = breakdown_of(records, args.steps, w, plans, peaks)
+        # the dominant kernel: the largest share of the step's launch time
+        dom = max(br["rooflines"].items(), key=lambda kv: kv[1]["ms_per_step"])
+        roofline = dict(dom[1])
+        roofline["kernel"] = dom[0]
+        roofline["traffic"] = committed_traffic(
+            {"up_proj": "kv_up_proj", "context_attention": "attn_ctx"}.get(dom[0], dom[0]),
+            w.name)
+        launches = roofline["launches_per_step"]
+        roofline["achieved_per_launch_basis"] = (
+            "algorithmic work per step / launches = per launch; / mean in-step launch time")
+        roofline["traffic_basis"] = "DRAM bytes per launch (ncu), null if not captured"
         step_ms_mean = max_ms / args.steps
-
+        merge = bench_merge(M, W, dev, peaks, flush)
+        comparator = bench_equal_window(M, w, g, M.Dims.of(w), dev, flush, step_ms_mean)
+        configs = {}
+        if not args.no_configs:
+            del host, host_out
+            for name in ("tiny", "uniform", "long"):
+                configs[name] = bench_config(M, W, name, dev, peaks, flush, args.config_steps,
+                                             3)
         result = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_mean,
+            "ms_per_step_without_launch_events": statistics.mean(plain_ms),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded host draws; random-init W_kv_b)",
-            "config": {"workload": f"{w.name}: {w.num_requests} requests, context rows "
-                                   f"{sum(w.context_lens)} (max {max(w.context_lens)}), "
-                                   f"{T} new tokens, {len(plans)} chunks",
-                       "heads": H, "kv_lora_rank": w.kv_lora_rank, "rope": w.qk_rope_dim,
-                       "nope": w.qk_nope_dim, "v": w.v_dim, "block_size": w.block_size,
-                       "row_budget": w.row_budget, "split_alignment": w.split_alignment,
-                       "chunks": len(plans), "parallelism": f"replicas x{world}",
-                       "l2": "flushed between timed steps (256 MB write outside the events); "
-                             "each step also streams >2 GB"},
+            "config": config_of(w, plans, world),
             "tflops": fl["total"] / (step_ms_mean / 1e3) / 1e12,
-            "tensor_frac_step": fl["total"] / (step_ms_mean / 1e3) / 1e12 / peaks["bf16_tflops_sustained"]
-            if peaks.get("bf16_tflops_sustained") else None,
+            "tensor_frac_step": fl["total"] / (step_ms_mean / 1e3) / 1e12 / peaks["bf16_tflops"],
+            "tensor_frac_step_sustained": (
+                fl["total"] / (step_ms_mean / 1e3) / 1e12 / peaks["bf16_tflops_sustained"]
+                if peaks.get("bf16_tflops_sustained") else None),
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launched,
             "roofline": roofline,
+            "rooflines": br["rooflines"],
+            "north_star_bar": br["north_star_bar"],
+            "breakdown": {"roles": br["roles"], "kernels": br["kernels"],
+                          "how": "CUDA events recorded by the library on the launching "
+                                 "stream around every launch of the timed steps "
+                                 "(mla_profile_begin/_end); side-stream launches overlap"},
             "merge": merge,
             "comparator": comparator,
-            "kernels": kernels,
+            "configs": configs,
             "flops_per_step": fl,
         }
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(w, x, heads=args.cpu_heads)
     return result
-
-
-def committed_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source files have not changed since it was taken (else null)."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
-        return None
-    d = json.load(open(p))
-    e = d.get(kernel)
-    if not e or e.get("sources_sha1") != sources_hash(e.get("sources", [])):
-        return None
-    return e.get("bytes_per_launch")
-
-
-def sources_hash(files):
-    """sha1 over the named files under the package's csrc/, in order."""
-    h = hashlib.sha1()
-    c = os.path.join(ROOT, "mla_chunked_context_gb300", "csrc")
-    for f in files:
-        h.update(open(os.path.join(c, f), "rb").read())
-    return h.hexdigest()
-
-
-def time_kernels(M, W, w, g, plans, dims, dev, args, flush):
-    """Replays one step through the per-step entry points with CUDA events
-    around each launch (same shapes, same stream), to split the step time."""
-    stream = torch.cuda.current_stream()
-    T, H = w.num_tokens, w.num_heads
-    qsl = [0]
-    for q in w.query_lens:
-        qsl.append(qsl[-1] + q)
-    max_rows = max([sum(p.seq_lens) for p in plans] + [1])
-    kv_dtype = M.mla_chunk_kv_dtype(dims)          # what mla_chunked_prefill uses
-    lat_ws = torch.empty(max_rows, w.latent_dim, dtype=w.torch_dtype, device=dev)
-    kv_ws = torch.empty(max_rows, H * (w.qk_nope_dim + w.v_dim), dtype=kv_dtype, device=dev)
-    kv_new = torch.empty(T, H * (w.qk_nope_dim + w.v_dim), dtype=kv_dtype, device=dev)
-    o_p = torch.zeros(T, H, w.v_dim, device=dev)
-    l_p = torch.zeros(H, T, device=dev)
-    o_s = torch.empty(T, H, w.v_dim, device=dev)
-    l_s = torch.empty(H, T, device=dev)
-    out = torch.empty(T, H, w.v_dim, dtype=w.torch_dtype, device=dev)
-    res = {k: {"ms": 0.0, "launches": 0} for k in
-           ("gather", "up_proj_ctx", "attn_ctx", "up_proj_new", "attn_new", "merge")}
-    meta = []
-    for p in plans:
-        n = p.request_end - p.request_start
-        cu = [0]
-        for l in p.seq_lens:
-            cu.append(cu[-1] + l)
-        meta.append(dict(
-            req=torch.arange(p.request_start, p.request_end, dtype=torch.int32, device=dev),
-            st=torch.tensor(p.starts, dtype=torch.int32, device=dev),
-            cu=torch.tensor(cu, dtype=torch.int32, device=dev), cu_h=cu,
-            ql=qsl[p.request_start:p.request_end + 1], rows=cu[-1],
-            ql_d=torch.tensor(qsl[p.request_start:p.request_end + 1], dtype=torch.int32,
-                              device=dev),
-            acc_d=torch.tensor([1 if s > 0 else 0 for s in p.starts], dtype=torch.int32,
-                               device=dev)))
-    qsl_d = torch.tensor(qsl, dtype=torch.int32, device=dev)
-
-    def timed(name, fn):
-        flush.fill_(1)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
-        b.synchronize()
-        res[name]["ms"] += a.elapsed_time(b)
-        res[name]["launches"] += 1
-
-    reps = 2
-    for _ in range(reps):
-        for m in meta:
-            timed("gather", lambda: M.mla_gather_context_rows(
-                dims, g["kv_cache"], g["block_table"], m["req"], m["st"], m["cu"], m["rows"],
-                lat_ws))
-            timed("up_proj_ctx", lambda: M.mla_kv_up_proj(dims, lat_ws, m["rows"], g["w_kv_b"],
-                                                          kv_ws))
-            timed("attn_ctx", lambda: M.mla_varlen_attn(dims, False, m["ql"], m["cu_h"], g["q"],
-                                                        kv_ws, lat_ws, o_p, l_p,
-                                                        q_loc_dev=m["ql_d"], k_loc_dev=m["cu"],
-                                                        accumulate_dev=m["acc_d"]))
-        timed("up_proj_new", lambda: M.mla_kv_up_proj(dims, g["new_latent"], T, g["w_kv_b"],
-                                                      kv_new))
-        timed("attn_new", lambda: M.mla_varlen_attn(dims, True, qsl, qsl, g["q"], kv_new,
-                                                    g["new_latent"], o_s, l_s,
-                                                    q_loc_dev=qsl_d, k_loc_dev=qsl_d))
-        pnt = 0
-        for r, c in enumerate(w.context_lens):
-            if c > 0:
-                pnt = qsl[r + 1]
-        timed("merge", lambda: M.merge_attn_states(out, None, o_p, l_p, o_s, l_s, pnt))
-    for k in res:
-        res[k]["ms"] /= reps
-        res[k]["launches"] //= reps
-    return res
 
 
 def bench_equal_window(M, w, g, dims, dev, flush, new_ms, steps=3):
@@ -527,8 +613,11 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     from mla_chunked_context_gb300 import workloads as W
+    from oracle import planner as OP
     w = W.workload(args.workload)
     x = W.make_inputs(w)
+    plans = OP.plan_mla_context_chunks(w.context_lens, w.row_budget, w.max_context_chunk,
+                                       w.split_alignment)
     cpu_baseline(W.scaled(w, context_lens=[64], query_lens=[4]), W.make_inputs(
         W.scaled(w, context_lens=[64], query_lens=[4])), heads=1)   # warm-up: imports, BLAS
     vals = []
@@ -546,7 +635,8 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "parallelism": "host oracle, rank 0 only"},
+            "config": config_of(w, plans, world),
+            "execution": "float64 oracle on the host cores, rank 0 only",
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -588,6 +678,10 @@ def run_kernel_case(args, dev):
         kd = torch.tensor(k_loc, dtype=torch.int32, device=dev)
         fn = lambda: M.mla_varlen_attn(dims, args.causal, q_loc, k_loc, q, kv, lat, o, lse,  # noqa
                                        q_loc_dev=qd, k_loc_dev=kd)
+        if args.profile_launches:
+            M.mla_profile_begin()
+            fn()
+            info["launches"] = M.mla_profile_end()
         pairs = n * (ql * (ql + 1) / 2 if args.causal else ql * kl)
         work, unit, peak = 2.0 * H * (192 + 128) * pairs, "TFLOP/s", peaks["bf16_tflops"]
         info = {"seqs": n, "q": ql, "k": kl, "causal": bool(args.causal)}
@@ -665,6 +759,11 @@ def main():
     ap.add_argument("--workload", default="hetero", choices=["hetero", "uniform", "long"])
     ap.add_argument("--cpu-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the tiny / uniform / long sub-records")
+    ap.add_argument("--config-steps", type=int, default=5)
+    ap.add_argument("--profile-launches", action="store_true",
+                    help="--kernel attn: list the launches of one call")
     ap.add_argument("--kernel", default=None,
                     choices=["up_proj", "attn", "fused", "merge", "gather"],
                     help="time one kernel alone on a small case instead of the full step")

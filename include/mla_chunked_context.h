@@ -20,9 +20,17 @@
  *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Arguments are
  *     validated on the host before anything is enqueued; on an error nothing
  *     has been enqueued.
- *   - The caller owns all memory.  The library allocates no device memory;
- *     calls that need scratch take a caller-provided device workspace whose
- *     size a *_workspace_bytes query returns.
+ *   - The caller owns all memory.  The library allocates no device memory,
+ *     with one exception: the fixed device array behind
+ *     mla_context_chunk_attn_noalloc.  Calls that need scratch take a
+ *     caller-provided device workspace whose size a *_workspace_bytes query
+ *     returns; workspaces must be 16-byte aligned.
+ *   - Kernels: bf16 storage with the DeepSeek-V3 head shape (L 512, P 64,
+ *     Dn 128, Dv 128) runs on the tcgen05 tensor-core kernels only.  Such a
+ *     call needs an sm_103a GPU and 16-byte aligned q, latent / new_latent,
+ *     kv_cache, w_kv_b and K/V pointers, else it returns MLA_ERR_UNSUPPORTED
+ *     before anything is enqueued; it never falls back to the CUDA-core
+ *     kernels.  Those serve float32 storage and all other head shapes.
  *   - "device" pointers are CUDA device pointers of the current device;
  *     work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
  *     stream) and nothing synchronises unless stated.  "host" pointers are
@@ -41,9 +49,17 @@
  *   - dtype (mla_dims_t.dtype) is the storage type of q, kv_cache,
  *     new_latent, w_kv_b and of the final output O.  Arithmetic is float32
  *     (tensor-core products of bf16 operands accumulate in float32).
- *   - dev_status (nullable, device int32): set to a nonzero MLA_STATUS_* bit
- *     when a kernel meets a block id outside [0, num_blocks); that row is
- *     then read as zeros.  The caller checks it when it chooses to.
+ *   - dev_status (nullable, device int32): kernels OR MLA_STATUS_* bits into
+ *     it; the caller clears it and checks it when it chooses to.
+ *       MLA_STATUS_BAD_BLOCK   a block id outside [0, num_blocks) was met;
+ *                              that row was read as zeros.
+ *       MLA_STATUS_FP16_RANGE  a value rounded to fp16 (q_nope on the
+ *                              tensor-core path, or an up-projected K/V
+ *                              element stored as fp16) had magnitude >= 65520
+ *                              and became +-inf: results that depend on it
+ *                              are not valid (bf16 keeps its range, fp16
+ *                              does not; the tensor-core path uses fp16 for
+ *                              its 3 extra mantissa bits).
  */
 #ifndef MLA_CHUNKED_CONTEXT_H
 #define MLA_CHUNKED_CONTEXT_H
@@ -75,7 +91,8 @@ enum {
  * mla_kv_up_proj). */
 enum { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1, MLA_DTYPE_F16 = 2 };
 
-enum { MLA_STATUS_BAD_BLOCK = 1 };
+/* Bits of the caller's dev_status word (see the conventions above). */
+enum { MLA_STATUS_BAD_BLOCK = 1, MLA_STATUS_FP16_RANGE = 2 };
 
 /* Bits of mla_device_error_flags(). */
 enum { MLA_DEVICE_ERR_WAIT_TIMEOUT = 1 };
@@ -147,7 +164,9 @@ int mla_plan_context_chunks(const int32_t *context_lens, int32_t num_requests,
  *                            out_dtype for out (bf16 output is rounded to
  *                            nearest even)
  *   prefix_lse, suffix_lse   device float32 [H, T];  out_lse nullable
- *   head_dim must be a multiple of 8.  out may alias either input O (each
+ *   head_dim must be a multiple of 8.  out, prefix_o and suffix_o must be
+ *   16-byte aligned and the LSE arrays 4-byte aligned (O moves as 16-byte
+ *   vectors), else MLA_ERR_INVALID.  out may alias either input O (each
  *   element is read before it is written, by the same thread); out_lse must
  *   not alias an input LSE (one LSE is read by all threads of its row).
  */
@@ -171,7 +190,8 @@ int merge_attn_states(void *out, float *out_lse, const void *prefix_o,
  *   cu_rows[i] + (j - seq_start[i]).
  *   seq_request, seq_start device [num_seqs]; cu_rows device [num_seqs+1];
  *   latent_ws device [total_rows, L+P] in dtype.  (L+P)*elem must be a
- *   multiple of 16 bytes.
+ *   multiple of 16 bytes and kv_cache, latent_ws 16-byte aligned (rows move
+ *   as 16-byte pieces), else MLA_ERR_UNSUPPORTED / MLA_ERR_INVALID.
  */
 int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache,
                             int32_t num_blocks, const int32_t *block_table,
@@ -187,14 +207,16 @@ int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache,
  *   F16; accumulation is float32, the result is rounded once to kv_dtype):
  *   columns [0, Dn) of head h are K_nope, [Dn, Dn+Dv) are V.  Head-major
  *   keeps every output tile of the GEMM and every key tile of the attention
- *   one contiguous block of HBM.  For bf16 inputs with L % 64 == 0,
- *   H*(Dn+Dv) % 256 == 0, (Dn+Dv) % 64 == 0 and a 16-bit kv_dtype this runs
- *   on the 2-SM tcgen05 GEMM.  The chunked path stores K/V as F16 on the
- *   tensor-core path: bf16 keeps 8 significant bits and its rounding of
- *   K_nope alone moves a one-key LSE by ~5e-4 (1 sigma), fp16 keeps 11. */
+ *   one contiguous block of HBM.  The tensor-core shape (see the
+ *   conventions) runs on the 2-SM tcgen05 GEMM, which writes F16 or BF16
+ *   (F32 output: MLA_ERR_UNSUPPORTED; latent_ld*2 a multiple of 16 bytes).
+ *   The chunked path stores K/V as F16 there: bf16 keeps 8 significant bits
+ *   and its rounding of K_nope alone moves a one-key LSE by ~5e-4 (1 sigma),
+ *   fp16 keeps 11.  An F16 result of magnitude >= 65520 sets
+ *   MLA_STATUS_FP16_RANGE in dev_status (nullable). */
 int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
                    int32_t rows, const void *w_kv_b, void *kv, int32_t kv_dtype,
-                   mla_stream_t stream);
+                   int32_t *dev_status, mla_stream_t stream);
 
 /* mla_varlen_attn: softmax attention per sequence, returning (O, LSE).
  *   Sequence i owns query tokens [q_loc[i], q_loc[i+1]) (rows of q, o, lse)
@@ -210,10 +232,11 @@ int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
  *   q_loc, k_loc device [num_seqs+1]; max_q / max_k: upper bounds of the
  *   per-sequence counts.  o device float32 [T, H, Dv]; lse float32 [H, T];
  *   num_tokens = T (the row count of q, o and lse).  kv is in kv_dtype
- *   (F32, BF16 or F16); q and latent in d->dtype.  The tcgen05 kernel runs
- *   for the DeepSeek-V3 head shape (L 512, P 64, Dn 128, Dv 128), bf16 q and
- *   latent and F16 kv; it converts q_nope to fp16 on chip (exact for bf16
- *   values of magnitude 2^-14 .. 65504).
+ *   (F32, BF16 or F16); q and latent in d->dtype.  The tensor-core shape
+ *   (see the conventions) runs on the tcgen05 kernels, which take F16 kv
+ *   only (other K/V types: MLA_ERR_UNSUPPORTED); they convert q_nope to
+ *   fp16 on chip (exact for bf16 values of magnitude 2^-14 .. 65504; beyond
+ *   65504 sets MLA_STATUS_FP16_RANGE in dev_status, nullable).
  *   A row that sees no key gets O = 0, LSE = -inf. */
 int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
                     const int32_t *q_loc, const int32_t *k_loc,
@@ -222,7 +245,7 @@ int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
                     int32_t kv_dtype, int32_t kv_rows, const void *latent,
                     int64_t latent_ld,
                     const int32_t *accumulate, float *o, float *lse,
-                    mla_stream_t stream);
+                    int32_t *dev_status, mla_stream_t stream);
 
 /* mla_fused_context_attn: the context attention of mla_varlen_attn
  *   (causal = 0, PR #50613 report, items 3-4) with the W_kv_b up-projection
@@ -243,9 +266,11 @@ int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_seqs,
  *   bytes (the queries head-major with q_nope in F16, and key-split scratch);
  *   owned by the caller, reusable once the stream has passed the call.
  *   Runs for the DeepSeek-V3 head shape (L 512, P 64, Dn 128, Dv 128) on a
- *   tcgen05 GPU; MLA_ERR_UNSUPPORTED otherwise or when a sequence has more
- *   than 128 queries.  Needs no K/V workspace; on GB300 it is slower than
- *   the two-step path (mla_chunked_prefill does not use it). */
+ *   tcgen05 GPU with q, latent, w_kv_b and workspace 16-byte aligned;
+ *   MLA_ERR_UNSUPPORTED otherwise or when a sequence has more than 128
+ *   queries.  dev_status (nullable) as in mla_varlen_attn / mla_kv_up_proj.
+ *   Needs no K/V workspace; on GB300 it is slower than the two-step path
+ *   (mla_chunked_prefill does not use it). */
 int mla_fused_attn_workspace_bytes(const mla_dims_t *d, int32_t num_tokens,
                                    size_t *bytes);
 int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
@@ -255,7 +280,8 @@ int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
                            int64_t latent_ld, int32_t latent_rows,
                            const void *w_kv_b, const int32_t *accumulate,
                            float *o, float *lse, void *workspace,
-                           size_t workspace_bytes, mla_stream_t stream);
+                           size_t workspace_bytes, int32_t *dev_status,
+                           mla_stream_t stream);
 
 /* mla_fused_attn_plan (host only, no GPU needed): how mla_fused_context_attn
  *   splits its work over `clusters` 2-SM clusters.  items[4*i .. 4*i+3] =
@@ -320,10 +346,15 @@ int mla_chunk_workspace_bytes(const mla_dims_t *d, int32_t max_rows,
  *   continued request (start > 0) is LSE-merged into what earlier chunks
  *   stored.
  *   chunk, starts, seq_lens: the planner's host outputs (starts/seq_lens
- *     indexed from chunk->entry_offset); query_start_loc host [R+1].
+ *     indexed from chunk->entry_offset); query_start_loc host [R+1].  The
+ *     library builds the chunk's device descriptor (request ids, starts,
+ *     workspace row offsets, query offsets) from them; whether a request
+ *     accumulates follows from its start, as on the page: start > 0 (the
+ *     request continues from an earlier chunk) merges, start 0 writes.
  *   o_partial device float32 [T, H, Dv]; lse_partial device float32 [H, T].
- *   workspace: device, at least mla_chunk_workspace_bytes bytes.
- *   The metadata is uploaded from host memory with cudaMemcpyAsync. */
+ *   workspace: device, 16-byte aligned, at least mla_chunk_workspace_bytes
+ *   bytes.  The metadata is uploaded from pageable host memory with
+ *   cudaMemcpyAsync, so the call is not for stream capture. */
 int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *chunk,
                            const int32_t *starts, const int32_t *seq_lens,
                            const int32_t *query_start_loc, int32_t num_tokens,
@@ -345,12 +376,15 @@ int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *chunk,
  *   (mla_chunk_workspace_bytes for its rows and requests) exceeds that size
  *   is rejected with MLA_ERR_TOO_SMALL before anything is enqueued.
  *   The first call on a device, with that device current, looks up the
- *   array's device address (cudaGetSymbolAddress); make that first call
- *   before any stream capture.  All calls share the one array and it keeps
- *   the last call's contents; nothing in it needs to start at zero (each call
- *   writes all it reads), but calls that overlap on the GPU race on it and
- *   must be serialised by the caller.  Other arguments and results as for
- *   mla_context_chunk_attn. */
+ *   array's device address (cudaGetSymbolAddress) and keeps it for the
+ *   process; after a cudaDeviceReset of that device the kept address is
+ *   stale, so do not call this entry point again on a device the process
+ *   has reset.  Like mla_context_chunk_attn it uploads its metadata from
+ *   pageable host memory, so it is not for stream capture.  All calls share
+ *   the one array and it keeps the last call's contents; nothing in it needs
+ *   to start at zero (each call writes all it reads), but calls that overlap
+ *   on the GPU race on it and must be serialised by the caller.  Other
+ *   arguments and results as for mla_context_chunk_attn. */
 #define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 int mla_context_chunk_attn_noalloc(const mla_dims_t *d, const mla_chunk_t *chunk,
                                    const int32_t *starts, const int32_t *seq_lens,
@@ -364,13 +398,20 @@ int mla_context_chunk_attn_noalloc(const mla_dims_t *d, const mla_chunk_t *chunk
                                    mla_stream_t stream);
 
 /* mla_prefill_workspace_bytes: device bytes mla_chunked_prefill needs for
- *   these lengths and planner settings (it runs the planner). */
+ *   these lengths and planner settings (it runs the planner).
+ * mla_prefill_pinned_bytes: host bytes of the metadata that
+ *   mla_chunked_prefill uploads for them (the size of its optional pinned
+ *   scratch). */
 int mla_prefill_workspace_bytes(const mla_dims_t *d,
                                 const int32_t *context_lens,
                                 const int32_t *query_lens,
                                 int32_t num_requests, int32_t row_budget,
                                 int32_t max_context_chunk,
                                 int32_t split_alignment, size_t *bytes);
+int mla_prefill_pinned_bytes(const mla_dims_t *d, const int32_t *context_lens,
+                             const int32_t *query_lens, int32_t num_requests,
+                             int32_t row_budget, int32_t max_context_chunk,
+                             int32_t split_alignment, size_t *bytes);
 
 /* mla_chunked_prefill  (the whole path: plan, init partial, per chunk
  *   gather + up-projection + attention + accumulate, new-token up-projection
@@ -379,8 +420,17 @@ int mla_prefill_workspace_bytes(const mla_dims_t *d,
  *   prefix_num_tokens = end of the last request with context (tokens of a
  *   context-free tail copy the suffix result).
  *   out device [T, H, Dv] in dtype; out_lse device float32 [H, T], nullable.
- *   workspace: device, >= mla_prefill_workspace_bytes.
- *   All metadata goes to the device in one cudaMemcpyAsync from host memory.
+ *   workspace: device, 16-byte aligned, >= mla_prefill_workspace_bytes.
+ *   Metadata (the plan's chunk descriptors, the empty-token slices and the
+ *   query offsets; the host lengths avoid any device-to-host read, PR #36540
+ *   report, comments) goes to the device in one cudaMemcpyAsync.
+ *   pinned_scratch (nullable): caller-owned page-locked host memory of at
+ *   least mla_prefill_pinned_bytes bytes (else MLA_ERR_TOO_SMALL); the
+ *   library writes the metadata there and copies it from there, so the copy
+ *   is a true asynchronous DMA.  Before rewriting pinned scratch a call waits
+ *   on the host until the previous call's copy out of pinned scratch on this
+ *   device has run, so one buffer can serve call after call; the library
+ *   never frees it.  NULL: the copy is made from pageable memory.
  *   On the tensor-core path the workspace keeps K/V in fp16 (see
  *   mla_kv_up_proj); on the CUDA-core path in float32.
  *   Streams: the chunks run as a two-buffer pipeline.  Gathers and
@@ -390,10 +440,10 @@ int mla_prefill_workspace_bytes(const mla_dims_t *d,
  *   after the work already on `stream` (an event recorded there), and
  *   `stream` waits for all of it before the call's last kernel, so to the
  *   caller the call behaves like work enqueued on `stream` alone.  (Not for
- *   stream capture: the metadata upload is a copy from pageable host
- *   memory.)  Calls from several host threads are serialised while they
- *   enqueue.  The workspace holds two chunk buffer sets and the
- *   key-split scratch of the context attention.
+ *   stream capture.)  Calls on one device from several host threads are
+ *   serialised while they enqueue (a lock per device); calls on different
+ *   devices are independent.  The workspace holds two chunk buffer sets and
+ *   the key-split scratch of the context attention.
  */
 int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
                         const int32_t *query_lens, int32_t num_requests,
@@ -403,8 +453,8 @@ int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
                         int32_t num_blocks, const int32_t *block_table,
                         int32_t block_table_stride, const void *w_kv_b,
                         void *workspace, size_t workspace_bytes, void *out,
-                        float *out_lse, int32_t *dev_status,
-                        mla_stream_t stream);
+                        float *out_lse, void *pinned_scratch, size_t pinned_bytes,
+                        int32_t *dev_status, mla_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * The old scheme, kept as a comparator (PR #50613 report, motivation: the
@@ -451,6 +501,31 @@ int mla_has_tcgen05(void);
  * to count the kernels that region launched.  Errors: MLA_ERR_INVALID for a
  * NULL count. */
 int mla_kernel_launches(uint64_t *count);
+
+/* Per-launch timing, for looking inside a call's pipeline in place.
+ * mla_profile_begin: from now on this host thread records a CUDA event on
+ *   the launching stream right before and right after every kernel the
+ *   library enqueues (for the calls this thread makes).
+ * mla_profile_end: stops, waits for those events, and returns one record per
+ *   launch in launch order: the kernel's name, the step of the method it
+ *   serves inside mla_chunked_prefill ("a4 gather", "a5 up-projection",
+ *   "a6-a7 context attention", ...; empty for the other calls), the stream
+ *   it ran on (numbered from 0 in order of first appearance), its start
+ *   relative to the first record's start and its duration, both in ms
+ *   (kernels that run side by side on different streams each show their
+ *   own span).
+ *   *count = number of launches; MLA_ERR_TOO_SMALL when it exceeds cap (the
+ *   first cap records are filled).  The events are freed either way.
+ *   Profiling adds two event records per launch: time a call with it off. */
+typedef struct {
+  char kernel[40];
+  char role[40];
+  int32_t stream;
+  float start_ms;
+  float ms;
+} mla_launch_record_t;
+int mla_profile_begin(void);
+int mla_profile_end(mla_launch_record_t *records, int32_t cap, int32_t *count);
 
 /* Failure-detection self test: launches one thread that waits on an
  * mbarrier nothing arrives on, with the same bounded wait the tensor-core

@@ -23,7 +23,7 @@ HEADER = os.path.join(HERE, "..", "include", "mla_chunked_context.h")
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_TOO_SMALL, MLA_ERR_PLANNER_STUCK, MLA_ERR_CUDA, \
     MLA_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 MLA_DTYPE_F32, MLA_DTYPE_BF16, MLA_DTYPE_F16 = 0, 1, 2
-MLA_STATUS_BAD_BLOCK = 1
+MLA_STATUS_BAD_BLOCK, MLA_STATUS_FP16_RANGE = 1, 2
 
 _ERRORS = {MLA_ERR_INVALID: "invalid argument", MLA_ERR_TOO_SMALL: "buffer too small",
            MLA_ERR_PLANNER_STUCK: "planner cannot progress (budget below one aligned split)",
@@ -37,7 +37,8 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_plan_equal_window_chunks", "mla_prefill_equal_window_workspace_bytes",
             "mla_chunked_prefill_equal_window", "mla_selftest_bounded_wait",
             "mla_kernel_launches", "mla_fused_attn_workspace_bytes",
-            "mla_fused_context_attn", "mla_fused_attn_plan")
+            "mla_fused_context_attn", "mla_fused_attn_plan", "mla_prefill_pinned_bytes",
+            "mla_profile_begin", "mla_profile_end")
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -59,6 +60,11 @@ class mla_chunk_t(C.Structure):
                 ("is_continuation", C.c_int32)]
 
 
+class mla_launch_record_t(C.Structure):
+    _fields_ = [("kernel", C.c_char * 40), ("role", C.c_char * 40), ("stream", C.c_int32),
+                ("start_ms", C.c_float), ("ms", C.c_float)]
+
+
 PADDED_ROWS_FN = C.CFUNCTYPE(C.c_int64, C.c_int64, C.c_void_p)
 
 _lib = None
@@ -78,22 +84,26 @@ def lib() -> C.CDLL:
                                         I32, P, P],
             "merge_attn_states": [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P],
             "mla_gather_context_rows": [P, P, I32, P, I32, I32, P, P, P, I32, P, P, P],
-            "mla_kv_up_proj": [P, P, I64, I32, P, P, I32, P],
-            "mla_varlen_attn": [P, I32, I32, P, P, P, P, I32, P, P, I32, I32, P, I64, P, P, P, P],
+            "mla_kv_up_proj": [P, P, I64, I32, P, P, I32, P, P],
+            "mla_varlen_attn": [P, I32, I32, P, P, P, P, I32, P, P, I32, I32, P, I64, P, P, P, P,
+                                P],
             "mla_fill_empty_rows": [P, P, I32, I32, I32, I32, P, P],
             "mla_mask_empty_context": [P, P, I32, I32, I32, I32, I32, P, P, P],
             "mla_chunk_workspace_bytes": [P, I32, I32, P],
             "mla_context_chunk_attn": [P, P, P, P, P, I32, P, P, I32, P, I32, P, P, SZ, P, P, P,
                                        P],
             "mla_prefill_workspace_bytes": [P, P, P, I32, I32, I32, I32, P],
+            "mla_prefill_pinned_bytes": [P, P, P, I32, I32, I32, I32, P],
             "mla_chunked_prefill": [P, P, P, I32, I32, I32, I32, P, P, P, I32, P, I32, P, P, SZ,
-                                    P, P, P, P],
+                                    P, P, P, SZ, P, P],
+            "mla_profile_begin": [],
+            "mla_profile_end": [P, I32, P],
             "mla_has_tcgen05": [],
             "mla_kernel_launches": [P],
             "mla_fused_attn_workspace_bytes": [P, I32, P],
             "mla_fused_attn_plan": [I32, I32, P, P, I32, I32, P, I32, P, I32, P, P, P],
             "mla_fused_context_attn": [P, I32, P, P, P, P, I32, P, P, I64, I32, P, P, P, P, P,
-                                       SZ, P],
+                                       SZ, P, P],
             "mla_device_error_flags": [P],
             "mla_chunk_kv_dtype": [P, P],
             "mla_context_chunk_attn_noalloc": [P, P, P, P, P, I32, P, P, I32, P, I32, P, P, P,
@@ -240,18 +250,19 @@ def mla_gather_context_rows(dims: Dims, kv_cache, block_table, seq_request, seq_
            "mla_gather_context_rows")
 
 
-def mla_kv_up_proj(dims: Dims, latent, rows: int, w_kv_b, kv, stream=None) -> None:
+def mla_kv_up_proj(dims: Dims, latent, rows: int, w_kv_b, kv, dev_status=None,
+                   stream=None) -> None:
     """kv's torch dtype (float32 / bfloat16 / float16) selects the output type."""
     d = dims.c()
     _check(lib().mla_kv_up_proj(C.byref(d), _ptr(latent), latent.stride(0), rows, _ptr(w_kv_b),
-                                _ptr(kv), dtype_code(kv.dtype), _stream(stream)),
-           "mla_kv_up_proj")
+                                _ptr(kv), dtype_code(kv.dtype), _ptr(dev_status),
+                                _stream(stream)), "mla_kv_up_proj")
 
 
 def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Sequence[int], q,
                     kv, latent, o, lse, accumulate: Optional[Sequence[int]] = None,
                     stream=None, q_loc_dev=None, k_loc_dev=None, accumulate_dev=None,
-                    kv_rows: Optional[int] = None) -> None:
+                    kv_rows: Optional[int] = None, dev_status=None) -> None:
     """q_loc / k_loc (and accumulate) are host sequences; they are copied to
     the device here unless device copies are passed as *_dev tensors.  kv is
     head-major [H, kv_rows, Dn+Dv]; kv_rows defaults to k_loc[-1]."""
@@ -270,7 +281,7 @@ def mla_varlen_attn(dims: Dims, causal: bool, q_loc: Sequence[int], k_loc: Seque
                                  _i32_host(q_loc), _i32_host(k_loc), q.shape[0], _ptr(q),
                                  _ptr(kv), dtype_code(kv.dtype), rows, _ptr(latent),
                                  latent.stride(0), _ptr(acc), _ptr(o), _ptr(lse),
-                                 _stream(stream)), "mla_varlen_attn")
+                                 _ptr(dev_status), _stream(stream)), "mla_varlen_attn")
 
 
 def mla_fused_attn_workspace_bytes(dims: Dims, num_tokens: int) -> int:
@@ -284,7 +295,7 @@ def mla_fused_attn_workspace_bytes(dims: Dims, num_tokens: int) -> int:
 def mla_fused_context_attn(dims: Dims, q_loc: Sequence[int], k_loc: Sequence[int], q, latent,
                            w_kv_b, o, lse, accumulate: Optional[Sequence[int]] = None,
                            workspace=None, stream=None, q_loc_dev=None, k_loc_dev=None,
-                           accumulate_dev=None) -> None:
+                           accumulate_dev=None, dev_status=None) -> None:
     """Context attention with the up-projection fused in: latent rows
     [k_loc[i], k_loc[i+1]) are sequence i's keys.  workspace: a uint8 device
     tensor of mla_fused_attn_workspace_bytes bytes (allocated here if None)."""
@@ -305,7 +316,7 @@ def mla_fused_context_attn(dims: Dims, q_loc: Sequence[int], k_loc: Sequence[int
                                         _i32_host(k_loc), q.shape[0], _ptr(q), _ptr(latent),
                                         latent.stride(0), latent.shape[0], _ptr(w_kv_b),
                                         _ptr(acc), _ptr(o), _ptr(lse), _ptr(workspace),
-                                        workspace.numel(), _stream(stream)),
+                                        workspace.numel(), _ptr(dev_status), _stream(stream)),
            "mla_fused_context_attn")
 
 
@@ -394,21 +405,53 @@ def mla_prefill_workspace_bytes(dims: Dims, context_lens, query_lens, row_budget
     return b.value
 
 
+def mla_prefill_pinned_bytes(dims: Dims, context_lens, query_lens, row_budget: int,
+                             max_context_chunk: int, split_alignment: int) -> int:
+    d = dims.c()
+    b = C.c_size_t(0)
+    _check(lib().mla_prefill_pinned_bytes(C.byref(d), _i32_host(context_lens),
+                                          _i32_host(query_lens), len(context_lens), row_budget,
+                                          max_context_chunk, split_alignment, C.byref(b)),
+           "mla_prefill_pinned_bytes")
+    return b.value
+
+
 def mla_chunked_prefill(dims: Dims, context_lens, query_lens, row_budget: int,
                         max_context_chunk: int, split_alignment: int, q, new_latent, kv_cache,
                         block_table, w_kv_b, workspace, out, out_lse=None, dev_status=None,
-                        stream=None) -> None:
+                        stream=None, pinned_scratch=None) -> None:
+    """pinned_scratch: optional page-locked uint8 host tensor of at least
+    mla_prefill_pinned_bytes bytes for the metadata upload."""
     d = dims.c()
+    pin = _ptr(pinned_scratch)
+    pin_bytes = 0 if pinned_scratch is None else pinned_scratch.numel() * \
+        pinned_scratch.element_size()
     _check(lib().mla_chunked_prefill(
         C.byref(d), _i32_host(context_lens), _i32_host(query_lens), len(context_lens),
         row_budget, max_context_chunk, split_alignment, _ptr(q), _ptr(new_latent),
         _ptr(kv_cache), kv_cache.shape[0], _ptr(block_table), block_table.shape[1],
         _ptr(w_kv_b), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
-        _ptr(out_lse), _ptr(dev_status), _stream(stream)), "mla_chunked_prefill")
+        _ptr(out_lse), pin, pin_bytes, _ptr(dev_status), _stream(stream)),
+        "mla_chunked_prefill")
 
 
 def mla_has_tcgen05() -> bool:
     return bool(lib().mla_has_tcgen05())
+
+
+def mla_profile_begin() -> None:
+    """Record CUDA events around every kernel this thread's calls enqueue."""
+    _check(lib().mla_profile_begin(), "mla_profile_begin")
+
+
+def mla_profile_end(cap: int = 8192) -> list:
+    """Stop profiling; (kernel, stream, start_ms, ms, role) per launch, in
+    launch order."""
+    recs = (mla_launch_record_t * cap)()
+    n = C.c_int32(0)
+    _check(lib().mla_profile_end(recs, cap, C.byref(n)), "mla_profile_end")
+    return [(recs[i].kernel.decode(), recs[i].stream, recs[i].start_ms, recs[i].ms,
+             recs[i].role.decode()) for i in range(n.value)]
 
 
 def mla_kernel_launches() -> int:

@@ -34,7 +34,8 @@ int launch_gather(const void *cache, int num_blocks, int block_size, int row_byt
                   cudaStream_t s);
 bool generic_dims_ok(const mla_dims_t &d);
 int launch_up_proj_simt(int dtype, int kv_dtype, const void *latent, int64_t lda, int rows,
-                        const void *w, void *kv, int N, int K, int hd, cudaStream_t s);
+                        const void *w, void *kv, int N, int K, int hd, int32_t *status,
+                        cudaStream_t s);
 int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                      const int32_t *k_loc, int num_q_rows, int T, int kv_rows, const void *q,
                      const void *kv, int kv_dtype, const void *latent, int64_t latent_ld,
@@ -42,7 +43,7 @@ int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_
 bool tc_gemm_ok(const mla_dims_t &d, int kv_dtype, int64_t lda, const void *latent,
                 const void *w, const void *kv);
 int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int64_t lda,
-                      int rows, const void *w, void *kv, cudaStream_t s);
+                      int rows, const void *w, void *kv, int32_t *status, cudaStream_t s);
 bool tc_attn_ok(const mla_dims_t &d, int kv_dtype, int64_t latent_ld);
 int gemm_take_errors();
 int attn_take_errors();
@@ -53,8 +54,8 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    const void *latent, int64_t latent_ld, const int32_t *accumulate,
                    float *o, float *lse, void *final_out, float *final_lse, int final_dtype,
                    int pnt, const SplitScratch *split, bool skip_keyless, bool q_prepared,
-                   cudaStream_t s);
-int launch_prepare_q(const void *q, void *qh, int T, int H, cudaStream_t s);
+                   int32_t *status, cudaStream_t s);
+int launch_prepare_q(const void *q, void *qh, int T, int H, int32_t *status, cudaStream_t s);
 bool fused_attn_ok(const mla_dims_t &d, int64_t latent_ld);
 bool fused_attn_fits(int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
                      int min_tiles);
@@ -62,7 +63,7 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
                       const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
                       int T, const void *q_prep, const void *latent, int64_t latent_ld, int rows,
                       const void *w, const int32_t *acc, float *o, float *lse,
-                      const SplitScratch *split, cudaStream_t s);
+                      const SplitScratch *split, int32_t *status, cudaStream_t s);
 int fused_take_errors();
 bool tc_available();
 
@@ -98,39 +99,55 @@ int check_dims(const mla_dims_t *d) {
 inline int kv_width(const mla_dims_t &d) { return d.num_heads * (d.qk_nope_dim + d.v_dim); }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
-// K/V workspace type of the chunked path: fp16 where the tensor-core
-// attention runs (bf16 inputs of the DeepSeek-V3 head shape), float32 for the
-// CUDA-core kernels.
+// The tensor-core kernels serve bf16 storage with the DeepSeek-V3 head shape
+// (latent 512, rope 64, nope 128, v 128); the CUDA-core kernels serve float32
+// storage and every other head shape.  A call of the tensor-core shape runs
+// on the tensor-core kernels or fails with MLA_ERR_UNSUPPORTED (no tcgen05
+// GPU, an operand not 16-byte aligned, a K/V type they do not take): it is
+// never handed to the CUDA-core kernels, which are 10-100x slower.
+bool tc_shape(const mla_dims_t &d) {
+  return d.dtype == MLA_DTYPE_BF16 && d.kv_lora_rank == 512 && d.qk_rope_dim == 64 &&
+         d.qk_nope_dim == 128 && d.v_dim == 128;
+}
+
+// K/V workspace type of the chunked path: fp16 for the tensor-core kernels,
+// float32 for the CUDA-core kernels.
 int path_kv_dtype(const mla_dims_t &d) {
-  const int LP = d.kv_lora_rank + d.qk_rope_dim;
-  return (tc_available() && tc_attn_ok(d, MLA_DTYPE_F16, LP)) ? MLA_DTYPE_F16 : MLA_DTYPE_F32;
+  return tc_shape(d) ? MLA_DTYPE_F16 : MLA_DTYPE_F32;
 }
 
 int up_proj(const mla_dims_t &d, const void *latent, int64_t lda, int rows, const void *w,
-            void *kv, int kv_dtype, cudaStream_t s) {
+            void *kv, int kv_dtype, int32_t *status, cudaStream_t s) {
   if (rows == 0) return MLA_OK;
-  if (tc_available() && tc_gemm_ok(d, kv_dtype, lda, latent, w, kv))
-    return launch_up_proj_tc(d, kv_dtype, latent, lda, rows, w, kv, s);
+  if (tc_shape(d)) {
+    if (!tc_gemm_ok(d, kv_dtype, lda, latent, w, kv) || !tc_available())
+      return MLA_ERR_UNSUPPORTED;
+    return launch_up_proj_tc(d, kv_dtype, latent, lda, rows, w, kv, status, s);
+  }
   return launch_up_proj_simt(d.dtype, kv_dtype, latent, lda, rows, w, kv, kv_width(d),
-                             d.kv_lora_rank, d.qk_nope_dim + d.v_dim, s);
+                             d.kv_lora_rank, d.qk_nope_dim + d.v_dim, status, s);
 }
 
 int attention(const mla_dims_t &d, int causal, int n, const int32_t *q_loc,
               const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
               int T, const void *q, const void *kv, int kv_dtype, int kv_rows,
               const void *latent, int64_t latent_ld, const int32_t *acc, float *o, float *lse,
-              cudaStream_t s, const SplitScratch *split = nullptr,
+              int32_t *status, cudaStream_t s, const SplitScratch *split = nullptr,
               bool skip_keyless = false, const void *q_prep = nullptr) {
   const int nq = q_loc_host[n] - q_loc_host[0];
   if (n == 0 || nq == 0) return MLA_OK;
   // q_prep: the same queries head-major with q_nope in fp16 (prepare_q), for
   // the tensor-core kernel
-  if (tc_available() && tc_attn_ok(d, kv_dtype, latent_ld) && aligned16(q) && aligned16(kv) &&
-      aligned16(latent))
+  if (tc_shape(d)) {
+    if (!tc_attn_ok(d, kv_dtype, latent_ld) || !aligned16(q) || !aligned16(kv) ||
+        !aligned16(latent) || (q_prep && !aligned16(q_prep)) || !tc_available())
+      return MLA_ERR_UNSUPPORTED;
     return launch_attn_tc(d, causal, n, q_loc, k_loc, q_loc_host, k_loc_host, T, kv_rows,
                           q_prep ? q_prep : q, kv, latent, latent_ld, acc, o, lse, nullptr,
-                          nullptr, 0, 0, split, skip_keyless, q_prep != nullptr, s);
+                          nullptr, 0, 0, split, skip_keyless, q_prep != nullptr, status, s);
+  }
   return launch_attn_simt(d, causal, n, q_loc, k_loc, nq, T, kv_rows, q, kv, kv_dtype, latent,
                           latent_ld, acc, o, lse, s);
 }
@@ -220,10 +237,10 @@ int run_chunk(const mla_dims_t &d, const ChunkMetaHost &m, const int32_t *meta_d
   int rc = launch_gather(kv_cache, num_blocks, d.block_size, LP * es, block_table, bt_stride,
                          n, req, st, cu, m.rows, b.latent_ws, status, s);
   if (rc) return rc;
-  rc = up_proj(d, b.latent_ws, LP, m.rows, w, b.kv_ws, b.kv_dtype, s);
+  rc = up_proj(d, b.latent_ws, LP, m.rows, w, b.kv_ws, b.kv_dtype, status, s);
   if (rc) return rc;
   return attention(d, 0, n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q, b.kv_ws, b.kv_dtype,
-                   m.rows, b.latent_ws, LP, acc, o, lse, s);
+                   m.rows, b.latent_ws, LP, acc, o, lse, status, s);
 }
 
 void carve_chunk_buffers(Carve &cv, const mla_dims_t &d, int64_t rows, ChunkBuffers &b) {
@@ -259,6 +276,11 @@ extern "C" int merge_attn_states(void *out, float *out_lse, const void *prefix_o
   if (num_tokens == 0) return MLA_OK;
   if (!out || !suffix_o || !suffix_lse) return MLA_ERR_INVALID;
   if (prefix_num_tokens > 0 && (!prefix_o || !prefix_lse)) return MLA_ERR_INVALID;
+  // the kernel moves O as 16-byte vectors and LSEs as 4-byte words
+  if (!aligned16(out) || !aligned16(suffix_o) || !aligned4(suffix_lse) ||
+      (out_lse && !aligned4(out_lse)) ||
+      (prefix_num_tokens > 0 && (!aligned16(prefix_o) || !aligned4(prefix_lse))))
+    return MLA_ERR_INVALID;
   return launch_merge(out, out_lse, prefix_o, prefix_lse, suffix_o, suffix_lse, num_tokens,
                       num_heads, head_dim, prefix_num_tokens < 0 ? 0 : prefix_num_tokens,
                       in_dtype, out_dtype, static_cast<cudaStream_t>(stream));
@@ -279,6 +301,7 @@ extern "C" int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache
   if (!kv_cache || !block_table || !seq_request || !seq_start || !cu_rows || !latent_ws ||
       num_seqs == 0)
     return MLA_ERR_INVALID;
+  if (!aligned16(kv_cache) || !aligned16(latent_ws)) return MLA_ERR_INVALID;  // 16-byte copies
   return launch_gather(kv_cache, num_blocks, d->block_size,
                        (d->kv_lora_rank + d->qk_rope_dim) * elem_bytes(d->dtype), block_table,
                        block_table_stride, num_seqs, seq_request, seq_start, cu_rows,
@@ -287,14 +310,14 @@ extern "C" int mla_gather_context_rows(const mla_dims_t *d, const void *kv_cache
 
 extern "C" int mla_kv_up_proj(const mla_dims_t *d, const void *latent, int64_t latent_ld,
                               int32_t rows, const void *w_kv_b, void *kv, int32_t kv_dtype,
-                              mla_stream_t stream) {
+                              int32_t *dev_status, mla_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (rows < 0 || latent_ld < d->kv_lora_rank || !valid_kv_dtype(kv_dtype))
     return MLA_ERR_INVALID;
   if (rows == 0) return MLA_OK;
   if (!latent || !w_kv_b || !kv) return MLA_ERR_INVALID;
-  return up_proj(*d, latent, latent_ld, rows, w_kv_b, kv, kv_dtype,
+  return up_proj(*d, latent, latent_ld, rows, w_kv_b, kv, kv_dtype, dev_status,
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -304,7 +327,7 @@ extern "C" int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_
                                int32_t num_tokens, const void *q, const void *kv,
                                int32_t kv_dtype, int32_t kv_rows, const void *latent,
                                int64_t latent_ld, const int32_t *accumulate, float *o,
-                               float *lse, mla_stream_t stream) {
+                               float *lse, int32_t *dev_status, mla_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (num_seqs < 0 || num_tokens < 0 || !valid_kv_dtype(kv_dtype)) return MLA_ERR_INVALID;
@@ -321,7 +344,7 @@ extern "C" int mla_varlen_attn(const mla_dims_t *d, int32_t causal, int32_t num_
   if (k_loc_host[0] < 0 || kv_rows < k_loc_host[num_seqs]) return MLA_ERR_INVALID;
   return attention(*d, causal ? 1 : 0, num_seqs, q_loc, k_loc, q_loc_host, k_loc_host,
                    num_tokens, q, kv, kv_dtype, kv_rows, latent, latent_ld, accumulate, o, lse,
-                   static_cast<cudaStream_t>(stream));
+                   dev_status, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int mla_fill_empty_rows(float *o, float *lse, int32_t num_tokens, int32_t num_heads,
@@ -383,6 +406,7 @@ extern "C" int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *ch
   if (!chunk || !starts || !seq_lens || !query_start_loc || !q || !kv_cache || !block_table ||
       !w_kv_b || !workspace || !o_partial || !lse_partial)
     return MLA_ERR_INVALID;
+  if (!aligned16(workspace) || !aligned16(kv_cache)) return MLA_ERR_INVALID;
   const int n = chunk->request_end - chunk->request_start;
   if (n < 1 || chunk->request_start < 0 || chunk->entry_offset < 0 || block_table_stride < 1)
     return MLA_ERR_INVALID;
@@ -412,21 +436,31 @@ extern "C" int mla_context_chunk_attn(const mla_dims_t *d, const mla_chunk_t *ch
 namespace {
 
 // Side streams and events of the chunk pipeline, one set per device, made on
-// first use and kept for the life of the process.  A prefill enqueues its
-// whole pipeline under g_pipeline_mu, so concurrent callers never interleave
-// their records and waits on these streams.
+// first use and kept for the life of the process, with the device's lock: a
+// prefill enqueues its whole pipeline (and its metadata upload) holding the
+// lock of its device, so concurrent callers never interleave their records
+// and waits on these streams.  Calls on different devices do not wait for
+// one another.
 struct Pipeline {
+  std::mutex mu;
   cudaStream_t gather = nullptr, gemm = nullptr;
   std::vector<cudaEvent_t> ev;
+  // the last metadata copy out of a caller's pinned scratch: the next call
+  // waits for it on the host before rewriting pinned memory
+  cudaEvent_t upload = nullptr;
+  bool upload_pending = false;
 };
-std::mutex g_pipeline_mu;
+constexpr int kMaxDevices = 64;
+Pipeline g_pipelines[kMaxDevices];
 
-int pipeline_for_current_device(size_t events, Pipeline **out) {
-  static std::vector<Pipeline> per_device;
+// Locks the current device's pipeline and makes its streams and at least
+// `events` events.
+int lock_pipeline(size_t events, std::unique_lock<std::mutex> &lock, Pipeline **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-  if (per_device.size() <= size_t(dev)) per_device.resize(dev + 1);
-  Pipeline &pl = per_device[dev];
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  Pipeline &pl = g_pipelines[dev];
+  lock = std::unique_lock<std::mutex>(pl.mu);
   if (!pl.gemm) {
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
@@ -434,6 +468,8 @@ int pipeline_for_current_device(size_t events, Pipeline **out) {
         cudaStreamCreateWithPriority(&pl.gemm, cudaStreamNonBlocking, greatest) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
+  if (!pl.upload && cudaEventCreateWithFlags(&pl.upload, cudaEventDisableTiming) != cudaSuccess)
+    return MLA_ERR_CUDA;
   while (pl.ev.size() < events) {
     cudaEvent_t e;
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return MLA_ERR_CUDA;
@@ -446,32 +482,50 @@ int pipeline_for_current_device(size_t events, Pipeline **out) {
 bool record(cudaEvent_t e, cudaStream_t s) { return cudaEventRecord(e, s) == cudaSuccess; }
 bool wait_on(cudaStream_t s, cudaEvent_t e) { return cudaStreamWaitEvent(s, e, 0) == cudaSuccess; }
 
-// The two-buffer pipeline of the chunked paths.  First pre(s) on the
-// caller's stream `s` (work only the consumers need, beside the first gather
-// and up-projection); then for units c = 0..n-1: gather(c, stream) on the
-// gather side stream once consume(c-2) has released buffer set c % 2,
-// up(c, stream) on the GEMM side stream after it, and consume(c, stream) on
-// `s` after that; then tail(stream) on the GEMM side stream (the new tokens'
-// up-projection, beside the last consume).  Both side streams start after the work already on `s` and are
-// joined back into `s` before returning, also after an error (the caller may
-// free the workspace once `s` has passed this point).  The side streams run
-// at the highest priority, so a GEMM takes SMs as soon as attention CTAs
-// retire.  Holds g_pipeline_mu while it enqueues.
+// One metadata upload: from the caller's pinned scratch when given (the
+// ints are written there first, after the previous copy out of pinned
+// scratch on this device has run), else from the pageable vector.  Called
+// with the device's pipeline locked.
+int upload_meta(Pipeline &pl, void *dst, const std::vector<int32_t> &src, void *pinned,
+                size_t pinned_bytes, cudaStream_t s) {
+  if (src.empty()) return MLA_OK;
+  const size_t bytes = src.size() * sizeof(int32_t);
+  if (!pinned) return upload(dst, src, s);
+  if (pinned_bytes < bytes) return MLA_ERR_TOO_SMALL;
+  if (pl.upload_pending && cudaEventSynchronize(pl.upload) != cudaSuccess) return MLA_ERR_CUDA;
+  pl.upload_pending = false;
+  std::memcpy(pinned, src.data(), bytes);
+  if (cudaMemcpyAsync(dst, pinned, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      !record(pl.upload, s))
+    return MLA_ERR_CUDA;
+  pl.upload_pending = true;
+  return MLA_OK;
+}
+
+// The two-buffer pipeline of the chunked paths, enqueued with the device's
+// pipeline `pl` locked.  First pre(s) on the caller's stream `s` (work only
+// the consumers need, beside the first gather and up-projection); then for
+// units c = 0..n-1: gather(c, stream) on the gather side stream once
+// consume(c-2) has released buffer set c % 2, up(c, stream) on the GEMM side
+// stream after it, and consume(c, stream) on `s` after that; then
+// tail(stream) on the GEMM side stream (the new tokens' up-projection,
+// beside the last consume).  Both side streams start after the work already
+// on `s` and are joined back into `s` before returning, also after an error
+// (the caller may free the workspace once `s` has passed this point).  The
+// side streams run at the highest priority, so a GEMM takes SMs as soon as
+// attention CTAs retire.
 template <class Pre, class Gather, class Up, class Consume, class Tail>
-int run_pipeline(cudaStream_t s, size_t n, Pre pre, Gather gather, Up up, Consume consume,
-                 Tail tail) {
-  std::lock_guard<std::mutex> lock(g_pipeline_mu);
-  Pipeline *pl = nullptr;
-  int rc = pipeline_for_current_device(3 * n + 3, &pl);
-  if (rc) return rc;
-  cudaEvent_t *ev = pl->ev.data();
-  const cudaStream_t sg = pl->gather, sm = pl->gemm;
+int run_pipeline(Pipeline &pl, cudaStream_t s, size_t n, Pre pre, Gather gather, Up up,
+                 Consume consume, Tail tail) {
+  if (pl.ev.size() < 3 * n + 3) return MLA_ERR_INVALID;
+  cudaEvent_t *ev = pl.ev.data();
+  const cudaStream_t sg = pl.gather, sm = pl.gemm;
   auto ev_lat = [&](size_t c) { return ev[1 + 3 * c]; };
   auto ev_kv = [&](size_t c) { return ev[2 + 3 * c]; };
   auto ev_used = [&](size_t c) { return ev[3 + 3 * c]; };
   cudaEvent_t ev_tail = ev[1 + 3 * n], ev_join = ev[2 + 3 * n];
   if (!record(ev[0], s) || !wait_on(sg, ev[0]) || !wait_on(sm, ev[0])) return MLA_ERR_CUDA;
-  rc = pre(s);
+  int rc = pre(s);
   for (size_t c = 0; c < n && rc == MLA_OK; ++c) {
     if (c >= 2 && !wait_on(sg, ev_used(c - 2))) rc = MLA_ERR_CUDA;
     if (!rc) rc = gather(c, sg);
@@ -601,6 +655,22 @@ extern "C" int mla_prefill_workspace_bytes(const mla_dims_t *d, const int32_t *c
   return MLA_OK;
 }
 
+extern "C" int mla_prefill_pinned_bytes(const mla_dims_t *d, const int32_t *context_lens,
+                                        const int32_t *query_lens, int32_t num_requests,
+                                        int32_t row_budget, int32_t max_context_chunk,
+                                        int32_t split_alignment, size_t *bytes) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!bytes || num_requests < 0 || (num_requests > 0 && (!context_lens || !query_lens)))
+    return MLA_ERR_INVALID;
+  PrefillLayout p;
+  rc = build_prefill(*d, context_lens, query_lens, num_requests, row_budget, max_context_chunk,
+                     split_alignment, p);
+  if (rc) return rc;
+  *bytes = p.meta_total * sizeof(int32_t);
+  return MLA_OK;
+}
+
 extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_lens,
                                    const int32_t *query_lens, int32_t num_requests,
                                    int32_t row_budget, int32_t max_context_chunk,
@@ -609,7 +679,8 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                                    int32_t num_blocks, const int32_t *block_table,
                                    int32_t block_table_stride, const void *w_kv_b,
                                    void *workspace, size_t workspace_bytes, void *out,
-                                   float *out_lse, int32_t *dev_status, mla_stream_t stream) {
+                                   float *out_lse, void *pinned_scratch, size_t pinned_bytes,
+                                   int32_t *dev_status, mla_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (num_requests < 0 || (num_requests > 0 && (!context_lens || !query_lens)))
@@ -625,9 +696,17 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   for (int r = 0; r < num_requests; ++r)
     if (int64_t(context_lens[r]) > int64_t(block_table_stride) * d->block_size)
       return MLA_ERR_INVALID;
+  // buffers carved from the workspace keep its alignment (offsets are
+  // multiples of 256); the gather moves 16-byte pieces of the cache
+  if (!aligned16(workspace) || (kv_cache && !aligned16(kv_cache))) return MLA_ERR_INVALID;
+  if (pinned_scratch && pinned_bytes < p.meta_total * sizeof(int32_t)) return MLA_ERR_TOO_SMALL;
   PrefillBuffers b;
   const size_t need = carve_prefill(nullptr, *d, p, b);
   if (workspace_bytes < need) return MLA_ERR_TOO_SMALL;
+  // the tensor-core shape runs on the tensor-core kernels only (see tc_shape)
+  const bool tc = tc_shape(*d);
+  if (tc && (!aligned16(q) || !aligned16(new_latent) || !aligned16(w_kv_b) || !tc_available()))
+    return MLA_ERR_UNSUPPORTED;
   carve_prefill(workspace, *d, p, b);
 
   std::vector<int32_t> meta(p.meta_total, 0);
@@ -640,7 +719,11 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   }
   std::memcpy(meta.data() + p.suffix_off, p.qsl.data(), p.qsl.size() * sizeof(int32_t));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = upload(b.meta, meta, s);
+  std::unique_lock<std::mutex> lock;
+  Pipeline *pl = nullptr;
+  rc = lock_pipeline(3 * p.metas.size() + 3, lock, &pl);
+  if (rc) return rc;
+  rc = upload_meta(*pl, b.meta, meta, pinned_scratch, pinned_bytes, s);
   if (rc) return rc;
 
   const int H = d->num_heads, Dv = d->v_dim, T = p.T;
@@ -650,9 +733,7 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   // the tensor-core attention reads the queries head-major with q_nope
   // already fp16: one pass (in the pipeline's pre step) instead of a strided
   // load and an fp16 conversion in every attention CTA
-  const bool tc_attn = tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q) &&
-                       aligned16(new_latent);
-  const void *q_prep = tc_attn ? b.q_prep : nullptr;
+  const void *q_prep = tc ? b.q_prep : nullptr;
 
   // The chunk pipeline (run_pipeline) over execution groups: consecutive
   // chunks with no continuation between them and rows within the budget
@@ -674,16 +755,22 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
     acc = ql + n + 1;
   };
   rc = run_pipeline(
-      s, p.metas.size(),
+      *pl, s, p.metas.size(),
       // the partial's context-free rows and the prepared queries, beside the
       // first gather and up-projection
       [&](cudaStream_t st_) {
-        int r = launch_fill_empty_rows(b.o_part, b.lse_part, T, H, Dv, int(p.empty.size()),
-                                       b.meta + p.slices_off, st_);
-        if (!r && q_prep) r = launch_prepare_q(q, b.q_prep, T, H, st_);
+        int r;
+        {
+          ProfRole role("a3 init partial");
+          r = launch_fill_empty_rows(b.o_part, b.lse_part, T, H, Dv, int(p.empty.size()),
+                                     b.meta + p.slices_off, st_);
+        }
+        ProfRole role("query preparation");
+        if (!r && q_prep) r = launch_prepare_q(q, b.q_prep, T, H, dev_status, st_);
         return r;
       },
       [&](size_t c, cudaStream_t st_) {
+        ProfRole role("a4 gather");
         const int32_t *req, *st, *cu, *ql, *acc;
         meta_of(c, req, st, cu, ql, acc);
         return launch_gather(kv_cache, num_blocks, d->block_size, LP * es, block_table,
@@ -691,33 +778,37 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                              b.chunk[c & 1].latent_ws, dev_status, st_);
       },
       [&](size_t c, cudaStream_t st_) {
+        ProfRole role("a5 up-projection");
         return up_proj(*d, b.chunk[c & 1].latent_ws, LP, p.metas[c].rows, w_kv_b,
-                       b.chunk[c & 1].kv_ws, kv_dtype, st_);
+                       b.chunk[c & 1].kv_ws, kv_dtype, dev_status, st_);
       },
       [&](size_t c, cudaStream_t st_) {
+        ProfRole role("a6-a7 context attention");
         const ChunkMetaHost &m = p.metas[c];
         const int32_t *req, *st, *cu, *ql, *acc;
         meta_of(c, req, st, cu, ql, acc);
         return attention(*d, 0, m.n, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
                          b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
-                         acc, b.o_part, b.lse_part, st_, &b.split, true, q_prep);
+                         acc, b.o_part, b.lse_part, dev_status, st_, &b.split, true, q_prep);
       },
       // new-token up-projection, beside the last group's attention
       [&](cudaStream_t st_) {
-        return up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, st_);
+        ProfRole role("a8 new-token up-projection");
+        return up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, dev_status, st_);
       });
   if (rc) return rc;
 
+  ProfRole role("a9-a10 new-token attention + merge");
   const int32_t *sq = b.meta + p.suffix_off;
-  if (tc_attn && aligned16(b.kv_suffix)) {
+  if (tc) {
     // new-token attention with the final merge in its epilogue (row f3): the
     // context partial is read where needed, the output written once
     return launch_attn_tc(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, T, q_prep,
                           b.kv_suffix, new_latent, LP, nullptr, b.o_part, b.lse_part, out,
-                          out_lse, d->dtype, p.pnt, nullptr, false, true, s);
+                          out_lse, d->dtype, p.pnt, nullptr, false, true, dev_status, s);
   }
   rc = attention(*d, 1, num_requests, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s);
+                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, dev_status, s);
   if (rc) return rc;
   return launch_merge(out, out_lse, b.o_part, b.lse_part, b.o_suf, b.lse_suf, T, H, Dv, p.pnt,
                       MLA_DTYPE_F32, d->dtype, s);
@@ -758,7 +849,7 @@ extern "C" int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
                                       int64_t latent_ld, int32_t latent_rows,
                                       const void *w_kv_b, const int32_t *accumulate, float *o,
                                       float *lse, void *workspace, size_t workspace_bytes,
-                                      mla_stream_t stream) {
+                                      int32_t *dev_status, mla_stream_t stream) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (num_seqs < 0 || num_tokens < 0 || latent_rows < 0) return MLA_ERR_INVALID;
@@ -772,7 +863,8 @@ extern "C" int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
       return MLA_ERR_INVALID;
   if (q_loc_host[0] < 0 || q_loc_host[num_seqs] > num_tokens) return MLA_ERR_INVALID;
   if (k_loc_host[0] < 0 || latent_rows < k_loc_host[num_seqs]) return MLA_ERR_INVALID;
-  if (!tc_available() || !fused_attn_ok(*d, latent_ld) ||
+  if (!aligned16(q) || !aligned16(latent) || !aligned16(w_kv_b) || !aligned16(workspace) ||
+      !tc_available() || !fused_attn_ok(*d, latent_ld) ||
       !fused_attn_fits(num_seqs, q_loc_host, k_loc_host, 1))
     return MLA_ERR_UNSUPPORTED;
   PrefillBuffers b{};
@@ -780,11 +872,11 @@ extern "C" int mla_fused_context_attn(const mla_dims_t *d, int32_t num_seqs,
     return MLA_ERR_TOO_SMALL;
   fused_workspace(*d, num_tokens, workspace, &b);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = launch_prepare_q(q, b.q_prep, num_tokens, d->num_heads, s);
+  rc = launch_prepare_q(q, b.q_prep, num_tokens, d->num_heads, dev_status, s);
   if (rc) return rc;
   return launch_attn_fused(*d, num_seqs, q_loc, k_loc, q_loc_host, k_loc_host, num_tokens,
                            b.q_prep, latent, latent_ld, latent_rows, w_kv_b, accumulate, o, lse,
-                           &b.split, s);
+                           &b.split, dev_status, s);
 }
 
 extern "C" int mla_has_tcgen05(void) { return tc_available() ? 1 : 0; }
@@ -793,6 +885,57 @@ extern "C" int mla_kernel_launches(uint64_t *count) {
   if (!count) return MLA_ERR_INVALID;
   *count = g_kernel_launches.load(std::memory_order_relaxed);
   return MLA_OK;
+}
+
+namespace {
+// the records' events go back to the thread's pool
+void drop_profile() {
+  for (const ProfRecord &r : g_prof.recs) {
+    g_prof.pool.push_back(r.start);
+    g_prof.pool.push_back(r.stop);
+  }
+  g_prof.recs.clear();
+  if (g_prof.pending) g_prof.pool.push_back(g_prof.pending);
+  g_prof.pending = nullptr;
+}
+}  // namespace
+
+extern "C" int mla_profile_begin(void) {
+  drop_profile();
+  g_prof.on = true;
+  return MLA_OK;
+}
+
+extern "C" int mla_profile_end(mla_launch_record_t *records, int32_t cap, int32_t *count) {
+  if (!count || cap < 0 || (cap > 0 && !records)) return MLA_ERR_INVALID;
+  g_prof.on = false;
+  const int n = int(g_prof.recs.size());
+  *count = n;
+  int rc = MLA_OK;
+  std::vector<cudaStream_t> streams;  // in order of first appearance
+  for (int i = 0; i < n && i < cap && rc == MLA_OK; ++i) {
+    const ProfRecord &r = g_prof.recs[i];
+    float ms = 0.f, at = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&at, g_prof.recs[0].start, r.start) != cudaSuccess) {
+      rc = MLA_ERR_CUDA;
+      break;
+    }
+    int sid = 0;
+    while (sid < int(streams.size()) && streams[sid] != r.stream) ++sid;
+    if (sid == int(streams.size())) streams.push_back(r.stream);
+    mla_launch_record_t &o = records[i];
+    std::memset(&o, 0, sizeof(o));
+    std::strncpy(o.kernel, r.name, sizeof(o.kernel) - 1);
+    std::strncpy(o.role, r.role, sizeof(o.role) - 1);
+    o.stream = sid;
+    o.start_ms = at;
+    o.ms = ms;
+  }
+  drop_profile();
+  if (rc) return rc;
+  return n > cap ? MLA_ERR_TOO_SMALL : MLA_OK;
 }
 
 extern "C" int mla_selftest_bounded_wait(int32_t limit_us, int32_t *gave_up,
@@ -984,8 +1127,12 @@ extern "C" int mla_chunked_prefill_equal_window(
   for (int r = 0; r < num_requests; ++r)
     if (int64_t(context_lens[r]) > int64_t(block_table_stride) * d->block_size)
       return MLA_ERR_INVALID;
+  if (!aligned16(workspace) || (kv_cache && !aligned16(kv_cache))) return MLA_ERR_INVALID;
   EqualWindowBuffers b;
   if (workspace_bytes < carve_equal_window(nullptr, *d, p, b)) return MLA_ERR_TOO_SMALL;
+  const bool tc = tc_shape(*d);
+  if (tc && (!aligned16(q) || !aligned16(new_latent) || !aligned16(w_kv_b) || !tc_available()))
+    return MLA_ERR_UNSUPPORTED;
   carve_equal_window(workspace, *d, p, b);
   std::vector<int32_t> meta(p.meta_total, 0);
   for (int c = 0; c < p.n_chunks; ++c)
@@ -995,24 +1142,27 @@ extern "C" int mla_chunked_prefill_equal_window(
   meta[p.slice_off + 1] = p.T;
   std::memcpy(meta.data() + p.suffix_off, p.qsl.data(), p.qsl.size() * sizeof(int32_t));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::unique_lock<std::mutex> lock;
+  Pipeline *pl = nullptr;
+  rc = lock_pipeline(3 * size_t(p.n_chunks) + 3, lock, &pl);
+  if (rc) return rc;
   rc = upload(b.meta, meta, s);
   if (rc) return rc;
   const int H = d->num_heads, Dv = d->v_dim, T = p.T, R = p.R;
   const int LP = d->kv_lora_rank + d->qk_rope_dim;
   const int es = elem_bytes(d->dtype);
   const int kv_dtype = b.chunk[0].kv_dtype;
-  const void *q_prep =
-      (tc_available() && tc_attn_ok(*d, kv_dtype, LP) && aligned16(q)) ? b.q_prep : nullptr;
+  const void *q_prep = tc ? b.q_prep : nullptr;
   // the chunks run through the same two-buffer pipeline as the new path, so
   // the two schemes differ in their chunks, not in how a chunk is executed
   rc = run_pipeline(
-      s, size_t(p.n_chunks),
+      *pl, s, size_t(p.n_chunks),
       // the running partial starts empty (O = 0, LSE = -inf); the prepared
       // queries
       [&](cudaStream_t st_) {
         int r = launch_fill_empty_rows(b.o_run[0], b.lse_run[0], T, H, Dv, 1,
                                        b.meta + p.slice_off, st_);
-        if (!r && q_prep) r = launch_prepare_q(q, b.q_prep, T, H, st_);
+        if (!r && q_prep) r = launch_prepare_q(q, b.q_prep, T, H, dev_status, st_);
         return r;
       },
       [&](size_t c, cudaStream_t st_) {
@@ -1025,7 +1175,7 @@ extern "C" int mla_chunked_prefill_equal_window(
       },
       [&](size_t c, cudaStream_t st_) {
         return up_proj(*d, b.chunk[c & 1].latent_ws, LP, p.metas[c].rows, w_kv_b,
-                       b.chunk[c & 1].kv_ws, kv_dtype, st_);
+                       b.chunk[c & 1].kv_ws, kv_dtype, dev_status, st_);
       },
       [&](size_t c, cudaStream_t st_) {
         const ChunkMetaHost &m = p.metas[c];
@@ -1033,7 +1183,8 @@ extern "C" int mla_chunked_prefill_equal_window(
                       *ql = cu + R + 1;
         int r = attention(*d, 0, R, ql, cu, m.q_loc.data(), m.cu_rows.data(), T, q,
                           b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
-                          nullptr, b.o_chunk, b.lse_chunk, st_, nullptr, false, q_prep);
+                          nullptr, b.o_chunk, b.lse_chunk, dev_status, st_, nullptr, false,
+                          q_prep);
         if (!r && p.has_empty[c])
           r = launch_mask_empty_context(b.lse_chunk, b.o_chunk, MLA_DTYPE_F32, T, H, Dv, R, ql,
                                         cu, st_);
@@ -1044,13 +1195,13 @@ extern "C" int mla_chunked_prefill_equal_window(
         return r;
       },
       [&](cudaStream_t st_) {
-        return up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, st_);
+        return up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, dev_status, st_);
       });
   if (rc) return rc;
   const int32_t *sq = b.meta + p.suffix_off;
   rc = attention(*d, 1, R, sq, sq, p.qsl.data(), p.qsl.data(), T, q, b.kv_suffix,
-                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, s, nullptr, false,
-                 q_prep);
+                 kv_dtype, T, new_latent, LP, nullptr, b.o_suf, b.lse_suf, dev_status, s,
+                 nullptr, false, q_prep);
   if (rc) return rc;
   const int fin = p.n_chunks & 1;  // the buffer the last chunk merged into
   return launch_merge(out, out_lse, b.o_run[fin], b.lse_run[fin], b.o_suf, b.lse_suf, T, H, Dv,

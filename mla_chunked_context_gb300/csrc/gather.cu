@@ -100,11 +100,12 @@ int launch_gather(const void *cache, int num_blocks, int block_size, int row_byt
   int64_t blocks = (warps_needed * 32 + 255) / 256;
   const int64_t cap = int64_t(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
+  launch_begin(s);
   gather_rows_kernel<<<int(blocks), 256, 0, s>>>(
       static_cast<const uint4 *>(cache), num_blocks, block_size, vec_per_row, block_table,
       bt_stride, num_seqs, seq_request, seq_start, cu_rows, total_rows,
       static_cast<uint4 *>(ws), status);
-  return launch_status();
+  return launch_status(s, "gather_rows_kernel");
 }
 
 }  // namespace mla

@@ -18,7 +18,8 @@ constexpr int GT = 64, GK = 16;
 template <typename T, typename TO>
 __global__ void __launch_bounds__(256) kv_up_proj_simt(const T *__restrict__ A, int64_t lda,
                                                        const T *__restrict__ B, TO *__restrict__ C,
-                                                       int M, int N, int K, int hd) {
+                                                       int M, int N, int K, int hd,
+                                                       int32_t *status) {
   __shared__ float As[GK][GT + 1];
   __shared__ float Bs[GK][GT + 1];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -47,15 +48,20 @@ __global__ void __launch_bounds__(256) kv_up_proj_simt(const T *__restrict__ A, 
     }
     __syncthreads();
   }
+  float amax = 0.f;  // largest magnitude written (fp16 output: range check)
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int gm = m0 + ty + 16 * i, gn = n0 + tx + 16 * j;
       // head-major output [N / hd, M, hd]
-      if (gm < M && gn < N)
+      if (gm < M && gn < N) {
         C[(int64_t(gn / hd) * M + gm) * hd + gn % hd] = from_f32<TO>(acc[i][j]);
+        amax = fmaxf(amax, fabsf(acc[i][j]));
+      }
     }
+  if (sizeof(TO) == 2 && !is_bf16<TO>() && amax >= kF16Overflow && status)
+    atomicOr(status, MLA_STATUS_FP16_RANGE);
 }
 
 constexpr int QK_PER_LANE = 8;  // qk dim up to 256
@@ -162,28 +168,30 @@ bool generic_dims_ok(const mla_dims_t &d) {
 
 template <typename T>
 int up_proj_simt_out(int kv_dtype, const T *latent, int64_t lda, int rows, const T *w, void *kv,
-                     int N, int K, int hd, dim3 grid, cudaStream_t s) {
+                     int N, int K, int hd, int32_t *status, dim3 grid, cudaStream_t s) {
+  launch_begin(s);
   if (kv_dtype == MLA_DTYPE_F32)
     kv_up_proj_simt<T, float><<<grid, 256, 0, s>>>(latent, lda, w, static_cast<float *>(kv), rows,
-                                                   N, K, hd);
+                                                   N, K, hd, status);
   else if (kv_dtype == MLA_DTYPE_F16)
     kv_up_proj_simt<T, __half><<<grid, 256, 0, s>>>(latent, lda, w, static_cast<__half *>(kv),
-                                                    rows, N, K, hd);
+                                                    rows, N, K, hd, status);
   else
     kv_up_proj_simt<T, __nv_bfloat16><<<grid, 256, 0, s>>>(
-        latent, lda, w, static_cast<__nv_bfloat16 *>(kv), rows, N, K, hd);
-  return launch_status();
+        latent, lda, w, static_cast<__nv_bfloat16 *>(kv), rows, N, K, hd, status);
+  return launch_status(s, "kv_up_proj_simt");
 }
 
 int launch_up_proj_simt(int dtype, int kv_dtype, const void *latent, int64_t lda, int rows,
-                        const void *w, void *kv, int N, int K, int hd, cudaStream_t s) {
+                        const void *w, void *kv, int N, int K, int hd, int32_t *status,
+                        cudaStream_t s) {
   if (rows == 0) return MLA_OK;
   dim3 grid((N + GT - 1) / GT, (rows + GT - 1) / GT);
   if (dtype == MLA_DTYPE_BF16)
     return up_proj_simt_out(kv_dtype, static_cast<const __nv_bfloat16 *>(latent), lda, rows,
-                            static_cast<const __nv_bfloat16 *>(w), kv, N, K, hd, grid, s);
+                            static_cast<const __nv_bfloat16 *>(w), kv, N, K, hd, status, grid, s);
   return up_proj_simt_out(kv_dtype, static_cast<const float *>(latent), lda, rows,
-                          static_cast<const float *>(w), kv, N, K, hd, grid, s);
+                          static_cast<const float *>(w), kv, N, K, hd, status, grid, s);
 }
 
 template <typename T>
@@ -206,11 +214,12 @@ int launch_attn_simt(const mla_dims_t &d, int causal, int num_seqs, const int32_
              kv_rows, d.softmax_scale * 1.4426950408889634f};
   const int64_t warps = int64_t(num_q_rows) * d.num_heads;
   const int blocks = int((warps * 32 + 127) / 128);
+  launch_begin(s);
   if (d.dtype == MLA_DTYPE_BF16)
     attn_simt_kv<__nv_bfloat16>(kv_dtype, blocks, a, s);
   else
     attn_simt_kv<float>(kv_dtype, blocks, a, s);
-  return launch_status();
+  return launch_status(s, "attn_simt");
 }
 
 }  // namespace mla

@@ -161,6 +161,7 @@ int launch_merge(void *out, float *out_lse, const void *prefix_o, const float *p
   const int vpr = D / 8;
   const bool pow2 = (vpr & (vpr - 1)) == 0 && (H & (H - 1)) == 0;
   const int vl = __builtin_ctz(unsigned(vpr)), hl = __builtin_ctz(unsigned(H));
+  launch_begin(s);
 #define MLA_MERGE_K(TI, TO, IDX, P2)                                                   \
   merge_kernel<TI, TO, IDX, P2><<<grid, 256, 0, s>>>(                                  \
       static_cast<TO *>(out), out_lse, static_cast<const TI *>(prefix_o), prefix_lse,  \
@@ -184,27 +185,29 @@ int launch_merge(void *out, float *out_lse, const void *prefix_o, const float *p
     MLA_MERGE(float, float);
 #undef MLA_MERGE
 #undef MLA_MERGE_K
-  return launch_status();
+  return launch_status(s, "merge_kernel");
 }
 
 int launch_fill_empty_rows(float *o, float *lse, int T, int H, int Dv, int num_slices,
                            const int32_t *slices, cudaStream_t s) {
   if (num_slices == 0) return MLA_OK;
   dim3 grid(32, num_slices);
+  launch_begin(s);
   fill_empty_rows_kernel<<<grid, 256, 0, s>>>(o, lse, T, H, Dv, slices);
-  return launch_status();
+  return launch_status(s, "fill_empty_rows_kernel");
 }
 
 int launch_mask_empty_context(float *lse, void *o, int dtype, int T, int H, int D, int R,
                               const int32_t *qsl, const int32_t *csl, cudaStream_t s) {
   const int blocks = (T * 32 + 255) / 256;
+  launch_begin(s);
   if (dtype == MLA_DTYPE_BF16)
     mask_empty_context_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
         lse, static_cast<__nv_bfloat16 *>(o), T, H, D, R, qsl, csl);
   else
     mask_empty_context_kernel<float><<<blocks, 256, 0, s>>>(
         lse, static_cast<float *>(o), T, H, D, R, qsl, csl);
-  return launch_status();
+  return launch_status(s, "mask_empty_context_kernel");
 }
 
 }  // namespace mla

@@ -87,6 +87,8 @@ struct AttnParams {
   // key-split scratch: slot k holds O [H][BQ][DV] (normalised) and LSE
   // [H][BQ] of one split
   float *split_o, *split_lse;
+  // nullable: MLA_STATUS_FP16_RANGE when a q_nope value overflowed fp16
+  int32_t *status;
   // (sequence, query tile | (split slot + 1) << 16, first key tile, end key
   // tile), the most key tiles first
   int4 items[MAX_ITEMS];
@@ -133,20 +135,29 @@ __device__ __forceinline__ int softmax_bar_and(int pred) {
   return int(r);
 }
 
-// q_nope (Q boxes 0 and 1) to fp16 in place, to meet the fp16 K_nope in the
-// S MMA; exact for bf16 values within fp16 range.  Thread tid of nthr.
-__device__ __forceinline__ void convert_q_nope(uint8_t *sQ, int tid, int nthr) {
-  uint4 *qv = reinterpret_cast<uint4 *>(sQ);
-#pragma unroll 4
-  for (int v = tid; v < 2 * QBOX / 16; v += nthr) {
-    uint4 x = qv[v];
-    uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+// Four packed bf16 pairs to fp16 pairs (exact for bf16 values of magnitude
+// 2^-14 .. 65504); amax collects the largest magnitude converted.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, float &amax) {
+  uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      w4[e] = pack_f16(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
-    qv[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  for (int e = 0; e < 4; ++e) {
+    const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+    w4[e] = pack_f16(lo, hi);
   }
+  return make_uint4(w4[0], w4[1], w4[2], w4[3]);
+}
+
+// q_nope (Q boxes 0 and 1) to fp16 in place, to meet the fp16 K_nope in the
+// S MMA.  Thread tid of nthr; a value beyond fp16's range sets
+// MLA_STATUS_FP16_RANGE in *status (nullable).
+__device__ __forceinline__ void convert_q_nope(uint8_t *sQ, int tid, int nthr, int32_t *status) {
+  uint4 *qv = reinterpret_cast<uint4 *>(sQ);
+  float amax = 0.f;
+#pragma unroll 4
+  for (int v = tid; v < 2 * QBOX / 16; v += nthr) qv[v] = bf16x8_to_f16x8(qv[v], amax);
   fence_async_smem();
+  if (status && amax >= kF16Overflow) atomicOr(status, MLA_STATUS_FP16_RANGE);
 }
 
 // Brings the half row of the stored partial that the epilogue will merge
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(b_q, 0))
         ok = false;
       else
-        if (!p.q_prepared) convert_q_nope(sQ, threadIdx.x - 64, 128);
+        if (!p.q_prepared) convert_q_nope(sQ, threadIdx.x - 64, 128, p.status);
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
     }
@@ -818,7 +829,7 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       const Unit x = unit_of(u);
       if (x.n_tiles <= 0) continue;
       const bool ok = mbar_wait(b_q, uint32_t(kq & 1));
-      if (ok && !p.q_prepared) convert_q_nope(sQ, lane, 32);
+      if (ok && !p.q_prepared) convert_q_nope(sQ, lane, 32, p.status);
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
       ++kq;
@@ -869,23 +880,20 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
 // copied: one warp per (token, head) row, 24 lanes x 16 bytes, reads and
 // writes both 384 contiguous bytes.
 __global__ void __launch_bounds__(256) prepare_q_kernel(const uint4 *__restrict__ q,
-                                                        uint4 *__restrict__ qh, int T, int H) {
+                                                        uint4 *__restrict__ qh, int T, int H,
+                                                        int32_t *status) {
   const int64_t rows = int64_t(T) * H;
   const int lane = threadIdx.x & 31;
+  float amax = 0.f;  // largest q_nope magnitude converted (fp16 range check)
   for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows;
        r += (int64_t(gridDim.x) * blockDim.x) >> 5) {
     if (lane >= DQK / 8) continue;
     const int64_t t = r / H, h = r - t * H;
     uint4 x = __ldg(q + r * (DQK / 8) + lane);
-    if (lane < DN / 8) {
-      uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w4[e] = pack_f16(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
-      x = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-    }
+    if (lane < DN / 8) x = bf16x8_to_f16x8(x, amax);
     qh[(h * T + t) * (DQK / 8) + lane] = x;
   }
+  if (status && amax >= kF16Overflow) atomicOr(status, MLA_STATUS_FP16_RANGE);
 }
 
 // LSE merge of the key splits of one (sequence, query tile, head) -- the
@@ -1028,7 +1036,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    int64_t latent_ld, const int32_t *accumulate, float *o, float *lse,
                    void *final_out, float *final_lse, int final_dtype, int pnt,
                    const SplitScratch *split, bool skip_keyless, bool q_prepared,
-                   cudaStream_t s) {
+                   int32_t *status, cudaStream_t s) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
   const int H = d.num_heads;
@@ -1081,6 +1089,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     prm.split_o = split ? split->o : nullptr;
     prm.split_lse = split ? split->lse : nullptr;
     prm.q_prepared = q_prepared ? 1 : 0;
+    prm.status = status;
     for (int k = 0; k < n; ++k) {
       const Item &it = items[b + k];
       prm.items[k] = make_int4(it.seq, it.qt | ((it.slot + 1) << 16), it.kt0, it.kt1);
@@ -1091,11 +1100,13 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     // retire
     int64_t tiles = 0;
     for (int k = 0; k < n; ++k) tiles += items[b + k].kt1 - items[b + k].kt0;
-    if (int64_t(n) * H > num_sms() && tiles <= int64_t(kLoopTiles) * n)
+    const bool loop = int64_t(n) * H > num_sms() && tiles <= int64_t(kLoopTiles) * n;
+    launch_begin(s);
+    if (loop)
       attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, prm);
     else
       attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES, s>>>(tq, tkv, tlat, prm);
-    const int rc = launch_status();
+    const int rc = launch_status(s, loop ? "attn_tc_loop_kernel" : "attn_tc_kernel");
     if (rc) return rc;
   }
   if (sg.n > 0) {
@@ -1108,21 +1119,23 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     sg.o = o;
     sg.lse = lse;
     const int64_t warps = int64_t(sg.n) * H * BQ;
+    launch_begin(s);
     split_combine_kernel<<<int((warps * 32 + 255) / 256), 256, 0, s>>>(sg);
-    return launch_status();
+    return launch_status(s, "split_combine_kernel");
   }
   return MLA_OK;
 }
 
-int launch_prepare_q(const void *q, void *qh, int T, int H, cudaStream_t s) {
+int launch_prepare_q(const void *q, void *qh, int T, int H, int32_t *status, cudaStream_t s) {
   if (T == 0) return MLA_OK;
   const int64_t warps = int64_t(T) * H;
   int64_t blocks = (warps * 32 + 255) / 256;
   const int64_t cap = int64_t(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
+  launch_begin(s);
   prepare_q_kernel<<<int(blocks), 256, 0, s>>>(static_cast<const uint4 *>(q),
-                                               static_cast<uint4 *>(qh), T, H);
-  return launch_status();
+                                               static_cast<uint4 *>(qh), T, H, status);
+  return launch_status(s, "prepare_q_kernel");
 }
 
 // The key-split merge on its own, for launches that cut (sequence, query
@@ -1145,8 +1158,9 @@ int launch_split_combine(int n_groups, const int4 *groups, int H, int T, const i
   sg.lse = lse;
   for (int k = 0; k < n_groups; ++k) sg.g[k] = groups[k];
   const int64_t warps = int64_t(n_groups) * H * BQ;
+  launch_begin(s);
   split_combine_kernel<<<int((warps * 32 + 255) / 256), 256, 0, s>>>(sg);
-  return launch_status();
+  return launch_status(s, "split_combine_kernel");
 }
 
 int attn_take_errors() { return sm103::take_error_flags_here(); }

@@ -139,6 +139,7 @@ struct FusedParams {
   const int32_t *q_loc, *k_loc, *acc;
   const uint16_t *w;                 // W_kv_b [H*(Dn+Dv)][L] bf16
   float *o, *lse, *split_o, *split_lse;
+  int32_t *status;                   // nullable: MLA_STATUS_FP16_RANGE on a K/V overflow
   int bounds[MAX_PAIRS + 1];         // cluster c: flattened key tiles [bounds[c], bounds[c+1])
   // (sequence, key tiles, first tile in a head's order, (slot base + 1) | max pieces << 16)
   int4 items[MAX_ITEMS];
@@ -551,15 +552,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t src = tmem + lane_off + COL_BUF + uint32_t(b * 128);
         uint32_t pk[64];
+        float amax = 0.f;  // fp16 range check of this row's K or V values
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
           tmem_ld32(src + uint32_t(c * 32), r);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[c * 16 + e] = pack_f16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
+            amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+            pk[c * 16 + e] = pack_f16(x0, x1);
+          }
         }
+        if (p.status && amax >= kF16Overflow) atomicOr(p.status, MLA_STATUS_FP16_RANGE);
         if (J >= 2 && !mbar_wait(bar(B_STGF + b), uint32_t(((J - 2) >> 1) & 1))) {
           ok = false;
           break;
@@ -890,7 +896,7 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
                       const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
                       int T, const void *q_prep, const void *latent, int64_t latent_ld, int rows,
                       const void *w, const int32_t *acc, float *o, float *lse,
-                      const SplitScratch *split, cudaStream_t s) {
+                      const SplitScratch *split, int32_t *status, cudaStream_t s) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!fused_attn_ok(d, latent_ld) || !al16(q_prep) || !al16(latent) || !al16(w))
     return MLA_ERR_UNSUPPORTED;
@@ -941,6 +947,7 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
   prm.lse = lse;
   prm.split_o = split ? split->o : nullptr;
   prm.split_lse = split ? split->lse : nullptr;
+  prm.status = status;
   for (int c = 0; c <= P; ++c) prm.bounds[c] = plan.bounds[c];
   for (size_t i = 0; i < plan.items.size(); ++i) prm.items[i] = plan.items[i];
 
@@ -951,9 +958,10 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
                        uint64_t(latent_ld) * 2, 64, BKV, true))
     return MLA_ERR_CUDA;
   cfg.gridDim = dim3(2 * P);
+  launch_begin(s);
   if (cudaLaunchKernelEx(&cfg, attn_fused_kernel, tq, tlat, prm) != cudaSuccess)
     return MLA_ERR_CUDA;
-  rc = launch_status();
+  rc = launch_status(s, "attn_fused_kernel");
   if (rc) return rc;
   if (!plan.groups.empty())
     rc = launch_split_combine(int(plan.groups.size()), plan.groups.data(), H, T, q_loc, acc,

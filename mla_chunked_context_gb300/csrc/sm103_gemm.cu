@@ -64,6 +64,7 @@ struct GemmArgs {
   int nseg;           // N segments per 256-row block: a unit is (block, segment)
   int hd;             // output columns per head (Dn + Dv): the output is [N/hd, M, hd]
   uint16_t *out;      // fp16 / bf16 bits
+  int32_t *status;    // nullable: MLA_STATUS_FP16_RANGE when an fp16 output overflowed
 };
 
 // Unit u: N tiles [t0, t1) of segment u / num_pm, row block u % num_pm.
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    float amax = 0.f;  // largest magnitude rounded to fp16 (range check)
     for (int u = first; u < num_units && ok; u += step) {
       int pm, t0, t1;
       unit_range(g, u, pm, t0, t1);
@@ -259,6 +261,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(t_row + j * 64, lo);
           tmem_ld32(t_row + j * 64 + 32, hi);
           tmem_wait_ld();
+          if (kF16Out) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(lo[e])), fabsf(__uint_as_float(hi[e]))));
+          }
           // lane = row: its 64 values as 8 16-byte pieces, XOR-swizzled so the
           // writes and the reads below are free of bank conflicts
           uint8_t *row = stg + lane * 128;
@@ -306,6 +313,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+    // a finite accumulator of magnitude >= 65520 became +-inf in fp16
+    if (kF16Out && g.status && amax >= kF16Overflow) atomicOr(g.status, MLA_STATUS_FP16_RANGE);
   }
   tc_fence_before();
   __syncthreads();
@@ -386,7 +395,7 @@ bool tc_gemm_ok(const mla_dims_t &d, int kv_dtype, int64_t lda, const void *late
 }
 
 int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int64_t lda,
-                      int rows, const void *w, void *kv, cudaStream_t s) {
+                      int rows, const void *w, void *kv, int32_t *status, cudaStream_t s) {
   using namespace sm103;
   const int K = d.kv_lora_rank;
   const int hd = d.qk_nope_dim + d.v_dim;
@@ -397,7 +406,7 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
       !make_tmap_2d_16(&tb, false, w, K, N, uint64_t(K) * 2, BK, BN / 2, true))
     return MLA_ERR_CUDA;
   GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, 1, hd,
-             static_cast<uint16_t *>(kv)};
+             static_cast<uint16_t *>(kv), status};
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(up_proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -443,10 +452,11 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
   const int units = g.num_pm * g.nseg;
   const int clusters = units < pairs ? units : pairs;
   cfg.gridDim = dim3(2 * clusters);
+  launch_begin(s);
   const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<true>, ta, tb, g)
                             : cudaLaunchKernelEx(&cfg, up_proj_tc_kernel<false>, ta, tb, g);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  return launch_status();
+  return launch_status(s, "up_proj_tc_kernel");
 }
 
 }  // namespace mla
@@ -467,7 +477,8 @@ __global__ void bounded_wait_selftest_kernel(long long limit, int32_t *gave_up) 
 int gemm_take_errors() { return sm103::take_error_flags_here(); }
 
 int launch_bounded_wait_selftest(long long limit_cycles, int32_t *gave_up, cudaStream_t s) {
+  launch_begin(s);
   bounded_wait_selftest_kernel<<<1, 1, 0, s>>>(limit_cycles, gave_up);
-  return launch_status();
+  return launch_status(s, "bounded_wait_selftest_kernel");
 }
 }  // namespace mla

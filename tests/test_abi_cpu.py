@@ -146,34 +146,107 @@ def test_argument_errors_before_any_launch():
         _lib.MLA_ERR_INVALID
     assert L.merge_attn_states(None, None, None, None, None, None, 4, 2, 12, 0, 1, 1, None) == \
         _lib.MLA_ERR_INVALID          # head_dim not a multiple of 8
-    assert L.mla_kv_up_proj(C.byref(d), None, 80, 5, None, None, 0, None) == \
+    assert L.mla_kv_up_proj(C.byref(d), None, 80, 5, None, None, 0, None, None) == \
         _lib.MLA_ERR_INVALID
-    assert L.mla_kv_up_proj(C.byref(d), None, 80, 5, None, None, 7, None) == \
+    assert L.mla_kv_up_proj(C.byref(d), None, 80, 5, None, None, 7, None, None) == \
         _lib.MLA_ERR_INVALID          # unknown K/V dtype
     bad = _lib.Dims.of(w)
     bad.v_dim = 12
-    assert L.mla_kv_up_proj(C.byref(bad.c()), None, 80, 5, None, None, 0, None) == \
+    assert L.mla_kv_up_proj(C.byref(bad.c()), None, 80, 5, None, None, 0, None, None) == \
         _lib.MLA_ERR_UNSUPPORTED
     ctx, ql = _lib._i32_host(w.context_lens), _lib._i32_host(w.query_lens)
     rc = L.mla_chunked_prefill(C.byref(d), ctx, ql, 4, w.row_budget, w.max_context_chunk,
                                w.split_alignment, None, None, None, 0, None, 1, None, None, 0,
-                               None, None, None, None)
+                               None, None, None, 0, None, None)
     assert rc == _lib.MLA_ERR_INVALID
     # a budget below one aligned split
     rc = L.mla_chunked_prefill(C.byref(d), ctx, ql, 4, 8, 8, 16, None, None, None, 0, None, 1,
-                               None, None, 0, None, None, None, None)
+                               None, None, 0, None, None, None, 0, None, None)
     assert rc == _lib.MLA_ERR_PLANNER_STUCK
     # workspace too small (non-null pointers that are never dereferenced)
     fake = C.c_void_p(16)
     rc = L.mla_chunked_prefill(C.byref(d), ctx, ql, 4, w.row_budget, w.max_context_chunk,
                                w.split_alignment, fake, fake, fake, 100, fake, 100, fake, fake,
-                               16, fake, None, None, None)
+                               16, fake, None, None, 0, None, None)
     assert rc == _lib.MLA_ERR_TOO_SMALL
     # a context longer than the block table can address
     rc = L.mla_chunked_prefill(C.byref(d), ctx, ql, 4, w.row_budget, w.max_context_chunk,
                                w.split_alignment, fake, fake, fake, 100, fake, 2, fake, fake,
-                               1 << 40, fake, None, None, None)
+                               1 << 40, fake, None, None, 0, None, None)
     assert rc == _lib.MLA_ERR_INVALID
+
+
+def test_alignment_and_dispatch_errors_before_any_launch():
+    """Pointer alignment and the no-fallback rule: a misaligned O for the
+    merge, a misaligned workspace or cache, and a DeepSeek-shaped bf16 call
+    whose operands the tensor-core kernels cannot take all return an error
+    code before anything is enqueued (fake pointers, never dereferenced)."""
+    L = _lib.lib()
+    ok, odd = C.c_void_p(256), C.c_void_p(256 + 8)
+    # merge: O pointers 16-byte aligned, LSE pointers 4-byte aligned
+    for args in ((odd, ok, ok), (ok, odd, ok), (ok, ok, odd)):
+        out, po, so = args
+        assert L.merge_attn_states(out, None, po, ok, so, ok, 4, 2, 8, 2, 1, 1, None) == \
+            _lib.MLA_ERR_INVALID
+    assert L.merge_attn_states(ok, None, ok, C.c_void_p(258), ok, ok, 4, 2, 8, 2, 1, 1,
+                               None) == _lib.MLA_ERR_INVALID
+    # a prefix that is never read (prefix_num_tokens = 0) needs no alignment
+    assert L.merge_attn_states(ok, None, odd, None, ok, C.c_void_p(258), 4, 2, 8, 0, 1, 1,
+                               None) == _lib.MLA_ERR_INVALID      # suffix LSE still checked
+    w = W.workload("uniform")
+    d = _lib.Dims.of(w).c()
+    # gather: cache and workspace move as 16-byte pieces
+    assert L.mla_gather_context_rows(C.byref(d), odd, 10, ok, 4, 1, ok, ok, ok, 64, ok, None,
+                                     None) == _lib.MLA_ERR_INVALID
+    # the tensor-core shape never takes the CUDA-core kernels: a misaligned
+    # operand (or no tcgen05 GPU, as here) is MLA_ERR_UNSUPPORTED
+    assert L.mla_kv_up_proj(C.byref(d), odd, 576, 64, ok, ok, _lib.MLA_DTYPE_F16, None,
+                            None) == _lib.MLA_ERR_UNSUPPORTED
+    assert L.mla_kv_up_proj(C.byref(d), ok, 576, 64, ok, ok, _lib.MLA_DTYPE_F32, None,
+                            None) == _lib.MLA_ERR_UNSUPPORTED      # F32 K/V: not on that path
+    ql, kl = _lib._i32_host([0, 4]), _lib._i32_host([0, 64])
+    for q, kv_dtype in ((odd, _lib.MLA_DTYPE_F16), (ok, _lib.MLA_DTYPE_BF16)):
+        assert L.mla_varlen_attn(C.byref(d), 0, 1, ok, ok, ql, kl, 4, q, ok, kv_dtype, 64, ok,
+                                 576, None, ok, ok, None, None) == _lib.MLA_ERR_UNSUPPORTED
+    ctx, qn = _lib._i32_host(w.context_lens), _lib._i32_host(w.query_lens)
+    n = len(w.context_lens)
+    big = 1 << 40
+
+    def prefill(q=ok, ws=ok, cache=ok, pinned=None, pinned_bytes=0):
+        return L.mla_chunked_prefill(C.byref(d), ctx, qn, n, w.row_budget, w.max_context_chunk,
+                                     w.split_alignment, q, ok, cache, 100, ok, 1 << 20, ok, ws,
+                                     big, ok, None, pinned, pinned_bytes, None, None)
+    assert prefill(ws=odd) == _lib.MLA_ERR_INVALID
+    assert prefill(cache=odd) == _lib.MLA_ERR_INVALID
+    assert prefill(q=odd) == _lib.MLA_ERR_UNSUPPORTED
+    # pinned metadata scratch below mla_prefill_pinned_bytes
+    need = M.mla_prefill_pinned_bytes(_lib.Dims.of(w), w.context_lens, w.query_lens,
+                                      w.row_budget, w.max_context_chunk, w.split_alignment)
+    assert need > 0
+    assert prefill(pinned=ok, pinned_bytes=need - 4) == _lib.MLA_ERR_TOO_SMALL
+
+
+def test_pinned_bytes_counts_the_metadata():
+    """The metadata of one prefill: per execution group (n requests) 5n + 2
+    ints, two ints per empty-token slice, and R + 1 query offsets."""
+    w = W.workload("tiny")
+    dims = _lib.Dims.of(w)
+    got = M.mla_prefill_pinned_bytes(dims, w.context_lens, w.query_lens, w.row_budget,
+                                     w.max_context_chunk, w.split_alignment)
+    # tiny: the plan's chunks run as groups; bound it by one group per chunk
+    plans = M.mla_plan_context_chunks(w.context_lens, w.row_budget, w.max_context_chunk,
+                                      w.split_alignment)
+    R = len(w.context_lens)
+    empty = len(P.empty_token_slices(w.context_lens, w.query_lens))
+    hi = sum(5 * (c.request_end - c.request_start) + 2 for c in plans) + 2 * empty + R + 1
+    assert 0 < got <= 4 * hi
+
+
+def test_profile_with_no_launches():
+    """mla_profile_begin / _end with nothing launched in between: no
+    records, no CUDA call needed."""
+    M.mla_profile_begin()
+    assert M.mla_profile_end() == []
 
 
 def test_c_equal_window_planner_matches_oracle():
@@ -214,7 +287,7 @@ def test_fused_entry_host_checks():
     def call(q_loc, k_loc, q=fake, latent_ld=576, rows=300, n=1):
         return L.mla_fused_context_attn(C.byref(d), n, fake, fake, q_loc, k_loc, T, q, fake,
                                         latent_ld, rows, fake, None, fake, fake, fake, 1 << 30,
-                                        None)
+                                        None, None)
     assert call(ql, kl, q=None) == _lib.MLA_ERR_INVALID
     assert call(ql, kl, latent_ld=500) == _lib.MLA_ERR_INVALID
     assert call(ql, kl, rows=299) == _lib.MLA_ERR_INVALID            # keys past the latent rows

@@ -69,9 +69,14 @@ def test_noalloc_matches_workspace_entry_two_calls():
                      dtype=torch.uint8, device=dev)
     ref_o, ref_l = run(lambda c, o, l: M.mla_context_chunk_attn(
         d, c, qsl, g["q"], g["kv_cache"], g["block_table"], g["w_kv_b"], ws, o, l))
+    # every row of the partial is written (the last request has context, so
+    # no token lies past prefix_num_tokens): a row both paths left unwritten
+    # would otherwise compare equal as NaN against NaN
+    assert not torch.isnan(ref_o).any() and not torch.isnan(ref_l).any()
     for _ in range(2):
         got_o, got_l = run(lambda c, o, l: M.mla_context_chunk_attn_noalloc(
             d, c, qsl, g["q"], g["kv_cache"], g["block_table"], g["w_kv_b"], o, l))
+        assert not torch.isnan(got_o).any() and not torch.isnan(got_l).any()
         _close(got_o, ref_o, 2e-2, 2e-2)
         _close(got_l, ref_l, 1e-3, 0.0)
     assert M.mla_device_error_flags() == 0
