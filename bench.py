@@ -201,16 +201,32 @@ def split_steps(records, steps):
     return [records[i * k:(i + 1) * k] for i in range(steps)]
 
 
+def attributed_ms(rs):
+    """Wall time of one step's launches with overlap shared out: every
+    instant is split equally among the launches running then, so the shares
+    add up to the time the GPU ran any of them (per role)."""
+    pts = sorted({p for r in rs for p in (r[2], r[2] + r[3])})
+    out = {}
+    for a, b in zip(pts, pts[1:]):
+        live = [r for r in rs if r[2] <= a and r[2] + r[3] >= b]
+        for r in live:
+            out[r[4]] = out.get(r[4], 0.0) + (b - a) / len(live)
+    return out
+
+
 def breakdown_of(records, steps, w, plans, peaks):
-    """Per step of the method: launches and summed in-place CUDA-event time
-    per prefill step; per kernel: its rooflines; the spec bar:
-    (a5 + a6 FLOPs) / (span from the first gather's start to the end of the
-    last context-attention launch)."""
+    """Per step of the method: launches, summed in-place CUDA-event time and
+    overlap-attributed time per prefill step; per kernel: its rooflines; the
+    spec bar: (a5 + a6 FLOPs) / (span from the first gather's start to
+    the end of the last context-attention launch)."""
     per_step = split_steps(records, steps)
     fl = flops_of(w, plans)
     roles, kernels = {}, {}
     spans = []
+    attributed = {}
     for rs in per_step:
+        for role, ms in attributed_ms(rs).items():
+            attributed[role or "(other)"] = attributed.get(role or "(other)", 0.0) + ms / steps
         ctx = [r for r in rs if r[4] in (ROLE_GATHER, ROLE_UP, ROLE_ATTN)]
         if ctx:
             t0 = min(r[2] for r in ctx)
@@ -225,10 +241,11 @@ def breakdown_of(records, steps, w, plans, peaks):
             k = kernels.setdefault(name, {"launches": 0, "ms": 0.0})
             k["launches"] += 1
             k["ms"] += ms
-    for e in roles.values():
+    for name, e in roles.items():
         e["launches"] /= steps
         e["ms"] /= steps
         e["kernels"] = sorted(e["kernels"])
+        e["attributed_ms"] = attributed.get(name, 0.0)
     for k in kernels.values():
         k["launches"] /= steps
         k["ms"] /= steps
@@ -236,14 +253,14 @@ def breakdown_of(records, steps, w, plans, peaks):
     es = 2 if w.dtype == "bf16" else 4
     row_bytes = (w.kv_lora_rank + w.qk_rope_dim) * es
 
-    def rl(ms, work, launches, unit, peak, peak_src, bound):
+    def rl(ms, work, launches, unit, peak, peak_src, bound, share):
         if not ms or not launches:
             return None
         sc = 1e12 if unit == "TFLOP/s" else 1e9
         ach = work / (ms / 1e3) / sc
         return {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
                 "peak_source": peak_src, "launches_per_step": launches,
-                "ms_per_step": ms, "work_per_step": work}
+                "ms_per_step": ms, "attributed_ms_per_step": share, "work_per_step": work}
     g = roles.get(ROLE_UP, {"ms": 0, "launches": 0})
     gn = roles.get(ROLE_UP_NEW, {"ms": 0, "launches": 0})
     a = roles.get(ROLE_ATTN, {"ms": 0, "launches": 0})
@@ -251,16 +268,17 @@ def breakdown_of(records, steps, w, plans, peaks):
     ga = roles.get(ROLE_GATHER, {"ms": 0, "launches": 0})
     bf = peaks["bf16_tflops"]
     src = peaks["source"]
+    at = lambda *rs: sum(attributed.get(r, 0.0) for r in rs)  # noqa: E731
     rooflines = {
         "up_proj": rl(g["ms"] + gn["ms"], fl["up_proj_ctx"] + fl["up_proj_new"],
                       g["launches"] + gn["launches"], "TFLOP/s", bf, src + " bf16 burst",
-                      "tensor"),
+                      "tensor", at(ROLE_UP, ROLE_UP_NEW)),
         "context_attention": rl(a["ms"], fl["attn_ctx"], a["launches"], "TFLOP/s", bf,
-                                src + " bf16 burst", "tensor"),
+                                src + " bf16 burst", "tensor", at(ROLE_ATTN)),
         "new_token_attention_merge": rl(an["ms"], fl["attn_new"], an["launches"], "TFLOP/s", bf,
-                                        src + " bf16 burst", "tensor"),
+                                        src + " bf16 burst", "tensor", at(ROLE_ATTN_NEW)),
         "gather": rl(ga["ms"], 2.0 * fl["context_rows"] * row_bytes, ga["launches"], "GB/s",
-                     peaks["hbm_gbs"], src + " copy", "hbm"),
+                     peaks["hbm_gbs"], src + " copy", "hbm", at(ROLE_GATHER)),
     }
     rooflines = {k: v for k, v in rooflines.items() if v is not None}
     bar = None
@@ -270,7 +288,10 @@ def breakdown_of(records, steps, w, plans, peaks):
                "a4_a7_span_ms": span_ms, "tflops": ach, "frac_burst": ach / bf,
                "frac_sustained": (ach / peaks["bf16_tflops_sustained"]
                                   if peaks.get("bf16_tflops_sustained") else None)}
-    return {"roles": roles, "kernels": kernels, "north_star_bar": bar, "rooflines": rooflines}
+    timeline = [{"kernel": r[0], "role": r[4], "stream": r[1], "start_ms": round(r[2] - per_step[0][0][2], 4),
+                 "ms": round(r[3], 4)} for r in per_step[0]] if per_step and per_step[0] else []
+    return {"roles": roles, "kernels": kernels, "north_star_bar": bar, "rooflines": rooflines,
+            "timeline_first_step": timeline}
 
 
 def committed_traffic(kernel, workload):
@@ -352,8 +373,9 @@ def bench_config(M, W, name, dev, peaks, flush, steps, warmup):
     throughput and the in-step breakdown (same method as the main line)."""
     w = W.workload(name)
     x, g, plans, pf, out, step = prefill_runner(M, W, w, dev)
-    ms, records, launched = timed_steps(M, step, steps, warmup, flush,
-                                        torch.cuda.current_stream())
+    stream = torch.cuda.current_stream()
+    ms, _, launched = timed_steps(M, step, steps, warmup, flush, stream, profile=False)
+    _, records, _ = timed_steps(M, step, steps, 1, flush, stream, profile=True)
     step_ms = statistics.median(ms)
     fl = flops_of(w, plans)
     br = breakdown_of(records, steps, w, plans, peaks)
@@ -386,13 +408,14 @@ def run_ours(args, rank, world, dev):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    step_ms, records, launched = timed_steps(M, step, args.steps, args.warmup, flush, stream,
-                                             profile=True, world=world, sampler=sampler)
+    step_ms, _, launched = timed_steps(M, step, args.steps, args.warmup, flush, stream,
+                                       profile=False, world=world, sampler=sampler)
     clocks = sampler.stop()
     max_ms = job_time_ms(sum(step_ms), world, dev)
     value = whole_job_rate(T, world, args.steps, max_ms)
-    # the same steps without the per-launch events, for the profile's cost
-    plain_ms, _, _ = timed_steps(M, step, args.steps, 1, flush, stream, profile=False)
+    # a second timed region of the same steps with the library's per-launch
+    # events on (the in-step breakdown and the kernels' rooflines)
+    prof_ms, records, _ = timed_steps(M, step, args.steps, 1, flush, stream, profile=True)
 
     # ---- e2e: host buffers, copies inside the timed region.  Inputs are
     # double-buffered on the device: step i+1's host->device copy (on a copy
@@ -454,8 +477,9 @@ def run_ours(args, rank, world, dev):
     if rank == 0:
         fl = flops_of(w, plans)
         br = breakdown_of(records, args.steps, w, plans, peaks)
-        # the dominant kernel: the largest share of the step's launch time
-        dom = max(br["rooflines"].items(), key=lambda kv: kv[1]["ms_per_step"])
+        # the dominant kernel: the largest share of the step's GPU time, with
+        # the time of launches that run side by side shared out among them
+        dom = max(br["rooflines"].items(), key=lambda kv: kv[1]["attributed_ms_per_step"])
         roofline = dict(dom[1])
         roofline["kernel"] = dom[0]
         roofline["traffic"] = committed_traffic(
@@ -477,7 +501,7 @@ def run_ours(args, rank, world, dev):
         result = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_mean,
-            "ms_per_step_without_launch_events": statistics.mean(plain_ms),
+            "ms_per_step_with_launch_events": statistics.mean(prof_ms),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded host draws; random-init W_kv_b)",
             "config": config_of(w, plans, world),
@@ -494,9 +518,12 @@ def run_ours(args, rank, world, dev):
             "rooflines": br["rooflines"],
             "north_star_bar": br["north_star_bar"],
             "breakdown": {"roles": br["roles"], "kernels": br["kernels"],
+                          "timeline_first_step": br["timeline_first_step"],
                           "how": "CUDA events recorded by the library on the launching "
-                                 "stream around every launch of the timed steps "
-                                 "(mla_profile_begin/_end); side-stream launches overlap"},
+                                 "stream around every launch of a second timed region of "
+                                 "the same steps (mla_profile_begin/_end); launches on the "
+                                 "side streams overlap the caller's, so ms adds up to more "
+                                 "than the step and attributed_ms shares overlap out"},
             "merge": merge,
             "comparator": comparator,
             "configs": configs,

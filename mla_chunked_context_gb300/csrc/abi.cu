@@ -65,6 +65,7 @@ int launch_attn_fused(const mla_dims_t &d, int num_seqs, const int32_t *q_loc,
                       const void *w, const int32_t *acc, float *o, float *lse,
                       const SplitScratch *split, int32_t *status, cudaStream_t s);
 int fused_take_errors();
+int gather_take_errors();
 bool tc_available();
 
 namespace {
@@ -953,9 +954,10 @@ extern "C" int mla_selftest_bounded_wait(int32_t limit_us, int32_t *gave_up,
 extern "C" int mla_device_error_flags(int32_t *flags) {
   if (!flags) return MLA_ERR_INVALID;
   if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
-  const int a = gemm_take_errors(), b = attn_take_errors(), c = fused_take_errors();
-  if (a < 0 || b < 0 || c < 0) return MLA_ERR_CUDA;
-  *flags = a | b | c;
+  const int a = gemm_take_errors(), b = attn_take_errors(), c = fused_take_errors(),
+            e = gather_take_errors();
+  if (a < 0 || b < 0 || c < 0 || e < 0) return MLA_ERR_CUDA;
+  *flags = a | b | c | e;
   return MLA_OK;
 }
 

@@ -197,11 +197,11 @@ def test_profile_records_every_launch_of_a_prefill():
     assert status == 0
     assert len(recs) == launched > 0
     names = [r[0] for r in recs]
-    assert "up_proj_tc_kernel" in names and "gather_rows_kernel" in names
+    assert "up_proj_tc_kernel" in names and "gather_bulk_kernel" in names
     assert any(n.startswith("attn_tc") for n in names)
     assert all(r[3] > 0 for r in recs) and all(r[2] >= 0 for r in recs)
     streams = {r[0]: r[1] for r in recs}
-    assert streams["gather_rows_kernel"] != streams["up_proj_tc_kernel"]
+    assert streams["gather_bulk_kernel"] != streams["up_proj_tc_kernel"]
     # profiling off again: nothing is recorded
     _prefill(w, x)
     M.mla_profile_begin()

@@ -248,6 +248,42 @@ def test_gather_bit_exact(name):
         assert status.item() == 0
 
 
+def test_gather_windows_runs_and_adjacent_blocks():
+    """The bulk-copy gather cuts the workspace into 32-row windows and copies
+    runs of rows that are consecutive in the cache: sequences of 1..70 rows
+    starting mid-block, a request whose physical blocks follow one another
+    in memory (runs that cross block boundaries), and a partial last window;
+    bit-exact against the oracle's row-by-row gather."""
+    w = W.scaled(W.workload("uniform"), context_lens=[1, 37, 70, 129, 5, 300, 2, 64],
+                 query_lens=[1] * 8, num_heads=2, seed=39)
+    x = W.make_inputs(w)
+    # request 5 (300 rows, 5 blocks) moved to 5 new physical blocks that
+    # follow one another in memory, holding the same rows
+    bt = x["block_table"].clone()
+    nblk = x["kv_cache"].shape[0]
+    x["kv_cache"] = torch.cat([x["kv_cache"], x["kv_cache"][bt[5, :5].long()]], 0)
+    bt[5, :5] = torch.arange(nblk, nblk + 5, dtype=torch.int32)
+    x["block_table"] = bt
+    g = to_dev(x)
+    starts = [0, 3, 60, 0, 1, 17, 40, 0]                 # mid-block starts
+    lens = [1, 34, 10, 129, 4, 283, 2, 64]
+    from oracle.planner import ChunkPlan
+    plan = ChunkPlan(0, 8, starts, lens)
+    req = torch.arange(8, dtype=torch.int32, device=DEV)
+    st = torch.tensor(starts, dtype=torch.int32, device=DEV)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=DEV)
+    rows = int(sum(lens))
+    assert rows % 32 != 0
+    ws = torch.full((rows, w.latent_dim), float("nan"), dtype=w.torch_dtype, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    M.mla_gather_context_rows(M.Dims.of(w), g["kv_cache"], g["block_table"], req, st, cu, rows,
+                              ws, status)
+    torch.cuda.synchronize()
+    ref = O.gather_chunk(f64(x["kv_cache"]), bt.numpy(), plan, w.block_size)
+    assert np.array_equal(f64(ws), ref)
+    assert status.item() == 0
+
+
 def test_gather_bad_block_sets_status():
     w = W.workload("tiny")
     plan = P.plan_mla_context_chunks(w.context_lens, 128, 128, 16)[0]
