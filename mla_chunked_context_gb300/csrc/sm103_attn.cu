@@ -123,18 +123,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ int softmax_bar_and(int pred) {
-  // named barrier 1 over the 256 softmax threads (warps 2-9), AND of pred
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(pred)
-      : "memory");
-  return int(r);
-}
-
 // Four packed bf16 pairs to fp16 pairs (exact for bf16 values of magnitude
 // 2^-14 .. 65504); amax collects the largest magnitude converted.
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, float &amax) {
@@ -273,11 +261,9 @@ __device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col
 // warpgroups' (max, sum) per row through xchg, merge O_A and O_B and write
 // the row -- or LSE-merge it into the stored partial (a continued request),
 // into the key-split scratch slot, or with the context partial into the
-// final output -- as the launch asks.  The softmax threads meet at one
-// barrier (named barrier 1 when kNamedBar, else all threads of the CTA).
-// b_ofree (nonzero): arrived on once the warp has read O from TMEM.
-// Returns the AND over the threads of `ok`.
-template <bool kNamedBar>
+// final output -- as the launch asks.  All threads of the CTA meet at one
+// barrier.  b_ofree (nonzero): arrived on once the warp has read O from
+// TMEM.  Returns the AND over the threads of `ok`.
 __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem,
                                               uint32_t lane_off, float *xchg, uint32_t b_odone,
                                               uint32_t odone_parity, uint32_t b_ofree, int wg,
@@ -316,7 +302,7 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
   tc_fence_before();
   // both warpgroups' O are complete after this barrier (each waited for
   // its own last P.V); all threads take part, the MMA warps too
-  const int okv = kNamedBar ? softmax_bar_and(ok ? 1 : 0) : __syncthreads_and(ok ? 1 : 0);
+  const int okv = __syncthreads_and(ok ? 1 : 0);
   tc_fence_after();
   const float mA = ym[row], lA = yl[row], mB = xm[row], lB = xl[row];
   const float mx = fmaxf(mA, mB);
@@ -592,8 +578,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         b_pfull + 8 * wg, j, (kt0 + j) * BKV + wg * HALF, nk, qpos, m_used, l,
                         lane);
     }
-    unit_epilogue<false>(p, tmem, lane_off, xchg, b_odone, uint32_t((n_tiles - 1) & 1), 0u, wg,
-                         row, lane, h, seq, slot, q_beg, nq, qpos, n_tiles, m_used, l, ok);
+    unit_epilogue(p, tmem, lane_off, xchg, b_odone, uint32_t((n_tiles - 1) & 1), 0u, wg, row,
+                  lane, h, seq, slot, q_beg, nq, qpos, n_tiles, m_used, l, ok);
   }
   if (warp < 2) __syncthreads_and(1);  // matches the softmax warps' vote
   tc_fence_before();
@@ -607,15 +593,261 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // The same attention for launches of many short units (a few key tiles per
 // (query tile, head)): a CTA per SM walks its units u = blockIdx.x,
-// + gridDim.x, ... in turn, keeping its barriers and TMEM.  The barriers
-// count on across units (key tile J is the CTA's J-th over all its units, a
-// unit with key tiles its kq-th such unit), and a converter warp (warp 10)
-// turns each unit's q_nope to fp16 as soon as it lands, so the next unit's
-// Q and K/V loads and its S MMAs overlap this unit's softmax and epilogue.
-// Barriers beyond the per-unit kernel: qfree (the unit's last S MMA is done
-// with Q) and ofree (the epilogue warps have read O_A, O_B).
+// + gridDim.x, ... in turn, keeping its barriers and TMEM.  The two softmax
+// warpgroups take alternate units (the CTA's k-th unit belongs to warpgroup
+// k % 2), each with full 128-key rows and its own O accumulator, so one
+// unit's epilogue (the read of O, the merge with the stored partial, the
+// stores) runs while the other warpgroup's unit is scored and
+// exponentiated.  The barriers count on across units (key tile J is the
+// CTA's J-th over all its units; a warpgroup's pfull / odone / ofree count
+// its own tiles and units), and a converter warp (warp 10) turns each
+// unit's q_nope to fp16 as soon as it lands when the queries are not
+// prepared, so the next unit's Q and K/V loads and its S MMAs overlap this
+// unit's softmax and epilogue.
+// TMEM: S0 [0,128) S1 [128,256) (P of a tile over the first 64 columns of
+// its S buffer), O of warpgroup 0 [256,384), of warpgroup 1 [384,512).
 constexpr int THREADS_LOOP = THREADS + 32;
-constexpr int SMEM_BYTES_LOOP = SMEM_BYTES + XCHG_BYTES;  // xchg per unit parity
+constexpr int SMEM_BYTES_LOOP = SMEM_BYTES;
+
+// One 128-key tile of the online softmax for a full query row (qpos) of a
+// warpgroup's unit: the row's scores come out of TMEM in two halves of 64
+// keys, each masked (past the sequence, and causal past the query), its max
+// raising the running max lazily (by more than 2^8 only), exponentiated and
+// written back as fp16 P over the first 64 columns of the S buffer.  When the
+// second half raises the max, the first half's P is rescaled in TMEM (rare).
+// O is rescaled after the warpgroup's previous P.V (odone, its jw-th tile)
+// has finished; then an arrival on pfull.  Returns false when a wait gave up.
+__device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t s_col,
+                                                  uint32_t o_col, uint32_t sfull_bar,
+                                                  uint32_t sfull_parity, uint32_t b_odone,
+                                                  uint32_t pfull_bar, int jw, int k0, int nk,
+                                                  int qpos, float &m_used, float &l, int lane) {
+  if (!mbar_wait(sfull_bar, sfull_parity)) return false;
+  tc_fence_after();
+  float alpha = 1.f;
+  bool rescale = false;
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    float sv[HALF];
+    {
+      uint32_t r0[32], r1[32];
+      tmem_ld32(s_col + uint32_t(hh * HALF), r0);
+      tmem_ld32(s_col + uint32_t(hh * HALF + 32), r1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        sv[e] = __uint_as_float(r0[e]);
+        sv[32 + e] = __uint_as_float(r1[e]);
+      }
+    }
+    const int kh = k0 + hh * HALF;
+    int valid = nk - kh;
+    if (p.causal) valid = min(valid, qpos - kh + 1);
+    if (valid < HALF) {
+#pragma unroll
+      for (int e = 0; e < HALF; ++e)
+        if (e >= valid) sv[e] = neg_inf();
+    }
+    float tm[HALF / 2];
+#pragma unroll
+    for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
+#pragma unroll
+    for (int w = HALF / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
+    const float mx = tm[0] * p.scale_log2;
+    if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
+      const float m_new = fmaxf(mx, m_used);
+      if (m_used != neg_inf() && m_new != neg_inf()) {
+        const float a = exp2f(m_used - m_new);
+        alpha *= a;
+        l *= a;
+        rescale = true;
+        if (hh == 1) {
+          // the first half's P was exponentiated against the old max
+          uint32_t r[32];
+          tmem_wait_st();
+          tmem_ld32(s_col, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const __half2 h2 = *reinterpret_cast<const __half2 *>(&r[e]);
+            const float2 f = __half22float2(h2);
+            r[e] = pack_f16(f.x * a, f.y * a);
+          }
+          tmem_st32(s_col, r);
+        }
+      }
+      m_used = m_new;
+    }
+    const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
+    uint32_t pk[HALF / 2];
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < HALF / 2; ++e) {
+      const float a = ex2_approx(fmaf(sv[2 * e], p.scale_log2, nbase));
+      const float b = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, nbase));
+      ls[e & 3] += a + b;
+      pk[e] = pack_f16(a, b);
+    }
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    // P of keys [hh*64, hh*64+64) over columns [hh*32, hh*32+32): those S
+    // columns are already read (the first half was read before it is
+    // overwritten; the second half's own columns lie beyond 64)
+    tmem_st32(s_col + uint32_t(hh * 32), pk);
+  }
+  // the warpgroup's previous P.V into O has finished before O is rescaled
+  if (jw > 0 && !mbar_wait(b_odone, uint32_t((jw - 1) & 1))) return false;
+  tc_fence_after();
+  if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+    for (int c = 0; c < DV / 32; ++c) {
+      uint32_t r[32];
+      const uint32_t oc = o_col + uint32_t(c * 32);
+      tmem_ld32(oc, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+      tmem_st32(oc, r);
+    }
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(pfull_bar);
+  return true;
+}
+
+// Epilogue of one unit for a full query row: after the unit's last P.V
+// (odone at odone_parity), O / l and the LSE are written -- or LSE-merged
+// into the stored partial (a continued request), into the key-split scratch
+// slot, or with the context partial into the final output -- as the launch
+// asks.  Each thread owns its row, so no barrier is needed; the warp
+// arrives on b_ofree once it has read O from TMEM.
+__device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t o_col,
+                                                   uint32_t b_odone, uint32_t odone_parity,
+                                                   uint32_t b_ofree, int lane, int h, int seq,
+                                                   int slot, int q_beg, int nq, int qpos,
+                                                   int n_tiles, float m_used, float l, bool ok) {
+  if (ok && n_tiles > 0 && !mbar_wait(b_odone, odone_parity)) ok = false;
+  ok = __all_sync(0xffffffffu, ok) != 0;
+  const int t = q_beg + qpos;
+  const int64_t li = int64_t(h) * p.T + t;
+  const bool fin = p.fout != nullptr;
+  const bool split = slot >= 0;
+  const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
+  const bool merge_old = accumulate || (fin && t < p.pnt);
+  const bool live = qpos < nq;
+  const float old = (merge_old && live) ? p.lse[li] : neg_inf();
+  float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + (qpos & (BQ - 1))) * DV
+                      : p.o + (int64_t(t) * p.H + h) * DV;
+  const bool have_old = merge_old && live && !is_neg_inf(old);
+  tc_fence_after();
+  const bool store = ok && live;
+  float lse = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : neg_inf();
+  float w_new = (l > 0.f) ? 1.f / l : 0.f, w_old = 0.f;
+  float *lse_dst = split ? p.split_lse + (int64_t(slot) * p.H + h) * BQ + (qpos & (BQ - 1))
+                         : p.lse + li;
+  bool write = store;
+  if (store && merge_old) {
+    if (l == 0.f) {
+      if (!fin) {
+        write = false;  // nothing new: keep the stored partial
+      } else if (!is_neg_inf(old)) {
+        w_old = 1.f;  // the result is the context partial alone
+        lse = old;
+      }
+    } else if (!is_neg_inf(old)) {
+      const float m2 = fmaxf(old, lse);
+      const float eo = expf(old - m2), en = expf(lse - m2);
+      w_old = eo / (eo + en);
+      w_new *= en / (eo + en);
+      lse = m2 + logf(eo + en);
+    }
+  }
+  if (ok && n_tiles > 0) {
+    // four pieces of 32 columns; the stored row's piece is loaded before
+    // the TMEM read of the same piece
+#pragma unroll 1
+    for (int c = 0; c < DV / 32; ++c) {
+      float4 ov[8];
+      if (have_old && w_old != 0.f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ov[i] = reinterpret_cast<const float4 *>(orow + c * 32)[i];
+      }
+      uint32_t r[32];
+      tmem_ld32(o_col + uint32_t(c * 32), r);
+      tmem_wait_ld();
+      if (c == DV / 32 - 1) {
+        // O is read: the warpgroup's next unit may accumulate into it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_ofree);
+      }
+      if (write) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float4 o4 = make_float4(__uint_as_float(r[4 * e]) * w_new,
+                                  __uint_as_float(r[4 * e + 1]) * w_new,
+                                  __uint_as_float(r[4 * e + 2]) * w_new,
+                                  __uint_as_float(r[4 * e + 3]) * w_new);
+          if (w_old != 0.f) {  // only when the stored LSE is finite (have_old)
+            o4.x += w_old * ov[e].x;
+            o4.y += w_old * ov[e].y;
+            o4.z += w_old * ov[e].z;
+            o4.w += w_old * ov[e].w;
+          }
+          const int64_t col = (int64_t(t) * p.H + h) * DV + c * 32 + e * 4;
+          if (!fin) {
+            reinterpret_cast<float4 *>(orow + c * 32)[e] = o4;
+          } else if (p.fout_bf16) {
+            uint2 b2;
+            b2.x = pack_bf16(o4.x, o4.y);
+            b2.y = pack_bf16(o4.z, o4.w);
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + col) = b2;
+          } else {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + col) = o4;
+          }
+        }
+      }
+    }
+  } else {
+    if (n_tiles > 0) {  // O unread (a wait gave up): release it all the same
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_ofree);
+    }
+    if (write && n_tiles == 0) {
+      if (!fin) {
+        // no key (an accumulating row kept its partial: write is false)
+        for (int c = 0; c < DV; c += 4)
+          *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        // no key: the context partial passes through (w_old = 1), or zeros
+        for (int c = 0; c < DV; c += 4) {
+          float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (w_old != 0.f) o4 = reinterpret_cast<const float4 *>(orow)[c / 4];
+          const int64_t col = (int64_t(t) * p.H + h) * DV + c;
+          if (p.fout_bf16) {
+            uint2 b2;
+            b2.x = pack_bf16(o4.x, o4.y);
+            b2.y = pack_bf16(o4.z, o4.w);
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + col) = b2;
+          } else {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + col) = o4;
+          }
+        }
+      }
+    }
+  }
+  if (write) {
+    if (!fin)
+      *lse_dst = lse;
+    else if (p.flse)
+      p.flse[li] = lse;
+  }
+  return ok;
+}
 
 __global__ void __launch_bounds__(THREADS_LOOP, 1)
     attn_tc_loop_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -628,17 +860,16 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + Q_BYTES;
   uint8_t *sV = sK + RING * K_BYTES;
-  float *xchg0 = reinterpret_cast<float *>(sV + RING * V_BYTES);  // [2 unit parities][4][128]
-  uint64_t *bars =
-      reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg0) + 2 * XCHG_BYTES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sV + RING * V_BYTES + XCHG_BYTES);
   const uint32_t b_q = smem_u32(bars + 0), b_qready = smem_u32(bars + 1);
   const uint32_t b_kfull = smem_u32(bars + 2), b_kempty = smem_u32(bars + 2 + RING);
   const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
   const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);  // [2]: per S buffer
   const uint32_t b_pfull = b_sfull + 16;                    // [2]: per warpgroup
-  const uint32_t b_odone = b_sfull + 32, b_done = b_sfull + 40;
-  const uint32_t b_qfree = b_sfull + 48, b_ofree = b_sfull + 56;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 8);
+  const uint32_t b_odone = b_sfull + 32;                    // [2]: per warpgroup
+  const uint32_t b_ofree = b_sfull + 48;                    // [2]: per warpgroup
+  const uint32_t b_qfree = b_sfull + 64, b_done = b_sfull + 72;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 10);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_units = p.n_items * p.H;
@@ -655,11 +886,11 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
     for (int w = 0; w < 2; ++w) {
       mbar_init(b_sfull + 8 * w, 1);
       mbar_init(b_pfull + 8 * w, 4);
+      mbar_init(b_odone + 8 * w, 1);
+      mbar_init(b_ofree + 8 * w, 4);
     }
-    mbar_init(b_odone, 1);
-    mbar_init(b_done, 1);
     mbar_init(b_qfree, 1);
-    mbar_init(b_ofree, 8);
+    mbar_init(b_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -723,11 +954,11 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
             ok = false;
             break;
           }
-          uint8_t *k = sK + s * K_BYTES;
+          uint8_t *kk = sK + s * K_BYTES;
           mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
-          tma_load_3d(smem_u32(k), &tm_kv, b_kfull + 8 * s, 0, krow, x.h);
-          tma_load_3d(smem_u32(k + KBOX), &tm_kv, b_kfull + 8 * s, 64, krow, x.h);
-          tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, b_kfull + 8 * s, 512, krow);
+          tma_load_3d(smem_u32(kk), &tm_kv, b_kfull + 8 * s, 0, krow, x.h);
+          tma_load_3d(smem_u32(kk + KBOX), &tm_kv, b_kfull + 8 * s, 64, krow, x.h);
+          tma_load_2d(smem_u32(kk + 2 * KBOX), &tm_lat, b_kfull + 8 * s, 512, krow);
           k_issued[s] = int(use & 1);
           if (J >= RING && !mbar_wait(b_vempty + 8 * s, (use - 1) & 1)) {
             ok = false;
@@ -754,14 +985,16 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       constexpr uint32_t idesc_rope = idesc_f16kind(BQ, BKV, false, false, true);   // bf16
       constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
       const uint32_t q_addr = smem_u32(sQ);
-      int J0 = 0, kq = 0;
+      int J0 = 0, kq = 0, ku = 0;
+      int jw[2] = {0, 0}, uw[2] = {0, 0};   // per warpgroup: P.V tiles, units with tiles
       bool ok = true;
-      for (int k = 0; ok; ++k) {
+      for (int k = 0; ok; ++k, ++ku) {
         const int u = unit_at(k);
         if (u >= n_units) break;
         const Unit x = unit_of(u);
         const int n_tiles = x.n_tiles;
         if (n_tiles <= 0) continue;
+        const int w = ku & 1;              // the warpgroup that owns this unit
         if (!mbar_wait(b_qready, uint32_t(kq & 1))) break;
         // S for key tile J into S buffer J & 1 (which held P of tile J-2,
         // whose P.V MMAs were issued before); after the unit's last S the
@@ -771,49 +1004,43 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
           if (!mbar_wait(b_kfull + 8 * s, uint32_t((J / RING) & 1))) return false;
           tc_fence_after();
           const uint32_t k_addr = smem_u32(sK + s * K_BYTES);
-          const uint32_t d = tmem + COL_S + uint32_t(s * BKV);
+          const uint32_t d = tmem + COL_S + uint32_t((J & 1) * BKV);
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = uint32_t((kk >> 2) * QBOX + (kk & 3) * 32);
             mma_bf16(d, desc_kmajor_sw128(q_addr + off), desc_kmajor_sw128(k_addr + off),
                      kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
           }
-          mma_commit(b_sfull + 8 * s);
+          mma_commit(b_sfull + 8 * (J & 1));
           mma_commit(b_kempty + 8 * s);
           if (j == n_tiles - 1) mma_commit(b_qfree);
           return true;
         };
         ok = issue_s(0);
         if (ok && n_tiles > 1) ok = issue_s(1);
-        // the previous unit's epilogue has read O_A and O_B
-        if (ok && kq > 0 && !mbar_wait(b_ofree, uint32_t((kq - 1) & 1))) ok = false;
+        // the warpgroup's previous unit's epilogue has read its O
+        if (ok && uw[w] > 0 && !mbar_wait(b_ofree + 8 * w, uint32_t((uw[w] - 1) & 1))) ok = false;
+        const uint32_t od = tmem + COL_O + uint32_t(w * DV);
         for (int j = 0; ok && j < n_tiles; ++j) {
           const int J = J0 + j, s = J % RING;
-          if (!mbar_wait(b_vfull + 8 * s, uint32_t((J / RING) & 1))) {
+          if (!mbar_wait(b_vfull + 8 * s, uint32_t((J / RING) & 1)) ||
+              !mbar_wait(b_pfull + 8 * w, uint32_t(jw[w] & 1))) {
             ok = false;
             break;
           }
-          const uint32_t v_addr = smem_u32(sV + s * V_BYTES);
-          for (int w = 0; w < 2 && ok; ++w) {
-            if (!mbar_wait(b_pfull + 8 * w, uint32_t(J & 1))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t pa = tmem + COL_S + uint32_t(s * BKV + w * HALF);
-            const uint32_t vb = v_addr + uint32_t(w * HALF * 128);
-            const uint32_t od = tmem + COL_O + uint32_t(w * DV);
+          tc_fence_after();
+          const uint32_t pa = tmem + COL_S + uint32_t((J & 1) * BKV);
+          const uint32_t vb = smem_u32(sV + s * V_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < HALF / 16; ++kk)
-              mma_f16_ts(od, pa + uint32_t(kk * 8),
-                         desc_mnmajor_sw128(vb + uint32_t(kk * 2048), KBOX), idesc_o,
-                         (j | kk) != 0);
-          }
-          if (!ok) break;
-          mma_commit(b_odone);
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            mma_f16_ts(od, pa + uint32_t(kk * 8), desc_mnmajor_sw128(vb + uint32_t(kk * 2048), KBOX),
+                       idesc_o, (j | kk) != 0);
+          mma_commit(b_odone + 8 * w);
           mma_commit(b_vempty + 8 * s);
+          ++jw[w];
           if (j + 2 < n_tiles) ok = issue_s(j + 2);
         }
+        ++uw[w];
         J0 += n_tiles;
         ++kq;
       }
@@ -836,34 +1063,51 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       if (!ok) break;
     }
   } else {
-    // ---------------- softmax warpgroups
-    const int wg = (warp - 2) >> 2;        // 0: A (keys 0-63 of a tile), 1: B (64-127)
+    // ---------------- softmax warpgroups, on alternate units
+    const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;   // query row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const uint32_t o_col = tmem + lane_off + COL_O + uint32_t(wg * DV);
-    int J0 = 0, ku = 0;                    // key tiles and units so far
+    int J0 = 0, jw = 0;                    // the CTA's key tiles; this warpgroup's
     bool ok = true;
-    for (int k = 0;; ++k, ++ku) {
+    for (int k = 0, ku = 0;; ++k, ++ku) {
       const int u = unit_at(k);
       if (u >= n_units) break;
       const Unit x = unit_of(u);
+      const int n_tiles = x.n_tiles > 0 ? x.n_tiles : 0;
+      if ((ku & 1) != wg) {
+        J0 += n_tiles;
+        continue;
+      }
       const int q_beg = __ldg(p.q_loc + x.seq), nq = __ldg(p.q_loc + x.seq + 1) - q_beg;
       const int nk = __ldg(p.k_loc + x.seq + 1) - __ldg(p.k_loc + x.seq);
       const int qpos = x.qt * BQ + row;    // position within the sequence
       float m_used = neg_inf(), l = 0.f;
-      prefetch_partial(p, x.h, x.seq, x.slot, q_beg, nq, qpos, wg);
-      for (int j = 0; ok && j < x.n_tiles; ++j) {
-        const int J = J0 + j, s = J % RING;
-        const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(s * BKV + wg * HALF);
-        ok = softmax_tile(p, s_col, o_col, b_sfull + 8 * s, uint32_t((J / RING) & 1), b_odone,
-                          b_pfull + 8 * wg, J, (x.kt0 + j) * BKV + wg * HALF, nk, qpos, m_used,
-                          l, lane);
+      if (qpos < nq && x.slot < 0) {
+        // the stored row the epilogue may merge with, into L2 meanwhile
+        const int t = q_beg + qpos;
+        const bool fin = p.fout != nullptr;
+        const bool acc = !fin && p.acc != nullptr && __ldg(p.acc + x.seq) != 0;
+        if (acc || (fin && t < p.pnt)) {
+          const float *r = p.o + (int64_t(t) * p.H + x.h) * DV;
+#pragma unroll
+          for (int c = 0; c < DV; c += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(r + c));
+        }
       }
-      ok = unit_epilogue<true>(p, tmem, lane_off, xchg0 + (ku & 1) * (XCHG_BYTES / 4), b_odone,
-                               uint32_t((J0 + x.n_tiles - 1) & 1), b_ofree, wg, row, lane, x.h,
-                               x.seq, x.slot, q_beg, nq, qpos, x.n_tiles, m_used, l, ok);
-      if (x.n_tiles > 0) J0 += x.n_tiles;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int J = J0 + j;
+        const uint32_t s_col = tmem + lane_off + COL_S + uint32_t((J & 1) * BKV);
+        ok = softmax_tile_full(p, s_col, o_col, b_sfull + 8 * (J & 1), uint32_t((J >> 1) & 1),
+                               b_odone + 8 * wg, b_pfull + 8 * wg, jw, (x.kt0 + j) * BKV, nk,
+                               qpos, m_used, l, lane);
+        ok = __all_sync(0xffffffffu, ok) != 0;
+        ++jw;
+      }
+      ok = unit_epilogue_full(p, o_col, b_odone + 8 * wg, uint32_t((jw - 1) & 1),
+                              b_ofree + 8 * wg, lane, x.h, x.seq, x.slot, q_beg, nq, qpos,
+                              n_tiles, m_used, l, ok);
+      J0 += n_tiles;
     }
   }
   tc_fence_before();
