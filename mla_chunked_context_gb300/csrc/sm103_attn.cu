@@ -169,14 +169,19 @@ __device__ __forceinline__ void prefetch_partial(const AttnParams &p, int h, int
 // TMEM (s_col), masked past the sequence (and, causal, past the query),
 // running max in base 2 raised lazily, P as fp16 over the S columns, O
 // (o_col) rescaled when the max grew -- after the previous tile's P.V (tile
-// J-1 of the CTA) is done -- then an arrival on pfull_bar.  Returns false
-// when a wait gave up.
+// J-1 of the CTA) is done -- then an arrival on pfull_bar.  The P.V of tile
+// J commits to done barrier J % 2 (b_odone + 8 * (J % 2)), and the MMA
+// thread observes the P.V of tile J-2 before it issues that of tile J, so a
+// wait for tile J-1 is one phase from its barrier's state either way: it
+// is only made when this warp rescales O.  Returns false when a wait gave
+// up.
 __device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col, uint32_t o_col,
                                              uint32_t sfull_bar, uint32_t sfull_parity,
                                              uint32_t b_odone, uint32_t pfull_bar, int J,
                                              int k0, int nk, int qpos, float &m_used, float &l,
                                              int lane) {
-  if (!mbar_wait(sfull_bar, sfull_parity)) return false;
+  // every exit is taken by the whole warp (its TMEM accesses are warp-wide)
+  if (!__all_sync(0xffffffffu, mbar_wait(sfull_bar, sfull_parity))) return false;
   tc_fence_after();
   float sv[HALF];  // raw scores (scale applied below)
   {
@@ -230,14 +235,17 @@ __device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col
     pk[e] = pack_f16(a, b);
   }
   l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-  // P over this warpgroup's own S columns (already read).  The previous
-  // tile's P.V must have finished before O is rescaled; waiting for it on
-  // every tile costs nothing (this tile's P.V runs after it anyway) and
-  // keeps the waits on the done barrier one phase apart.
+  // P over this warpgroup's own S columns (already read).  Only when O must
+  // be rescaled does the warp wait for the previous tile's P.V (the P.V of
+  // this tile cannot be issued before this warp arrives, so the barrier of
+  // tile J-1 is at most one phase ahead); otherwise this tile's P.V is
+  // issued while the previous one may still run.
   tmem_st32(s_col, pk);
-  if (J > 0 && !mbar_wait(b_odone, uint32_t((J - 1) & 1))) return false;
-  tc_fence_after();
   if (__any_sync(0xffffffffu, rescale)) {
+    const bool done =
+        J == 0 || mbar_wait(b_odone + 8u * uint32_t((J - 1) & 1), uint32_t(((J - 1) >> 1) & 1));
+    if (!__all_sync(0xffffffffu, done)) return false;
+    tc_fence_after();
 #pragma unroll 1
     for (int c = 0; c < DV / 32; ++c) {
       uint32_t r[32];
@@ -337,6 +345,7 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
 #pragma unroll
     for (int c = 0; c < DV / 2 / 16; ++c) {
       uint32_t ra[16], rb[16];
+      __syncwarp();  // converged after the per-lane stores of the previous piece
       tmem_ld16(oa + uint32_t(c * 16), ra);
       tmem_ld16(ob + uint32_t(c * 16), rb);
       tmem_wait_ld();
@@ -417,8 +426,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
   const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);  // [2]: per S buffer
   const uint32_t b_pfull = b_sfull + 16;                    // [2]: per warpgroup
-  const uint32_t b_odone = b_sfull + 32, b_done = b_sfull + 40;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 6);
+  const uint32_t b_odone = b_sfull + 32, b_done = b_sfull + 48;  // odone: [2], per tile parity
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 7);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x / p.n_items;
@@ -445,6 +454,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(b_pfull + 8 * w, 4);
     }
     mbar_init(b_odone, 1);
+    mbar_init(b_odone + 8, 1);
     mbar_init(b_done, 1);
     fence_mbar_init();
   }
@@ -523,7 +533,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok && n_tiles > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int s = j % RING;
-        if (!mbar_wait(b_vfull + 8 * s, uint32_t((j / RING) & 1))) {
+        // the P.V of tile j-2 (the last user of done barrier j % 2) has
+        // finished: long done by now, and it keeps every wait on that
+        // barrier one phase from its state
+        if (!mbar_wait(b_vfull + 8 * s, uint32_t((j / RING) & 1)) ||
+            (j >= 2 && !mbar_wait(b_odone + 8 * (j & 1), uint32_t(((j - 2) >> 1) & 1)))) {
           ok = false;
           break;
         }
@@ -545,7 +559,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                        (j | kk) != 0);
         }
         if (!ok) break;
-        mma_commit(b_odone);
+        mma_commit(b_odone + 8 * (j & 1));
         mma_commit(b_vempty + 8 * s);
         if (j + 2 < n_tiles) ok = issue_s(j + 2);
       }
@@ -578,8 +592,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         b_pfull + 8 * wg, j, (kt0 + j) * BKV + wg * HALF, nk, qpos, m_used, l,
                         lane);
     }
-    unit_epilogue(p, tmem, lane_off, xchg, b_odone, uint32_t((n_tiles - 1) & 1), 0u, wg, row,
-                  lane, h, seq, slot, q_beg, nq, qpos, n_tiles, m_used, l, ok);
+    // the unit's last P.V: done barrier (n_tiles-1) % 2, its ((n_tiles-1)/2)-th phase
+    unit_epilogue(p, tmem, lane_off, xchg, b_odone + 8u * uint32_t((n_tiles - 1) & 1),
+                  uint32_t(((n_tiles - 1) >> 1) & 1), 0u, wg, row, lane, h, seq, slot, q_beg, nq,
+                  qpos, n_tiles, m_used, l, ok);
   }
   if (warp < 2) __syncthreads_and(1);  // matches the softmax warps' vote
   tc_fence_before();
@@ -622,13 +638,15 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
                                                   uint32_t sfull_parity, uint32_t b_odone,
                                                   uint32_t pfull_bar, int jw, int k0, int nk,
                                                   int qpos, float &m_used, float &l, int lane) {
-  if (!mbar_wait(sfull_bar, sfull_parity)) return false;
+  // every exit is taken by the whole warp (its TMEM accesses are warp-wide)
+  if (!__all_sync(0xffffffffu, mbar_wait(sfull_bar, sfull_parity))) return false;
   tc_fence_after();
   float alpha = 1.f;
   bool rescale = false;
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     float sv[HALF];
+    __syncwarp();  // tcgen05.ld/st are warp-wide: the warp is converged here
     {
       uint32_t r0[32], r1[32];
       tmem_ld32(s_col + uint32_t(hh * HALF), r0);
@@ -656,6 +674,7 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
 #pragma unroll
       for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
     const float mx = tm[0] * p.scale_log2;
+    float a_first = 1.f;  // this lane's rescale of the tile's first half of P
     if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
       const float m_new = fmaxf(mx, m_used);
       if (m_used != neg_inf() && m_new != neg_inf()) {
@@ -663,22 +682,25 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
         alpha *= a;
         l *= a;
         rescale = true;
-        if (hh == 1) {
-          // the first half's P was exponentiated against the old max
-          uint32_t r[32];
-          tmem_wait_st();
-          tmem_ld32(s_col, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const __half2 h2 = *reinterpret_cast<const __half2 *>(&r[e]);
-            const float2 f = __half22float2(h2);
-            r[e] = pack_f16(f.x * a, f.y * a);
-          }
-          tmem_st32(s_col, r);
-        }
+        if (hh == 1) a_first = a;
       }
       m_used = m_new;
+    }
+    if (hh == 1 && __any_sync(0xffffffffu, a_first != 1.f)) {
+      // the first half's P was exponentiated against the old max (rows
+      // whose max did not move multiply by 1, exactly); the whole warp
+      // takes part in the TMEM read and write
+      uint32_t r[32];
+      tmem_wait_st();
+      tmem_ld32(s_col, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const __half2 h2 = *reinterpret_cast<const __half2 *>(&r[e]);
+        const float2 f = __half22float2(h2);
+        r[e] = pack_f16(f.x * a_first, f.y * a_first);
+      }
+      tmem_st32(s_col, r);
     }
     const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
     uint32_t pk[HALF / 2];
@@ -694,10 +716,12 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
     // P of keys [hh*64, hh*64+64) over columns [hh*32, hh*32+32): those S
     // columns are already read (the first half was read before it is
     // overwritten; the second half's own columns lie beyond 64)
+    __syncwarp();
     tmem_st32(s_col + uint32_t(hh * 32), pk);
   }
   // the warpgroup's previous P.V into O has finished before O is rescaled
-  if (jw > 0 && !mbar_wait(b_odone, uint32_t((jw - 1) & 1))) return false;
+  if (!__all_sync(0xffffffffu, jw == 0 || mbar_wait(b_odone, uint32_t((jw - 1) & 1))))
+    return false;
   tc_fence_after();
   if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
@@ -776,6 +800,7 @@ __device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t
         for (int i = 0; i < 8; ++i) ov[i] = reinterpret_cast<const float4 *>(orow + c * 32)[i];
       }
       uint32_t r[32];
+      __syncwarp();  // converged again after the per-lane loads above
       tmem_ld32(o_col + uint32_t(c * 32), r);
       tmem_wait_ld();
       if (c == DV / 32 - 1) {

@@ -460,6 +460,42 @@ def test_varlen_attention_many_short_units(causal):
         assert_close(f64(lse), rl2, 1e-3, what="LSE accumulated")
 
 
+@pytest.mark.parametrize("heads,ql,kl", [(4, [130, 5], [1000, 300]),
+                                         (64, [130, 1, 77, 40, 9, 128], [500, 3, 129, 256, 64, 400])])
+def test_varlen_attention_running_max_rescales(heads, ql, kl):
+    """Keys whose K_nope grows every 64 keys, so the running max of a row
+    rises by more than 2^8 again and again, inside a tile and from tile to
+    tile: O is rescaled (after the previous P.V) and, in the looping kernel,
+    the first half of a tile's P is rescaled when the second half raises the
+    max.  4 heads: one CTA per unit; 64 heads and short sequences: the
+    looping kernel."""
+    w = W.scaled(W.workload("uniform"), num_heads=heads, seed=47)
+    q_loc = [0] + list(np.cumsum(ql))
+    k_loc = [0] + list(np.cumsum(kl))
+    q, kv, lat = _attn_inputs(w, k_loc[-1], q_loc[-1], 11, torch.float16)
+    grow = torch.ones(k_loc[-1])
+    for i in range(len(kl)):
+        j = torch.arange(kl[i], dtype=torch.float32)
+        grow[k_loc[i]:k_loc[i + 1]] = 1.0 + 0.75 * (j // 64)
+    kv = kv.float()
+    kv[:, :, :128] *= grow[None, :, None]
+    kv = kv.to(torch.float16)
+    o = torch.full((q_loc[-1], heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((heads, q_loc[-1]), float("nan"), device=DEV)
+    M.mla_varlen_attn(M.Dims.of(w), False, q_loc, k_loc, q.to(DEV), kv.to(DEV), lat.to(DEV), o,
+                      lse)
+    torch.cuda.synchronize()
+    ro, rl = _oracle_attn(w, q, kv, lat, q_loc, k_loc, False)
+    # the scores really do grow by more than 2^8 (base 2) between the first
+    # and the last 64 keys of the longest sequence
+    kvr = f64(kv).transpose(1, 0, 2)
+    qn = f64(q[:ql[0]])
+    s = np.einsum("mhd,nhd->hmn", qn[:, :, :128], kvr[:kl[0], :, :128]) * w.softmax_scale
+    assert (s[:, :, -64:].max(axis=2) - s[:, :, :64].max(axis=2)).mean() / math.log(2) > 8
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_varlen_attention_accumulate():
     """Chunk 2 continues the requests of chunk 1 and merges into its partial;
     the result equals attention over both key ranges at once."""
