@@ -425,9 +425,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t b_kfull = smem_u32(bars + 2), b_kempty = smem_u32(bars + 2 + RING);
   const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
   const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);  // [2]: per S buffer
-  const uint32_t b_pfull = b_sfull + 16;                    // [2]: per warpgroup
-  const uint32_t b_odone = b_sfull + 32, b_done = b_sfull + 48;  // odone: [2], per tile parity
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 7);
+  // pfull: [2 warpgroups][2 tile parities] -- a warpgroup may write the P of
+  // tile j+1 before the MMA thread has taken tile j's (it no longer waits
+  // for the previous P.V), but not that of tile j+2 (its S needs the P.V of
+  // tile j issued), so each barrier is at most one phase ahead of its waiter
+  const uint32_t b_pfull = b_sfull + 16;
+  const uint32_t b_odone = b_sfull + 48, b_done = b_sfull + 64;  // odone: [2], per tile parity
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 9);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x / p.n_items;
@@ -451,7 +455,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(b_sfull + 8 * w, 1);
-      mbar_init(b_pfull + 8 * w, 4);
+      mbar_init(b_pfull + 16 * w, 4);
+      mbar_init(b_pfull + 16 * w + 8, 4);
     }
     mbar_init(b_odone, 1);
     mbar_init(b_odone + 8, 1);
@@ -543,7 +548,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const uint32_t v_addr = smem_u32(sV + s * V_BYTES);
         for (int w = 0; w < 2 && ok; ++w) {
-          if (!mbar_wait(b_pfull + 8 * w, uint32_t(j & 1))) {
+          if (!mbar_wait(b_pfull + 16 * w + 8 * (j & 1), uint32_t((j >> 1) & 1))) {
             ok = false;
             break;
           }
@@ -589,7 +594,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int s = j % RING;
       const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(s * BKV + wg * HALF);
       ok = softmax_tile(p, s_col, o_col, b_sfull + 8 * s, uint32_t((j / RING) & 1), b_odone,
-                        b_pfull + 8 * wg, j, (kt0 + j) * BKV + wg * HALF, nk, qpos, m_used, l,
+                        b_pfull + 16 * wg + 8 * (j & 1), j, (kt0 + j) * BKV + wg * HALF, nk,
+                        qpos, m_used, l,
                         lane);
     }
     // the unit's last P.V: done barrier (n_tiles-1) % 2, its ((n_tiles-1)/2)-th phase
@@ -889,12 +895,16 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   const uint32_t b_q = smem_u32(bars + 0), b_qready = smem_u32(bars + 1);
   const uint32_t b_kfull = smem_u32(bars + 2), b_kempty = smem_u32(bars + 2 + RING);
   const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
-  const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);  // [2]: per S buffer
-  const uint32_t b_pfull = b_sfull + 16;                    // [2]: per warpgroup
-  const uint32_t b_odone = b_sfull + 32;                    // [2]: per warpgroup
-  const uint32_t b_ofree = b_sfull + 48;                    // [2]: per warpgroup
-  const uint32_t b_qfree = b_sfull + 64, b_done = b_sfull + 72;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 10);
+  // sfull: [2 warpgroups][2 S buffers] -- the S MMA of a tile arrives on its
+  // owner's barrier for that buffer, so each warpgroup sees every phase of
+  // its barriers in order (a barrier shared by both would let a warpgroup
+  // that skipped the other's phases take an old phase for the new one)
+  const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);
+  const uint32_t b_pfull = b_sfull + 32;                    // [2]: per warpgroup
+  const uint32_t b_odone = b_sfull + 48;                    // [2]: per warpgroup
+  const uint32_t b_ofree = b_sfull + 64;                    // [2]: per warpgroup
+  const uint32_t b_qfree = b_sfull + 80, b_done = b_sfull + 88;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 12);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_units = p.n_items * p.H;
@@ -909,7 +919,8 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       mbar_init(b_vempty + 8 * s, 1);
     }
     for (int w = 0; w < 2; ++w) {
-      mbar_init(b_sfull + 8 * w, 1);
+      mbar_init(b_sfull + 16 * w, 1);
+      mbar_init(b_sfull + 16 * w + 8, 1);
       mbar_init(b_pfull + 8 * w, 4);
       mbar_init(b_odone + 8 * w, 1);
       mbar_init(b_ofree + 8 * w, 4);
@@ -1036,7 +1047,7 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
             mma_bf16(d, desc_kmajor_sw128(q_addr + off), desc_kmajor_sw128(k_addr + off),
                      kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
           }
-          mma_commit(b_sfull + 8 * (J & 1));
+          mma_commit(b_sfull + 16 * w + 8 * (J & 1));
           mma_commit(b_kempty + 8 * s);
           if (j == n_tiles - 1) mma_commit(b_qfree);
           return true;
@@ -1095,6 +1106,7 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const uint32_t o_col = tmem + lane_off + COL_O + uint32_t(wg * DV);
     int J0 = 0, jw = 0;                    // the CTA's key tiles; this warpgroup's
+    int sc0 = 0, sc1 = 0;                  // this warpgroup's tiles in S buffer 0 / 1
     bool ok = true;
     for (int k = 0, ku = 0;; ++k, ++ku) {
       const int u = unit_at(k);
@@ -1123,9 +1135,10 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int J = J0 + j;
         const uint32_t s_col = tmem + lane_off + COL_S + uint32_t((J & 1) * BKV);
-        ok = softmax_tile_full(p, s_col, o_col, b_sfull + 8 * (J & 1), uint32_t((J >> 1) & 1),
-                               b_odone + 8 * wg, b_pfull + 8 * wg, jw, (x.kt0 + j) * BKV, nk,
-                               qpos, m_used, l, lane);
+        const int sc = (J & 1) ? sc1++ : sc0++;
+        ok = softmax_tile_full(p, s_col, o_col, b_sfull + 16 * wg + 8 * (J & 1),
+                               uint32_t(sc & 1), b_odone + 8 * wg, b_pfull + 8 * wg, jw,
+                               (x.kt0 + j) * BKV, nk, qpos, m_used, l, lane);
         ok = __all_sync(0xffffffffu, ok) != 0;
         ++jw;
       }
