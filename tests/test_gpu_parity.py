@@ -476,7 +476,7 @@ def test_varlen_attention_running_max_rescales(heads, ql, kl):
     grow = torch.ones(k_loc[-1])
     for i in range(len(kl)):
         j = torch.arange(kl[i], dtype=torch.float32)
-        grow[k_loc[i]:k_loc[i + 1]] = 1.0 + 0.75 * (j // 64)
+        grow[k_loc[i]:k_loc[i + 1]] = 1.0 + 1.5 * (j // 64)
     kv = kv.float()
     kv[:, :, :128] *= grow[None, :, None]
     kv = kv.to(torch.float16)
