@@ -112,18 +112,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Non-blocking test for the completion of the phase of parity `parity`.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // 16 consecutive 32-bit TMEM columns of the warp's 32 lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -1029,112 +1017,68 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      // Two cursors walk the CTA's tiles in order: the S cursor issues S of
-      // tile Js once the unit's Q is ready (qready), its K landed and S
-      // buffer Js % 2 is free (the P.V of tile Js-2 issued); the P.V cursor
-      // issues tile Jp's P.V once its S was issued, its V landed, its
-      // warpgroup wrote P (pfull) and, at a unit's first tile, that
-      // warpgroup's previous epilogue read O (ofree).  The thread polls
-      // both (test_wait, no blocking), so the next unit's S -- and with it
-      // the other warpgroup's softmax -- goes ahead while this unit's P is
-      // still being written.  Each barrier's phases are tested in order,
-      // and none can run two phases ahead of its tester (see the cursors'
-      // conditions), so a test is never fooled by an old phase.
       constexpr uint32_t idesc_nope = idesc_f16kind(BQ, BKV, false, false, false);  // fp16
       constexpr uint32_t idesc_rope = idesc_f16kind(BQ, BKV, false, false, true);   // bf16
       constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
       const uint32_t q_addr = smem_u32(sQ);
-      struct Cursor {
-        int k, ku, kq;  // CTA unit index; units so far (all / with key tiles)
-        int j, J;       // tile within the unit; the CTA's tile index
-        int n, w;       // the unit's key tiles; its warpgroup
-        bool live;
-      };
-      // from c.k on, the next unit with key tiles
-      auto seek = [&](Cursor &c) {
-        for (;; ++c.k, ++c.ku) {
-          const int u = unit_at(c.k);
-          if (u >= n_units) {
-            c.live = false;
-            return;
-          }
-          const Unit x = unit_of(u);
-          if (x.n_tiles > 0) {
-            c.n = x.n_tiles;
-            c.w = c.ku & 1;
-            c.j = 0;
-            c.live = true;
-            return;
-          }
-        }
-      };
-      auto step = [&](Cursor &c) {
-        ++c.J;
-        if (++c.j == c.n) {
-          ++c.k;
-          ++c.ku;
-          ++c.kq;
-          seek(c);
-        }
-      };
-      Cursor cs{0, 0, 0, 0, 0, 0, 0, false}, cp{0, 0, 0, 0, 0, 0, 0, false};
-      seek(cs);
-      seek(cp);
-      int jw0 = 0, jw1 = 0, uw0 = 0, uw1 = 0;  // per warpgroup: P.V tiles, finished units
+      int J0 = 0, kq = 0, ku = 0;
+      int jw[2] = {0, 0}, uw[2] = {0, 0};   // per warpgroup: P.V tiles, units with tiles
       bool ok = true;
-      long long idle_since = clock64();
-      while (ok && (cs.live || cp.live)) {
-        bool progress = false;
-        if (cs.live && cs.J < cp.J + 2 && (cs.j > 0 || mbar_test(b_qready, uint32_t(cs.kq & 1))) &&
-            mbar_test(b_kfull + 8 * (cs.J % RING), uint32_t((cs.J / RING) & 1))) {
+      for (int k = 0; ok; ++k, ++ku) {
+        const int u = unit_at(k);
+        if (u >= n_units) break;
+        const Unit x = unit_of(u);
+        const int n_tiles = x.n_tiles;
+        if (n_tiles <= 0) continue;
+        const int w = ku & 1;              // the warpgroup that owns this unit
+        if (!mbar_wait(b_qready, uint32_t(kq & 1))) break;
+        // S for key tile J into S buffer J & 1 (which held P of tile J-2,
+        // whose P.V MMAs were issued before); after the unit's last S the
+        // Q tile is released
+        auto issue_s = [&](int j) -> bool {
+          const int J = J0 + j, s = J % RING;
+          if (!mbar_wait(b_kfull + 8 * s, uint32_t((J / RING) & 1))) return false;
           tc_fence_after();
-          const int sl = cs.J % RING;
-          const uint32_t k_addr = smem_u32(sK + sl * K_BYTES);
-          const uint32_t d = tmem + COL_S + uint32_t((cs.J & 1) * BKV);
+          const uint32_t k_addr = smem_u32(sK + s * K_BYTES);
+          const uint32_t d = tmem + COL_S + uint32_t((J & 1) * BKV);
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = uint32_t((kk >> 2) * QBOX + (kk & 3) * 32);
             mma_bf16(d, desc_kmajor_sw128(q_addr + off), desc_kmajor_sw128(k_addr + off),
                      kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
           }
-          mma_commit(b_sfull + 16 * cs.w + 8 * (cs.J & 1));
-          mma_commit(b_kempty + 8 * sl);
-          if (cs.j == cs.n - 1) mma_commit(b_qfree);  // the unit's last S: Q is free
-          step(cs);
-          progress = true;
-        }
-        if (cp.live && cp.J < cs.J) {
-          const int w = cp.w;
-          const int jw = w ? jw1 : jw0, uw = w ? uw1 : uw0;
-          if (mbar_test(b_vfull + 8 * (cp.J % RING), uint32_t((cp.J / RING) & 1)) &&
-              mbar_test(b_pfull + 8 * w, uint32_t(jw & 1)) &&
-              (cp.j > 0 || uw == 0 || mbar_test(b_ofree + 8 * w, uint32_t((uw - 1) & 1)))) {
-            tc_fence_after();
-            const int sl = cp.J % RING;
-            const uint32_t od = tmem + COL_O + uint32_t(w * DV);
-            const uint32_t pa = tmem + COL_S + uint32_t((cp.J & 1) * BKV);
-            const uint32_t vb = smem_u32(sV + sl * V_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < BKV / 16; ++kk)
-              mma_f16_ts(od, pa + uint32_t(kk * 8),
-                         desc_mnmajor_sw128(vb + uint32_t(kk * 2048), KBOX), idesc_o,
-                         (cp.j | kk) != 0);
-            mma_commit(b_odone + 8 * w);
-            mma_commit(b_vempty + 8 * sl);
-            if (w) ++jw1; else ++jw0;
-            if (cp.j == cp.n - 1) {
-              if (w) ++uw1; else ++uw0;
-            }
-            step(cp);
-            progress = true;
+          mma_commit(b_sfull + 16 * w + 8 * (J & 1));
+          mma_commit(b_kempty + 8 * s);
+          if (j == n_tiles - 1) mma_commit(b_qfree);
+          return true;
+        };
+        ok = issue_s(0);
+        if (ok && n_tiles > 1) ok = issue_s(1);
+        // the warpgroup's previous unit's epilogue has read its O
+        if (ok && uw[w] > 0 && !mbar_wait(b_ofree + 8 * w, uint32_t((uw[w] - 1) & 1))) ok = false;
+        const uint32_t od = tmem + COL_O + uint32_t(w * DV);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int J = J0 + j, s = J % RING;
+          if (!mbar_wait(b_vfull + 8 * s, uint32_t((J / RING) & 1)) ||
+              !mbar_wait(b_pfull + 8 * w, uint32_t(jw[w] & 1))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          const uint32_t pa = tmem + COL_S + uint32_t((J & 1) * BKV);
+          const uint32_t vb = smem_u32(sV + s * V_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            mma_f16_ts(od, pa + uint32_t(kk * 8), desc_mnmajor_sw128(vb + uint32_t(kk * 2048), KBOX),
+                       idesc_o, (j | kk) != 0);
+          mma_commit(b_odone + 8 * w);
+          mma_commit(b_vempty + 8 * s);
+          ++jw[w];
+          if (j + 2 < n_tiles) ok = issue_s(j + 2);
         }
-        if (progress) {
-          idle_since = clock64();
-        } else if (clock64() - idle_since > kWaitCycles) {
-          atomicOr(&g_error_flags, kErrWaitTimeout);  // nothing moved: give up
-          ok = false;
-        }
+        ++uw[w];
+        J0 += n_tiles;
+        ++kq;
       }
       mma_commit(b_done);
       mbar_wait(b_done, 0);
