@@ -140,7 +140,26 @@ def flops_of(w, plans):
     attn_suf = 2.0 * H * (Dn + P + Dv) * sum(q * (q + 1) / 2 for q in w.query_lens)
     return dict(up_proj_ctx=2.0 * L * H * (Dn + Dv) * ctx_rows,
                 up_proj_new=2.0 * L * H * (Dn + Dv) * T, attn_ctx=attn_ctx, attn_new=attn_suf,
-                total=up + attn_ctx + attn_suf, context_rows=ctx_rows)
+                total=up + attn_ctx + attn_suf, context_rows=ctx_rows,
+                attn_ctx_bytes=attn_ctx_bytes(w, plans))
+
+
+def attn_ctx_bytes(w, plans):
+    """Bytes the context attention kernel must move per prefill: every
+    context row's fp16 K_nope and V for every head and its bf16 k_pe (once),
+    each chunk's queries of its requests (q_nope fp16 + q_pe bf16), and the
+    float32 partial (O and LSE) written -- and read back where the request
+    continues from an earlier chunk."""
+    H, Dn, Dv, P = w.num_heads, w.qk_nope_dim, w.v_dim, w.qk_rope_dim
+    b = 0.0
+    for p in plans:
+        rows = sum(p.seq_lens)
+        b += rows * (H * (Dn + Dv) * 2 + P * 2)
+        for i, r in enumerate(range(p.request_start, p.request_end)):
+            q = w.query_lens[r]
+            part = q * H * (Dv + 1) * 4
+            b += q * H * (Dn + P) * 2 + part * (2 if p.starts[i] > 0 else 1)
+    return b
 
 
 def config_of(w, plans, world):
@@ -261,6 +280,26 @@ def breakdown_of(records, steps, w, plans, peaks):
         return {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
                 "peak_source": peak_src, "launches_per_step": launches,
                 "ms_per_step": ms, "attributed_ms_per_step": share, "work_per_step": work}
+    def attn_rl(ms, launches, share):
+        # tensor- or HBM-bound by which lower bound on the time is larger:
+        # FLOPs at the bf16 peak, or the bytes the kernel must move at the
+        # copy bandwidth (a chunk of few queries over many context rows is
+        # bound by its K/V reads)
+        t_tc = fl["attn_ctx"] / (bf * 1e12)
+        t_hbm = fl["attn_ctx_bytes"] / (peaks["hbm_gbs"] * 1e9)
+        if t_hbm > t_tc:
+            r = rl(ms, fl["attn_ctx_bytes"], launches, "GB/s", peaks["hbm_gbs"],
+                   src + " copy", "hbm", share)
+        else:
+            r = rl(ms, fl["attn_ctx"], launches, "TFLOP/s", bf, src + " bf16 burst", "tensor",
+                   share)
+        if r is not None:
+            r["flops_per_step"] = fl["attn_ctx"]
+            r["bytes_per_step"] = fl["attn_ctx_bytes"]
+            r["bound_basis"] = ("max(FLOPs / bf16 peak, K/V + k_pe + q + partial bytes / copy "
+                                "bandwidth): t_tensor %.3f ms, t_hbm %.3f ms" %
+                                (t_tc * 1e3, t_hbm * 1e3))
+        return r
     g = roles.get(ROLE_UP, {"ms": 0, "launches": 0})
     gn = roles.get(ROLE_UP_NEW, {"ms": 0, "launches": 0})
     a = roles.get(ROLE_ATTN, {"ms": 0, "launches": 0})
@@ -273,8 +312,7 @@ def breakdown_of(records, steps, w, plans, peaks):
         "up_proj": rl(g["ms"] + gn["ms"], fl["up_proj_ctx"] + fl["up_proj_new"],
                       g["launches"] + gn["launches"], "TFLOP/s", bf, src + " bf16 burst",
                       "tensor", at(ROLE_UP, ROLE_UP_NEW)),
-        "context_attention": rl(a["ms"], fl["attn_ctx"], a["launches"], "TFLOP/s", bf,
-                                src + " bf16 burst", "tensor", at(ROLE_ATTN)),
+        "context_attention": attn_rl(a["ms"], a["launches"], at(ROLE_ATTN)),
         "new_token_attention_merge": rl(an["ms"], fl["attn_new"], an["launches"], "TFLOP/s", bf,
                                         src + " bf16 burst", "tensor", at(ROLE_ATTN_NEW)),
         "gather": rl(ga["ms"], 2.0 * fl["context_rows"] * row_bytes, ga["launches"], "GB/s",
@@ -712,6 +750,14 @@ def run_kernel_case(args, dev):
         pairs = n * (ql * (ql + 1) / 2 if args.causal else ql * kl)
         work, unit, peak = 2.0 * H * (192 + 128) * pairs, "TFLOP/s", peaks["bf16_tflops"]
         info = {"seqs": n, "q": ql, "k": kl, "causal": bool(args.causal)}
+    elif args.kernel == "step":
+        # whole prefills of --workload (the launches of one step, for a
+        # traffic capture); work = the step's algorithmic FLOPs
+        w = W.workload(args.workload)
+        x, g, plans, pf, out, step = prefill_runner(M, W, w, dev)
+        fn = step
+        work, unit, peak = flops_of(w, plans)["total"], "TFLOP/s", peaks["bf16_tflops"]
+        info = {"workload": args.workload}
     elif args.kernel == "fused":
         # context attention with the up-projection fused in (one query tile
         # per sequence); work = the up-projection plus the attention
@@ -792,7 +838,7 @@ def main():
     ap.add_argument("--profile-launches", action="store_true",
                     help="--kernel attn: list the launches of one call")
     ap.add_argument("--kernel", default=None,
-                    choices=["up_proj", "attn", "fused", "merge", "gather"],
+                    choices=["up_proj", "attn", "fused", "merge", "gather", "step"],
                     help="time one kernel alone on a small case instead of the full step")
     ap.add_argument("--heads", type=int, default=128)
     ap.add_argument("--rows", type=int, default=8192)
