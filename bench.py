@@ -141,7 +141,21 @@ def flops_of(w, plans):
     return dict(up_proj_ctx=2.0 * L * H * (Dn + Dv) * ctx_rows,
                 up_proj_new=2.0 * L * H * (Dn + Dv) * T, attn_ctx=attn_ctx, attn_new=attn_suf,
                 total=up + attn_ctx + attn_suf, context_rows=ctx_rows,
-                attn_ctx_bytes=attn_ctx_bytes(w, plans))
+                attn_ctx_bytes=attn_ctx_bytes(w, plans), attn_new_bytes=attn_new_bytes(w))
+
+
+def attn_new_bytes(w):
+    """Bytes the new-token attention (with the final merge in its epilogue)
+    must move per prefill: every new token's queries and its fp16 K_nope / V
+    (every head) and bf16 k_pe, the float32 context partial of the tokens
+    whose request has context (O and LSE), and the output (O in the storage
+    type, LSE)."""
+    H, Dn, Dv, P = w.num_heads, w.qk_nope_dim, w.v_dim, w.qk_rope_dim
+    es = 2 if w.dtype == "bf16" else 4
+    T = w.num_tokens
+    with_ctx = sum(q for q, c in zip(w.query_lens, w.context_lens) if c > 0)
+    return (T * H * (Dn + P) * 2 + T * (H * (Dn + Dv) * 2 + P * 2)
+            + with_ctx * H * (Dv + 1) * 4 + T * H * (Dv * es + 4))
 
 
 def attn_ctx_bytes(w, plans):
@@ -280,24 +294,22 @@ def breakdown_of(records, steps, w, plans, peaks):
         return {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
                 "peak_source": peak_src, "launches_per_step": launches,
                 "ms_per_step": ms, "attributed_ms_per_step": share, "work_per_step": work}
-    def attn_rl(ms, launches, share):
+    def attn_rl(ms, launches, share, flops, nbytes):
         # tensor- or HBM-bound by which lower bound on the time is larger:
         # FLOPs at the bf16 peak, or the bytes the kernel must move at the
         # copy bandwidth (a chunk of few queries over many context rows is
-        # bound by its K/V reads)
-        t_tc = fl["attn_ctx"] / (bf * 1e12)
-        t_hbm = fl["attn_ctx_bytes"] / (peaks["hbm_gbs"] * 1e9)
+        # bound by its K/V reads; so is attention over short causal windows)
+        t_tc = flops / (bf * 1e12)
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
         if t_hbm > t_tc:
-            r = rl(ms, fl["attn_ctx_bytes"], launches, "GB/s", peaks["hbm_gbs"],
-                   src + " copy", "hbm", share)
+            r = rl(ms, nbytes, launches, "GB/s", peaks["hbm_gbs"], src + " copy", "hbm", share)
         else:
-            r = rl(ms, fl["attn_ctx"], launches, "TFLOP/s", bf, src + " bf16 burst", "tensor",
-                   share)
+            r = rl(ms, flops, launches, "TFLOP/s", bf, src + " bf16 burst", "tensor", share)
         if r is not None:
-            r["flops_per_step"] = fl["attn_ctx"]
-            r["bytes_per_step"] = fl["attn_ctx_bytes"]
-            r["bound_basis"] = ("max(FLOPs / bf16 peak, K/V + k_pe + q + partial bytes / copy "
-                                "bandwidth): t_tensor %.3f ms, t_hbm %.3f ms" %
+            r["flops_per_step"] = flops
+            r["bytes_per_step"] = nbytes
+            r["bound_basis"] = ("max(FLOPs / bf16 peak, q + K/V + k_pe + partial + output bytes "
+                                "/ copy bandwidth): t_tensor %.3f ms, t_hbm %.3f ms" %
                                 (t_tc * 1e3, t_hbm * 1e3))
         return r
     g = roles.get(ROLE_UP, {"ms": 0, "launches": 0})
@@ -312,9 +324,10 @@ def breakdown_of(records, steps, w, plans, peaks):
         "up_proj": rl(g["ms"] + gn["ms"], fl["up_proj_ctx"] + fl["up_proj_new"],
                       g["launches"] + gn["launches"], "TFLOP/s", bf, src + " bf16 burst",
                       "tensor", at(ROLE_UP, ROLE_UP_NEW)),
-        "context_attention": attn_rl(a["ms"], a["launches"], at(ROLE_ATTN)),
-        "new_token_attention_merge": rl(an["ms"], fl["attn_new"], an["launches"], "TFLOP/s", bf,
-                                        src + " bf16 burst", "tensor", at(ROLE_ATTN_NEW)),
+        "context_attention": attn_rl(a["ms"], a["launches"], at(ROLE_ATTN), fl["attn_ctx"],
+                                     fl["attn_ctx_bytes"]),
+        "new_token_attention_merge": attn_rl(an["ms"], an["launches"], at(ROLE_ATTN_NEW),
+                                             fl["attn_new"], fl["attn_new_bytes"]),
         "gather": rl(ga["ms"], 2.0 * fl["context_rows"] * row_bytes, ga["launches"], "GB/s",
                      peaks["hbm_gbs"], src + " copy", "hbm", at(ROLE_GATHER)),
     }

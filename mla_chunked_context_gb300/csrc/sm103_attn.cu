@@ -20,29 +20,35 @@
 // go to a scratch slot and are LSE-merged by split_combine_kernel (the same
 // merge as the chunk accumulation, over a split of the key set).
 // Two softmax warpgroups share every S tile: A takes its keys 0-63, B keys
-// 64-127, each with its own running max and sum and its own O accumulator
-// (a split of the key set, merged by LSE in the epilogue).  Each thread thus
-// exponentiates half a row per tile and two warps share each SM sub-partition,
-// so the softmax keeps up with the tensor cores.
+// 64-127, each thread half a query row; the two exchange their half-row
+// maxima through shared memory every tile, so both apply the same running
+// max and accumulate into one O.
 //   warp 0     TMA producer: the 128x192 Q tile once, then per key tile
 //              K = [K_nope (2 boxes) | k_pe (1 box)] and V (2 boxes),
-//              double-buffered, 128-byte swizzle.
+//              double-buffered, 128-byte swizzle; a stage is reloaded once
+//              the MMA that read it has completed (the S-full / P.V-done
+//              commits).
 //   warp 1     TMEM owner + MMA issuer: S = Q K^T (M=128, N=128, K=192: 8
 //              fp16 tcgen05.mma for the nope part, 4 bf16 for the rope part)
-//              into a double-buffered S; O_A += P_A V[0:64] and O_B += P_B
-//              V[64:128] (M=128, N=128, K=64: 4 fp16 tcgen05.mma each, P read
-//              from TMEM, V an MN-major shared-memory operand).
+//              into one of three S buffers; O += P V (M=128, N=128, K=128:
+//              8 fp16 tcgen05.mma, P read from TMEM, V an MN-major
+//              shared-memory operand).  Three S buffers let S of tiles j+1
+//              and j+2 run on the tensor pipe while tile j is exponentiated,
+//              so the pipe does not wait for the softmax (with two, the S of
+//              tile j+2 had to follow the P.V of tile j, and the pipe idled
+//              half the time).  Operand descriptors are built once; a K step
+//              adds its offset.
 //   warps 2-5  softmax warpgroup A, warps 6-9 warpgroup B: one thread per
 //              query row and half row; tcgen05.ld the half row of S, mask,
-//              online softmax in base 2 with a lazily raised running max (O
-//              is rescaled in TMEM only when the max grows by more than 2^8;
-//              exact, since O/l and LSE use the same max), P as fp16 written
-//              over the warpgroup's own S columns with tcgen05.st.
-//              Epilogue: A writes columns 0-63 of O, B columns 64-127, after
-//              merging the two partials; the result is written or LSE-merged
-//              into the stored partial (accumulate).
-// TMEM: S0 [0,128) S1 [128,256) (P_A over S cols [0,32), P_B over [64,96)),
-//       O_A [256,384) O_B [384,512).
+//              half-row max, exchange, online softmax in base 2 with a
+//              lazily raised running max (O is rescaled in TMEM only when
+//              the max grows by more than 2^8; exact, since O/l and LSE use
+//              the same max), P as fp16 written over the warpgroup's own S
+//              columns with tcgen05.st.  Epilogue: A writes columns 0-63 of
+//              O, B columns 64-127; the result is written or LSE-merged into
+//              the stored partial (accumulate).
+// TMEM: S0 [0,128) S1 [128,256) S2 [256,384) (P_A over S cols [0,32), P_B
+//       over [64,96)), O [384,512).
 #include <algorithm>
 #include <vector>
 
@@ -62,6 +68,12 @@ constexpr int K_BYTES = 3 * KBOX;            // 48 KB: K_nope (2 boxes) + k_pe
 constexpr int V_BYTES = 2 * KBOX;            // 32 KB
 constexpr int XCHG_BYTES = 4 * 128 * 4;       // per-row (m, l) of both warpgroups
 constexpr int SMEM_BYTES = 1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + XCHG_BYTES + 256;
+// one-CTA kernel: half-row maxima [2 warpgroups][2 tile parities][128],
+// row sums [2][128], per-warp ok flags [2 parities][8]
+constexpr int XCHG1_BYTES = (2 * 2 * 128 + 2 * 128) * 4 + 2 * 8 * 4;
+constexpr int SMEM_BYTES1 = 1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + XCHG1_BYTES + 256;
+constexpr int NSBUF = 3;                      // S buffers of the one-CTA kernel
+constexpr uint32_t COL_O1 = NSBUF * BKV;      // its O accumulator
 constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256;
@@ -164,27 +176,41 @@ __device__ __forceinline__ void prefetch_partial(const AttnParams &p, int h, int
   asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 32));
 }
 
-// One 128-key tile of the online softmax, for one warpgroup's half (64
-// keys, the first being key k0 of the sequence) of query row qpos: S from
-// TMEM (s_col), masked past the sequence (and, causal, past the query),
-// running max in base 2 raised lazily, P as fp16 over the S columns, O
-// (o_col) rescaled when the max grew -- after the previous tile's P.V (tile
-// J-1 of the CTA) is done -- then an arrival on pfull_bar.  The P.V of tile
-// J commits to done barrier J % 2 (b_odone + 8 * (J % 2)), and the MMA
-// thread observes the P.V of tile J-2 before it issues that of tile J, so a
-// wait for tile J-1 is one phase from its barrier's state either way: it
-// is only made when this warp rescales O.  Returns false when a wait gave
-// up.
-__device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col, uint32_t o_col,
-                                             uint32_t sfull_bar, uint32_t sfull_parity,
-                                             uint32_t b_odone, uint32_t pfull_bar, int J,
-                                             int k0, int nk, int qpos, float &m_used, float &l,
-                                             int lane) {
-  // every exit is taken by the whole warp (its TMEM accesses are warp-wide)
-  if (!__all_sync(0xffffffffu, mbar_wait(sfull_bar, sfull_parity))) return false;
-  tc_fence_after();
+// The 256 softmax threads of the one-CTA kernel meet at named barrier 1;
+// the result is the AND of `ok` over them (every warp passes the same
+// value for all its lanes).
+__device__ __forceinline__ bool softmax_bar_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.and.pred b, 1, 256, a;\n"
+      " selp.u32 %0, 1, 0, b;\n}\n"
+      : "=r"(r)
+      : "r"(ok ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// One 128-key tile (tile J of the CTA, S buffer J % 3) of the online
+// softmax, for one warpgroup's half (64 keys, the first being key k0 of the
+// sequence) of query row qpos: S from TMEM (s_col), masked past the
+// sequence (and, causal, past the query); the half-row maxima of both
+// warpgroups meet in xm (parity J % 2) at named barrier 1, so both raise the
+// shared running max alike; P as fp16 over the warpgroup's S columns; the
+// warpgroup's 64 columns of O (o_col) rescaled when the max grew -- after
+// the P.V of tile J-1 -- then an arrival on pfull_bar.  A warp whose wait
+// gives up still reaches the barrier with ok_w false, and every warp leaves
+// at that tile (returns false), so the barrier counts always match.
+__device__ __forceinline__ bool softmax_tile1(const AttnParams &p, uint32_t s_col, uint32_t o_col,
+                                              uint32_t sfull_bar, uint32_t sfull_parity,
+                                              uint32_t b_odone, uint32_t pfull_bar, int J,
+                                              int k0, int nk, int qpos, float *xm, int wg,
+                                              int row, bool &ok_w, float &m_used, float &l,
+                                              int lane) {
   float sv[HALF];  // raw scores (scale applied below)
-  {
+  float mh = neg_inf();
+  if (ok_w) ok_w = __all_sync(0xffffffffu, mbar_wait(sfull_bar, sfull_parity)) != 0;
+  if (ok_w) {
+    tc_fence_after();
     uint32_t r0[32], r1[32];
     tmem_ld32(s_col, r0);  // both halves in flight before the wait
     tmem_ld32(s_col + 32u, r1);
@@ -194,25 +220,33 @@ __device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col
       sv[e] = __uint_as_float(r0[e]);
       sv[32 + e] = __uint_as_float(r1[e]);
     }
+    // mask keys past the sequence (and, causal, past the query)
+    int valid = nk - k0;
+    if (p.causal) valid = min(valid, qpos - k0 + 1);
+    if (valid < HALF) {
+#pragma unroll
+      for (int e = 0; e < HALF; ++e)
+        if (e >= valid) sv[e] = neg_inf();
+    }
+    // half-row max as a tree (no serial dependency chain)
+    float tm[HALF / 2];
+#pragma unroll
+    for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
+#pragma unroll
+    for (int w = HALF / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
+    mh = tm[0];
   }
-  // mask keys past the sequence (and, causal, past the query)
-  int valid = nk - k0;
-  if (p.causal) valid = min(valid, qpos - k0 + 1);
-  if (valid < HALF) {
-#pragma unroll
-    for (int e = 0; e < HALF; ++e)
-      if (e >= valid) sv[e] = neg_inf();
+  const int par = J & 1;
+  xm[(wg * 2 + par) * BQ + row] = mh;
+  if (!softmax_bar_and(ok_w)) {
+    ok_w = false;
+    return false;
   }
-  // row max as a tree (no serial dependency chain); scale > 0, so the
-  // max of the scaled scores is the scaled max
-  float tm[HALF / 2];
-#pragma unroll
-  for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
-#pragma unroll
-  for (int w = HALF / 4; w >= 1; w >>= 1)
-#pragma unroll
-    for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
-  const float mx = tm[0] * p.scale_log2;
+  // the row max (scale > 0: the max of the scaled scores is the scaled
+  // max); fmaxf of the two halves gives both warpgroups the same value
+  const float mx = fmaxf(mh, xm[((1 - wg) * 2 + par) * BQ + row]) * p.scale_log2;
   float alpha = 1.f;
   bool rescale = false;
   if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
@@ -235,26 +269,29 @@ __device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col
     pk[e] = pack_f16(a, b);
   }
   l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-  // P over this warpgroup's own S columns (already read).  Only when O must
-  // be rescaled does the warp wait for the previous tile's P.V (the P.V of
-  // this tile cannot be issued before this warp arrives, so the barrier of
-  // tile J-1 is at most one phase ahead); otherwise this tile's P.V is
-  // issued while the previous one may still run.
+  // P over this warpgroup's own S columns (already read).  O is rescaled
+  // once the previous tile's P.V is done (the P.V of this tile cannot be
+  // issued before this warp arrives, and that of tile J-3 finished before S
+  // of this tile was computed, so the wait is one phase from its barrier's
+  // state); otherwise this tile's P.V may follow the previous one directly.
   tmem_st32(s_col, pk);
   if (__any_sync(0xffffffffu, rescale)) {
     const bool done =
         J == 0 || mbar_wait(b_odone + 8u * uint32_t((J - 1) & 1), uint32_t(((J - 1) >> 1) & 1));
-    if (!__all_sync(0xffffffffu, done)) return false;
-    tc_fence_after();
+    if (!__all_sync(0xffffffffu, done)) {
+      ok_w = false;  // reported at the next tile's barrier or in the epilogue
+    } else {
+      tc_fence_after();
 #pragma unroll 1
-    for (int c = 0; c < DV / 32; ++c) {
-      uint32_t r[32];
-      const uint32_t oc = o_col + uint32_t(c * 32);
-      tmem_ld32(oc, r);
-      tmem_wait_ld();
+      for (int c = 0; c < DV / 2 / 32; ++c) {
+        uint32_t r[32];
+        const uint32_t oc = o_col + uint32_t(c * 32);
+        tmem_ld32(oc, r);
+        tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-      tmem_st32(oc, r);
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+        tmem_st32(oc, r);
+      }
     }
   }
   tmem_wait_st();
@@ -264,30 +301,20 @@ __device__ __forceinline__ bool softmax_tile(const AttnParams &p, uint32_t s_col
   return true;
 }
 
-// Epilogue of one (query tile, head) unit, run by both softmax warpgroups:
-// after the unit's last P.V (odone at odone_parity), exchange the two
-// warpgroups' (max, sum) per row through xchg, merge O_A and O_B and write
-// the row -- or LSE-merge it into the stored partial (a continued request),
-// into the key-split scratch slot, or with the context partial into the
-// final output -- as the launch asks.  All threads of the CTA meet at one
-// barrier.  b_ofree (nonzero): arrived on once the warp has read O from
-// TMEM.  Returns the AND over the threads of `ok`.
-__device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem,
-                                              uint32_t lane_off, float *xchg, uint32_t b_odone,
-                                              uint32_t odone_parity, uint32_t b_ofree, int wg,
-                                              int row, int lane, int h, int seq, int slot,
-                                              int q_beg, int nq, int qpos, int n_tiles,
-                                              float m_used, float l, bool ok) {
-  if (ok && n_tiles > 0 && !mbar_wait(b_odone, odone_parity)) ok = false;
-  float *xm = xchg, *xl = xchg + 128;        // warpgroup B's (m, l) per row
-  float *ym = xchg + 256, *yl = xchg + 384;  // warpgroup A's (m, l) per row
-  if (wg == 1) {
-    xm[row] = m_used;
-    xl[row] = l;
-  } else {
-    ym[row] = m_used;
-    yl[row] = l;
-  }
+// Epilogue of one (query tile, head) unit of the one-CTA kernel, run by both
+// softmax warpgroups: after the unit's last P.V (odone at odone_parity), the
+// row sum is the sum of the two warpgroups' (same running max); each writes
+// its 64 columns of O / l -- or LSE-merges them into the stored partial (a
+// continued request), into the key-split scratch slot, or with the context
+// partial into the final output -- as the launch asks.  All threads of the
+// CTA meet at one barrier.  Returns the AND over the threads of `ok`.
+__device__ __forceinline__ bool unit_epilogue1(const AttnParams &p, uint32_t o_col, float *xl,
+                                               uint32_t b_odone, uint32_t odone_parity, int wg,
+                                               int row, int lane, int h, int seq, int slot,
+                                               int q_beg, int nq, int qpos, int n_tiles,
+                                               float m_used, float l, bool ok) {
+  if (ok && n_tiles > 0 && !__all_sync(0xffffffffu, mbar_wait(b_odone, odone_parity))) ok = false;
+  xl[wg * BQ + row] = l;
   const int t = q_beg + qpos;
   const int64_t li = int64_t(h) * p.T + t;
   const bool fin = p.fout != nullptr;
@@ -300,7 +327,7 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
   float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + row) * DV + wg * (DV / 2)
                       : p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
   // the stored half row, when it holds a result (finite LSE), read now with
-  // all 16 loads in flight, not one 64-byte piece at a time below
+  // all 16 loads in flight
   float4 ov[DV / 2 / 4];
   const bool have_old = merge_old && qpos < nq && !is_neg_inf(old);
   if (have_old) {
@@ -308,17 +335,13 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
     for (int i = 0; i < DV / 2 / 4; ++i) ov[i] = reinterpret_cast<const float4 *>(orow)[i];
   }
   tc_fence_before();
-  // both warpgroups' O are complete after this barrier (each waited for
-  // its own last P.V); all threads take part, the MMA warps too
+  // both warpgroups' sums are in xl after this barrier; all threads take
+  // part, the MMA warps too
   const int okv = __syncthreads_and(ok ? 1 : 0);
   tc_fence_after();
-  const float mA = ym[row], lA = yl[row], mB = xm[row], lB = xl[row];
-  const float mx = fmaxf(mA, mB);
-  const float fA = (lA > 0.f) ? exp2f(mA - mx) : 0.f;  // scale of each partial
-  const float fB = (lB > 0.f) ? exp2f(mB - mx) : 0.f;
-  const float lsum = lA * fA + lB * fB;
+  const float lsum = xl[row] + xl[BQ + row];
   const bool store = okv && qpos < nq;
-  float lse = (lsum > 0.f) ? (mx + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
+  float lse = (lsum > 0.f) ? (m_used + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
   float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
   float *lse_dst = split ? p.split_lse + (int64_t(slot) * p.H + h) * BQ + row : p.lse + li;
   bool write = store;
@@ -339,32 +362,19 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
     }
   }
   if (okv && n_tiles > 0) {
-    // O = (fA O_A + fB O_B) / lsum over this warpgroup's 64 columns
-    const uint32_t oa = tmem + lane_off + COL_O + uint32_t(wg * (DV / 2));
-    const uint32_t ob = oa + uint32_t(DV);
 #pragma unroll
     for (int c = 0; c < DV / 2 / 16; ++c) {
-      uint32_t ra[16], rb[16];
+      uint32_t ra[16];
       __syncwarp();  // converged after the per-lane stores of the previous piece
-      tmem_ld16(oa + uint32_t(c * 16), ra);
-      tmem_ld16(ob + uint32_t(c * 16), rb);
+      tmem_ld16(o_col + uint32_t(c * 16), ra);
       tmem_wait_ld();
-      if (b_ofree != 0 && c == DV / 2 / 16 - 1) {
-        // O_A and O_B are read: the next unit's P.V may overwrite them
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_ofree);
-      }
       if (write) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float v[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float a = (fA != 0.f) ? __uint_as_float(ra[4 * e + k]) * fA : 0.f;
-            const float b = (fB != 0.f) ? __uint_as_float(rb[4 * e + k]) * fB : 0.f;
-            v[k] = (a + b) * w_new;
-          }
+          for (int k = 0; k < 4; ++k)
+            v[k] = (w_new != 0.f) ? __uint_as_float(ra[4 * e + k]) * w_new : 0.f;
           float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
           if (w_old != 0.f) {  // only when the stored LSE is finite (have_old)
             const float4 ovv = ov[c * 4 + e];
@@ -387,16 +397,9 @@ __device__ __forceinline__ bool unit_epilogue(const AttnParams &p, uint32_t tmem
         }
       }
     }
-  } else {
-    if (b_ofree != 0 && n_tiles > 0) {  // O unread (a wait gave up): release it all the same
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_ofree);
-    }
-    if (write && n_tiles == 0 && !accumulate) {
-      for (int c = 0; c < DV / 2; c += 4)
-        *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+  } else if (write && n_tiles == 0 && !accumulate) {
+    for (int c = 0; c < DV / 2; c += 4)
+      *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (write && wg == 0) {
     if (!fin)
@@ -418,20 +421,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + Q_BYTES;
   uint8_t *sV = sK + RING * K_BYTES;
-  float *xchg = reinterpret_cast<float *>(sV + RING * V_BYTES);  // [4][128]: m, l of B then A
-  uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + XCHG_BYTES);
-  // barriers
+  float *xm = reinterpret_cast<float *>(sV + RING * V_BYTES);  // [2 wg][2 parities][128]
+  float *xl = xm + 2 * 2 * BQ;                                 // [2 wg][128]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xm) + XCHG1_BYTES);
+  // q, qready, K full [2 stages], V full [2 stages], S full [3 buffers], P
+  // full [3 buffers] (8 softmax warps), P.V done [2 tile parities], MMAs done
   const uint32_t b_q = smem_u32(bars + 0), b_qready = smem_u32(bars + 1);
-  const uint32_t b_kfull = smem_u32(bars + 2), b_kempty = smem_u32(bars + 2 + RING);
-  const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
-  const uint32_t b_sfull = smem_u32(bars + 2 + 4 * RING);  // [2]: per S buffer
-  // pfull: [2 warpgroups][2 tile parities] -- a warpgroup may write the P of
-  // tile j+1 before the MMA thread has taken tile j's (it no longer waits
-  // for the previous P.V), but not that of tile j+2 (its S needs the P.V of
-  // tile j issued), so each barrier is at most one phase ahead of its waiter
-  const uint32_t b_pfull = b_sfull + 16;
-  const uint32_t b_odone = b_sfull + 48, b_done = b_sfull + 64;  // odone: [2], per tile parity
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 + 4 * RING + 9);
+  const uint32_t b_kfull = smem_u32(bars + 2), b_vfull = smem_u32(bars + 4);
+  const uint32_t b_sfull = smem_u32(bars + 6), b_pfull = smem_u32(bars + 9);
+  const uint32_t b_odone = smem_u32(bars + 12), b_done = smem_u32(bars + 14);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x / p.n_items;
@@ -449,14 +448,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(b_qready, 4);
     for (int s = 0; s < RING; ++s) {
       mbar_init(b_kfull + 8 * s, 1);
-      mbar_init(b_kempty + 8 * s, 1);
       mbar_init(b_vfull + 8 * s, 1);
-      mbar_init(b_vempty + 8 * s, 1);
     }
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(b_sfull + 8 * w, 1);
-      mbar_init(b_pfull + 16 * w, 4);
-      mbar_init(b_pfull + 16 * w + 8, 4);
+    for (int b = 0; b < NSBUF; ++b) {
+      mbar_init(b_sfull + 8 * b, 1);
+      mbar_init(b_pfull + 8 * b, 8);
     }
     mbar_init(b_odone, 1);
     mbar_init(b_odone + 8, 1);
@@ -470,42 +466,53 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0 && n_tiles > 0) {
-      // ---------------- TMA producer
-      prefetch_map(&tm_q);
-      prefetch_map(&tm_kv);
-      prefetch_map(&tm_lat);
-      const int qx = p.q_prepared ? 0 : h * DQK, qy = (p.q_prepared ? h * p.T : 0) + q_beg + q0;
-      mbar_expect_tx(b_q, Q_BYTES);
-      tma_load_2d(smem_u32(sQ), &tm_q, b_q, qx, qy);
-      tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, qx + 64, qy);
-      tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, qx + 128, qy);
-      int k_issued[RING], v_issued[RING];
-      for (int s = 0; s < RING; ++s) k_issued[s] = v_issued[s] = -1;
+    if (lane < 2 && n_tiles > 0) {
+      // ---------------- TMA producers: lane 0 Q and K, lane 1 V, so that a
+      // K stage is refilled as soon as its S is done and a V stage as soon
+      // as its P.V is, each in its own order
+      const bool kl = lane == 0;
+      if (kl) {
+        prefetch_map(&tm_q);
+        prefetch_map(&tm_kv);
+        prefetch_map(&tm_lat);
+        const int qx = p.q_prepared ? 0 : h * DQK;
+        const int qy = (p.q_prepared ? h * p.T : 0) + q_beg + q0;
+        mbar_expect_tx(b_q, Q_BYTES);
+        tma_load_2d(smem_u32(sQ), &tm_q, b_q, qx, qy);
+        tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, qx + 64, qy);
+        tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, qx + 128, qy);
+      }
+      int issued[RING];
+      for (int s = 0; s < RING; ++s) issued[s] = -1;
+      const uint32_t full = kl ? b_kfull : b_vfull;
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % RING;
-        const uint32_t use = uint32_t(j / RING);          // use count of slot s
+        const uint32_t use = uint32_t(j / RING);  // use count of stage s
         const int krow = k_beg + (kt0 + j) * BKV;
-        if (j >= RING && !mbar_wait(b_kempty + 8 * s, (use - 1) & 1)) break;
-        uint8_t *k = sK + s * K_BYTES;
-        mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
-        tma_load_3d(smem_u32(k), &tm_kv, b_kfull + 8 * s, 0, krow, h);
-        tma_load_3d(smem_u32(k + KBOX), &tm_kv, b_kfull + 8 * s, 64, krow, h);
-        tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, b_kfull + 8 * s, 512, krow);
-        k_issued[s] = int(use & 1);
-        if (j >= RING && !mbar_wait(b_vempty + 8 * s, (use - 1) & 1)) break;
-        uint8_t *v = sV + s * V_BYTES;
-        mbar_expect_tx(b_vfull + 8 * s, V_BYTES);
-        tma_load_3d(smem_u32(v), &tm_kv, b_vfull + 8 * s, DN, krow, h);
-        tma_load_3d(smem_u32(v + KBOX), &tm_kv, b_vfull + 8 * s, DN + 64, krow, h);
-        v_issued[s] = int(use & 1);
+        // stage s held tile j-2: its K is free once S of tile j-2 is done,
+        // its V once the P.V of tile j-2 is
+        if (j >= RING &&
+            !(kl ? mbar_wait(b_sfull + 8 * ((j - 2) % NSBUF), uint32_t(((j - 2) / NSBUF) & 1))
+                 : mbar_wait(b_odone + 8 * ((j - 2) & 1), uint32_t(((j - 2) >> 1) & 1))))
+          break;
+        if (kl) {
+          uint8_t *k = sK + s * K_BYTES;
+          mbar_expect_tx(full + 8 * s, K_BYTES);
+          tma_load_3d(smem_u32(k), &tm_kv, full + 8 * s, 0, krow, h);
+          tma_load_3d(smem_u32(k + KBOX), &tm_kv, full + 8 * s, 64, krow, h);
+          tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, full + 8 * s, 512, krow);
+        } else {
+          uint8_t *v = sV + s * V_BYTES;
+          mbar_expect_tx(full + 8 * s, V_BYTES);
+          tma_load_3d(smem_u32(v), &tm_kv, full + 8 * s, DN, krow, h);
+          tma_load_3d(smem_u32(v + KBOX), &tm_kv, full + 8 * s, DN + 64, krow, h);
+        }
+        issued[s] = int(use & 1);
       }
       // every issued load has landed before the CTA may exit
-      mbar_wait(b_q, 0);
-      for (int s = 0; s < RING; ++s) {
-        if (k_issued[s] >= 0) mbar_wait(b_kfull + 8 * s, uint32_t(k_issued[s]));
-        if (v_issued[s] >= 0) mbar_wait(b_vfull + 8 * s, uint32_t(v_issued[s]));
-      }
+      if (kl) mbar_wait(b_q, 0);
+      for (int s = 0; s < RING; ++s)
+        if (issued[s] >= 0) mbar_wait(full + 8 * s, uint32_t(issued[s]));
     }
   } else if (warp == 1) {
     if (lane == 0 && n_tiles > 0) {
@@ -513,60 +520,59 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc_nope = idesc_f16kind(BQ, BKV, false, false, false);  // fp16
       constexpr uint32_t idesc_rope = idesc_f16kind(BQ, BKV, false, false, true);   // bf16
       constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
-      const uint32_t q_addr = smem_u32(sQ);
+      // descriptors built once; a K step or a stage adds its byte offset / 16
+      // to the start-address field (shared addresses stay below 2^18, so the
+      // 14-bit field never carries)
+      const uint64_t dq = desc_kmajor_sw128(smem_u32(sQ));
+      const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK));
+      const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), KBOX);
       bool ok = mbar_wait(b_qready, 0);
-      // S for key tile j into S buffer j & 1.  The buffer held P of tile
-      // j-2, whose P.V MMAs were issued before: the tensor pipe runs them in
-      // order, so they read P before this S overwrites it.
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % RING;
-        if (!mbar_wait(b_kfull + 8 * s, uint32_t((j / RING) & 1))) return false;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + s * K_BYTES);
-        const uint32_t d = tmem + COL_S + uint32_t(s * BKV);
-#pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = uint32_t((kk >> 2) * QBOX + (kk & 3) * 32);
-          mma_bf16(d, desc_kmajor_sw128(q_addr + off), desc_kmajor_sw128(k_addr + off),
-                   kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
-        }
-        mma_commit(b_sfull + 8 * s);
-        mma_commit(b_kempty + 8 * s);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && n_tiles > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % RING;
-        // the P.V of tile j-2 (the last user of done barrier j % 2) has
-        // finished: long done by now, and it keeps every wait on that
-        // barrier one phase from its state
-        if (!mbar_wait(b_vfull + 8 * s, uint32_t((j / RING) & 1)) ||
-            (j >= 2 && !mbar_wait(b_odone + 8 * (j & 1), uint32_t(((j - 2) >> 1) & 1)))) {
-          ok = false;
-          break;
-        }
-        const uint32_t v_addr = smem_u32(sV + s * V_BYTES);
-        for (int w = 0; w < 2 && ok; ++w) {
-          if (!mbar_wait(b_pfull + 16 * w + 8 * (j & 1), uint32_t((j >> 1) & 1))) {
-            ok = false;
-            break;
-          }
+      // Issue whichever is ready, S first: S of tile ns (into S buffer
+      // ns % 3, which held P of tile ns-3, whose P.V was issued before: the
+      // tensor pipe runs in order) once its K has landed, P.V of tile np
+      // once its V has landed and both warpgroups wrote its P.  S runs up
+      // to two tiles ahead of the P.V, so the pipe has the S of the next
+      // tiles while a tile is exponentiated, and neither kind waits behind
+      // the other's operands.  Every wait is a non-blocking test; no
+      // progress for kWaitCycles gives up.
+      int ns = 0, np = 0;
+      long long t_last = clock64();
+      while (ok && np < n_tiles) {
+        bool progressed = false;
+        if (ns < n_tiles && ns <= np + 2 &&
+            mbar_test(b_kfull + 8 * (ns % RING), uint32_t((ns / RING) & 1))) {
           tc_fence_after();
-          // warpgroup w's keys are rows [w*64, w*64+64) of the V tile
-          const uint32_t pa = tmem + COL_S + uint32_t(s * BKV + w * HALF);
-          const uint32_t vb = v_addr + uint32_t(w * HALF * 128);
-          const uint32_t od = tmem + COL_O + uint32_t(w * DV);
+          const uint64_t dk = dk0 + uint64_t(((ns % RING) * K_BYTES) >> 4);
+          const uint32_t d = tmem + COL_S + uint32_t((ns % NSBUF) * BKV);
 #pragma unroll
-          for (int kk = 0; kk < HALF / 16; ++kk)
-            mma_f16_ts(od, pa + uint32_t(kk * 8),
-                       desc_mnmajor_sw128(vb + uint32_t(kk * 2048), KBOX), idesc_o,
-                       (j | kk) != 0);
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint64_t off = uint64_t(((kk >> 2) * QBOX + (kk & 3) * 32) >> 4);
+            mma_bf16(d, dq + off, dk + off, kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
+          }
+          mma_commit(b_sfull + 8 * (ns % NSBUF));  // S ready; K stage free
+          ++ns;
+          progressed = true;
         }
-        if (!ok) break;
-        mma_commit(b_odone + 8 * (j & 1));
-        mma_commit(b_vempty + 8 * s);
-        if (j + 2 < n_tiles) ok = issue_s(j + 2);
+        if (np < ns && mbar_test(b_vfull + 8 * (np % RING), uint32_t((np / RING) & 1)) &&
+            mbar_test(b_pfull + 8 * (np % NSBUF), uint32_t((np / NSBUF) & 1))) {
+          tc_fence_after();
+          // P_A (keys 0-63) over S columns [0, 32), P_B (keys 64-127) over [64, 96)
+          const uint32_t pa = tmem + COL_S + uint32_t((np % NSBUF) * BKV);
+          const uint64_t dv = dv0 + uint64_t(((np % RING) * V_BYTES) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            mma_f16_ts(tmem + COL_O1, pa + uint32_t((kk >> 2) * HALF + (kk & 3) * 8),
+                       dv + uint64_t((kk * 2048) >> 4), idesc_o, (np | kk) != 0);
+          mma_commit(b_odone + 8 * (np & 1));  // P.V done; V stage free
+          ++np;
+          progressed = true;
+        }
+        if (progressed) {
+          t_last = clock64();
+        } else if (clock64() - t_last > kWaitCycles) {
+          atomicOr(&g_error_flags, kErrWaitTimeout);
+          ok = false;
+        }
       }
       mma_commit(b_done);
       mbar_wait(b_done, 0);
@@ -583,25 +589,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (n_tiles > 0 && wg == 0) {
       if (!mbar_wait(b_q, 0))
         ok = false;
-      else
-        if (!p.q_prepared) convert_q_nope(sQ, threadIdx.x - 64, 128, p.status);
+      else if (!p.q_prepared)
+        convert_q_nope(sQ, threadIdx.x - 64, 128, p.status);
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qready);
     }
+    ok = __all_sync(0xffffffffu, ok) != 0;
     prefetch_partial(p, h, seq, slot, q_beg, nq, qpos, wg);
-    const uint32_t o_col = tmem + lane_off + COL_O + uint32_t(wg * DV);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % RING;
-      const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(s * BKV + wg * HALF);
-      ok = softmax_tile(p, s_col, o_col, b_sfull + 8 * s, uint32_t((j / RING) & 1), b_odone,
-                        b_pfull + 16 * wg + 8 * (j & 1), j, (kt0 + j) * BKV + wg * HALF, nk,
-                        qpos, m_used, l,
-                        lane);
+    // this warpgroup's 64 columns of O
+    const uint32_t o_col = tmem + lane_off + COL_O1 + uint32_t(wg * (DV / 2));
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j % NSBUF;
+      const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(b * BKV + wg * HALF);
+      if (!softmax_tile1(p, s_col, o_col, b_sfull + 8 * b, uint32_t((j / NSBUF) & 1), b_odone,
+                         b_pfull + 8 * b, j, (kt0 + j) * BKV + wg * HALF, nk, qpos, xm, wg, row,
+                         ok, m_used, l, lane))
+        break;
     }
     // the unit's last P.V: done barrier (n_tiles-1) % 2, its ((n_tiles-1)/2)-th phase
-    unit_epilogue(p, tmem, lane_off, xchg, b_odone + 8u * uint32_t((n_tiles - 1) & 1),
-                  uint32_t(((n_tiles - 1) >> 1) & 1), 0u, wg, row, lane, h, seq, slot, q_beg, nq,
-                  qpos, n_tiles, m_used, l, ok);
+    unit_epilogue1(p, o_col, xl, b_odone + 8u * uint32_t((n_tiles - 1) & 1),
+                   uint32_t(((n_tiles - 1) >> 1) & 1), wg, row, lane, h, seq, slot, q_beg, nq,
+                   qpos, n_tiles, m_used, l, ok);
   }
   if (warp < 2) __syncthreads_and(1);  // matches the softmax warps' vote
   tc_fence_before();
@@ -1345,7 +1353,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess ||
+                             SMEM_BYTES1) != cudaSuccess ||
         cudaFuncSetAttribute(attn_tc_loop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES_LOOP) != cudaSuccess)
       return MLA_ERR_CUDA;
@@ -1387,7 +1395,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     if (loop)
       attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, prm);
     else
-      attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES, s>>>(tq, tkv, tlat, prm);
+      attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES1, s>>>(tq, tkv, tlat, prm);
     const int rc = launch_status(s, loop ? "attn_tc_loop_kernel" : "attn_tc_kernel");
     if (rc) return rc;
   }

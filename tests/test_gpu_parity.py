@@ -728,6 +728,27 @@ def test_prefill_key_split_and_pipeline():
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+def test_prefill_multi_tile_key_split():
+    # requests of three and two query tiles over long contexts: several
+    # query tiles of a request, each split over its keys into scratch slots
+    # and merged, also into the stored partial of each continued request
+    # (budget 4096: two chunks each); the new-token attention runs with the
+    # final merge
+    w = W.scaled(W.workload("uniform"), context_lens=[8192, 5000], query_lens=[300, 256],
+                 num_heads=4, row_budget=4096, max_context_chunk=4096, split_alignment=64,
+                 seed=55)
+    x = W.make_inputs(w)
+    M.mla_profile_begin()
+    out, lse = _run_prefill(w, x)
+    names = [r[0] for r in M.mla_profile_end()]
+    assert "attn_tc_kernel" in names and "split_combine_kernel" in names
+    ro, rl, plans = _oracle_prefill(w, x)
+    assert len(plans) >= 4 and any(p.is_continuation for p in plans)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_prefill_groups_small_chunks_into_one_launch_set():
     # three chunks, separated only by context-free requests and together
     # within the budget, run as one execution group: one gather, one
