@@ -332,6 +332,10 @@ def breakdown_of(records, steps, w, plans, peaks):
                      peaks["hbm_gbs"], src + " copy", "hbm", at(ROLE_GATHER)),
     }
     rooflines = {k: v for k, v in rooflines.items() if v is not None}
+    for k, v in rooflines.items():
+        # DRAM bytes per launch of the role on this workload (ncu), null when
+        # not captured or the kernel's sources changed since
+        v["traffic"] = committed_traffic(TRAFFIC_KEY.get(k, k), w.name)
     bar = None
     if span_ms:
         ach = (fl["up_proj_ctx"] + fl["attn_ctx"]) / (span_ms / 1e3) / 1e12
@@ -343,6 +347,10 @@ def breakdown_of(records, steps, w, plans, peaks):
                  "ms": round(r[3], 4)} for r in per_step[0]] if per_step and per_step[0] else []
     return {"roles": roles, "kernels": kernels, "north_star_bar": bar, "rooflines": rooflines,
             "timeline_first_step": timeline}
+
+
+# roofline role -> key of profiles/traffic.json
+TRAFFIC_KEY = {"up_proj": "kv_up_proj", "context_attention": "attn_ctx"}
 
 
 def committed_traffic(kernel, workload):
@@ -533,9 +541,7 @@ def run_ours(args, rank, world, dev):
         dom = max(br["rooflines"].items(), key=lambda kv: kv[1]["attributed_ms_per_step"])
         roofline = dict(dom[1])
         roofline["kernel"] = dom[0]
-        roofline["traffic"] = committed_traffic(
-            {"up_proj": "kv_up_proj", "context_attention": "attn_ctx"}.get(dom[0], dom[0]),
-            w.name)
+        roofline["traffic"] = committed_traffic(TRAFFIC_KEY.get(dom[0], dom[0]), w.name)
         launches = roofline["launches_per_step"]
         roofline["achieved_per_launch_basis"] = (
             "algorithmic work per step / launches = per launch; / mean in-step launch time")
