@@ -430,6 +430,39 @@ def test_varlen_attention_multi_tile(causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_varlen_attention_many_units_several_tiles(causal):
+    """Several (query tile, head) units per SM with several key tiles each
+    (the one-CTA kernel, a CTA per unit, many waves): a sequence without
+    keys in between (O=0, LSE=-inf), odd and ragged tile counts; non-causal
+    also a second, accumulating pass over the same keys (LSE + ln 2)."""
+    w = W.scaled(W.workload("uniform"), num_heads=64 if not causal else 16, seed=48)
+    ql = [300, 520, 129, 200] if not causal else [2000, 900]
+    kl = [700, 1030, 0, 2000] if not causal else ql
+    q_loc = [0] + list(np.cumsum(ql))
+    k_loc = [0] + list(np.cumsum(kl))
+    q, kv, lat = _attn_inputs(w, k_loc[-1], q_loc[-1], 12, torch.float16)
+    o = torch.full((q_loc[-1], w.num_heads, w.v_dim), float("nan"), device=DEV)
+    lse = torch.full((w.num_heads, q_loc[-1]), float("nan"), device=DEV)
+    d = M.Dims.of(w)
+    gq, gkv, glat = q.to(DEV), kv.to(DEV), lat.to(DEV)
+    M.mla_profile_begin()
+    M.mla_varlen_attn(d, causal, q_loc, k_loc, gq, gkv, glat, o, lse)
+    names = [r[0] for r in M.mla_profile_end()]
+    torch.cuda.synchronize()
+    assert "attn_tc_kernel" in names
+    ro, rl = _oracle_attn(w, q, kv, lat, q_loc, k_loc, causal)
+    assert_close(f64(o), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+    if not causal:
+        acc = [1] * len(ql)
+        M.mla_varlen_attn(d, False, q_loc, k_loc, gq, gkv, glat, o, lse, accumulate=acc)
+        torch.cuda.synchronize()
+        rl2 = np.where(np.isfinite(rl), rl + np.log(2.0), rl)
+        assert_close(f64(o), ro, 2e-2, 2e-2, what="O accumulated")
+        assert_close(f64(lse), rl2, 1e-3, what="LSE accumulated")
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_varlen_attention_many_short_units(causal):
     """Many more (query tile, head) units than SMs, each of one or two key
     tiles; context sequences without keys between them write O=0,
