@@ -75,6 +75,7 @@ constexpr int SMEM_BYTES1 = 1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + XCHG1_
 constexpr int NSBUF = 3;                      // S buffers of the one-CTA kernel
 constexpr uint32_t COL_O1 = NSBUF * BKV;      // its O accumulator
 constexpr int THREADS = 320;
+constexpr int THREADS1 = THREADS + 32;        // the one-CTA kernel: + a P.V issuer warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256;
 constexpr int MAX_ITEMS = 1536;
@@ -270,14 +271,15 @@ __device__ __forceinline__ bool softmax_tile1(const AttnParams &p, uint32_t s_co
   }
   l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
   // P over this warpgroup's own S columns (already read).  O is rescaled
-  // once the previous tile's P.V is done (the P.V of this tile cannot be
-  // issued before this warp arrives, and that of tile J-3 finished before S
-  // of this tile was computed, so the wait is one phase from its barrier's
-  // state); otherwise this tile's P.V may follow the previous one directly.
+  // once the previous tile's P.V is done (done barrier (J-1) % 3: the P.V of
+  // tile J+2 cannot run before this warp arrives, and that of tile J-4
+  // finished before S of tile J-1 was issued, so the wait is one phase from
+  // its barrier's state); otherwise this tile's P.V may follow the previous
+  // one directly.
   tmem_st32(s_col, pk);
   if (__any_sync(0xffffffffu, rescale)) {
-    const bool done =
-        J == 0 || mbar_wait(b_odone + 8u * uint32_t((J - 1) & 1), uint32_t(((J - 1) >> 1) & 1));
+    const bool done = J == 0 || mbar_wait(b_odone + 8u * uint32_t((J - 1) % NSBUF),
+                                          uint32_t(((J - 1) / NSBUF) & 1));
     if (!__all_sync(0xffffffffu, done)) {
       ok_w = false;  // reported at the next tile's barrier or in the epilogue
     } else {
@@ -410,7 +412,7 @@ __device__ __forceinline__ bool unit_epilogue1(const AttnParams &p, uint32_t o_c
   return okv != 0;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS1, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_kv,
                    const __grid_constant__ CUtensorMap tm_lat,
@@ -425,12 +427,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   float *xl = xm + 2 * 2 * BQ;                                 // [2 wg][128]
   uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xm) + XCHG1_BYTES);
   // q, qready, K full [2 stages], V full [2 stages], S full [3 buffers], P
-  // full [3 buffers] (8 softmax warps), P.V done [2 tile parities], MMAs done
+  // full [3 buffers] (8 softmax warps), P.V done [3 buffers], each issuer's
+  // MMAs done
   const uint32_t b_q = smem_u32(bars + 0), b_qready = smem_u32(bars + 1);
   const uint32_t b_kfull = smem_u32(bars + 2), b_vfull = smem_u32(bars + 4);
   const uint32_t b_sfull = smem_u32(bars + 6), b_pfull = smem_u32(bars + 9);
-  const uint32_t b_odone = smem_u32(bars + 12), b_done = smem_u32(bars + 14);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+  const uint32_t b_odone = smem_u32(bars + 12), b_done = smem_u32(bars + 15);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x / p.n_items;
@@ -453,10 +456,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int b = 0; b < NSBUF; ++b) {
       mbar_init(b_sfull + 8 * b, 1);
       mbar_init(b_pfull + 8 * b, 8);
+      mbar_init(b_odone + 8 * b, 1);
     }
-    mbar_init(b_odone, 1);
-    mbar_init(b_odone + 8, 1);
     mbar_init(b_done, 1);
+    mbar_init(b_done + 8, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -492,8 +495,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // stage s held tile j-2: its K is free once S of tile j-2 is done,
         // its V once the P.V of tile j-2 is
         if (j >= RING &&
-            !(kl ? mbar_wait(b_sfull + 8 * ((j - 2) % NSBUF), uint32_t(((j - 2) / NSBUF) & 1))
-                 : mbar_wait(b_odone + 8 * ((j - 2) & 1), uint32_t(((j - 2) >> 1) & 1))))
+            !mbar_wait((kl ? b_sfull : b_odone) + 8 * ((j - 2) % NSBUF),
+                       uint32_t(((j - 2) / NSBUF) & 1)))
           break;
         if (kl) {
           uint8_t *k = sK + s * K_BYTES;
@@ -514,68 +517,68 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int s = 0; s < RING; ++s)
         if (issued[s] >= 0) mbar_wait(full + 8 * s, uint32_t(issued[s]));
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == THREADS1 / 32 - 1) {
     if (lane == 0 && n_tiles > 0) {
-      // ---------------- MMA issuer
+      // ---------------- MMA issuers: warp 1 the S products, the last warp
+      // the P.V products, each committing its own.  A tcgen05.mma holds its
+      // issuing thread for about 50 cycles (more beside busy softmax warps),
+      // so one issuer for both kinds left the tensor pipe idle while it
+      // issued the other kind; split, S of tiles j+1 and j+2 and P.V of tile
+      // j are issued side by side.  S of tile j reuses S buffer j % 3 once
+      // the P.V of tile j-3 is done (they are issued by different threads,
+      // so issue order alone would not order them).
       constexpr uint32_t idesc_nope = idesc_f16kind(BQ, BKV, false, false, false);  // fp16
       constexpr uint32_t idesc_rope = idesc_f16kind(BQ, BKV, false, false, true);   // bf16
       constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
       // descriptors built once; a K step or a stage adds its byte offset / 16
       // to the start-address field (shared addresses stay below 2^18, so the
       // 14-bit field never carries)
-      const uint64_t dq = desc_kmajor_sw128(smem_u32(sQ));
-      const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK));
-      const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), KBOX);
-      bool ok = mbar_wait(b_qready, 0);
-      // Issue whichever is ready, S first: S of tile ns (into S buffer
-      // ns % 3, which held P of tile ns-3, whose P.V was issued before: the
-      // tensor pipe runs in order) once its K has landed, P.V of tile np
-      // once its V has landed and both warpgroups wrote its P.  S runs up
-      // to two tiles ahead of the P.V, so the pipe has the S of the next
-      // tiles while a tile is exponentiated, and neither kind waits behind
-      // the other's operands.  Every wait is a non-blocking test; no
-      // progress for kWaitCycles gives up.
-      int ns = 0, np = 0;
-      long long t_last = clock64();
-      while (ok && np < n_tiles) {
-        bool progressed = false;
-        if (ns < n_tiles && ns <= np + 2 &&
-            mbar_test(b_kfull + 8 * (ns % RING), uint32_t((ns / RING) & 1))) {
+      bool ok = true;
+      if (warp == 1) {
+        const uint64_t dq = desc_kmajor_sw128(smem_u32(sQ));
+        const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK));
+        ok = mbar_wait(b_qready, 0);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int s = j % RING, b = j % NSBUF;
+          if ((j >= NSBUF && !mbar_wait(b_odone + 8 * b, uint32_t(((j - NSBUF) / NSBUF) & 1))) ||
+              !mbar_wait(b_kfull + 8 * s, uint32_t((j / RING) & 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint64_t dk = dk0 + uint64_t(((ns % RING) * K_BYTES) >> 4);
-          const uint32_t d = tmem + COL_S + uint32_t((ns % NSBUF) * BKV);
+          const uint64_t dk = dk0 + uint64_t((s * K_BYTES) >> 4);
+          const uint32_t d = tmem + COL_S + uint32_t(b * BKV);
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint64_t off = uint64_t(((kk >> 2) * QBOX + (kk & 3) * 32) >> 4);
             mma_bf16(d, dq + off, dk + off, kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
           }
-          mma_commit(b_sfull + 8 * (ns % NSBUF));  // S ready; K stage free
-          ++ns;
-          progressed = true;
+          mma_commit(b_sfull + 8 * b);  // S ready; K stage s free
         }
-        if (np < ns && mbar_test(b_vfull + 8 * (np % RING), uint32_t((np / RING) & 1)) &&
-            mbar_test(b_pfull + 8 * (np % NSBUF), uint32_t((np / NSBUF) & 1))) {
+      } else {
+        const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), KBOX);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int s = j % RING, b = j % NSBUF;
+          if (!mbar_wait(b_vfull + 8 * s, uint32_t((j / RING) & 1)) ||
+              !mbar_wait(b_pfull + 8 * b, uint32_t((j / NSBUF) & 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           // P_A (keys 0-63) over S columns [0, 32), P_B (keys 64-127) over [64, 96)
-          const uint32_t pa = tmem + COL_S + uint32_t((np % NSBUF) * BKV);
-          const uint64_t dv = dv0 + uint64_t(((np % RING) * V_BYTES) >> 4);
+          const uint32_t pa = tmem + COL_S + uint32_t(b * BKV);
+          const uint64_t dv = dv0 + uint64_t((s * V_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)
             mma_f16_ts(tmem + COL_O1, pa + uint32_t((kk >> 2) * HALF + (kk & 3) * 8),
-                       dv + uint64_t((kk * 2048) >> 4), idesc_o, (np | kk) != 0);
-          mma_commit(b_odone + 8 * (np & 1));  // P.V done; V stage free
-          ++np;
-          progressed = true;
-        }
-        if (progressed) {
-          t_last = clock64();
-        } else if (clock64() - t_last > kWaitCycles) {
-          atomicOr(&g_error_flags, kErrWaitTimeout);
-          ok = false;
+                       dv + uint64_t((kk * 2048) >> 4), idesc_o, (j | kk) != 0);
+          mma_commit(b_odone + 8 * b);  // P.V done; V stage s and S buffer b free
         }
       }
-      mma_commit(b_done);
-      mbar_wait(b_done, 0);
+      // every MMA this thread issued has completed before TMEM is released
+      const uint32_t dbar = b_done + (warp == 1 ? 0u : 8u);
+      mma_commit(dbar);
+      mbar_wait(dbar, 0);
     }
   } else {
     // ---------------- softmax warpgroups
@@ -606,12 +609,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                          ok, m_used, l, lane))
         break;
     }
-    // the unit's last P.V: done barrier (n_tiles-1) % 2, its ((n_tiles-1)/2)-th phase
-    unit_epilogue1(p, o_col, xl, b_odone + 8u * uint32_t((n_tiles - 1) & 1),
-                   uint32_t(((n_tiles - 1) >> 1) & 1), wg, row, lane, h, seq, slot, q_beg, nq,
+    // the unit's last P.V: done barrier (n_tiles-1) % 3, its ((n_tiles-1)/3)-th phase
+    unit_epilogue1(p, o_col, xl, b_odone + 8u * uint32_t((n_tiles + NSBUF - 1) % NSBUF),
+                   uint32_t(((n_tiles - 1) / NSBUF) & 1), wg, row, lane, h, seq, slot, q_beg, nq,
                    qpos, n_tiles, m_used, l, ok);
   }
-  if (warp < 2) __syncthreads_and(1);  // matches the softmax warps' vote
+  if (warp < 2 || warp == THREADS1 / 32 - 1) __syncthreads_and(1);  // the softmax warps' vote
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1395,7 +1398,7 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     if (loop)
       attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, prm);
     else
-      attn_tc_kernel<<<n * H, THREADS, SMEM_BYTES1, s>>>(tq, tkv, tlat, prm);
+      attn_tc_kernel<<<n * H, THREADS1, SMEM_BYTES1, s>>>(tq, tkv, tlat, prm);
     const int rc = launch_status(s, loop ? "attn_tc_loop_kernel" : "attn_tc_kernel");
     if (rc) return rc;
   }
