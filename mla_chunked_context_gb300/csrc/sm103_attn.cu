@@ -23,21 +23,23 @@
 // 64-127, each thread half a query row; the two exchange their half-row
 // maxima through shared memory every tile, so both apply the same running
 // max and accumulate into one O.
-//   warp 0     TMA producer: the 128x192 Q tile once, then per key tile
-//              K = [K_nope (2 boxes) | k_pe (1 box)] and V (2 boxes),
-//              double-buffered, 128-byte swizzle; a stage is reloaded once
-//              the MMA that read it has completed (the S-full / P.V-done
-//              commits).
-//   warp 1     TMEM owner + MMA issuer: S = Q K^T (M=128, N=128, K=192: 8
-//              fp16 tcgen05.mma for the nope part, 4 bf16 for the rope part)
-//              into one of three S buffers; O += P V (M=128, N=128, K=128:
-//              8 fp16 tcgen05.mma, P read from TMEM, V an MN-major
-//              shared-memory operand).  Three S buffers let S of tiles j+1
+//   warp 0     TMA producers: lane 0 the 128x192 Q tile once and per key
+//              tile K = [K_nope (2 boxes) | k_pe (1 box)], lane 1 V (2
+//              boxes), each double-buffered, 128-byte swizzle; a stage is
+//              reloaded once the MMA that read it has completed (the S-full
+//              / P.V-done commits).
+//   warp 1     TMEM owner + S issuer: S = Q K^T (M=128, N=128, K=192: 8 fp16
+//              tcgen05.mma for the nope part, 4 bf16 for the rope part) into
+//              one of three S buffers.  Three S buffers let S of tiles j+1
 //              and j+2 run on the tensor pipe while tile j is exponentiated,
 //              so the pipe does not wait for the softmax (with two, the S of
 //              tile j+2 had to follow the P.V of tile j, and the pipe idled
-//              half the time).  Operand descriptors are built once; a K step
-//              adds its offset.
+//              half the time).
+//   warp 10    P.V issuer: O += P V (M=128, N=128, K=128: 8 fp16
+//              tcgen05.mma, P read from TMEM, V an MN-major shared-memory
+//              operand).  A tcgen05.mma holds its issuing thread for about
+//              50 cycles, so one thread issuing both kinds was the bound.
+//              Operand descriptors are built once; a K step adds its offset.
 //   warps 2-5  softmax warpgroup A, warps 6-9 warpgroup B: one thread per
 //              query row and half row; tcgen05.ld the half row of S, mask,
 //              half-row max, exchange, online softmax in base 2 with a
