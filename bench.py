@@ -19,7 +19,10 @@ Printed JSON line (rank 0):
              of the method; the spec bar = (up-projection + context
              attention FLOPs) / (span of the gather .. context attention)
   rooflines  per kernel: algorithmic work / its in-step CUDA-event time vs the
-             measured peak; roofline = the one with the largest share
+             measured peak, from a third timed region with the pipeline's
+             overlap off (each kernel alone inside real steps); roofline =
+             the one with the largest share of that region's kernel time;
+             rooflines_overlapped: the same from the overlapped region
   configs    the other workloads (tiny, uniform, long) through the same call
   merge      merge_attn_states alone on 8192 tokens x 128 heads x 128 (bf16,
              15% empty prefix rows, prefix_num_tokens 6144): GB/s of the bytes
@@ -427,6 +430,18 @@ def prefill_runner(M, W, w, dev):
     return x, g, plans, pf, out, step
 
 
+def serial_region(M, step, steps, flush, stream):
+    """K steps with the pipeline's overlap off and the per-launch profile on:
+    every kernel of a step alone, one after another, on the caller's
+    stream."""
+    prev = M.mla_set_pipeline_overlap(False)
+    try:
+        ms, records, _ = timed_steps(M, step, steps, 1, flush, stream, profile=True)
+    finally:
+        M.mla_set_pipeline_overlap(prev)
+    return ms, records
+
+
 def bench_config(M, W, name, dev, peaks, flush, steps, warmup):
     """One more workload through mla_chunked_prefill: step time, algorithmic
     throughput and the in-step breakdown (same method as the main line)."""
@@ -435,9 +450,11 @@ def bench_config(M, W, name, dev, peaks, flush, steps, warmup):
     stream = torch.cuda.current_stream()
     ms, _, launched = timed_steps(M, step, steps, warmup, flush, stream, profile=False)
     _, records, _ = timed_steps(M, step, steps, 1, flush, stream, profile=True)
+    ser_ms, ser_records = serial_region(M, step, steps, flush, stream)
     step_ms = statistics.median(ms)
     fl = flops_of(w, plans)
     br = breakdown_of(records, steps, w, plans, peaks)
+    br_ser = breakdown_of(ser_records, steps, w, plans, peaks)
     tf = fl["total"] / (step_ms / 1e3) / 1e12
     res = {"config": config_of(w, plans, 1), "steps": steps, "ms_per_step": step_ms,
            "ms_per_step_all": ms, "tok_per_s": w.num_tokens / (step_ms / 1e3),
@@ -445,8 +462,9 @@ def bench_config(M, W, name, dev, peaks, flush, steps, warmup):
            "frac_burst": tf / peaks["bf16_tflops"],
            "frac_sustained": (tf / peaks["bf16_tflops_sustained"]
                               if peaks.get("bf16_tflops_sustained") else None),
-           "north_star_bar": br["north_star_bar"], "rooflines": br["rooflines"],
-           "roles": br["roles"]}
+           "ms_per_step_serial": statistics.median(ser_ms),
+           "north_star_bar": br["north_star_bar"], "rooflines": br_ser["rooflines"],
+           "rooflines_overlapped": br["rooflines"], "roles": br["roles"]}
     if w.dtype != "bf16":
         res["note"] = ("float32 storage: the CUDA-core kernels (the tensor-core kernels serve "
                        "bf16); fractions are of the bf16 tensor peak for reference only")
@@ -473,8 +491,13 @@ def run_ours(args, rank, world, dev):
     max_ms = job_time_ms(sum(step_ms), world, dev)
     value = whole_job_rate(T, world, args.steps, max_ms)
     # a second timed region of the same steps with the library's per-launch
-    # events on (the in-step breakdown and the kernels' rooflines)
+    # events on (the in-step breakdown and timeline, kernels side by side)
     prof_ms, records, _ = timed_steps(M, step, args.steps, 1, flush, stream, profile=True)
+    # a third with the pipeline's overlap off: the same kernels one after
+    # another, so each launch's time is its own (the kernels' rooflines and
+    # the dominant kernel, whose shares then match a serialised ncu launch
+    # list)
+    ser_ms, ser_records = serial_region(M, step, args.steps, flush, stream)
 
     # ---- e2e: host buffers, copies inside the timed region.  Inputs are
     # double-buffered on the device: step i+1's host->device copy (on a copy
@@ -536,15 +559,17 @@ def run_ours(args, rank, world, dev):
     if rank == 0:
         fl = flops_of(w, plans)
         br = breakdown_of(records, args.steps, w, plans, peaks)
-        # the dominant kernel: the largest share of the step's GPU time, with
-        # the time of launches that run side by side shared out among them
-        dom = max(br["rooflines"].items(), key=lambda kv: kv[1]["attributed_ms_per_step"])
+        br_ser = breakdown_of(ser_records, args.steps, w, plans, peaks)
+        # the dominant kernel: the largest share of the step's kernel time
+        # with the kernels run one after another
+        dom = max(br_ser["rooflines"].items(), key=lambda kv: kv[1]["ms_per_step"])
         roofline = dict(dom[1])
         roofline["kernel"] = dom[0]
         roofline["traffic"] = committed_traffic(TRAFFIC_KEY.get(dom[0], dom[0]), w.name)
         launches = roofline["launches_per_step"]
         roofline["achieved_per_launch_basis"] = (
-            "algorithmic work per step / launches = per launch; / mean in-step launch time")
+            "algorithmic work per step / launches = per launch; / mean launch time in steps "
+            "run with the pipeline's overlap off (each kernel alone, warm, in a real step)")
         roofline["traffic_basis"] = "DRAM bytes per launch (ncu), null if not captured"
         step_ms_mean = max_ms / args.steps
         merge = bench_merge(M, W, dev, peaks, flush)
@@ -572,7 +597,9 @@ def run_ours(args, rank, world, dev):
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launched,
             "roofline": roofline,
-            "rooflines": br["rooflines"],
+            "rooflines": br_ser["rooflines"],
+            "rooflines_overlapped": br["rooflines"],
+            "ms_per_step_serial": statistics.mean(ser_ms),
             "north_star_bar": br["north_star_bar"],
             "breakdown": {"roles": br["roles"], "kernels": br["kernels"],
                           "timeline_first_step": br["timeline_first_step"],
@@ -580,7 +607,10 @@ def run_ours(args, rank, world, dev):
                                  "stream around every launch of a second timed region of "
                                  "the same steps (mla_profile_begin/_end); launches on the "
                                  "side streams overlap the caller's, so ms adds up to more "
-                                 "than the step and attributed_ms shares overlap out"},
+                                 "than the step and attributed_ms shares overlap out; "
+                                 "rooflines come from a third region with the overlap off "
+                                 "(mla_set_pipeline_overlap(False))",
+                          "kernels_serial": br_ser["kernels"]},
             "merge": merge,
             "comparator": comparator,
             "configs": configs,

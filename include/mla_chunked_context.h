@@ -527,6 +527,16 @@ typedef struct {
 int mla_profile_begin(void);
 int mla_profile_end(mla_launch_record_t *records, int32_t cap, int32_t *count);
 
+/* Overlap of the chunk pipeline (mla_chunked_prefill and
+ * mla_chunked_prefill_equal_window): on (1, the default), the gathers and
+ * up-projections run on two library-owned side streams, one chunk ahead of
+ * the attention on the caller's stream; off (0), every kernel of the call
+ * runs on the caller's stream, one after another in the same order, with
+ * identical results.  Off lets each kernel be timed alone inside a real
+ * prefill (per-launch profile above).  Process-wide, read when a call is
+ * enqueued; returns the previous setting.  No errors. */
+int32_t mla_set_pipeline_overlap(int32_t on);
+
 /* Failure-detection self test: launches one thread that waits on an
  * mbarrier nothing arrives on, with the same bounded wait the tensor-core
  * kernels use but a limit of limit_us microseconds (1 .. 10^6).  The wait

@@ -17,7 +17,7 @@ from ._lib import (Chunk, Dims, MlaError, lib, merge_attn_states, mla_chunk_kv_d
                    mla_selftest_bounded_wait, mla_kernel_launches,
                    mla_fused_attn_workspace_bytes, mla_fused_context_attn,
                    mla_fused_attn_plan, mla_prefill_pinned_bytes, mla_profile_begin,
-                   mla_profile_end, MLA_STATUS_FP16_RANGE)
+                   mla_profile_end, mla_set_pipeline_overlap, MLA_STATUS_FP16_RANGE)
 
 __all__ = ["Chunk", "Dims", "MlaError", "lib", "merge_attn_states", "mla_chunk_kv_dtype",
            "mla_chunk_workspace_bytes", "mla_device_error_flags",
@@ -29,7 +29,8 @@ __all__ = ["Chunk", "Dims", "MlaError", "lib", "merge_attn_states", "mla_chunk_k
            "mla_prefill_equal_window_workspace_bytes", "mla_chunked_prefill_equal_window",
            "mla_selftest_bounded_wait", "mla_kernel_launches", "mla_fused_attn_workspace_bytes",
            "mla_fused_context_attn", "mla_fused_attn_plan", "mla_prefill_pinned_bytes",
-           "mla_profile_begin", "mla_profile_end", "MLA_STATUS_FP16_RANGE", "ChunkedPrefill"]
+           "mla_profile_begin", "mla_profile_end", "mla_set_pipeline_overlap",
+           "MLA_STATUS_FP16_RANGE", "ChunkedPrefill"]
 
 
 class ChunkedPrefill:

@@ -38,7 +38,7 @@ EXPORTED = ("mla_plan_context_chunks", "merge_attn_states", "mla_gather_context_
             "mla_chunked_prefill_equal_window", "mla_selftest_bounded_wait",
             "mla_kernel_launches", "mla_fused_attn_workspace_bytes",
             "mla_fused_context_attn", "mla_fused_attn_plan", "mla_prefill_pinned_bytes",
-            "mla_profile_begin", "mla_profile_end")
+            "mla_profile_begin", "mla_profile_end", "mla_set_pipeline_overlap")
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -437,6 +437,16 @@ def mla_chunked_prefill(dims: Dims, context_lens, query_lens, row_budget: int,
 
 def mla_has_tcgen05() -> bool:
     return bool(lib().mla_has_tcgen05())
+
+
+def mla_set_pipeline_overlap(on: bool) -> bool:
+    """Overlap the chunk pipeline's gathers and up-projections with the
+    attention on side streams (True, the default) or run every kernel of a
+    prefill on the caller's stream in order (False); returns the previous
+    setting."""
+    L = lib()
+    L.mla_set_pipeline_overlap.restype = C.c_int32
+    return bool(L.mla_set_pipeline_overlap(C.c_int32(1 if on else 0)))
 
 
 def mla_profile_begin() -> None:

@@ -11,6 +11,7 @@
 //   stream, which waits for the side streams before the last kernel.
 #include <algorithm>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -515,12 +516,17 @@ int upload_meta(Pipeline &pl, void *dst, const std::vector<int32_t> &src, void *
 // (the caller may free the workspace once `s` has passed this point).  The
 // side streams run at the highest priority, so a GEMM takes SMs as soon as
 // attention CTAs retire.
+// With the overlap switched off (mla_set_pipeline_overlap) every step runs
+// on `s` in the same order, one kernel after another.
+std::atomic<int> g_overlap{1};
+
 template <class Pre, class Gather, class Up, class Consume, class Tail>
 int run_pipeline(Pipeline &pl, cudaStream_t s, size_t n, Pre pre, Gather gather, Up up,
                  Consume consume, Tail tail) {
   if (pl.ev.size() < 3 * n + 3) return MLA_ERR_INVALID;
   cudaEvent_t *ev = pl.ev.data();
-  const cudaStream_t sg = pl.gather, sm = pl.gemm;
+  const bool overlap = g_overlap.load() != 0;
+  const cudaStream_t sg = overlap ? pl.gather : s, sm = overlap ? pl.gemm : s;
   auto ev_lat = [&](size_t c) { return ev[1 + 3 * c]; };
   auto ev_kv = [&](size_t c) { return ev[2 + 3 * c]; };
   auto ev_used = [&](size_t c) { return ev[3 + 3 * c]; };
@@ -900,6 +906,10 @@ void drop_profile() {
   g_prof.pending = nullptr;
 }
 }  // namespace
+
+extern "C" int32_t mla_set_pipeline_overlap(int32_t on) {
+  return g_overlap.exchange(on != 0 ? 1 : 0);
+}
 
 extern "C" int mla_profile_begin(void) {
   drop_profile();

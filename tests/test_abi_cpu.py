@@ -30,7 +30,7 @@ def built_library():
 def header_functions():
     text = open(os.path.join(ROOT, "include", "mla_chunked_context.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^int\s+(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^(?:int|int32_t)\s+(\w+)\s*\(", text, flags=re.M)))
 
 
 def test_library_exports_every_declared_symbol():

@@ -206,3 +206,28 @@ def test_profile_records_every_launch_of_a_prefill():
     _prefill(w, x)
     M.mla_profile_begin()
     assert M.mla_profile_end() == []
+
+
+# ------------------------------------------------- pipeline overlap --
+def test_serial_and_overlapped_pipeline_are_identical():
+    """With the pipeline's overlap switched off every kernel of a prefill
+    runs on the caller's stream, in the same order; the numbers are the
+    same, bit for bit, and the setting comes back."""
+    w = _small_batch(seed=95, heads=8)
+    x = W.make_inputs(w)
+    a_out, a_lse, sa = _prefill(w, x)
+    prev = M.mla_set_pipeline_overlap(False)
+    try:
+        M.mla_profile_begin()
+        b_out, b_lse, sb = _prefill(w, x)
+        recs = M.mla_profile_end()
+    finally:
+        assert M.mla_set_pipeline_overlap(prev) is False
+    assert prev is True
+    assert sa == 0 and sb == 0
+    assert torch.equal(a_out, b_out) and torch.equal(a_lse, b_lse)
+    assert len(recs) > 3 and len({r[1] for r in recs}) == 1
+    M.mla_profile_begin()
+    _prefill(w, x)
+    recs = M.mla_profile_end()
+    assert len({r[1] for r in recs}) == 3  # caller's, gathers, up-projections
