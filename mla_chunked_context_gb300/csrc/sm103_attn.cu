@@ -127,6 +127,33 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Three-input max (NaN inputs ignored, as fmaxf), and packed pairs of
+// floats in one 64-bit register for the paired fp32 FMA / add of sm_100+:
+// one instruction per two elements where the softmax has one per element.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t x, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // 16 consecutive 32-bit TMEM columns of the warp's 32 lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -231,15 +258,16 @@ __device__ __forceinline__ bool softmax_tile1(const AttnParams &p, uint32_t s_co
       for (int e = 0; e < HALF; ++e)
         if (e >= valid) sv[e] = neg_inf();
     }
-    // half-row max as a tree (no serial dependency chain)
-    float tm[HALF / 2];
+    // half-row max as a tree of three-input maxima (32 instructions for the
+    // 64 values, no serial dependency chain)
+    float t[22], u[8];
 #pragma unroll
-    for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
+    for (int i = 0; i < 21; ++i) t[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+    t[21] = sv[63];
 #pragma unroll
-    for (int w = HALF / 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
-    mh = tm[0];
+    for (int i = 0; i < 7; ++i) u[i] = fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    u[7] = t[21];
+    mh = fmaxf(fmax3(u[0], u[1], u[2]), fmax3(fmax3(u[3], u[4], u[5]), u[6], u[7]));
   }
   const int par = J & 1;
   xm[(wg * 2 + par) * BQ + row] = mh;
@@ -263,15 +291,22 @@ __device__ __forceinline__ bool softmax_tile1(const AttnParams &p, uint32_t s_co
   const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
   l *= alpha;
   uint32_t pk[HALF / 2];
-  float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+  // exponent arguments two at a time (paired FMA), sums in two paired
+  // accumulators (four independent partial sums)
+  const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nb2 = f2pack(nbase, nbase);
+  uint64_t acc[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
   for (int e = 0; e < HALF / 2; ++e) {
-    const float a = ex2_approx(fmaf(sv[2 * e], p.scale_log2, nbase));
-    const float b = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, nbase));
-    ls[e & 3] += a + b;
+    float xa, xb;
+    f2unpack(f2fma(f2pack(sv[2 * e], sv[2 * e + 1]), sc2, nb2), xa, xb);
+    const float a = ex2_approx(xa), b = ex2_approx(xb);
+    acc[e & 1] = f2add(acc[e & 1], f2pack(a, b));
     pk[e] = pack_f16(a, b);
   }
-  l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  float s0, s1, s2, s3;
+  f2unpack(acc[0], s0, s1);
+  f2unpack(acc[1], s2, s3);
+  l += (s0 + s1) + (s2 + s3);
   // P over this warpgroup's own S columns (already read).  O is rescaled
   // once the previous tile's P.V is done (done barrier (J-1) % 3: the P.V of
   // tile J+2 cannot run before this warp arrives, and that of tile J-4
