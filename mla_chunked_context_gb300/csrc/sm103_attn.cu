@@ -348,7 +348,8 @@ __device__ __forceinline__ bool softmax_tile1(const AttnParams &p, uint32_t s_co
 // partial into the final output -- as the launch asks.  All threads of the
 // CTA meet at one barrier.  Returns the AND over the threads of `ok`.
 __device__ __forceinline__ bool unit_epilogue1(const AttnParams &p, uint32_t o_col, float *xl,
-                                               uint32_t b_odone, uint32_t odone_parity, int wg,
+                                               uint8_t *stage, uint32_t b_odone,
+                                               uint32_t odone_parity, int wg,
                                                int row, int lane, int h, int seq, int slot,
                                                int q_beg, int nq, int qpos, int n_tiles,
                                                float m_used, float l, bool ok) {
@@ -400,6 +401,13 @@ __device__ __forceinline__ bool unit_epilogue1(const AttnParams &p, uint32_t o_c
       lse = m2 + logf(eo + en);
     }
   }
+  // the result rows go through shared memory (`stage`: 128 rows x 512 B of
+  // float32, 16-byte chunk k of row r at chunk k ^ (r % 32), conflict-free
+  // both ways; then a write flag per row), so that each warp store below
+  // writes one whole row: a thread per row storing its own row made each
+  // warp instruction touch 32 rows H x 512 B apart
+  float4 *st4 = reinterpret_cast<float4 *>(stage);
+  int *row_write = reinterpret_cast<int *>(stage + BQ * DV * 4);
   if (okv && n_tiles > 0) {
 #pragma unroll
     for (int c = 0; c < DV / 2 / 16; ++c) {
@@ -407,44 +415,60 @@ __device__ __forceinline__ bool unit_epilogue1(const AttnParams &p, uint32_t o_c
       __syncwarp();  // converged after the per-lane stores of the previous piece
       tmem_ld16(o_col + uint32_t(c * 16), ra);
       tmem_wait_ld();
-      if (write) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v[4];
+      for (int e = 0; e < 4; ++e) {
+        float v[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            v[k] = (w_new != 0.f) ? __uint_as_float(ra[4 * e + k]) * w_new : 0.f;
-          float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
-          if (w_old != 0.f) {  // only when the stored LSE is finite (have_old)
-            const float4 ovv = ov[c * 4 + e];
-            o4.x += w_old * ovv.x;
-            o4.y += w_old * ovv.y;
-            o4.z += w_old * ovv.z;
-            o4.w += w_old * ovv.w;
-          }
-          const int64_t col = (int64_t(t) * p.H + h) * DV + wg * (DV / 2) + c * 16 + e * 4;
-          if (!fin) {
-            reinterpret_cast<float4 *>(orow + c * 16)[e] = o4;
-          } else if (p.fout_bf16) {
-            uint2 b2;
-            b2.x = pack_bf16(o4.x, o4.y);
-            b2.y = pack_bf16(o4.z, o4.w);
-            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + col) = b2;
-          } else {
-            *reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + col) = o4;
-          }
+        for (int k = 0; k < 4; ++k)
+          v[k] = (w_new != 0.f) ? __uint_as_float(ra[4 * e + k]) * w_new : 0.f;
+        float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
+        if (w_old != 0.f) {  // only when the stored LSE is finite (have_old)
+          const float4 ovv = ov[c * 4 + e];
+          o4.x += w_old * ovv.x;
+          o4.y += w_old * ovv.y;
+          o4.z += w_old * ovv.z;
+          o4.w += w_old * ovv.w;
         }
+        const int k = wg * (DV / 8) + c * 4 + e;  // 16-byte chunk of the row
+        st4[row * (DV / 4) + (k ^ (row & 31))] = o4;
       }
     }
-  } else if (write && n_tiles == 0 && !accumulate) {
-    for (int c = 0; c < DV / 2; c += 4)
-      *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    // no key tiles: zeros (stored only where the row is written)
+#pragma unroll 1
+    for (int c = 0; c < DV / 8; ++c)
+      st4[row * (DV / 4) + ((wg * (DV / 8) + c) ^ (row & 31))] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  if (wg == 0) row_write[row] = write ? 1 : 0;
   if (write && wg == 0) {
     if (!fin)
       *lse_dst = lse;
     else if (p.flse)
       p.flse[li] = lse;
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");  // the 256 softmax threads
+  // warp w of the softmax warpgroups writes rows 16w .. 16w+15, 16 bytes a lane
+  const int wi = wg * 4 + (row >> 5);
+  const int t0 = t - row;  // the tile's first token
+#pragma unroll 1
+  for (int i = 0; i < BQ / 8; ++i) {
+    const int rr = wi * (BQ / 8) + i;
+    if (!row_write[rr]) continue;
+    const float4 v = st4[rr * (DV / 4) + (lane ^ (rr & 31))];
+    const int64_t rowbase = split ? ((int64_t(slot) * p.H + h) * BQ + rr) * DV
+                                   : (int64_t(t0 + rr) * p.H + h) * DV;
+    if (split) {
+      reinterpret_cast<float4 *>(p.split_o + rowbase)[lane] = v;
+    } else if (!fin) {
+      reinterpret_cast<float4 *>(p.o + rowbase)[lane] = v;
+    } else if (p.fout_bf16) {
+      uint2 b2;
+      b2.x = pack_bf16(v.x, v.y);
+      b2.y = pack_bf16(v.z, v.w);
+      reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + rowbase)[lane] = b2;
+    } else {
+      reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + rowbase)[lane] = v;
+    }
   }
   return okv != 0;
 }
@@ -647,7 +671,9 @@ __global__ void __launch_bounds__(THREADS1, 1)
         break;
     }
     // the unit's last P.V: done barrier (n_tiles-1) % 3, its ((n_tiles-1)/3)-th phase
-    unit_epilogue1(p, o_col, xl, b_odone + 8u * uint32_t((n_tiles + NSBUF - 1) % NSBUF),
+    // the K ring is free once the unit's last P.V is done: the epilogue
+    // stages its rows there
+    unit_epilogue1(p, o_col, xl, sK, b_odone + 8u * uint32_t((n_tiles + NSBUF - 1) % NSBUF),
                    uint32_t(((n_tiles - 1) / NSBUF) & 1), wg, row, lane, h, seq, slot, q_beg, nq,
                    qpos, n_tiles, m_used, l, ok);
   }
