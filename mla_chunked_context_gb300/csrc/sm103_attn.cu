@@ -746,14 +746,16 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
       for (int e = 0; e < HALF; ++e)
         if (e >= valid) sv[e] = neg_inf();
     }
-    float tm[HALF / 2];
+    // the half's max as a tree of three-input maxima
+    float t[22], u[8];
 #pragma unroll
-    for (int e = 0; e < HALF / 2; ++e) tm[e] = fmaxf(sv[e], sv[e + HALF / 2]);
+    for (int i = 0; i < 21; ++i) t[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+    t[21] = sv[63];
 #pragma unroll
-    for (int w = HALF / 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int e = 0; e < w; ++e) tm[e] = fmaxf(tm[e], tm[e + w]);
-    const float mx = tm[0] * p.scale_log2;
+    for (int i = 0; i < 7; ++i) u[i] = fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    u[7] = t[21];
+    const float mx =
+        fmaxf(fmax3(u[0], u[1], u[2]), fmax3(fmax3(u[3], u[4], u[5]), u[6], u[7])) * p.scale_log2;
     float a_first = 1.f;  // this lane's rescale of the tile's first half of P
     if (mx > m_used + kRescaleThreshold || m_used == neg_inf()) {
       const float m_new = fmaxf(mx, m_used);
@@ -784,15 +786,22 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
     }
     const float nbase = (m_used == neg_inf()) ? 0.f : -m_used;
     uint32_t pk[HALF / 2];
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    // exponent arguments two at a time (paired FMA), sums in two paired
+    // accumulators
+    const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nb2 = f2pack(nbase, nbase);
+    uint64_t acc[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
     for (int e = 0; e < HALF / 2; ++e) {
-      const float a = ex2_approx(fmaf(sv[2 * e], p.scale_log2, nbase));
-      const float b = ex2_approx(fmaf(sv[2 * e + 1], p.scale_log2, nbase));
-      ls[e & 3] += a + b;
+      float xa, xb;
+      f2unpack(f2fma(f2pack(sv[2 * e], sv[2 * e + 1]), sc2, nb2), xa, xb);
+      const float a = ex2_approx(xa), b = ex2_approx(xb);
+      acc[e & 1] = f2add(acc[e & 1], f2pack(a, b));
       pk[e] = pack_f16(a, b);
     }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    float s0, s1, s2, s3;
+    f2unpack(acc[0], s0, s1);
+    f2unpack(acc[1], s2, s3);
+    l += (s0 + s1) + (s2 + s3);
     // P of keys [hh*64, hh*64+64) over columns [hh*32, hh*32+32): those S
     // columns are already read (the first half was read before it is
     // overwritten; the second half's own columns lie beyond 64)
