@@ -703,7 +703,10 @@ __global__ void __launch_bounds__(THREADS1, 1)
 // TMEM: S0 [0,128) S1 [128,256) (P of a tile over the first 64 columns of
 // its S buffer), O of warpgroup 0 [256,384), of warpgroup 1 [384,512).
 constexpr int THREADS_LOOP = THREADS + 32;
-constexpr int SMEM_BYTES_LOOP = SMEM_BYTES;
+constexpr int STG_LOOP_BYTES = 8 * 32 * 64;  // a 32 x 64-byte staging tile per softmax warp
+constexpr int SMEM_BYTES_LOOP =
+    1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + STG_LOOP_BYTES + 256;
+static_assert(SMEM_BYTES_LOOP <= 227 * 1024, "looping kernel: shared memory");
 
 // One 128-key tile of the online softmax for a full query row (qpos) of a
 // warpgroup's unit: the row's scores come out of TMEM in two halves of 64
@@ -839,8 +842,8 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
 // arrives on b_ofree once it has read O from TMEM.
 __device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t o_col,
                                                    uint32_t b_odone, uint32_t odone_parity,
-                                                   uint32_t b_ofree, int lane, int h, int seq,
-                                                   int slot, int q_beg, int nq, int qpos,
+                                                   uint32_t b_ofree, uint4 *stg, int lane, int h,
+                                                   int seq, int slot, int q_beg, int nq, int qpos,
                                                    int n_tiles, float m_used, float l, bool ok) {
   if (ok && n_tiles > 0 && !mbar_wait(b_odone, odone_parity)) ok = false;
   ok = __all_sync(0xffffffffu, ok) != 0;
@@ -880,7 +883,24 @@ __device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t
   }
   if (ok && n_tiles > 0) {
     // four pieces of 32 columns; the stored row's piece is loaded before
-    // the TMEM read of the same piece
+    // the TMEM read of the same piece.  The warp's 32 rows go out through
+    // its 32 x 64-byte staging tile: each thread writes its row's 64 bytes
+    // (four 16-byte chunks, XOR-swizzled by row), then each store
+    // instruction writes 64 contiguous bytes of 8 rows (4 lanes per row)
+    // instead of 16 bytes of 32 rows.
+    const int srow = lane >> 2, sk = lane & 3;
+    const int qpos0 = qpos - lane;  // the warp's first row
+    const bool out16 = fin && p.fout_bf16;
+    const uint32_t wmask = __ballot_sync(0xffffffffu, write);
+    // row 8i + srow of the warp starts at dst + i * step (rows 8 apart: 8
+    // query positions, in the same (slot, head) block when split)
+    const int qr = qpos0 + srow;
+    const int64_t row0 = split ? (int64_t(slot) * p.H + h) * BQ + (qr & (BQ - 1))
+                               : int64_t(q_beg + qr) * p.H + h;
+    const int64_t es = out16 ? 2 : 4;
+    char *dst = reinterpret_cast<char *>(split ? p.split_o : (fin ? p.fout : p.o)) +
+                row0 * DV * es;
+    const int64_t step = (split ? 8 : int64_t(8) * p.H) * DV * es;
 #pragma unroll 1
     for (int c = 0; c < DV / 32; ++c) {
       float4 ov[8];
@@ -898,31 +918,52 @@ __device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t
         __syncwarp();
         if (lane == 0) mbar_arrive(b_ofree);
       }
-      if (write) {
+      // float32: two rounds of 16 values (64 bytes a row); bf16: the two
+      // halves of the piece are packed into one 64-byte round
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float4 o4 = make_float4(__uint_as_float(r[4 * e]) * w_new,
-                                  __uint_as_float(r[4 * e + 1]) * w_new,
-                                  __uint_as_float(r[4 * e + 2]) * w_new,
-                                  __uint_as_float(r[4 * e + 3]) * w_new);
+      for (int hh = 0; hh < 2; ++hh) {
+        float4 o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ee = hh * 4 + e;
+          o4[e] = make_float4(__uint_as_float(r[4 * ee]) * w_new,
+                              __uint_as_float(r[4 * ee + 1]) * w_new,
+                              __uint_as_float(r[4 * ee + 2]) * w_new,
+                              __uint_as_float(r[4 * ee + 3]) * w_new);
           if (w_old != 0.f) {  // only when the stored LSE is finite (have_old)
-            o4.x += w_old * ov[e].x;
-            o4.y += w_old * ov[e].y;
-            o4.z += w_old * ov[e].z;
-            o4.w += w_old * ov[e].w;
-          }
-          const int64_t col = (int64_t(t) * p.H + h) * DV + c * 32 + e * 4;
-          if (!fin) {
-            reinterpret_cast<float4 *>(orow + c * 32)[e] = o4;
-          } else if (p.fout_bf16) {
-            uint2 b2;
-            b2.x = pack_bf16(o4.x, o4.y);
-            b2.y = pack_bf16(o4.z, o4.w);
-            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.fout) + col) = b2;
-          } else {
-            *reinterpret_cast<float4 *>(static_cast<float *>(p.fout) + col) = o4;
+            o4[e].x += w_old * ov[ee].x;
+            o4[e].y += w_old * ov[ee].y;
+            o4[e].z += w_old * ov[ee].z;
+            o4[e].w += w_old * ov[ee].w;
           }
         }
+        if (out16) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint4 v = make_uint4(pack_bf16(o4[2 * k].x, o4[2 * k].y),
+                                       pack_bf16(o4[2 * k].z, o4[2 * k].w),
+                                       pack_bf16(o4[2 * k + 1].x, o4[2 * k + 1].y),
+                                       pack_bf16(o4[2 * k + 1].z, o4[2 * k + 1].w));
+            stg[lane * 4 + ((hh * 2 + k) ^ ((lane >> 1) & 3))] = v;
+          }
+          if (hh == 0) continue;  // the row's 64 bytes are complete after the second half
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            stg[lane * 4 + (k ^ ((lane >> 1) & 3))] =
+                make_uint4(__float_as_uint(o4[k].x), __float_as_uint(o4[k].y),
+                           __float_as_uint(o4[k].z), __float_as_uint(o4[k].w));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 8 * i + srow;
+          const uint4 v = stg[rr * 4 + (sk ^ ((rr >> 1) & 3))];
+          if ((wmask >> rr) & 1u)
+            reinterpret_cast<uint4 *>(dst + i * step + (out16 ? c * 64 : (c * 32 + hh * 16) * 4))[sk] =
+                v;
+        }
+        __syncwarp();  // the staging tile is rewritten next round
       }
     }
   } else {
@@ -974,7 +1015,8 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + Q_BYTES;
   uint8_t *sV = sK + RING * K_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sV + RING * V_BYTES + XCHG_BYTES);
+  uint8_t *sStg = sV + RING * V_BYTES;  // the softmax warps' epilogue staging tiles
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sStg + STG_LOOP_BYTES);
   const uint32_t b_q = smem_u32(bars + 0), b_qready = smem_u32(bars + 1);
   const uint32_t b_kfull = smem_u32(bars + 2), b_kempty = smem_u32(bars + 2 + RING);
   const uint32_t b_vfull = smem_u32(bars + 2 + 2 * RING), b_vempty = smem_u32(bars + 2 + 3 * RING);
@@ -1226,8 +1268,8 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
         ++jw;
       }
       ok = unit_epilogue_full(p, o_col, b_odone + 8 * wg, uint32_t((jw - 1) & 1),
-                              b_ofree + 8 * wg, lane, x.h, x.seq, x.slot, q_beg, nq, qpos,
-                              n_tiles, m_used, l, ok);
+                              b_ofree + 8 * wg, reinterpret_cast<uint4 *>(sStg) + (warp - 2) * 128,
+                              lane, x.h, x.seq, x.slot, q_beg, nq, qpos, n_tiles, m_used, l, ok);
       J0 += n_tiles;
     }
   }
