@@ -121,6 +121,19 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 // 2^x with the SFU's approximate exponent (relative error below 2^-21; P is
 // then rounded to fp16, 2^-11).  Arguments here are at most 8 (the lazily
 // raised running max), results below 2^-126 flush to zero.
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -842,7 +855,7 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
 // arrives on b_ofree once it has read O from TMEM.
 __device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t o_col,
                                                    uint32_t b_odone, uint32_t odone_parity,
-                                                   uint32_t b_ofree, uint4 *stg, int lane, int h,
+                                                   uint32_t b_ofree, uint32_t stg, int lane, int h,
                                                    int seq, int slot, int q_beg, int nq, int qpos,
                                                    int n_tiles, float m_used, float l, bool ok) {
   if (ok && n_tiles > 0 && !mbar_wait(b_odone, odone_parity)) ok = false;
@@ -944,21 +957,21 @@ __device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t
                                        pack_bf16(o4[2 * k].z, o4[2 * k].w),
                                        pack_bf16(o4[2 * k + 1].x, o4[2 * k + 1].y),
                                        pack_bf16(o4[2 * k + 1].z, o4[2 * k + 1].w));
-            stg[lane * 4 + ((hh * 2 + k) ^ ((lane >> 1) & 3))] = v;
+            st_shared_v4(stg + uint32_t(lane * 64 + (((hh * 2 + k) ^ ((lane >> 1) & 3)) << 4)), v);
           }
           if (hh == 0) continue;  // the row's 64 bytes are complete after the second half
         } else {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            stg[lane * 4 + (k ^ ((lane >> 1) & 3))] =
-                make_uint4(__float_as_uint(o4[k].x), __float_as_uint(o4[k].y),
-                           __float_as_uint(o4[k].z), __float_as_uint(o4[k].w));
+            st_shared_v4(stg + uint32_t(lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)),
+                         make_uint4(__float_as_uint(o4[k].x), __float_as_uint(o4[k].y),
+                                    __float_as_uint(o4[k].z), __float_as_uint(o4[k].w)));
         }
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int rr = 8 * i + srow;
-          const uint4 v = stg[rr * 4 + (sk ^ ((rr >> 1) & 3))];
+          const uint4 v = ld_shared_v4(stg + uint32_t(rr * 64 + ((sk ^ ((rr >> 1) & 3)) << 4)));
           if ((wmask >> rr) & 1u)
             reinterpret_cast<uint4 *>(dst + i * step + (out16 ? c * 64 : (c * 32 + hh * 16) * 4))[sk] =
                 v;
@@ -1268,7 +1281,7 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
         ++jw;
       }
       ok = unit_epilogue_full(p, o_col, b_odone + 8 * wg, uint32_t((jw - 1) & 1),
-                              b_ofree + 8 * wg, reinterpret_cast<uint4 *>(sStg) + (warp - 2) * 128,
+                              b_ofree + 8 * wg, smem_u32(sStg) + uint32_t((warp - 2) * 2048),
                               lane, x.h, x.seq, x.slot, q_beg, nq, qpos, n_tiles, m_used, l, ok);
       J0 += n_tiles;
     }
