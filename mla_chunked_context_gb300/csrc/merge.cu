@@ -11,6 +11,8 @@
 // is loaded only when that side is needed (its LSE finite and the token below
 // prefix_num_tokens), so garbage or NaN in an unused side is never read into
 // arithmetic and its bytes never move.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace mla {
@@ -115,9 +117,17 @@ __global__ void fill_empty_rows_kernel(float *__restrict__ o, float *__restrict_
   const int lo = slices[2 * blockIdx.y], hi = slices[2 * blockIdx.y + 1];
   const int64_t n_o = int64_t(hi - lo) * H * Dv;
   const int64_t base = int64_t(lo) * H * Dv;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_o;
-       i += int64_t(gridDim.x) * blockDim.x)
-    o[base + i] = 0.f;
+  if ((Dv & 3) == 0 && (reinterpret_cast<uintptr_t>(o) & 15) == 0) {
+    // 16-byte stores: the slice's rows are one contiguous block
+    float4 *o4 = reinterpret_cast<float4 *>(o + base);
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_o / 4;
+         i += int64_t(gridDim.x) * blockDim.x)
+      o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_o;
+         i += int64_t(gridDim.x) * blockDim.x)
+      o[base + i] = 0.f;
+  }
   const int64_t n_l = int64_t(hi - lo) * H;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_l;
        i += int64_t(gridDim.x) * blockDim.x) {
@@ -191,7 +201,9 @@ int launch_merge(void *out, float *out_lse, const void *prefix_o, const float *p
 int launch_fill_empty_rows(float *o, float *lse, int T, int H, int Dv, int num_slices,
                            const int32_t *slices, cudaStream_t s) {
   if (num_slices == 0) return MLA_OK;
-  dim3 grid(32, num_slices);
+  // about four blocks per SM over all slices
+  const int per_slice = std::max(4, std::min(256, 4 * num_sms() / num_slices));
+  dim3 grid(per_slice, num_slices);
   launch_begin(s);
   fill_empty_rows_kernel<<<grid, 256, 0, s>>>(o, lse, T, H, Dv, slices);
   return launch_status(s, "fill_empty_rows_kernel");
