@@ -805,6 +805,26 @@ def test_prefill_groups_small_chunks_into_one_launch_set():
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+def test_prefill_long_new_tokens_loop_path():
+    """Long runs of new tokens (8.5 causal key tiles per unit on average)
+    with prepared queries: the new-token attention and the final merge run
+    on the looping kernel (its limit for prepared queries is above the one
+    for the caller's queries); a request with context, one without, one
+    with context after it; compared in full."""
+    ctx, ql = [300, 0, 130], [2048, 700, 1100]
+    w = W.scaled(W.workload("uniform"), context_lens=ctx, query_lens=ql, num_heads=16,
+                 row_budget=1024, max_context_chunk=512, split_alignment=64, seed=59)
+    x = W.make_inputs(w)
+    M.mla_profile_begin()
+    out, lse = _run_prefill(w, x)
+    names = [r[0] for r in M.mla_profile_end()]
+    assert names[-1] == "attn_tc_loop_kernel"
+    ro, rl, _ = _oracle_prefill(w, x)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_prefill_many_short_requests_loop_path():
     # 64 heads and many short requests: more (query tile, head) units than
     # SMs with few key tiles each, so the group attention and the new-token
