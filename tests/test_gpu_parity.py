@@ -825,6 +825,26 @@ def test_prefill_long_new_tokens_loop_path():
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+def test_prefill_loop_path_continuation_chunks():
+    """Context chunks of 1024 keys (8 key tiles per unit) over 64 heads and a
+    few query tiles: with prepared queries the group attention runs on the
+    looping kernel, and the later chunks of a split request accumulate into
+    its partial there; compared in full."""
+    ctx, ql = [2500, 1800, 0, 2200], [300, 260, 50, 280]
+    w = W.scaled(W.workload("uniform"), context_lens=ctx, query_lens=ql, num_heads=64,
+                 row_budget=2048, max_context_chunk=1024, split_alignment=64, seed=61)
+    x = W.make_inputs(w)
+    M.mla_profile_begin()
+    out, lse = _run_prefill(w, x)
+    names = [r[0] for r in M.mla_profile_end()]
+    assert names.count("attn_tc_loop_kernel") >= 2
+    ro, rl, plans = _oracle_prefill(w, x)
+    assert any(p.is_continuation for p in plans)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_prefill_many_short_requests_loop_path():
     # 64 heads and many short requests: more (query tile, head) units than
     # SMs with few key tiles each, so the group attention and the new-token
