@@ -1076,15 +1076,18 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
   struct Unit {
     int h, seq, qt, slot, kt0, n_tiles;
   };
-  // units item-major (the items come longest first), the CTA's k-th unit
-  // taken from the k-th block of gridDim.x units in zigzag order, so the
-  // long items spread over the CTAs
+  // units head-major (unit u: head u / n_items, item u % n_items; the items
+  // come longest first), the CTA's k-th unit taken from the k-th block of
+  // gridDim.x units in zigzag order: the units that run at the same time
+  // are every query tile of a few heads, so each (sequence, head)'s keys are
+  // read from DRAM once and shared in L2 by its query tiles, and the long
+  // items spread over the CTAs
   const int G = int(gridDim.x), b = int(blockIdx.x);
   auto unit_at = [&](int k) { return k * G + ((k & 1) ? G - 1 - b : b); };
   auto unit_of = [&](int u) {
     Unit x;
-    const int item = u / p.H;
-    x.h = u - item * p.H;
+    x.h = u / p.n_items;
+    const int item = u - x.h * p.n_items;
     const int4 it = p.items[item];
     x.seq = it.x;
     x.qt = it.y & 0xffff;
