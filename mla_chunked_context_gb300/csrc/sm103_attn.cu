@@ -118,9 +118,7 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
-// 2^x with the SFU's approximate exponent (relative error below 2^-21; P is
-// then rounded to fp16, 2^-11).  Arguments here are at most 8 (the lazily
-// raised running max), results below 2^-126 flush to zero.
+// 16-byte shared-memory store / load at a 32-bit shared address
 __device__ __forceinline__ void st_shared_v4(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
@@ -134,6 +132,10 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
                : "memory");
   return v;
 }
+
+// 2^x with the SFU's approximate exponent (relative error below 2^-21; P is
+// then rounded to fp16, 2^-11).  Arguments here are at most 8 (the lazily
+// raised running max), results below 2^-126 flush to zero.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
