@@ -68,8 +68,6 @@ constexpr int KBOX = BKV * 64 * 2;           // 16 KB: 128 rows x 64 16-bit
 constexpr int Q_BYTES = 3 * QBOX;            // 48 KB
 constexpr int K_BYTES = 3 * KBOX;            // 48 KB: K_nope (2 boxes) + k_pe
 constexpr int V_BYTES = 2 * KBOX;            // 32 KB
-constexpr int XCHG_BYTES = 4 * 128 * 4;       // per-row (m, l) of both warpgroups
-constexpr int SMEM_BYTES = 1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + XCHG_BYTES + 256;
 // one-CTA kernel: half-row maxima [2 warpgroups][2 tile parities][128],
 // row sums [2][128], per-warp ok flags [2 parities][8]
 constexpr int XCHG1_BYTES = (2 * 2 * 128 + 2 * 128) * 4 + 2 * 8 * 4;
@@ -693,6 +691,386 @@ __global__ void __launch_bounds__(THREADS1, 1)
                    qpos, n_tiles, m_used, l, ok);
   }
   if (warp < 2 || warp == THREADS1 / 32 - 1) __syncthreads_and(1);  // the softmax warps' vote
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Epilogue of one unit of the persistent one-CTA kernel: as
+// unit_epilogue1, except that the two softmax warpgroups meet at named
+// barrier 1 (the other warps have run ahead into the next unit), the row
+// sums alternate between two buffers by unit (xl: this unit's), and each
+// warp writes its own 32 half rows through its 1 KB staging tile (`stg`,
+// 32 rows x 32 bytes, 16-byte chunks XOR-swizzled by row; the K ring holds
+// the next unit's keys): each store instruction writes 32 contiguous bytes
+// of 16 rows.  Returns the AND over the softmax threads of `ok`.
+__device__ __forceinline__ bool unit_epilogue_p(const AttnParams &p, uint32_t o_col, float *xl,
+                                                uint32_t stg, uint32_t b_odone,
+                                                uint32_t odone_parity, int wg, int row, int lane,
+                                                int h, int seq, int slot, int q_beg, int nq,
+                                                int qpos, int n_tiles, float m_used, float l,
+                                                bool ok) {
+  if (ok && n_tiles > 0 && !__all_sync(0xffffffffu, mbar_wait(b_odone, odone_parity))) ok = false;
+  xl[wg * BQ + row] = l;
+  const int t = q_beg + qpos;
+  const int64_t li = int64_t(h) * p.T + t;
+  const bool fin = p.fout != nullptr;
+  const bool split = slot >= 0;
+  const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
+  const bool merge_old = accumulate || (fin && t < p.pnt);
+  const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
+  const float *orow = p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);  // the stored partial
+  tc_fence_before();
+  const bool okv = softmax_bar_and(ok);  // both warpgroups' sums are in xl
+  tc_fence_after();
+  const float lsum = xl[row] + xl[BQ + row];
+  const bool store = okv && qpos < nq;
+  float lse = (lsum > 0.f) ? (m_used + __log2f(lsum)) * 0.69314718055994531f : neg_inf();
+  float w_new = (lsum > 0.f) ? 1.f / lsum : 0.f, w_old = 0.f;
+  bool write = store;
+  if (store && merge_old) {
+    if (lsum == 0.f) {
+      if (!fin) {
+        write = false;  // nothing new: keep the stored partial
+      } else if (!is_neg_inf(old)) {
+        w_old = 1.f;  // the result is the context partial alone
+        lse = old;
+      }
+    } else if (!is_neg_inf(old)) {
+      const float m2 = fmaxf(old, lse);
+      const float eo = expf(old - m2), en = expf(lse - m2);
+      w_old = eo / (eo + en);
+      w_new *= en / (eo + en);
+      lse = m2 + logf(eo + en);
+    }
+  }
+  if (write && wg == 0) {
+    if (split)
+      p.split_lse[(int64_t(slot) * p.H + h) * BQ + row] = lse;
+    else if (!fin)
+      p.lse[li] = lse;
+    else if (p.flse)
+      p.flse[li] = lse;
+  }
+  // the warp's rows: row 16i + (lane >> 1) of the warp at dst + i * step,
+  // this warpgroup's 64 columns; lane & 1 the 16-byte chunk of a round
+  const uint32_t wmask = __ballot_sync(0xffffffffu, write);
+  const int srow = lane >> 1, sk = lane & 1;
+  const int r0 = row - lane + srow;  // tile row of this lane's first stored row
+  const bool out16 = fin && p.fout_bf16;
+  const int64_t es = out16 ? 2 : 4;
+  const int64_t grow = split ? (int64_t(slot) * p.H + h) * BQ + r0
+                             : int64_t(t - row + r0) * p.H + h;
+  char *dst = reinterpret_cast<char *>(split ? p.split_o : (fin ? p.fout : p.o)) +
+              (grow * DV + wg * (DV / 2)) * es;
+  const int64_t step = (split ? 16 : int64_t(16) * p.H) * DV * es;
+  const bool have = okv && n_tiles > 0;
+#pragma unroll
+  for (int c = 0; c < DV / 2 / 16; ++c) {
+    // the stored row's piece first, then the TMEM read of the same piece
+    float4 ov[4];
+    if (w_old != 0.f) {  // only when the stored LSE is finite
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ov[i] = reinterpret_cast<const float4 *>(orow)[c * 4 + i];
+    }
+    uint32_t ra[16];
+    if (have) {
+      __syncwarp();
+      tmem_ld16(o_col + uint32_t(c * 16), ra);
+      tmem_wait_ld();
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {  // 8 values (32 bytes) of the row a round
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = hh * 2 + k;     // float4 e of this piece of 16
+        float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (have) {
+          o4 = make_float4(__uint_as_float(ra[4 * e]) * w_new, __uint_as_float(ra[4 * e + 1]) * w_new,
+                           __uint_as_float(ra[4 * e + 2]) * w_new,
+                           __uint_as_float(ra[4 * e + 3]) * w_new);
+          if (w_new == 0.f) o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (w_old != 0.f) {
+          const float4 ovv = ov[e];
+          o4.x += w_old * ovv.x;
+          o4.y += w_old * ovv.y;
+          o4.z += w_old * ovv.z;
+          o4.w += w_old * ovv.w;
+        }
+        st_shared_v4(stg + uint32_t(lane * 32 + ((k ^ ((lane >> 2) & 1)) << 4)),
+                     make_uint4(__float_as_uint(o4.x), __float_as_uint(o4.y),
+                                __float_as_uint(o4.z), __float_as_uint(o4.w)));
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int rr = 16 * i + srow;
+        const uint4 v = ld_shared_v4(stg + uint32_t(rr * 32 + ((sk ^ ((rr >> 2) & 1)) << 4)));
+        if ((wmask >> rr) & 1u) {
+          const int64_t col = int64_t(c * 16 + hh * 8 + sk * 4);  // within the half row
+          if (out16) {
+            uint2 b2;
+            b2.x = pack_bf16(__uint_as_float(v.x), __uint_as_float(v.y));
+            b2.y = pack_bf16(__uint_as_float(v.z), __uint_as_float(v.w));
+            *reinterpret_cast<uint2 *>(dst + i * step + col * 2) = b2;
+          } else {
+            *reinterpret_cast<uint4 *>(dst + i * step + col * 4) = v;
+          }
+        }
+      }
+      __syncwarp();  // the staging tile is rewritten next round
+    }
+  }
+  return okv;
+}
+
+// The one-CTA attention as a persistent kernel, for launches of prepared
+// queries with several units per SM: a CTA per SM walks the units
+// u = blockIdx.x, + gridDim.x, ... (head-major, as the one-unit kernel's
+// CTAs run) with its barriers and TMEM kept and the tiles of all its units
+// numbered on (tile J of the CTA: S buffer, P-full and P.V-done J % 3, K/V
+// stage J % 2).  The next unit's Q is loaded once the last S of the current
+// unit is done, and its K/V tiles and first S products follow while the
+// softmax warps still run the current unit's last tiles and epilogue (with
+// a CTA per unit, the start and the end of each were exposed: about a
+// quarter of a 32-key-tile unit).  The next unit's first P.V overwrites O
+// only after the softmax warps have read it: they arrive on that tile's
+// P-full after their epilogue.  The softmax warps re-read a unit's
+// description from the launch parameters.
+constexpr int XCHG2_BYTES = (2 * 2 * 128 + 2 * 2 * 128) * 4;  // xm; xl [2 unit parities]
+constexpr int STG2_BYTES = 8 * 32 * 32;                         // 1 KB per softmax warp
+constexpr int SMEM_BYTES2 =
+    1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + XCHG2_BYTES + STG2_BYTES + 256;
+static_assert(SMEM_BYTES2 <= 227 * 1024, "persistent kernel: shared memory");
+
+__global__ void __launch_bounds__(THREADS1, 1)
+    attn_tc_persist_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_kv,
+                           const __grid_constant__ CUtensorMap tm_lat,
+                           const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sQ = smem;
+  uint8_t *sK = sQ + Q_BYTES;
+  uint8_t *sV = sK + RING * K_BYTES;
+  float *xm = reinterpret_cast<float *>(sV + RING * V_BYTES);  // [2 wg][2 tile parities][128]
+  float *xl = xm + 2 * 2 * BQ;                                 // [2 unit parities][2 wg][128]
+  uint8_t *sStg = reinterpret_cast<uint8_t *>(xl + 2 * 2 * BQ);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sStg + STG2_BYTES);
+  // q, qfree, K full [2], V full [2], S full [3], P full [3] (8 softmax
+  // warps), P.V done [3], each issuer's MMAs done
+  const uint32_t b_q = smem_u32(bars + 0), b_qfree = smem_u32(bars + 1);
+  const uint32_t b_kfull = smem_u32(bars + 2), b_vfull = smem_u32(bars + 4);
+  const uint32_t b_sfull = smem_u32(bars + 6), b_pfull = smem_u32(bars + 9);
+  const uint32_t b_odone = smem_u32(bars + 12), b_done = smem_u32(bars + 15);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_units = p.n_items * p.H;
+  const int G = int(gridDim.x), b0 = int(blockIdx.x);
+  // unit u: head u / n_items, item u % n_items
+  auto item_of = [&](int u, int &h) {
+    h = u / p.n_items;
+    return p.items[u - h * p.n_items];
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    mbar_init(b_qfree, 1);
+    for (int s = 0; s < RING; ++s) {
+      mbar_init(b_kfull + 8 * s, 1);
+      mbar_init(b_vfull + 8 * s, 1);
+    }
+    for (int b = 0; b < NSBUF; ++b) {
+      mbar_init(b_sfull + 8 * b, 1);
+      mbar_init(b_pfull + 8 * b, 8);
+      mbar_init(b_odone + 8 * b, 1);
+    }
+    mbar_init(b_done, 1);
+    mbar_init(b_done + 8, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane < 2) {
+      // ---------------- TMA producers: lane 0 Q and K, lane 1 V
+      const bool kl = lane == 0;
+      if (kl) {
+        prefetch_map(&tm_q);
+        prefetch_map(&tm_kv);
+        prefetch_map(&tm_lat);
+      }
+      int issued[RING];
+      for (int s = 0; s < RING; ++s) issued[s] = -1;
+      int q_issued = -1;
+      const uint32_t full = kl ? b_kfull : b_vfull;
+      int J = 0, kq = 0;  // the CTA's key tiles; its units with tiles
+      bool ok = true;
+      for (int u = b0; ok && u < n_units; u += G) {
+        int h;
+        const int4 it = item_of(u, h);
+        const int n_tiles = it.w - it.z;
+        if (n_tiles <= 0) continue;
+        const int seq = it.x, qt = it.y & 0xffff, kt0 = it.z;
+        const int k_beg = __ldg(p.k_loc + seq);
+        if (kl) {
+          // the previous unit's S products are done with the Q tile
+          if (kq > 0 && !mbar_wait(b_qfree, uint32_t((kq - 1) & 1))) break;
+          const int qy = h * p.T + __ldg(p.q_loc + seq) + qt * BQ;
+          mbar_expect_tx(b_q, Q_BYTES);
+          tma_load_2d(smem_u32(sQ), &tm_q, b_q, 0, qy);
+          tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, 64, qy);
+          tma_load_2d(smem_u32(sQ + 2 * QBOX), &tm_q, b_q, 128, qy);
+          q_issued = kq & 1;
+        }
+        ++kq;
+        for (int j = 0; j < n_tiles; ++j, ++J) {
+          const int s = J % RING;
+          const int krow = k_beg + (kt0 + j) * BKV;
+          // stage s held tile J-2: its K is free once S of tile J-2 is done,
+          // its V once the P.V of tile J-2 is
+          if (J >= RING && !mbar_wait((kl ? b_sfull : b_odone) + 8 * ((J - 2) % NSBUF),
+                                      uint32_t(((J - 2) / NSBUF) & 1))) {
+            ok = false;
+            break;
+          }
+          if (kl) {
+            uint8_t *k = sK + s * K_BYTES;
+            mbar_expect_tx(full + 8 * s, K_BYTES);
+            tma_load_3d(smem_u32(k), &tm_kv, full + 8 * s, 0, krow, h);
+            tma_load_3d(smem_u32(k + KBOX), &tm_kv, full + 8 * s, 64, krow, h);
+            tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, full + 8 * s, 512, krow);
+          } else {
+            uint8_t *v = sV + s * V_BYTES;
+            mbar_expect_tx(full + 8 * s, V_BYTES);
+            tma_load_3d(smem_u32(v), &tm_kv, full + 8 * s, DN, krow, h);
+            tma_load_3d(smem_u32(v + KBOX), &tm_kv, full + 8 * s, DN + 64, krow, h);
+          }
+          issued[s] = int((J / RING) & 1);
+        }
+      }
+      // every issued load has landed before the CTA may exit
+      if (kl && q_issued >= 0) mbar_wait(b_q, uint32_t(q_issued));
+      for (int s = 0; s < RING; ++s)
+        if (issued[s] >= 0) mbar_wait(full + 8 * s, uint32_t(issued[s]));
+    }
+  } else if (warp == 1 || warp == THREADS1 / 32 - 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuers: warp 1 the S products, the last warp
+      // the P.V products, each committing its own (as in the one-unit kernel)
+      constexpr uint32_t idesc_nope = idesc_f16kind(BQ, BKV, false, false, false);  // fp16
+      constexpr uint32_t idesc_rope = idesc_f16kind(BQ, BKV, false, false, true);   // bf16
+      constexpr uint32_t idesc_o = idesc_f16kind(BQ, DV, false, true, false);       // fp16
+      bool ok = true;
+      int J = 0, kq = 0;
+      if (warp == 1) {
+        const uint64_t dq = desc_kmajor_sw128(smem_u32(sQ));
+        const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK));
+        for (int u = b0; ok && u < n_units; u += G) {
+          int h;
+          const int4 it = item_of(u, h);
+          const int n_tiles = it.w - it.z;
+          if (n_tiles <= 0) continue;
+          if (!mbar_wait(b_q, uint32_t(kq & 1))) break;
+          ++kq;
+          for (int j = 0; j < n_tiles; ++j, ++J) {
+            const int s = J % RING, b = J % NSBUF;
+            if ((J >= NSBUF &&
+                 !mbar_wait(b_odone + 8 * b, uint32_t(((J - NSBUF) / NSBUF) & 1))) ||
+                !mbar_wait(b_kfull + 8 * s, uint32_t((J / RING) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dk = dk0 + uint64_t((s * K_BYTES) >> 4);
+            const uint32_t d = tmem + COL_S + uint32_t(b * BKV);
+#pragma unroll
+            for (int kk = 0; kk < DQK / 16; ++kk) {
+              const uint64_t off = uint64_t(((kk >> 2) * QBOX + (kk & 3) * 32) >> 4);
+              mma_bf16(d, dq + off, dk + off, kk < DN / 16 ? idesc_nope : idesc_rope, kk != 0);
+            }
+            mma_commit(b_sfull + 8 * b);  // S ready; K stage s free
+            if (j == n_tiles - 1) mma_commit(b_qfree);  // the unit's last S: Q is free
+          }
+        }
+      } else {
+        const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), KBOX);
+        for (int u = b0; ok && u < n_units; u += G) {
+          int h;
+          const int4 it = item_of(u, h);
+          const int n_tiles = it.w - it.z;
+          for (int j = 0; j < n_tiles; ++j, ++J) {
+            const int s = J % RING, b = J % NSBUF;
+            // P-full of the unit's first tile also means the softmax warps
+            // have read the previous unit's O
+            if (!mbar_wait(b_vfull + 8 * s, uint32_t((J / RING) & 1)) ||
+                !mbar_wait(b_pfull + 8 * b, uint32_t((J / NSBUF) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t pa = tmem + COL_S + uint32_t(b * BKV);
+            const uint64_t dv = dv0 + uint64_t((s * V_BYTES) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk)
+              mma_f16_ts(tmem + COL_O1, pa + uint32_t((kk >> 2) * HALF + (kk & 3) * 8),
+                         dv + uint64_t((kk * 2048) >> 4), idesc_o, (j | kk) != 0);
+            mma_commit(b_odone + 8 * b);  // P.V done; V stage s and S buffer b free
+          }
+        }
+      }
+      const uint32_t dbar = b_done + (warp == 1 ? 0u : 8u);
+      mma_commit(dbar);
+      mbar_wait(dbar, 0);
+    }
+  } else {
+    // ---------------- softmax warpgroups
+    const int wg = (warp - 2) >> 2;        // 0: A (keys 0-63 of a tile), 1: B (64-127)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;   // query row of the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const uint32_t o_col = tmem + lane_off + COL_O1 + uint32_t(wg * (DV / 2));
+    const uint32_t stg = smem_u32(sStg) + uint32_t((warp - 2) * 1024);
+    int J = 0, ku = 0;
+    bool ok = true;
+    for (int u = b0; u < n_units; u += G, ++ku) {
+      int h;
+      const int4 it = item_of(u, h);
+      const int seq = it.x, qt = it.y & 0xffff, slot = (it.y >> 16) - 1;
+      const int kt0 = it.z, n_tiles = it.w - it.z > 0 ? it.w - it.z : 0;
+      const int q_beg = __ldg(p.q_loc + seq), nq = __ldg(p.q_loc + seq + 1) - q_beg;
+      const int nk = __ldg(p.k_loc + seq + 1) - __ldg(p.k_loc + seq);
+      const int qpos = qt * BQ + row;
+      float m_used = neg_inf(), l = 0.f;
+      prefetch_partial(p, h, seq, slot, q_beg, nq, qpos, wg);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int JJ = J + j, b = JJ % NSBUF;
+        const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(b * BKV + wg * HALF);
+        if (!softmax_tile1(p, s_col, o_col, b_sfull + 8 * b, uint32_t((JJ / NSBUF) & 1), b_odone,
+                           b_pfull + 8 * b, JJ, (kt0 + j) * BKV + wg * HALF, nk, qpos, xm, wg,
+                           row, ok, m_used, l, lane))
+          break;
+      }
+      const int JL = J + n_tiles - 1;  // the unit's last tile
+      ok = unit_epilogue_p(p, o_col, xl + (ku & 1) * 2 * BQ, stg,
+                           b_odone + 8u * uint32_t((JL + NSBUF) % NSBUF),
+                           uint32_t((JL / NSBUF) & 1), wg, row, lane, h, seq, slot, q_beg, nq,
+                           qpos, n_tiles, m_used, l, ok);
+      J += n_tiles;
+      if (!ok) break;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1409,6 +1787,13 @@ constexpr int kMinSplitTiles = 16;
 // final merge: 0.96 against 1.10 ms)
 constexpr int kLoopTiles = 4;
 constexpr int kLoopTilesPrepared = 16;
+// the persistent one-unit kernel: launches of prepared queries with at
+// least this many units per SM, and at most this many key tiles per unit on
+// average (longer units hide a CTA's start and end themselves, and a CTA
+// per unit lets the hardware even out the last wave: 4 x 2048 x 65536 took
+// 28.96-29.16 ms persistent against 28.56-28.58 ms)
+constexpr int kPersistUnits = 2;
+constexpr int kPersistTiles = 64;
 
 int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
                int H, const SplitScratch *split, bool skip_keyless, std::vector<Item> &items,
@@ -1495,7 +1880,10 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES1) != cudaSuccess ||
         cudaFuncSetAttribute(attn_tc_loop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES_LOOP) != cudaSuccess)
+                             SMEM_BYTES_LOOP) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_tc_persist_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES2) != cudaSuccess)
       return MLA_ERR_CUDA;
     attr_set = true;
   }
@@ -1532,12 +1920,22 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     for (int k = 0; k < n; ++k) tiles += items[b + k].kt1 - items[b + k].kt0;
     const int loop_tiles = q_prepared ? kLoopTilesPrepared : kLoopTiles;
     const bool loop = int64_t(n) * H > num_sms() && tiles <= int64_t(loop_tiles) * n;
+    // prepared queries, at least kPersistUnits units per SM and at most
+    // kPersistTiles key tiles per unit on average: one CTA per SM walks
+    // them, the next unit's loads and first S products overlapping this
+    // one's last tiles and epilogue
+    const bool persist = !loop && q_prepared &&
+                         int64_t(n) * H >= int64_t(kPersistUnits) * num_sms() &&
+                         tiles <= int64_t(kPersistTiles) * n;
     launch_begin(s);
     if (loop)
       attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, prm);
+    else if (persist)
+      attn_tc_persist_kernel<<<num_sms(), THREADS1, SMEM_BYTES2, s>>>(tq, tkv, tlat, prm);
     else
       attn_tc_kernel<<<n * H, THREADS1, SMEM_BYTES1, s>>>(tq, tkv, tlat, prm);
-    const int rc = launch_status(s, loop ? "attn_tc_loop_kernel" : "attn_tc_kernel");
+    const int rc = launch_status(
+        s, loop ? "attn_tc_loop_kernel" : (persist ? "attn_tc_persist_kernel" : "attn_tc_kernel"));
     if (rc) return rc;
   }
   if (sg.n > 0) {
