@@ -18,7 +18,10 @@
 // tiles: all of them, or -- when a launch has too few (sequence, tile, head)
 // units to fill the GPU -- one of several key splits, whose partial (O, LSE)
 // go to a scratch slot and are LSE-merged by split_combine_kernel (the same
-// merge as the chunk accumulation, over a split of the key set).
+// merge as the chunk accumulation, over a split of the key set).  The same
+// unit also runs in two kernels where one CTA per SM walks many units: the
+// persistent one-unit kernel (prepared queries, units of a few dozen key
+// tiles) and the looping kernel (many short units, a warpgroup per unit).
 // Two softmax warpgroups share every S tile: A takes its keys 0-63, B keys
 // 64-127, each thread half a query row; the two exchange their half-row
 // maxima through shared memory every tile, so both apply the same running
