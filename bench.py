@@ -502,8 +502,9 @@ def run_ours(args, rank, world, dev):
     # ---- e2e: host buffers, copies inside the timed region.  Inputs are
     # double-buffered on the device: step i+1's host->device copy (on a copy
     # stream) overlaps step i's compute; each step's output is read back to
-    # pinned host memory.  The region runs from the first copy to the last
-    # read-back.
+    # pinned host memory on a second copy stream, so the two directions of
+    # the host link run side by side.  The region runs from the first copy
+    # to the last read-back.
     host = {k: v.pin_memory() for k, v in x.items()}
     sets = [g, {k: torch.empty_like(v) for k, v in g.items()}]
     outs = [out, torch.empty_like(out)]
@@ -511,6 +512,7 @@ def run_ours(args, rank, world, dev):
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = host_out[0].numel() * host_out[0].element_size()
     copy_stream = torch.cuda.Stream(device=dev)
+    back_stream = torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
     if world > 1:
         torch.distributed.barrier()
@@ -518,6 +520,7 @@ def run_ours(args, rank, world, dev):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     copy_stream.wait_event(e0)
+    back_stream.wait_event(e0)
     in_ready, done, read_back = [None, None], [None, None], [None, None]
 
     def h2d_into(k):
@@ -542,11 +545,11 @@ def run_ours(args, rank, world, dev):
            None)
         done[k] = ev()
         done[k].record(stream)
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(done[k])
+        with torch.cuda.stream(back_stream):
+            back_stream.wait_event(done[k])
             host_out[k].copy_(outs[k], non_blocking=True)
             read_back[k] = ev()
-            read_back[k].record(copy_stream)
+            read_back[k].record(back_stream)
     for k in range(2):
         if read_back[k] is not None:
             stream.wait_event(read_back[k])
