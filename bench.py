@@ -806,10 +806,13 @@ def run_kernel_case(args, dev):
         # whole prefills of --workload (the launches of one step, for a
         # traffic capture); work = the step's algorithmic FLOPs
         w = W.workload(args.workload)
+        if args.requests:  # the first N requests only (a smaller capture)
+            w = W.scaled(w, context_lens=list(w.context_lens[:args.requests]),
+                         query_lens=list(w.query_lens[:args.requests]))
         x, g, plans, pf, out, step = prefill_runner(M, W, w, dev)
         fn = step
         work, unit, peak = flops_of(w, plans)["total"], "TFLOP/s", peaks["bf16_tflops"]
-        info = {"workload": args.workload}
+        info = {"workload": args.workload, "requests": w.num_requests}
     elif args.kernel == "fused":
         # context attention with the up-projection fused in (one query tile
         # per sequence); work = the up-projection plus the attention
@@ -899,6 +902,8 @@ def main():
     ap.add_argument("--klen", type=int, default=4096)
     ap.add_argument("--causal", type=int, default=0)
     ap.add_argument("--launches", type=int, default=10)
+    ap.add_argument("--requests", type=int, default=0,
+                    help="--kernel step: the workload's first N requests only")
     args = ap.parse_args()
     if args.kernel:
         torch.cuda.set_device(0)
