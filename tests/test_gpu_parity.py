@@ -882,6 +882,27 @@ def test_prefill_persistent_attention(ctx, ql, heads, budget, split):
         assert_close(f64(lse[h]), rl[0], 1e-3, what=f"LSE head {h}")
 
 
+def test_prefill_persistent_new_token_attention():
+    """A request with 4200 new tokens (33 query tiles, 17 causal key tiles
+    per unit on average, past the looping kernel's limit) over 16 heads:
+    the new-token attention with the final merge runs on the persistent
+    one-unit kernel (causal masking, the context partial merged in its
+    epilogue, bf16 output); a second request without context; compared in
+    full."""
+    w = W.scaled(W.workload("uniform"), context_lens=[300, 0], query_lens=[4200, 90],
+                 num_heads=16, row_budget=4096, max_context_chunk=4096, split_alignment=64,
+                 seed=67)
+    x = W.make_inputs(w)
+    M.mla_profile_begin()
+    out, lse = _run_prefill(w, x)
+    names = [r[0] for r in M.mla_profile_end()]
+    assert names[-1] == "attn_tc_persist_kernel"
+    ro, rl, _ = _oracle_prefill(w, x)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_prefill_many_short_requests_loop_path():
     # 64 heads and many short requests: more (query tile, head) units than
     # SMs with few key tiles each, so the group attention and the new-token
