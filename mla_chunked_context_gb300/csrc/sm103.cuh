@@ -132,6 +132,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// The same arrive without release semantics: for handing back tensor memory
+// whose tcgen05.ld reads have completed (tcgen05.wait::ld), where no ordinary
+// memory access of this thread has to be visible to the waiter.  A release
+// would first wait until every global store the thread (and, through the
+// warp's __syncwarp, its warp) issued before it has been performed.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -304,9 +304,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           __syncwarp();  // the staging tile is rewritten by the next chunk
         }
+        // the accumulator is read (every tcgen05.ld waited for): hand it
+        // back without waiting for this tile's output stores to drain -- a
+        // release arrive waited for them, and the MMAs of the tile after next
+        // waited on it (0.79 of the bf16 peak on 32768 rows; 0.86 without)
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acce0_lead + 8 * acc);
+        if (lane == 0) mbar_arrive_cluster_relaxed(acce0_lead + 8 * acc);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
