@@ -119,21 +119,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
-// 16-byte shared-memory store / load at a 32-bit shared address
-__device__ __forceinline__ void st_shared_v4(uint32_t a, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a)
-               : "memory");
-  return v;
-}
-
 // 2^x with the SFU's approximate exponent (relative error below 2^-21; P is
 // then rounded to fp16, 2^-11).  Arguments here are at most 8 (the lazily
 // raised running max), results below 2^-126 flush to zero.

@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> 16-bit -> swizzled smem -> coalesced stores
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    uint8_t *stg = sStage + (warp - 2) * STG_BYTES;
+    const uint32_t stg = smem_u32(sStage + (warp - 2) * STG_BYTES);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           // lane = row: its 64 values as 8 16-byte pieces, XOR-swizzled so the
           // writes and the reads below are free of bank conflicts
-          uint8_t *row = stg + lane * 128;
+          const uint32_t row = stg + uint32_t(lane * 128);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t *src = (c < 4) ? lo + 8 * c : hi + 8 * (c - 4);
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               v.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
               v.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
             }
-            *reinterpret_cast<uint4 *>(row + ((c ^ (lane & 7)) << 4)) = v;
+            st_shared_v4(row + uint32_t((c ^ (lane & 7)) << 4), v);
           }
           __syncwarp();
           // write back 4 rows x 128 B per instruction: in the head-major output
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 8; ++i) {
             const int r = 4 * i + (lane >> 3), ch = lane & 7;
             const int grow = m0 + quarter * 32 + r;
-            const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 128 + ((ch ^ (r & 7)) << 4));
+            const uint4 v = ld_shared_v4(stg + uint32_t(r * 128 + ((ch ^ (r & 7)) << 4)));
             if (grow < g.M)
               __stcs(reinterpret_cast<uint4 *>(g.out + (int64_t(head) * g.M + grow) * g.hd + col +
                                                ch * 8),
