@@ -64,7 +64,7 @@ struct GemmArgs {
   int num_pm, num_n;  // pair tiles along M, tiles along N
   int nseg;           // N segments per 256-row block: a unit is (block, segment)
   int hd;             // output columns per head (Dn + Dv): the output is [N/hd, M, hd]
-  uint16_t *out;      // fp16 / bf16 bits
+                      // (written through the output tensor map)
   int32_t *status;    // nullable: MLA_STATUS_FP16_RANGE when an fp16 output overflowed
 };
 
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mma_commit_pair_mc(done_bar, uint16_t(0x1));
     mbar_wait(done_bar, 0);
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM -> 16-bit -> swizzled smem -> coalesced stores
+    // ---------------- epilogue: TMEM -> 16-bit -> swizzled smem -> tensor stores
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const uint32_t stg = smem_u32(sStage + (warp - 2) * STG_BYTES);
     int acc = 0;
@@ -415,8 +415,7 @@ int launch_up_proj_tc(const mla_dims_t &d, int kv_dtype, const void *latent, int
       !make_tmap_3d_16(&to, f16, kv, hd, rows, N / hd, uint64_t(hd) * 2,
                        uint64_t(rows) * hd * 2, 64, 32, true))
     return MLA_ERR_CUDA;
-  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, 1, hd,
-             static_cast<uint16_t *>(kv), status};
+  GemmArgs g{rows, N, K, (rows + PAIR_M - 1) / PAIR_M, N / BN, 1, hd, status};
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(up_proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
