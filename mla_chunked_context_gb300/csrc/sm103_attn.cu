@@ -1783,6 +1783,27 @@ constexpr int kLoopTilesPrepared = 16;
 constexpr int kPersistUnits = 2;
 constexpr int kPersistTiles = 64;
 
+// A unit's cost beyond its key tiles (its Q tile and its partial's store,
+// about two key tiles of traffic), for the balance estimate below.
+constexpr int kUnitCostTiles = 2;
+
+// The load of the busiest of G CTAs, in key tiles, when a launch's units
+// (unit u: item u % n of head u / n) are dealt to them round robin -- as
+// the persistent kernels walk them, and about as the hardware deals a CTA
+// per unit to SMs that each hold one.
+int64_t busiest_cta(const std::vector<Item> &items, int H, int G) {
+  const size_t n = items.size();
+  const int64_t units = int64_t(n) * H;
+  std::vector<int64_t> load(size_t(G), 0);
+  size_t i = 0, c = 0;
+  for (int64_t u = 0; u < units; ++u) {
+    load[c] += items[i].kt1 - items[i].kt0 + kUnitCostTiles;
+    if (++i == n) i = 0;
+    if (++c == size_t(G)) c = 0;
+  }
+  return *std::max_element(load.begin(), load.end());
+}
+
 int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
                int H, const SplitScratch *split, bool skip_keyless, std::vector<Item> &items,
                SplitGroups &sg) {
@@ -1803,23 +1824,41 @@ int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_
   std::stable_sort(items.begin(), items.end(), by_cost);
   const int64_t units = int64_t(items.size()) * H;
   if (split && split->o && !causal && units > 0 && units < split->target_ctas) {
-    const int want = int((split->target_ctas + units - 1) / units);
-    std::vector<Item> out;
-    int used = 0;
-    for (const Item &it : items) {
-      const int nt = it.kt1 - it.kt0;
-      const int f = std::min(want, nt / kMinSplitTiles);
-      if (f < 2 || used + f > split->slots || sg.n == MAX_SPLIT_GROUPS) {
-        out.push_back(it);
-        continue;
+    // at least `want` splits an item, so that the units reach the target;
+    // beyond it, the split count whose units spread most evenly over the
+    // SMs (the long request's 99 x 32768 chunk over 128 heads: 5 splits put
+    // 5 units on 32 SMs and 4 on the rest, 7 splits 6 and 5)
+    const int want0 = int((split->target_ctas + units - 1) / units);
+    const int G = num_sms();
+    std::vector<Item> best;
+    SplitGroups best_sg = sg;
+    int64_t best_load = -1;
+    for (int want = want0; want <= std::max(want0, split->slots); ++want) {
+      std::vector<Item> out;
+      SplitGroups g = sg;
+      int used = 0;
+      for (const Item &it : items) {
+        const int nt = it.kt1 - it.kt0;
+        const int f = std::min(want, nt / kMinSplitTiles);
+        if (f < 2 || used + f > split->slots || g.n == MAX_SPLIT_GROUPS) {
+          out.push_back(it);
+          continue;
+        }
+        g.g[g.n++] = make_int4(it.seq, it.qt, used, f);
+        for (int k = 0; k < f; ++k)
+          out.push_back({it.seq, it.qt, it.kt0 + nt * k / f, it.kt0 + nt * (k + 1) / f, used + k});
+        used += f;
       }
-      sg.g[sg.n++] = make_int4(it.seq, it.qt, used, f);
-      for (int k = 0; k < f; ++k)
-        out.push_back({it.seq, it.qt, it.kt0 + nt * k / f, it.kt0 + nt * (k + 1) / f, used + k});
-      used += f;
+      std::stable_sort(out.begin(), out.end(), by_cost);
+      const int64_t load = busiest_cta(out, H, G);
+      if (best_load < 0 || load < best_load) {
+        best.swap(out);
+        best_sg = g;
+        best_load = load;
+      }
     }
-    items.swap(out);
-    std::stable_sort(items.begin(), items.end(), by_cost);
+    items.swap(best);
+    sg = best_sg;
   }
   return MLA_OK;
 }
