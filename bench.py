@@ -179,6 +179,52 @@ def attn_ctx_bytes(w, plans):
     return b
 
 
+def execution_groups(plans, budget):
+    """The chunks as mla_chunked_prefill runs them: consecutive chunks with
+    no continuation after the first and rows within the budget together."""
+    groups, c0 = [], 0
+    while c0 < len(plans):
+        c1, rows = c0 + 1, plans[c0].rows
+        while (c1 < len(plans) and not plans[c1].is_continuation
+               and rows + plans[c1].rows <= budget):
+            rows += plans[c1].rows
+            c1 += 1
+        groups.append(plans[c0:c1])
+        c0 = c1
+    return groups
+
+
+def last_group_work(w, plans):
+    """FLOPs and bytes of the final launch that attends the last execution
+    group's context rows and the new tokens at once (when the prefill runs
+    it that way): the new-token attention's work plus the last group's
+    context attention, with queries read once, no partial written for the
+    last group and the partial read only for tokens whose request has
+    context in an earlier group; and the context attention of the other
+    groups (FLOPs, bytes)."""
+    H, Dn, Dv, P = w.num_heads, w.qk_nope_dim, w.v_dim, w.qk_rope_dim
+    es = 2 if w.dtype == "bf16" else 4
+    groups = execution_groups(plans, w.row_budget)
+    last = groups[-1] if groups else []
+    rest = [c for g in groups[:-1] for c in g]
+    per_pair = 2.0 * H * (Dn + P + Dv)
+    ctx_flops = lambda cs: per_pair * sum(  # noqa: E731
+        w.query_lens[r] * c.seq_lens[i] for c in cs
+        for i, r in enumerate(range(c.request_start, c.request_end)))
+    last_rows = sum(sum(c.seq_lens) for c in last)
+    earlier = set(r for c in rest for r, n in zip(range(c.request_start, c.request_end),
+                                                   c.seq_lens) if n > 0)
+    for c in last:  # a request continued into the last group has an earlier partial
+        if c.is_continuation:
+            earlier.add(c.request_start)
+    T = w.num_tokens
+    merge_tokens = sum(w.query_lens[r] for r in earlier)
+    fl_last = per_pair * sum(q * (q + 1) / 2 for q in w.query_lens) + ctx_flops(last)
+    by_last = (T * H * (Dn + P) * 2 + (T + last_rows) * (H * (Dn + Dv) * 2 + P * 2)
+               + merge_tokens * H * (Dv + 1) * 4 + T * H * (Dv * es + 4))
+    return fl_last, by_last, ctx_flops(rest), attn_ctx_bytes(w, rest)
+
+
 def config_of(w, plans, world):
     """The workload description both arms print."""
     return {"workload": f"{w.name}: {w.num_requests} requests, context rows "
@@ -225,6 +271,8 @@ def whole_job_rate(units_per_rank_step: float, world: int, steps: int, job_ms: f
 # ------------------------------------------------- in-step launch profile --
 ROLE_GATHER, ROLE_UP, ROLE_ATTN = "a4 gather", "a5 up-projection", "a6-a7 context attention"
 ROLE_UP_NEW, ROLE_ATTN_NEW = "a8 new-token up-projection", "a9-a10 new-token attention + merge"
+# the last group's context attention and the new-token attention as one launch
+ROLE_LAST = "a6-a10 last context group + new tokens"
 
 
 def split_steps(records, steps):
@@ -263,11 +311,14 @@ def breakdown_of(records, steps, w, plans, peaks):
     for rs in per_step:
         for role, ms in attributed_ms(rs).items():
             attributed[role or "(other)"] = attributed.get(role or "(other)", 0.0) + ms / steps
-        ctx = [r for r in rs if r[4] in (ROLE_GATHER, ROLE_UP, ROLE_ATTN)]
+        # the span ends with the last context attention (in the final launch
+        # when the last group's attention runs there: the span then also
+        # holds the new-token attention, which only lowers the bar)
+        ctx = [r for r in rs if r[4] in (ROLE_GATHER, ROLE_UP, ROLE_ATTN, ROLE_LAST)]
         if ctx:
             t0 = min(r[2] for r in ctx)
-            t1 = max(r[2] + r[3] for r in ctx if r[4] == ROLE_ATTN) if any(
-                r[4] == ROLE_ATTN for r in ctx) else max(r[2] + r[3] for r in ctx)
+            ends = [r[2] + r[3] for r in ctx if r[4] in (ROLE_ATTN, ROLE_LAST)]
+            t1 = max(ends) if ends else max(r[2] + r[3] for r in ctx)
             spans.append(t1 - t0)
         for name, stream, start, ms, role in rs:
             e = roles.setdefault(role or "(other)", {"launches": 0, "ms": 0.0, "kernels": set()})
@@ -319,7 +370,11 @@ def breakdown_of(records, steps, w, plans, peaks):
     gn = roles.get(ROLE_UP_NEW, {"ms": 0, "launches": 0})
     a = roles.get(ROLE_ATTN, {"ms": 0, "launches": 0})
     an = roles.get(ROLE_ATTN_NEW, {"ms": 0, "launches": 0})
+    al = roles.get(ROLE_LAST, {"ms": 0, "launches": 0})
     ga = roles.get(ROLE_GATHER, {"ms": 0, "launches": 0})
+    ctx_fl, ctx_by = fl["attn_ctx"], fl["attn_ctx_bytes"]
+    if al["launches"]:
+        last_fl, last_by, ctx_fl, ctx_by = last_group_work(w, plans)
     bf = peaks["bf16_tflops"]
     src = peaks["source"]
     at = lambda *rs: sum(attributed.get(r, 0.0) for r in rs)  # noqa: E731
@@ -327,10 +382,12 @@ def breakdown_of(records, steps, w, plans, peaks):
         "up_proj": rl(g["ms"] + gn["ms"], fl["up_proj_ctx"] + fl["up_proj_new"],
                       g["launches"] + gn["launches"], "TFLOP/s", bf, src + " bf16 burst",
                       "tensor", at(ROLE_UP, ROLE_UP_NEW)),
-        "context_attention": attn_rl(a["ms"], a["launches"], at(ROLE_ATTN), fl["attn_ctx"],
-                                     fl["attn_ctx_bytes"]),
+        "context_attention": attn_rl(a["ms"], a["launches"], at(ROLE_ATTN), ctx_fl, ctx_by),
         "new_token_attention_merge": attn_rl(an["ms"], an["launches"], at(ROLE_ATTN_NEW),
                                              fl["attn_new"], fl["attn_new_bytes"]),
+        "last_group_and_new_token_attention": (
+            attn_rl(al["ms"], al["launches"], at(ROLE_LAST), last_fl, last_by)
+            if al["launches"] else None),
         "gather": rl(ga["ms"], 2.0 * fl["context_rows"] * row_bytes, ga["launches"], "GB/s",
                      peaks["hbm_gbs"], src + " copy", "hbm", at(ROLE_GATHER)),
     }

@@ -432,7 +432,14 @@ int mla_prefill_pinned_bytes(const mla_dims_t *d, const int32_t *context_lens,
  *   device has run, so one buffer can serve call after call; the library
  *   never frees it.  NULL: the copy is made from pageable memory.
  *   On the tensor-core path the workspace keeps K/V in fp16 (see
- *   mla_kv_up_proj); on the CUDA-core path in float32.
+ *   mla_kv_up_proj); on the CUDA-core path in float32.  There, when the
+ *   last execution group is short (on average at most 16 key tiles of 128
+ *   per (request, query tile) with the new tokens' causal tiles, and more
+ *   units than SMs), its context attention and the new-token attention run
+ *   as one launch: each (request, query tile, head) walks the request's
+ *   context rows of that group and then its own new tokens, and merges with
+ *   the context partial only where an earlier group left one.  The result
+ *   is the same composition, one LSE merge order apart.
  *   Streams: the chunks run as a two-buffer pipeline.  Gathers and
  *   up-projections go to two library-owned side streams of the highest
  *   priority (one pair per device, made on first use); attention, merges

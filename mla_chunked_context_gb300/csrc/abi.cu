@@ -10,6 +10,7 @@
 //   Everything that writes the partial or the output runs on the caller's
 //   stream, which waits for the side streams before the last kernel.
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -55,7 +56,9 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    const void *latent, int64_t latent_ld, const int32_t *accumulate,
                    float *o, float *lse, void *final_out, float *final_lse, int final_dtype,
                    int pnt, const SplitScratch *split, bool skip_keyless, bool q_prepared,
-                   int32_t *status, cudaStream_t s);
+                   int32_t *status, cudaStream_t s, const NewKeySource *new_keys = nullptr);
+bool attn_tc_new_keys_ok(int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                         int H);
 int launch_prepare_q(const void *q, void *qh, int T, int H, int32_t *status, cudaStream_t s);
 bool fused_attn_ok(const mla_dims_t &d, int64_t latent_ld);
 bool fused_attn_fits(int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
@@ -511,7 +514,9 @@ int upload_meta(Pipeline &pl, void *dst, const std::vector<int32_t> &src, void *
 // consume(c-2) has released buffer set c % 2, up(c, stream) on the GEMM side
 // stream after it, and consume(c, stream) on `s` after that; then
 // tail(stream) on the GEMM side stream (the new tokens' up-projection,
-// beside the last consume).  Both side streams start after the work already
+// beside the last consume; or, with tail_before = k < n, on that stream
+// just before unit k's gather is waited for and its up-projection
+// enqueued).  Both side streams start after the work already
 // on `s` and are joined back into `s` before returning, also after an error
 // (the caller may free the workspace once `s` has passed this point).  The
 // side streams run at the highest priority, so a GEMM takes SMs as soon as
@@ -522,7 +527,7 @@ std::atomic<int> g_overlap{1};
 
 template <class Pre, class Gather, class Up, class Consume, class Tail>
 int run_pipeline(Pipeline &pl, cudaStream_t s, size_t n, Pre pre, Gather gather, Up up,
-                 Consume consume, Tail tail) {
+                 Consume consume, Tail tail, size_t tail_before = SIZE_MAX) {
   if (pl.ev.size() < 3 * n + 3) return MLA_ERR_INVALID;
   cudaEvent_t *ev = pl.ev.data();
   const bool overlap = g_overlap.load() != 0;
@@ -533,16 +538,21 @@ int run_pipeline(Pipeline &pl, cudaStream_t s, size_t n, Pre pre, Gather gather,
   cudaEvent_t ev_tail = ev[1 + 3 * n], ev_join = ev[2 + 3 * n];
   if (!record(ev[0], s) || !wait_on(sg, ev[0]) || !wait_on(sm, ev[0])) return MLA_ERR_CUDA;
   int rc = pre(s);
+  bool tail_done = false;
   for (size_t c = 0; c < n && rc == MLA_OK; ++c) {
     if (c >= 2 && !wait_on(sg, ev_used(c - 2))) rc = MLA_ERR_CUDA;
     if (!rc) rc = gather(c, sg);
+    if (!rc && c == tail_before) {
+      rc = tail(sm);
+      tail_done = true;
+    }
     if (!rc && (!record(ev_lat(c), sg) || !wait_on(sm, ev_lat(c)))) rc = MLA_ERR_CUDA;
     if (!rc) rc = up(c, sm);
     if (!rc && (!record(ev_kv(c), sm) || !wait_on(s, ev_kv(c)))) rc = MLA_ERR_CUDA;
     if (!rc) rc = consume(c, s);
     if (!rc && !record(ev_used(c), s)) rc = MLA_ERR_CUDA;
   }
-  if (!rc) rc = tail(sm);
+  if (!rc && !tail_done) rc = tail(sm);
   const bool joined = record(ev_tail, sm) && record(ev_join, sg) && wait_on(s, ev_tail) &&
                       wait_on(s, ev_join);
   if (rc) return rc;
@@ -555,7 +565,12 @@ struct PrefillLayout {
   std::vector<ChunkMetaHost> metas;        // one per execution group
   std::vector<size_t> meta_off;            // int offset of each group's metadata
   std::vector<std::pair<int, int>> empty;  // token slices of context-free requests
-  size_t slices_off = 0, suffix_off = 0, meta_total = 0;
+  // the last group's context rows per request (prefix sums over all
+  // requests: rows of the group's workspace) and, per request, whether its
+  // context partial holds an earlier group's result -- for the final
+  // launch that attends the last group's context and the new tokens at once
+  std::vector<int32_t> last_rows, last_merge;
+  size_t slices_off = 0, suffix_off = 0, last_off = 0, meta_total = 0;
   int T = 0, pnt = 0, max_rows = 0;
 };
 
@@ -598,6 +613,22 @@ int build_prefill(const mla_dims_t &d, const int32_t *ctx, const int32_t *ql, in
   off += 2 * p.empty.size();
   p.suffix_off = off;
   off += R + 1;
+  p.last_rows.assign(R + 1, 0);
+  p.last_merge.assign(R, 0);
+  if (!p.metas.empty()) {
+    // the last group's sequences are requests r0 .. r0+n-1 (build_group_meta)
+    const ChunkMetaHost &m = p.metas.back();
+    const int32_t *req = m.ints.data(), *acc = req + 4 * m.n + 2;  // req st cu ql acc
+    const int r0 = m.n > 0 ? req[0] : R;
+    for (int r = 0; r < R; ++r) {
+      const int k = r - r0;
+      const int rows = (k >= 0 && k < m.n) ? m.cu_rows[k + 1] - m.cu_rows[k] : 0;
+      p.last_rows[r + 1] = p.last_rows[r] + rows;
+      p.last_merge[r] = (k >= 0 && k < m.n) ? acc[k] : (k < 0 && ctx[r] > 0 ? 1 : 0);
+    }
+  }
+  p.last_off = off;
+  off += 2 * size_t(R) + 1;
   p.meta_total = off;
   return MLA_OK;
 }
@@ -725,6 +756,10 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
     meta[p.slices_off + 2 * k + 1] = p.empty[k].second;
   }
   std::memcpy(meta.data() + p.suffix_off, p.qsl.data(), p.qsl.size() * sizeof(int32_t));
+  std::memcpy(meta.data() + p.last_off, p.last_rows.data(),
+              p.last_rows.size() * sizeof(int32_t));
+  std::memcpy(meta.data() + p.last_off + p.last_rows.size(), p.last_merge.data(),
+              p.last_merge.size() * sizeof(int32_t));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::unique_lock<std::mutex> lock;
   Pipeline *pl = nullptr;
@@ -741,6 +776,16 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   // already fp16: one pass (in the pipeline's pre step) instead of a strided
   // load and an fp16 conversion in every attention CTA
   const void *q_prep = tc ? b.q_prep : nullptr;
+  // The last group's context attention and the new-token attention as one
+  // launch of the looping kernel (when its units are short enough for it):
+  // each (request, query tile, head) unit walks the request's context rows
+  // of that group, then its own new tokens causally, and merges with the
+  // context partial only where an earlier group left one -- no second Q
+  // load, no partial written and read back between the two.
+  const size_t n_groups = p.metas.size();
+  const bool merged = tc && n_groups > 0 &&
+                      attn_tc_new_keys_ok(num_requests, p.qsl.data(), p.last_rows.data(),
+                                          d->num_heads);
 
   // The chunk pipeline (run_pipeline) over execution groups: consecutive
   // chunks with no continuation between them and rows within the budget
@@ -790,6 +835,7 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                        b.chunk[c & 1].kv_ws, kv_dtype, dev_status, st_);
       },
       [&](size_t c, cudaStream_t st_) {
+        if (merged && c + 1 == n_groups) return int(MLA_OK);  // in the final launch
         ProfRole role("a6-a7 context attention");
         const ChunkMetaHost &m = p.metas[c];
         const int32_t *req, *st, *cu, *ql, *acc;
@@ -798,15 +844,31 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
                          b.chunk[c & 1].kv_ws, kv_dtype, m.rows, b.chunk[c & 1].latent_ws, LP,
                          acc, b.o_part, b.lse_part, dev_status, st_, &b.split, true, q_prep);
       },
-      // new-token up-projection, beside the last group's attention
+      // new-token up-projection, beside the last group's attention (or,
+      // when that attention is in the final launch, before the last
+      // group's up-projection, so that the final launch waits on neither)
       [&](cudaStream_t st_) {
         ProfRole role("a8 new-token up-projection");
         return up_proj(*d, new_latent, LP, T, w_kv_b, b.kv_suffix, kv_dtype, dev_status, st_);
-      });
+      },
+      merged ? n_groups - 1 : SIZE_MAX);
   if (rc) return rc;
 
-  ProfRole role("a9-a10 new-token attention + merge");
   const int32_t *sq = b.meta + p.suffix_off;
+  if (merged) {
+    ProfRole role("a6-a10 last context group + new tokens");
+    const ChunkBuffers &cb = b.chunk[(n_groups - 1) & 1];
+    const int32_t *lrows = b.meta + p.last_off, *lmerge = lrows + num_requests + 1;
+    NewKeySource nks;
+    nks.kv = b.kv_suffix;
+    nks.latent = new_latent;
+    nks.latent_ld = LP;
+    return launch_attn_tc(*d, 0, num_requests, sq, lrows, p.qsl.data(), p.last_rows.data(), T,
+                          p.metas.back().rows, q_prep, cb.kv_ws, cb.latent_ws, LP, lmerge,
+                          b.o_part, b.lse_part, out, out_lse, d->dtype, p.pnt, nullptr, false,
+                          true, dev_status, s, &nks);
+  }
+  ProfRole role("a9-a10 new-token attention + merge");
   if (tc) {
     // new-token attention with the final merge in its epilogue (row f3): the
     // context partial is read where needed, the output written once

@@ -143,6 +143,15 @@ struct SplitScratch {
   int slots = 0, target_ctas = 0;
 };
 
+// The keys a context attention launch appends to each sequence's context
+// keys: the sequence's own new tokens (rows q_loc[i] .. q_loc[i+1] of kv
+// [T, H, 256] fp16 and latent [T, latent_ld] bf16, k_pe at column 512),
+// attended causally.
+struct NewKeySource {
+  const void *kv = nullptr, *latent = nullptr;
+  int64_t latent_ld = 0;
+};
+
 inline int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);

@@ -105,6 +105,10 @@ struct AttnParams {
   float *split_o, *split_lse;
   // nullable: MLA_STATUS_FP16_RANGE when a q_nope value overflowed fp16
   int32_t *status;
+  // looping kernel only: after its context keys, each sequence attends its
+  // own new tokens (rows q_loc[i] .. q_loc[i+1] of the second K/V and
+  // latent maps), causally; items are never split then
+  int new_keys;
   // (sequence, query tile | (split slot + 1) << 16, first key tile, end key
   // tile), the most key tiles first
   int4 items[MAX_ITEMS];
@@ -191,6 +195,14 @@ __device__ __forceinline__ void convert_q_nope(uint8_t *sQ, int tid, int nthr, i
   if (status && amax >= kF16Overflow) atomicOr(status, MLA_STATUS_FP16_RANGE);
 }
 
+// Final-merge mode: whether token t (of sequence seq) is LSE-merged with
+// the stored context partial -- a token below pnt, unless the launch's
+// per-sequence flags (acc, when given) say that the partial holds no earlier
+// result for the sequence.
+__device__ __forceinline__ bool fin_merges(const AttnParams &p, int seq, int t) {
+  return t < p.pnt && (p.acc == nullptr || __ldg(p.acc + seq) != 0);
+}
+
 // Brings the half row of the stored partial that the epilogue will merge
 // with (a continued request, or the context partial in final-merge mode)
 // into L2 while the unit computes, instead of leaving the epilogue to wait
@@ -201,7 +213,7 @@ __device__ __forceinline__ void prefetch_partial(const AttnParams &p, int h, int
   const int t = q_beg + qpos;
   const bool fin = p.fout != nullptr;
   const bool acc = !fin && p.acc != nullptr && __ldg(p.acc + seq) != 0;
-  if (!acc && !(fin && t < p.pnt)) return;
+  if (!acc && !(fin && fin_merges(p, seq, t))) return;
   const float *row = p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);
   asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
   asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 32));
@@ -361,7 +373,7 @@ __device__ __forceinline__ bool unit_epilogue1(const AttnParams &p, uint32_t o_c
   const bool fin = p.fout != nullptr;
   const bool split = slot >= 0;  // a key split: its own partial goes to the scratch slot
   const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
-  const bool merge_old = accumulate || (fin && t < p.pnt);
+  const bool merge_old = accumulate || (fin && fin_merges(p, seq, t));
   // the stored LSE is read by both warpgroups before either writes it
   const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
   // this warpgroup's half of the output row, and the row's LSE
@@ -709,7 +721,7 @@ __device__ __forceinline__ bool unit_epilogue_p(const AttnParams &p, uint32_t o_
   const bool fin = p.fout != nullptr;
   const bool split = slot >= 0;
   const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
-  const bool merge_old = accumulate || (fin && t < p.pnt);
+  const bool merge_old = accumulate || (fin && fin_merges(p, seq, t));
   const float old = (merge_old && qpos < nq) ? p.lse[li] : neg_inf();
   const float *orow = p.o + (int64_t(t) * p.H + h) * DV + wg * (DV / 2);  // the stored partial
   tc_fence_before();
@@ -1100,8 +1112,8 @@ static_assert(SMEM_BYTES_LOOP <= 227 * 1024, "looping kernel: shared memory");
 __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t s_col,
                                                   uint32_t o_col, uint32_t sfull_bar,
                                                   uint32_t sfull_parity, uint32_t b_odone,
-                                                  uint32_t pfull_bar, int jw, int k0, int nk,
-                                                  int qpos, float &m_used, float &l, int lane) {
+                                                  uint32_t pfull_bar, int jw, int k0,
+                                                  int kend, float &m_used, float &l, int lane) {
   // every exit is taken by the whole warp (its TMEM accesses are warp-wide)
   if (!__all_sync(0xffffffffu, mbar_wait(sfull_bar, sfull_parity))) return false;
   tc_fence_after();
@@ -1122,9 +1134,9 @@ __device__ __forceinline__ bool softmax_tile_full(const AttnParams &p, uint32_t 
         sv[32 + e] = __uint_as_float(r1[e]);
       }
     }
-    const int kh = k0 + hh * HALF;
-    int valid = nk - kh;
-    if (p.causal) valid = min(valid, qpos - kh + 1);
+    // keys k0 + hh * HALF + e, valid below kend (the row's key bound: the
+    // source's key count, and with a causal mask its query position + 1)
+    const int valid = kend - (k0 + hh * HALF);
     if (valid < HALF) {
 #pragma unroll
       for (int e = 0; e < HALF; ++e)
@@ -1233,7 +1245,7 @@ __device__ __forceinline__ bool unit_epilogue_full(const AttnParams &p, uint32_t
   const bool fin = p.fout != nullptr;
   const bool split = slot >= 0;
   const bool accumulate = !fin && !split && p.acc != nullptr && __ldg(p.acc + seq) != 0;
-  const bool merge_old = accumulate || (fin && t < p.pnt);
+  const bool merge_old = accumulate || (fin && fin_merges(p, seq, t));
   const bool live = qpos < nq;
   const float old = (merge_old && live) ? p.lse[li] : neg_inf();
   float *orow = split ? p.split_o + ((int64_t(slot) * p.H + h) * BQ + (qpos & (BQ - 1))) * DV
@@ -1389,6 +1401,8 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
     attn_tc_loop_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_kv,
                         const __grid_constant__ CUtensorMap tm_lat,
+                        const __grid_constant__ CUtensorMap tm_kv2,
+                        const __grid_constant__ CUtensorMap tm_lat2,
                         const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1471,6 +1485,10 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
       prefetch_map(&tm_q);
       prefetch_map(&tm_kv);
       prefetch_map(&tm_lat);
+      if (p.new_keys) {
+        prefetch_map(&tm_kv2);
+        prefetch_map(&tm_lat2);
+      }
       int k_issued[RING], v_issued[RING], q_issued = -1;
       for (int s = 0; s < RING; ++s) k_issued[s] = v_issued[s] = -1;
       int J = 0, kq = 0;
@@ -1481,6 +1499,9 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
         const Unit x = unit_of(u);
         if (x.n_tiles <= 0) continue;
         const int q_beg = __ldg(p.q_loc + x.seq), k_beg = __ldg(p.k_loc + x.seq);
+        // with new keys: the unit's first ct tiles are context keys, the
+        // rest the sequence's new tokens
+        const int ct = p.new_keys ? (__ldg(p.k_loc + x.seq + 1) - k_beg + BKV - 1) / BKV : x.n_tiles;
         // the previous unit's S MMAs are done with the Q tile
         if (kq > 0 && !mbar_wait(b_qfree, uint32_t((kq - 1) & 1))) break;
         const int qx = p.q_prepared ? 0 : x.h * DQK;
@@ -1494,16 +1515,19 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
         for (int j = 0; j < x.n_tiles; ++j, ++J) {
           const int s = J % RING;
           const uint32_t use = uint32_t(J / RING);        // use count of slot s
-          const int krow = k_beg + (x.kt0 + j) * BKV;
+          const bool nk_tile = j >= ct;                   // a new-token key tile
+          const int krow = nk_tile ? q_beg + (j - ct) * BKV : k_beg + (x.kt0 + j) * BKV;
+          const CUtensorMap *mkv = nk_tile ? &tm_kv2 : &tm_kv;
+          const CUtensorMap *mlat = nk_tile ? &tm_lat2 : &tm_lat;
           if (J >= RING && !mbar_wait(b_kempty + 8 * s, (use - 1) & 1)) {
             ok = false;
             break;
           }
           uint8_t *kk = sK + s * K_BYTES;
           mbar_expect_tx(b_kfull + 8 * s, K_BYTES);
-          tma_load_3d(smem_u32(kk), &tm_kv, b_kfull + 8 * s, 0, krow, x.h);
-          tma_load_3d(smem_u32(kk + KBOX), &tm_kv, b_kfull + 8 * s, 64, krow, x.h);
-          tma_load_2d(smem_u32(kk + 2 * KBOX), &tm_lat, b_kfull + 8 * s, 512, krow);
+          tma_load_3d(smem_u32(kk), mkv, b_kfull + 8 * s, 0, krow, x.h);
+          tma_load_3d(smem_u32(kk + KBOX), mkv, b_kfull + 8 * s, 64, krow, x.h);
+          tma_load_2d(smem_u32(kk + 2 * KBOX), mlat, b_kfull + 8 * s, 512, krow);
           k_issued[s] = int(use & 1);
           if (J >= RING && !mbar_wait(b_vempty + 8 * s, (use - 1) & 1)) {
             ok = false;
@@ -1511,8 +1535,8 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
           }
           uint8_t *v = sV + s * V_BYTES;
           mbar_expect_tx(b_vfull + 8 * s, V_BYTES);
-          tma_load_3d(smem_u32(v), &tm_kv, b_vfull + 8 * s, DN, krow, x.h);
-          tma_load_3d(smem_u32(v + KBOX), &tm_kv, b_vfull + 8 * s, DN + 64, krow, x.h);
+          tma_load_3d(smem_u32(v), mkv, b_vfull + 8 * s, DN, krow, x.h);
+          tma_load_3d(smem_u32(v + KBOX), mkv, b_vfull + 8 * s, DN + 64, krow, x.h);
           v_issued[s] = int(use & 1);
         }
       }
@@ -1635,19 +1659,25 @@ __global__ void __launch_bounds__(THREADS_LOOP, 1)
         const int t = q_beg + qpos;
         const bool fin = p.fout != nullptr;
         const bool acc = !fin && p.acc != nullptr && __ldg(p.acc + x.seq) != 0;
-        if (acc || (fin && t < p.pnt)) {
+        if (acc || (fin && fin_merges(p, x.seq, t))) {
           const float *r = p.o + (int64_t(t) * p.H + x.h) * DV;
 #pragma unroll
           for (int c = 0; c < DV; c += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(r + c));
         }
       }
+      // the context key tiles (keys x.kt0 * BKV + ...), then with new keys
+      // the sequence's own new tokens (keys 0 .. nq-1, causal): tile j's
+      // keys counted from the unit's first, valid below kend
+      const int ct = p.new_keys ? (nk + BKV - 1) / BKV : n_tiles;
+      int kend = (p.causal ? min(nk, qpos + 1) : nk) - x.kt0 * BKV;
       for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j == ct) kend = min(nq, qpos + 1) + ct * BKV;
         const int J = J0 + j;
         const uint32_t s_col = tmem + lane_off + COL_S + uint32_t((J & 1) * BKV);
         const int sc = (J & 1) ? sc1++ : sc0++;
         ok = softmax_tile_full(p, s_col, o_col, b_sfull + 16 * wg + 8 * (J & 1),
                                uint32_t(sc & 1), b_odone + 8 * wg, b_pfull + 8 * wg, jw,
-                               (x.kt0 + j) * BKV, nk, qpos, m_used, l, lane);
+                               j * BKV, kend, m_used, l, lane);
         ok = __all_sync(0xffffffffu, ok) != 0;
         ++jw;
       }
@@ -1805,8 +1835,8 @@ int64_t busiest_cta(const std::vector<Item> &items, int H, int G) {
 }
 
 int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
-               int H, const SplitScratch *split, bool skip_keyless, std::vector<Item> &items,
-               SplitGroups &sg) {
+               int H, const SplitScratch *split, bool skip_keyless, bool new_keys,
+               std::vector<Item> &items, SplitGroups &sg) {
   auto by_cost = [](const Item &a, const Item &b) { return a.kt1 - a.kt0 > b.kt1 - b.kt0; };
   items.clear();
   sg.n = 0;
@@ -1814,14 +1844,17 @@ int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_
     const int nq = q_loc_host[i + 1] - q_loc_host[i];
     const int nk = k_loc_host[i + 1] - k_loc_host[i];
     if ((nq + BQ - 1) / BQ > 0xffff) return MLA_ERR_UNSUPPORTED;  // 16-bit tile index
-    if (skip_keyless && nk == 0) continue;  // its rows already hold O=0, LSE=-inf
+    if (skip_keyless && !new_keys && nk == 0) continue;  // its rows already hold O=0, LSE=-inf
     for (int qt = 0; qt * BQ < nq; ++qt) {
       int tiles = (nk + BKV - 1) / BKV;
       if (causal) tiles = std::min(tiles, qt + 1);
+      // then the new tokens' keys up to the tile's last query
+      if (new_keys) tiles += std::min((nq + BKV - 1) / BKV, qt + 1);
       items.push_back({i, qt, 0, tiles, -1});
     }
   }
   std::stable_sort(items.begin(), items.end(), by_cost);
+  if (new_keys) return MLA_OK;  // never split
   const int64_t units = int64_t(items.size()) * H;
   if (split && split->o && !causal && units > 0 && units < split->target_ctas) {
     // at least `want` splits an item, so that the units reach the target;
@@ -1872,15 +1905,42 @@ bool tc_attn_ok(const mla_dims_t &d, int kv_dtype, int64_t latent_ld) {
          latent_ld >= 576;
 }
 
+namespace {
+// Many short units: one CTA per SM walks them (the next unit's loads and S
+// MMAs overlapping this one's softmax and epilogue); otherwise a CTA per
+// unit, so that a kernel running beside this one gets SMs as they retire.
+bool takes_loop(int n_items, int64_t tiles, int H, bool q_prepared) {
+  const int loop_tiles = q_prepared ? kLoopTilesPrepared : kLoopTiles;
+  return int64_t(n_items) * H > num_sms() && tiles <= int64_t(loop_tiles) * n_items;
+}
+}  // namespace
+
+bool attn_tc_new_keys_ok(int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
+                         int H) {
+  std::vector<Item> items;
+  SplitGroups sg{};
+  if (plan_items(0, num_seqs, q_loc_host, k_loc_host, H, nullptr, false, true, items, sg) ||
+      items.empty() || items.size() > size_t(MAX_ITEMS))
+    return false;
+  int64_t tiles = 0;
+  for (const Item &it : items) tiles += it.kt1 - it.kt0;
+  return takes_loop(int(items.size()), tiles, H, true);
+}
+
 int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
                    const int32_t *k_loc, const int32_t *q_loc_host, const int32_t *k_loc_host,
                    int T, int kv_rows, const void *q, const void *kv, const void *latent,
                    int64_t latent_ld, const int32_t *accumulate, float *o, float *lse,
                    void *final_out, float *final_lse, int final_dtype, int pnt,
                    const SplitScratch *split, bool skip_keyless, bool q_prepared,
-                   int32_t *status, cudaStream_t s) {
+                   int32_t *status, cudaStream_t s, const NewKeySource *new_keys) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
+  // new keys: the looping kernel only, non-causal context keys, prepared
+  // queries (checked by attn_tc_new_keys_ok before the caller commits to it)
+  if (new_keys && (causal || !q_prepared || !al16(new_keys->kv) || !al16(new_keys->latent) ||
+                   (new_keys->latent_ld * 2) % 16 != 0 || new_keys->latent_ld < 576))
+    return MLA_ERR_UNSUPPORTED;
   const int H = d.num_heads;
   const int rows = k_loc_host[num_seqs];
   CUtensorMap tq, tkv, tlat;
@@ -1896,11 +1956,21 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
       !make_tmap_2d_16(&tlat, false, latent, 576, uint64_t(rows > 0 ? rows : 1),
                        uint64_t(latent_ld) * 2, 64, BKV, true))
     return MLA_ERR_CUDA;
+  // the new tokens' K/V and latent rows (T of them), else copies of the
+  // context maps that no tile reads
+  CUtensorMap tkv2 = tkv, tlat2 = tlat;
+  if (new_keys &&
+      (!make_tmap_3d_16(&tkv2, true, new_keys->kv, HD, uint64_t(T), uint64_t(H),
+                        uint64_t(HD) * 2, uint64_t(T) * HD * 2, 64, BKV, true) ||
+       !make_tmap_2d_16(&tlat2, false, new_keys->latent, 576, uint64_t(T),
+                        uint64_t(new_keys->latent_ld) * 2, 64, BKV, true)))
+    return MLA_ERR_CUDA;
   std::vector<Item> items;
   SplitGroups sg{};
   const int rc = plan_items(causal, num_seqs, q_loc_host, k_loc_host, H,
-                            final_out == nullptr ? split : nullptr,
-                            skip_keyless && !causal && final_out == nullptr, items, sg);
+                            final_out == nullptr && !new_keys ? split : nullptr,
+                            skip_keyless && !causal && final_out == nullptr, new_keys != nullptr,
+                            items, sg);
   if (rc) return rc;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1935,18 +2005,15 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     prm.split_lse = split ? split->lse : nullptr;
     prm.q_prepared = q_prepared ? 1 : 0;
     prm.status = status;
+    prm.new_keys = new_keys ? 1 : 0;
     for (int k = 0; k < n; ++k) {
       const Item &it = items[b + k];
       prm.items[k] = make_int4(it.seq, it.qt | ((it.slot + 1) << 16), it.kt0, it.kt1);
     }
-    // many short units: one CTA per SM walks them (the next unit's loads and
-    // S MMAs overlapping this one's softmax and epilogue); otherwise a CTA
-    // per unit, so that a kernel running beside this one gets SMs as they
-    // retire
     int64_t tiles = 0;
     for (int k = 0; k < n; ++k) tiles += items[b + k].kt1 - items[b + k].kt0;
-    const int loop_tiles = q_prepared ? kLoopTilesPrepared : kLoopTiles;
-    const bool loop = int64_t(n) * H > num_sms() && tiles <= int64_t(loop_tiles) * n;
+    const bool loop = takes_loop(n, tiles, H, q_prepared);
+    if (new_keys && !loop) return MLA_ERR_UNSUPPORTED;  // only the looping kernel takes them
     // prepared queries, at least kPersistUnits units per SM and at most
     // kPersistTiles key tiles per unit on average: one CTA per SM walks
     // them, the next unit's loads and first S products overlapping this
@@ -1956,7 +2023,8 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                          tiles <= int64_t(kPersistTiles) * n;
     launch_begin(s);
     if (loop)
-      attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, prm);
+      attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, tkv2,
+                                                                           tlat2, prm);
     else if (persist)
       attn_tc_persist_kernel<<<num_sms(), THREADS1, SMEM_BYTES2, s>>>(tq, tkv, tlat, prm);
     else

@@ -228,7 +228,9 @@ def test_alignment_and_dispatch_errors_before_any_launch():
 
 def test_pinned_bytes_counts_the_metadata():
     """The metadata of one prefill: per execution group (n requests) 5n + 2
-    ints, two ints per empty-token slice, and R + 1 query offsets."""
+    ints, two ints per empty-token slice, R + 1 query offsets, and the last
+    group's context-row offsets (R + 1) and merge flags (R) over all
+    requests."""
     w = W.workload("tiny")
     dims = _lib.Dims.of(w)
     got = M.mla_prefill_pinned_bytes(dims, w.context_lens, w.query_lens, w.row_budget,
@@ -238,7 +240,8 @@ def test_pinned_bytes_counts_the_metadata():
                                       w.split_alignment)
     R = len(w.context_lens)
     empty = len(P.empty_token_slices(w.context_lens, w.query_lens))
-    hi = sum(5 * (c.request_end - c.request_start) + 2 for c in plans) + 2 * empty + R + 1
+    hi = (sum(5 * (c.request_end - c.request_start) + 2 for c in plans) + 2 * empty + R + 1
+          + 2 * R + 1)
     assert 0 < got <= 4 * hi
 
 

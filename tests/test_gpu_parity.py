@@ -845,6 +845,36 @@ def test_prefill_loop_path_continuation_chunks():
     assert_close(f64(lse), rl, 1e-3, what="LSE")
 
 
+def test_prefill_last_group_with_new_tokens_in_one_launch():
+    """Short last group: its context attention and the new-token attention
+    run as one looping-kernel launch (each unit walks its request's context
+    rows of that group, then its own new tokens causally).  Every kind of
+    request: context only in earlier groups (A, its partial merged in the
+    epilogue), continued into the last group (B, merged), context only in
+    the last group (C, E: nothing to merge), none (D); compared in full."""
+    ctx, ql = [1500, 900, 200, 0, 150], [99, 130, 60, 20, 200]
+    w = W.scaled(W.workload("uniform"), context_lens=ctx, query_lens=ql, num_heads=64,
+                 row_budget=1024, max_context_chunk=1024, split_alignment=64, seed=67)
+    x = W.make_inputs(w)
+    plans = M.mla_plan_context_chunks(ctx, w.row_budget, w.max_context_chunk,
+                                      w.split_alignment)
+    # chunks: A | A's rest + B | B's rest + C | E; the last execution group
+    # is the last two (B's continuation with C, then E)
+    assert [c.is_continuation for c in plans] == [False, True, True, False]
+    assert plans[2].request_start == 1 and plans[2].rows + plans[3].rows <= w.row_budget
+    M.mla_profile_begin()
+    out, lse = _run_prefill(w, x)
+    recs = M.mla_profile_end()
+    roles = [r[4] for r in recs]
+    assert recs[-1][0] == "attn_tc_loop_kernel"
+    assert recs[-1][4] == "a6-a10 last context group + new tokens"
+    assert "a9-a10 new-token attention + merge" not in roles
+    ro, rl, _ = _oracle_prefill(w, x)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 @pytest.mark.parametrize("ctx,ql,heads,budget,split", [
     ([4800, 0, 5000, 4500], [250, 10, 200, 400], 96, 6144, False),
     ([6000, 9000], [300, 300], 64, 8192, True)])
