@@ -83,6 +83,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_O = 256;
 constexpr int MAX_ITEMS = 1536;
 constexpr int MAX_SPLIT_GROUPS = 16;   // split (sequence, tile)s per launch
+constexpr int MAX_GROUP_SPLITS = 16;   // key splits of one (sequence, tile)
 constexpr float kRescaleThreshold = 8.0f;    // log2 of the tolerated growth
 
 struct AttnParams {
@@ -1740,23 +1741,40 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constan
   const int qpos = g.y * BQ + row;
   if (qpos >= nq) return;
   const int t = q_beg + qpos;
+  // every split's LSE, then the splits' O rows four at a time: the loads of
+  // a round are independent (indices past the last split repeat it), so
+  // they are in flight together instead of one slot's after the other's
+  auto slot_row = [&](int k) {
+    return (int64_t(g.z + min(k, g.w - 1)) * a.H + h) * BQ + row;
+  };
+  float ls[MAX_GROUP_SPLITS];
   float m = neg_inf();
-  for (int k = 0; k < g.w; ++k)
-    m = fmaxf(m, __ldg(a.split_lse + (int64_t(g.z + k) * a.H + h) * BQ + row));
+#pragma unroll
+  for (int k = 0; k < MAX_GROUP_SPLITS; ++k) {
+    ls[k] = k < g.w ? __ldg(a.split_lse + slot_row(k)) : neg_inf();
+    m = fmaxf(m, ls[k]);
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
   if (!is_neg_inf(m)) {
-    for (int k = 0; k < g.w; ++k) {
-      const int64_t r = (int64_t(g.z + k) * a.H + h) * BQ + row;
-      const float ls = __ldg(a.split_lse + r);
-      if (is_neg_inf(ls)) continue;  // an empty split is never read
-      const float w = expf(ls - m);
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(a.split_o + r * DV) + lane);
-      l += w;
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+#pragma unroll
+    for (int k0 = 0; k0 < MAX_GROUP_SPLITS; k0 += 4) {
+      if (k0 >= g.w) break;
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[i] = __ldg(reinterpret_cast<const float4 *>(a.split_o + slot_row(k0 + i) * DV) + lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // an empty split (and a repeated index) is never used
+        if (is_neg_inf(ls[k0 + i])) continue;
+        const float w = expf(ls[k0 + i] - m);
+        l += w;
+        acc.x += w * v[i].x;
+        acc.y += w * v[i].y;
+        acc.z += w * v[i].z;
+        acc.w += w * v[i].w;
+      }
     }
   }
   float lse = (l > 0.f) ? m + logf(l) : neg_inf();
@@ -1872,7 +1890,7 @@ int plan_items(int causal, int num_seqs, const int32_t *q_loc_host, const int32_
       int used = 0;
       for (const Item &it : items) {
         const int nt = it.kt1 - it.kt0;
-        const int f = std::min(want, nt / kMinSplitTiles);
+        const int f = std::min({want, nt / kMinSplitTiles, MAX_GROUP_SPLITS});
         if (f < 2 || used + f > split->slots || g.n == MAX_SPLIT_GROUPS) {
           out.push_back(it);
           continue;
@@ -2080,7 +2098,10 @@ int launch_split_combine(int n_groups, const int4 *groups, int H, int T, const i
   sg.split_lse = split.lse;
   sg.o = o;
   sg.lse = lse;
-  for (int k = 0; k < n_groups; ++k) sg.g[k] = groups[k];
+  for (int k = 0; k < n_groups; ++k) {
+    if (groups[k].w < 0 || groups[k].w > MAX_GROUP_SPLITS) return MLA_ERR_UNSUPPORTED;
+    sg.g[k] = groups[k];
+  }
   const int64_t warps = int64_t(n_groups) * H * BQ;
   launch_begin(s);
   split_combine_kernel<<<int((warps * 32 + 255) / 256), 256, 0, s>>>(sg);
