@@ -433,10 +433,11 @@ int mla_prefill_pinned_bytes(const mla_dims_t *d, const int32_t *context_lens,
  *   never frees it.  NULL: the copy is made from pageable memory.
  *   On the tensor-core path the workspace keeps K/V in fp16 (see
  *   mla_kv_up_proj); on the CUDA-core path in float32.  There, when the
- *   last execution group is short (on average at most 16 key tiles of 128
- *   per (request, query tile) with the new tokens' causal tiles, and more
- *   units than SMs), its context attention and the new-token attention run
- *   as one launch: each (request, query tile, head) walks the request's
+ *   last execution group's units with the new tokens' causal tiles suit
+ *   the looping or the persistent attention kernel (on average at most 16
+ *   key tiles of 128 per (request, query tile, head) and more units than
+ *   SMs, or at most 64 and at least two units per SM), its context
+ *   attention and the new-token attention run as one launch: each (request, query tile, head) walks the request's
  *   context rows of that group and then its own new tokens, and merges with
  *   the context partial only where an earlier group left one.  The result
  *   is the same composition, one LSE merge order apart.

@@ -777,7 +777,8 @@ extern "C" int mla_chunked_prefill(const mla_dims_t *d, const int32_t *context_l
   // load and an fp16 conversion in every attention CTA
   const void *q_prep = tc ? b.q_prep : nullptr;
   // The last group's context attention and the new-token attention as one
-  // launch of the looping kernel (when its units are short enough for it):
+  // launch of the looping or the persistent kernel (when the units suit
+  // one of them):
   // each (request, query tile, head) unit walks the request's context rows
   // of that group, then its own new tokens causally, and merges with the
   // context partial only where an earlier group left one -- no second Q

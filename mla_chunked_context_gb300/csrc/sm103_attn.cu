@@ -106,9 +106,10 @@ struct AttnParams {
   float *split_o, *split_lse;
   // nullable: MLA_STATUS_FP16_RANGE when a q_nope value overflowed fp16
   int32_t *status;
-  // looping kernel only: after its context keys, each sequence attends its
-  // own new tokens (rows q_loc[i] .. q_loc[i+1] of the second K/V and
-  // latent maps), causally; items are never split then
+  // looping and persistent kernels: after its context keys, each sequence
+  // attends its own new tokens (rows q_loc[i] .. q_loc[i+1] of the second
+  // K/V and latent maps), causally; context keys are then neither causal
+  // nor split
   int new_keys;
   // (sequence, query tile | (split slot + 1) << 16, first key tile, end key
   // tile), the most key tiles first
@@ -247,7 +248,7 @@ __device__ __forceinline__ bool softmax_bar_and(bool ok) {
 __device__ __forceinline__ bool softmax_tile1(const AttnParams &p, uint32_t s_col, uint32_t o_col,
                                               uint32_t sfull_bar, uint32_t sfull_parity,
                                               uint32_t b_odone, uint32_t pfull_bar, int J,
-                                              int k0, int nk, int qpos, float *xm, int wg,
+                                              int k0, int kend, float *xm, int wg,
                                               int row, bool &ok_w, float &m_used, float &l,
                                               int lane) {
   float sv[HALF];  // raw scores (scale applied below)
@@ -264,9 +265,9 @@ __device__ __forceinline__ bool softmax_tile1(const AttnParams &p, uint32_t s_co
       sv[e] = __uint_as_float(r0[e]);
       sv[32 + e] = __uint_as_float(r1[e]);
     }
-    // mask keys past the sequence (and, causal, past the query)
-    int valid = nk - k0;
-    if (p.causal) valid = min(valid, qpos - k0 + 1);
+    // mask keys from kend on (past the sequence, and with a causal mask past
+    // the query)
+    const int valid = kend - k0;
     if (valid < HALF) {
 #pragma unroll
       for (int e = 0; e < HALF; ++e)
@@ -676,12 +677,14 @@ __global__ void __launch_bounds__(THREADS1, 1)
     prefetch_partial(p, h, seq, slot, q_beg, nq, qpos, wg);
     // this warpgroup's 64 columns of O
     const uint32_t o_col = tmem + lane_off + COL_O1 + uint32_t(wg * (DV / 2));
+    // the row's key bound, counted from the unit's first key
+    const int kend = (p.causal ? min(nk, qpos + 1) : nk) - kt0 * BKV;
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j % NSBUF;
       const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(b * BKV + wg * HALF);
       if (!softmax_tile1(p, s_col, o_col, b_sfull + 8 * b, uint32_t((j / NSBUF) & 1), b_odone,
-                         b_pfull + 8 * b, j, (kt0 + j) * BKV + wg * HALF, nk, qpos, xm, wg, row,
-                         ok, m_used, l, lane))
+                         b_pfull + 8 * b, j, j * BKV + wg * HALF, kend, xm, wg, row, ok, m_used,
+                         l, lane))
         break;
     }
     // the unit's last P.V: done barrier (n_tiles-1) % 3, its ((n_tiles-1)/3)-th phase
@@ -853,6 +856,8 @@ __global__ void __launch_bounds__(THREADS1, 1)
     attn_tc_persist_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_kv,
                            const __grid_constant__ CUtensorMap tm_lat,
+                           const __grid_constant__ CUtensorMap tm_kv2,
+                           const __grid_constant__ CUtensorMap tm_lat2,
                            const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -911,7 +916,9 @@ __global__ void __launch_bounds__(THREADS1, 1)
         prefetch_map(&tm_q);
         prefetch_map(&tm_kv);
         prefetch_map(&tm_lat);
+        if (p.new_keys) prefetch_map(&tm_lat2);
       }
+      if (p.new_keys) prefetch_map(&tm_kv2);
       int issued[RING];
       for (int s = 0; s < RING; ++s) issued[s] = -1;
       int q_issued = -1;
@@ -924,11 +931,14 @@ __global__ void __launch_bounds__(THREADS1, 1)
         const int n_tiles = it.w - it.z;
         if (n_tiles <= 0) continue;
         const int seq = it.x, qt = it.y & 0xffff, kt0 = it.z;
-        const int k_beg = __ldg(p.k_loc + seq);
+        const int k_beg = __ldg(p.k_loc + seq), q_beg = __ldg(p.q_loc + seq);
+        // with new keys: the unit's first ct tiles are context keys, the
+        // rest the sequence's new tokens
+        const int ct = p.new_keys ? (__ldg(p.k_loc + seq + 1) - k_beg + BKV - 1) / BKV : n_tiles;
         if (kl) {
           // the previous unit's S products are done with the Q tile
           if (kq > 0 && !mbar_wait(b_qfree, uint32_t((kq - 1) & 1))) break;
-          const int qy = h * p.T + __ldg(p.q_loc + seq) + qt * BQ;
+          const int qy = h * p.T + q_beg + qt * BQ;
           mbar_expect_tx(b_q, Q_BYTES);
           tma_load_2d(smem_u32(sQ), &tm_q, b_q, 0, qy);
           tma_load_2d(smem_u32(sQ + QBOX), &tm_q, b_q, 64, qy);
@@ -938,7 +948,9 @@ __global__ void __launch_bounds__(THREADS1, 1)
         ++kq;
         for (int j = 0; j < n_tiles; ++j, ++J) {
           const int s = J % RING;
-          const int krow = k_beg + (kt0 + j) * BKV;
+          const bool nk_tile = j >= ct;  // a new-token key tile
+          const int krow = nk_tile ? q_beg + (j - ct) * BKV : k_beg + (kt0 + j) * BKV;
+          const CUtensorMap *mkv = nk_tile ? &tm_kv2 : &tm_kv;
           // stage s held tile J-2: its K is free once S of tile J-2 is done,
           // its V once the P.V of tile J-2 is
           if (J >= RING && !mbar_wait((kl ? b_sfull : b_odone) + 8 * ((J - 2) % NSBUF),
@@ -949,14 +961,15 @@ __global__ void __launch_bounds__(THREADS1, 1)
           if (kl) {
             uint8_t *k = sK + s * K_BYTES;
             mbar_expect_tx(full + 8 * s, K_BYTES);
-            tma_load_3d(smem_u32(k), &tm_kv, full + 8 * s, 0, krow, h);
-            tma_load_3d(smem_u32(k + KBOX), &tm_kv, full + 8 * s, 64, krow, h);
-            tma_load_2d(smem_u32(k + 2 * KBOX), &tm_lat, full + 8 * s, 512, krow);
+            tma_load_3d(smem_u32(k), mkv, full + 8 * s, 0, krow, h);
+            tma_load_3d(smem_u32(k + KBOX), mkv, full + 8 * s, 64, krow, h);
+            tma_load_2d(smem_u32(k + 2 * KBOX), nk_tile ? &tm_lat2 : &tm_lat, full + 8 * s, 512,
+                        krow);
           } else {
             uint8_t *v = sV + s * V_BYTES;
             mbar_expect_tx(full + 8 * s, V_BYTES);
-            tma_load_3d(smem_u32(v), &tm_kv, full + 8 * s, DN, krow, h);
-            tma_load_3d(smem_u32(v + KBOX), &tm_kv, full + 8 * s, DN + 64, krow, h);
+            tma_load_3d(smem_u32(v), mkv, full + 8 * s, DN, krow, h);
+            tma_load_3d(smem_u32(v + KBOX), mkv, full + 8 * s, DN + 64, krow, h);
           }
           issued[s] = int((J / RING) & 1);
         }
@@ -1055,12 +1068,21 @@ __global__ void __launch_bounds__(THREADS1, 1)
       const int qpos = qt * BQ + row;
       float m_used = neg_inf(), l = 0.f;
       prefetch_partial(p, h, seq, slot, q_beg, nq, qpos, wg);
+      // the context key tiles, then with new keys the sequence's own new
+      // tokens (keys 0 .. nq-1, causal): keys counted from the unit's
+      // first, valid below kend.  With new keys the context keys are not
+      // causal and not split, so their bound is nk on every row and the
+      // first tile at or past it is the first new-token tile; until then
+      // kend holds ~nk (negative: the context phase).
+      int kend = (p.causal ? min(nk, qpos + 1) : nk) - kt0 * BKV;
+      if (p.new_keys) kend = ~kend;
       for (int j = 0; j < n_tiles; ++j) {
+        if (kend < 0 && j * BKV >= ~kend) kend = min(nq, qpos + 1) + j * BKV;
         const int JJ = J + j, b = JJ % NSBUF;
         const uint32_t s_col = tmem + lane_off + COL_S + uint32_t(b * BKV + wg * HALF);
         if (!softmax_tile1(p, s_col, o_col, b_sfull + 8 * b, uint32_t((JJ / NSBUF) & 1), b_odone,
-                           b_pfull + 8 * b, JJ, (kt0 + j) * BKV + wg * HALF, nk, qpos, xm, wg,
-                           row, ok, m_used, l, lane))
+                           b_pfull + 8 * b, JJ, j * BKV + wg * HALF, kend < 0 ? ~kend : kend, xm,
+                           wg, row, ok, m_used, l, lane))
           break;
       }
       const int JL = J + n_tiles - 1;  // the unit's last tile
@@ -1931,6 +1953,14 @@ bool takes_loop(int n_items, int64_t tiles, int H, bool q_prepared) {
   const int loop_tiles = q_prepared ? kLoopTilesPrepared : kLoopTiles;
   return int64_t(n_items) * H > num_sms() && tiles <= int64_t(loop_tiles) * n_items;
 }
+// Otherwise, with prepared queries, at least kPersistUnits units per SM and
+// at most kPersistTiles key tiles per unit on average: one CTA per SM walks
+// them, the next unit's loads and first S products overlapping this one's
+// last tiles and epilogue.
+bool takes_persist(int n_items, int64_t tiles, int H, bool q_prepared) {
+  return q_prepared && int64_t(n_items) * H >= int64_t(kPersistUnits) * num_sms() &&
+         tiles <= int64_t(kPersistTiles) * n_items;
+}
 }  // namespace
 
 bool attn_tc_new_keys_ok(int num_seqs, const int32_t *q_loc_host, const int32_t *k_loc_host,
@@ -1942,7 +1972,8 @@ bool attn_tc_new_keys_ok(int num_seqs, const int32_t *q_loc_host, const int32_t 
     return false;
   int64_t tiles = 0;
   for (const Item &it : items) tiles += it.kt1 - it.kt0;
-  return takes_loop(int(items.size()), tiles, H, true);
+  return takes_loop(int(items.size()), tiles, H, true) ||
+         takes_persist(int(items.size()), tiles, H, true);
 }
 
 int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t *q_loc,
@@ -1954,8 +1985,9 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
                    int32_t *status, cudaStream_t s, const NewKeySource *new_keys) {
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al16(q) || !al16(kv) || !al16(latent)) return MLA_ERR_UNSUPPORTED;
-  // new keys: the looping kernel only, non-causal context keys, prepared
-  // queries (checked by attn_tc_new_keys_ok before the caller commits to it)
+  // new keys: the looping or the persistent kernel, non-causal context keys,
+  // prepared queries (checked by attn_tc_new_keys_ok before the caller
+  // commits to it)
   if (new_keys && (causal || !q_prepared || !al16(new_keys->kv) || !al16(new_keys->latent) ||
                    (new_keys->latent_ld * 2) % 16 != 0 || new_keys->latent_ld < 576))
     return MLA_ERR_UNSUPPORTED;
@@ -2031,20 +2063,16 @@ int launch_attn_tc(const mla_dims_t &d, int causal, int num_seqs, const int32_t 
     int64_t tiles = 0;
     for (int k = 0; k < n; ++k) tiles += items[b + k].kt1 - items[b + k].kt0;
     const bool loop = takes_loop(n, tiles, H, q_prepared);
-    if (new_keys && !loop) return MLA_ERR_UNSUPPORTED;  // only the looping kernel takes them
-    // prepared queries, at least kPersistUnits units per SM and at most
-    // kPersistTiles key tiles per unit on average: one CTA per SM walks
-    // them, the next unit's loads and first S products overlapping this
-    // one's last tiles and epilogue
-    const bool persist = !loop && q_prepared &&
-                         int64_t(n) * H >= int64_t(kPersistUnits) * num_sms() &&
-                         tiles <= int64_t(kPersistTiles) * n;
+    const bool persist = !loop && takes_persist(n, tiles, H, q_prepared);
+    // only the looping and the persistent kernel take new keys
+    if (new_keys && !loop && !persist) return MLA_ERR_UNSUPPORTED;
     launch_begin(s);
     if (loop)
       attn_tc_loop_kernel<<<num_sms(), THREADS_LOOP, SMEM_BYTES_LOOP, s>>>(tq, tkv, tlat, tkv2,
                                                                            tlat2, prm);
     else if (persist)
-      attn_tc_persist_kernel<<<num_sms(), THREADS1, SMEM_BYTES2, s>>>(tq, tkv, tlat, prm);
+      attn_tc_persist_kernel<<<num_sms(), THREADS1, SMEM_BYTES2, s>>>(tq, tkv, tlat, tkv2, tlat2,
+                                                                      prm);
     else
       attn_tc_kernel<<<n * H, THREADS1, SMEM_BYTES1, s>>>(tq, tkv, tlat, prm);
     const int rc = launch_status(

@@ -912,6 +912,43 @@ def test_prefill_persistent_attention(ctx, ql, heads, budget, split):
         assert_close(f64(lse[h]), rl[0], 1e-3, what=f"LSE head {h}")
 
 
+def test_prefill_last_group_with_new_tokens_persistent():
+    """A long last group (a 3544-row continuation, 28 key tiles) with the
+    new tokens over 96 heads: the final launch takes the persistent kernel
+    (about 23 key tiles per unit), each unit walking the group's context
+    rows and then its new tokens causally; the continued request merges
+    with its first chunk's partial, the other has no context in that group
+    but its own partial; compared on every token for six heads, every head
+    checked for NaN."""
+    ctx, ql = [600, 7000], [100, 300]
+    w = W.scaled(W.workload("uniform"), context_lens=ctx, query_lens=ql, num_heads=96,
+                 row_budget=4096, max_context_chunk=4096, split_alignment=64, seed=71)
+    x = W.make_inputs(w)
+    plans = M.mla_plan_context_chunks(ctx, w.row_budget, w.max_context_chunk,
+                                      w.split_alignment)
+    assert [c.is_continuation for c in plans] == [False, True]
+    M.mla_profile_begin()
+    out, lse = _run_prefill(w, x)
+    recs = M.mla_profile_end()
+    assert recs[-1][0] == "attn_tc_persist_kernel"
+    assert recs[-1][4] == "a6-a10 last context group + new tokens"
+    assert not torch.isnan(out).any().item() and not torch.isnan(lse).any().item()
+    H, Dn, Dv = w.num_heads, w.qk_nope_dim, w.v_dim
+    q = x["q"].float().numpy()
+    lat = x["new_latent"].float().numpy()
+    cache = x["kv_cache"].float().numpy()
+    bt = x["block_table"].numpy()
+    wk = x["w_kv_b"].float().numpy()
+    d1 = O.MlaDims(1, w.kv_lora_rank, w.qk_rope_dim, Dn, Dv, w.block_size, w.softmax_scale)
+    for h in (0, 1, 37, 50, H - 2, H - 1):
+        ro, rl, _ = O.chunked_prefill(q[:, h:h + 1], lat, cache, bt,
+                                      wk[h * (Dn + Dv):(h + 1) * (Dn + Dv)], w.context_lens,
+                                      w.query_lens, d1, w.row_budget, w.max_context_chunk,
+                                      w.split_alignment)
+        assert_close(f64(out[:, h]), ro[:, 0], 2e-2, 2e-2, what=f"O head {h}")
+        assert_close(f64(lse[h]), rl[0], 1e-3, what=f"LSE head {h}")
+
+
 def test_prefill_persistent_new_token_attention():
     """A request with 4200 new tokens (33 query tiles, 17 causal key tiles
     per unit on average, past the looping kernel's limit) over 16 heads:
