@@ -863,9 +863,12 @@ def run_kernel_case(args, dev):
         # whole prefills of --workload (the launches of one step, for a
         # traffic capture); work = the step's algorithmic FLOPs
         w = W.workload(args.workload)
-        if args.requests:  # the first N requests only (a smaller capture)
-            w = W.scaled(w, context_lens=list(w.context_lens[:args.requests]),
-                         query_lens=list(w.query_lens[:args.requests]))
+        if args.requests or args.first_request:
+            # N requests from the K-th on only (a smaller capture)
+            r0 = args.first_request
+            r1 = r0 + args.requests if args.requests else w.num_requests
+            w = W.scaled(w, context_lens=list(w.context_lens[r0:r1]),
+                         query_lens=list(w.query_lens[r0:r1]))
         x, g, plans, pf, out, step = prefill_runner(M, W, w, dev)
         fn = step
         work, unit, peak = flops_of(w, plans)["total"], "TFLOP/s", peaks["bf16_tflops"]
@@ -960,7 +963,9 @@ def main():
     ap.add_argument("--causal", type=int, default=0)
     ap.add_argument("--launches", type=int, default=10)
     ap.add_argument("--requests", type=int, default=0,
-                    help="--kernel step: the workload's first N requests only")
+                    help="--kernel step: N requests of the workload only")
+    ap.add_argument("--first-request", type=int, default=0,
+                    help="--kernel step: start at the workload's K-th request")
     args = ap.parse_args()
     if args.kernel:
         torch.cuda.set_device(0)
