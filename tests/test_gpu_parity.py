@@ -912,6 +912,36 @@ def test_prefill_persistent_attention(ctx, ql, heads, budget, split):
         assert_close(f64(lse[h]), rl[0], 1e-3, what=f"LSE head {h}")
 
 
+@pytest.mark.parametrize("seed", [73, 74, 75, 76])
+def test_prefill_final_launch_edge_cases(seed):
+    """The final launch with the last group's context over ragged shapes,
+    compared in full.  Seed 73 is fixed: the last group holds a context of
+    exactly one key tile (128 rows) and a request with one new token, an
+    earlier group a request with context but no new tokens, and
+    context-free requests sit between and after the groups.  The others
+    draw 10 requests (context 0-700 rows, 0-260 new tokens) and take
+    whichever final launch their plan gives."""
+    if seed == 73:
+        ctx, ql = [256, 700, 0, 128, 390, 0], [40, 0, 130, 200, 1, 77]
+    else:
+        rng = np.random.default_rng(seed)
+        ctx = [int(c) if rng.random() > 0.25 else 0 for c in rng.integers(1, 700, 10)]
+        ql = [int(q) for q in rng.integers(0, 260, 10)]
+    w = W.scaled(W.workload("uniform"), context_lens=ctx, query_lens=ql, num_heads=32,
+                 row_budget=1024, max_context_chunk=512, split_alignment=64, seed=seed)
+    x = W.make_inputs(w)
+    M.mla_profile_begin()
+    out, lse = _run_prefill(w, x)
+    recs = M.mla_profile_end()
+    if seed == 73:
+        assert recs[-1][0] == "attn_tc_loop_kernel"
+        assert recs[-1][4] == "a6-a10 last context group + new tokens"
+    ro, rl, _ = _oracle_prefill(w, x)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert_close(f64(out), ro, 2e-2, 2e-2, what="O")
+    assert_close(f64(lse), rl, 1e-3, what="LSE")
+
+
 def test_prefill_last_group_with_new_tokens_persistent():
     """A long last group (a 3544-row continuation, 28 key tiles) with the
     new tokens over 96 heads: the final launch takes the persistent kernel
