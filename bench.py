@@ -182,12 +182,13 @@ def attn_ctx_bytes(w, plans):
 def execution_groups(plans, budget):
     """The chunks as mla_chunked_prefill runs them: consecutive chunks with
     no continuation after the first and rows within the budget together."""
+    rows_of = lambda c: sum(c.seq_lens)  # noqa: E731  (no padding here)
     groups, c0 = [], 0
     while c0 < len(plans):
-        c1, rows = c0 + 1, plans[c0].rows
+        c1, rows = c0 + 1, rows_of(plans[c0])
         while (c1 < len(plans) and not plans[c1].is_continuation
-               and rows + plans[c1].rows <= budget):
-            rows += plans[c1].rows
+               and rows + rows_of(plans[c1]) <= budget):
+            rows += rows_of(plans[c1])
             c1 += 1
         groups.append(plans[c0:c1])
         c0 = c1

@@ -56,3 +56,64 @@ def test_breakdown_bar_and_rooflines():
         g["achieved"], 2 * fl["context_rows"] * 576 * 2 / 0.1e-3 / 1e9)
     assert [e["kernel"] for e in br["timeline_first_step"]] == ["gather", "gemm", "attn", "gemm",
                                                                "attn"]
+
+
+def _plans(w):
+    return P.plan_mla_context_chunks(w.context_lens, w.row_budget, w.max_context_chunk,
+                                     w.split_alignment)
+
+
+def test_execution_groups_follow_the_prefill():
+    """Chunks run together until a continuation or the row budget ends the
+    group: the hetero batch's four long-request chunks alone, its seven
+    small chunks together; the uniform batch in one group."""
+    w = W.workload("hetero")
+    assert [len(g) for g in bench.execution_groups(_plans(w), w.row_budget)] == [1, 1, 1, 1, 7]
+    w = W.workload("uniform")
+    assert [len(g) for g in bench.execution_groups(_plans(w), w.row_budget)] == [1]
+
+
+def test_last_group_work_splits_the_context_attention():
+    """The final launch's FLOPs are the last group's context attention plus
+    the new-token attention, the rest stay with the context attention; its
+    bytes are fewer than those of the two launches it replaces."""
+    w = W.workload("hetero")
+    plans = _plans(w)
+    fl = bench.flops_of(w, plans)
+    last_fl, last_by, ctx_fl, ctx_by = bench.last_group_work(w, plans)
+    assert math.isclose(last_fl + ctx_fl, fl["attn_ctx"] + fl["attn_new"], rel_tol=1e-12)
+    assert ctx_fl < fl["attn_ctx"] and ctx_by < fl["attn_ctx_bytes"]
+    last_ctx_by = fl["attn_ctx_bytes"] - ctx_by
+    assert last_by < last_ctx_by + fl["attn_new_bytes"]
+    # the queries once, the new tokens' and the group's K/V, the output
+    H, Dn, Dv, Pd = w.num_heads, w.qk_nope_dim, w.v_dim, w.qk_rope_dim
+    rows = sum(sum(c.seq_lens) for c in bench.execution_groups(plans, w.row_budget)[-1])
+    T = w.num_tokens
+    assert last_by >= (T * H * (Dn + Pd) * 2 + (T + rows) * (H * (Dn + Dv) * 2 + Pd * 2)
+                       + T * H * (Dv * 2 + 4))
+
+
+def test_breakdown_with_the_final_launch_role():
+    """With the last group's context attention in the final launch, that
+    launch is its own roofline class and the context attention class counts
+    the other groups only."""
+    w = W.workload("hetero")
+    plans = _plans(w)
+    peaks = dict(hbm_gbs=6000.0, bf16_tflops=2000.0, bf16_tflops_sustained=1800.0,
+                 source="test")
+    one = [_rec("gather", 1, 0.0, 0.1, bench.ROLE_GATHER),
+           _rec("gemm", 2, 0.1, 1.5, bench.ROLE_UP),
+           _rec("attn", 0, 1.6, 2.5, bench.ROLE_ATTN),
+           _rec("gemm", 2, 1.7, 0.2, bench.ROLE_UP_NEW),
+           _rec("loop", 0, 4.1, 0.5, bench.ROLE_LAST)]
+    br = bench.breakdown_of(one, 1, w, plans, peaks)
+    last_fl, last_by, ctx_fl, ctx_by = bench.last_group_work(w, plans)
+    rl = br["rooflines"]
+    assert "new_token_attention_merge" not in rl
+    assert rl["context_attention"]["flops_per_step"] == ctx_fl
+    assert rl["context_attention"]["bytes_per_step"] == ctx_by
+    fin = rl["last_group_and_new_token_attention"]
+    assert fin["flops_per_step"] == last_fl and fin["bytes_per_step"] == last_by
+    assert math.isclose(fin["ms_per_step"], 0.5)
+    # the bar's span ends with the final launch
+    assert math.isclose(br["north_star_bar"]["a4_a7_span_ms"], 4.6)
