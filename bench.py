@@ -16,7 +16,7 @@ Printed JSON line (rank 0):
              timed region
   breakdown  every launch of the timed steps timed in place (the library's
              per-launch CUDA events on the launching streams), summed per step
-             of the method; the spec bar = (up-projection + context
+             of the method; the tensor-target bar = (up-projection + context
              attention FLOPs) / (span of the gather .. context attention)
   rooflines  per kernel: algorithmic work / its in-step CUDA-event time vs the
              measured peak, from a third timed region with the pipeline's
@@ -302,7 +302,7 @@ def attributed_ms(rs):
 def breakdown_of(records, steps, w, plans, peaks):
     """Per step of the method: launches, summed in-place CUDA-event time and
     overlap-attributed time per prefill step; per kernel: its rooflines; the
-    spec bar: (a5 + a6 FLOPs) / (span from the first gather's start to
+    tensor-target bar: (a5 + a6 FLOPs) / (span from the first gather's start to
     the end of the last context-attention launch)."""
     per_step = split_steps(records, steps)
     fl = flops_of(w, plans)
@@ -406,7 +406,7 @@ def breakdown_of(records, steps, w, plans, peaks):
                                   if peaks.get("bf16_tflops_sustained") else None)}
     timeline = [{"kernel": r[0], "role": r[4], "stream": r[1], "start_ms": round(r[2] - per_step[0][0][2], 4),
                  "ms": round(r[3], 4)} for r in per_step[0]] if per_step and per_step[0] else []
-    return {"roles": roles, "kernels": kernels, "north_star_bar": bar, "rooflines": rooflines,
+    return {"roles": roles, "kernels": kernels, "target_bar": bar, "rooflines": rooflines,
             "timeline_first_step": timeline}
 
 
@@ -521,7 +521,7 @@ def bench_config(M, W, name, dev, peaks, flush, steps, warmup):
            "frac_sustained": (tf / peaks["bf16_tflops_sustained"]
                               if peaks.get("bf16_tflops_sustained") else None),
            "ms_per_step_serial": statistics.median(ser_ms),
-           "north_star_bar": br["north_star_bar"], "rooflines": br_ser["rooflines"],
+           "target_bar": br["target_bar"], "rooflines": br_ser["rooflines"],
            "rooflines_overlapped": br["rooflines"], "roles": br["roles"]}
     if w.dtype != "bf16":
         res["note"] = ("float32 storage: the CUDA-core kernels (the tensor-core kernels serve "
@@ -661,7 +661,7 @@ def run_ours(args, rank, world, dev):
             "rooflines": br_ser["rooflines"],
             "rooflines_overlapped": br["rooflines"],
             "ms_per_step_serial": statistics.mean(ser_ms),
-            "north_star_bar": br["north_star_bar"],
+            "target_bar": br["target_bar"],
             "breakdown": {"roles": br["roles"], "kernels": br["kernels"],
                           "timeline_first_step": br["timeline_first_step"],
                           "how": "CUDA events recorded by the library on the launching "

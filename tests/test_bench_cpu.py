@@ -1,6 +1,6 @@
 """Host logic of bench.py (no GPU): the per-step split of the launch
 records, the overlap-attributed time, the in-step rooflines and the
-spec bar, on synthetic launch records."""
+tensor-target bar, on synthetic launch records."""
 
 import math
 
@@ -45,7 +45,7 @@ def test_breakdown_bar_and_rooflines():
            _rec("attn", 0, 4.1, 0.6, bench.ROLE_ATTN_NEW)]
     two = [(k, s, t + 10.0, ms, r) for k, s, t, ms, r in one]
     br = bench.breakdown_of(one + two, 2, w, plans, peaks)
-    bar = br["north_star_bar"]
+    bar = br["target_bar"]
     assert math.isclose(bar["a4_a7_span_ms"], 4.1)
     assert math.isclose(bar["tflops"], (fl["up_proj_ctx"] + fl["attn_ctx"]) / 4.1e-3 / 1e12)
     up = br["rooflines"]["up_proj"]
@@ -116,4 +116,4 @@ def test_breakdown_with_the_final_launch_role():
     assert fin["flops_per_step"] == last_fl and fin["bytes_per_step"] == last_by
     assert math.isclose(fin["ms_per_step"], 0.5)
     # the bar's span ends with the final launch
-    assert math.isclose(br["north_star_bar"]["a4_a7_span_ms"], 4.6)
+    assert math.isclose(br["target_bar"]["a4_a7_span_ms"], 4.6)
